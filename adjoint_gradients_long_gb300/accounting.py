@@ -1,0 +1,44 @@
+"""Storage and traffic accounting for the adjoint-sharding path (host-side arithmetic only).
+
+``paper_state_values`` is the stored-state count of the review page "Adjoint
+sharding for very long context training of state space models" (Referee Report,
+major comment on Section 4.5): storing {A_t, C_t, h_t, y_t} for T tokens and K
+layers costs T K (2N + P) + T P values.  ``stored_bytes`` is what this library
+actually keeps per layer: a, c, h in fp32 plus the layer input xhat.
+"""
+from __future__ import annotations
+
+
+def paper_state_values(T: int, K: int, N: int, P: int) -> int:
+    """Section 4.5 stored-value count T K (2N + P) + T P."""
+    return T * K * (2 * N + P) + T * P
+
+
+def stored_bytes(B: int, T: int, K: int, N: int, P: int, x_bytes: int) -> int:
+    """Bytes this library keeps between the forward and the backward pass: per layer and
+    token, a, c, h (3N fp32) and the layer input xhat (P values of x_bytes each)."""
+    return B * T * K * (3 * N * 4 + P * x_bytes)
+
+
+def step_bytes(P: int, N: int, x_bytes: int, d_bytes: int, window: bool, stacked: bool) -> dict:
+    """Algorithmic HBM bytes per token per layer of each call of the library as built
+    (inputs read once, outputs written once, workspace round trips included)."""
+    fwd = {
+        "proj_in": P * x_bytes + 3 * N * 4,           # read xhat; write a, c, u
+        "fwd_scan": 2 * N * 4 + N * 4,                # read a, u; write h
+        "proj_out": 2 * N * 4 + P * x_bytes + P * 4 + (P * 2 if x_bytes == 2 else 0),
+    }
+    bwd = {
+        "cot_proj": P * 4 + N * 4,                    # read gy; write g
+        "bwd_scan": 4 * N * 4 + 4 * N * d_bytes,      # read g, c, a, h; write D_a, D_u, D_c, E
+    }
+    if window:
+        bwd["win_scan"] = 3 * N * 4 + N * 4           # read g, c, a; write R
+        bwd["bwd_scan"] += N * 4                      # read R
+    par = {
+        "param_grad": P * x_bytes + 3 * N * d_bytes + N * d_bytes + P * 4,
+        "colsum": N * d_bytes,
+    }
+    if stacked:
+        par["input_grad"] = 3 * N * d_bytes + P * 4 + P * 4
+    return {"fwd": fwd, "bwd": bwd, "param": par}

@@ -1,0 +1,68 @@
+"""Plant plausible mistakes in copies of the C oracle (on the CPU) and check that the
+pins catch each of them: a dropped term, a wrong index or sign, a transposed operand."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import bptt
+from adjoint_gradients_long_gb300 import synth
+from conftest import rel_fro
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "adj_oracle.c")
+
+MUTATIONS = {
+    "h_i_for_h_im1": ("i > 0 ? hb + (i - 1) * N : NULL", "hb + i * N"),
+    "no_sigmoid_slope": ("a_i[n] * (1.0 - a_i[n])", "a_i[n]"),
+    "dropped_db_a": ("db_a[n] += s_scratch[n];", ";"),
+    "W_o_transposed": ("acc += gyb[t * P + p] * W_o[n * P + p];", "acc += gyb[t * P + p] * W_o[p * N + n];"),
+    "gate_index_shift": ("v[n] *= ab[i * N + n];", "v[n] *= ab[(i > 0 ? i - 1 : 0) * N + n];"),
+    "literal_product_short": ("for (int64_t j = i + 1; j <= t; ++j)", "for (int64_t j = i + 1; j < t; ++j)"),
+    "dx_sign": ("acc += s_scratch[n] * W_a[p * N + n] + v[n] * W_B[p * N + n];",
+                "acc -= s_scratch[n] * W_a[p * N + n] + v[n] * W_B[p * N + n];"),
+    "no_gate_in_scan": ("ht[n] = at[n] * (hprev ? hprev[n] : 0.0) + ut[n];",
+                        "ht[n] = (hprev ? hprev[n] : 0.0) + ut[n];"),
+    "window_off_by_one": ("int64_t lo = t - Tbar + 1;", "int64_t lo = t - Tbar;"),
+}
+
+
+@pytest.fixture(scope="module")
+def case():
+    d = synth.make_inputs("ssm8_p512", T=20, B=2, P=8, N=8, K=2)
+    layers = [{k: np.asarray(v, np.float64) for k, v in W.items()} for W in d["layers"]]
+    x, tgt = d["xhat"].astype(np.float64), d["target"].astype(np.float64)
+    return layers, x, tgt, bptt.bptt_grad(layers, x, tgt)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, case, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, name
+    path_c = tmp_path / "mut.c"
+    path_c.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", str(so), str(path_c), "-lm"])
+    layers, x, tgt, ref = case
+    oracle.use_library(str(so))
+    try:
+        worst = 0.0
+        for mode in (oracle.LITERAL, oracle.AGGREGATED):
+            res = oracle.stack_grad(layers, x, tgt, None, mode)
+            for k in range(2):
+                for nm in bptt.PARAMS:
+                    worst = max(worst, rel_fro(res["grads"][k]["d" + nm], ref["grads"][k][nm]))
+            # a window of 5 against per-term truncated BPTT
+            cache = bptt.forward(layers, x)
+            tr, _ = bptt.backward(layers, cache, cache[-1]["y"] - tgt, 5)
+            res5 = oracle.stack_grad(layers, x, tgt, 5, mode)
+            for k in range(2):
+                for nm in bptt.PARAMS:
+                    worst = max(worst, rel_fro(res5["grads"][k]["d" + nm], tr[k][nm]))
+    finally:
+        oracle.use_library(None)
+    assert worst > 1e-6, (name, worst)
