@@ -1,0 +1,349 @@
+// adj_abi.cu -- the extern "C" entry points of libadj.so: host-side validation,
+// workspace layout and the launch sequence of each call.  The operations and their
+// sources are documented in include/adj.h.
+#include <string.h>
+
+#include "adj_internal.cuh"
+#include "adj_profile.cuh"
+
+using namespace adj;
+
+namespace {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// largest grid the scans launch (tickets are 32-bit)
+constexpr int64_t MAX_CHUNKS = int64_t(1) << 31;
+
+adj_status check_dims(const adj_dims *d) {
+    if (!d) return ADJ_EINVAL;
+    if (d->B < 0 || d->T < 0 || d->P <= 0 || d->N <= 0) return ADJ_ESHAPE;
+    if (d->P % 8 || d->N % 8) return ADJ_ESHAPE;
+    if ((d->x_dtype != ADJ_F32 && d->x_dtype != ADJ_BF16) || (d->d_dtype != ADJ_F32 && d->d_dtype != ADJ_BF16))
+        return ADJ_EDTYPE;
+    if (d->B * cdiv(d->N, 128) * cdiv(d->T, 32) >= MAX_CHUNKS) return ADJ_ESHAPE;
+    return ADJ_OK;
+}
+
+adj_status check_ptrs(std::initializer_list<const void *> ps) {
+    for (const void *p : ps) {
+        if (!p) return ADJ_EINVAL;
+        if (!al16(p)) return ADJ_EALIGN;
+    }
+    return ADJ_OK;
+}
+adj_status check_opt(std::initializer_list<const void *> ps) {
+    for (const void *p : ps)
+        if (p && !al16(p)) return ADJ_EALIGN;
+    return ADJ_OK;
+}
+
+int param_splits(const adj_dims *d) {
+    const int64_t BT = d->B * d->T;
+    const int64_t tiles = cdiv(d->P, 64) * cdiv(3 * int64_t(d->N), 64);
+    int64_t s = cdiv(608, tiles);
+    if (s > BT / 512) s = BT / 512;
+    if (s < 1) s = 1;
+    if (s > 64) s = 64;
+    return int(s);
+}
+int colsum_blocks(const adj_dims *d) {
+    int64_t n = cdiv(d->B * d->T, 64);
+    if (n > 1024) n = 1024;
+    return n < 1 ? 1 : int(n);
+}
+int loss_blocks(int64_t count) {
+    int64_t n = cdiv(count, 256 * 8);
+    if (n > 1024) n = 1024;
+    return n < 1 ? 1 : int(n);
+}
+
+// Workspace layouts (offsets from ws; the first WS_HEADER bytes hold the status word).
+struct Layout {
+    size_t buf0 = 0, buf1 = 0, scan = 0, part0 = 0, part1 = 0, part2 = 0, total = 0;
+};
+
+Layout layout(const adj_dims *d, int op, int64_t Tbar) {
+    Layout L;
+    const size_t btn = al256(size_t(d->B * d->T) * d->N * 4);
+    size_t off = WS_HEADER;
+    switch (op) {
+    case ADJ_OP_FWD:            // u
+    case ADJ_OP_BWD_FULL:       // g
+        L.buf0 = off; off += btn;
+        L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
+        break;
+    case ADJ_OP_BWD_TRUNC:      // g, R
+        L.buf0 = off; off += btn;
+        L.buf1 = off; off += (Tbar < d->T ? btn : 0);
+        L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
+        break;
+    case ADJ_OP_PARAM: {
+        const int s = param_splits(d);
+        L.part0 = off; off += al256(size_t(s) * d->P * 3 * d->N * 4);
+        L.part1 = off; off += al256(size_t(s) * d->N * d->P * 4);
+        L.part2 = off; off += al256(size_t(colsum_blocks(d)) * d->N * 4);
+        break;
+    }
+    case ADJ_OP_LOSS:
+        L.part0 = off; off += al256(size_t(loss_blocks(d->B * d->T * d->P)) * 8);
+        break;
+    default:
+        return Layout{};
+    }
+    L.total = off;
+    return L;
+}
+
+adj_status check_ws(const adj_dims *d, int op, int64_t Tbar, void *ws, size_t ws_bytes, Layout *L) {
+    *L = layout(d, op, Tbar);
+    if (!ws) return ADJ_EINVAL;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return ADJ_EALIGN;
+    if (ws_bytes < L->total) return ADJ_EWORKSPACE;
+    return ADJ_OK;
+}
+
+inline char *at(void *ws, size_t off) { return static_cast<char *>(ws) + off; }
+inline unsigned *status_word(void *ws) { return static_cast<unsigned *>(ws); }
+
+#define ADJ_TRY(x)                                  \
+    do {                                            \
+        adj_status s_ = (x);                        \
+        if (s_ != ADJ_OK) return s_;                \
+    } while (0)
+#define ADJ_CUDA(x)                                 \
+    do {                                            \
+        if ((x) != cudaSuccess) return ADJ_ECUDA;   \
+    } while (0)
+
+GemmOperand op1(const void *p, int64_t s_row, int64_t s_k, bool bf16, const float *mul = nullptr) {
+    GemmOperand o;
+    o.p[0] = p; o.p[1] = p; o.p[2] = p;
+    o.blk = int64_t(1) << 62;
+    o.s_row = s_row; o.s_k = s_k; o.bf16 = bf16; o.mul = mul;
+    return o;
+}
+GemmOperand op3(const void *p0, const void *p1, const void *p2, int64_t blk, int64_t s_row, int64_t s_k, bool bf16) {
+    GemmOperand o;
+    o.p[0] = p0; o.p[1] = p1; o.p[2] = p2;
+    o.blk = blk; o.s_row = s_row; o.s_k = s_k; o.bf16 = bf16; o.mul = nullptr;
+    return o;
+}
+GemmEpilogue epi(Epi k) {
+    GemmEpilogue e;
+    memset(&e, 0, sizeof(e));
+    e.kind = k;
+    return e;
+}
+
+adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a, const float *c, const float *h,
+                      const float *gy, void *D_a, void *D_u, void *D_c, void *E, int64_t Tbar, int op, void *ws,
+                      size_t ws_bytes, void *stream) {
+    ADJ_TRY(check_dims(dims));
+    if (!w) return ADJ_EINVAL;
+    ADJ_TRY(check_ptrs({w->W_o, a, c, h, gy, D_a, D_u, D_c, E}));
+    if (op == ADJ_OP_BWD_TRUNC && Tbar < 1) return ADJ_EINVAL;
+    Layout L;
+    ADJ_TRY(check_ws(dims, op, Tbar, ws, ws_bytes, &L));
+    const int64_t B = dims->B, T = dims->T, BT = B * T;
+    const int P = dims->P, N = dims->N;
+    if (BT == 0) return ADJ_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *g = reinterpret_cast<float *>(at(ws, L.buf0));
+    // g = gy W_o^T  (the cotangent of c . h)
+    GemmEpilogue e = epi(Epi::Store);
+    e.out0 = g;
+    e.ld = N;
+    {
+        ProfScope ps(K_COT_PROJ, st);
+        ADJ_CUDA(launch_gemm(BT, N, P, op1(gy, P, 1, false), op1(w->W_o, P, 1, dims->x_dtype == ADJ_BF16), e, 1, st));
+    }
+    const bool trunc = op == ADJ_OP_BWD_TRUNC && Tbar < T;
+    float *R = nullptr;
+    if (trunc) {
+        R = reinterpret_cast<float *>(at(ws, L.buf1));
+        ProfScope ps(K_WIN_SCAN, st);
+        ADJ_CUDA(launch_win_scan(g, c, a, R, B, T, N, Tbar, at(ws, L.scan), status_word(ws), st));
+    }
+    ProfScope ps(K_BWD_SCAN, st);
+    ADJ_CUDA(launch_bwd_scan(g, c, a, h, R, D_a, D_u, D_c, E, dims->d_dtype == ADJ_BF16, B, T, N, trunc ? Tbar : 0,
+                             at(ws, L.scan), status_word(ws), st));
+    return ADJ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t adj_workspace_bytes(const adj_dims *dims, int op, int64_t Tbar) {
+    if (check_dims(dims) != ADJ_OK) return 0;
+    if (op == ADJ_OP_BWD_TRUNC && Tbar < 1) return 0;
+    return layout(dims, op, Tbar).total;
+}
+
+adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *xhat, const float *xres, float *a,
+                        float *c, float *h, float *y, void *y_x, void *ws, size_t ws_bytes, void *stream) {
+    ADJ_TRY(check_dims(dims));
+    if (!w) return ADJ_EINVAL;
+    ADJ_TRY(check_ptrs({w->W_in, w->b_a, w->W_o, xhat, a, c, h}));
+    ADJ_TRY(check_opt({xres, y, y_x}));
+    if (y_x && (!y || dims->x_dtype != ADJ_BF16)) return ADJ_EINVAL;
+    Layout L;
+    ADJ_TRY(check_ws(dims, ADJ_OP_FWD, 0, ws, ws_bytes, &L));
+    const int64_t B = dims->B, T = dims->T, BT = B * T;
+    const int P = dims->P, N = dims->N;
+    if (BT == 0) return ADJ_OK;
+    const bool xbf = dims->x_dtype == ADJ_BF16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *u = reinterpret_cast<float *>(at(ws, L.buf0));
+    // [z_a | u | c] = xhat W_in;  a = sigmoid(z_a + b_a)
+    GemmEpilogue e = epi(Epi::ProjIn);
+    e.out0 = a; e.out1 = u; e.out2 = c; e.bias = w->b_a; e.N = N;
+    {
+        ProfScope ps(K_PROJ_IN, st);
+        ADJ_CUDA(launch_gemm(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), op1(w->W_in, 1, 3 * int64_t(N), xbf), e, 1, st));
+    }
+    // h_t = a_t h_{t-1} + u_t
+    {
+        ProfScope ps(K_FWD_SCAN, st);
+        ADJ_CUDA(launch_fwd_scan(a, u, h, B, T, N, at(ws, L.scan), status_word(ws), st));
+    }
+    if (y) {
+        // y = xres + (c . h) W_o
+        GemmEpilogue e2 = epi(Epi::StoreAdd);
+        e2.out0 = y; e2.out_x = y_x; e2.ld = P;
+        e2.add = xres ? static_cast<const void *>(xres) : xhat;
+        e2.add_bf16 = !xres && xbf;
+        ProfScope ps(K_PROJ_OUT, st);
+        ADJ_CUDA(launch_gemm(BT, P, N, op1(c, N, 1, false, h), op1(w->W_o, 1, P, xbf), e2, 1, st));
+    }
+    return ADJ_OK;
+}
+
+adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *target, float *gy, double *loss,
+                        void *ws, size_t ws_bytes, void *stream) {
+    ADJ_TRY(check_dims(dims));
+    ADJ_TRY(check_ptrs({y, target}));
+    ADJ_TRY(check_opt({gy, loss}));
+    if (!gy && !loss) return ADJ_EINVAL;
+    Layout L;
+    ADJ_TRY(check_ws(dims, ADJ_OP_LOSS, 0, ws, ws_bytes, &L));
+    const int64_t count = dims->B * dims->T * dims->P;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (count == 0) {
+        if (loss) ADJ_CUDA(cudaMemsetAsync(loss, 0, sizeof(double), st));
+        return ADJ_OK;
+    }
+    ProfScope ps(K_LOSS, st, loss ? 2 : 1);
+    ADJ_CUDA(launch_loss(y, target, gy, count, reinterpret_cast<double *>(at(ws, L.part0)), loss_blocks(count), loss, st));
+    return ADJ_OK;
+}
+
+adj_status adj_bwd_full(const adj_dims *dims, const adj_weights *w, const float *a, const float *c, const float *h,
+                        const float *gy, void *D_a, void *D_u, void *D_c, void *E, void *ws, size_t ws_bytes,
+                        void *stream) {
+    return bwd_common(dims, w, a, c, h, gy, D_a, D_u, D_c, E, 0, ADJ_OP_BWD_FULL, ws, ws_bytes, stream);
+}
+
+adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float *a, const float *c, const float *h,
+                         const float *gy, void *D_a, void *D_u, void *D_c, void *E, int64_t Tbar, void *ws,
+                         size_t ws_bytes, void *stream) {
+    return bwd_common(dims, w, a, c, h, gy, D_a, D_u, D_c, E, Tbar, ADJ_OP_BWD_TRUNC, ws, ws_bytes, stream);
+}
+
+adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void *xhat, const void *D_a,
+                          const void *D_u, const void *D_c, const void *E, const float *gy, float *dW_in,
+                          float *db_a, float *dW_o, float *gy_prev, int accumulate, void *ws, size_t ws_bytes,
+                          void *stream) {
+    ADJ_TRY(check_dims(dims));
+    if (!w) return ADJ_EINVAL;
+    ADJ_TRY(check_ptrs({w->W_in, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o}));
+    ADJ_TRY(check_opt({gy_prev}));
+    if (accumulate != 0 && accumulate != 1) return ADJ_EINVAL;
+    Layout L;
+    ADJ_TRY(check_ws(dims, ADJ_OP_PARAM, 0, ws, ws_bytes, &L));
+    const int64_t BT = dims->B * dims->T;
+    const int P = dims->P, N = dims->N;
+    const bool xbf = dims->x_dtype == ADJ_BF16, dbf = dims->d_dtype == ADJ_BF16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (BT == 0) {
+        if (!accumulate) {
+            ADJ_CUDA(cudaMemsetAsync(dW_in, 0, size_t(P) * 3 * N * 4, st));
+            ADJ_CUDA(cudaMemsetAsync(db_a, 0, size_t(N) * 4, st));
+            ADJ_CUDA(cudaMemsetAsync(dW_o, 0, size_t(N) * P * 4, st));
+        }
+        return ADJ_OK;
+    }
+    const int s = param_splits(dims);
+    float *part_in = reinterpret_cast<float *>(at(ws, L.part0));
+    float *part_o = reinterpret_cast<float *>(at(ws, L.part1));
+    // dW_in = xhat^T [D_a | D_u | D_c]
+    GemmEpilogue e = epi(Epi::Partial);
+    e.out0 = part_in;
+    {
+        ProfScope ps(K_PARAM_DWIN, st);
+        ADJ_CUDA(launch_gemm(P, 3 * int64_t(N), BT, op1(xhat, 1, P, xbf), op3(D_a, D_u, D_c, N, 1, N, dbf), e, s, st));
+    }
+    {
+        ProfScope ps(K_SPLITK, st);
+        ADJ_CUDA(launch_splitk_reduce(part_in, s, int64_t(P) * 3 * N, dW_in, accumulate, st));
+    }
+    // dW_o = E^T gy
+    GemmEpilogue e2 = epi(Epi::Partial);
+    e2.out0 = part_o;
+    {
+        ProfScope ps(K_PARAM_DWO, st);
+        ADJ_CUDA(launch_gemm(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s, st));
+    }
+    {
+        ProfScope ps(K_SPLITK, st);
+        ADJ_CUDA(launch_splitk_reduce(part_o, s, int64_t(N) * P, dW_o, accumulate, st));
+    }
+    // db_a = sum_t D_a
+    {
+        ProfScope ps(K_COLSUM, st, 2);
+        ADJ_CUDA(launch_colsum(D_a, dbf, BT, N, reinterpret_cast<float *>(at(ws, L.part2)), colsum_blocks(dims), db_a,
+                               accumulate, st));
+    }
+    if (gy_prev) {
+        // gy_prev = gy + [D_a | D_u | D_c] W_in^T
+        GemmEpilogue e3 = epi(Epi::StoreAdd);
+        e3.out0 = gy_prev; e3.add = gy; e3.ld = P;
+        ProfScope ps(K_INPUT_GRAD, st);
+        ADJ_CUDA(launch_gemm(BT, P, 3 * int64_t(N), op3(D_a, D_u, D_c, N, N, 1, dbf),
+                             op1(w->W_in, 3 * int64_t(N), 1, xbf), e3, 1, st));
+    }
+    return ADJ_OK;
+}
+
+adj_status adj_stream_status(void *ws, void *stream) {
+    if (!ws) return ADJ_EINVAL;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return ADJ_EALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return ADJ_ECUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ADJ_ECUDA;
+    if (word) {
+        if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return ADJ_ECUDA;
+        return ADJ_ETIMEOUT;
+    }
+    return ADJ_OK;
+}
+
+const char *adj_status_str(adj_status s) {
+    switch (s) {
+    case ADJ_OK: return "ok";
+    case ADJ_EINVAL: return "invalid argument";
+    case ADJ_ESHAPE: return "unsupported shape";
+    case ADJ_EALIGN: return "misaligned pointer";
+    case ADJ_EDTYPE: return "unsupported dtype";
+    case ADJ_EWORKSPACE: return "workspace too small";
+    case ADJ_ECUDA: return "CUDA error";
+    case ADJ_ETIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+// adj_internal.cuh -- helpers shared by the kernels of libadj.so (device side and
+// launcher declarations).  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/adj.h"
+
+namespace adj {
+
+// ---------------------------------------------------------------- status word
+// Word 0 of the workspace: sticky device status; bit ADJ_ST_TIMEOUT is set by a
+// bounded wait that gave up.  Words 1..63 are reserved.
+constexpr unsigned ST_TIMEOUT = 1u;
+constexpr size_t WS_HEADER = 256;
+
+// Iteration limit of every device-side spin (look-back flags, mbarriers).  With
+// the back-off below one wait gives up after well under a second.
+constexpr int SPIN_LIMIT = 1 << 22;
+
+__device__ __forceinline__ void record_timeout(unsigned *status) {
+    atomicOr(status, ST_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- memory ops
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// L2-coherent loads/stores for look-back descriptors (never served from a stale L1 line).
+__device__ __forceinline__ float4 ld_cg4(const float4 *p) { return __ldcg(p); }
+__device__ __forceinline__ void st_cg4(float4 *p, float4 v) { __stcg(p, v); }
+
+// streaming loads/stores of the big token-major arrays
+__device__ __forceinline__ float4 ld_stream4(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
+__device__ __forceinline__ float4 ld_keep4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
+__device__ __forceinline__ void st_stream4(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
+
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<unsigned *>(&lo);
+    u.y = *reinterpret_cast<unsigned *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
+// Wait until *flag != 0; returns the flag, or 0 after SPIN_LIMIT polls (status recorded).
+__device__ __forceinline__ unsigned wait_flag(const unsigned *flag, unsigned *status) {
+    for (int it = 0; it < SPIN_LIMIT; ++it) {
+        unsigned v = ld_acquire(flag);
+        if (v) return v;
+        if (it > 64) __nanosleep(128);
+    }
+    record_timeout(status);
+    return 0;
+}
+
+// ---------------------------------------------------------------- float4 arithmetic
+__device__ __forceinline__ float4 f4(float s) { return make_float4(s, s, s, s); }
+__device__ __forceinline__ float4 operator*(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+__device__ __forceinline__ float4 operator+(float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ float4 operator-(float4 a, float4 b) { return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+// a * b + c, one rounding per lane
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
+    return make_float4(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y), fmaf(a.z, b.z, c.z), fmaf(a.w, b.w, c.w));
+}
+
+// ---------------------------------------------------------------- launchers
+struct ScanWs {               // look-back descriptors carved from the workspace
+    unsigned *ticket;         // 1 counter
+    unsigned *flags;          // [nseq * nchunks]
+    float4 *agg0, *agg1;      // [nseq * nchunks * 32] chunk aggregates (2 components)
+    float4 *inc0, *inc1;      // [nseq * nchunks * 32] inclusive prefixes
+};
+
+size_t scan_ws_bytes(int64_t B, int64_t T, int N);
+ScanWs scan_ws_carve(void *base, int64_t B, int64_t T, int N);
+
+cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
+                            void *scan_ws, unsigned *status, cudaStream_t st);
+cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
+                            int64_t T, int N, int64_t Tbar, void *scan_ws, unsigned *status,
+                            cudaStream_t st);
+cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, const float *h,
+                            const float *R, void *D_a, void *D_u, void *D_c, void *E, bool d_bf16,
+                            int64_t B, int64_t T, int N, int64_t Tbar, void *scan_ws,
+                            unsigned *status, cudaStream_t st);
+
+// Generic GEMM C[M,Nc] = A[M,K] B[K,Nc] with strided, optionally blocked operands.
+struct GemmOperand {
+    const void *p[3];    // up to three arrays split along K (A) or along Nc (B)
+    int64_t blk;         // split size (K for A, Nc for B); >= the dimension if one array
+    int64_t s_row;       // stride of the M (A) / Nc (B) index within one array
+    int64_t s_k;         // stride of the K index
+    bool bf16;           // element type: bf16 or fp32
+    const float *mul;    // optional fp32 array multiplied elementwise (A only, same strides)
+};
+
+enum class Epi { ProjIn, Store, StoreAdd, Partial };
+
+struct GemmEpilogue {
+    Epi kind;
+    float *out0, *out1, *out2;  // ProjIn: a, u, c [M,N]; Store/StoreAdd: out0 [M,ld]; Partial: out0 base
+    void *out_x;                // Store/StoreAdd: optional bf16 copy of out0
+    const void *add;            // StoreAdd: out0 = acc + add (fp32, or bf16 if add_bf16)
+    bool add_bf16;
+    const float *bias;          // ProjIn: b_a [N]
+    int64_t ld;                 // row stride of out0/add/out_x
+    int N;                      // ProjIn: width of each block
+};
+
+cudaError_t launch_gemm(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
+                        const GemmEpilogue &ep, int splits, cudaStream_t st);
+
+cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out,
+                                 int accumulate, cudaStream_t st);
+cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk,
+                          float *out, int accumulate, cudaStream_t st);
+cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t count,
+                        double *part, int nblk, double *loss, cudaStream_t st);
+
+}  // namespace adj

@@ -1,0 +1,163 @@
+"""ctypes binding of libadj.so (include/adj.h): argument marshalling only.
+
+Every function takes device pointers as ints, torch tensors or None, forwards them
+to the C ABI unchanged and raises ``AdjError`` on a non-zero status.  There is no
+fallback: if the library has not been built the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libadj.so")
+
+F32, BF16 = 0, 1
+OP_FWD, OP_BWD_FULL, OP_BWD_TRUNC, OP_PARAM, OP_LOSS = 0, 1, 2, 3, 4
+STATUS = {0: "ADJ_OK", 1: "ADJ_EINVAL", 2: "ADJ_ESHAPE", 3: "ADJ_EALIGN", 4: "ADJ_EDTYPE",
+          5: "ADJ_EWORKSPACE", 6: "ADJ_ECUDA", 7: "ADJ_ETIMEOUT"}
+EXPORTS = ("adj_workspace_bytes", "adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc",
+           "adj_param_grad", "adj_stream_status", "adj_status_str", "adj_launch_count", "adj_profile_enable",
+           "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read")
+
+
+class AdjError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("P", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("x_dtype", ctypes.c_int32), ("d_dtype", ctypes.c_int32)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("W_in", ctypes.c_void_p), ("b_a", ctypes.c_void_p), ("W_o", ctypes.c_void_p)]
+
+
+_lib = None
+_VP, _SZ, _I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
+_PD, _PW = ctypes.POINTER(Dims), ctypes.POINTER(Weights)
+
+
+def load(path: str = LIB_PATH):
+    """Open libadj.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libadj.so is not built ({path}); run adjoint_gradients_long_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        lib.adj_workspace_bytes.argtypes = [_PD, ctypes.c_int, _I64]
+        lib.adj_workspace_bytes.restype = _SZ
+        lib.adj_fwd_scan.argtypes = [_PD, _PW] + [_VP] * 8 + [_SZ, _VP]
+        lib.adj_loss_mse.argtypes = [_PD] + [_VP] * 5 + [_SZ, _VP]
+        lib.adj_bwd_full.argtypes = [_PD, _PW] + [_VP] * 9 + [_SZ, _VP]
+        lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 8 + [_I64, _VP, _SZ, _VP]
+        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 11 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_stream_status.argtypes = [_VP, _VP]
+        lib.adj_status_str.argtypes = [ctypes.c_int]
+        lib.adj_status_str.restype = ctypes.c_char_p
+        lib.adj_launch_count.restype = ctypes.c_ulonglong
+        lib.adj_profile_enable.argtypes = [ctypes.c_int]
+        lib.adj_profile_name.argtypes = [ctypes.c_int]
+        lib.adj_profile_name.restype = ctypes.c_char_p
+        lib.adj_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
+        lib.adj_profile_read.restype = ctypes.c_int
+        for f in ("adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc", "adj_param_grad",
+                  "adj_stream_status"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def ptr(x):
+    """Device address of a tensor / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise AdjError(what, st)
+
+
+def dims(B, T, P, N, x_dtype=F32, d_dtype=F32) -> Dims:
+    return Dims(B, T, P, N, x_dtype, d_dtype)
+
+
+def weights(W_in, b_a, W_o) -> Weights:
+    return Weights(ptr(W_in), ptr(b_a), ptr(W_o))
+
+
+def workspace_bytes(d: Dims, op: int, Tbar: int = 0) -> int:
+    return load().adj_workspace_bytes(ctypes.byref(d), op, Tbar)
+
+
+def fwd_scan(d, w, xhat, xres, a, c, h, y, y_x, ws, ws_bytes, stream=None):
+    _check(load().adj_fwd_scan(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(xres), ptr(a), ptr(c), ptr(h),
+                               ptr(y), ptr(y_x), ptr(ws), ws_bytes, _stream(stream)), "adj_fwd_scan")
+
+
+def loss_mse(d, y, target, gy, loss, ws, ws_bytes, stream=None):
+    _check(load().adj_loss_mse(ctypes.byref(d), ptr(y), ptr(target), ptr(gy), ptr(loss), ptr(ws), ws_bytes,
+                               _stream(stream)), "adj_loss_mse")
+
+
+def bwd_full(d, w, a, c, h, gy, D_a, D_u, D_c, E, ws, ws_bytes, stream=None):
+    _check(load().adj_bwd_full(ctypes.byref(d), ctypes.byref(w), ptr(a), ptr(c), ptr(h), ptr(gy), ptr(D_a),
+                               ptr(D_u), ptr(D_c), ptr(E), ptr(ws), ws_bytes, _stream(stream)), "adj_bwd_full")
+
+
+def bwd_trunc(d, w, a, c, h, gy, D_a, D_u, D_c, E, Tbar, ws, ws_bytes, stream=None):
+    _check(load().adj_bwd_trunc(ctypes.byref(d), ctypes.byref(w), ptr(a), ptr(c), ptr(h), ptr(gy), ptr(D_a),
+                                ptr(D_u), ptr(D_c), ptr(E), int(Tbar), ptr(ws), ws_bytes, _stream(stream)),
+           "adj_bwd_trunc")
+
+
+def param_grad(d, w, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o, gy_prev, accumulate, ws, ws_bytes, stream=None):
+    _check(load().adj_param_grad(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(D_a), ptr(D_u), ptr(D_c), ptr(E),
+                                 ptr(gy), ptr(dW_in), ptr(db_a), ptr(dW_o), ptr(gy_prev), int(accumulate), ptr(ws),
+                                 ws_bytes, _stream(stream)), "adj_param_grad")
+
+
+def stream_status(ws, stream=None) -> int:
+    return load().adj_stream_status(ptr(ws), _stream(stream))
+
+
+def status_str(s: int) -> str:
+    return load().adj_status_str(s).decode()
+
+
+def launch_count() -> int:
+    return int(load().adj_launch_count())
+
+
+def profile_enable(on: bool = True):
+    load().adj_profile_enable(int(on))
+
+
+def profile_reset():
+    load().adj_profile_reset()
+
+
+def profile_read() -> dict:
+    """{kernel kind: (launches, total device ms)} recorded since the last reset."""
+    L = load()
+    out = {}
+    for i in range(L.adj_profile_kernels()):
+        n, ms = ctypes.c_int64(0), ctypes.c_double(0.0)
+        _check(L.adj_profile_read(i, ctypes.byref(n), ctypes.byref(ms)), "adj_profile_read")
+        if n.value:
+            out[L.adj_profile_name(i).decode()] = (int(n.value), float(ms.value))
+    return out

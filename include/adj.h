@@ -1,0 +1,159 @@
+/*
+ * adj.h -- C ABI of libadj.so, the GB300 (sm_103a) adjoint-sharding gradient path
+ * for residual stacks of diagonal selective state-space layers.
+ *
+ * Source of the operations: the review page "Adjoint sharding for very long
+ * context training of state space models" (pith.science), cited as [AS].
+ *
+ * Layer model ([AS] Assumptions: Sec. 3.1 SSM dynamics h_t = A_t h_{t-1} + B_t x_t,
+ * y_t = C_t h_t; Sec. 3.2 residual structure y^K = y^0 + sum_k ytilde^k), in the
+ * diagonal selective form A_t = diag(a_t), B_t xhat_t = u_t, C_t = W_o^T diag(c_t):
+ *     a_t = sigmoid(xhat_t W_a + b_a),  u_t = xhat_t W_B,  c_t = xhat_t W_c,
+ *     h_t = a_t . h_{t-1} + u_t  (h_0 = 0),   y_t = xhat_t + (c_t . h_t) W_o.
+ *
+ * Conventions shared by every call:
+ *  - Arrays are row-major and token-major: [B,T,P] and [B,T,N] with the last
+ *    index contiguous.  Every array pointer is a DEVICE pointer owned by the
+ *    caller; the library never allocates, frees or keeps a pointer after a call.
+ *  - Every pointer must be 16-byte aligned; P and N must be multiples of 8;
+ *    B, T >= 0 are arbitrary (B*T == 0 launches nothing and returns ADJ_OK).
+ *  - `ws` is caller-owned device scratch of at least adj_workspace_bytes() bytes,
+ *    256-byte aligned.  Its first 256 bytes hold the sticky device status word
+ *    read by adj_stream_status(); zero them once (cudaMemset) before first use.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on that stream.  Calls sharing one `ws` must be
+ *    ordered on one stream.
+ *  - Every argument is validated on the host before anything is launched; on an
+ *    error nothing is launched and nothing is written.  Launch failures return
+ *    ADJ_ECUDA.  Bounded device-side waits that give up record ADJ_ETIMEOUT in
+ *    the workspace status word and return without hanging; read it with
+ *    adj_stream_status().  Nothing throws, traps or exits.
+ */
+#ifndef ADJ_H_
+#define ADJ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ADJ_OK = 0,
+    ADJ_EINVAL = 1,      /* null pointer, bad enum, bad window */
+    ADJ_ESHAPE = 2,      /* negative or unsupported sizes */
+    ADJ_EALIGN = 3,      /* a pointer not 16-byte aligned (ws: 256-byte) */
+    ADJ_EDTYPE = 4,      /* unsupported dtype combination */
+    ADJ_EWORKSPACE = 5,  /* ws_bytes below adj_workspace_bytes() */
+    ADJ_ECUDA = 6,       /* a CUDA launch or runtime call failed */
+    ADJ_ETIMEOUT = 7     /* a bounded device wait gave up (see adj_stream_status) */
+} adj_status;
+
+typedef enum { ADJ_F32 = 0, ADJ_BF16 = 1 } adj_dtype;
+
+/* Problem sizes and storage types of one layer call.
+ * x_dtype: storage of the GEMM operands xhat, W_in, W_o (and of y_x below).
+ * d_dtype: storage of the VJP factors D_a, D_u, D_c and of E. */
+typedef struct {
+    int64_t B, T;
+    int32_t P, N;
+    int32_t x_dtype, d_dtype;
+} adj_dims;
+
+/* Layer weights (device pointers).
+ * W_in [P,3N] x_dtype: column blocks [W_a | W_B | W_c].
+ * b_a  [N]   fp32.
+ * W_o  [N,P] x_dtype. */
+typedef struct {
+    const void *W_in;
+    const float *b_a;
+    const void *W_o;
+} adj_weights;
+
+enum { ADJ_OP_FWD = 0, ADJ_OP_BWD_FULL = 1, ADJ_OP_BWD_TRUNC = 2, ADJ_OP_PARAM = 3, ADJ_OP_LOSS = 4 };
+
+/* Workspace bytes that call `op` needs for these sizes (Tbar: the window of
+ * ADJ_OP_BWD_TRUNC, ignored otherwise).  One workspace of the maximum over the
+ * ops used serves them all.  Returns 0 for invalid sizes. */
+size_t adj_workspace_bytes(const adj_dims *dims, int op, int64_t Tbar);
+
+/* Forward pass of one layer storing the states the adjoint needs
+ * ([AS] Referee Report, comment on Algorithm 1: per-token, per-layer states are
+ * kept; here a_t, c_t and h_t, the layer input being the caller's xhat).
+ *   xhat [B,T,P] x_dtype  layer input as GEMM operand
+ *   xres [B,T,P] fp32     residual input; NULL = use xhat's values
+ *   a, c, h [B,T,N] fp32  stored gate, output gate and state (written)
+ *   y    [B,T,P] fp32     layer output xres + (c . h) W_o (written; NULL to skip)
+ *   y_x  [B,T,P] x_dtype  y rounded to x_dtype for the next layer's xhat
+ *                         (written; NULL to skip; must be NULL if x_dtype is fp32) */
+adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *xhat,
+                        const float *xres, float *a, float *c, float *h, float *y, void *y_x,
+                        void *ws, size_t ws_bytes, void *stream);
+
+/* Loss of the last layer and its cotangent: L = sum_{b,t} 1/2 ||y_t - target_t||^2,
+ * gy = y - target.  y, target, gy [B,T,P] fp32 (gy written; may alias y);
+ * loss: one device double (written; NULL to skip).  Uses dims->B, T, P only. */
+adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *target, float *gy,
+                        double *loss, void *ws, size_t ws_bytes, void *stream);
+
+/* Adjoint pass of one layer, full window ([AS] Core claim, Proposition 2, with
+ * lambda_{t,i} = C_t prod_{j=i+1..t} A_j; the sum over t of dl_t/dy_t lambda_{t,i}
+ * is the reverse recurrence of [AS] What carries the argument, Proposition 1).
+ * With g_t = gy_t W_o^T and mu_i = sum_{t>=i} g_t . c_t . prod_{j=i+1..t} a_j it
+ * writes the per-token VJP seeds
+ *   D_a = mu_i . h_{i-1} . a_i (1 - a_i)   (vjp^{A_i}),   D_u = mu_i   (vjp^{B_i}),
+ *   D_c = g_t . h_t,  E = c_t . h_t        (vjp^{C_t}),
+ * all [B,T,N] in d_dtype.  a, c, h [B,T,N] fp32 from adj_fwd_scan; gy [B,T,P]
+ * fp32 = dL/dy of this layer (the total cotangent). */
+adj_status adj_bwd_full(const adj_dims *dims, const adj_weights *w, const float *a,
+                        const float *c, const float *h, const float *gy, void *D_a, void *D_u,
+                        void *D_c, void *E, void *ws, size_t ws_bytes, void *stream);
+
+/* As adj_bwd_full, truncated to the window Tbar ([AS] Core claim, last sentence;
+ * Referee Report on Section 4.3): mu_i sums only t with t - i < Tbar.  Tbar >= 1;
+ * Tbar >= T gives the full result. */
+adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float *a,
+                         const float *c, const float *h, const float *gy, void *D_a, void *D_u,
+                         void *D_c, void *E, int64_t Tbar, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/* Parameter gradients as reductions over all tokens ([AS] Core claim: the sum over
+ * t and i of the VJPs, applied once per token to the summed seeds):
+ *   dW_in [P,3N] = xhat^T [D_a | D_u | D_c],  db_a [N] = sum_t D_a,
+ *   dW_o  [N,P]  = E^T gy,
+ * fp32, overwritten (accumulate = 0) or added to (accumulate = 1).
+ * gy_prev [B,T,P] fp32 (NULL to skip) = gy + [D_a | D_u | D_c] W_in^T, the total
+ * cotangent of the layer below ([AS] residual identity; Proposition 3). */
+adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void *xhat,
+                          const void *D_a, const void *D_u, const void *D_c, const void *E,
+                          const float *gy, float *dW_in, float *db_a, float *dW_o,
+                          float *gy_prev, int accumulate, void *ws, size_t ws_bytes,
+                          void *stream);
+
+/* Synchronise `stream`, return and clear the sticky device status of `ws`
+ * (ADJ_OK or ADJ_ETIMEOUT); ADJ_ECUDA if the stream reports an error. */
+adj_status adj_stream_status(void *ws, void *stream);
+
+/* Static description of a status code. */
+const char *adj_status_str(adj_status s);
+
+/* ---- Launch accounting and per-kernel timing (a library facility; the pages
+ * describe no implementation, so these have no counterpart there).
+ * adj_launch_count: kernels launched by this library since it was loaded.
+ * adj_profile_enable(1): from now on every launch is bracketed by CUDA events
+ *   on its stream; adj_profile_read(id, &n, &ms) synchronises on those events and
+ *   returns the launch count and summed device time of kernel kind `id`
+ *   (0 <= id < adj_profile_kernels(), named by adj_profile_name(id));
+ *   adj_profile_reset() forgets all records.  Host-thread safe. */
+unsigned long long adj_launch_count(void);
+void adj_profile_enable(int on);
+void adj_profile_reset(void);
+int adj_profile_kernels(void);
+const char *adj_profile_name(int id);
+adj_status adj_profile_read(int id, int64_t *launches, double *total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ADJ_H_ */

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads, exports every symbol include/adj.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from adjoint_gradients_long_gb300 import build as adj_build, lib, synth, accounting
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    adj_build.build()
+    return lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "adj.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(adj_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert set(lib.EXPORTS) <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert lib.status_str(s) != "unknown status"
+
+
+FAKE = 1 << 40  # 16-byte aligned address never dereferenced by validation
+
+
+def _w():
+    return lib.Weights(FAKE, FAKE, FAKE)
+
+
+def _call_fwd(d, w=None, xhat=FAKE, a=FAKE, ws=FAKE, ws_bytes=1 << 40, y=None, y_x=None, xres=None):
+    w = w or _w()
+    return lib.load().adj_fwd_scan(ctypes.byref(d), ctypes.byref(w), xhat, xres, a, FAKE, FAKE, y, y_x, ws,
+                                   ws_bytes, None)
+
+
+def test_rejects_bad_shapes(L):
+    assert _call_fwd(lib.dims(1, 16, 12, 8)) == 2          # P not a multiple of 8
+    assert _call_fwd(lib.dims(1, 16, 16, 6)) == 2          # N not a multiple of 8
+    assert _call_fwd(lib.dims(-1, 16, 16, 8)) == 2
+    assert _call_fwd(lib.dims(1, 16, 16, 8, 3, 0)) == 4    # bad dtype
+
+
+def test_rejects_null_and_misaligned(L):
+    d = lib.dims(1, 16, 16, 8)
+    assert _call_fwd(d, xhat=None) == 1
+    assert _call_fwd(d, a=FAKE + 4) == 3
+    assert _call_fwd(d, ws=FAKE + 16) == 3                  # workspace must be 256-byte aligned
+    assert _call_fwd(d, ws=None) == 1
+    assert _call_fwd(d, y=FAKE, y_x=FAKE) == 1              # y_x needs bf16 operands
+
+
+def test_rejects_small_workspace(L):
+    d = lib.dims(2, 1000, 128, 256)
+    need = lib.workspace_bytes(d, lib.OP_FWD)
+    assert need > 0
+    assert _call_fwd(d, ws_bytes=need - 1) == 5
+
+
+def test_rejects_bad_window(L):
+    d = lib.dims(1, 64, 16, 8)
+    st = L.adj_bwd_trunc(ctypes.byref(d), ctypes.byref(_w()), *([FAKE] * 8), 0, FAKE, 1 << 40, None)
+    assert st == 1
+    assert lib.workspace_bytes(d, lib.OP_BWD_TRUNC, 0) == 0
+
+
+def test_workspace_sizes_grow_with_problem(L):
+    small = lib.dims(1, 1024, 128, 256)
+    big = lib.dims(4, 16384, 128, 256)
+    for op in (lib.OP_FWD, lib.OP_BWD_FULL, lib.OP_PARAM, lib.OP_LOSS):
+        assert 0 < lib.workspace_bytes(small, op) <= lib.workspace_bytes(big, op)
+    assert lib.workspace_bytes(big, lib.OP_BWD_TRUNC, 2048) > lib.workspace_bytes(big, lib.OP_BWD_FULL)
+
+
+def test_empty_problem_is_a_noop(L):
+    d = lib.dims(0, 64, 16, 8)
+    need = lib.workspace_bytes(d, lib.OP_FWD)
+    assert _call_fwd(d, ws_bytes=need) == 0
+
+
+def test_workload_table():
+    w = synth.workload("ssm1_p128")
+    assert (w.B, w.T, w.P, w.N, w.K) == (4, 16384, 128, 256, 1)
+    assert synth.workload(5).P == 2048
+    assert accounting.stored_bytes(4, 16384, 1, 256, 128, 4) == 4 * 16384 * (3 * 256 * 4 + 128 * 4)
+
+
+def test_synth_prefix_is_a_slice():
+    full = synth.make_inputs("ssm1_p16", T=5000)
+    part = synth.make_inputs("ssm1_p16", T=1000, t0=4000)
+    assert (full["xhat"][:, 4000:5000] == part["xhat"]).all()
+    assert (full["target"][:, 4000:5000] == part["target"]).all()

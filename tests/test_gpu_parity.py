@@ -1,0 +1,122 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on the
+same seeded inputs.  Tolerances (relative Frobenius error per tensor) are the ones
+fixed for this path: 1e-4 where every operand is fp32, 2e-2 where the GEMM
+operands (xhat, W, D, E) are bf16.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from adjoint_gradients_long_gb300 import synth  # noqa: E402
+from conftest import rel_fro  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = {False: 1e-4, True: 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from adjoint_gradients_long_gb300 import build
+    build.build()
+
+
+def _layers64(inputs):
+    return [{k: np.asarray(v, np.float64) for k, v in W.items()} for W in inputs["layers"]]
+
+
+def run_gpu(inputs, Tbar, bf16):
+    from adjoint_gradients_long_gb300.stack import AdjStack
+    B, T, P, N, K = (inputs[k] for k in ("B", "T", "P", "N", "K"))
+    st = AdjStack(B, T, P, N, K, x_bf16=bf16, d_bf16=bf16, Tbar=Tbar)
+    st.load(inputs)
+    seeds = {}
+
+    def grab(k, s):
+        seeds[k] = [t.float().cpu().numpy() for t in s.D] + [s.gy[(s.K - 1 - k) % 2].cpu().numpy()]
+
+    st.forward()
+    st.loss_grad()
+    st.backward(Tbar, on_layer=grab)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    return st, seeds
+
+
+def compare(inputs, Tbar, bf16, check_states=True):
+    tol = TOL[bf16]
+    st, seeds = run_gpu(inputs, Tbar, bf16)
+    ref = oracle.stack_grad(_layers64(inputs), inputs["xhat"], inputs["target"], Tbar)
+    errs = {}
+    errs["loss"] = abs(float(st.loss.item()) - ref["loss"]) / abs(ref["loss"])
+    for k in range(inputs["K"]):
+        g = st.grads_numpy(k)
+        r = ref["grads"][k]
+        for nm in ("W_a", "W_B", "W_c", "b_a", "W_o"):
+            errs[f"d{nm}[{k}]"] = rel_fro(g[nm], r["d" + nm])
+        errs[f"mu[{k}]"] = rel_fro(seeds[k][1], r["mu"])
+        errs[f"gy[{k}]"] = rel_fro(seeds[k][4], ref["gy"][k])
+        if check_states:
+            so = ref["states"][k]
+            for nm in ("a", "c", "h"):
+                errs[f"{nm}[{k}]"] = rel_fro(getattr(st, nm)[k].cpu().numpy(), so[nm])
+            errs[f"y[{k}]"] = rel_fro(st.y[k].cpu().numpy(), so["y"])
+    errs["gx"] = None
+    bad = {k: v for k, v in errs.items() if v is not None and not v <= tol}
+    assert not bad, (bad, tol)
+    return errs
+
+
+# --------------------------------------------------------------- the five workloads, resized
+
+@pytest.mark.parametrize("Tbar", [None, 1, 5, 37, 256, 1000])
+def test_ssm1_p16_full_size(Tbar):
+    """P=16, N=8, T=256, B=1 at its full size (fp32); windows incl. the degenerate ones."""
+    compare(synth.make_inputs("ssm1_p16"), Tbar, False)
+
+
+@pytest.mark.parametrize("Tbar", [None, 128, 100])
+def test_ssm1_p128_shape(Tbar):
+    """P=128, N=256, B=2, T=1000 (ragged against every chunk size), fp32."""
+    compare(synth.make_inputs("ssm1_p128", T=1000, B=2), Tbar, False)
+
+
+def test_ssm8_p512_shape():
+    """K=8 residual layers, P=512, N=256, T=300, bf16 GEMM operands, window 64."""
+    compare(synth.make_inputs("ssm8_p512", T=300), 64, True)
+
+
+@pytest.mark.parametrize("Tbar", [256, None])
+def test_ssm1_1m_shape(Tbar):
+    """P=256, N=256, b_a=4, T=2000, bf16 GEMM operands, window 256 and full."""
+    compare(synth.make_inputs("ssm1_1m", T=2000), Tbar, True)
+
+
+def test_ssm4_p2048_shape():
+    """K=4 residual layers, P=2048, N=256, T=200, bf16 GEMM operands, window 48."""
+    compare(synth.make_inputs("ssm4_p2048", T=200), 48, True)
+
+
+# --------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("T,B,Tbar", [(1, 1, None), (1, 2, 1), (33, 3, None), (33, 3, 32), (64, 1, 64), (65, 2, 2)])
+def test_small_and_ragged(T, B, Tbar):
+    compare(synth.make_inputs("ssm1_p16", T=T, B=B), Tbar, False)
+
+
+def test_two_layer_fp32_stack():
+    compare(synth.make_inputs("ssm8_p512", T=150, B=2, P=32, N=16, K=2), 40, False)
+
+
+def test_repeat_calls_are_identical():
+    inputs = synth.make_inputs("ssm1_p128", T=777, B=1)
+    st1, _ = run_gpu(inputs, 128, False)
+    st2, _ = run_gpu(inputs, 128, False)
+    for k in range(1):
+        a, b = st1.grads_numpy(k), st2.grads_numpy(k)
+        for nm in a:
+            assert np.array_equal(a[nm], b[nm]), nm
