@@ -10,6 +10,7 @@
 //   param      dW_in = xhat^T [D_a|D_u|D_c], dW_o = E^T gy      (split over tokens, Partial)
 //   input_grad gy_prev = gy + [D_a|D_u|D_c] W_in^T              (StoreAdd)
 #include "adj_internal.cuh"
+#include "adj_epilogue.cuh"
 
 namespace adj {
 
@@ -36,33 +37,6 @@ __device__ __forceinline__ float ld_B(const GemmOperand &Bm, int64_t k, int64_t 
     const int blk = int(n / Bm.blk);
     const int64_t i = (n - blk * Bm.blk) * Bm.s_row + k * Bm.s_k;
     return ld_elem<BF>(Bm.p[blk], i);
-}
-
-__device__ __forceinline__ void epilogue(const GemmEpilogue &ep, int64_t M, int64_t Nc, int z, int64_t m,
-                                         int64_t n, float acc) {
-    switch (ep.kind) {
-    case Epi::ProjIn: {
-        const int blk = int(n / ep.N);
-        const int64_t j = n - int64_t(blk) * ep.N;
-        if (blk == 0) ep.out0[m * ep.N + j] = 1.f / (1.f + expf(-(acc + ep.bias[j])));
-        else if (blk == 1) ep.out1[m * ep.N + j] = acc;
-        else ep.out2[m * ep.N + j] = acc;
-        break;
-    }
-    case Epi::Store:
-    case Epi::StoreAdd: {
-        float v = acc;
-        if (ep.kind == Epi::StoreAdd)
-            v += ep.add_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(ep.add)[m * ep.ld + n])
-                             : static_cast<const float *>(ep.add)[m * ep.ld + n];
-        ep.out0[m * ep.ld + n] = v;
-        if (ep.out_x) static_cast<__nv_bfloat16 *>(ep.out_x)[m * ep.ld + n] = __float2bfloat16_rn(v);
-        break;
-    }
-    case Epi::Partial:
-        ep.out0[(int64_t(z) * M + m) * Nc + n] = acc;
-        break;
-    }
 }
 
 template <bool ABF, bool BBF>

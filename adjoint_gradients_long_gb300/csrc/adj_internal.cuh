@@ -120,6 +120,11 @@ struct GemmEpilogue {
 cudaError_t launch_gemm(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
                         const GemmEpilogue &ep, int splits, cudaStream_t st);
 
+// tcgen05 GEMM (same operand/epilogue contract as launch_gemm); split3: fp32-accurate
+// hi/lo bf16 split, otherwise bf16 operands.
+cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
+                           const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st);
+
 cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out,
                                  int accumulate, cudaStream_t st);
 cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk,

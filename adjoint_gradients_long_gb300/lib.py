@@ -54,7 +54,7 @@ def load(path: str = LIB_PATH):
         lib.adj_loss_mse.argtypes = [_PD] + [_VP] * 5 + [_SZ, _VP]
         lib.adj_bwd_full.argtypes = [_PD, _PW] + [_VP] * 9 + [_SZ, _VP]
         lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 8 + [_I64, _VP, _SZ, _VP]
-        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 11 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 10 + [ctypes.c_int, _VP, _SZ, _VP]
         lib.adj_stream_status.argtypes = [_VP, _VP]
         lib.adj_status_str.argtypes = [ctypes.c_int]
         lib.adj_status_str.restype = ctypes.c_char_p

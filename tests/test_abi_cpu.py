@@ -104,3 +104,14 @@ def test_synth_prefix_is_a_slice():
     part = synth.make_inputs("ssm1_p16", T=1000, t0=4000)
     assert (full["xhat"][:, 4000:5000] == part["xhat"]).all()
     assert (full["target"][:, 4000:5000] == part["target"]).all()
+
+
+def test_binding_arities_match_header(L):
+    src = open(os.path.join(ROOT, "include", "adj.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for name, params in re.findall(r"\b(adj_[a-z_]+)\s*\(([^)]*)\)\s*;", src):
+        params = params.strip()
+        n = 0 if params in ("", "void") else len(params.split(","))
+        fn = getattr(L, name)
+        if fn.argtypes is not None:
+            assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
