@@ -40,15 +40,18 @@ adj_status check_opt(std::initializer_list<const void *> ps) {
     return ADJ_OK;
 }
 
-int param_splits(const adj_dims *d) {
-    const int64_t BT = d->B * d->T;
-    const int64_t tiles = cdiv(d->P, 64) * cdiv(3 * int64_t(d->N), 64);
-    int64_t s = cdiv(608, tiles);
-    if (s > BT / 512) s = BT / 512;
+// Split of the token reduction of a parameter-gradient GEMM: about one wave of CTAs
+// (one 128 x 256 output tile per CTA), at least 4 k-blocks of 64 tokens per split.
+int gemm_splits(int64_t M, int64_t Nc, int64_t K) {
+    const int64_t tiles = cdiv(M, 128) * cdiv(Nc, 256);
+    int64_t s = cdiv(152, tiles);
+    if (s > K / 256) s = K / 256;
     if (s < 1) s = 1;
-    if (s > 64) s = 64;
+    if (s > 128) s = 128;
     return int(s);
 }
+int splits_in(const adj_dims *d) { return gemm_splits(d->P, 3 * int64_t(d->N), d->B * d->T); }
+int splits_o(const adj_dims *d) { return gemm_splits(d->N, d->P, d->B * d->T); }
 int colsum_blocks(const adj_dims *d) {
     int64_t n = cdiv(d->B * d->T, 64);
     if (n > 1024) n = 1024;
@@ -81,9 +84,8 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
         L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
         break;
     case ADJ_OP_PARAM: {
-        const int s = param_splits(d);
-        L.part0 = off; off += al256(size_t(s) * d->P * 3 * d->N * 4);
-        L.part1 = off; off += al256(size_t(s) * d->N * d->P * 4);
+        L.part0 = off; off += al256(size_t(splits_in(d)) * d->P * 3 * d->N * 4);
+        L.part1 = off; off += al256(size_t(splits_o(d)) * d->N * d->P * 4);
         L.part2 = off; off += al256(size_t(colsum_blocks(d)) * d->N * 4);
         break;
     }
@@ -158,7 +160,8 @@ adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a
     e.ld = N;
     {
         ProfScope ps(K_COT_PROJ, st);
-        ADJ_CUDA(launch_gemm(BT, N, P, op1(gy, P, 1, false), op1(w->W_o, P, 1, dims->x_dtype == ADJ_BF16), e, 1, st));
+        ADJ_CUDA(launch_gemm_tc(BT, N, P, op1(gy, P, 1, false), op1(w->W_o, P, 1, dims->x_dtype == ADJ_BF16), e, 1,
+                                dims->x_dtype == ADJ_F32, status_word(ws), st));
     }
     const bool trunc = op == ADJ_OP_BWD_TRUNC && Tbar < T;
     float *R = nullptr;
@@ -203,7 +206,8 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
     e.out0 = a; e.out1 = u; e.out2 = c; e.bias = w->b_a; e.N = N;
     {
         ProfScope ps(K_PROJ_IN, st);
-        ADJ_CUDA(launch_gemm(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), op1(w->W_in, 1, 3 * int64_t(N), xbf), e, 1, st));
+        ADJ_CUDA(launch_gemm_tc(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), op1(w->W_in, 1, 3 * int64_t(N), xbf), e, 1,
+                                !xbf, status_word(ws), st));
     }
     // h_t = a_t h_{t-1} + u_t
     {
@@ -217,7 +221,7 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
         e2.add = xres ? static_cast<const void *>(xres) : xhat;
         e2.add_bf16 = !xres && xbf;
         ProfScope ps(K_PROJ_OUT, st);
-        ADJ_CUDA(launch_gemm(BT, P, N, op1(c, N, 1, false, h), op1(w->W_o, 1, P, xbf), e2, 1, st));
+        ADJ_CUDA(launch_gemm_tc(BT, P, N, op1(c, N, 1, false, h), op1(w->W_o, 1, P, xbf), e2, 1, !xbf, status_word(ws), st));
     }
     return ADJ_OK;
 }
@@ -255,12 +259,13 @@ adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float
 
 adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void *xhat, const void *D_a,
                           const void *D_u, const void *D_c, const void *E, const float *gy, float *dW_in,
-                          float *db_a, float *dW_o, float *gy_prev, int accumulate, void *ws, size_t ws_bytes,
-                          void *stream) {
+                          float *db_a, float *dW_o, float *gy_prev, float *dxhat, int accumulate, void *ws,
+                          size_t ws_bytes, void *stream) {
     ADJ_TRY(check_dims(dims));
     if (!w) return ADJ_EINVAL;
     ADJ_TRY(check_ptrs({w->W_in, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o}));
-    ADJ_TRY(check_opt({gy_prev}));
+    ADJ_TRY(check_opt({gy_prev, dxhat}));
+    if (gy_prev && dxhat) return ADJ_EINVAL;
     if (accumulate != 0 && accumulate != 1) return ADJ_EINVAL;
     Layout L;
     ADJ_TRY(check_ws(dims, ADJ_OP_PARAM, 0, ws, ws_bytes, &L));
@@ -276,7 +281,7 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         }
         return ADJ_OK;
     }
-    const int s = param_splits(dims);
+    const int s_in = splits_in(dims), s_o = splits_o(dims);
     float *part_in = reinterpret_cast<float *>(at(ws, L.part0));
     float *part_o = reinterpret_cast<float *>(at(ws, L.part1));
     // dW_in = xhat^T [D_a | D_u | D_c]
@@ -284,22 +289,23 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
     e.out0 = part_in;
     {
         ProfScope ps(K_PARAM_DWIN, st);
-        ADJ_CUDA(launch_gemm(P, 3 * int64_t(N), BT, op1(xhat, 1, P, xbf), op3(D_a, D_u, D_c, N, 1, N, dbf), e, s, st));
+        ADJ_CUDA(launch_gemm_tc(P, 3 * int64_t(N), BT, op1(xhat, 1, P, xbf), op3(D_a, D_u, D_c, N, 1, N, dbf), e, s_in,
+                                !xbf, status_word(ws), st));
     }
     {
         ProfScope ps(K_SPLITK, st);
-        ADJ_CUDA(launch_splitk_reduce(part_in, s, int64_t(P) * 3 * N, dW_in, accumulate, st));
+        ADJ_CUDA(launch_splitk_reduce(part_in, s_in, int64_t(P) * 3 * N, dW_in, accumulate, st));
     }
     // dW_o = E^T gy
     GemmEpilogue e2 = epi(Epi::Partial);
     e2.out0 = part_o;
     {
         ProfScope ps(K_PARAM_DWO, st);
-        ADJ_CUDA(launch_gemm(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s, st));
+        ADJ_CUDA(launch_gemm_tc(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s_o, !xbf, status_word(ws), st));
     }
     {
         ProfScope ps(K_SPLITK, st);
-        ADJ_CUDA(launch_splitk_reduce(part_o, s, int64_t(N) * P, dW_o, accumulate, st));
+        ADJ_CUDA(launch_splitk_reduce(part_o, s_o, int64_t(N) * P, dW_o, accumulate, st));
     }
     // db_a = sum_t D_a
     {
@@ -307,14 +313,37 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         ADJ_CUDA(launch_colsum(D_a, dbf, BT, N, reinterpret_cast<float *>(at(ws, L.part2)), colsum_blocks(dims), db_a,
                                accumulate, st));
     }
-    if (gy_prev) {
-        // gy_prev = gy + [D_a | D_u | D_c] W_in^T
-        GemmEpilogue e3 = epi(Epi::StoreAdd);
-        e3.out0 = gy_prev; e3.add = gy; e3.ld = P;
+    if (gy_prev || dxhat) {
+        // dxhat = [D_a | D_u | D_c] W_in^T, or gy_prev = gy + dxhat
+        GemmEpilogue e3 = epi(gy_prev ? Epi::StoreAdd : Epi::Store);
+        e3.out0 = gy_prev ? gy_prev : dxhat; e3.add = gy; e3.ld = P;
         ProfScope ps(K_INPUT_GRAD, st);
-        ADJ_CUDA(launch_gemm(BT, P, 3 * int64_t(N), op3(D_a, D_u, D_c, N, N, 1, dbf),
-                             op1(w->W_in, 3 * int64_t(N), 1, xbf), e3, 1, st));
+        ADJ_CUDA(launch_gemm_tc(BT, P, 3 * int64_t(N), op3(D_a, D_u, D_c, N, N, 1, dbf),
+                                op1(w->W_in, 3 * int64_t(N), 1, xbf), e3, 1, !xbf, status_word(ws), st));
     }
+    return ADJ_OK;
+}
+
+adj_status adj_rms_norm(const adj_dims *dims, const float *y, void *xhat, float *r, void *stream) {
+    ADJ_TRY(check_dims(dims));
+    ADJ_TRY(check_ptrs({y, xhat, r}));
+    const int64_t rows = dims->B * dims->T;
+    if (rows == 0) return ADJ_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ProfScope ps(K_RMS_NORM, st);
+    ADJ_CUDA(launch_rms_norm(y, xhat, dims->x_dtype == ADJ_BF16, r, rows, dims->P, ADJ_NORM_EPS, st));
+    return ADJ_OK;
+}
+
+adj_status adj_rms_norm_bwd(const adj_dims *dims, const float *y, const float *r, const float *dxhat,
+                            const float *gy, float *gy_prev, void *stream) {
+    ADJ_TRY(check_dims(dims));
+    ADJ_TRY(check_ptrs({y, r, dxhat, gy, gy_prev}));
+    const int64_t rows = dims->B * dims->T;
+    if (rows == 0) return ADJ_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ProfScope ps(K_RMS_NORM_BWD, st);
+    ADJ_CUDA(launch_rms_norm_bwd(y, r, dxhat, gy, gy_prev, rows, dims->P, st));
     return ADJ_OK;
 }
 

@@ -12,8 +12,8 @@ __device__ __forceinline__ void epilogue(const GemmEpilogue &ep, int64_t M, int6
                                          int64_t n, float acc) {
     switch (ep.kind) {
     case Epi::ProjIn: {
-        const int blk = int(n / ep.N);
-        const int64_t j = n - int64_t(blk) * ep.N;
+        const int nn = int(n), blk = nn / ep.N;
+        const int j = nn - blk * ep.N;
         if (blk == 0) ep.out0[m * ep.N + j] = 1.f / (1.f + expf(-(acc + ep.bias[j])));
         else if (blk == 1) ep.out1[m * ep.N + j] = acc;
         else ep.out2[m * ep.N + j] = acc;

@@ -169,54 +169,115 @@ __device__ __forceinline__ float ld1(const void *p, int64_t i) {
     return __ldg(static_cast<const float *>(p) + i);
 }
 
-// Stage rows [row0, row0+R) x k [k0, k0+64) of an operand.  IS_A: arrays split along k
-// (A); otherwise split along the row index (B, whose rows are output columns).
+// Operand element addressing: A (IS_A) is split along k, B along its row index
+// (its rows are output columns).  Returns the array and the element index.
+template <bool IS_A>
+__device__ __forceinline__ const void *op_at(const GemmOperand &O, int64_t row, int64_t k, int64_t &idx) {
+    int blk;
+    if (IS_A) {
+        blk = int(k / O.blk);
+        idx = row * O.s_row + (k - int64_t(blk) * O.blk) * O.s_k;
+    } else {
+        blk = int(row / O.blk);
+        idx = (row - int64_t(blk) * O.blk) * O.s_row + k * O.s_k;
+    }
+    return O.p[blk];
+}
+
+// Stage rows [row0, row0+R) x k [k0, k0+64) of an operand into a swizzled tile.
+// k-contiguous sources: a work item is 8 consecutive k of one row (two float4 or one
+// 16-byte bf16 vector).  Row-contiguous sources (the token-major operands of the
+// parameter reductions): a work item is a 4-row (fp32) or 8-row (bf16) by 8-k block,
+// loaded as 8 row vectors and transposed in registers.  Loads of a thread's items are
+// issued before any is converted, so several vectors are in flight per thread.
 template <bool BF, bool SPLIT, bool IS_A>
 __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, int64_t rows, int R, int64_t k0,
                                            int64_t kend, uint8_t *hi, uint8_t *lo, int tid) {
-    const bool kfast = O.s_k == 1;
-    const int items = R * 8;
-    for (int it = tid; it < items; it += TC_PROD) {
-        const int r = kfast ? it >> 3 : it % R;
-        const int kc = kfast ? it & 7 : it / R;
-        const int64_t row = row0 + r, k = k0 + kc * 8;
-        float v[8];
-        if (row < rows && k < kend) {
-            int blk;
-            int64_t base;
-            if (IS_A) {
-                blk = int(k / O.blk);
-                base = row * O.s_row + (k - int64_t(blk) * O.blk) * O.s_k;
-            } else {
-                blk = int(row / O.blk);
-                base = (row - int64_t(blk) * O.blk) * O.s_row + k * O.s_k;
-            }
-            const void *p = O.p[blk];
-            if (kfast && k + 8 <= kend) {
-                ld8_contig<BF>(p, base, v);
-                if (IS_A && O.mul) {
-                    float m[8];
-                    ld8_contig<false>(O.mul, base, m);
+    constexpr int BATCH = 2;
+    if (O.s_k == 1) {
+        const int items = R * 8;
+        for (int base_it = tid; base_it < items; base_it += TC_PROD * BATCH) {
+            float v[BATCH][8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] *= m[j];
-                }
-            } else {
+            for (int b = 0; b < BATCH; ++b) {
+                const int it = base_it + b * TC_PROD;
+                const int r = it >> 3, kc = it & 7;
+                const int64_t row = row0 + r, k = k0 + kc * 8;
+                if (it < items && row < rows && k < kend) {
+                    int64_t i;
+                    const void *p = op_at<IS_A>(O, row, k, i);
+                    if (k + 8 <= kend) {
+                        ld8_contig<BF>(p, i, v[b]);
+                        if (IS_A && O.mul) {
+                            float m[8];
+                            ld8_contig<false>(O.mul, i, m);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (k + j < kend) {
-                        const int64_t i = base + int64_t(j) * O.s_k;
-                        v[j] = ld1<BF>(p, i);
-                        if (IS_A && O.mul) v[j] *= __ldg(O.mul + i);
+                            for (int j = 0; j < 8; ++j) v[b][j] *= m[j];
+                        }
                     } else {
-                        v[j] = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            v[b][j] = (k + j < kend) ? ld1<BF>(p, i + j) : 0.f;
+                            if (IS_A && O.mul && k + j < kend) v[b][j] *= __ldg(O.mul + i + j);
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[b][j] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int it = base_it + b * TC_PROD;
+                if (it < items) put8<SPLIT>(hi, lo, it >> 3, it & 7, v[b]);
+            }
+        }
+        return;
+    }
+    // row-contiguous source: RB rows x 8 k per item
+    constexpr int RB = BF ? 8 : 4;
+    const int groups = R / RB, items = groups * 8;
+    for (int it = tid; it < items; it += TC_PROD) {
+        const int g = it % groups, kc = it / groups;
+        const int r0 = g * RB;
+        const int64_t row = row0 + r0, k = k0 + kc * 8;
+        float v[RB][8];   // v[row][k]
+        const bool full = row + RB <= rows && k + 8 <= kend;
+        if (full) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int64_t i;
+                const void *p = op_at<IS_A>(O, row, k + j, i);
+                if (BF) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p) + i));
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                    for (int q = 0; q < RB / 2; ++q) {
+                        const float2 f = __bfloat1622float2(b2[q]);
+                        v[2 * q][j] = f.x;
+                        v[2 * q + 1][j] = f.y;
+                    }
+                } else {
+                    const float4 f = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
+                    v[0][j] = f.x; v[1 % RB][j] = f.y; v[2 % RB][j] = f.z; v[3 % RB][j] = f.w;
                 }
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.f;
+            for (int q = 0; q < RB; ++q)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float x = 0.f;
+                    if (row + q < rows && k + j < kend) {
+                        int64_t i;
+                        const void *p = op_at<IS_A>(O, row + q, k + j, i);
+                        x = ld1<BF>(p, i);
+                    }
+                    v[q][j] = x;
+                }
         }
-        put8<SPLIT>(hi, lo, r, kc, v);
+#pragma unroll
+        for (int q = 0; q < RB; ++q) put8<SPLIT>(hi, lo, r0 + q, kc, v[q]);
     }
 }
 
@@ -288,10 +349,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const TcArgs args) {
             mbar_arrive(smem_u32(&full[s]));
         }
         // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., column chunks (w/4), (w/4)+2, ...
+        // Each 32 x 32 chunk goes through shared memory (the drained stage buffers) so that
+        // the stores of a warp cover one output row segment of 32 consecutive columns.
         const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(accum), 0, abort, args.status));
         tc_fence_after();
+        float *sbuf = reinterpret_cast<float *>(base) + warp * (32 * 33);
         const int q = warp & 3;
-        const int64_t m = m0 + q * 32 + lane;
         for (int c = (warp >> 2) * 32; c < BN; c += 64) {
             float v[32];
             if (ok && nkb > 0) {
@@ -300,13 +363,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const TcArgs args) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
-            if (m < args.M) {
-#pragma unroll 4
-                for (int j = 0; j < 32; ++j) {
-                    const int64_t n = n0 + c + j;
-                    if (n < args.Nc) epilogue(args.ep, args.M, args.Nc, z, m, n, v[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sbuf[lane * 33 + j] = v[j];
+            __syncwarp();
+            const int n = int(n0) + c + lane;
+            if (n < args.Nc) {
+                for (int i = 0; i < 32; ++i) {
+                    const int64_t m = m0 + q * 32 + i;
+                    if (m < args.M) epilogue(args.ep, args.M, args.Nc, z, m, n, sbuf[i * 33 + lane]);
                 }
             }
+            __syncwarp();
         }
     } else if (lane == 0) {
         // ---------------- MMA issuer
@@ -363,9 +430,13 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.M = M; a.Nc = Nc; a.K = K;
     int64_t kper = (K + splits - 1) / splits;
     a.kper = (kper + TC_BK - 1) / TC_BK * TC_BK;
-    int BN = int(Nc < 256 ? (Nc + 31) / 32 * 32 : 256);
-    a.BN = BN;
     const int nkb = int((a.kper + TC_BK - 1) / TC_BK);
+    // Short reductions (a few k-blocks per tile) with many tiles: 128-column tiles, so two
+    // CTAs fit per SM and one's loads overlap the other's epilogue.
+    const int64_t tiles256 = ((Nc + 255) / 256) * ((M + TC_BM - 1) / TC_BM) * splits;
+    int BN = int(Nc < 256 ? (Nc + 31) / 32 * 32 : 256);
+    if (BN > 128 && nkb <= 4 && tiles256 >= 2 * 152) BN = 128;
+    a.BN = BN;
     const int max_stages = split3 ? 2 : 4;
     a.stages = nkb < 1 ? 1 : (nkb < max_stages ? nkb : max_stages);
     a.A = A; a.Bm = Bm; a.ep = ep; a.status = status;

@@ -94,7 +94,7 @@ cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, cons
                             int64_t B, int64_t T, int N, int64_t Tbar, void *scan_ws,
                             unsigned *status, cudaStream_t st);
 
-// Generic GEMM C[M,Nc] = A[M,K] B[K,Nc] with strided, optionally blocked operands.
+// GEMM operands: strided, optionally split over up to three arrays.
 struct GemmOperand {
     const void *p[3];    // up to three arrays split along K (A) or along Nc (B)
     int64_t blk;         // split size (K for A, Nc for B); >= the dimension if one array
@@ -117,11 +117,8 @@ struct GemmEpilogue {
     int N;                      // ProjIn: width of each block
 };
 
-cudaError_t launch_gemm(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
-                        const GemmEpilogue &ep, int splits, cudaStream_t st);
-
-// tcgen05 GEMM (same operand/epilogue contract as launch_gemm); split3: fp32-accurate
-// hi/lo bf16 split, otherwise bf16 operands.
+// tcgen05 GEMM C[M,Nc] = A[M,K] B[K,Nc] with the operand and epilogue contracts above;
+// split3: fp32-accurate hi/lo bf16 split, otherwise bf16 operands.
 cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
                            const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st);
 
@@ -129,6 +126,10 @@ cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, f
                                  int accumulate, cudaStream_t st);
 cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk,
                           float *out, int accumulate, cudaStream_t st);
+cudaError_t launch_rms_norm(const float *y, void *xhat, bool xbf, float *r, int64_t rows, int P, float eps,
+                            cudaStream_t st);
+cudaError_t launch_rms_norm_bwd(const float *y, const float *r, const float *dx, const float *gy, float *gy_prev,
+                                int64_t rows, int P, cudaStream_t st);
 cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t count,
                         double *part, int nblk, double *loss, cudaStream_t st);
 

@@ -6,25 +6,28 @@
 namespace adj {
 
 // ---------------------------------------------------------------- loss
-// L = sum 1/2 (y - target)^2, gy = y - target; one fp64 partial per block, then one
-// block sums the partials in a fixed order (deterministic).
+// L = sum 1/2 (y - target)^2, gy = y - target.  Each thread sums its elements in fp32
+// (a few dozen terms), the block combines the thread sums in fp64 and writes one
+// partial; one block then sums the partials in a fixed order (deterministic).  FP64
+// arithmetic is kept out of the per-element loop: GB300's fp64 rate is a small
+// fraction of its fp32 rate.
 __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const float *__restrict__ tg,
                                               float *__restrict__ gy, int64_t count, double *__restrict__ part) {
     __shared__ double red[256];
-    double s = 0.0;
+    float s = 0.f;
     const int64_t n4 = count / 4;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
         const float4 r = ld_stream4(y + 4 * i) - ld_stream4(tg + 4 * i);
         if (gy) st_stream4(gy + 4 * i, r);
-        s += 0.5 * (double(r.x) * r.x + double(r.y) * r.y + double(r.z) * r.z + double(r.w) * r.w);
+        s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
     }
     for (int64_t i = 4 * n4 + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count;
          i += int64_t(gridDim.x) * blockDim.x) {
         const float r = y[i] - tg[i];
         if (gy) gy[i] = r;
-        s += 0.5 * double(r) * r;
+        s += 0.5f * r * r;
     }
-    red[threadIdx.x] = s;
+    red[threadIdx.x] = double(s);
     __syncthreads();
     for (int o = 128; o > 0; o >>= 1) {
         if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
@@ -55,18 +58,50 @@ cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t 
 
 // ---------------------------------------------------------------- column sums
 // part[blk][n] = sum over the block's rows of D[row][n]; out[n] (+)= sum_blk part[blk][n].
+// A block is 256 threads = (N/4 column groups of 4) x (256/(N/4) row lanes); each thread
+// reads 4 columns (one 8- or 16-byte vector) of every row-lane-th row, several rows in
+// flight, and the row lanes are combined in shared memory.
+template <bool BF>
+__device__ __forceinline__ float4 ld_row4(const void *D, int64_t i) {
+    if (BF) {
+        const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(D) + i));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    return ld_stream4(static_cast<const float *>(D) + i);
+}
+
 template <bool BF>
 __global__ void __launch_bounds__(256) k_colsum(const void *__restrict__ D, int64_t rows, int N,
                                                 int64_t rows_per_blk, float *__restrict__ part) {
+    __shared__ float4 red[256];
+    const int groups = N / 4 < 256 ? N / 4 : 256;   // column groups handled at once
+    const int lanes = 256 / groups;                  // row lanes
+    const int gq = threadIdx.x % groups, rl = threadIdx.x / groups;
     const int64_t r0 = blockIdx.x * rows_per_blk;
     const int64_t r1 = r0 + rows_per_blk < rows ? r0 + rows_per_blk : rows;
-    for (int n = threadIdx.x; n < N; n += blockDim.x) {
-        float s = 0.f;
-        for (int64_t r = r0; r < r1; ++r) {
-            if (BF) s += __bfloat162float(static_cast<const __nv_bfloat16 *>(D)[r * N + n]);
-            else s += static_cast<const float *>(D)[r * N + n];
+    for (int c0 = 0; c0 < N; c0 += groups * 4) {
+        const int col = c0 + gq * 4;
+        float4 acc = f4(0.f);
+        if (rl < lanes && col < N) {
+            int64_t r = r0 + rl;
+            for (; r + 3 * lanes < r1; r += 4 * lanes) {
+                const float4 v0 = ld_row4<BF>(D, r * N + col), v1 = ld_row4<BF>(D, (r + lanes) * N + col);
+                const float4 v2 = ld_row4<BF>(D, (r + 2 * lanes) * N + col);
+                const float4 v3 = ld_row4<BF>(D, (r + 3 * lanes) * N + col);
+                acc = acc + ((v0 + v1) + (v2 + v3));
+            }
+            for (; r < r1; r += lanes) acc = acc + ld_row4<BF>(D, r * N + col);
         }
-        part[int64_t(blockIdx.x) * N + n] = s;
+        red[threadIdx.x] = acc;
+        __syncthreads();
+        if (threadIdx.x < groups && col < N) {
+            float4 t = f4(0.f);
+            for (int l = 0; l < lanes; ++l) t = t + red[l * groups + threadIdx.x];
+            *reinterpret_cast<float4 *>(part + int64_t(blockIdx.x) * N + col) = t;
+        }
+        __syncthreads();
     }
 }
 
@@ -103,6 +138,77 @@ cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, f
     int64_t blocks = (count + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     k_splitk_reduce<<<unsigned(blocks), 256, 0, st>>>(part, splits, count, out, accumulate);
+    return cudaGetLastError();
+}
+
+}  // namespace adj
+
+namespace adj {
+
+// ---------------------------------------------------------------- normalised layer inputs
+// xhat = y / r, r = sqrt(mean_p y_p^2 + eps), per token row; one warp per row, the row
+// read as float4 (P is a multiple of 8).
+template <bool XBF>
+__global__ void __launch_bounds__(256) k_rms_norm(const float *__restrict__ y, void *__restrict__ xhat,
+                                                  float *__restrict__ r, int64_t rows, int P, float eps) {
+    const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float *yr = y + row * P;
+    float ss = 0.f;
+    for (int p = lane * 4; p < P; p += 128) {
+        const float4 v = ld_keep4(yr + p);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rr = sqrtf(ss / float(P) + eps), inv = 1.f / rr;
+    for (int p = lane * 4; p < P; p += 128) {
+        const float4 v = ld_keep4(yr + p) * f4(inv);
+        if (XBF) st4(static_cast<__nv_bfloat16 *>(xhat) + row * P + p, v);
+        else st4(static_cast<float *>(xhat) + row * P + p, v);
+    }
+    if (lane == 0) r[row] = rr;
+}
+
+// gy_prev = gy + (dx - xhat mean_p(xhat dx)) / r with xhat = y / r recomputed in fp32.
+// gy_prev may alias dx or gy (each element is read before it is written, by one lane).
+__global__ void __launch_bounds__(256) k_rms_norm_bwd(const float *__restrict__ y, const float *__restrict__ r,
+                                                      const float *dx, const float *gy, float *gy_prev,
+                                                      int64_t rows, int P) {
+    const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float inv = 1.f / r[row];
+    const float *yr = y + row * P;
+    const float *dr = dx + row * P;
+    float s = 0.f;
+    for (int p = lane * 4; p < P; p += 128) {
+        const float4 xv = ld_keep4(yr + p) * f4(inv), dv = *reinterpret_cast<const float4 *>(dr + p);
+        s += xv.x * dv.x + xv.y * dv.y + xv.z * dv.z + xv.w * dv.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float4 m = f4(s / float(P));
+    for (int p = lane * 4; p < P; p += 128) {
+        const float4 xv = ld_keep4(yr + p) * f4(inv);
+        const float4 dv = *reinterpret_cast<const float4 *>(dr + p);
+        const float4 gv = *reinterpret_cast<const float4 *>(gy + row * P + p);
+        *reinterpret_cast<float4 *>(gy_prev + row * P + p) = gv + (dv - xv * m) * f4(inv);
+    }
+}
+
+cudaError_t launch_rms_norm(const float *y, void *xhat, bool xbf, float *r, int64_t rows, int P, float eps,
+                            cudaStream_t st) {
+    const unsigned grid = unsigned((rows + 7) / 8);
+    if (xbf) k_rms_norm<true><<<grid, 256, 0, st>>>(y, xhat, r, rows, P, eps);
+    else k_rms_norm<false><<<grid, 256, 0, st>>>(y, xhat, r, rows, P, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rms_norm_bwd(const float *y, const float *r, const float *dx, const float *gy, float *gy_prev,
+                                int64_t rows, int P, cudaStream_t st) {
+    k_rms_norm_bwd<<<unsigned((rows + 7) / 8), 256, 0, st>>>(y, r, dx, gy, gy_prev, rows, P);
     return cudaGetLastError();
 }
 

@@ -17,6 +17,8 @@ enum KernelId {
     K_SPLITK,
     K_COLSUM,
     K_INPUT_GRAD,
+    K_RMS_NORM,
+    K_RMS_NORM_BWD,
     K_COUNT
 };
 

@@ -18,7 +18,8 @@ STATUS = {0: "ADJ_OK", 1: "ADJ_EINVAL", 2: "ADJ_ESHAPE", 3: "ADJ_EALIGN", 4: "AD
           5: "ADJ_EWORKSPACE", 6: "ADJ_ECUDA", 7: "ADJ_ETIMEOUT"}
 EXPORTS = ("adj_workspace_bytes", "adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc",
            "adj_param_grad", "adj_stream_status", "adj_status_str", "adj_launch_count", "adj_profile_enable",
-           "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read")
+           "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read", "adj_rms_norm",
+           "adj_rms_norm_bwd")
 
 
 class AdjError(RuntimeError):
@@ -54,7 +55,9 @@ def load(path: str = LIB_PATH):
         lib.adj_loss_mse.argtypes = [_PD] + [_VP] * 5 + [_SZ, _VP]
         lib.adj_bwd_full.argtypes = [_PD, _PW] + [_VP] * 9 + [_SZ, _VP]
         lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 8 + [_I64, _VP, _SZ, _VP]
-        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 10 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 11 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_rms_norm.argtypes = [_PD] + [_VP] * 4
+        lib.adj_rms_norm_bwd.argtypes = [_PD] + [_VP] * 6
         lib.adj_stream_status.argtypes = [_VP, _VP]
         lib.adj_status_str.argtypes = [ctypes.c_int]
         lib.adj_status_str.restype = ctypes.c_char_p
@@ -65,7 +68,7 @@ def load(path: str = LIB_PATH):
         lib.adj_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
         lib.adj_profile_read.restype = ctypes.c_int
         for f in ("adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc", "adj_param_grad",
-                  "adj_stream_status"):
+                  "adj_stream_status", "adj_rms_norm", "adj_rms_norm_bwd"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -125,10 +128,20 @@ def bwd_trunc(d, w, a, c, h, gy, D_a, D_u, D_c, E, Tbar, ws, ws_bytes, stream=No
            "adj_bwd_trunc")
 
 
-def param_grad(d, w, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o, gy_prev, accumulate, ws, ws_bytes, stream=None):
+def param_grad(d, w, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o, gy_prev, dxhat, accumulate, ws, ws_bytes,
+               stream=None):
     _check(load().adj_param_grad(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(D_a), ptr(D_u), ptr(D_c), ptr(E),
-                                 ptr(gy), ptr(dW_in), ptr(db_a), ptr(dW_o), ptr(gy_prev), int(accumulate), ptr(ws),
-                                 ws_bytes, _stream(stream)), "adj_param_grad")
+                                 ptr(gy), ptr(dW_in), ptr(db_a), ptr(dW_o), ptr(gy_prev), ptr(dxhat), int(accumulate),
+                                 ptr(ws), ws_bytes, _stream(stream)), "adj_param_grad")
+
+
+def rms_norm(d, y, xhat, r, stream=None):
+    _check(load().adj_rms_norm(ctypes.byref(d), ptr(y), ptr(xhat), ptr(r), _stream(stream)), "adj_rms_norm")
+
+
+def rms_norm_bwd(d, y, r, dxhat, gy, gy_prev, stream=None):
+    _check(load().adj_rms_norm_bwd(ctypes.byref(d), ptr(y), ptr(r), ptr(dxhat), ptr(gy), ptr(gy_prev),
+                                   _stream(stream)), "adj_rms_norm_bwd")
 
 
 def stream_status(ws, stream=None) -> int:

@@ -4,11 +4,14 @@ every arithmetic step runs in the library's kernels.
 
 Order of one gradient step ([AS] = review page "Adjoint sharding for very long
 context training of state space models"; [AS] Referee Report on Algorithm 1 for
-the stored states, Core claim for Propositions 2 and 3):
-  for k = 1..K: adj_fwd_scan(k)            stores a^k, c^k, h^k; y^k = xhat^{k+1}
+the stored states, Core claim for Propositions 2 and 3, Load-bearing premise for
+the normalised layer inputs):
+  for k = 1..K: adj_rms_norm(y^{k-1})      xhat^k = y^{k-1} / r^{k-1}   (k >= 2; xhat^1 = input)
+                adj_fwd_scan(k)            stores a^k, c^k, h^k; y^k = y^{k-1} + ytilde^k
   adj_loss_mse                             gy^K = y^K - target, L
   for k = K..1: adj_bwd_{full,trunc}(k)    VJP seeds D_a, D_u, D_c, E of layer k
-                adj_param_grad(k)          dW_in^k, db_a^k, dW_o^k and gy^{k-1}
+                adj_param_grad(k)          dW_in^k, db_a^k, dW_o^k and dxhat^k
+                adj_rms_norm_bwd(k)        gy^{k-1} = gy^k + J^T dxhat^k   (k >= 2)
 """
 from __future__ import annotations
 
@@ -46,13 +49,12 @@ class AdjStack:
         dev = self.device
         z = lambda *s, dtype=torch.float32: torch.zeros(*s, dtype=dtype, device=dev)  # noqa: E731
         # per-layer stored states and outputs
-        self.x = [z(B, T, P, dtype=xt)]                       # GEMM operand of layer k
+        self.x = [z(B, T, P, dtype=xt) for _ in range(K)]    # layer inputs xhat^k (GEMM operands)
+        self.r = [z(B, T) for _ in range(K - 1)]              # rms of y^k for the next layer's input
         self.a = [z(B, T, N) for _ in range(K)]
         self.c = [z(B, T, N) for _ in range(K)]
         self.h = [z(B, T, N) for _ in range(K)]
         self.y = [z(B, T, P) for _ in range(K)]                # fp32 residual stream y^k
-        for _ in range(K - 1):
-            self.x.append(z(B, T, P, dtype=xt) if x_bf16 else None)
         self.target = z(B, T, P)
         self.D = [z(B, T, N, dtype=dt) for _ in range(4)]     # D_a, D_u, D_c, E
         self.gy = [z(B, T, P), z(B, T, P)]
@@ -72,7 +74,7 @@ class AdjStack:
 
     # ------------------------------------------------------------------ inputs
     def layer_input(self, k):
-        return self.x[k] if (k == 0 or self.x_bf16) else self.y[k - 1]
+        return self.x[k]
 
     def load(self, inputs: dict):
         """Copy seeded host inputs (synth.make_inputs) to the device."""
@@ -93,10 +95,12 @@ class AdjStack:
     # ------------------------------------------------------------------ calls
     def forward(self, stream=None):
         for k in range(self.K):
-            y_x = self.x[k + 1] if (self.x_bf16 and k + 1 < self.K) else None
-            xres = self.y[k - 1] if k > 0 else None
-            lib.fwd_scan(self.dims, self.w[k], self.layer_input(k), xres, self.a[k], self.c[k], self.h[k],
-                         self.y[k], y_x, self.ws, self.ws_bytes, stream)
+            xres = None
+            if k > 0:
+                lib.rms_norm(self.dims, self.y[k - 1], self.x[k], self.r[k - 1], stream)
+                xres = self.y[k - 1]
+            lib.fwd_scan(self.dims, self.w[k], self.x[k], xres, self.a[k], self.c[k], self.h[k],
+                         self.y[k], None, self.ws, self.ws_bytes, stream)
 
     def loss_grad(self, stream=None):
         lib.loss_mse(self.dims, self.y[-1], self.target, self.gy[0], self.loss, self.ws, self.ws_bytes, stream)
@@ -115,9 +119,12 @@ class AdjStack:
                               self.ws, self.ws_bytes, stream)
             if on_layer is not None:
                 on_layer(k, self)
-            gy_prev = self.gy[1 - cur] if k > 0 else None
-            lib.param_grad(self.dims, self.w[k], self.layer_input(k), Da, Du, Dc, E, gy, self.dW_in[k],
-                           self.db_a[k], self.dW_o[k], gy_prev, int(accumulate), self.ws, self.ws_bytes, stream)
+            dx = self.gy[1 - cur] if k > 0 else None
+            lib.param_grad(self.dims, self.w[k], self.x[k], Da, Du, Dc, E, gy, self.dW_in[k],
+                           self.db_a[k], self.dW_o[k], None, dx, int(accumulate), self.ws, self.ws_bytes, stream)
+            if k > 0:
+                # gy^{k-1} = gy^k + J^T dxhat^k, in place over dxhat
+                lib.rms_norm_bwd(self.dims, self.y[k - 1], self.r[k - 1], dx, gy, dx, stream)
             cur = 1 - cur
 
     def step(self, Tbar=None, stream=None):

@@ -123,13 +123,30 @@ adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float
  *   dW_in [P,3N] = xhat^T [D_a | D_u | D_c],  db_a [N] = sum_t D_a,
  *   dW_o  [N,P]  = E^T gy,
  * fp32, overwritten (accumulate = 0) or added to (accumulate = 1).
- * gy_prev [B,T,P] fp32 (NULL to skip) = gy + [D_a | D_u | D_c] W_in^T, the total
- * cotangent of the layer below ([AS] residual identity; Proposition 3). */
+ * The cotangent of the layer input, at most one of (NULL to skip):
+ *   gy_prev [B,T,P] fp32 = gy + [D_a | D_u | D_c] W_in^T: the total cotangent of the
+ *           layer below when that layer's output is this layer's input unchanged
+ *           ([AS] residual identity; Proposition 3);
+ *   dxhat   [B,T,P] fp32 = [D_a | D_u | D_c] W_in^T alone, for a normalised input
+ *           (pass it to adj_rms_norm_bwd). */
 adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void *xhat,
                           const void *D_a, const void *D_u, const void *D_c, const void *E,
                           const float *gy, float *dW_in, float *db_a, float *dW_o,
-                          float *gy_prev, int accumulate, void *ws, size_t ws_bytes,
+                          float *gy_prev, float *dxhat, int accumulate, void *ws, size_t ws_bytes,
                           void *stream);
+
+/* Normalised layer input of a stacked layer ([AS] Load-bearing premise: the layers
+ * read "normalized inputs"): per token, xhat = y / r with
+ * r = sqrt(mean_p y_p^2 + ADJ_NORM_EPS).  y [B,T,P] fp32 (the residual stream y^{k-1});
+ * xhat [B,T,P] in dims->x_dtype and r [B,T] fp32 are written.  No workspace. */
+#define ADJ_NORM_EPS 1e-6f
+adj_status adj_rms_norm(const adj_dims *dims, const float *y, void *xhat, float *r, void *stream);
+
+/* Cotangent through the normalisation: gy_prev = gy + (dxhat - xhat mean_p(xhat dxhat)) / r,
+ * xhat = y / r recomputed from y [B,T,P] fp32 and r [B,T] from adj_rms_norm.
+ * gy_prev [B,T,P] fp32 may alias dxhat or gy. */
+adj_status adj_rms_norm_bwd(const adj_dims *dims, const float *y, const float *r, const float *dxhat,
+                            const float *gy, float *gy_prev, void *stream);
 
 /* Synchronise `stream`, return and clear the sticky device status of `ws`
  * (ADJ_OK or ADJ_ETIMEOUT); ADJ_ECUDA if the stream reports an error. */

@@ -14,7 +14,8 @@
  *   a_t = sigmoid(xhat_t W_a + b_a), u_t = xhat_t W_B, c_t = xhat_t W_c     ([AS] Assumptions, Sec. 3.1)
  *   h_t = a_t . h_{t-1} + u_t,  h_0 = 0   (A_t = diag(a_t), B_t xhat_t = u_t)
  *   ytilde_t = (c_t . h_t) W_o            (C_t = W_o^T diag(c_t))
- *   y_t = xhat_t + ytilde_t               ([AS] What carries the argument, residual identity)
+ *   y_t = xres_t + ytilde_t               ([AS] What carries the argument, residual identity;
+ *                                          xres = y^{k-1}, the residual stream entering the layer)
  *
  * Gradient ([AS] Core claim, Proposition 2), for a cotangent gy_t = dL/dy_t:
  *
@@ -54,10 +55,11 @@
 #define ORC_LITERAL 0
 #define ORC_AGGREGATED 1
 
-/* one layer forward, [AS] Assumptions (Sec. 3.1 SSM dynamics, Sec. 3.2 residual) */
+/* one layer forward, [AS] Assumptions (Sec. 3.1 SSM dynamics, Sec. 3.2 residual);
+ * xres (the residual input) may be NULL, meaning xhat itself */
 void orc_layer_forward(int64_t B, int64_t T, int64_t P, int64_t N,
                        const double *W_a, const double *W_B, const double *W_c,
-                       const double *b_a, const double *W_o, const double *xhat,
+                       const double *b_a, const double *W_o, const double *xhat, const double *xres,
                        double *a, double *u, double *c, double *h, double *y)
 {
     for (int64_t b = 0; b < B; ++b) {
@@ -79,8 +81,9 @@ void orc_layer_forward(int64_t B, int64_t T, int64_t P, int64_t N,
                 ht[n] = at[n] * (hprev ? hprev[n] : 0.0) + ut[n];
             }
             double *yt = y + (b * T + t) * P;
+            const double *xr = xres ? xres + (b * T + t) * P : x;
             for (int64_t p = 0; p < P; ++p) {
-                double s = x[p];
+                double s = xr[p];
                 for (int64_t n = 0; n < N; ++n) s += ct[n] * ht[n] * W_o[n * P + p];
                 yt[p] = s;
             }

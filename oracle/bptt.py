@@ -9,21 +9,29 @@ reproduces exactly ([AS] The reading; If this is right, 4th bullet).
 
 Model and stack: [AS] Assumptions (Sec. 3.1 SSM dynamics, Sec. 3.2 residual
 structure), diagonal selective form a = sigmoid(x W_a + b_a), u = x W_B,
-c = x W_c, h_t = a_t h_{t-1} + u_t, y = x + (c h) W_o.
+c = x W_c, h_t = a_t h_{t-1} + u_t, y^k = y^{k-1} + (c h) W_o with y^0 the input;
+layer 1 reads the input, layer k >= 2 reads y^{k-1} scaled to unit root-mean-square
+per token ([AS] Load-bearing premise: "normalized inputs"; EPS below).
 """
 from __future__ import annotations
 
 import numpy as np
 
 PARAMS = ("W_a", "W_B", "W_c", "b_a", "W_o")
+EPS = 1e-6
 
 
 def forward(layers, xhat, dtype=np.float64):
     """Forward pass storing every intermediate; works for float64 and complex128."""
-    x = np.asarray(xhat, dtype=dtype)
+    y_prev = np.asarray(xhat, dtype=dtype)
     cache = []
-    for W in layers:
+    for li, W in enumerate(layers):
         Wa, WB, Wc, ba, Wo = (np.asarray(W[k], dtype=dtype) for k in PARAMS)
+        if li == 0:
+            x, rms = y_prev, None
+        else:
+            rms = np.sqrt(np.sum(y_prev * y_prev, axis=-1, keepdims=True) / y_prev.shape[-1] + EPS)
+            x = y_prev / rms
         z = x @ Wa + ba
         a = 1.0 / (1.0 + np.exp(-z))
         u = x @ WB
@@ -33,9 +41,9 @@ def forward(layers, xhat, dtype=np.float64):
         for t in range(x.shape[1]):
             prev = a[:, t] * prev + u[:, t]
             h[:, t] = prev
-        y = x + (c * h) @ Wo
-        cache.append(dict(x=x, a=a, u=u, c=c, h=h, y=y))
-        x = y
+        y = y_prev + (c * h) @ Wo
+        cache.append(dict(x=x, a=a, u=u, c=c, h=h, y=y, y_in=y_prev, rms=rms))
+        y_prev = y
     return cache
 
 
@@ -92,7 +100,12 @@ def backward(layers, cache, gy_top, Tbar=None):
             W_c=np.einsum("btp,btn->pn", x, dc), b_a=dz.sum(axis=(0, 1)), W_o=dWo,
             mu=dh,
         )
-        gy = gy + dz @ Wa.T + du @ WB.T + dc @ Wc.T
+        dx = dz @ Wa.T + du @ WB.T + dc @ Wc.T
+        if st["rms"] is not None:
+            # through x = y_in / rms(y_in): d y_in = dx / rms - y_in (y_in . dx) / (P rms^3)
+            yi, rms = st["y_in"], st["rms"]
+            dx = dx / rms - yi * np.sum(yi * dx, axis=-1, keepdims=True) / (yi.shape[-1] * rms ** 3)
+        gy = gy + dx
     return grads, gy
 
 

@@ -6,11 +6,15 @@ Source: the review page "Adjoint sharding for very long context training of stat
 space models" (pith.science), cited as [AS].
 
 Stack semantics ([AS] What carries the argument: residual identity
-y^K = y^0 + sum_k ytilde^k; Core claim: Proposition 3):
-  xhat^1 = the input, xhat^{k+1} = y^k, y^k = xhat^k + ytilde^k.
+y^K = y^0 + sum_k ytilde^k; Core claim: Proposition 3; Load-bearing premise: the
+layers read "normalized inputs"):
+  y^0 = xhat^1 = the input; for k >= 2 the layer input is the normalised residual
+  stream xhat^k = y^{k-1} / r^{k-1}, r = sqrt(mean_p (y^{k-1}_p)^2 + EPS) per token;
+  y^k = y^{k-1} + ytilde^k(xhat^k).
   L = sum_{b,t} 1/2 ||y^K_t - target_t||^2, gy^K = y^K - target.
   Layer k's VJP sums are seeded with its total cotangent gy^k = dL/dy^k, and
-  gy^{k-1} = gy^k + dxhat^k (the residual path plus the layer's input path).
+  gy^{k-1} = gy^k + J_k^T dxhat^k (the residual path plus the layer's input path,
+  J_k = dxhat^k/dy^{k-1}: dy = (dxhat - xhat mean_p(xhat dxhat)) / r; J_1 = identity).
   ``cotangent="top"`` instead seeds every layer with gy^K, holding the layer
   inputs fixed -- the other reading of Proposition 3, kept for comparison.
 """
@@ -24,6 +28,7 @@ import numpy as np
 
 LITERAL = 0
 AGGREGATED = 1
+EPS = 1e-6      # normalisation epsilon of the stacked layer inputs
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "adj_oracle.c")
@@ -47,7 +52,7 @@ def build(force: bool = False) -> str:
 
 def _bind(path: str):
     lib = ctypes.CDLL(path)
-    lib.orc_layer_forward.argtypes = [_I64] * 4 + [_D] * 11
+    lib.orc_layer_forward.argtypes = [_I64] * 4 + [_D] * 12
     lib.orc_layer_forward.restype = None
     lib.orc_layer_grad.argtypes = [_I64] * 5 + [ctypes.c_int] + [_D] * 16
     lib.orc_layer_grad.restype = _I64
@@ -78,17 +83,19 @@ def _f64(x):
     return np.ascontiguousarray(x, dtype=np.float64)
 
 
-def layer_forward(W: dict, xhat: np.ndarray) -> dict:
-    """One layer forward in fp64.  xhat [B,T,P]; returns a, u, c, h [B,T,N] and y [B,T,P]."""
+def layer_forward(W: dict, xhat: np.ndarray, xres=None) -> dict:
+    """One layer forward in fp64.  xhat [B,T,P] (layer input), xres [B,T,P] (residual
+    input, default xhat); returns a, u, c, h [B,T,N] and y = xres + ytilde [B,T,P]."""
     lib = _load()
     xhat = _f64(xhat)
+    xr = None if xres is None else _f64(xres)
     B, T, P = xhat.shape
     N = W["W_a"].shape[1]
     Wa, WB, Wc, ba, Wo = (_f64(W[k]) for k in ("W_a", "W_B", "W_c", "b_a", "W_o"))
     a, u, c, h = (np.empty((B, T, N)) for _ in range(4))
     y = np.empty((B, T, P))
     lib.orc_layer_forward(B, T, P, N, _p(Wa), _p(WB), _p(Wc), _p(ba), _p(Wo), _p(xhat),
-                          _p(a), _p(u), _p(c), _p(h), _p(y))
+                          None if xr is None else _p(xr), _p(a), _p(u), _p(c), _p(h), _p(y))
     return dict(a=a, u=u, c=c, h=h, y=y, xhat=xhat)
 
 
@@ -116,14 +123,30 @@ def layer_grad(W: dict, st: dict, gy: np.ndarray, Tbar=None, mode: int = AGGREGA
     return dict(dW_a=dWa, dW_B=dWB, dW_c=dWc, db_a=dba, dW_o=dWo, dxhat=dx, mu=mu, vjp_count=int(count))
 
 
+def normalize(y: np.ndarray):
+    """xhat = y / r, r = sqrt(mean_p y_p^2 + EPS) per token.  Returns (xhat, r[...,1])."""
+    r = np.sqrt(np.mean(y * y, axis=-1, keepdims=True) + EPS)
+    return y / r, r
+
+
+def normalize_vjp(xhat: np.ndarray, r: np.ndarray, dxhat: np.ndarray) -> np.ndarray:
+    """Cotangent of y for xhat = y / r: (dxhat - xhat mean_p(xhat dxhat)) / r."""
+    return (dxhat - xhat * np.mean(xhat * dxhat, axis=-1, keepdims=True)) / r
+
+
 def stack_forward(layers: list, xhat: np.ndarray) -> list:
     """Forward through the residual stack; returns the per-layer states (each with y)."""
     states = []
-    x = _f64(xhat)
-    for W in layers:
-        st = layer_forward(W, x)
+    y_prev = _f64(xhat)
+    for k, W in enumerate(layers):
+        if k == 0:
+            st = layer_forward(W, y_prev)
+        else:
+            x, r = normalize(y_prev)
+            st = layer_forward(W, x, y_prev)
+            st["r_in"] = r
         states.append(st)
-        x = st["y"]
+        y_prev = st["y"]
     return states
 
 
@@ -153,5 +176,8 @@ def stack_grad(layers: list, xhat: np.ndarray, target: np.ndarray, Tbar=None,
         grads[k] = gk
         count += gk["vjp_count"]
         if cotangent == "total":
-            gy = gy + gk["dxhat"]
+            dx = gk["dxhat"]
+            if k > 0:
+                dx = normalize_vjp(states[k]["xhat"], states[k]["r_in"], dx)
+            gy = gy + dx
     return dict(loss=loss, states=states, grads=grads, gy=seeds, gx=gy, vjp_count=count)

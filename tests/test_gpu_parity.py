@@ -112,11 +112,13 @@ def test_two_layer_fp32_stack():
     compare(synth.make_inputs("ssm8_p512", T=150, B=2, P=32, N=16, K=2), 40, False)
 
 
-def test_repeat_calls_are_identical():
+def test_repeat_calls_agree_to_rounding():
+    """The look-back scans combine chunk carries along whichever chain is ready first, so
+    repeated calls agree to fp32 rounding, not bit for bit."""
     inputs = synth.make_inputs("ssm1_p128", T=777, B=1)
     st1, _ = run_gpu(inputs, 128, False)
     st2, _ = run_gpu(inputs, 128, False)
     for k in range(1):
         a, b = st1.grads_numpy(k), st2.grads_numpy(k)
         for nm in a:
-            assert np.array_equal(a[nm], b[nm]), nm
+            assert rel_fro(a[nm], b[nm]) <= 1e-6, nm

@@ -261,3 +261,22 @@ def test_section45_storage_figures():
     gb = vals * i["bytes_per_value"] / 1e9
     assert round(gb) == p["total_GB"]
     assert round(gb / i["gpus"]) == p["per_gpu_GB"]
+
+
+# ---------------------------------------------------------------- normalised stack inputs
+
+def test_normalized_inputs_have_unit_rms():
+    layers, x, tgt = _inputs("ssm8_p512", T=20, B=2, P=16, N=8, K=3)
+    states = oracle.stack_forward(layers, x)
+    for st in states[1:]:
+        rms = np.sqrt(np.mean(st["xhat"] ** 2, axis=-1))
+        assert np.allclose(rms, 1.0, atol=1e-6)
+
+
+def test_normalize_vjp_mutation_is_caught(monkeypatch):
+    """Drop the projection term of the normalisation VJP: BPTT must disagree."""
+    layers, x, tgt = _inputs("ssm8_p512", T=12, B=1, P=8, N=8, K=2)
+    ref = bptt.bptt_grad(layers, x, tgt)
+    monkeypatch.setattr(oracle.oracle, "normalize_vjp", lambda xh, r, dx: dx / r)
+    bad = oracle.stack_grad(layers, x, tgt, None)
+    assert rel_fro(bad["grads"][0]["dW_B"], ref["grads"][0]["W_B"]) > 1e-6
