@@ -155,6 +155,21 @@ adj_status adj_stream_status(void *ws, void *stream);
 /* Static description of a status code. */
 const char *adj_status_str(adj_status s);
 
+/* The forward pass of adj_fwd_scan for callers that cannot allocate device memory
+ * (the paper has no counterpart: it concerns how scratch memory is obtained).
+ * Scratch comes from a 32 MiB array inside the library, which every GPU that loads
+ * the library holds until the process exits, so no workspace is passed.  Inputs and
+ * outputs are as in adj_fwd_scan.  Problems whose adj_workspace_bytes(dims,
+ * ADJ_OP_FWD, 0) exceeds 32 MiB are rejected with ADJ_EWORKSPACE before anything is
+ * launched.  `status` (device pointer to one unsigned, NULL to skip) receives the
+ * call's device status word after the launches (non-zero: a bounded wait gave up).
+ * The first call on a device looks up the array's device address and must come
+ * before any stream capture.  All calls share the array: calls that overlap on the
+ * GPU race.  Allocates nothing (no cudaMalloc/cudaFree). */
+adj_status adj_fwd_scan_noalloc(const adj_dims *dims, const adj_weights *w, const void *xhat,
+                                const float *xres, float *a, float *c, float *h, float *y, void *y_x,
+                                unsigned *status, void *stream);
+
 /* ---- Launch accounting and per-kernel timing (a library facility; the pages
  * describe no implementation, so these have no counterpart there).
  * adj_launch_count: kernels launched by this library since it was loaded.
