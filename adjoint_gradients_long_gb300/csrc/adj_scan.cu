@@ -30,6 +30,7 @@
 namespace adj {
 
 constexpr int SC_WARPS = 8;
+constexpr int SC_LB_BATCH = 2;       // descriptor loads in flight per look-back batch
 constexpr int SC_SLICE = 128;        // channels per CTA
 constexpr int SC_MIN_CHUNK = 32;     // smallest chunk (L = 4); sizes the descriptor arrays
 constexpr unsigned F_AGG = 1u, F_INC = 2u;
@@ -64,16 +65,6 @@ static size_t scan_reset_bytes(int64_t B, int64_t T, int N) {
     return 256 + al256(size_t(n) * 4);
 }
 
-// Lane 0 waits for the descriptor flag, the warp agrees on its value, and every lane
-// then performs its own acquire so that its following descriptor loads are ordered.
-__device__ __forceinline__ unsigned warp_wait_flag(const unsigned *flag, unsigned *status, int lane) {
-    unsigned f = 0;
-    if (lane == 0) f = wait_flag(flag, status);
-    f = __shfl_sync(0xffffffffu, f, 0);
-    if (f) (void)ld_acquire(flag);
-    return f;
-}
-
 // Publish one or two float4 per lane and then the flag (release after a fence).
 __device__ __forceinline__ void warp_publish(float4 *p0, float4 v0, float4 *p1, float4 v1,
                                              unsigned *flag, unsigned fval, int lane) {
@@ -84,10 +75,60 @@ __device__ __forceinline__ void warp_publish(float4 *p0, float4 v0, float4 *p1, 
     if (lane == 0) st_release(flag, fval);
 }
 
+
+// Warp-wide decoupled look-back.  The predecessors of a chunk, nearest first, are
+// p0, p0 + dir, p0 + 2 dir, ... (count of them).  Each round, lane i reads the flag of
+// the i-th not yet consumed predecessor; the warp then folds, for its own channels,
+// every published aggregate up to the nearest inclusive prefix (or up to the first
+// predecessor that has published nothing yet, which it then waits for).  Descriptor
+// loads of one round are issued in batches, so a round costs about two L2 round trips
+// however many predecessors it folds.  extend(acc, agg) folds one more aggregate;
+// finish(acc, inc) returns the carry.  A wait that gives up finishes with `zero_inc`.
+template <class C, class LA, class LI, class EX, class FI>
+__device__ __forceinline__ C warp_lookback(const unsigned *flags, int64_t p0, int dir, int64_t count, C acc,
+                                           LA load_agg, LI load_inc, EX extend, FI finish, C zero_inc,
+                                           unsigned *status, int lane) {
+    int64_t done = 0;
+    for (int round = 0; round < SPIN_LIMIT; ++round) {
+        const bool exists = done + lane < count;
+        const unsigned f = exists ? ld_acquire(&flags[p0 + dir * (done + lane)]) : 0u;
+        const unsigned incl = __ballot_sync(0xffffffffu, exists && f == F_INC);
+        const unsigned miss = __ballot_sync(0xffffffffu, exists && f == 0u);
+        __syncwarp();   // orders every lane's descriptor loads after the flag acquires above
+        const int ji = incl ? __ffs(int(incl)) - 1 : 32, jm = miss ? __ffs(int(miss)) - 1 : 32;
+        int m = ji < jm ? ji : jm;
+        if (int64_t(m) > count - done) m = int(count - done);
+        for (int i0 = 0; i0 < m; i0 += SC_LB_BATCH) {
+            C t[SC_LB_BATCH];
+#pragma unroll
+            for (int b = 0; b < SC_LB_BATCH; ++b)
+                if (i0 + b < m) t[b] = load_agg(p0 + dir * (done + i0 + b));
+#pragma unroll
+            for (int b = 0; b < SC_LB_BATCH; ++b)
+                if (i0 + b < m) acc = extend(acc, t[b]);
+        }
+        done += m;
+        if (ji < jm && ji == m) return finish(acc, load_inc(p0 + dir * done));
+        if (done >= count) return finish(acc, zero_inc);   // not reached: the first chunk is always inclusive
+        if (m == 0) {
+            // the nearest predecessor has published nothing yet: wait for it
+            unsigned fw = 0;
+            if (lane == 0) fw = wait_flag(&flags[p0 + dir * done], status);
+            fw = __shfl_sync(0xffffffffu, fw, 0);
+            if (fw == 0) return finish(acc, zero_inc);
+        }
+    }
+    record_timeout(status);
+    return finish(acc, zero_inc);
+}
+
 // ============================================================================ forward state scan
 // Composite of a token range: h_out = A h_in + H.  (A2,H2) after (A1,H1) = (A2 A1, A2 H1 + H2).
+struct float2x4 {
+    float4 x, y;
+};
 template <int L>
-__global__ void __launch_bounds__(256) k_fwd_scan(const float *__restrict__ a, const float *__restrict__ u,
+__global__ void __launch_bounds__(256, 2) k_fwd_scan(const float *__restrict__ a, const float *__restrict__ u,
                                                   float *__restrict__ h, int64_t T, int N, int nslices,
                                                   int64_t nseq, int64_t nchunks, ScanWs d, unsigned *status) {
     __shared__ unsigned s_ticket;
@@ -135,19 +176,16 @@ __global__ void __launch_bounds__(256) k_fwd_scan(const float *__restrict__ a, c
         float4 carry = f4(0.f);
         if (chunk > 0) {
             warp_publish(&d.agg0[di * 32 + lane], cA, &d.agg1[di * 32 + lane], cH, &d.flags[di], F_AGG, lane);
-            float4 accA = f4(1.f), accH = f4(0.f);
-            for (int64_t p = chunk - 1; p >= 0; --p) {
-                const int64_t pi = seq * nchunks + p;
-                const unsigned f = warp_wait_flag(&d.flags[pi], status, lane);
-                if (f != F_AGG) {  // inclusive (or a wait that gave up: continue with zero)
-                    const float4 iH = f ? ld_cg4(&d.inc1[pi * 32 + lane]) : f4(0.f);
-                    carry = fma4(accA, iH, accH);
-                    break;
-                }
-                const float4 pA = ld_cg4(&d.agg0[pi * 32 + lane]), pH = ld_cg4(&d.agg1[pi * 32 + lane]);
-                accH = fma4(accA, pH, accH);
-                accA = accA * pA;
-            }
+            const int64_t fb = seq * nchunks;
+            // acc = composite of the chunks between the inclusive prefix found and this chunk
+            const float2x4 r = warp_lookback<float2x4>(
+                d.flags + fb, chunk - 1, -1, chunk, float2x4{f4(1.f), f4(0.f)},
+                [&](int64_t p) { return float2x4{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane])}; },
+                [&](int64_t p) { return float2x4{f4(0.f), ld_cg4(&d.inc1[(fb + p) * 32 + lane])}; },
+                [](const float2x4 &acc, const float2x4 &g) { return float2x4{acc.x * g.x, fma4(acc.x, g.y, acc.y)}; },
+                [](const float2x4 &acc, const float2x4 &inc) { return float2x4{f4(0.f), fma4(acc.x, inc.y, acc.y)}; },
+                float2x4{f4(0.f), f4(0.f)}, status, lane);
+            carry = r.y;
         }
         warp_publish(nullptr, f4(0.f), &d.inc1[di * 32 + lane], fma4(cA, carry, cH), &d.flags[di], F_INC, lane);
         sC[lane] = carry;
@@ -179,7 +217,7 @@ __device__ __forceinline__ FwdSeg fseg_then(const FwdSeg &X, const FwdSeg &Y) {
 }
 
 template <int L>
-__global__ void __launch_bounds__(256) k_win_scan(const float *__restrict__ g, const float *__restrict__ c,
+__global__ void __launch_bounds__(256, 2) k_win_scan(const float *__restrict__ g, const float *__restrict__ c,
                                                   const float *__restrict__ a, float *__restrict__ R, int64_t T,
                                                   int N, int nslices, int64_t nseq, int64_t nchunks, int64_t W,
                                                   ScanWs d, unsigned *status) {
@@ -232,22 +270,14 @@ __global__ void __launch_bounds__(256) k_win_scan(const float *__restrict__ g, c
         else warp_publish(&d.agg0[di * 32 + lane], agg.P, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
         FwdSeg carry{f4(1.f), f4(0.f), true};
         if (chunk > 0) {
-            FwdSeg acc{f4(1.f), f4(0.f), false};
-            for (int64_t p = chunk - 1; p >= 0; --p) {
-                const int64_t pi = seq * nchunks + p;
-                const unsigned f = warp_wait_flag(&d.flags[pi], status, lane);
-                if (f != F_AGG) {  // inclusive (or a wait that gave up: continue from the reset state)
-                    FwdSeg inc{f4(1.f), f4(0.f), true};
-                    if (f) inc = FwdSeg{ld_cg4(&d.inc0[pi * 32 + lane]), ld_cg4(&d.inc1[pi * 32 + lane]), true};
-                    carry = fseg_then(inc, acc);
-                    break;
-                }
-                acc = fseg_then(FwdSeg{ld_cg4(&d.agg0[pi * 32 + lane]), ld_cg4(&d.agg1[pi * 32 + lane]), false}, acc);
-                if (acc.cl) {
-                    carry = acc;
-                    break;
-                }
-            }
+            const int64_t fb = seq * nchunks;
+            carry = warp_lookback<FwdSeg>(
+                d.flags + fb, chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
+                [&](int64_t p) { return FwdSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
+                [&](int64_t p) { return FwdSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
+                [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
+                [](const FwdSeg &acc, const FwdSeg &inc) { return fseg_then(inc, acc); },
+                FwdSeg{f4(1.f), f4(0.f), true}, status, lane);
         }
         if (!agg.cl) {
             const FwdSeg inc = fseg_then(carry, agg);
@@ -285,7 +315,7 @@ __device__ __forceinline__ RevSeg rseg_then(const RevSeg &X, const RevSeg &Y) {
 }
 
 template <int L, bool TRUNC, typename TD>
-__global__ void __launch_bounds__(256) k_bwd_scan(const float *__restrict__ g, const float *__restrict__ c,
+__global__ void __launch_bounds__(256, 2) k_bwd_scan(const float *__restrict__ g, const float *__restrict__ c,
                                                   const float *__restrict__ a, const float *__restrict__ h,
                                                   const float *__restrict__ R, TD *__restrict__ Da,
                                                   TD *__restrict__ Du, TD *__restrict__ Dc, TD *__restrict__ E,
@@ -362,22 +392,14 @@ __global__ void __launch_bounds__(256) k_bwd_scan(const float *__restrict__ g, c
         else warp_publish(&d.agg0[di * 32 + lane], agg.Q, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
         RevSeg carry{f4(0.f), f4(0.f), true};
         if (chunk + 1 < nchunks) {
-            RevSeg acc{f4(1.f), f4(0.f), false};
-            for (int64_t p = chunk + 1; p < nchunks; ++p) {
-                const int64_t pi = seq * nchunks + p;
-                const unsigned f = warp_wait_flag(&d.flags[pi], status, lane);
-                if (f != F_AGG) {  // inclusive (or a wait that gave up: continue with zero)
-                    RevSeg inc{f4(0.f), f4(0.f), true};
-                    if (f) inc = RevSeg{ld_cg4(&d.inc0[pi * 32 + lane]), ld_cg4(&d.inc1[pi * 32 + lane]), true};
-                    carry = rseg_then(acc, inc);
-                    break;
-                }
-                acc = rseg_then(acc, RevSeg{ld_cg4(&d.agg0[pi * 32 + lane]), ld_cg4(&d.agg1[pi * 32 + lane]), false});
-                if (acc.cl) {
-                    carry = acc;
-                    break;
-                }
-            }
+            const int64_t fb = seq * nchunks;
+            carry = warp_lookback<RevSeg>(
+                d.flags + fb, chunk + 1, 1, nchunks - 1 - chunk, RevSeg{f4(1.f), f4(0.f), false},
+                [&](int64_t p) { return RevSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
+                [&](int64_t p) { return RevSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
+                [](const RevSeg &acc, const RevSeg &g) { return rseg_then(acc, g); },
+                [](const RevSeg &acc, const RevSeg &inc) { return rseg_then(acc, inc); },
+                RevSeg{f4(0.f), f4(0.f), true}, status, lane);
         }
         if (!agg.cl) {
             const RevSeg inc = rseg_then(agg, carry);
