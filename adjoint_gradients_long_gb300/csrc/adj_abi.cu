@@ -54,7 +54,7 @@ int splits_in(const adj_dims *d) { return gemm_splits(d->P, 3 * int64_t(d->N), d
 int splits_o(const adj_dims *d) { return gemm_splits(d->N, d->P, d->B * d->T); }
 int colsum_blocks(const adj_dims *d) {
     int64_t n = cdiv(d->B * d->T, 64);
-    if (n > 1024) n = 1024;
+    if (n > 608) n = 608;
     return n < 1 ? 1 : int(n);
 }
 int loss_blocks(int64_t count) {

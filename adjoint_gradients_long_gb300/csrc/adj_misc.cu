@@ -105,13 +105,23 @@ __global__ void __launch_bounds__(256) k_colsum(const void *__restrict__ D, int6
     }
 }
 
-__global__ void k_colsum_final(const float *__restrict__ part, int nblk, int N, float *__restrict__ out,
-                               int accumulate) {
-    const int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
+// out[n] (+)= sum over blocks of part[blk][n]: a block owns 32 columns, its 8 row lanes
+// each sum every 8th partial and are combined in a fixed order (deterministic).
+__global__ void __launch_bounds__(256) k_colsum_final(const float *__restrict__ part, int nblk, int N,
+                                                      float *__restrict__ out, int accumulate) {
+    __shared__ float red[8][33];
+    const int col = blockIdx.x * 32 + (threadIdx.x & 31), rl = threadIdx.x >> 5;
     float s = 0.f;
-    for (int b = 0; b < nblk; ++b) s += part[int64_t(b) * N + n];
-    out[n] = accumulate ? out[n] + s : s;
+    if (col < N)
+        for (int b = rl; b < nblk; b += 8) s += part[int64_t(b) * N + col];
+    red[rl][threadIdx.x & 31] = s;
+    __syncthreads();
+    if (rl == 0 && col < N) {
+        float t = 0.f;
+#pragma unroll
+        for (int l = 0; l < 8; ++l) t += red[l][threadIdx.x & 31];
+        out[col] = accumulate ? out[col] + t : t;
+    }
 }
 
 cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk, float *out,
@@ -119,7 +129,7 @@ cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *
     const int64_t rpb = (rows + nblk - 1) / nblk;
     if (bf16) k_colsum<true><<<nblk, 256, 0, st>>>(D, rows, N, rpb, part);
     else k_colsum<false><<<nblk, 256, 0, st>>>(D, rows, N, rpb, part);
-    k_colsum_final<<<(N + 255) / 256, 256, 0, st>>>(part, nblk, N, out, accumulate);
+    k_colsum_final<<<(N + 31) / 32, 256, 0, st>>>(part, nblk, N, out, accumulate);
     return cudaGetLastError();
 }
 

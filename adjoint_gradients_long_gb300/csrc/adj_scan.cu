@@ -128,7 +128,7 @@ struct float2x4 {
     float4 x, y;
 };
 template <int L>
-__global__ void __launch_bounds__(256, 2) k_fwd_scan(const float *__restrict__ a, const float *__restrict__ u,
+__global__ void __launch_bounds__(256, 3) k_fwd_scan(const float *__restrict__ a, const float *__restrict__ u,
                                                   float *__restrict__ h, int64_t T, int N, int nslices,
                                                   int64_t nseq, int64_t nchunks, ScanWs d, unsigned *status) {
     __shared__ unsigned s_ticket;
@@ -143,23 +143,24 @@ __global__ void __launch_bounds__(256, 2) k_fwd_scan(const float *__restrict__ a
     const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
     const int64_t base = b * T * N + ch;
 
-    float4 av[L], uv[L];
-#pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        if (act && t < T) {
-            av[k] = ld_stream4(a + base + t * N);
-            uv[k] = ld_stream4(u + base + t * N);
-        } else {
-            av[k] = f4(1.f);
-            uv[k] = f4(0.f);
-        }
-    }
+    // pass 1: only the composite of this thread's L tokens is kept; the rows stay in L2
+    // and are read again in pass 2, so few registers are live across the look-back and
+    // three CTAs fit per SM.
     float4 A = f4(1.f), H = f4(0.f);
+    {
+        float4 av[L], uv[L];
 #pragma unroll
-    for (int k = 0; k < L; ++k) {
-        H = fma4(av[k], H, uv[k]);
-        A = A * av[k];
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            const bool ok = act && t < T;
+            av[k] = ok ? ld_l2keep4(a + base + t * N) : f4(1.f);
+            uv[k] = ok ? ld_l2keep4(u + base + t * N) : f4(0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            H = fma4(av[k], H, uv[k]);
+            A = A * av[k];
+        }
     }
     sA[w][lane] = A;
     sH[w][lane] = H;
@@ -194,6 +195,14 @@ __global__ void __launch_bounds__(256, 2) k_fwd_scan(const float *__restrict__ a
 
     float4 hc = sC[lane];
     for (int j = 0; j < w; ++j) hc = fma4(sA[j][lane], hc, sH[j][lane]);
+    float4 av[L], uv[L];
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+        const int64_t t = t0 + k;
+        const bool ok = act && t < T;
+        av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
+        uv[k] = ok ? ld_stream4(u + base + t * N) : f4(0.f);
+    }
 #pragma unroll
     for (int k = 0; k < L; ++k) {
         hc = fma4(av[k], hc, uv[k]);
@@ -217,7 +226,7 @@ __device__ __forceinline__ FwdSeg fseg_then(const FwdSeg &X, const FwdSeg &Y) {
 }
 
 template <int L>
-__global__ void __launch_bounds__(256, 2) k_win_scan(const float *__restrict__ g, const float *__restrict__ c,
+__global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g, const float *__restrict__ c,
                                                   const float *__restrict__ a, float *__restrict__ R, int64_t T,
                                                   int N, int nslices, int64_t nseq, int64_t nchunks, int64_t W,
                                                   ScanWs d, unsigned *status) {
@@ -234,25 +243,23 @@ __global__ void __launch_bounds__(256, 2) k_win_scan(const float *__restrict__ g
     const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
     const int64_t base = b * T * N + ch;
 
-    float4 av[L], ev[L];
-#pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        if (act && t < T) {
-            av[k] = ld_stream4(a + base + t * N);
-            ev[k] = ld_stream4(g + base + t * N) * ld_stream4(c + base + t * N);
-        } else {
-            av[k] = f4(1.f);
-            ev[k] = f4(0.f);
-        }
-    }
     FwdSeg G{f4(1.f), f4(0.f), false};
+    {
+        float4 av[L], ev[L];
 #pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        if (t >= T) break;
-        if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
-        else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            const bool ok = act && t < T;
+            av[k] = ok ? ld_l2keep4(a + base + t * N) : f4(1.f);
+            ev[k] = ok ? ld_l2keep4(g + base + t * N) * ld_l2keep4(c + base + t * N) : f4(0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            if (t >= T) break;
+            if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
+            else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
+        }
     }
     sP[w][lane] = G.P;
     sS[w][lane] = G.S;
@@ -290,6 +297,14 @@ __global__ void __launch_bounds__(256, 2) k_win_scan(const float *__restrict__ g
 
     G = FwdSeg{sCP[lane], sCS[lane], true};
     for (int j = 0; j < w; ++j) G = fseg_then(G, FwdSeg{sP[j][lane], sS[j][lane], sCl[j]});
+    float4 av[L], ev[L];
+#pragma unroll
+    for (int k = 0; k < L; ++k) {
+        const int64_t t = t0 + k;
+        const bool ok = act && t < T;
+        av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
+        ev[k] = ok ? ld_stream4(g + base + t * N) * ld_stream4(c + base + t * N) : f4(0.f);
+    }
 #pragma unroll
     for (int k = 0; k < L; ++k) {
         const int64_t t = t0 + k;
@@ -315,7 +330,7 @@ __device__ __forceinline__ RevSeg rseg_then(const RevSeg &X, const RevSeg &Y) {
 }
 
 template <int L, bool TRUNC, typename TD>
-__global__ void __launch_bounds__(256, 2) k_bwd_scan(const float *__restrict__ g, const float *__restrict__ c,
+__global__ void __launch_bounds__(256, 3) k_bwd_scan(const float *__restrict__ g, const float *__restrict__ c,
                                                   const float *__restrict__ a, const float *__restrict__ h,
                                                   const float *__restrict__ R, TD *__restrict__ Da,
                                                   TD *__restrict__ Du, TD *__restrict__ Dc, TD *__restrict__ E,
@@ -334,47 +349,26 @@ __global__ void __launch_bounds__(256, 2) k_bwd_scan(const float *__restrict__ g
     const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
     const int64_t base = b * T * N + ch;
 
-    // rows: a at t0..t0+L, h at t0-1..t0+L-1, g and c at t0..t0+L-1
-    float4 av[L + 1], hv[L + 1], gv[L], cv[L];
-#pragma unroll
-    for (int k = 0; k <= L; ++k) {
-        const int64_t ta = t0 + k, th = t0 + k - 1;
-        av[k] = (act && ta < T) ? ld_keep4(a + base + ta * N) : f4(0.f);
-        hv[k] = (act && th >= 0 && th < T) ? ld_keep4(h + base + th * N) : f4(0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        const bool ok = act && t < T;
-        gv[k] = ok ? ld_stream4(g + base + t * N) : f4(0.f);
-        cv[k] = ok ? ld_stream4(c + base + t * N) : f4(0.f);
-    }
-    // pass 1: the vjp^{C_t} seeds, and per token e_i, b_i, k_i = h_{i-1} a_i (1 - a_i)
-    float4 ev[L], bv[L], kv[L], rv[L];
-#pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        ev[k] = gv[k] * cv[k];
-        bv[k] = av[k + 1];
-        kv[k] = hv[k] * av[k] * (f4(1.f) - av[k]);
-        if (act && t < T) {
-            st4(Dc + base + t * N, gv[k] * hv[k + 1]);
-            st4(E + base + t * N, cv[k] * hv[k + 1]);
-        }
-        rv[k] = f4(0.f);
-        if (TRUNC && act && t < T && t % W != 0 && (t / W + 1) * W < T) {
-            const int64_t m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
-            rv[k] = ld_stream4(R + base + m * N);
-        }
-    }
+    // pass 1: composite of this thread's tokens from e_i = g_i c_i and b_i = a_{i+1}
+    // (0 past the last token); the rows stay in L2 for pass 2.
     RevSeg G{f4(1.f), f4(0.f), false};
+    {
+        float4 ev[L], bv[L];
 #pragma unroll
-    for (int k = L - 1; k >= 0; --k) {
-        const int64_t t = t0 + k;
-        if (t >= T) continue;
-        const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
-        if (end) G = RevSeg{bv[k], ev[k], true};
-        else G = RevSeg{bv[k] * G.Q, fma4(bv[k], G.S, ev[k]), G.cl};
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            const bool ok = act && t < T;
+            ev[k] = ok ? ld_l2keep4(g + base + t * N) * ld_l2keep4(c + base + t * N) : f4(0.f);
+            bv[k] = (act && t + 1 < T) ? ld_l2keep4(a + base + (t + 1) * N) : f4(0.f);
+        }
+#pragma unroll
+        for (int k = L - 1; k >= 0; --k) {
+            const int64_t t = t0 + k;
+            if (t >= T) continue;
+            const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
+            if (end) G = RevSeg{bv[k], ev[k], true};
+            else G = RevSeg{bv[k] * G.Q, fma4(bv[k], G.S, ev[k]), G.cl};
+        }
     }
     sQ[w][lane] = G.Q;
     sS[w][lane] = G.S;
@@ -413,18 +407,34 @@ __global__ void __launch_bounds__(256, 2) k_bwd_scan(const float *__restrict__ g
     // composite of everything after this warp's tokens, then pass 2 backwards
     G = RevSeg{sCQ[lane], sCS[lane], true};
     for (int j = SC_WARPS - 1; j > w; --j) G = rseg_then(RevSeg{sQ[j][lane], sS[j][lane], sCl[j]}, G);
+    // rows: a at t0..t0+L, h at t0-1..t0+L-1, g and c at t0..t0+L-1
+    float4 anext = (act && t0 + L < T) ? ld_keep4(a + base + (t0 + L) * N) : f4(0.f);
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
         const int64_t t = t0 + k;
         if (t >= T) continue;
+        const float4 gk = act ? ld_stream4(g + base + t * N) : f4(0.f);
+        const float4 ck = act ? ld_stream4(c + base + t * N) : f4(0.f);
+        const float4 ak = act ? ld_keep4(a + base + t * N) : f4(0.f);
+        const float4 hk = act ? ld_keep4(h + base + t * N) : f4(0.f);
+        const float4 hp = (act && t > 0) ? ld_keep4(h + base + (t - 1) * N) : f4(0.f);
+        const float4 bk = t + 1 < T ? anext : f4(0.f);
+        const float4 ek = gk * ck;
         const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
-        if (end) G = RevSeg{bv[k], ev[k], true};
-        else G = RevSeg{bv[k] * G.Q, fma4(bv[k], G.S, ev[k]), true};
-        const float4 mu = TRUNC ? fma4(G.Q, rv[k], G.S) : G.S;
-        if (act) {
-            st4(Du + base + t * N, mu);
-            st4(Da + base + t * N, mu * kv[k]);
+        if (end) G = RevSeg{bk, ek, true};
+        else G = RevSeg{bk * G.Q, fma4(bk, G.S, ek), true};
+        float4 mu = G.S;
+        if (TRUNC && act && t % W != 0 && (t / W + 1) * W < T) {
+            const int64_t m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
+            mu = fma4(G.Q, ld_stream4(R + base + m * N), G.S);
         }
+        if (act) {
+            st4(Dc + base + t * N, gk * hk);
+            st4(E + base + t * N, ck * hk);
+            st4(Du + base + t * N, mu);
+            st4(Da + base + t * N, mu * hp * ak * (f4(1.f) - ak));
+        }
+        anext = ak;
     }
 }
 
@@ -443,7 +453,7 @@ cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B,
 
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t W, void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 8;
+    constexpr int L = 4;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);

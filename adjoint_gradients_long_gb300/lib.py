@@ -19,7 +19,7 @@ STATUS = {0: "ADJ_OK", 1: "ADJ_EINVAL", 2: "ADJ_ESHAPE", 3: "ADJ_EALIGN", 4: "AD
 EXPORTS = ("adj_workspace_bytes", "adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc",
            "adj_param_grad", "adj_stream_status", "adj_status_str", "adj_launch_count", "adj_profile_enable",
            "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read", "adj_rms_norm",
-           "adj_rms_norm_bwd")
+           "adj_rms_norm_bwd", "adj_selftest_waits")
 
 
 class AdjError(RuntimeError):
@@ -57,6 +57,8 @@ def load(path: str = LIB_PATH):
         lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 8 + [_I64, _VP, _SZ, _VP]
         lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 11 + [ctypes.c_int, _VP, _SZ, _VP]
         lib.adj_rms_norm.argtypes = [_PD] + [_VP] * 4
+        lib.adj_selftest_waits.argtypes = [_VP, _SZ, ctypes.c_int, _VP]
+        lib.adj_selftest_waits.restype = ctypes.c_int
         lib.adj_rms_norm_bwd.argtypes = [_PD] + [_VP] * 6
         lib.adj_stream_status.argtypes = [_VP, _VP]
         lib.adj_status_str.argtypes = [ctypes.c_int]
@@ -174,3 +176,7 @@ def profile_read() -> dict:
         if n.value:
             out[L.adj_profile_name(i).decode()] = (int(n.value), float(ms.value))
     return out
+
+
+def selftest_waits(ws, ws_bytes, which, stream=None):
+    _check(load().adj_selftest_waits(ptr(ws), ws_bytes, int(which), _stream(stream)), "adj_selftest_waits")

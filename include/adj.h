@@ -170,6 +170,13 @@ adj_status adj_fwd_scan_noalloc(const adj_dims *dims, const adj_weights *w, cons
                                 const float *xres, float *a, float *c, float *h, float *y, void *y_x,
                                 unsigned *status, void *stream);
 
+/* Failure-path self test (a library facility with no counterpart on the pages): runs
+ * the bounded device waits the kernels rely on against a look-back flag that is never
+ * set (which & 1) and an mbarrier that is never arrived on (which & 2).  Each wait gives
+ * up after its limit (about 0.5 s and 2 s), records the timeout in ws's status word and
+ * returns; adj_stream_status(ws) then reports ADJ_ETIMEOUT.  ws needs 512 bytes. */
+adj_status adj_selftest_waits(void *ws, size_t ws_bytes, int which, void *stream);
+
 /* ---- Launch accounting and per-kernel timing (a library facility; the pages
  * describe no implementation, so these have no counterpart there).
  * adj_launch_count: kernels launched by this library since it was loaded.
