@@ -127,7 +127,7 @@ __device__ __forceinline__ C warp_lookback(const unsigned *flags, int64_t p0, in
 struct float2x4 {
     float4 x, y;
 };
-template <int L>
+template <int L, int LB>
 __global__ void __launch_bounds__(256, 3) k_fwd_scan(const float *__restrict__ a, const float *__restrict__ u,
                                                   float *__restrict__ h, int64_t T, int N, int nslices,
                                                   int64_t nseq, int64_t nchunks, ScanWs d, unsigned *status) {
@@ -143,21 +143,21 @@ __global__ void __launch_bounds__(256, 3) k_fwd_scan(const float *__restrict__ a
     const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
     const int64_t base = b * T * N + ch;
 
-    // pass 1: only the composite of this thread's L tokens is kept; the rows stay in L2
-    // and are read again in pass 2, so few registers are live across the look-back and
-    // three CTAs fit per SM.
+    // pass 1: only the composite of this thread's L tokens is kept (folded LB rows at a
+    // time); the rows stay in L2 and are read again in pass 2, so few registers are
+    // live across the look-back and three CTAs fit per SM.
     float4 A = f4(1.f), H = f4(0.f);
-    {
-        float4 av[L], uv[L];
+    for (int k0 = 0; k0 < L; k0 += LB) {
+        float4 av[LB], uv[LB];
 #pragma unroll
-        for (int k = 0; k < L; ++k) {
-            const int64_t t = t0 + k;
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
             const bool ok = act && t < T;
             av[k] = ok ? ld_l2keep4(a + base + t * N) : f4(1.f);
             uv[k] = ok ? ld_l2keep4(u + base + t * N) : f4(0.f);
         }
 #pragma unroll
-        for (int k = 0; k < L; ++k) {
+        for (int k = 0; k < LB; ++k) {
             H = fma4(av[k], H, uv[k]);
             A = A * av[k];
         }
@@ -195,19 +195,21 @@ __global__ void __launch_bounds__(256, 3) k_fwd_scan(const float *__restrict__ a
 
     float4 hc = sC[lane];
     for (int j = 0; j < w; ++j) hc = fma4(sA[j][lane], hc, sH[j][lane]);
-    float4 av[L], uv[L];
+    for (int k0 = 0; k0 < L; k0 += LB) {
+        float4 av[LB], uv[LB];
 #pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        const bool ok = act && t < T;
-        av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
-        uv[k] = ok ? ld_stream4(u + base + t * N) : f4(0.f);
-    }
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
+            const bool ok = act && t < T;
+            av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
+            uv[k] = ok ? ld_stream4(u + base + t * N) : f4(0.f);
+        }
 #pragma unroll
-    for (int k = 0; k < L; ++k) {
-        hc = fma4(av[k], hc, uv[k]);
-        const int64_t t = t0 + k;
-        if (act && t < T) st_stream4(h + base + t * N, hc);
+        for (int k = 0; k < LB; ++k) {
+            hc = fma4(av[k], hc, uv[k]);
+            const int64_t t = t0 + k0 + k;
+            if (act && t < T) st_stream4(h + base + t * N, hc);
+        }
     }
 }
 
@@ -225,7 +227,7 @@ __device__ __forceinline__ FwdSeg fseg_then(const FwdSeg &X, const FwdSeg &Y) {
     return FwdSeg{X.P * Y.P, fma4(X.P, Y.S, X.S), X.cl};
 }
 
-template <int L>
+template <int L, int LB>
 __global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g, const float *__restrict__ c,
                                                   const float *__restrict__ a, float *__restrict__ R, int64_t T,
                                                   int N, int nslices, int64_t nseq, int64_t nchunks, int64_t W,
@@ -244,18 +246,18 @@ __global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g
     const int64_t base = b * T * N + ch;
 
     FwdSeg G{f4(1.f), f4(0.f), false};
-    {
-        float4 av[L], ev[L];
+    for (int k0 = 0; k0 < L; k0 += LB) {
+        float4 av[LB], ev[LB];
 #pragma unroll
-        for (int k = 0; k < L; ++k) {
-            const int64_t t = t0 + k;
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
             const bool ok = act && t < T;
             av[k] = ok ? ld_l2keep4(a + base + t * N) : f4(1.f);
             ev[k] = ok ? ld_l2keep4(g + base + t * N) * ld_l2keep4(c + base + t * N) : f4(0.f);
         }
 #pragma unroll
-        for (int k = 0; k < L; ++k) {
-            const int64_t t = t0 + k;
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
             if (t >= T) break;
             if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
             else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
@@ -297,21 +299,23 @@ __global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g
 
     G = FwdSeg{sCP[lane], sCS[lane], true};
     for (int j = 0; j < w; ++j) G = fseg_then(G, FwdSeg{sP[j][lane], sS[j][lane], sCl[j]});
-    float4 av[L], ev[L];
+    for (int k0 = 0; k0 < L; k0 += LB) {
+        float4 av[LB], ev[LB];
 #pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        const bool ok = act && t < T;
-        av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
-        ev[k] = ok ? ld_stream4(g + base + t * N) * ld_stream4(c + base + t * N) : f4(0.f);
-    }
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
+            const bool ok = act && t < T;
+            av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
+            ev[k] = ok ? ld_stream4(g + base + t * N) * ld_stream4(c + base + t * N) : f4(0.f);
+        }
 #pragma unroll
-    for (int k = 0; k < L; ++k) {
-        const int64_t t = t0 + k;
-        if (t >= T) break;
-        if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
-        else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
-        if (act) st_stream4(R + base + t * N, G.S);
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
+            if (t >= T) break;
+            if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
+            else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
+            if (act) st_stream4(R + base + t * N, G.S);
+        }
     }
 }
 
@@ -329,7 +333,7 @@ __device__ __forceinline__ RevSeg rseg_then(const RevSeg &X, const RevSeg &Y) {
     return RevSeg{X.Q * Y.Q, fma4(X.Q, Y.S, X.S), Y.cl};
 }
 
-template <int L, bool TRUNC, typename TD>
+template <int L, int LB, bool TRUNC, typename TD>
 __global__ void __launch_bounds__(256, 3) k_bwd_scan(const float *__restrict__ g, const float *__restrict__ c,
                                                   const float *__restrict__ a, const float *__restrict__ h,
                                                   const float *__restrict__ R, TD *__restrict__ Da,
@@ -352,18 +356,18 @@ __global__ void __launch_bounds__(256, 3) k_bwd_scan(const float *__restrict__ g
     // pass 1: composite of this thread's tokens from e_i = g_i c_i and b_i = a_{i+1}
     // (0 past the last token); the rows stay in L2 for pass 2.
     RevSeg G{f4(1.f), f4(0.f), false};
-    {
-        float4 ev[L], bv[L];
+    for (int k0 = L - LB; k0 >= 0; k0 -= LB) {
+        float4 ev[LB], bv[LB];
 #pragma unroll
-        for (int k = 0; k < L; ++k) {
-            const int64_t t = t0 + k;
+        for (int k = 0; k < LB; ++k) {
+            const int64_t t = t0 + k0 + k;
             const bool ok = act && t < T;
             ev[k] = ok ? ld_l2keep4(g + base + t * N) * ld_l2keep4(c + base + t * N) : f4(0.f);
             bv[k] = (act && t + 1 < T) ? ld_l2keep4(a + base + (t + 1) * N) : f4(0.f);
         }
 #pragma unroll
-        for (int k = L - 1; k >= 0; --k) {
-            const int64_t t = t0 + k;
+        for (int k = LB - 1; k >= 0; --k) {
+            const int64_t t = t0 + k0 + k;
             if (t >= T) continue;
             const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
             if (end) G = RevSeg{bv[k], ev[k], true};
@@ -441,32 +445,32 @@ __global__ void __launch_bounds__(256, 3) k_bwd_scan(const float *__restrict__ g
 // ============================================================================ launchers
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
                             void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 8;
+    constexpr int L = 16, LB = 8;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
     cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
     if (e != cudaSuccess) return e;
-    k_fwd_scan<L><<<unsigned(nseq * nchunks), 256, 0, st>>>(a, u, h, T, N, nslices, nseq, nchunks, d, status);
+    k_fwd_scan<L, LB><<<unsigned(nseq * nchunks), 256, 0, st>>>(a, u, h, T, N, nslices, nseq, nchunks, d, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t W, void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 4;
+    constexpr int L = 16, LB = 4;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
     cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
     if (e != cudaSuccess) return e;
-    k_win_scan<L><<<unsigned(nseq * nchunks), 256, 0, st>>>(g, c, a, R, T, N, nslices, nseq, nchunks, W, d, status);
+    k_win_scan<L, LB><<<unsigned(nseq * nchunks), 256, 0, st>>>(g, c, a, R, T, N, nslices, nseq, nchunks, W, d, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, const float *h, const float *R,
                             void *D_a, void *D_u, void *D_c, void *E, bool d_bf16, int64_t B, int64_t T, int N,
                             int64_t W, void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 4;
+    constexpr int L = 16, LB = 4;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
@@ -475,7 +479,7 @@ cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, cons
     const bool trunc = W > 0 && W < T;
     const unsigned grid = unsigned(nseq * nchunks);
 #define ADJ_BWD(TR, TD)                                                                                      \
-    k_bwd_scan<L, TR, TD><<<grid, 256, 0, st>>>(g, c, a, h, R, static_cast<TD *>(D_a), static_cast<TD *>(D_u), \
+    k_bwd_scan<L, LB, TR, TD><<<grid, 256, 0, st>>>(g, c, a, h, R, static_cast<TD *>(D_a), static_cast<TD *>(D_u), \
                                                 static_cast<TD *>(D_c), static_cast<TD *>(E), T, N, nslices,   \
                                                 nseq, nchunks, trunc ? W : T, d, status)
     if (d_bf16) {
