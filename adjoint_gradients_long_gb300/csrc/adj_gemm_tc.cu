@@ -18,6 +18,11 @@
 // Tile: BM = 128 rows (TMEM lanes), BN <= 256 columns (TMEM columns), BK = 64
 // (one 128-byte swizzle row of bf16).  Shared-memory element (r, k) of a tile lives
 // at byte r*128 + ((k/8) ^ (r%8))*16 + (k%8)*2 (8-row atoms of 1024 bytes).
+#include <string.h>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "adj_internal.cuh"
 #include "adj_epilogue.cuh"
 #include "adj_ptx.cuh"
@@ -40,9 +45,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= uint64_t(2) << 61;                          // swizzle: 128 bytes
     return d;
 }
-// Instruction descriptor: kind::f16, bf16 x bf16 -> fp32, both operands K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(TC_BM >> 4) << 24);
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle.  The tile is stored as
+// blocks of 64 M (or N) elements x 64 k rows (8 KB, one TMA box each): 128-byte rows of
+// 64 elements, 8-row groups 1024 B apart (stride byte offset), 64-element blocks 8 KB
+// apart (leading byte offset).  One MMA k-step of 16 rows advances the start by 2 KB.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);
+    d |= uint64_t(8192 >> 4) << 16;
+    d |= uint64_t(1024 >> 4) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
+    return d;
+}
+// Instruction descriptor: kind::f16, bf16 x bf16 -> fp32; a_mn / b_mn select MN-major operands.
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+           (uint32_t(n >> 3) << 17) | (uint32_t(TC_BM >> 4) << 24);
 }
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -152,6 +171,9 @@ template <bool BF, bool SPLIT, bool IS_A>
 __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, int64_t rows, int R, int64_t k0,
                                            int64_t kend, uint8_t *hi, uint8_t *lo, int tid) {
     constexpr int BATCH = 2;
+    // vector loads need every row (k-contiguous source) or every k row (row-contiguous
+    // source) to start on a 16-byte boundary; other strides take the element-wise path
+    const bool kvec = O.s_row % (BF ? 8 : 4) == 0;
     if (O.s_k == 1) {
         const int items = R * 8;
         for (int base_it = tid; base_it < items; base_it += TC_PROD * BATCH) {
@@ -164,7 +186,7 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
                 if (it < items && row < rows && k < kend) {
                     int64_t i;
                     const void *p = op_at<IS_A>(O, row, k, i);
-                    if (k + 8 <= kend) {
+                    if (k + 8 <= kend && kvec) {
                         ld8_contig<BF>(p, i, v[b]);
                         if (IS_A && O.mul) {
                             float m[8];
@@ -200,7 +222,7 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
         const int r0 = g * RB;
         const int64_t row = row0 + r0, k = k0 + kc * 8;
         float v[RB][8];   // v[row][k]
-        const bool full = row + RB <= rows && k + 8 <= kend;
+        const bool full = row + RB <= rows && k + 8 <= kend && O.s_k % RB == 0;
         if (full) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -249,32 +271,124 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
 //               shared memory, 16-byte coalesced stores
 //   warps 8-15  producers: stage A (and B) k-blocks into a ring of S stages
 //   warp 16     TMEM owner; lane 0 issues tcgen05.mma into one of two accumulators
+//   warp 17     lane 0 issues the TMA tile loads, running ahead of the producers by up to
+//               S stages (bf16 tiles land in the MMA layout; fp32 tiles land raw and the
+//               producers convert them in place)
 // Barriers: full[s]/empty[s] hand stages producer -> MMA -> producer; accf[b]/acce[b]
 // hand accumulator b MMA -> epilogue -> MMA; bres marks the resident B tile ready.
-constexpr int TC_EPI_WARPS = 8, TC_THREADS_P = (TC_EPI_WARPS + TC_PROD_WARPS + 1) * 32;
-constexpr int TC_MMA_WARP = TC_EPI_WARPS + TC_PROD_WARPS;
+constexpr int TC_EPI_WARPS = 8, TC_THREADS_P = (TC_EPI_WARPS + TC_PROD_WARPS + 2) * 32;
+constexpr int TC_MMA_WARP = TC_EPI_WARPS + TC_PROD_WARPS, TC_TMA_WARP = TC_MMA_WARP + 1;
 constexpr uint32_t TC_EPI_SMEM = TC_EPI_WARPS * 32 * 32 * 4;
 
+// Operand load mode: register staging, or TMA tiles of a bf16 array (K-major: one box of
+// 64 k x R rows; MN-major: R/64 boxes of 64 rows x 64 k).
+enum { LD_REG = 0, LD_TMA_K = 1, LD_TMA_MN = 2, LD_RAW_K = 3, LD_RAW_MN = 4 };
+__host__ __device__ inline bool ld_raw(int m) { return m >= LD_RAW_K; }
+__host__ __device__ inline bool ld_tma(int m) { return m != LD_REG; }
+
 struct TcArgs {
+    CUtensorMap tmA[3], tmB[3];   // one map per array of a blocked operand
     int64_t M, Nc, K, kper;
     int BN, stages, n_tiles, m_tiles, splits;
+    int a_ld, b_ld;
     bool b_res;
     GemmOperand A, Bm;
     GemmEpilogue ep;
     unsigned *status;
 };
 
+// Issue the TMA loads of rows [row0, row0+R) x k [k0, k0+64) of an operand into dst.
+template <bool IS_A>
+__device__ __forceinline__ void tma_tile(const CUtensorMap *maps, const GemmOperand &O, int mode, int64_t row0, int R,
+                                         int64_t k0, uint8_t *dst, uint32_t bar) {
+    int blk = 0;
+    int64_t rr = row0, kk = k0;
+    if (O.blk < (int64_t(1) << 30)) {
+        if (IS_A) {
+            blk = int(k0 / O.blk);
+            kk = k0 - int64_t(blk) * O.blk;
+        } else {
+            blk = int(row0 / O.blk);
+            rr = row0 - int64_t(blk) * O.blk;
+        }
+    }
+    const void *m = &maps[blk];
+    if (mode == LD_TMA_K || mode == LD_RAW_K) {
+        tma_load_2d(smem_u32(dst), m, int(kk), int(rr), bar);
+    } else {
+        const int box = mode == LD_RAW_MN ? 16384 : 8192;   // 64 x 64 fp32 or bf16
+        for (int j = 0; j < R / 64; ++j) tma_load_2d(smem_u32(dst + j * box), m, int(rr) + 64 * j, int(kk), bar);
+    }
+}
+
+// Convert a raw fp32 tile (R = 128 rows x 64 k, as TMA wrote it) in place into the bf16
+// hi (and lo) tiles of the swizzled K-major layout.  Raw layouts: k-contiguous source:
+// row r at r*256 B; row-contiguous source: boxes of 64 rows, box j at j*16 KB holding
+// [k][row] with 256-byte k rows.  Every producer thread reads all its values first, the
+// producers meet at a named barrier, then write (hi at region, lo at region + 16 KB).
+template <bool SPLIT, bool MN>
+__device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
+    constexpr int R = TC_BM;
+    const float *raw = reinterpret_cast<const float *>(region);
+    if (!MN) {
+        constexpr int PER = R * 8 / TC_PROD;     // items (8 values) per thread
+        float v[PER][8];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int it = ptid + i * TC_PROD, r = it >> 3, kc = it & 7;
+            const float4 x = *reinterpret_cast<const float4 *>(raw + r * 64 + kc * 8);
+            const float4 y = *reinterpret_cast<const float4 *>(raw + r * 64 + kc * 8 + 4);
+            v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
+            v[i][4] = y.x; v[i][5] = y.y; v[i][6] = y.z; v[i][7] = y.w;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int it = ptid + i * TC_PROD;
+            put8<SPLIT>(region, region + R * 128, it >> 3, it & 7, v[i]);
+        }
+    } else {
+        constexpr int PER = (R / 4) * 8 / TC_PROD;   // items (4 rows x 8 k) per thread
+        float v[PER][4][8];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int it = ptid + i * TC_PROD, g = it % (R / 4), kc = it / (R / 4);
+            const int r0 = g * 4, box = r0 >> 6, rin = r0 & 63;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 x = *reinterpret_cast<const float4 *>(raw + box * 4096 + (kc * 8 + j) * 64 + rin);
+                v[i][0][j] = x.x; v[i][1][j] = x.y; v[i][2][j] = x.z; v[i][3][j] = x.w;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int it = ptid + i * TC_PROD, g = it % (R / 4), kc = it / (R / 4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) put8<SPLIT>(region, region + R * 128, g * 4 + q, kc, v[i][q]);
+        }
+    }
+}
+
+// Shared-memory layout.  A stage holds the A region then (unless B is resident) the B
+// region.  A region: bf16 hi tile, then the lo tile (split mode); an operand loaded raw
+// (fp32 by TMA, converted in place) needs twice the bf16 tile, which the split mode's
+// hi + lo already provides.  Resident B: per k-block a hi tile then a lo tile.
 struct TcLayout {
-    uint32_t a_bytes, b_bytes, stage_bytes, bres_bytes;
+    uint32_t a_bytes, b_bytes, a_reg, b_reg, stage_bytes, bres_kb, bres_bytes;
 };
-__host__ __device__ inline TcLayout tc_layout(int BN, int64_t K, bool b_res, bool split) {
+__host__ __device__ inline TcLayout tc_layout(int BN, int64_t K, bool b_res, bool split, bool a_raw = false,
+                                              bool b_raw = false) {
     TcLayout L;
     const uint32_t f = split ? 2u : 1u;
     L.a_bytes = TC_BM * 128u;
     L.b_bytes = uint32_t(BN) * 128u;
-    L.stage_bytes = (L.a_bytes + (b_res ? 0u : L.b_bytes)) * f;
+    L.a_reg = L.a_bytes * ((split || a_raw) ? 2u : 1u);
+    L.b_reg = b_res ? 0u : L.b_bytes * ((split || b_raw) ? 2u : 1u);
+    L.stage_bytes = L.a_reg + L.b_reg;
     const uint32_t kb = uint32_t((K + TC_BK - 1) / TC_BK);
-    L.bres_bytes = b_res ? L.b_bytes * kb * f : 0u;
+    L.bres_kb = L.b_bytes * f;
+    L.bres_bytes = b_res ? L.bres_kb * kb : 0u;
     return L;
 }
 
@@ -341,35 +455,44 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
 }
 
 template <bool ABF, bool BBF, bool SPLIT>
-__global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const TcArgs args) {
+__global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_constant__ TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int BN = args.BN, S = args.stages;
-    const TcLayout Lo = tc_layout(BN, args.kper, args.b_res, SPLIT);
+    const TcLayout Lo = tc_layout(BN, args.kper, args.b_res, SPLIT, ld_raw(args.a_ld), ld_raw(args.b_ld));
     uint8_t *bres = base;                                         // resident B (hi k-blocks, then lo)
     uint8_t *stages = base + Lo.bres_bytes;                       // ring of A (+B) stages
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + TC_EPI_SMEM);
     uint64_t *full = bars, *empty = bars + S, *accf = bars + 2 * S, *acce = bars + 2 * S + 2, *bready = bars + 2 * S + 4;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 2 * S + 5);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 2 * S + 5) + 1;
+    uint64_t *rawfull = bars + 2 * S + 5;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3 * S + 5) + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t ntiles = int64_t(args.n_tiles) * args.m_tiles * args.splits;
     const int64_t nkb_full = (args.kper + TC_BK - 1) / TC_BK;
     uint32_t ncols = 32;
     while (ncols < uint32_t(2 * BN)) ncols <<= 1;
+    // who fills a stage: the producers (register staging or in-place conversion of raw
+    // tiles) and/or the TMA warp (bf16 tiles straight into the MMA layout)
+    const bool b_here = !args.b_res;
+    const bool a_raw = ld_raw(args.a_ld), b_raw = b_here && ld_raw(args.b_ld);
+    const bool a_dir = ld_tma(args.a_ld) && !a_raw, b_dir = b_here && ld_tma(args.b_ld) && !b_raw;
+    const bool a_reg = args.a_ld == LD_REG, b_reg = b_here && args.b_ld == LD_REG;
+    const bool prod_full = a_reg || b_reg || a_raw || b_raw, tma_full = a_dir || b_dir;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&full[s]), TC_PROD);
+            mbar_init(smem_u32(&full[s]), (prod_full ? TC_PROD : 0) + (tma_full ? 1 : 0));
             mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&rawfull[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
             mbar_init(smem_u32(&acce[b]), TC_EPI_WARPS * 32);
         }
-        mbar_init(smem_u32(bready), TC_PROD);
+        mbar_init(smem_u32(bready), ld_tma(args.b_ld) ? 1 : TC_PROD);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -400,21 +523,22 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const TcArgs args) 
         // ---------------- producers
         const int ptid = tid - TC_EPI_WARPS * 32;
         bool ok = true;
-        if (args.b_res) {
+        if (args.b_res && !ld_tma(args.b_ld)) {
             // the n tile is the same for every tile of this CTA
             int64_t m0, n0, kb0, ke;
             int z;
             tile_of(blockIdx.x, m0, n0, z, kb0, ke);
             for (int64_t kb = 0; kb < nkb_full; ++kb) {
-                uint8_t *hi = bres + size_t(kb) * Lo.b_bytes;
-                uint8_t *lo = SPLIT ? bres + size_t(nkb_full + kb) * Lo.b_bytes : nullptr;
+                uint8_t *hi = bres + size_t(kb) * Lo.bres_kb;
+                uint8_t *lo = SPLIT ? hi + Lo.b_bytes : nullptr;
                 stage_tile<BBF, SPLIT, false>(args.Bm, n0, args.Nc, BN, kb0 + kb * TC_BK, ke, hi, lo, ptid);
             }
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(bready));
         }
+        const bool any_raw = a_raw || b_raw;
         int64_t kbg = 0;   // k-blocks staged so far (ring position)
-        for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        for (int64_t t = blockIdx.x; t < ntiles && ok && prod_full; t += gridDim.x) {
             int64_t m0, n0, kb0, ke;
             int z;
             tile_of(t, m0, n0, z, kb0, ke);
@@ -422,25 +546,96 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const TcArgs args) 
             for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
                 const int s = int(kbg % S);
                 const int64_t r = kbg / S;
-                if (r > 0 && !mbar_wait(smem_u32(&empty[s]), uint32_t((r - 1) & 1), abort, args.status)) {
-                    ok = false;
-                    break;
-                }
                 uint8_t *st = stages + size_t(s) * Lo.stage_bytes;
-                const uint32_t half = Lo.stage_bytes / (SPLIT ? 2 : 1);
+                uint8_t *sa = st, *sbb = st + Lo.a_reg;
                 const int64_t k0 = kb0 + kb * TC_BK;
-                stage_tile<ABF, SPLIT, true>(args.A, m0, args.M, TC_BM, k0, ke, st, SPLIT ? st + half : nullptr, ptid);
-                if (!args.b_res)
-                    stage_tile<BBF, SPLIT, false>(args.Bm, n0, args.Nc, BN, k0, ke, st + Lo.a_bytes,
-                                                  SPLIT ? st + half + Lo.a_bytes : nullptr, ptid);
+                if (a_reg || b_reg) {
+                    // register-staged tiles overwrite the stage: wait until the MMAs released it
+                    bool got = r == 0 || mbar_wait(smem_u32(&empty[s]), uint32_t((r - 1) & 1), abort, args.status);
+                    // with raw tiles the producers meet at named barriers, so they decide together
+                    if (any_raw) got = bar_red_and(1, TC_PROD, got);
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    if (a_reg)
+                        stage_tile<ABF, SPLIT, true>(args.A, m0, args.M, TC_BM, k0, ke, sa,
+                                                     SPLIT ? sa + Lo.a_bytes : nullptr, ptid);
+                    if (b_reg)
+                        stage_tile<BBF, SPLIT, false>(args.Bm, n0, args.Nc, BN, k0, ke, sbb,
+                                                      SPLIT ? sbb + Lo.b_bytes : nullptr, ptid);
+                }
+                if (any_raw) {
+                    // the raw tile of round r lands only after the MMAs released round r-1
+                    if (!bar_red_and(1, TC_PROD, mbar_wait(smem_u32(&rawfull[s]), uint32_t(r & 1), abort, args.status))) {
+                        ok = false;
+                        break;
+                    }
+                    if (a_raw) {
+                        if (args.a_ld == LD_RAW_MN) convert_raw128<SPLIT, true>(sa, ptid);
+                        else convert_raw128<SPLIT, false>(sa, ptid);
+                    }
+                    if (b_raw) {
+                        if (args.b_ld == LD_RAW_MN) convert_raw128<SPLIT, true>(sbb, ptid);
+                        else convert_raw128<SPLIT, false>(sbb, ptid);
+                    }
+                }
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full[s]));
             }
         }
+    } else if (warp == TC_TMA_WARP) {
+        // ---------------- TMA issuer
+        if (lane == 0) {
+            if (args.b_res && ld_tma(args.b_ld)) {
+                int64_t m0, n0, kb0, ke;
+                int z;
+                tile_of(blockIdx.x, m0, n0, z, kb0, ke);
+                mbar_arrive_expect_tx(smem_u32(bready), uint32_t(nkb_full) * Lo.b_bytes);
+                for (int64_t kb = 0; kb < nkb_full; ++kb)
+                    tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
+                                    bres + size_t(kb) * Lo.bres_kb, smem_u32(bready));
+            }
+            bool ok = a_dir || b_dir || a_raw || b_raw;
+            int64_t kbg = 0;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                int64_t m0, n0, kb0, ke;
+                int z;
+                tile_of(t, m0, n0, z, kb0, ke);
+                const int64_t nkb = ke > kb0 ? (ke - kb0 + TC_BK - 1) / TC_BK : 0;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
+                    const int s = int(kbg % S);
+                    const int64_t r = kbg / S;
+                    if (r > 0 && !mbar_wait(smem_u32(&empty[s]), uint32_t((r - 1) & 1), abort, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = stages + size_t(s) * Lo.stage_bytes;
+                    uint8_t *sa = st, *sbb = st + Lo.a_reg;
+                    const int64_t k0 = kb0 + kb * TC_BK;
+                    const uint32_t txd = (a_dir ? Lo.a_bytes : 0u) + (b_dir ? Lo.b_bytes : 0u);
+                    const uint32_t txr = (a_raw ? 2u * Lo.a_bytes : 0u) + (b_raw ? 2u * Lo.b_bytes : 0u);
+                    if (txd) {
+                        const uint32_t fb = smem_u32(&full[s]);
+                        mbar_arrive_expect_tx(fb, txd);
+                        if (a_dir) tma_tile<true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, fb);
+                        if (b_dir) tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, k0, sbb, fb);
+                    }
+                    if (txr) {
+                        const uint32_t rb = smem_u32(&rawfull[s]);
+                        mbar_arrive_expect_tx(rb, txr);
+                        if (a_raw) tma_tile<true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, rb);
+                        if (b_raw) tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, k0, sbb, rb);
+                    }
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp == TC_MMA_WARP) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(BN);
+            const bool a_mn = args.a_ld == LD_TMA_MN, b_mn = args.b_ld == LD_TMA_MN;
+            const uint32_t idesc = idesc_bf16(BN, a_mn, b_mn);
             bool ok = !args.b_res || mbar_wait(smem_u32(bready), 0, abort, args.status);
             if (ok) tc_fence_after();
             int64_t kbg = 0, i = 0;
@@ -463,24 +658,29 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const TcArgs args) 
                     }
                     tc_fence_after();
                     const uint32_t st = smem_u32(stages + size_t(s) * Lo.stage_bytes);
-                    const uint32_t half = Lo.stage_bytes / (SPLIT ? 2 : 1);
-                    const uint32_t a_hi = st, a_lo = st + half;
+                    const uint32_t a_hi = st, a_lo = st + Lo.a_bytes;
                     uint32_t b_hi, b_lo;
                     if (args.b_res) {
-                        b_hi = smem_u32(bres + size_t(kb) * Lo.b_bytes);
-                        b_lo = smem_u32(bres + size_t(nkb_full + kb) * Lo.b_bytes);
+                        b_hi = smem_u32(bres + size_t(kb) * Lo.bres_kb);
+                        b_lo = b_hi + Lo.b_bytes;
                     } else {
-                        b_hi = st + Lo.a_bytes;
-                        b_lo = st + half + Lo.a_bytes;
+                        b_hi = st + Lo.a_reg;
+                        b_lo = b_hi + Lo.b_bytes;
                     }
 #pragma unroll
                     for (int ks = 0; ks < TC_BK / 16; ++ks) {
-                        const uint32_t koff = uint32_t(ks) * 32u;
                         const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-                        mma_bf16(dacc, sw128_desc(a_hi + koff), sw128_desc(b_hi + koff), idesc, acc);
                         if (SPLIT) {
+                            const uint32_t koff = uint32_t(ks) * 32u;
+                            mma_bf16(dacc, sw128_desc(a_hi + koff), sw128_desc(b_hi + koff), idesc, acc);
                             mma_bf16(dacc, sw128_desc(a_hi + koff), sw128_desc(b_lo + koff), idesc, 1u);
                             mma_bf16(dacc, sw128_desc(a_lo + koff), sw128_desc(b_hi + koff), idesc, 1u);
+                        } else {
+                            const uint64_t ad = a_mn ? sw128_desc_mn(a_hi + uint32_t(ks) * 2048u)
+                                                     : sw128_desc(a_hi + uint32_t(ks) * 32u);
+                            const uint64_t bd = b_mn ? sw128_desc_mn(b_hi + uint32_t(ks) * 2048u)
+                                                     : sw128_desc(b_hi + uint32_t(ks) * 32u);
+                            mma_bf16(dacc, ad, bd, idesc, acc);
                         }
                     }
                     mma_commit(smem_u32(&empty[s]));
@@ -533,6 +733,75 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const TcArgs args) 
 
 // ---------------------------------------------------------------- launcher
 static int g_num_sms = 0;
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static bool g_encode_tried = false;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return g_encode;
+}
+
+// 2-D tensor map: inner (contiguous) extent x outer extent, row pitch in bytes, box
+// box_in x box_out; bf16 maps use the 128-byte swizzle of the MMA layout, fp32 (raw) maps
+// none.  Out-of-range elements read as zero.
+static bool make_map(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint64_t outer,
+                     uint64_t pitch_bytes, uint32_t box_in, uint32_t box_out) {
+    auto enc = encode_fn();
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15u) || (pitch_bytes & 15u) || inner == 0 || outer == 0)
+        return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_in, box_out};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Load mode an operand can use (no maps built): bf16 without a prologue product -> TMA
+// straight into the MMA layout (not in split mode); fp32 without a product, 128-row tiles
+// -> TMA raw + in-place conversion; otherwise register staging.
+static int tma_mode(const GemmOperand &O, bool is_a, int64_t rows, int64_t K, int R, bool split3) {
+    if (O.mul) return LD_REG;
+    const bool blocked = O.blk < (int64_t(1) << 30);
+    if (blocked && (((is_a ? K : rows) + O.blk - 1) / O.blk > 3 || (is_a ? O.blk % TC_BK : O.blk % R))) return LD_REG;
+    const int vec = O.bf16 ? 8 : 4;   // elements per 16 bytes
+    int mode;
+    if (O.s_k == 1 && O.s_row % vec == 0) mode = LD_TMA_K;
+    else if (O.s_row == 1 && O.s_k % vec == 0 && R % 64 == 0) mode = LD_TMA_MN;
+    else return LD_REG;
+    if (O.bf16) return split3 ? LD_REG : mode;
+    return R == TC_BM ? (mode == LD_TMA_K ? LD_RAW_K : LD_RAW_MN) : LD_REG;
+}
+
+// Build the maps of an operand for the chosen mode; returns the mode, or LD_REG if a map
+// cannot be built.
+static int tma_build(CUtensorMap *maps, const GemmOperand &O, int mode, bool is_a, int64_t rows, int64_t K, int R) {
+    if (mode == LD_REG) return LD_REG;
+    const bool blocked = O.blk < (int64_t(1) << 30);
+    const int nmaps = blocked ? int(((is_a ? K : rows) + O.blk - 1) / O.blk) : 1;
+    const int64_t kext = (is_a && blocked) ? O.blk : K;
+    const int64_t rext = (!is_a && blocked) ? O.blk : rows;
+    const uint64_t es = O.bf16 ? 2 : 4;
+    const bool kmaj = mode == LD_TMA_K || mode == LD_RAW_K;
+    for (int i = 0; i < nmaps; ++i) {
+        const bool ok = kmaj ? make_map(&maps[i], O.p[i], O.bf16, uint64_t(kext), uint64_t(rext), uint64_t(O.s_row) * es,
+                                        64, uint32_t(R))
+                             : make_map(&maps[i], O.p[i], O.bf16, uint64_t(rext), uint64_t(kext), uint64_t(O.s_k) * es,
+                                        64, 64);
+        if (!ok) return LD_REG;
+    }
+    return mode;
+}
 
 template <bool ABF, bool BBF, bool SPLIT>
 static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st) {
@@ -554,19 +823,30 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
         if (g_num_sms <= 0) g_num_sms = 1;
     }
     TcArgs a;
+    memset(&a, 0, sizeof(a));
     a.M = M; a.Nc = Nc; a.K = K; a.splits = splits;
     int64_t kper = (K + splits - 1) / splits;
     a.kper = (kper + TC_BK - 1) / TC_BK * TC_BK;
     // Tile width: the widest (<= 256, a multiple of 32) whose stages fit; B resident when its
-    // whole k extent fits next to two A stages and the epilogue buffer.
-    const size_t budget = 227 * 1024 - 1024 - TC_EPI_SMEM - 256;
+    // whole k extent fits next to two A stages and the epilogue buffer.  A streamed fp32 B
+    // that TMA can load raw takes 128-column tiles (the in-place conversion works on 128 rows).
+    const size_t budget = 227 * 1024 - 1024 - TC_EPI_SMEM - 512;
+    const int a_mode = tma_mode(A, true, M, K, TC_BM, split3);
     int BN = int(Nc < 256 ? (Nc + 31) / 32 * 32 : 256);
-    int S = 0;
-    for (;; BN = BN > 32 ? (BN / 2 + 31) / 32 * 32 : 0) {
+    int S = 0, b_mode = LD_REG;
+    for (int next = BN;; BN = next) {
         if (BN == 0) return cudaErrorInvalidConfiguration;
-        const TcLayout res = tc_layout(BN, a.kper, true, split3);
+        next = BN > 32 ? (BN / 2 + 31) / 32 * 32 : 0;
+        const TcLayout res = tc_layout(BN, a.kper, true, split3, ld_raw(a_mode), false);
         a.b_res = splits == 1 && size_t(res.bres_bytes) + 2 * size_t(res.stage_bytes) <= budget;
-        const TcLayout Lt = tc_layout(BN, a.kper, a.b_res, split3);
+        b_mode = a.b_res ? (split3 ? LD_REG : tma_mode(Bm, false, Nc, K, BN, false))
+                         : tma_mode(Bm, false, Nc, K, BN, split3);
+        if (a.b_res && ld_raw(b_mode)) b_mode = LD_REG;          // a resident B is converted once, by registers
+        if (!a.b_res && !Bm.bf16 && !Bm.mul && BN > TC_BM && tma_mode(Bm, false, Nc, K, TC_BM, split3) != LD_REG) {
+            next = TC_BM;                                         // take 128-column tiles to load B raw
+            continue;
+        }
+        const TcLayout Lt = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode));
         S = int((budget - Lt.bres_bytes) / Lt.stage_bytes);
         if (S >= 2) break;
     }
@@ -576,8 +856,12 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.n_tiles = int((Nc + BN - 1) / BN);
     a.m_tiles = int((M + TC_BM - 1) / TC_BM);
     a.A = A; a.Bm = Bm; a.ep = ep; a.status = status;
-    const TcLayout L = tc_layout(BN, a.kper, a.b_res, split3);
-    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + TC_EPI_SMEM + (2 * S + 6) * 8;
+    a.a_ld = tma_build(a.tmA, A, a_mode, true, M, K, TC_BM);
+    a.b_ld = tma_build(a.tmB, Bm, b_mode, false, Nc, K, BN);
+    // the layout was sized for the modes asked for; a mode that fell back to registers
+    // uses only part of its region
+    const TcLayout L = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode));
+    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + TC_EPI_SMEM + (3 * S + 6) * 8;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
     int64_t grid = ntiles;
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;

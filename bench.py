@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the short runs of the bf16 workloads reported under 'workloads'")
     return ap.parse_args()
 
 
@@ -116,6 +118,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ multi-rank reduction (weak scaling)
+def max_over_ranks(v, world, device=None):
+    """Max of a per-rank timing over all ranks (any torch.distributed backend)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank, world, ms_per_step_max):
+    """Whole-job throughput: all ranks' tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step_max * 1e-3)
+
+
 # ------------------------------------------------------------------ per-kernel algorithmic work
 def kernel_table(P, N, xb, db, trunc):
     """Algorithmic bytes (and flops) per token of each kernel kind, as built."""
@@ -188,6 +207,63 @@ def run_reference(args, rank):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ the other workloads (context lines)
+OTHER = (("ssm8_p512", 4096), ("ssm1_1m", 4096), ("ssm1_1m", None), ("ssm4_p2048", 8192))
+
+
+def measure_workload(key, window, dev, peaks, steps=3, warmup=2):
+    """Short device-timed run of one of the bf16 workloads at full size (weak evidence:
+    few steps, L2 not flushed, inputs larger than L2).  Returns tokens/s per layer and
+    the per-kernel roofline entries."""
+    import torch
+    from adjoint_gradients_long_gb300 import lib, synth
+    from adjoint_gradients_long_gb300.stack import AdjStack
+    w = synth.workload(key)
+    inputs = synth.make_inputs(w)
+    st = AdjStack(w.B, w.T, w.P, w.N, w.K, x_bf16=True, d_bf16=True, Tbar=window, device=dev)
+    st.load(inputs)
+    del inputs
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        st.step(window)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        st.step(window)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    lib.profile_reset()
+    lib.profile_enable(True)
+    st.step(window)
+    torch.cuda.synchronize(dev)
+    lib.profile_enable(False)
+    prof = lib.profile_read()
+    lib.profile_reset()
+    status = st.status()
+    tab = kernel_table(w.P, w.N, 2, 2, window is not None and window < w.T)
+    tok = w.B * w.T
+    kern = {}
+    tot = sum(v[1] for v in prof.values())
+    for name, (n, t) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        per = t / n
+        ent = {"launches": n, "ms_per_launch": per, "share": t / tot}
+        if name in tab:
+            ent["achieved_gbs"] = tab[name]["bytes"] * tok / (per * 1e-3) / 1e9
+            if "flops" in tab[name]:
+                ent["achieved_tflops"] = tab[name]["flops"] * tok / (per * 1e-3) / 1e12
+            r = roofline_of(name, ent, peaks, split3=False)
+            ent["roofline_bound"], ent["roofline_frac"] = r["bound"], r["frac"]
+        kern[name] = ent
+    del st
+    torch.cuda.empty_cache()
+    return {"workload": key, "window": window if window is not None else "full", "B": w.B, "T": w.T, "P": w.P,
+            "N": w.N, "K": w.K, "dtype": "bf16 GEMM operands, fp32 scans",
+            "value": tok * w.K / (ms * 1e-3), "unit": "tokens/s per layer", "ms_per_step": ms, "steps": steps,
+            "device_status": lib.STATUS.get(status, status), "kernels": dict(list(kern.items())[:6])}
 
 
 # ------------------------------------------------------------------ our arm
@@ -288,16 +364,9 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # max over ranks
-    def allmax(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    mean_full = allmax(sum(ms_full) / len(ms_full))
-    mean_trunc = allmax(sum(ms_trunc) / len(ms_trunc))
-    e2e_ms = allmax(e2e_ms)
+    mean_full = max_over_ranks(sum(ms_full) / len(ms_full), world, dev)
+    mean_trunc = max_over_ranks(sum(ms_trunc) / len(ms_trunc), world, dev)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     tokens = B * T * K * world
 
     peaks, peak_src = load_peaks()
@@ -338,9 +407,17 @@ def run_ours(args, rank, world, local_rank):
                "sample": f"first {toks} tokens of one sequence of {WORKLOAD}, full window, aggregated-literal "
                          f"mode, single thread ({dt:.1f} s)"}
 
+    others = []
+    if rank == 0 and world == 1 and not args.no_other_workloads:
+        del st
+        torch.cuda.empty_cache()
+        for key, window in OTHER:
+            others.append(measure_workload(key, window, dev, peaks))
+
     if rank == 0:
         line = {
-            "metric": METRIC, "value": tokens / (mean_full * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "metric": METRIC, "value": weak_scaling_value(B * T * K, world, mean_full), "unit": "tokens/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_full, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "B": B, "T": T, "P": P, "N": N, "K": K, "window": "full",
@@ -357,6 +434,7 @@ def run_ours(args, rank, world, local_rank):
             "clocks": clk,
             "peaks": {"source": peak_src, **peaks},
             "device_status": lib.STATUS.get(status, status),
+            "workloads": others,
         }
         print(json.dumps(line), flush=True)
 
