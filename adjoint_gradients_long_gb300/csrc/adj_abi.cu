@@ -40,11 +40,12 @@ adj_status check_opt(std::initializer_list<const void *> ps) {
     return ADJ_OK;
 }
 
-// Split of the token reduction of a parameter-gradient GEMM: about one wave of CTAs
-// (one 128 x 256 output tile per CTA), at least 4 k-blocks of 64 tokens per split.
+// Largest split of the token reduction of a parameter-gradient GEMM: one wave of CTAs at
+// 128 x 256 output tiles, at least 4 k-blocks of 64 tokens per split.  The launch lowers it
+// when it takes narrower tiles, so that every CTA still owns one tile.
 int gemm_splits(int64_t M, int64_t Nc, int64_t K) {
     const int64_t tiles = cdiv(M, 128) * cdiv(Nc, 256);
-    int64_t s = cdiv(152, tiles);
+    int64_t s = 152 / tiles;
     if (s > K / 256) s = K / 256;
     if (s < 1) s = 1;
     if (s > 128) s = 128;
@@ -282,6 +283,7 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         return ADJ_OK;
     }
     const int s_in = splits_in(dims), s_o = splits_o(dims);
+    int su_in = s_in, su_o = s_o;   // split counts the launches took (at most the above)
     float *part_in = reinterpret_cast<float *>(at(ws, L.part0));
     float *part_o = reinterpret_cast<float *>(at(ws, L.part1));
     // dW_in = xhat^T [D_a | D_u | D_c]
@@ -290,22 +292,22 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
     {
         ProfScope ps(K_PARAM_DWIN, st);
         ADJ_CUDA(launch_gemm_tc(P, 3 * int64_t(N), BT, op1(xhat, 1, P, xbf), op3(D_a, D_u, D_c, N, 1, N, dbf), e, s_in,
-                                !xbf, status_word(ws), st));
+                                !xbf, status_word(ws), st, &su_in));
     }
     {
         ProfScope ps(K_SPLITK, st);
-        ADJ_CUDA(launch_splitk_reduce(part_in, s_in, int64_t(P) * 3 * N, dW_in, accumulate, st));
+        ADJ_CUDA(launch_splitk_reduce(part_in, su_in, int64_t(P) * 3 * N, dW_in, accumulate, st));
     }
     // dW_o = E^T gy
     GemmEpilogue e2 = epi(Epi::Partial);
     e2.out0 = part_o;
     {
         ProfScope ps(K_PARAM_DWO, st);
-        ADJ_CUDA(launch_gemm_tc(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s_o, !xbf, status_word(ws), st));
+        ADJ_CUDA(launch_gemm_tc(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s_o, !xbf, status_word(ws), st, &su_o));
     }
     {
         ProfScope ps(K_SPLITK, st);
-        ADJ_CUDA(launch_splitk_reduce(part_o, s_o, int64_t(N) * P, dW_o, accumulate, st));
+        ADJ_CUDA(launch_splitk_reduce(part_o, su_o, int64_t(N) * P, dW_o, accumulate, st));
     }
     // db_a = sum_t D_a
     {

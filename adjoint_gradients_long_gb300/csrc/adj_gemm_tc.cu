@@ -8,12 +8,9 @@
 //          lo = bf16(x - hi); the product uses hi*hi + hi*lo + lo*hi (the lo*lo
 //          term is below 2^-16 of the product), three MMAs into one accumulator.
 //
-// CTA: 9 warps.  Warps 0-7 stage operand tiles (any stride, fp32 or bf16, optional
-// elementwise product) into shared memory in the 128-byte-swizzled K-major layout,
-// then run the epilogue.  Warp 8 owns the tensor memory and one of its lanes issues
-// tcgen05.mma.  Stages are handed over with mbarriers: producers arrive on full[s];
-// tcgen05.commit arrives on empty[s] when the MMAs reading stage s are done, and on
-// `accum` after the last k-block.  Every wait is bounded by a wall-clock limit.
+// CTA: 18 warps in four roles (epilogue, producers, MMA issuer, TMA issuer; see the
+// kernel below).  Stages, accumulators and the resident B tile are handed over with
+// mbarriers, and every wait is bounded by a wall-clock limit.
 //
 // Tile: BM = 128 rows (TMEM lanes), BN <= 256 columns (TMEM columns), BK = 64
 // (one 128-byte swizzle row of bf16).  Shared-memory element (r, k) of a tile lives
@@ -326,46 +323,54 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *maps, const GemmOper
 // row r at r*256 B; row-contiguous source: boxes of 64 rows, box j at j*16 KB holding
 // [k][row] with 256-byte k rows.  Every producer thread reads all its values first, the
 // producers meet at a named barrier, then write (hi at region, lo at region + 16 KB).
+// Both mappings keep shared-memory reads and writes free of bank conflicts: k-contiguous
+// tiles are read as 16-byte vectors, 32 lanes covering two full rows, and written as
+// 8-byte halves of the swizzled 16-byte chunks; row-contiguous tiles are read one value
+// per lane (32 consecutive rows) and written as whole chunks of one row per lane.
+__device__ __forceinline__ void put4(uint8_t *hi, uint8_t *lo, int r, int k4, float4 v, bool split) {
+    const uint32_t off = uint32_t(r) * 128u + (uint32_t((k4 >> 1) ^ (r & 7)) << 4) + uint32_t(k4 & 1) * 8u;
+    uint2 h;
+    h.x = pack_bf16(v.x, v.y);
+    h.y = pack_bf16(v.z, v.w);
+    *reinterpret_cast<uint2 *>(hi + off) = h;
+    if (split) {
+        uint2 l;
+        l.x = pack_bf16(v.x - bf16_round(v.x), v.y - bf16_round(v.y));
+        l.y = pack_bf16(v.z - bf16_round(v.z), v.w - bf16_round(v.w));
+        *reinterpret_cast<uint2 *>(lo + off) = l;
+    }
+}
+
 template <bool SPLIT, bool MN>
 __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
     constexpr int R = TC_BM;
     const float *raw = reinterpret_cast<const float *>(region);
     if (!MN) {
-        constexpr int PER = R * 8 / TC_PROD;     // items (8 values) per thread
+        constexpr int PER = R * 16 / TC_PROD;    // float4 (4 k of one row) per thread
+        float4 v[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) v[i] = reinterpret_cast<const float4 *>(raw)[ptid + i * TC_PROD];
+        asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int q = ptid + i * TC_PROD;    // float4 index: row q/16, k4 q%16
+            put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
+        }
+    } else {
+        constexpr int PER = R * 8 / TC_PROD;     // items (one row, 8 k) per thread
         float v[PER][8];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int it = ptid + i * TC_PROD, r = it >> 3, kc = it & 7;
-            const float4 x = *reinterpret_cast<const float4 *>(raw + r * 64 + kc * 8);
-            const float4 y = *reinterpret_cast<const float4 *>(raw + r * 64 + kc * 8 + 4);
-            v[i][0] = x.x; v[i][1] = x.y; v[i][2] = x.z; v[i][3] = x.w;
-            v[i][4] = y.x; v[i][5] = y.y; v[i][6] = y.z; v[i][7] = y.w;
+            const int it = ptid + i * TC_PROD, r = it % R, kc = it / R;
+            const float *src = raw + (r >> 6) * 4096 + (r & 63);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
         }
         asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int it = ptid + i * TC_PROD;
-            put8<SPLIT>(region, region + R * 128, it >> 3, it & 7, v[i]);
-        }
-    } else {
-        constexpr int PER = (R / 4) * 8 / TC_PROD;   // items (4 rows x 8 k) per thread
-        float v[PER][4][8];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int it = ptid + i * TC_PROD, g = it % (R / 4), kc = it / (R / 4);
-            const int r0 = g * 4, box = r0 >> 6, rin = r0 & 63;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 x = *reinterpret_cast<const float4 *>(raw + box * 4096 + (kc * 8 + j) * 64 + rin);
-                v[i][0][j] = x.x; v[i][1][j] = x.y; v[i][2][j] = x.z; v[i][3][j] = x.w;
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int it = ptid + i * TC_PROD, g = it % (R / 4), kc = it / (R / 4);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) put8<SPLIT>(region, region + R * 128, g * 4 + q, kc, v[i][q]);
+            put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
         }
     }
 }
@@ -813,7 +818,8 @@ static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cuda
 }
 
 cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
-                           const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st) {
+                           const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
+                           int *splits_used) {
     if (M <= 0 || Nc <= 0) return cudaSuccess;
     if (splits < 1) splits = 1;
     if (g_num_sms == 0) {
@@ -851,6 +857,18 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
         if (S >= 2) break;
     }
     if (S > 6) S = 6;
+    // split K no further than one wave of CTAs: every CTA then owns exactly one tile
+    {
+        const int64_t per_split = ((Nc + BN - 1) / BN) * ((M + TC_BM - 1) / TC_BM);
+        const int64_t cap = (g_num_sms / ((Nc + BN - 1) / BN)) * ((Nc + BN - 1) / BN);
+        if (splits > 1 && int64_t(splits) * per_split > cap) {
+            splits = int(cap / per_split > 1 ? cap / per_split : 1);
+            a.splits = splits;
+            kper = (K + splits - 1) / splits;
+            a.kper = (kper + TC_BK - 1) / TC_BK * TC_BK;
+        }
+    }
+    if (splits_used) *splits_used = splits;
     a.BN = BN;
     a.stages = S;
     a.n_tiles = int((Nc + BN - 1) / BN);

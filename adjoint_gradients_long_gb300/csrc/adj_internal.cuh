@@ -122,7 +122,8 @@ struct GemmEpilogue {
 // tcgen05 GEMM C[M,Nc] = A[M,K] B[K,Nc] with the operand and epilogue contracts above;
 // split3: fp32-accurate hi/lo bf16 split, otherwise bf16 operands.
 cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
-                           const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st);
+                           const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
+                           int *splits_used = nullptr);
 
 cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out,
                                  int accumulate, cudaStream_t st);
