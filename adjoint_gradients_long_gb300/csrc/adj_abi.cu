@@ -66,28 +66,40 @@ int loss_blocks(int64_t count) {
 
 // Workspace layouts (offsets from ws; the first WS_HEADER bytes hold the status word).
 struct Layout {
-    size_t buf0 = 0, buf1 = 0, scan = 0, part0 = 0, part1 = 0, part2 = 0, total = 0;
+    size_t buf0 = 0, buf1 = 0, scan = 0, part0 = 0, part1 = 0, part2 = 0, wsplit = 0, total = 0;
 };
 
 Layout layout(const adj_dims *d, int op, int64_t Tbar) {
     Layout L;
     const size_t btn = al256(size_t(d->B * d->T) * d->N * 4);
+    // fp32 weights are split once per call into bf16 hi/lo copies (4 bytes per value):
+    // W_in and W_o for the forward, W_o for the backward, W_in for the input gradient
+    const bool wsplit = d->x_dtype == ADJ_F32;
+    const size_t win_s = wsplit ? al256(size_t(d->P) * 3 * d->N * 4) : 0;
+    const size_t wo_s = wsplit ? al256(size_t(d->N) * d->P * 4) : 0;
     size_t off = WS_HEADER;
     switch (op) {
     case ADJ_OP_FWD:            // u
+        L.buf0 = off; off += btn;
+        L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
+        L.wsplit = off; off += win_s + wo_s;
+        break;
     case ADJ_OP_BWD_FULL:       // g
         L.buf0 = off; off += btn;
         L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
+        L.wsplit = off; off += wo_s;
         break;
     case ADJ_OP_BWD_TRUNC:      // g, R
         L.buf0 = off; off += btn;
         L.buf1 = off; off += (Tbar < d->T ? btn : 0);
         L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
+        L.wsplit = off; off += wo_s;
         break;
     case ADJ_OP_PARAM: {
         L.part0 = off; off += al256(size_t(splits_in(d)) * d->P * 3 * d->N * 4);
         L.part1 = off; off += al256(size_t(splits_o(d)) * d->N * d->P * 4);
         L.part2 = off; off += al256(size_t(colsum_blocks(d)) * d->N * 4);
+        L.wsplit = off; off += win_s;
         break;
     }
     case ADJ_OP_LOSS:
@@ -124,6 +136,7 @@ inline unsigned *status_word(void *ws) { return static_cast<unsigned *>(ws); }
 GemmOperand op1(const void *p, int64_t s_row, int64_t s_k, bool bf16, const float *mul = nullptr) {
     GemmOperand o;
     o.p[0] = p; o.p[1] = p; o.p[2] = p;
+    o.lo[0] = o.lo[1] = o.lo[2] = nullptr;
     o.blk = int64_t(1) << 62;
     o.s_row = s_row; o.s_k = s_k; o.bf16 = bf16; o.mul = mul;
     return o;
@@ -131,7 +144,19 @@ GemmOperand op1(const void *p, int64_t s_row, int64_t s_k, bool bf16, const floa
 GemmOperand op3(const void *p0, const void *p1, const void *p2, int64_t blk, int64_t s_row, int64_t s_k, bool bf16) {
     GemmOperand o;
     o.p[0] = p0; o.p[1] = p1; o.p[2] = p2;
+    o.lo[0] = o.lo[1] = o.lo[2] = nullptr;
     o.blk = blk; o.s_row = s_row; o.s_k = s_k; o.bf16 = bf16; o.mul = nullptr;
+    return o;
+}
+// A weight operand: fp32 weights are split into bf16 hi/lo copies at `split` (n values
+// each) for the split-precision GEMM; bf16 weights are used as they are.
+GemmOperand opw(const void *w, int64_t n, bool xbf, void *split, int64_t s_row, int64_t s_k, cudaStream_t st,
+                cudaError_t *err) {
+    if (xbf) return op1(w, s_row, s_k, true);
+    __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(split), *lo = hi + n;
+    *err = launch_split_bf16(static_cast<const float *>(w), n, hi, lo, st);
+    GemmOperand o = op1(hi, s_row, s_k, true);
+    o.lo[0] = o.lo[1] = o.lo[2] = lo;
     return o;
 }
 GemmEpilogue epi(Epi k) {
@@ -161,8 +186,10 @@ adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a
     e.ld = N;
     {
         ProfScope ps(K_COT_PROJ, st);
-        ADJ_CUDA(launch_gemm_tc(BT, N, P, op1(gy, P, 1, false), op1(w->W_o, P, 1, dims->x_dtype == ADJ_BF16), e, 1,
-                                dims->x_dtype == ADJ_F32, status_word(ws), st));
+        cudaError_t err = cudaSuccess;
+        const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, dims->x_dtype == ADJ_BF16, at(ws, L.wsplit), P, 1, st, &err);
+        ADJ_CUDA(err);
+        ADJ_CUDA(launch_gemm_tc(BT, N, P, op1(gy, P, 1, false), Wo, e, 1, dims->x_dtype == ADJ_F32, status_word(ws), st));
     }
     const bool trunc = op == ADJ_OP_BWD_TRUNC && Tbar < T;
     float *R = nullptr;
@@ -205,10 +232,12 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
     // [z_a | u | c] = xhat W_in;  a = sigmoid(z_a + b_a)
     GemmEpilogue e = epi(Epi::ProjIn);
     e.out0 = a; e.out1 = u; e.out2 = c; e.bias = w->b_a; e.N = N;
+    cudaError_t err = cudaSuccess;
+    const GemmOperand Win = opw(w->W_in, int64_t(P) * 3 * N, xbf, at(ws, L.wsplit), 1, 3 * int64_t(N), st, &err);
+    ADJ_CUDA(err);
     {
         ProfScope ps(K_PROJ_IN, st);
-        ADJ_CUDA(launch_gemm_tc(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), op1(w->W_in, 1, 3 * int64_t(N), xbf), e, 1,
-                                !xbf, status_word(ws), st));
+        ADJ_CUDA(launch_gemm_tc(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), Win, e, 1, !xbf, status_word(ws), st));
     }
     // h_t = a_t h_{t-1} + u_t
     {
@@ -221,8 +250,11 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
         e2.out0 = y; e2.out_x = y_x; e2.ld = P;
         e2.add = xres ? static_cast<const void *>(xres) : xhat;
         e2.add_bf16 = !xres && xbf;
+        const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, xbf, at(ws, L.wsplit + al256(size_t(P) * 3 * N * 4)), 1, P, st,
+                                   &err);
+        ADJ_CUDA(err);
         ProfScope ps(K_PROJ_OUT, st);
-        ADJ_CUDA(launch_gemm_tc(BT, P, N, op1(c, N, 1, false, h), op1(w->W_o, 1, P, xbf), e2, 1, !xbf, status_word(ws), st));
+        ADJ_CUDA(launch_gemm_tc(BT, P, N, op1(c, N, 1, false, h), Wo, e2, 1, !xbf, status_word(ws), st));
     }
     return ADJ_OK;
 }
@@ -319,9 +351,12 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         // dxhat = [D_a | D_u | D_c] W_in^T, or gy_prev = gy + dxhat
         GemmEpilogue e3 = epi(gy_prev ? Epi::StoreAdd : Epi::Store);
         e3.out0 = gy_prev ? gy_prev : dxhat; e3.add = gy; e3.ld = P;
+        cudaError_t err = cudaSuccess;
+        const GemmOperand Win = opw(w->W_in, int64_t(P) * 3 * N, xbf, at(ws, L.wsplit), 3 * int64_t(N), 1, st, &err);
+        ADJ_CUDA(err);
         ProfScope ps(K_INPUT_GRAD, st);
-        ADJ_CUDA(launch_gemm_tc(BT, P, 3 * int64_t(N), op3(D_a, D_u, D_c, N, N, 1, dbf),
-                                op1(w->W_in, 3 * int64_t(N), 1, xbf), e3, 1, !xbf, status_word(ws), st));
+        ADJ_CUDA(launch_gemm_tc(BT, P, 3 * int64_t(N), op3(D_a, D_u, D_c, N, N, 1, dbf), Win, e3, 1, !xbf,
+                                status_word(ws), st));
     }
     return ADJ_OK;
 }

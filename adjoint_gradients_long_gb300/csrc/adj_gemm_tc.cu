@@ -8,7 +8,7 @@
 //          lo = bf16(x - hi); the product uses hi*hi + hi*lo + lo*hi (the lo*lo
 //          term is below 2^-16 of the product), three MMAs into one accumulator.
 //
-// CTA: 18 warps in four roles (epilogue, producers, MMA issuer, TMA issuer; see the
+// CTA: 16 warps (4 per SM sub-partition, so 128 registers a thread) in four roles (epilogue, producers, MMA issuer, TMA issuer; see the
 // kernel below).  Stages, accumulators and the resident B tile are handed over with
 // mbarriers, and every wait is bounded by a wall-clock limit.
 //
@@ -27,7 +27,7 @@
 namespace adj {
 
 #ifndef ADJ_TC_PROD_WARPS
-#define ADJ_TC_PROD_WARPS 8
+#define ADJ_TC_PROD_WARPS 6
 #endif
 constexpr int TC_BM = 128, TC_BK = 64;
 constexpr int TC_PROD_WARPS = ADJ_TC_PROD_WARPS, TC_PROD = TC_PROD_WARPS * 32;
@@ -158,7 +158,13 @@ __device__ __forceinline__ const void *op_at(const GemmOperand &O, int64_t row, 
     return O.p[blk];
 }
 
-// Stage rows [row0, row0+R) x k [k0, k0+64) of an operand into a swizzled tile.
+// Low-part array of the array p of a pre-split operand.
+__device__ __forceinline__ const void *lo_of(const GemmOperand &O, const void *p) {
+    return p == O.p[0] ? O.lo[0] : p == O.p[1] ? O.lo[1] : O.lo[2];
+}
+
+// Stage rows [row0, row0+R) x k [k0, k0+64) of an operand into a swizzled tile.  A
+// pre-split operand is staged as hi + lo (and split again in split mode).
 // k-contiguous sources: a work item is 8 consecutive k of one row (two float4 or one
 // 16-byte bf16 vector).  Row-contiguous sources (the token-major operands of the
 // parameter reductions): a work item is a 4-row (fp32) or 8-row (bf16) by 8-k block,
@@ -185,6 +191,12 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
                     const void *p = op_at<IS_A>(O, row, k, i);
                     if (k + 8 <= kend && kvec) {
                         ld8_contig<BF>(p, i, v[b]);
+                        if (BF && O.lo[0]) {
+                            float l[8];
+                            ld8_contig<true>(lo_of(O, p), i, l);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) v[b][j] += l[j];
+                        }
                         if (IS_A && O.mul) {
                             float m[8];
                             ld8_contig<false>(O.mul, i, m);
@@ -195,6 +207,7 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             v[b][j] = (k + j < kend) ? ld1<BF>(p, i + j) : 0.f;
+                            if (BF && O.lo[0] && k + j < kend) v[b][j] += ld1<true>(lo_of(O, p), i + j);
                             if (IS_A && O.mul && k + j < kend) v[b][j] *= __ldg(O.mul + i + j);
                         }
                     }
@@ -218,26 +231,41 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
         const int g = it % groups, kc = it / groups;
         const int r0 = g * RB;
         const int64_t row = row0 + r0, k = k0 + kc * 8;
-        float v[RB][8];   // v[row][k]
         const bool full = row + RB <= rows && k + 8 <= kend && O.s_k % RB == 0;
-        if (full) {
+        if (BF && full) {
+            // 8 k rows of 8 bf16 each, kept packed (and the low parts of a pre-split
+            // operand), unpacked one output row at a time
+            uint4 u[8], ul[8];
+            const bool pre = O.lo[0] != nullptr;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 int64_t i;
                 const void *p = op_at<IS_A>(O, row, k + j, i);
-                if (BF) {
-                    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p) + i));
-                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+                u[j] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p) + i));
+                ul[j] = pre ? __ldg(reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(lo_of(O, p)) + i))
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-                    for (int q = 0; q < RB / 2; ++q) {
-                        const float2 f = __bfloat1622float2(b2[q]);
-                        v[2 * q][j] = f.x;
-                        v[2 * q + 1][j] = f.y;
-                    }
-                } else {
-                    const float4 f = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
-                    v[0][j] = f.x; v[1 % RB][j] = f.y; v[2 % RB][j] = f.z; v[3 % RB][j] = f.w;
+            for (int q = 0; q < RB; ++q) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t w = (&u[j].x)[q >> 1], wl = (&ul[j].x)[q >> 1];
+                    v[j] = __uint_as_float((q & 1) ? (w & 0xFFFF0000u) : (w << 16)) +
+                           __uint_as_float((q & 1) ? (wl & 0xFFFF0000u) : (wl << 16));
                 }
+                put8<SPLIT>(hi, lo, r0 + q, kc, v);
+            }
+            continue;
+        }
+        float v[RB][8];   // v[row][k]
+        if (!BF && full) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int64_t i;
+                const void *p = op_at<IS_A>(O, row, k + j, i);
+                const float4 f = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i));
+                v[0][j] = f.x; v[1 % RB][j] = f.y; v[2 % RB][j] = f.z; v[3 % RB][j] = f.w;
             }
         } else {
 #pragma unroll
@@ -249,6 +277,7 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
                         int64_t i;
                         const void *p = op_at<IS_A>(O, row + q, k + j, i);
                         x = ld1<BF>(p, i);
+                        if (BF && O.lo[0]) x += ld1<true>(lo_of(O, p), i);
                     }
                     v[q][j] = x;
                 }
@@ -266,9 +295,9 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
 // stays resident; otherwise B streams with A.
 //   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. for column half w/4, through
 //               shared memory, 16-byte coalesced stores
-//   warps 8-15  producers: stage A (and B) k-blocks into a ring of S stages
-//   warp 16     TMEM owner; lane 0 issues tcgen05.mma into one of two accumulators
-//   warp 17     lane 0 issues the TMA tile loads, running ahead of the producers by up to
+//   warps 8-13  producers: stage A (and B) k-blocks into a ring of S stages
+//   warp 14     TMEM owner; lane 0 issues tcgen05.mma into one of two accumulators
+//   warp 15     lane 0 issues the TMA tile loads, running ahead of the producers by up to
 //               S stages (bf16 tiles land in the MMA layout; fp32 tiles land raw and the
 //               producers convert them in place)
 // Barriers: full[s]/empty[s] hand stages producer -> MMA -> producer; accf[b]/acce[b]
@@ -285,10 +314,12 @@ __host__ __device__ inline bool ld_tma(int m) { return m != LD_REG; }
 
 struct TcArgs {
     CUtensorMap tmA[3], tmB[3];   // one map per array of a blocked operand
+    CUtensorMap tmBlo[3];         // low parts of a pre-split B
+    CUtensorMap tmAmul;           // the elementwise factor of a raw-loaded A
     int64_t M, Nc, K, kper;
     int BN, stages, n_tiles, m_tiles, splits;
     int a_ld, b_ld;
-    bool b_res;
+    bool b_res, a_mul, b_lo;
     GemmOperand A, Bm;
     GemmEpilogue ep;
     unsigned *status;
@@ -341,36 +372,50 @@ __device__ __forceinline__ void put4(uint8_t *hi, uint8_t *lo, int r, int k4, fl
     }
 }
 
-template <bool SPLIT, bool MN>
+template <bool SPLIT, bool MN, bool MUL = false>
 __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
     constexpr int R = TC_BM;
     const float *raw = reinterpret_cast<const float *>(region);
     if (!MN) {
-        constexpr int PER = R * 16 / TC_PROD;    // float4 (4 k of one row) per thread
+        constexpr int ITEMS = R * 16, PER = (ITEMS + TC_PROD - 1) / TC_PROD;   // float4 (4 k of one row)
         float4 v[PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) v[i] = reinterpret_cast<const float4 *>(raw)[ptid + i * TC_PROD];
+        for (int i = 0; i < PER; ++i) {
+            const int q = ptid + i * TC_PROD;
+            if (q < ITEMS) v[i] = reinterpret_cast<const float4 *>(raw)[q];
+        }
+        if (MUL) {
+            // the factor tile (same layout) follows the operand tile
+            const float4 *mraw = reinterpret_cast<const float4 *>(region + R * 256);
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int q = ptid + i * TC_PROD;
+                if (q < ITEMS) v[i] = v[i] * mraw[q];
+            }
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int q = ptid + i * TC_PROD;    // float4 index: row q/16, k4 q%16
-            put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
+            if (q < ITEMS) put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
         }
     } else {
-        constexpr int PER = R * 8 / TC_PROD;     // items (one row, 8 k) per thread
+        constexpr int ITEMS = R * 8, PER = (ITEMS + TC_PROD - 1) / TC_PROD;    // items (one row, 8 k)
         float v[PER][8];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int it = ptid + i * TC_PROD, r = it % R, kc = it / R;
             const float *src = raw + (r >> 6) * 4096 + (r & 63);
+            if (it < ITEMS) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
+                for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int it = ptid + i * TC_PROD;
-            put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
+            if (it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
         }
     }
 }
@@ -378,17 +423,18 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
 // Shared-memory layout.  A stage holds the A region then (unless B is resident) the B
 // region.  A region: bf16 hi tile, then the lo tile (split mode); an operand loaded raw
 // (fp32 by TMA, converted in place) needs twice the bf16 tile, which the split mode's
-// hi + lo already provides.  Resident B: per k-block a hi tile then a lo tile.
+// hi + lo already provides, and a raw operand with an elementwise factor twice that
+// again (the factor's raw tile follows).  Resident B: per k-block a hi tile then a lo tile.
 struct TcLayout {
     uint32_t a_bytes, b_bytes, a_reg, b_reg, stage_bytes, bres_kb, bres_bytes;
 };
 __host__ __device__ inline TcLayout tc_layout(int BN, int64_t K, bool b_res, bool split, bool a_raw = false,
-                                              bool b_raw = false) {
+                                              bool b_raw = false, bool a_mul = false) {
     TcLayout L;
     const uint32_t f = split ? 2u : 1u;
     L.a_bytes = TC_BM * 128u;
     L.b_bytes = uint32_t(BN) * 128u;
-    L.a_reg = L.a_bytes * ((split || a_raw) ? 2u : 1u);
+    L.a_reg = L.a_bytes * (a_mul ? 4u : (split || a_raw) ? 2u : 1u);
     L.b_reg = b_res ? 0u : L.b_bytes * ((split || b_raw) ? 2u : 1u);
     L.stage_bytes = L.a_reg + L.b_reg;
     const uint32_t kb = uint32_t((K + TC_BK - 1) / TC_BK);
@@ -464,7 +510,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int BN = args.BN, S = args.stages;
-    const TcLayout Lo = tc_layout(BN, args.kper, args.b_res, SPLIT, ld_raw(args.a_ld), ld_raw(args.b_ld));
+    const TcLayout Lo = tc_layout(BN, args.kper, args.b_res, SPLIT, ld_raw(args.a_ld), ld_raw(args.b_ld), args.a_mul);
     uint8_t *bres = base;                                         // resident B (hi k-blocks, then lo)
     uint8_t *stages = base + Lo.bres_bytes;                       // ring of A (+B) stages
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
@@ -578,6 +624,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     }
                     if (a_raw) {
                         if (args.a_ld == LD_RAW_MN) convert_raw128<SPLIT, true>(sa, ptid);
+                        else if (args.a_mul) convert_raw128<SPLIT, false, true>(sa, ptid);
                         else convert_raw128<SPLIT, false>(sa, ptid);
                     }
                     if (b_raw) {
@@ -596,10 +643,14 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 int64_t m0, n0, kb0, ke;
                 int z;
                 tile_of(blockIdx.x, m0, n0, z, kb0, ke);
-                mbar_arrive_expect_tx(smem_u32(bready), uint32_t(nkb_full) * Lo.b_bytes);
-                for (int64_t kb = 0; kb < nkb_full; ++kb)
+                mbar_arrive_expect_tx(smem_u32(bready), uint32_t(nkb_full) * Lo.b_bytes * (args.b_lo ? 2u : 1u));
+                for (int64_t kb = 0; kb < nkb_full; ++kb) {
                     tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
                                     bres + size_t(kb) * Lo.bres_kb, smem_u32(bready));
+                    if (args.b_lo)
+                        tma_tile<false>(args.tmBlo, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
+                                        bres + size_t(kb) * Lo.bres_kb + Lo.b_bytes, smem_u32(bready));
+                }
             }
             bool ok = a_dir || b_dir || a_raw || b_raw;
             int64_t kbg = 0;
@@ -618,18 +669,24 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     uint8_t *st = stages + size_t(s) * Lo.stage_bytes;
                     uint8_t *sa = st, *sbb = st + Lo.a_reg;
                     const int64_t k0 = kb0 + kb * TC_BK;
-                    const uint32_t txd = (a_dir ? Lo.a_bytes : 0u) + (b_dir ? Lo.b_bytes : 0u);
-                    const uint32_t txr = (a_raw ? 2u * Lo.a_bytes : 0u) + (b_raw ? 2u * Lo.b_bytes : 0u);
+                    const uint32_t txd = (a_dir ? Lo.a_bytes : 0u) + (b_dir ? Lo.b_bytes * (args.b_lo ? 2u : 1u) : 0u);
+                    const uint32_t txr = (a_raw ? (args.a_mul ? 4u : 2u) * Lo.a_bytes : 0u) + (b_raw ? 2u * Lo.b_bytes : 0u);
                     if (txd) {
                         const uint32_t fb = smem_u32(&full[s]);
                         mbar_arrive_expect_tx(fb, txd);
                         if (a_dir) tma_tile<true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, fb);
-                        if (b_dir) tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, k0, sbb, fb);
+                        if (b_dir) {
+                            tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, k0, sbb, fb);
+                            if (args.b_lo) tma_tile<false>(args.tmBlo, args.Bm, args.b_ld, n0, BN, k0, sbb + Lo.b_bytes, fb);
+                        }
                     }
                     if (txr) {
                         const uint32_t rb = smem_u32(&rawfull[s]);
                         mbar_arrive_expect_tx(rb, txr);
-                        if (a_raw) tma_tile<true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, rb);
+                        if (a_raw) {
+                            tma_tile<true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, rb);
+                            if (args.a_mul) tma_tile<true>(&args.tmAmul, args.A, args.a_ld, m0, TC_BM, k0, sa + 2 * Lo.a_bytes, rb);
+                        }
                         if (b_raw) tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, k0, sbb, rb);
                     }
                 }
@@ -676,10 +733,15 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     for (int ks = 0; ks < TC_BK / 16; ++ks) {
                         const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
                         if (SPLIT) {
-                            const uint32_t koff = uint32_t(ks) * 32u;
-                            mma_bf16(dacc, sw128_desc(a_hi + koff), sw128_desc(b_hi + koff), idesc, acc);
-                            mma_bf16(dacc, sw128_desc(a_hi + koff), sw128_desc(b_lo + koff), idesc, 1u);
-                            mma_bf16(dacc, sw128_desc(a_lo + koff), sw128_desc(b_hi + koff), idesc, 1u);
+                            const uint32_t ka = a_mn ? uint32_t(ks) * 2048u : uint32_t(ks) * 32u;
+                            const uint32_t kb2 = b_mn ? uint32_t(ks) * 2048u : uint32_t(ks) * 32u;
+                            const uint64_t ah = a_mn ? sw128_desc_mn(a_hi + ka) : sw128_desc(a_hi + ka);
+                            const uint64_t al = a_mn ? sw128_desc_mn(a_lo + ka) : sw128_desc(a_lo + ka);
+                            const uint64_t bh = b_mn ? sw128_desc_mn(b_hi + kb2) : sw128_desc(b_hi + kb2);
+                            const uint64_t bl = b_mn ? sw128_desc_mn(b_lo + kb2) : sw128_desc(b_lo + kb2);
+                            mma_bf16(dacc, ah, bh, idesc, acc);
+                            mma_bf16(dacc, ah, bl, idesc, 1u);
+                            mma_bf16(dacc, al, bh, idesc, 1u);
                         } else {
                             const uint64_t ad = a_mn ? sw128_desc_mn(a_hi + uint32_t(ks) * 2048u)
                                                      : sw128_desc(a_hi + uint32_t(ks) * 32u);
@@ -776,7 +838,10 @@ static bool make_map(CUtensorMap *m, const void *base, bool bf16, uint64_t inner
 // straight into the MMA layout (not in split mode); fp32 without a product, 128-row tiles
 // -> TMA raw + in-place conversion; otherwise register staging.
 static int tma_mode(const GemmOperand &O, bool is_a, int64_t rows, int64_t K, int R, bool split3) {
-    if (O.mul) return LD_REG;
+    // an elementwise factor: only a k-contiguous fp32 A of one array, loaded raw
+    if (O.mul && (!is_a || O.bf16 || O.s_k != 1 || O.blk < (int64_t(1) << 30) || O.s_row % 4 || R != TC_BM ||
+                  (reinterpret_cast<uintptr_t>(O.mul) & 15u)))
+        return LD_REG;
     const bool blocked = O.blk < (int64_t(1) << 30);
     if (blocked && (((is_a ? K : rows) + O.blk - 1) / O.blk > 3 || (is_a ? O.blk % TC_BK : O.blk % R))) return LD_REG;
     const int vec = O.bf16 ? 8 : 4;   // elements per 16 bytes
@@ -784,13 +849,14 @@ static int tma_mode(const GemmOperand &O, bool is_a, int64_t rows, int64_t K, in
     if (O.s_k == 1 && O.s_row % vec == 0) mode = LD_TMA_K;
     else if (O.s_row == 1 && O.s_k % vec == 0 && R % 64 == 0) mode = LD_TMA_MN;
     else return LD_REG;
-    if (O.bf16) return split3 ? LD_REG : mode;
+    if (O.bf16) return (split3 && !O.lo[0]) || (!split3 && O.lo[0]) ? LD_REG : mode;   // split mode: bf16 pre-split only
     return R == TC_BM ? (mode == LD_TMA_K ? LD_RAW_K : LD_RAW_MN) : LD_REG;
 }
 
 // Build the maps of an operand for the chosen mode; returns the mode, or LD_REG if a map
 // cannot be built.
-static int tma_build(CUtensorMap *maps, const GemmOperand &O, int mode, bool is_a, int64_t rows, int64_t K, int R) {
+static int tma_build(CUtensorMap *maps, CUtensorMap *lo_maps, CUtensorMap *mul_map, const GemmOperand &O, int mode,
+                     bool is_a, int64_t rows, int64_t K, int R) {
     if (mode == LD_REG) return LD_REG;
     const bool blocked = O.blk < (int64_t(1) << 30);
     const int nmaps = blocked ? int(((is_a ? K : rows) + O.blk - 1) / O.blk) : 1;
@@ -798,13 +864,15 @@ static int tma_build(CUtensorMap *maps, const GemmOperand &O, int mode, bool is_
     const int64_t rext = (!is_a && blocked) ? O.blk : rows;
     const uint64_t es = O.bf16 ? 2 : 4;
     const bool kmaj = mode == LD_TMA_K || mode == LD_RAW_K;
+    auto build = [&](CUtensorMap *m, const void *base) {
+        return kmaj ? make_map(m, base, O.bf16, uint64_t(kext), uint64_t(rext), uint64_t(O.s_row) * es, 64, uint32_t(R))
+                    : make_map(m, base, O.bf16, uint64_t(rext), uint64_t(kext), uint64_t(O.s_k) * es, 64, 64);
+    };
     for (int i = 0; i < nmaps; ++i) {
-        const bool ok = kmaj ? make_map(&maps[i], O.p[i], O.bf16, uint64_t(kext), uint64_t(rext), uint64_t(O.s_row) * es,
-                                        64, uint32_t(R))
-                             : make_map(&maps[i], O.p[i], O.bf16, uint64_t(rext), uint64_t(kext), uint64_t(O.s_k) * es,
-                                        64, 64);
-        if (!ok) return LD_REG;
+        if (!build(&maps[i], O.p[i])) return LD_REG;
+        if (O.lo[0] && (!lo_maps || !build(&lo_maps[i], O.lo[i]))) return LD_REG;
     }
+    if (O.mul && (!mul_map || !build(mul_map, O.mul))) return LD_REG;
     return mode;
 }
 
@@ -838,21 +906,21 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     // that TMA can load raw takes 128-column tiles (the in-place conversion works on 128 rows).
     const size_t budget = 227 * 1024 - 1024 - TC_EPI_SMEM - 512;
     const int a_mode = tma_mode(A, true, M, K, TC_BM, split3);
+    const bool a_mul = A.mul && ld_raw(a_mode);
     int BN = int(Nc < 256 ? (Nc + 31) / 32 * 32 : 256);
     int S = 0, b_mode = LD_REG;
     for (int next = BN;; BN = next) {
         if (BN == 0) return cudaErrorInvalidConfiguration;
         next = BN > 32 ? (BN / 2 + 31) / 32 * 32 : 0;
-        const TcLayout res = tc_layout(BN, a.kper, true, split3, ld_raw(a_mode), false);
+        const TcLayout res = tc_layout(BN, a.kper, true, split3, ld_raw(a_mode), false, a_mul);
         a.b_res = splits == 1 && size_t(res.bres_bytes) + 2 * size_t(res.stage_bytes) <= budget;
-        b_mode = a.b_res ? (split3 ? LD_REG : tma_mode(Bm, false, Nc, K, BN, false))
-                         : tma_mode(Bm, false, Nc, K, BN, split3);
+        b_mode = tma_mode(Bm, false, Nc, K, BN, split3);
         if (a.b_res && ld_raw(b_mode)) b_mode = LD_REG;          // a resident B is converted once, by registers
         if (!a.b_res && !Bm.bf16 && !Bm.mul && BN > TC_BM && tma_mode(Bm, false, Nc, K, TC_BM, split3) != LD_REG) {
             next = TC_BM;                                         // take 128-column tiles to load B raw
             continue;
         }
-        const TcLayout Lt = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode));
+        const TcLayout Lt = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
         S = int((budget - Lt.bres_bytes) / Lt.stage_bytes);
         if (S >= 2) break;
     }
@@ -874,11 +942,13 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.n_tiles = int((Nc + BN - 1) / BN);
     a.m_tiles = int((M + TC_BM - 1) / TC_BM);
     a.A = A; a.Bm = Bm; a.ep = ep; a.status = status;
-    a.a_ld = tma_build(a.tmA, A, a_mode, true, M, K, TC_BM);
-    a.b_ld = tma_build(a.tmB, Bm, b_mode, false, Nc, K, BN);
+    a.a_ld = tma_build(a.tmA, nullptr, &a.tmAmul, A, a_mode, true, M, K, TC_BM);
+    a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, BN);
+    a.a_mul = a_mul && a.a_ld != LD_REG;
+    a.b_lo = Bm.lo[0] && a.b_ld != LD_REG;
     // the layout was sized for the modes asked for; a mode that fell back to registers
     // uses only part of its region
-    const TcLayout L = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode));
+    const TcLayout L = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
     const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + TC_EPI_SMEM + (3 * S + 6) * 8;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
     int64_t grid = ntiles;

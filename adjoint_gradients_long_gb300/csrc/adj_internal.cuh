@@ -99,6 +99,8 @@ cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, cons
 // GEMM operands: strided, optionally split over up to three arrays.
 struct GemmOperand {
     const void *p[3];    // up to three arrays split along K (A) or along Nc (B)
+    const void *lo[3];   // pre-split operand: bf16 low parts of p (then p holds the bf16
+                         // high parts, x = hi + lo); null otherwise
     int64_t blk;         // split size (K for A, Nc for B); >= the dimension if one array
     int64_t s_row;       // stride of the M (A) / Nc (B) index within one array
     int64_t s_k;         // stride of the K index
@@ -125,6 +127,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
                            const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
                            int *splits_used = nullptr);
 
+// hi = bf16(w), lo = bf16(w - hi) for n fp32 values (operands of the split-precision GEMM)
+cudaError_t launch_split_bf16(const float *w, int64_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo, cudaStream_t st);
 cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out,
                                  int accumulate, cudaStream_t st);
 cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk,

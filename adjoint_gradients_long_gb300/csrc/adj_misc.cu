@@ -151,6 +151,25 @@ cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, f
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- bf16 hi/lo split of an operand
+__global__ void __launch_bounds__(256) k_split_bf16(const float *__restrict__ w, int64_t n,
+                                                    __nv_bfloat16 *__restrict__ hi, __nv_bfloat16 *__restrict__ lo) {
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+        const float x = w[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        hi[i] = h;
+        lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    }
+}
+
+cudaError_t launch_split_bf16(const float *w, int64_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo, cudaStream_t st) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 1024) blocks = 1024;
+    if (blocks < 1) return cudaSuccess;
+    k_split_bf16<<<unsigned(blocks), 256, 0, st>>>(w, n, hi, lo);
+    return cudaGetLastError();
+}
+
 }  // namespace adj
 
 namespace adj {
