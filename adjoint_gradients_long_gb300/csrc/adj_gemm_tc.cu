@@ -316,10 +316,13 @@ struct TcArgs {
     CUtensorMap tmA[3], tmB[3];   // one map per array of a blocked operand
     CUtensorMap tmBlo[3];         // low parts of a pre-split B
     CUtensorMap tmAmul;           // the elementwise factor of a raw-loaded A
+    CUtensorMap tmO[3];           // epilogue outputs stored by TMA (ProjIn: a, u, c)
+    CUtensorMap tmAdd;            // StoreAdd: the residual, loaded by TMA
     int64_t M, Nc, K, kper;
     int BN, stages, n_tiles, m_tiles, splits;
     int a_ld, b_ld;
     bool b_res, a_mul, b_lo;
+    bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
     GemmOperand A, Bm;
     GemmEpilogue ep;
     unsigned *status;
@@ -516,9 +519,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + TC_EPI_SMEM);
     uint64_t *full = bars, *empty = bars + S, *accf = bars + 2 * S, *acce = bars + 2 * S + 2, *bready = bars + 2 * S + 4;
-    uint64_t *rawfull = bars + 2 * S + 5;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3 * S + 5) + 1;
+    uint64_t *rawfull = bars + 2 * S + 5, *addb = bars + 3 * S + 5;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5 + TC_EPI_WARPS);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3 * S + 5 + TC_EPI_WARPS) + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t ntiles = int64_t(args.n_tiles) * args.m_tiles * args.splits;
@@ -544,6 +547,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             mbar_init(smem_u32(&acce[b]), TC_EPI_WARPS * 32);
         }
         mbar_init(smem_u32(bready), ld_tma(args.b_ld) ? 1 : TC_PROD);
+        for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(smem_u32(&addb[w]), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -758,8 +762,15 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         __syncwarp();
     } else {
         // ---------------- epilogue (warp w: TMEM lanes 32*(w%4).., columns of half w/4)
+        // A 32 x 32 chunk goes TMEM -> registers (lane = row) -> the warp's swizzled
+        // shared buffer -> global.  With TMA stores (epi_tma) the fused op is applied in
+        // registers, the residual of StoreAdd arrives in the buffer by TMA while TMEM is
+        // read, and one lane stores the chunk; otherwise lanes store column quads.
         float *sb = esm + warp * (32 * 32);
+        const uint32_t sb_s = smem_u32(sb), addbar = smem_u32(&addb[warp]);
         const int q = warp & 3, half = warp >> 2;
+        const GemmEpilogue &ep = args.ep;
+        uint32_t add_phase = 0;
         int64_t i = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             int64_t m0, n0, kb0, ke;
@@ -771,6 +782,23 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             tc_fence_after();
             const int64_t m0r = m0 + q * 32;
             for (int c = half * 32; c < BN; c += 64) {
+                const int n = int(n0) + c;
+                const bool live = m0r < args.M && n < args.Nc;
+                // a chunk outside the output is skipped (with TMA stores its buffer may still
+                // be the source of the previous chunk's store)
+                if (args.epi_tma && !live) continue;
+                const bool via_tma = args.epi_tma;
+                const bool add_tma = via_tma && ep.kind == Epi::StoreAdd;
+                if (via_tma) {
+                    if (lane == 0) {
+                        bulk_wait_read();   // the previous chunk's store has read the buffer
+                        if (add_tma) {
+                            mbar_arrive_expect_tx(addbar, 32 * 32 * 4);
+                            tma_load_2d(sb_s, &args.tmAdd, n, int(m0r), addbar);
+                        }
+                    }
+                    __syncwarp();
+                }
                 float v[32];
                 if (ok && nkb > 0) {
                     tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(buf * BN + c), v);
@@ -778,17 +806,61 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
+                if (via_tma) {
+                    if (ep.kind == Epi::ProjIn && n < ep.N) {
+                        // a = sigmoid(z + b_a) (the chunk lies within one block: N % 32 == 0)
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(sb + epi_at(lane, j >> 2)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                __syncwarp();
-                if (m0r < args.M) epi_chunk(args, sb, m0r, int(n0) + c, z, lane);
-                __syncwarp();
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(ep.bias + n + j));
+                            v[j] = sigmoidf_fast(v[j] + b4.x);
+                            v[j + 1] = sigmoidf_fast(v[j + 1] + b4.y);
+                            v[j + 2] = sigmoidf_fast(v[j + 2] + b4.z);
+                            v[j + 3] = sigmoidf_fast(v[j + 3] + b4.w);
+                        }
+                    }
+                    if (add_tma) {
+                        mbar_wait(addbar, add_phase, abort, args.status);
+                        add_phase ^= 1u;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 r4 = *reinterpret_cast<const float4 *>(sb + epi_at(lane, j >> 2));
+                            v[j] += r4.x;
+                            v[j + 1] += r4.y;
+                            v[j + 2] += r4.z;
+                            v[j + 3] += r4.w;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(sb + epi_at(lane, j >> 2)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (ep.kind == Epi::Partial) {
+                            tma_store_3d(&args.tmO[0], n, int(m0r), z, sb_s);
+                        } else if (ep.kind == Epi::ProjIn) {
+                            const int blk = n / ep.N;
+                            tma_store_2d(&args.tmO[blk], n - blk * ep.N, int(m0r), sb_s);
+                        } else {
+                            tma_store_2d(&args.tmO[0], n, int(m0r), sb_s);
+                        }
+                        bulk_commit();
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(sb + epi_at(lane, j >> 2)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    __syncwarp();
+                    if (m0r < args.M) epi_chunk(args, sb, m0r, n, z, lane);
+                    __syncwarp();
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&acce[buf]));
             if (!ok) break;
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -832,6 +904,50 @@ static bool make_map(CUtensorMap *m, const void *base, bool bf16, uint64_t inner
                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of an fp32 epilogue output (or residual) for 32 x 32 chunks in the 128-byte
+// swizzled layout of the epilogue buffer.  Rank 2, or (depth > 0) rank 3 with `depth`
+// matrices `mat_stride` bytes apart (split-K partials, stored with 3-D coordinates).
+static bool make_out_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t pitch_bytes,
+                         uint64_t depth = 0, uint64_t mat_stride = 0) {
+    auto enc = encode_fn();
+    if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || (pitch_bytes & 15u) || (mat_stride & 15u) ||
+        cols == 0 || rows == 0)
+        return false;
+    const cuuint64_t dims[3] = {cols, rows, depth > 0 ? depth : 1};
+    const cuuint64_t strides[2] = {pitch_bytes, depth > 0 ? mat_stride : pitch_bytes * rows};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, depth > 0 ? 3 : 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Epilogue through TMA stores when every map builds: fp32 outputs (no bf16 copy), an
+// fp32 residual, ProjIn blocks that 32-column chunks do not straddle.
+static bool epi_maps(TcArgs &a, const GemmEpilogue &ep, int64_t M, int64_t Nc, int splits) {
+    switch (ep.kind) {
+    case Epi::ProjIn:
+        if (ep.N % 32) return false;
+        for (int b = 0; b < 3; ++b) {
+            float *o = b == 0 ? ep.out0 : b == 1 ? ep.out1 : ep.out2;
+            if (!make_out_map(&a.tmO[b], o, uint64_t(ep.N), uint64_t(M), uint64_t(ep.N) * 4)) return false;
+        }
+        return true;
+    case Epi::Store:
+    case Epi::StoreAdd:
+        if (ep.out_x) return false;
+        if (!make_out_map(&a.tmO[0], ep.out0, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4)) return false;
+        if (ep.kind == Epi::StoreAdd &&
+            (ep.add_bf16 || !make_out_map(&a.tmAdd, ep.add, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4)))
+            return false;
+        return true;
+    case Epi::Partial:
+        return make_out_map(&a.tmO[0], ep.out0, uint64_t(Nc), uint64_t(M), uint64_t(Nc) * 4, uint64_t(splits),
+                            uint64_t(M) * uint64_t(Nc) * 4);
+    }
+    return false;
 }
 
 // Load mode an operand can use (no maps built): bf16 without a prologue product -> TMA
@@ -945,11 +1061,12 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.a_ld = tma_build(a.tmA, nullptr, &a.tmAmul, A, a_mode, true, M, K, TC_BM);
     a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, BN);
     a.a_mul = a_mul && a.a_ld != LD_REG;
+    a.epi_tma = epi_maps(a, ep, M, Nc, splits);
     a.b_lo = Bm.lo[0] && a.b_ld != LD_REG;
     // the layout was sized for the modes asked for; a mode that fell back to registers
     // uses only part of its region
     const TcLayout L = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
-    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + TC_EPI_SMEM + (3 * S + 6) * 8;
+    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + TC_EPI_SMEM + (3 * S + 6 + TC_EPI_WARPS) * 8;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
     int64_t grid = ntiles;
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;
