@@ -8,7 +8,7 @@
 //          lo = bf16(x - hi); the product uses hi*hi + hi*lo + lo*hi (the lo*lo
 //          term is below 2^-16 of the product), three MMAs into one accumulator.
 //
-// CTA: 16 warps (4 per SM sub-partition, so 128 registers a thread) in four roles (epilogue, producers, MMA issuer, TMA issuer; see the
+// CTA: 18 warps in four roles (epilogue, producers, MMA issuer, TMA issuer; see the
 // kernel below).  Stages, accumulators and the resident B tile are handed over with
 // mbarriers, and every wait is bounded by a wall-clock limit.
 //
@@ -27,7 +27,7 @@
 namespace adj {
 
 #ifndef ADJ_TC_PROD_WARPS
-#define ADJ_TC_PROD_WARPS 6
+#define ADJ_TC_PROD_WARPS 8
 #endif
 constexpr int TC_BM = 128, TC_BK = 64;
 constexpr int TC_PROD_WARPS = ADJ_TC_PROD_WARPS, TC_PROD = TC_PROD_WARPS * 32;
@@ -295,14 +295,18 @@ __device__ __forceinline__ void stage_tile(const GemmOperand &O, int64_t row0, i
 // stays resident; otherwise B streams with A.
 //   warps 0-7   epilogue: warp w reads TMEM lanes 32*(w%4).. for column half w/4, through
 //               shared memory, 16-byte coalesced stores
-//   warps 8-13  producers: stage A (and B) k-blocks into a ring of S stages
-//   warp 14     TMEM owner; lane 0 issues tcgen05.mma into one of two accumulators
-//   warp 15     lane 0 issues the TMA tile loads, running ahead of the producers by up to
+//   warps 8-15  producers: stage A (and B) k-blocks into a ring of S stages
+//   warp 16     TMEM owner; lane 0 issues tcgen05.mma into one of two accumulators
+//   warp 17     lane 0 issues the TMA tile loads, running ahead of the producers by up to
 //               S stages (bf16 tiles land in the MMA layout; fp32 tiles land raw and the
 //               producers convert them in place)
 // Barriers: full[s]/empty[s] hand stages producer -> MMA -> producer; accf[b]/acce[b]
 // hand accumulator b MMA -> epilogue -> MMA; bres marks the resident B tile ready.
-constexpr int TC_EPI_WARPS = 8, TC_THREADS_P = (TC_EPI_WARPS + TC_PROD_WARPS + 2) * 32;
+#ifndef ADJ_TC_EPI_WARPS
+#define ADJ_TC_EPI_WARPS 8
+#endif
+constexpr int TC_EPI_WARPS = ADJ_TC_EPI_WARPS, TC_THREADS_P = (TC_EPI_WARPS + TC_PROD_WARPS + 2) * 32;
+static_assert(TC_EPI_WARPS % 4 == 0, "epilogue warps cover the four TMEM lane quarters");
 constexpr int TC_MMA_WARP = TC_EPI_WARPS + TC_PROD_WARPS, TC_TMA_WARP = TC_MMA_WARP + 1;
 constexpr uint32_t TC_EPI_SMEM = TC_EPI_WARPS * 32 * 32 * 4;
 
@@ -385,7 +389,7 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int q = ptid + i * TC_PROD;
-            if (q < ITEMS) v[i] = reinterpret_cast<const float4 *>(raw)[q];
+            if (ITEMS % TC_PROD == 0 || q < ITEMS) v[i] = reinterpret_cast<const float4 *>(raw)[q];
         }
         if (MUL) {
             // the factor tile (same layout) follows the operand tile
@@ -393,14 +397,14 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int q = ptid + i * TC_PROD;
-                if (q < ITEMS) v[i] = v[i] * mraw[q];
+                if (ITEMS % TC_PROD == 0 || q < ITEMS) v[i] = v[i] * mraw[q];
             }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int q = ptid + i * TC_PROD;    // float4 index: row q/16, k4 q%16
-            if (q < ITEMS) put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
+            if (ITEMS % TC_PROD == 0 || q < ITEMS) put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
         }
     } else {
         constexpr int ITEMS = R * 8, PER = (ITEMS + TC_PROD - 1) / TC_PROD;    // items (one row, 8 k)
@@ -409,7 +413,7 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
         for (int i = 0; i < PER; ++i) {
             const int it = ptid + i * TC_PROD, r = it % R, kc = it / R;
             const float *src = raw + (r >> 6) * 4096 + (r & 63);
-            if (it < ITEMS) {
+            if (ITEMS % TC_PROD == 0 || it < ITEMS) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
             }
@@ -418,7 +422,7 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int it = ptid + i * TC_PROD;
-            if (it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
+            if (ITEMS % TC_PROD == 0 || it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
         }
     }
 }
@@ -768,7 +772,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         // read, and one lane stores the chunk; otherwise lanes store column quads.
         float *sb = esm + warp * (32 * 32);
         const uint32_t sb_s = smem_u32(sb), addbar = smem_u32(&addb[warp]);
-        const int q = warp & 3, half = warp >> 2;
+        const int q = warp & 3, half = warp >> 2;   // lane quarter; column-chunk phase
+        constexpr int CSTEP = 32 * (TC_EPI_WARPS / 4);
         const GemmEpilogue &ep = args.ep;
         uint32_t add_phase = 0;
         int64_t i = 0;
@@ -781,7 +786,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&accf[buf]), uint32_t((i >> 1) & 1), abort, args.status));
             tc_fence_after();
             const int64_t m0r = m0 + q * 32;
-            for (int c = half * 32; c < BN; c += 64) {
+            for (int c = half * 32; c < BN; c += CSTEP) {
                 const int n = int(n0) + c;
                 const bool live = m0r < args.M && n < args.Nc;
                 // a chunk outside the output is skipped (with TMA stores its buffer may still
