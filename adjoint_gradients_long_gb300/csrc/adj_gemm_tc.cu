@@ -23,6 +23,7 @@
 #include "adj_internal.cuh"
 #include "adj_epilogue.cuh"
 #include "adj_ptx.cuh"
+#include "adj_tmap.cuh"
 
 namespace adj {
 
@@ -877,21 +878,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
 
 // ---------------------------------------------------------------- launcher
 static int g_num_sms = 0;
-static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-static bool g_encode_tried = false;
-
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    if (!g_encode_tried) {
-        g_encode_tried = true;
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    return g_encode;
-}
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tmap_encoder(); }
 
 // 2-D tensor map: inner (contiguous) extent x outer extent, row pitch in bytes, box
 // box_in x box_out; bf16 maps use the 128-byte swizzle of the MMA layout, fp32 (raw) maps

@@ -15,8 +15,24 @@ __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const
                                               float *__restrict__ gy, int64_t count, double *__restrict__ part) {
     __shared__ double red[256];
     float s = 0.f;
-    const int64_t n4 = count / 4;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t n4 = count / 4, stride = int64_t(gridDim.x) * blockDim.x;
+    int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    // four vectors of each input in flight per thread
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+        float4 a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            a[u] = ld_stream4(y + 4 * (i + u * stride));
+            b[u] = ld_stream4(tg + 4 * (i + u * stride));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 r = a[u] - b[u];
+            if (gy) st_stream4(gy + 4 * (i + u * stride), r);
+            s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
+        }
+    }
+    for (; i < n4; i += stride) {
         const float4 r = ld_stream4(y + 4 * i) - ld_stream4(tg + 4 * i);
         if (gy) st_stream4(gy + 4 * i, r);
         s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
@@ -86,11 +102,12 @@ __global__ void __launch_bounds__(256) k_colsum(const void *__restrict__ D, int6
         float4 acc = f4(0.f);
         if (rl < lanes && col < N) {
             int64_t r = r0 + rl;
-            for (; r + 3 * lanes < r1; r += 4 * lanes) {
-                const float4 v0 = ld_row4<BF>(D, r * N + col), v1 = ld_row4<BF>(D, (r + lanes) * N + col);
-                const float4 v2 = ld_row4<BF>(D, (r + 2 * lanes) * N + col);
-                const float4 v3 = ld_row4<BF>(D, (r + 3 * lanes) * N + col);
-                acc = acc + ((v0 + v1) + (v2 + v3));
+            // eight rows in flight per thread
+            for (; r + 7 * lanes < r1; r += 8 * lanes) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = ld_row4<BF>(D, (r + u * lanes) * N + col);
+                acc = acc + (((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7])));
             }
             for (; r < r1; r += lanes) acc = acc + ld_row4<BF>(D, r * N + col);
         }

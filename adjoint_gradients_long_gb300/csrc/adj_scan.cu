@@ -17,20 +17,34 @@
 //     scan restarted at every block start (k_win_scan).  Every product spans at most
 //     W factors.
 //
-// Work decomposition (all three kernels): a CTA of 8 warps owns one chunk of
-// 8*L consecutive tokens of one sequence and 128 channels (lane = 4 channels, one
-// float4 per token row, so every warp access is a 512-byte coalesced row segment).
-// Warp w owns tokens [chunk*8L + w*L, +L).  Each thread reduces its L tokens to one
-// composite map, the 8 warp composites are combined in shared memory, and warp 0
-// publishes the chunk aggregate and looks back over its predecessors' descriptors
-// (decoupled look-back).  Chunks are numbered by an atomic ticket in scan order,
-// so a CTA only ever waits for CTAs that started before it; every wait is bounded.
+// Work decomposition (all three kernels): a CTA of 8 warps owns one chunk of 8*L
+// consecutive tokens of one sequence and 128 channels.  The chunk's input rows are
+// staged in shared memory by one TMA load per array (rows of 128 fp32, 512 bytes), so
+// both passes read them from shared memory and HBM sees every input byte once.  Lane
+// = 4 channels (one float4 per token row), warp w = tokens [w*L, (w+1)*L) of the
+// chunk.  Pass 1 reduces each thread's L tokens to one composite map; the 8 warp
+// composites are combined in shared memory and warp 0 publishes the chunk aggregate
+// and looks back over its predecessors' descriptors (decoupled look-back).  Pass 2
+// applies the carry and writes the outputs.  Chunks are numbered by an atomic ticket
+// in scan order, so a CTA only ever waits for CTAs that started before it; every wait
+// is bounded.
+#include <string.h>
+
 #include "adj_internal.cuh"
+#include "adj_ptx.cuh"
+#include "adj_tmap.cuh"
 
 namespace adj {
 
 constexpr int SC_WARPS = 8;
-constexpr int SC_LB_BATCH = 2;       // descriptor loads in flight per look-back batch
+#ifndef ADJ_SCAN_FWD_L
+#define ADJ_SCAN_FWD_L 12
+#endif
+#ifndef ADJ_SCAN_BWD_L
+#define ADJ_SCAN_BWD_L 8
+#endif
+// tokens per warp (chunk = 8 L tokens) of the forward scan and of the window and reverse scans
+constexpr int SC_FWD_L = ADJ_SCAN_FWD_L, SC_BWD_L = ADJ_SCAN_BWD_L;
 constexpr int SC_SLICE = 128;        // channels per CTA
 constexpr int SC_MIN_CHUNK = 32;     // smallest chunk (L = 4); sizes the descriptor arrays
 constexpr unsigned F_AGG = 1u, F_INC = 2u;
@@ -76,140 +90,232 @@ __device__ __forceinline__ void warp_publish(float4 *p0, float4 v0, float4 *p1, 
 }
 
 
-// Warp-wide decoupled look-back.  The predecessors of a chunk, nearest first, are
-// p0, p0 + dir, p0 + 2 dir, ... (count of them).  Each round, lane i reads the flag of
-// the i-th not yet consumed predecessor; the warp then folds, for its own channels,
-// every published aggregate up to the nearest inclusive prefix (or up to the first
-// predecessor that has published nothing yet, which it then waits for).  Descriptor
-// loads of one round are issued in batches, so a round costs about two L2 round trips
-// however many predecessors it folds.  extend(acc, agg) folds one more aggregate;
-// finish(acc, inc) returns the carry.  A wait that gives up finishes with `zero_inc`.
+// ============================================================================ segment composites
+// Composite maps of token ranges (see each scan below).  Each packs into two float4
+// and a closed flag, so a CTA can pass them through shared memory.
+struct float2x4 {   // forward state scan: h_out = x h_in + y
+    float4 x, y;
+};
+struct FwdSeg {     // window scan R
+    float4 P, S;
+    bool cl;
+};
+struct RevSeg {     // reverse adjoint scan
+    float4 Q, S;
+    bool cl;
+};
+__device__ __forceinline__ void seg_put(const float2x4 &c, float4 &a, float4 &b, bool &cl) { a = c.x; b = c.y; cl = false; }
+__device__ __forceinline__ void seg_put(const FwdSeg &c, float4 &a, float4 &b, bool &cl) { a = c.P; b = c.S; cl = c.cl; }
+__device__ __forceinline__ void seg_put(const RevSeg &c, float4 &a, float4 &b, bool &cl) { a = c.Q; b = c.S; cl = c.cl; }
+__device__ __forceinline__ void seg_get(float2x4 &c, float4 a, float4 b, bool) { c = float2x4{a, b}; }
+__device__ __forceinline__ void seg_get(FwdSeg &c, float4 a, float4 b, bool cl) { c = FwdSeg{a, b, cl}; }
+__device__ __forceinline__ void seg_get(RevSeg &c, float4 a, float4 b, bool cl) { c = RevSeg{a, b, cl}; }
+
+// CTA-wide decoupled look-back (all threads call it).  Each round, warp 0 reads the
+// flags of the next 32 predecessors (nearest first: p0, p0 + dir, ...) and finds how
+// many published aggregates precede the nearest inclusive prefix (or the nearest
+// predecessor that has published nothing); then warp j folds predecessors 4j..4j+3 of
+// them, all warps' descriptor loads in flight at once, and warp 0 folds the 8 partial
+// composites in order.  A round costs about three L2 round trips however many
+// aggregates it consumes.  extend(acc, agg) composes one more (older) predecessor;
+// finish(acc, inc) returns the carry.  sx, sy, scl (8 x 32 entries) and ctl (2 words)
+// are shared scratch.  The result is valid in warp 0; a wait that gives up finishes
+// with zero_inc.
+constexpr int LB_MORE = 0, LB_WAIT = 1, LB_INC = 2, LB_END = 3, LB_TIMEOUT = 4;
 template <class C, class LA, class LI, class EX, class FI>
-__device__ __forceinline__ C warp_lookback(const unsigned *flags, int64_t p0, int dir, int64_t count, C acc,
-                                           LA load_agg, LI load_inc, EX extend, FI finish, C zero_inc,
-                                           unsigned *status, int lane) {
+__device__ __forceinline__ C cta_lookback(const unsigned *flags, int64_t p0, int dir, int64_t count, C ident,
+                                          LA load_agg, LI load_inc, EX extend, FI finish, C zero_inc,
+                                          unsigned *status, float4 (*sx)[32], float4 (*sy)[32], bool *scl, int *ctl,
+                                          int w, int lane) {
+    C acc = ident, result = zero_inc;
     int64_t done = 0;
+    bool wait_first = false;
     for (int round = 0; round < SPIN_LIMIT; ++round) {
-        const bool exists = done + lane < count;
-        const unsigned f = exists ? ld_acquire(&flags[p0 + dir * (done + lane)]) : 0u;
-        const unsigned incl = __ballot_sync(0xffffffffu, exists && f == F_INC);
-        const unsigned miss = __ballot_sync(0xffffffffu, exists && f == 0u);
-        __syncwarp();   // orders every lane's descriptor loads after the flag acquires above
-        const int ji = incl ? __ffs(int(incl)) - 1 : 32, jm = miss ? __ffs(int(miss)) - 1 : 32;
-        int m = ji < jm ? ji : jm;
-        if (int64_t(m) > count - done) m = int(count - done);
-        for (int i0 = 0; i0 < m; i0 += SC_LB_BATCH) {
-            C t[SC_LB_BATCH];
+        if (w == 0) {
+            int m = 0, state;
+            unsigned ok = 1;
+            if (wait_first) {
+                if (lane == 0) ok = wait_flag(&flags[p0 + dir * done], status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+            if (!ok) {
+                state = LB_TIMEOUT;
+            } else {
+                const bool exists = done + lane < count;
+                const unsigned f = exists ? ld_acquire(&flags[p0 + dir * (done + lane)]) : 0u;
+                const unsigned incl = __ballot_sync(0xffffffffu, exists && f == F_INC);
+                const unsigned miss = __ballot_sync(0xffffffffu, exists && f == 0u);
+                const int ji = incl ? __ffs(int(incl)) - 1 : 32, jm = miss ? __ffs(int(miss)) - 1 : 32;
+                m = ji < jm ? ji : jm;
+                if (int64_t(m) > count - done) m = int(count - done);
+                state = (ji < jm && ji == m) ? LB_INC : (done + m >= count) ? LB_END : (m == 0 ? LB_WAIT : LB_MORE);
+            }
+            if (lane == 0) {
+                ctl[0] = m;
+                ctl[1] = state;
+            }
+        }
+        __syncthreads();   // orders the other warps' descriptor loads after warp 0's flag acquires
+        const int m = ctl[0], state = ctl[1];
+        if (state == LB_TIMEOUT) {
+            result = finish(acc, zero_inc);
+            break;
+        }
+        if (m > 4 * w) {
+            C t[4];
 #pragma unroll
-            for (int b = 0; b < SC_LB_BATCH; ++b)
-                if (i0 + b < m) t[b] = load_agg(p0 + dir * (done + i0 + b));
+            for (int i = 0; i < 4; ++i)
+                if (4 * w + i < m) t[i] = load_agg(p0 + dir * (done + 4 * w + i));
+            C part = ident;
 #pragma unroll
-            for (int b = 0; b < SC_LB_BATCH; ++b)
-                if (i0 + b < m) acc = extend(acc, t[b]);
+            for (int i = 0; i < 4; ++i)
+                if (4 * w + i < m) part = extend(part, t[i]);
+            bool cl;
+            seg_put(part, sx[w][lane], sy[w][lane], cl);
+            if (lane == 0) scl[w] = cl;
+        }
+        __syncthreads();
+        if (w == 0) {
+            for (int j = 0; j < SC_WARPS && 4 * j < m; ++j) {
+                C part;
+                seg_get(part, sx[j][lane], sy[j][lane], scl[j]);
+                acc = extend(acc, part);
+            }
+            if (state == LB_INC) result = finish(acc, load_inc(p0 + dir * (done + m)));
+            else if (state == LB_END) result = finish(acc, zero_inc);
         }
         done += m;
-        if (ji < jm && ji == m) return finish(acc, load_inc(p0 + dir * done));
-        if (done >= count) return finish(acc, zero_inc);   // not reached: the first chunk is always inclusive
-        if (m == 0) {
-            // the nearest predecessor has published nothing yet: wait for it
-            unsigned fw = 0;
-            if (lane == 0) fw = wait_flag(&flags[p0 + dir * done], status);
-            fw = __shfl_sync(0xffffffffu, fw, 0);
-            if (fw == 0) return finish(acc, zero_inc);
-        }
+        if (state == LB_INC || state == LB_END) break;
+        wait_first = state == LB_WAIT;
     }
-    record_timeout(status);
-    return finish(acc, zero_inc);
+    return result;
+}
+
+// ============================================================================ chunk staging
+// Up to three input arrays of a scan, each a TMA map over [B*T rows, N cols] fp32 with a
+// box of 128 channels x (rows of the chunk).
+struct ScanMaps {
+    CUtensorMap m[3];
+};
+
+__device__ __forceinline__ float *smem_1k(uint8_t *p) {
+    return reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Take the chunk ticket and set up the staging barrier (thread 0), then the CTA syncs.
+__device__ __forceinline__ unsigned chunk_ticket(const ScanWs &d, unsigned *s_ticket, uint64_t *bar, int *abort_flag) {
+    if (threadIdx.x == 0) {
+        *s_ticket = atomicAdd(d.ticket, 1u);
+        mbar_init(smem_u32(bar), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    return *s_ticket;
+}
+
+// Thread 0: load rows [y, y + rows_i) x channels [x, x + 128) of map i into dst_i
+// (n arrays), all counted on one barrier.  Rows past the array read as zero.
+__device__ __forceinline__ void stage_chunk(const ScanMaps &mp, int n, float *const *dst, const int *rows, int x,
+                                            int64_t y, uint64_t *bar) {
+    if (threadIdx.x != 0) return;
+    uint32_t bytes = 0;
+    for (int i = 0; i < n; ++i) bytes += uint32_t(rows[i]) * SC_SLICE * 4u;
+    mbar_arrive_expect_tx(smem_u32(bar), bytes);
+    for (int i = 0; i < n; ++i) tma_load_2d(smem_u32(dst[i]), &mp.m[i], x, int(y), smem_u32(bar));
+}
+
+// Row r of a staged array as this lane's float4.
+__device__ __forceinline__ float4 srow(const float *s, int r, int lane) {
+    return *reinterpret_cast<const float4 *>(s + r * SC_SLICE + lane * 4);
 }
 
 // ============================================================================ forward state scan
 // Composite of a token range: h_out = A h_in + H.  (A2,H2) after (A1,H1) = (A2 A1, A2 H1 + H2).
-struct float2x4 {
-    float4 x, y;
-};
-template <int L, int LB>
-__global__ void __launch_bounds__(256, 3) k_fwd_scan(const float *__restrict__ a, const float *__restrict__ u,
-                                                  float *__restrict__ h, int64_t T, int N, int nslices,
-                                                  int64_t nseq, int64_t nchunks, ScanWs d, unsigned *status) {
+// Staged: a and u, rows [c0, c0 + 8L).
+template <int L>
+__global__ void __launch_bounds__(256, (L <= 8 ? 3 : L <= 12 ? 2 : 1)) k_fwd_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ h,
+                                                  int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
+                                                  ScanWs d, unsigned *status) {
+    constexpr int TT = SC_WARPS * L;
+    extern __shared__ uint8_t sm_dyn[];
+    float *sa = smem_1k(sm_dyn), *su = sa + TT * SC_SLICE;
     __shared__ unsigned s_ticket;
+    __shared__ uint64_t s_bar;
+    __shared__ int s_abort;
     __shared__ float4 sA[SC_WARPS][32], sH[SC_WARPS][32], sC[32];
+    __shared__ bool s_cl[SC_WARPS];
+    __shared__ int s_ctl[2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) s_ticket = atomicAdd(d.ticket, 1u);
-    __syncthreads();
-    const int64_t tk = s_ticket, chunk = tk / nseq, seq = tk % nseq;
+    const int64_t tk = chunk_ticket(d, &s_ticket, &s_bar, &s_abort), chunk = tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
-    const int ch = int(seq % nslices) * SC_SLICE + lane * 4;
+    const int slice = int(seq % nslices), ch = slice * SC_SLICE + lane * 4;
     const bool act = ch < N;
-    const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
-    const int64_t base = b * T * N + ch;
+    const int64_t c0 = chunk * TT, t0 = c0 + w * L;
+    {
+        float *dst[2] = {sa, su};
+        const int rows[2] = {TT, TT};
+        stage_chunk(mp, 2, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+    }
+    mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
 
-    // pass 1: only the composite of this thread's L tokens is kept (folded LB rows at a
-    // time); the rows stay in L2 and are read again in pass 2, so few registers are
-    // live across the look-back and three CTAs fit per SM.
+    // pass 1: composite of this thread's L tokens
     float4 A = f4(1.f), H = f4(0.f);
-    for (int k0 = 0; k0 < L; k0 += LB) {
-        float4 av[LB], uv[LB];
 #pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            const bool ok = act && t < T;
-            av[k] = ok ? ld_l2keep4(a + base + t * N) : f4(1.f);
-            uv[k] = ok ? ld_l2keep4(u + base + t * N) : f4(0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            H = fma4(av[k], H, uv[k]);
-            A = A * av[k];
-        }
+    for (int k = 0; k < L; ++k) {
+        if (t0 + k >= T) break;
+        const float4 av = srow(sa, w * L + k, lane), uv = srow(su, w * L + k, lane);
+        H = fma4(av, H, uv);
+        A = A * av;
     }
     sA[w][lane] = A;
     sH[w][lane] = H;
     __syncthreads();
 
+    // this warp's prefix (warps before it) and, in warp 0, the chunk aggregate
+    float4 pA = f4(1.f), pH = f4(0.f);
+    for (int j = 0; j < w; ++j) {
+        pH = fma4(sA[j][lane], pH, sH[j][lane]);
+        pA = pA * sA[j][lane];
+    }
+    float4 cA = f4(1.f), cH = f4(0.f);
+    const int64_t di = seq * nchunks + chunk, fb = seq * nchunks;
     if (w == 0) {
-        float4 cA = f4(1.f), cH = f4(0.f);
 #pragma unroll
         for (int j = 0; j < SC_WARPS; ++j) {
             cH = fma4(sA[j][lane], cH, sH[j][lane]);
             cA = cA * sA[j][lane];
         }
-        const int64_t di = seq * nchunks + chunk;
-        float4 carry = f4(0.f);
-        if (chunk > 0) {
-            warp_publish(&d.agg0[di * 32 + lane], cA, &d.agg1[di * 32 + lane], cH, &d.flags[di], F_AGG, lane);
-            const int64_t fb = seq * nchunks;
-            // acc = composite of the chunks between the inclusive prefix found and this chunk
-            const float2x4 r = warp_lookback<float2x4>(
-                d.flags + fb, chunk - 1, -1, chunk, float2x4{f4(1.f), f4(0.f)},
-                [&](int64_t p) { return float2x4{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane])}; },
-                [&](int64_t p) { return float2x4{f4(0.f), ld_cg4(&d.inc1[(fb + p) * 32 + lane])}; },
-                [](const float2x4 &acc, const float2x4 &g) { return float2x4{acc.x * g.x, fma4(acc.x, g.y, acc.y)}; },
-                [](const float2x4 &acc, const float2x4 &inc) { return float2x4{f4(0.f), fma4(acc.x, inc.y, acc.y)}; },
-                float2x4{f4(0.f), f4(0.f)}, status, lane);
-            carry = r.y;
-        }
+        if (chunk > 0) warp_publish(&d.agg0[di * 32 + lane], cA, &d.agg1[di * 32 + lane], cH, &d.flags[di], F_AGG, lane);
+    }
+    __syncthreads();   // sA/sH now serve as look-back scratch
+    float4 carry = f4(0.f);
+    if (chunk > 0) {
+        // acc = composite of the chunks between the inclusive prefix found and this chunk
+        const float2x4 r = cta_lookback<float2x4>(
+            d.flags + fb, chunk - 1, -1, chunk, float2x4{f4(1.f), f4(0.f)},
+            [&](int64_t p) { return float2x4{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane])}; },
+            [&](int64_t p) { return float2x4{f4(0.f), ld_cg4(&d.inc1[(fb + p) * 32 + lane])}; },
+            [](const float2x4 &acc, const float2x4 &g) { return float2x4{acc.x * g.x, fma4(acc.x, g.y, acc.y)}; },
+            [](const float2x4 &acc, const float2x4 &inc) { return float2x4{f4(0.f), fma4(acc.x, inc.y, acc.y)}; },
+            float2x4{f4(0.f), f4(0.f)}, status, sA, sH, s_cl, s_ctl, w, lane);
+        carry = r.y;
+    }
+    if (w == 0) {
         warp_publish(nullptr, f4(0.f), &d.inc1[di * 32 + lane], fma4(cA, carry, cH), &d.flags[di], F_INC, lane);
         sC[lane] = carry;
     }
     __syncthreads();
 
-    float4 hc = sC[lane];
-    for (int j = 0; j < w; ++j) hc = fma4(sA[j][lane], hc, sH[j][lane]);
-    for (int k0 = 0; k0 < L; k0 += LB) {
-        float4 av[LB], uv[LB];
+    // pass 2: h from the carry into this warp's first token
+    float4 hc = fma4(pA, sC[lane], pH);
+    const int64_t base = b * T * N + ch;
 #pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            const bool ok = act && t < T;
-            av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
-            uv[k] = ok ? ld_stream4(u + base + t * N) : f4(0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            hc = fma4(av[k], hc, uv[k]);
-            const int64_t t = t0 + k0 + k;
-            if (act && t < T) st_stream4(h + base + t * N, hc);
-        }
+    for (int k = 0; k < L; ++k) {
+        const int64_t t = t0 + k;
+        if (t >= T) break;
+        hc = fma4(srow(sa, w * L + k, lane), hc, srow(su, w * L + k, lane));
+        if (act) st_stream4(h + base + t * N, hc);
     }
 }
 
@@ -218,76 +324,78 @@ __global__ void __launch_bounds__(256, 3) k_fwd_scan(const float *__restrict__ a
 // (a_m P, R + e_m a_m P); a block-start token resets it to (1, e_m).  Composite of a
 // range: (Pi, Sig, closed); Y after X = Y.closed ? Y : (X.Pi Y.Pi, X.Sig + X.Pi Y.Sig, X.closed).
 // Output R_m = Sig of the composite from the block start to m.
-struct FwdSeg {
-    float4 P, S;
-    bool cl;
-};
 __device__ __forceinline__ FwdSeg fseg_then(const FwdSeg &X, const FwdSeg &Y) {
     if (Y.cl) return Y;
     return FwdSeg{X.P * Y.P, fma4(X.P, Y.S, X.S), X.cl};
 }
 
-template <int L, int LB>
-__global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g, const float *__restrict__ c,
-                                                  const float *__restrict__ a, float *__restrict__ R, int64_t T,
-                                                  int N, int nslices, int64_t nseq, int64_t nchunks, int64_t W,
-                                                  ScanWs d, unsigned *status) {
+// Staged: g, c and a, rows [c0, c0 + 8L).
+template <int L>
+__global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_win_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ R,
+                                                  int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
+                                                  int64_t W, ScanWs d, unsigned *status) {
+    constexpr int TT = SC_WARPS * L;
+    extern __shared__ uint8_t sm_dyn[];
+    float *sg = smem_1k(sm_dyn), *sc = sg + TT * SC_SLICE, *sa = sc + TT * SC_SLICE;
     __shared__ unsigned s_ticket;
+    __shared__ uint64_t s_bar;
+    __shared__ int s_abort;
     __shared__ float4 sP[SC_WARPS][32], sS[SC_WARPS][32], sCP[32], sCS[32];
     __shared__ bool sCl[SC_WARPS];
+    __shared__ int s_ctl[2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) s_ticket = atomicAdd(d.ticket, 1u);
-    __syncthreads();
-    const int64_t tk = s_ticket, chunk = tk / nseq, seq = tk % nseq;
+    const int64_t tk = chunk_ticket(d, &s_ticket, &s_bar, &s_abort), chunk = tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
-    const int ch = int(seq % nslices) * SC_SLICE + lane * 4;
+    const int slice = int(seq % nslices), ch = slice * SC_SLICE + lane * 4;
     const bool act = ch < N;
-    const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
-    const int64_t base = b * T * N + ch;
+    const int64_t c0 = chunk * TT, t0 = c0 + w * L;
+    {
+        float *dst[3] = {sg, sc, sa};
+        const int rows[3] = {TT, TT, TT};
+        stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+    }
+    mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
 
     FwdSeg G{f4(1.f), f4(0.f), false};
-    for (int k0 = 0; k0 < L; k0 += LB) {
-        float4 av[LB], ev[LB];
 #pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            const bool ok = act && t < T;
-            av[k] = ok ? ld_l2keep4(a + base + t * N) : f4(1.f);
-            ev[k] = ok ? ld_l2keep4(g + base + t * N) * ld_l2keep4(c + base + t * N) : f4(0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            if (t >= T) break;
-            if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
-            else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
-        }
+    for (int k = 0; k < L; ++k) {
+        const int64_t t = t0 + k;
+        if (t >= T) break;
+        const int r = w * L + k;
+        const float4 ev = srow(sg, r, lane) * srow(sc, r, lane), av = srow(sa, r, lane);
+        if (t % W == 0) G = FwdSeg{f4(1.f), ev, true};
+        else G = FwdSeg{G.P * av, fma4(G.P * av, ev, G.S), G.cl};
     }
     sP[w][lane] = G.P;
     sS[w][lane] = G.S;
     if (lane == 0) sCl[w] = G.cl;
     __syncthreads();
 
+    // this warp's prefix (warps before it) and, in warp 0, the chunk aggregate
+    FwdSeg pre{f4(1.f), f4(0.f), false};
+    for (int j = 0; j < w; ++j) pre = fseg_then(pre, FwdSeg{sP[j][lane], sS[j][lane], sCl[j]});
+    FwdSeg agg{sP[0][lane], sS[0][lane], sCl[0]};
+    const int64_t di = seq * nchunks + chunk, fb = seq * nchunks;
     if (w == 0) {
-        FwdSeg agg{sP[0][lane], sS[0][lane], sCl[0]};
 #pragma unroll
         for (int j = 1; j < SC_WARPS; ++j) agg = fseg_then(agg, FwdSeg{sP[j][lane], sS[j][lane], sCl[j]});
-        const int64_t di = seq * nchunks + chunk;
         // A closed aggregate is already the inclusive composite: publish it before looking
         // back.  The look-back still runs, for the tokens before the chunk's first block start.
         if (agg.cl) warp_publish(&d.inc0[di * 32 + lane], agg.P, &d.inc1[di * 32 + lane], agg.S, &d.flags[di], F_INC, lane);
         else warp_publish(&d.agg0[di * 32 + lane], agg.P, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
-        FwdSeg carry{f4(1.f), f4(0.f), true};
-        if (chunk > 0) {
-            const int64_t fb = seq * nchunks;
-            carry = warp_lookback<FwdSeg>(
-                d.flags + fb, chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
-                [&](int64_t p) { return FwdSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
-                [&](int64_t p) { return FwdSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
-                [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
-                [](const FwdSeg &acc, const FwdSeg &inc) { return fseg_then(inc, acc); },
-                FwdSeg{f4(1.f), f4(0.f), true}, status, lane);
-        }
+    }
+    __syncthreads();   // sP/sS/sCl now serve as look-back scratch
+    FwdSeg carry{f4(1.f), f4(0.f), true};
+    if (chunk > 0) {
+        carry = cta_lookback<FwdSeg>(
+            d.flags + fb, chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
+            [&](int64_t p) { return FwdSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
+            [&](int64_t p) { return FwdSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
+            [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
+            [](const FwdSeg &acc, const FwdSeg &inc) { return fseg_then(inc, acc); },
+            FwdSeg{f4(1.f), f4(0.f), true}, status, sP, sS, sCl, s_ctl, w, lane);
+    }
+    if (w == 0) {
         if (!agg.cl) {
             const FwdSeg inc = fseg_then(carry, agg);
             warp_publish(&d.inc0[di * 32 + lane], inc.P, &d.inc1[di * 32 + lane], inc.S, &d.flags[di], F_INC, lane);
@@ -297,25 +405,17 @@ __global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g
     }
     __syncthreads();
 
-    G = FwdSeg{sCP[lane], sCS[lane], true};
-    for (int j = 0; j < w; ++j) G = fseg_then(G, FwdSeg{sP[j][lane], sS[j][lane], sCl[j]});
-    for (int k0 = 0; k0 < L; k0 += LB) {
-        float4 av[LB], ev[LB];
+    G = fseg_then(FwdSeg{sCP[lane], sCS[lane], true}, pre);
+    const int64_t base = b * T * N + ch;
 #pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            const bool ok = act && t < T;
-            av[k] = ok ? ld_stream4(a + base + t * N) : f4(1.f);
-            ev[k] = ok ? ld_stream4(g + base + t * N) * ld_stream4(c + base + t * N) : f4(0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            if (t >= T) break;
-            if (t % W == 0) G = FwdSeg{f4(1.f), ev[k], true};
-            else G = FwdSeg{G.P * av[k], fma4(G.P * av[k], ev[k], G.S), G.cl};
-            if (act) st_stream4(R + base + t * N, G.S);
-        }
+    for (int k = 0; k < L; ++k) {
+        const int64_t t = t0 + k;
+        if (t >= T) break;
+        const int r = w * L + k;
+        const float4 ev = srow(sg, r, lane) * srow(sc, r, lane), av = srow(sa, r, lane);
+        if (t % W == 0) G = FwdSeg{f4(1.f), ev, true};
+        else G = FwdSeg{G.P * av, fma4(G.P * av, ev, G.S), G.cl};
+        if (act) st_stream4(R + base + t * N, G.S);
     }
 }
 
@@ -324,81 +424,104 @@ __global__ void __launch_bounds__(256, 3) k_win_scan(const float *__restrict__ g
 // and e_i = g_i c_i.  The composite of tokens i..j is x -> Q x + S.  A block-end token
 // (i+1 multiple of W, or i = T-1) closes the composite: tokens after it do not reach i.
 // Y after X (X earlier tokens) = X.closed ? X : (X.Q Y.Q, X.Q Y.S + X.S, Y.closed).
-struct RevSeg {
-    float4 Q, S;
-    bool cl;
-};
 __device__ __forceinline__ RevSeg rseg_then(const RevSeg &X, const RevSeg &Y) {
     if (X.cl) return X;
     return RevSeg{X.Q * Y.Q, fma4(X.Q, Y.S, X.S), Y.cl};
 }
 
-template <int L, int LB, bool TRUNC, typename TD>
-__global__ void __launch_bounds__(256, 3) k_bwd_scan(const float *__restrict__ g, const float *__restrict__ c,
-                                                  const float *__restrict__ a, const float *__restrict__ h,
+// Staged: g and c, rows [c0, c0 + 8L), and a, rows [c0, c0 + 8L] (one more: b of the
+// chunk's last token).  h (and R) are read from global memory, their loads issued
+// before the staging wait.  D_c and E are written right after pass 1, before the
+// look-back; D_u and D_a in pass 2.
+template <int L, bool TRUNC, typename TD>
+__global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
                                                   const float *__restrict__ R, TD *__restrict__ Da,
                                                   TD *__restrict__ Du, TD *__restrict__ Dc, TD *__restrict__ E,
                                                   int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
                                                   int64_t W, ScanWs d, unsigned *status) {
+    constexpr int TT = SC_WARPS * L;
+    extern __shared__ uint8_t sm_dyn[];
+    float *sg = smem_1k(sm_dyn), *sc = sg + TT * SC_SLICE, *sa = sc + TT * SC_SLICE;
     __shared__ unsigned s_ticket;
+    __shared__ uint64_t s_bar;
+    __shared__ int s_abort;
     __shared__ float4 sQ[SC_WARPS][32], sS[SC_WARPS][32], sCQ[32], sCS[32];
     __shared__ bool sCl[SC_WARPS];
+    __shared__ int s_ctl[2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) s_ticket = atomicAdd(d.ticket, 1u);
-    __syncthreads();
-    const int64_t tk = s_ticket, chunk = nchunks - 1 - tk / nseq, seq = tk % nseq;
+    const int64_t tk = chunk_ticket(d, &s_ticket, &s_bar, &s_abort), chunk = nchunks - 1 - tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
-    const int ch = int(seq % nslices) * SC_SLICE + lane * 4;
+    const int slice = int(seq % nslices), ch = slice * SC_SLICE + lane * 4;
     const bool act = ch < N;
-    const int64_t t0 = chunk * (SC_WARPS * L) + w * L;
+    const int64_t c0 = chunk * TT, t0 = c0 + w * L;
     const int64_t base = b * T * N + ch;
+    {
+        float *dst[3] = {sg, sc, sa};
+        const int rows[3] = {TT, TT, TT + 1};
+        stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+    }
+    // h_{t-1} and h_t of this thread's tokens, from global
+    float4 hv[L + 1];
+    hv[0] = (act && t0 > 0 && t0 - 1 < T) ? ld_keep4(h + base + (t0 - 1) * N) : f4(0.f);
+#pragma unroll
+    for (int k = 0; k < L; ++k) hv[k + 1] = (act && t0 + k < T) ? ld_keep4(h + base + (t0 + k) * N) : f4(0.f);
+    mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
 
     // pass 1: composite of this thread's tokens from e_i = g_i c_i and b_i = a_{i+1}
-    // (0 past the last token); the rows stay in L2 for pass 2.
     RevSeg G{f4(1.f), f4(0.f), false};
-    for (int k0 = L - LB; k0 >= 0; k0 -= LB) {
-        float4 ev[LB], bv[LB];
 #pragma unroll
-        for (int k = 0; k < LB; ++k) {
-            const int64_t t = t0 + k0 + k;
-            const bool ok = act && t < T;
-            ev[k] = ok ? ld_l2keep4(g + base + t * N) * ld_l2keep4(c + base + t * N) : f4(0.f);
-            bv[k] = (act && t + 1 < T) ? ld_l2keep4(a + base + (t + 1) * N) : f4(0.f);
-        }
-#pragma unroll
-        for (int k = LB - 1; k >= 0; --k) {
-            const int64_t t = t0 + k0 + k;
-            if (t >= T) continue;
-            const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
-            if (end) G = RevSeg{bv[k], ev[k], true};
-            else G = RevSeg{bv[k] * G.Q, fma4(bv[k], G.S, ev[k]), G.cl};
-        }
+    for (int k = L - 1; k >= 0; --k) {
+        const int64_t t = t0 + k;
+        if (t >= T) continue;
+        const int r = w * L + k;
+        const float4 ev = srow(sg, r, lane) * srow(sc, r, lane);
+        const float4 bv = t + 1 < T ? srow(sa, r + 1, lane) : f4(0.f);
+        const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
+        if (end) G = RevSeg{bv, ev, true};
+        else G = RevSeg{bv * G.Q, fma4(bv, G.S, ev), G.cl};
     }
     sQ[w][lane] = G.Q;
     sS[w][lane] = G.S;
     if (lane == 0) sCl[w] = G.cl;
+    // D_c = g h and E = c h need no carry: store them now, so these writes overlap the
+    // look-back
+    if (act) {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            if (t >= T) break;
+            const int r = w * L + k;
+            st4(Dc + base + t * N, srow(sg, r, lane) * hv[k + 1]);
+            st4(E + base + t * N, srow(sc, r, lane) * hv[k + 1]);
+        }
+    }
     __syncthreads();
 
+    // composite of the warps after this one and, in warp 0, the chunk aggregate
+    RevSeg post{f4(1.f), f4(0.f), false};
+    for (int j = w + 1; j < SC_WARPS; ++j) post = rseg_then(post, RevSeg{sQ[j][lane], sS[j][lane], sCl[j]});
+    RevSeg agg{sQ[0][lane], sS[0][lane], sCl[0]};
+    const int64_t di = seq * nchunks + chunk, fb = seq * nchunks;
     if (w == 0) {
-        RevSeg agg{sQ[0][lane], sS[0][lane], sCl[0]};
 #pragma unroll
         for (int j = 1; j < SC_WARPS; ++j) agg = rseg_then(agg, RevSeg{sQ[j][lane], sS[j][lane], sCl[j]});
-        const int64_t di = seq * nchunks + chunk;
         // A closed aggregate is already the inclusive composite: publish it before looking
         // back.  The look-back still runs, for the tokens after the chunk's last block end.
         if (agg.cl) warp_publish(&d.inc0[di * 32 + lane], agg.Q, &d.inc1[di * 32 + lane], agg.S, &d.flags[di], F_INC, lane);
         else warp_publish(&d.agg0[di * 32 + lane], agg.Q, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
-        RevSeg carry{f4(0.f), f4(0.f), true};
-        if (chunk + 1 < nchunks) {
-            const int64_t fb = seq * nchunks;
-            carry = warp_lookback<RevSeg>(
-                d.flags + fb, chunk + 1, 1, nchunks - 1 - chunk, RevSeg{f4(1.f), f4(0.f), false},
-                [&](int64_t p) { return RevSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
-                [&](int64_t p) { return RevSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
-                [](const RevSeg &acc, const RevSeg &g) { return rseg_then(acc, g); },
-                [](const RevSeg &acc, const RevSeg &inc) { return rseg_then(acc, inc); },
-                RevSeg{f4(0.f), f4(0.f), true}, status, lane);
-        }
+    }
+    __syncthreads();   // sQ/sS/sCl now serve as look-back scratch
+    RevSeg carry{f4(0.f), f4(0.f), true};
+    if (chunk + 1 < nchunks) {
+        carry = cta_lookback<RevSeg>(
+            d.flags + fb, chunk + 1, 1, nchunks - 1 - chunk, RevSeg{f4(1.f), f4(0.f), false},
+            [&](int64_t p) { return RevSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
+            [&](int64_t p) { return RevSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
+            [](const RevSeg &acc, const RevSeg &g) { return rseg_then(acc, g); },
+            [](const RevSeg &acc, const RevSeg &inc) { return rseg_then(acc, inc); },
+            RevSeg{f4(0.f), f4(0.f), true}, status, sQ, sS, sCl, s_ctl, w, lane);
+    }
+    if (w == 0) {
         if (!agg.cl) {
             const RevSeg inc = rseg_then(agg, carry);
             warp_publish(&d.inc0[di * 32 + lane], inc.Q, &d.inc1[di * 32 + lane], inc.S, &d.flags[di], F_INC, lane);
@@ -409,79 +532,115 @@ __global__ void __launch_bounds__(256, 3) k_bwd_scan(const float *__restrict__ g
     __syncthreads();
 
     // composite of everything after this warp's tokens, then pass 2 backwards
-    G = RevSeg{sCQ[lane], sCS[lane], true};
-    for (int j = SC_WARPS - 1; j > w; --j) G = rseg_then(RevSeg{sQ[j][lane], sS[j][lane], sCl[j]}, G);
-    // rows: a at t0..t0+L, h at t0-1..t0+L-1, g and c at t0..t0+L-1
-    float4 anext = (act && t0 + L < T) ? ld_keep4(a + base + (t0 + L) * N) : f4(0.f);
+    G = rseg_then(post, RevSeg{sCQ[lane], sCS[lane], true});
+    // R at the end of each token's window (truncated mode)
+    float4 rv[TRUNC ? L : 1];
+    if (TRUNC) {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            rv[k] = f4(0.f);
+            if (act && t < T && t % W != 0 && (t / W + 1) * W < T) {
+                const int64_t m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
+                rv[k] = ld_keep4(R + base + m * N);
+            }
+        }
+    }
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
         const int64_t t = t0 + k;
         if (t >= T) continue;
-        const float4 gk = act ? ld_stream4(g + base + t * N) : f4(0.f);
-        const float4 ck = act ? ld_stream4(c + base + t * N) : f4(0.f);
-        const float4 ak = act ? ld_keep4(a + base + t * N) : f4(0.f);
-        const float4 hk = act ? ld_keep4(h + base + t * N) : f4(0.f);
-        const float4 hp = (act && t > 0) ? ld_keep4(h + base + (t - 1) * N) : f4(0.f);
-        const float4 bk = t + 1 < T ? anext : f4(0.f);
-        const float4 ek = gk * ck;
+        const int r = w * L + k;
+        const float4 ak = srow(sa, r, lane);
+        const float4 bk = t + 1 < T ? srow(sa, r + 1, lane) : f4(0.f);
+        const float4 ek = srow(sg, r, lane) * srow(sc, r, lane);
         const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
         if (end) G = RevSeg{bk, ek, true};
         else G = RevSeg{bk * G.Q, fma4(bk, G.S, ek), true};
         float4 mu = G.S;
-        if (TRUNC && act && t % W != 0 && (t / W + 1) * W < T) {
-            const int64_t m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
-            mu = fma4(G.Q, ld_stream4(R + base + m * N), G.S);
-        }
+        if (TRUNC && t % W != 0 && (t / W + 1) * W < T) mu = fma4(G.Q, rv[k], G.S);
         if (act) {
-            st4(Dc + base + t * N, gk * hk);
-            st4(E + base + t * N, ck * hk);
             st4(Du + base + t * N, mu);
-            st4(Da + base + t * N, mu * hp * ak * (f4(1.f) - ak));
+            st4(Da + base + t * N, mu * hv[k] * ak * (f4(1.f) - ak));
         }
-        anext = ak;
     }
 }
 
 // ============================================================================ launchers
+// Maps of the staged arrays ([B*T rows, N cols] fp32, boxes of 128 channels x rows[i]).
+static bool scan_maps(ScanMaps &mp, int n, const float *const *arr, const int *rows, int64_t B, int64_t T, int N) {
+    memset(&mp, 0, sizeof(mp));
+    for (int i = 0; i < n; ++i)
+        if (!tmap_rows_f32(&mp.m[i], arr[i], uint64_t(N), uint64_t(B * T), uint64_t(N) * 4, SC_SLICE, uint32_t(rows[i])))
+            return false;
+    return true;
+}
+static size_t staged_bytes(int total_rows) { return size_t(total_rows) * SC_SLICE * 4 + 1024; }
+
+template <class K>
+static cudaError_t set_smem(K kern, size_t smem) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+}
+
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
                             void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 16, LB = 8;
+    constexpr int L = SC_FWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
-    const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
+    const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
+    ScanMaps mp;
+    const float *arr[2] = {a, u};
+    const int rows[2] = {TT, TT};
+    if (!scan_maps(mp, 2, arr, rows, B, T, N)) return cudaErrorInvalidValue;
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
     cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
     if (e != cudaSuccess) return e;
-    k_fwd_scan<L, LB><<<unsigned(nseq * nchunks), 256, 0, st>>>(a, u, h, T, N, nslices, nseq, nchunks, d, status);
+    const size_t smem = staged_bytes(2 * TT);
+    if ((e = set_smem(k_fwd_scan<L>, smem)) != cudaSuccess) return e;
+    k_fwd_scan<L><<<unsigned(nseq * nchunks), 256, smem, st>>>(mp, h, T, N, nslices, nseq, nchunks, d, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t W, void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 16, LB = 4;
+    constexpr int L = SC_BWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
-    const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
+    const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
+    ScanMaps mp;
+    const float *arr[3] = {g, c, a};
+    const int rows[3] = {TT, TT, TT};
+    if (!scan_maps(mp, 3, arr, rows, B, T, N)) return cudaErrorInvalidValue;
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
     cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
     if (e != cudaSuccess) return e;
-    k_win_scan<L, LB><<<unsigned(nseq * nchunks), 256, 0, st>>>(g, c, a, R, T, N, nslices, nseq, nchunks, W, d, status);
+    const size_t smem = staged_bytes(3 * TT);
+    if ((e = set_smem(k_win_scan<L>, smem)) != cudaSuccess) return e;
+    k_win_scan<L><<<unsigned(nseq * nchunks), 256, smem, st>>>(mp, R, T, N, nslices, nseq, nchunks, W, d, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, const float *h, const float *R,
                             void *D_a, void *D_u, void *D_c, void *E, bool d_bf16, int64_t B, int64_t T, int N,
                             int64_t W, void *scan_ws, unsigned *status, cudaStream_t st) {
-    constexpr int L = 16, LB = 4;
+    constexpr int L = SC_BWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
-    const int64_t nseq = B * nslices, nchunks = cdiv(T, SC_WARPS * L);
+    const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
+    ScanMaps mp;
+    const float *arr[3] = {g, c, a};
+    const int rows[3] = {TT, TT, TT + 1};
+    if (!scan_maps(mp, 3, arr, rows, B, T, N)) return cudaErrorInvalidValue;
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
     cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
     if (e != cudaSuccess) return e;
     const bool trunc = W > 0 && W < T;
     const unsigned grid = unsigned(nseq * nchunks);
-#define ADJ_BWD(TR, TD)                                                                                      \
-    k_bwd_scan<L, LB, TR, TD><<<grid, 256, 0, st>>>(g, c, a, h, R, static_cast<TD *>(D_a), static_cast<TD *>(D_u), \
-                                                static_cast<TD *>(D_c), static_cast<TD *>(E), T, N, nslices,   \
-                                                nseq, nchunks, trunc ? W : T, d, status)
+    const size_t smem = staged_bytes(3 * TT + 1);
+#define ADJ_BWD(TR, TDT)                                                                                          \
+    do {                                                                                                          \
+        if ((e = set_smem(k_bwd_scan<L, TR, TDT>, smem)) != cudaSuccess) return e;                                \
+        k_bwd_scan<L, TR, TDT><<<grid, 256, smem, st>>>(mp, h, R, static_cast<TDT *>(D_a), static_cast<TDT *>(D_u), \
+                                                        static_cast<TDT *>(D_c), static_cast<TDT *>(E), T, N, nslices,  \
+                                                        nseq, nchunks, trunc ? W : T, d, status);                 \
+    } while (0)
     if (d_bf16) {
         if (trunc) ADJ_BWD(true, __nv_bfloat16);
         else ADJ_BWD(false, __nv_bfloat16);
