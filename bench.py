@@ -158,15 +158,16 @@ def roofline_of(name, ent, peaks, split3):
     against both the bandwidth and the tensor peak of their arithmetic (the fp32-accurate
     three-term bf16 split issues 3 bf16 MMAs per product, so its tensor peak is 1/3 of
     bf16's), reporting the bound they sit closer to."""
-    hbm = {"kernel": name, "bound": "hbm", "achieved": ent["achieved_gbs"], "peak": peaks["hbm_gbs"],
-           "unit": "GB/s", "frac": ent["achieved_gbs"] / peaks["hbm_gbs"], "traffic": None}
+    gbs = ent.get("achieved_gbs")
+    hbm = {"kernel": name, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+           "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"] if gbs is not None else None, "traffic": None}
     if "achieved_tflops" not in ent:
         return hbm
     tpk = peaks["bf16_tflops"] / (3.0 if split3 else 1.0)
     ten = {"kernel": name, "bound": "tensor", "achieved": ent["achieved_tflops"], "peak": tpk, "unit": "TFLOP/s",
            "frac": ent["achieved_tflops"] / tpk, "traffic": None,
            "note": "fp32-accurate 3-term bf16 split: peak = bf16 peak / 3" if split3 else "bf16"}
-    return ten if ten["frac"] >= hbm["frac"] else hbm
+    return ten if hbm["frac"] is None or ten["frac"] >= hbm["frac"] else hbm
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
@@ -392,7 +393,8 @@ def run_ours(args, rank, world, local_rank):
 
     kf = kernels_summary(prof_full, table)
     kt = kernels_summary(prof_trunc, tableT)
-    dom = next(iter(kf))
+    # the dominant kernel among those with an algorithmic byte count
+    dom = next((n for n, e in kf.items() if "achieved_gbs" in e), next(iter(kf)))
     roof = roofline_of(dom, kf[dom], peaks, split3=True)
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
     for name, ent in kf.items():
