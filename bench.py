@@ -153,6 +153,31 @@ def kernel_table(P, N, xb, db, trunc):
     }
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel, from
+# the committed ncu summary of the bench workload (profiles/), with the code state it
+# was captured at; None when no summary covers the kernel.
+PROFILE_OF = {"bwd_scan": "k_bwd_scan_ssm1_p128.md", "fwd_scan": "k_fwd_scan_ssm1_p128.md",
+              "proj_in": "k_gemm_tc_proj_in_ssm1_p128.md", "proj_out": "k_gemm_tc_proj_out_ssm1_p128.md",
+              "param_dW_in": "k_gemm_tc_param_dWin_ssm1_p128.md"}
+
+
+def profiled_traffic(name):
+    fn = PROFILE_OF.get(name)
+    path = os.path.join(ROOT, "profiles", fn) if fn else None
+    if not path or not os.path.exists(path):
+        return None, None
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    tot, state = 0.0, None
+    for line in open(path):
+        for key in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            if line.startswith("| " + key + " |"):
+                val, unit = line.split("|")[2].split()
+                tot += float(val) * scale[unit]
+        if line.startswith("Code state:"):
+            state = line.split(":", 1)[1].split("(")[0].strip().rstrip(".")
+    return (tot if tot > 0 else None), state
+
+
 def roofline_of(name, ent, peaks, split3):
     """Roofline entry of one kernel: HBM-bound kernels against the copy bandwidth; GEMMs
     against both the bandwidth and the tensor peak of their arithmetic (the fp32-accurate
@@ -396,6 +421,10 @@ def run_ours(args, rank, world, local_rank):
     # the dominant kernel among those with an algorithmic byte count
     dom = next((n for n, e in kf.items() if "achieved_gbs" in e), next(iter(kf)))
     roof = roofline_of(dom, kf[dom], peaks, split3=True)
+    roof["traffic"], state = profiled_traffic(dom)
+    if roof["traffic"] is not None:
+        roof["traffic_unit"] = "bytes per launch"
+        roof["traffic_source"] = f"ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/{PROFILE_OF[dom]} ({state})"
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
     for name, ent in kf.items():
         if "achieved_gbs" in ent:
