@@ -513,7 +513,10 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
     }
 }
 
-template <bool ABF, bool BBF, bool SPLIT>
+// REGS: whether register staging may be needed (any operand with LD_REG, or a resident B
+// not loaded by TMA).  Without it the kernel carries no staging code, which keeps the
+// producers' hot loop free of register spills; ABF/BBF only matter with REGS.
+template <bool ABF, bool BBF, bool SPLIT, bool REGS>
 __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_constant__ TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -583,7 +586,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         // ---------------- producers
         const int ptid = tid - TC_EPI_WARPS * 32;
         bool ok = true;
-        if (args.b_res && !ld_tma(args.b_ld)) {
+        if constexpr (REGS) if (args.b_res && !ld_tma(args.b_ld)) {
             // the n tile is the same for every tile of this CTA
             int64_t m0, n0, kb0, ke;
             int z;
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 uint8_t *st = stages + size_t(s) * Lo.stage_bytes;
                 uint8_t *sa = st, *sbb = st + Lo.a_reg;
                 const int64_t k0 = kb0 + kb * TC_BK;
-                if (a_reg || b_reg) {
+                if constexpr (REGS) if (a_reg || b_reg) {
                     // register-staged tiles overwrite the stage: wait until the MMAs released it
                     bool got = r == 0 || mbar_wait(smem_u32(&empty[s]), uint32_t((r - 1) & 1), abort, args.status);
                     // with raw tiles the producers meet at named barriers, so they decide together
@@ -984,9 +987,9 @@ static int tma_build(CUtensorMap *maps, CUtensorMap *lo_maps, CUtensorMap *mul_m
     return mode;
 }
 
-template <bool ABF, bool BBF, bool SPLIT>
+template <bool ABF, bool BBF, bool SPLIT, bool REGS = true>
 static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st) {
-    auto kern = k_gemm_tc<ABF, BBF, SPLIT>;
+    auto kern = k_gemm_tc<ABF, BBF, SPLIT, REGS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, TC_THREADS_P, smem, st>>>(a);
@@ -1064,6 +1067,11 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;
     if (grid < a.n_tiles) grid = a.n_tiles;
     if (grid > ntiles) grid = ntiles;
+    const bool need_regs = a.a_ld == LD_REG || (!a.b_res && a.b_ld == LD_REG) || (a.b_res && !ld_tma(a.b_ld));
+    if (!need_regs) {
+        if (split3) return launch_tc_t<false, false, true, false>(a, unsigned(grid), smem, st);
+        return launch_tc_t<false, false, false, false>(a, unsigned(grid), smem, st);
+    }
     if (split3) {
         if (A.bf16 && Bm.bf16) return launch_tc_t<true, true, true>(a, unsigned(grid), smem, st);
         if (A.bf16) return launch_tc_t<true, false, true>(a, unsigned(grid), smem, st);
