@@ -77,12 +77,15 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
     const bool wsplit = d->x_dtype == ADJ_F32;
     const size_t win_s = wsplit ? al256(size_t(d->P) * 3 * d->N * 4) : 0;
     const size_t wo_s = wsplit ? al256(size_t(d->N) * d->P * 4) : 0;
+    // the forward's W_in copy (interleaved columns; hi/lo for fp32 weights) is made for bf16
+    // weights too
+    const size_t win_f = al256(size_t(d->P) * 3 * d->N * (wsplit ? 4 : 2));
     size_t off = WS_HEADER;
     switch (op) {
     case ADJ_OP_FWD:            // u
         L.buf0 = off; off += btn;
         L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
-        L.wsplit = off; off += win_s + wo_s;
+        L.wsplit = off; off += win_f + wo_s;
         break;
     case ADJ_OP_BWD_FULL:       // g
         L.buf0 = off; off += btn;
@@ -233,8 +236,20 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
     GemmEpilogue e = epi(Epi::ProjIn);
     e.out0 = a; e.out1 = u; e.out2 = c; e.bias = w->b_a; e.N = N;
     cudaError_t err = cudaSuccess;
-    const GemmOperand Win = opw(w->W_in, int64_t(P) * 3 * N, xbf, at(ws, L.wsplit), 1, 3 * int64_t(N), st, &err);
-    ADJ_CUDA(err);
+    GemmOperand Win;
+    if (N % 32 == 0) {
+        // interleave the a, u, c column chunks so every output tile carries a share of the
+        // sigmoid (the epilogue maps the chunks back)
+        __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(at(ws, L.wsplit));
+        __nv_bfloat16 *lo = xbf ? nullptr : hi + int64_t(P) * 3 * N;
+        ADJ_CUDA(launch_prep_win(w->W_in, xbf, P, N, hi, lo, st));
+        Win = op1(hi, 1, 3 * int64_t(N), true);
+        if (lo) Win.lo[0] = Win.lo[1] = Win.lo[2] = lo;
+        e.interleave = true;
+    } else {
+        Win = opw(w->W_in, int64_t(P) * 3 * N, xbf, at(ws, L.wsplit), 1, 3 * int64_t(N), st, &err);
+        ADJ_CUDA(err);
+    }
     {
         ProfScope ps(K_PROJ_IN, st);
         ADJ_CUDA(launch_gemm_tc(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), Win, e, 1, !xbf, status_word(ws), st));
@@ -250,8 +265,8 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
         e2.out0 = y; e2.out_x = y_x; e2.ld = P;
         e2.add = xres ? static_cast<const void *>(xres) : xhat;
         e2.add_bf16 = !xres && xbf;
-        const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, xbf, at(ws, L.wsplit + al256(size_t(P) * 3 * N * 4)), 1, P, st,
-                                   &err);
+        const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, xbf, at(ws, L.wsplit + al256(size_t(P) * 3 * N * (xbf ? 2 : 4))),
+                                   1, P, st, &err);
         ADJ_CUDA(err);
         ProfScope ps(K_PROJ_OUT, st);
         ADJ_CUDA(launch_gemm_tc(BT, P, N, op1(c, N, 1, false, h), Wo, e2, 1, !xbf, status_word(ws), st));

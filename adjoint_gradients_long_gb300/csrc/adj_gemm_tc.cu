@@ -467,7 +467,8 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
     const int rows = M - m0r < 32 ? int(M - m0r) : 32;
     switch (ep.kind) {
     case Epi::ProjIn: {
-        const int blk = n / ep.N, j = n - blk * ep.N;
+        int blk, j;
+        projin_col(ep, n, blk, j);
         float *out = (blk == 0 ? ep.out0 : blk == 1 ? ep.out1 : ep.out2) + m0r * ep.N + j;
         const float4 bias = blk == 0 ? *reinterpret_cast<const float4 *>(ep.bias + j) : f4(0.f);
         for (int i = lane >> 3; i < rows; i += 4) {
@@ -816,11 +817,13 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
                 if (via_tma) {
-                    if (ep.kind == Epi::ProjIn && n < ep.N) {
+                    int pblk = 0, pch = 0;   // ProjIn: block and first channel of the chunk
+                    if (ep.kind == Epi::ProjIn) projin_col(ep, n, pblk, pch);
+                    if (ep.kind == Epi::ProjIn && pblk == 0) {
                         // a = sigmoid(z + b_a) (the chunk lies within one block: N % 32 == 0)
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
-                            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(ep.bias + n + j));
+                            const float4 b4 = __ldg(reinterpret_cast<const float4 *>(ep.bias + pch + j));
                             v[j] = sigmoidf_fast(v[j] + b4.x);
                             v[j + 1] = sigmoidf_fast(v[j + 1] + b4.y);
                             v[j + 2] = sigmoidf_fast(v[j + 2] + b4.z);
@@ -848,8 +851,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         if (ep.kind == Epi::Partial) {
                             tma_store_3d(&args.tmO[0], n, int(m0r), z, sb_s);
                         } else if (ep.kind == Epi::ProjIn) {
-                            const int blk = n / ep.N;
-                            tma_store_2d(&args.tmO[blk], n - blk * ep.N, int(m0r), sb_s);
+                            tma_store_2d(&args.tmO[pblk], pch, int(m0r), sb_s);
                         } else {
                             tma_store_2d(&args.tmO[0], n, int(m0r), sb_s);
                         }

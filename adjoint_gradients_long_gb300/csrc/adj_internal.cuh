@@ -119,7 +119,21 @@ struct GemmEpilogue {
     const float *bias;          // ProjIn: b_a [N]
     int64_t ld;                 // row stride of out0/add/out_x
     int N;                      // ProjIn: width of each block
+    bool interleave;            // ProjIn: product column chunk j (32 columns) is block j % 3,
+                                // channels 32 (j / 3) ...; needs N % 32 == 0 (see prep_win)
 };
+
+// ProjIn output column n of the product -> block (0 a, 1 u, 2 c) and channel.
+__host__ __device__ inline void projin_col(const GemmEpilogue &ep, int n, int &blk, int &ch) {
+    if (ep.interleave) {
+        const int j = n >> 5;
+        blk = j % 3;
+        ch = (j / 3) * 32 + (n & 31);
+    } else {
+        blk = n / ep.N;
+        ch = n - blk * ep.N;
+    }
+}
 
 // tcgen05 GEMM C[M,Nc] = A[M,K] B[K,Nc] with the operand and epilogue contracts above;
 // split3: fp32-accurate hi/lo bf16 split, otherwise bf16 operands.
@@ -127,6 +141,11 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
                            const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
                            int *splits_used = nullptr);
 
+// W_in [P, 3N] with its columns interleaved in 32-column chunks (chunk j of the copy =
+// columns 32 (j / 3) ... of block j % 3, so every wide output tile mixes the a, u and c
+// blocks): fp32 weights -> bf16 hi and lo copies, bf16 weights -> a bf16 copy (lo null).
+cudaError_t launch_prep_win(const void *w, bool w_bf16, int P, int N, __nv_bfloat16 *hi, __nv_bfloat16 *lo,
+                            cudaStream_t st);
 // hi = bf16(w), lo = bf16(w - hi) for n fp32 values (operands of the split-precision GEMM)
 cudaError_t launch_split_bf16(const float *w, int64_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo, cudaStream_t st);
 cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out,

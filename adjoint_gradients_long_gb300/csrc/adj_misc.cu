@@ -179,6 +179,33 @@ __global__ void __launch_bounds__(256) k_split_bf16(const float *__restrict__ w,
     }
 }
 
+__global__ void __launch_bounds__(256) k_prep_win(const void *__restrict__ w, bool w_bf16, int P, int N,
+                                                  __nv_bfloat16 *__restrict__ hi, __nv_bfloat16 *__restrict__ lo) {
+    const int64_t n3 = 3 * int64_t(N), total = int64_t(P) * n3;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t p = i / n3;
+        const int c = int(i - p * n3), j = c >> 5;
+        const int64_t src = p * n3 + int64_t(j % 3) * N + (j / 3) * 32 + (c & 31);
+        if (w_bf16) {
+            hi[i] = static_cast<const __nv_bfloat16 *>(w)[src];
+        } else {
+            const float x = static_cast<const float *>(w)[src];
+            const __nv_bfloat16 h = __float2bfloat16_rn(x);
+            hi[i] = h;
+            lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+        }
+    }
+}
+
+cudaError_t launch_prep_win(const void *w, bool w_bf16, int P, int N, __nv_bfloat16 *hi, __nv_bfloat16 *lo,
+                            cudaStream_t st) {
+    int64_t blocks = (int64_t(P) * 3 * N + 255) / 256;
+    if (blocks > 1024) blocks = 1024;
+    if (blocks < 1) return cudaSuccess;
+    k_prep_win<<<unsigned(blocks), 256, 0, st>>>(w, w_bf16, P, N, hi, lo);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_split_bf16(const float *w, int64_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo, cudaStream_t st) {
     int64_t blocks = (n + 255) / 256;
     if (blocks > 1024) blocks = 1024;
