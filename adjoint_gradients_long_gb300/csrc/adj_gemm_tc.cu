@@ -380,50 +380,50 @@ __device__ __forceinline__ void put4(uint8_t *hi, uint8_t *lo, int r, int k4, fl
     }
 }
 
-template <bool SPLIT, bool MN, bool MUL = false>
+template <bool SPLIT, bool MN, bool MUL = false, int NP = TC_PROD>
 __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
     constexpr int R = TC_BM;
     const float *raw = reinterpret_cast<const float *>(region);
     if (!MN) {
-        constexpr int ITEMS = R * 16, PER = (ITEMS + TC_PROD - 1) / TC_PROD;   // float4 (4 k of one row)
+        constexpr int ITEMS = R * 16, PER = (ITEMS + NP - 1) / NP;   // float4 (4 k of one row)
         float4 v[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int q = ptid + i * TC_PROD;
-            if (ITEMS % TC_PROD == 0 || q < ITEMS) v[i] = reinterpret_cast<const float4 *>(raw)[q];
+            const int q = ptid + i * NP;
+            if (ITEMS % NP == 0 || q < ITEMS) v[i] = reinterpret_cast<const float4 *>(raw)[q];
         }
         if (MUL) {
             // the factor tile (same layout) follows the operand tile
             const float4 *mraw = reinterpret_cast<const float4 *>(region + R * 256);
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
-                const int q = ptid + i * TC_PROD;
-                if (ITEMS % TC_PROD == 0 || q < ITEMS) v[i] = v[i] * mraw[q];
+                const int q = ptid + i * NP;
+                if (ITEMS % NP == 0 || q < ITEMS) v[i] = v[i] * mraw[q];
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(NP) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int q = ptid + i * TC_PROD;    // float4 index: row q/16, k4 q%16
-            if (ITEMS % TC_PROD == 0 || q < ITEMS) put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
+            const int q = ptid + i * NP;    // float4 index: row q/16, k4 q%16
+            if (ITEMS % NP == 0 || q < ITEMS) put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
         }
     } else {
-        constexpr int ITEMS = R * 8, PER = (ITEMS + TC_PROD - 1) / TC_PROD;    // items (one row, 8 k)
+        constexpr int ITEMS = R * 8, PER = (ITEMS + NP - 1) / NP;    // items (one row, 8 k)
         float v[PER][8];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int it = ptid + i * TC_PROD, r = it % R, kc = it / R;
+            const int it = ptid + i * NP, r = it % R, kc = it / R;
             const float *src = raw + (r >> 6) * 4096 + (r & 63);
-            if (ITEMS % TC_PROD == 0 || it < ITEMS) {
+            if (ITEMS % NP == 0 || it < ITEMS) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(TC_PROD) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(NP) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int it = ptid + i * TC_PROD;
-            if (ITEMS % TC_PROD == 0 || it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
+            const int it = ptid + i * NP;
+            if (ITEMS % NP == 0 || it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
         }
     }
 }
@@ -649,7 +649,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 mbar_arrive(smem_u32(&full[s]));
             }
         }
-    } else if (warp == TC_TMA_WARP) {
+    }
+    if (warp == TC_TMA_WARP) {
         // ---------------- TMA issuer
         if (lane == 0) {
             if (args.b_res && ld_tma(args.b_ld)) {
@@ -769,7 +770,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < TC_EPI_WARPS) {
         // ---------------- epilogue (warp w: TMEM lanes 32*(w%4).., columns of half w/4)
         // A 32 x 32 chunk goes TMEM -> registers (lane = row) -> the warp's swizzled
         // shared buffer -> global.  With TMA stores (epi_tma) the fused op is applied in
