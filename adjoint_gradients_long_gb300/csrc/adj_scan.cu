@@ -115,18 +115,18 @@ __device__ __forceinline__ void seg_get(RevSeg &c, float4 a, float4 b, bool cl) 
 // flags of the next 32 predecessors (nearest first: p0, p0 + dir, ...) and finds how
 // many published aggregates precede the nearest inclusive prefix (or the nearest
 // predecessor that has published nothing); then warp j folds predecessors 4j..4j+3 of
-// them, all warps' descriptor loads in flight at once, and warp 0 folds the 8 partial
-// composites in order.  A round costs about three L2 round trips however many
-// aggregates it consumes.  extend(acc, agg) composes one more (older) predecessor;
-// finish(acc, inc) returns the carry.  sx, sy, scl (8 x 32 entries) and ctl (2 words)
-// are shared scratch.  The result is valid in warp 0; a wait that gives up finishes
-// with zero_inc.
+// them, all warps' descriptor loads in flight at once (the last warp also loads the
+// inclusive prefix found), and warp 0 folds the 8 partial composites in order.  A round
+// costs about two L2 round trips however many aggregates it consumes.  extend(acc, agg)
+// composes one more (older) predecessor; finish(acc, inc) returns the carry.  sx, sy,
+// scl (8 x 32 entries), ix, iy (32 entries) and ctl (2 words) are shared scratch.  The
+// result is valid in warp 0; a wait that gives up finishes with zero_inc.
 constexpr int LB_MORE = 0, LB_WAIT = 1, LB_INC = 2, LB_END = 3, LB_TIMEOUT = 4;
 template <class C, class LA, class LI, class EX, class FI>
 __device__ __forceinline__ C cta_lookback(const unsigned *flags, int64_t p0, int dir, int64_t count, C ident,
                                           LA load_agg, LI load_inc, EX extend, FI finish, C zero_inc,
-                                          unsigned *status, float4 (*sx)[32], float4 (*sy)[32], bool *scl, int *ctl,
-                                          int w, int lane) {
+                                          unsigned *status, float4 (*sx)[32], float4 (*sy)[32], bool *scl, float4 *ix,
+                                          float4 *iy, int *ctl, int w, int lane) {
     C acc = ident, result = zero_inc;
     int64_t done = 0;
     bool wait_first = false;
@@ -174,6 +174,10 @@ __device__ __forceinline__ C cta_lookback(const unsigned *flags, int64_t p0, int
             seg_put(part, sx[w][lane], sy[w][lane], cl);
             if (lane == 0) scl[w] = cl;
         }
+        if (state == LB_INC && w == SC_WARPS - 1) {
+            bool cl;
+            seg_put(load_inc(p0 + dir * (done + m)), ix[lane], iy[lane], cl);
+        }
         __syncthreads();
         if (w == 0) {
             for (int j = 0; j < SC_WARPS && 4 * j < m; ++j) {
@@ -181,7 +185,11 @@ __device__ __forceinline__ C cta_lookback(const unsigned *flags, int64_t p0, int
                 seg_get(part, sx[j][lane], sy[j][lane], scl[j]);
                 acc = extend(acc, part);
             }
-            if (state == LB_INC) result = finish(acc, load_inc(p0 + dir * (done + m)));
+            if (state == LB_INC) {
+                C inc;
+                seg_get(inc, ix[lane], iy[lane], true);
+                result = finish(acc, inc);
+            }
             else if (state == LB_END) result = finish(acc, zero_inc);
         }
         done += m;
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(256, (L <= 8 ? 3 : L <= 12 ? 2 : 1)) k_fwd_sca
     __shared__ unsigned s_ticket;
     __shared__ uint64_t s_bar;
     __shared__ int s_abort;
-    __shared__ float4 sA[SC_WARPS][32], sH[SC_WARPS][32], sC[32];
+    __shared__ float4 sA[SC_WARPS][32], sH[SC_WARPS][32], sC[32], sI0[32], sI1[32];
     __shared__ bool s_cl[SC_WARPS];
     __shared__ int s_ctl[2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -298,7 +306,7 @@ __global__ void __launch_bounds__(256, (L <= 8 ? 3 : L <= 12 ? 2 : 1)) k_fwd_sca
             [&](int64_t p) { return float2x4{f4(0.f), ld_cg4(&d.inc1[(fb + p) * 32 + lane])}; },
             [](const float2x4 &acc, const float2x4 &g) { return float2x4{acc.x * g.x, fma4(acc.x, g.y, acc.y)}; },
             [](const float2x4 &acc, const float2x4 &inc) { return float2x4{f4(0.f), fma4(acc.x, inc.y, acc.y)}; },
-            float2x4{f4(0.f), f4(0.f)}, status, sA, sH, s_cl, s_ctl, w, lane);
+            float2x4{f4(0.f), f4(0.f)}, status, sA, sH, s_cl, sI0, sI1, s_ctl, w, lane);
         carry = r.y;
     }
     if (w == 0) {
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_win_scan
     __shared__ unsigned s_ticket;
     __shared__ uint64_t s_bar;
     __shared__ int s_abort;
-    __shared__ float4 sP[SC_WARPS][32], sS[SC_WARPS][32], sCP[32], sCS[32];
+    __shared__ float4 sP[SC_WARPS][32], sS[SC_WARPS][32], sCP[32], sCS[32], sI0[32], sI1[32];
     __shared__ bool sCl[SC_WARPS];
     __shared__ int s_ctl[2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,7 +401,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_win_scan
             [&](int64_t p) { return FwdSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
             [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
             [](const FwdSeg &acc, const FwdSeg &inc) { return fseg_then(inc, acc); },
-            FwdSeg{f4(1.f), f4(0.f), true}, status, sP, sS, sCl, s_ctl, w, lane);
+            FwdSeg{f4(1.f), f4(0.f), true}, status, sP, sS, sCl, sI0, sI1, s_ctl, w, lane);
     }
     if (w == 0) {
         if (!agg.cl) {
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
     __shared__ unsigned s_ticket;
     __shared__ uint64_t s_bar;
     __shared__ int s_abort;
-    __shared__ float4 sQ[SC_WARPS][32], sS[SC_WARPS][32], sCQ[32], sCS[32];
+    __shared__ float4 sQ[SC_WARPS][32], sS[SC_WARPS][32], sCQ[32], sCS[32], sI0[32], sI1[32];
     __shared__ bool sCl[SC_WARPS];
     __shared__ int s_ctl[2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -483,18 +491,6 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
     sQ[w][lane] = G.Q;
     sS[w][lane] = G.S;
     if (lane == 0) sCl[w] = G.cl;
-    // D_c = g h and E = c h need no carry: store them now, so these writes overlap the
-    // look-back
-    if (act) {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-            const int64_t t = t0 + k;
-            if (t >= T) break;
-            const int r = w * L + k;
-            st4(Dc + base + t * N, srow(sg, r, lane) * hv[k + 1]);
-            st4(E + base + t * N, srow(sc, r, lane) * hv[k + 1]);
-        }
-    }
     __syncthreads();
 
     // composite of the warps after this one and, in warp 0, the chunk aggregate
@@ -510,6 +506,18 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
         if (agg.cl) warp_publish(&d.inc0[di * 32 + lane], agg.Q, &d.inc1[di * 32 + lane], agg.S, &d.flags[di], F_INC, lane);
         else warp_publish(&d.agg0[di * 32 + lane], agg.Q, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
     }
+    // D_c = g h and E = c h need no carry: store them now, so these writes overlap the
+    // look-back (after warp 0's publish, whose fence would otherwise wait for them)
+    if (act) {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            if (t >= T) break;
+            const int r = w * L + k;
+            st4(Dc + base + t * N, srow(sg, r, lane) * hv[k + 1]);
+            st4(E + base + t * N, srow(sc, r, lane) * hv[k + 1]);
+        }
+    }
     __syncthreads();   // sQ/sS/sCl now serve as look-back scratch
     RevSeg carry{f4(0.f), f4(0.f), true};
     if (chunk + 1 < nchunks) {
@@ -519,7 +527,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
             [&](int64_t p) { return RevSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
             [](const RevSeg &acc, const RevSeg &g) { return rseg_then(acc, g); },
             [](const RevSeg &acc, const RevSeg &inc) { return rseg_then(acc, inc); },
-            RevSeg{f4(0.f), f4(0.f), true}, status, sQ, sS, sCl, s_ctl, w, lane);
+            RevSeg{f4(0.f), f4(0.f), true}, status, sQ, sS, sCl, sI0, sI1, s_ctl, w, lane);
     }
     if (w == 0) {
         if (!agg.cl) {
