@@ -288,8 +288,9 @@ adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *targe
         if (loss) ADJ_CUDA(cudaMemsetAsync(loss, 0, sizeof(double), st));
         return ADJ_OK;
     }
-    ProfScope ps(K_LOSS, st, loss ? 2 : 1);
-    ADJ_CUDA(launch_loss(y, target, gy, count, reinterpret_cast<double *>(at(ws, L.part0)), loss_blocks(count), loss, st));
+    ProfScope ps(K_LOSS, st);
+    ADJ_CUDA(launch_loss(y, target, gy, count, reinterpret_cast<double *>(at(ws, L.part0)), loss_blocks(count),
+                         status_word(ws) + 1, loss, st));
     return ADJ_OK;
 }
 

@@ -12,7 +12,8 @@ namespace adj {
 
 // ---------------------------------------------------------------- status word
 // Word 0 of the workspace: sticky device status; bit ADJ_ST_TIMEOUT is set by a
-// bounded wait that gave up.  Words 1..63 are reserved.
+// bounded wait that gave up.  Word 1: the loss kernel's wrapping block ticket.  Words
+// 2..63 are reserved.
 constexpr unsigned ST_TIMEOUT = 1u;
 constexpr size_t WS_HEADER = 256;
 
@@ -156,7 +157,9 @@ cudaError_t launch_rms_norm(const float *y, void *xhat, bool xbf, float *r, int6
                             cudaStream_t st);
 cudaError_t launch_rms_norm_bwd(const float *y, const float *r, const float *dx, const float *gy, float *gy_prev,
                                 int64_t rows, int P, cudaStream_t st);
+// ticket: a word of the workspace header (zero before the first call, back at zero after
+// every launch)
 cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t count,
-                        double *part, int nblk, double *loss, cudaStream_t st);
+                        double *part, int nblk, unsigned *ticket, double *loss, cudaStream_t st);
 
 }  // namespace adj

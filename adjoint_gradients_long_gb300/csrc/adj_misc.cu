@@ -8,12 +8,15 @@ namespace adj {
 // ---------------------------------------------------------------- loss
 // L = sum 1/2 (y - target)^2, gy = y - target.  Each thread sums its elements in fp32
 // (a few dozen terms), the block combines the thread sums in fp64 and writes one
-// partial; one block then sums the partials in a fixed order (deterministic).  FP64
-// arithmetic is kept out of the per-element loop: GB300's fp64 rate is a small
-// fraction of its fp32 rate.
+// partial; the block that finishes last (a wrapping ticket in the workspace header,
+// back at zero after every launch) sums the partials in a fixed order, so the result
+// does not depend on block order.  FP64 arithmetic is kept out of the per-element loop:
+// GB300's fp64 rate is a small fraction of its fp32 rate.
 __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const float *__restrict__ tg,
-                                              float *__restrict__ gy, int64_t count, double *__restrict__ part) {
+                                              float *__restrict__ gy, int64_t count, double *__restrict__ part,
+                                              unsigned *ticket, double *__restrict__ loss) {
     __shared__ double red[256];
+    __shared__ bool last;
     float s = 0.f;
     const int64_t n4 = count / 4, stride = int64_t(gridDim.x) * blockDim.x;
     int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
@@ -49,26 +52,29 @@ __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const
         if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
         __syncthreads();
     }
-    if (threadIdx.x == 0) part[blockIdx.x] = red[0];
-}
-
-__global__ void k_sum_partials(const double *__restrict__ part, int n, double *__restrict__ out) {
-    __shared__ double red[256];
-    double s = 0.0;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) s += part[i];
-    red[threadIdx.x] = s;
+    if (!loss) return;
+    if (threadIdx.x == 0) {
+        part[blockIdx.x] = red[0];
+        __threadfence();
+        last = atomicInc(ticket, gridDim.x - 1) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double t = 0.0;
+    for (int i = threadIdx.x; i < int(gridDim.x); i += blockDim.x) t += __ldcg(&part[i]);
+    red[threadIdx.x] = t;
     __syncthreads();
     for (int o = 128; o > 0; o >>= 1) {
         if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
         __syncthreads();
     }
-    if (threadIdx.x == 0) *out = red[0];
+    if (threadIdx.x == 0) *loss = red[0];
 }
 
 cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t count, double *part, int nblk,
-                        double *loss, cudaStream_t st) {
-    k_loss<<<nblk, 256, 0, st>>>(y, target, gy, count, part);
-    if (loss) k_sum_partials<<<1, 256, 0, st>>>(part, nblk, loss);
+                        unsigned *ticket, double *loss, cudaStream_t st) {
+    k_loss<<<nblk, 256, 0, st>>>(y, target, gy, count, part, ticket, loss);
     return cudaGetLastError();
 }
 
@@ -122,22 +128,32 @@ __global__ void __launch_bounds__(256) k_colsum(const void *__restrict__ D, int6
     }
 }
 
-// out[n] (+)= sum over blocks of part[blk][n]: a block owns 32 columns, its 8 row lanes
-// each sum every 8th partial and are combined in a fixed order (deterministic).
+// out[n] (+)= sum over blocks of part[blk][n]: a block owns 4 columns (one float4); its
+// 256 threads each sum every 256th partial (several loads in flight), then a fixed tree
+// combines them (deterministic).
 __global__ void __launch_bounds__(256) k_colsum_final(const float *__restrict__ part, int nblk, int N,
                                                       float *__restrict__ out, int accumulate) {
-    __shared__ float red[8][33];
-    const int col = blockIdx.x * 32 + (threadIdx.x & 31), rl = threadIdx.x >> 5;
-    float s = 0.f;
-    if (col < N)
-        for (int b = rl; b < nblk; b += 8) s += part[int64_t(b) * N + col];
-    red[rl][threadIdx.x & 31] = s;
-    __syncthreads();
-    if (rl == 0 && col < N) {
-        float t = 0.f;
+    __shared__ float4 red[256];
+    const int col = blockIdx.x * 4;
+    float4 s = f4(0.f);
+    int b = threadIdx.x;
+    for (; b + 3 * 256 < nblk; b += 4 * 256) {
+        float4 v[4];
 #pragma unroll
-        for (int l = 0; l < 8; ++l) t += red[l][threadIdx.x & 31];
-        out[col] = accumulate ? out[col] + t : t;
+        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4 *>(part + int64_t(b + u * 256) * N + col);
+        s = s + ((v[0] + v[1]) + (v[2] + v[3]));
+    }
+    for (; b < nblk; b += 256) s = s + *reinterpret_cast<const float4 *>(part + int64_t(b) * N + col);
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] = red[threadIdx.x] + red[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        float4 t = red[0];
+        if (accumulate) t = t + *reinterpret_cast<const float4 *>(out + col);
+        *reinterpret_cast<float4 *>(out + col) = t;
     }
 }
 
@@ -146,7 +162,7 @@ cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *
     const int64_t rpb = (rows + nblk - 1) / nblk;
     if (bf16) k_colsum<true><<<nblk, 256, 0, st>>>(D, rows, N, rpb, part);
     else k_colsum<false><<<nblk, 256, 0, st>>>(D, rows, N, rpb, part);
-    k_colsum_final<<<(N + 31) / 32, 256, 0, st>>>(part, nblk, N, out, accumulate);
+    k_colsum_final<<<N / 4, 256, 0, st>>>(part, nblk, N, out, accumulate);
     return cudaGetLastError();
 }
 
