@@ -54,8 +54,8 @@ int gemm_splits(int64_t M, int64_t Nc, int64_t K) {
 int splits_in(const adj_dims *d) { return gemm_splits(d->P, 3 * int64_t(d->N), d->B * d->T); }
 int splits_o(const adj_dims *d) { return gemm_splits(d->N, d->P, d->B * d->T); }
 int colsum_blocks(const adj_dims *d) {
-    int64_t n = cdiv(d->B * d->T, 64);
-    if (n > 608) n = 608;
+    int64_t n = cdiv(d->B * d->T, 32);   // ~32 rows a block: every thread's loads in one batch
+    if (n > 2432) n = 2432;
     return n < 1 ? 1 : int(n);
 }
 int loss_blocks(int64_t count) {
