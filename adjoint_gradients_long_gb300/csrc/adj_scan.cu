@@ -200,10 +200,10 @@ __device__ __forceinline__ C cta_lookback(const unsigned *flags, int64_t p0, int
 }
 
 // ============================================================================ chunk staging
-// Up to three input arrays of a scan, each a TMA map over [B*T rows, N cols] fp32 with a
+// Up to four input arrays of a scan, each a TMA map over [B*T rows, N cols] fp32 with a
 // box of 128 channels x (rows of the chunk).
 struct ScanMaps {
-    CUtensorMap m[3];
+    CUtensorMap m[4];
 };
 
 __device__ __forceinline__ float *smem_1k(uint8_t *p) {
@@ -507,18 +507,28 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
         else warp_publish(&d.agg0[di * 32 + lane], agg.Q, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
     }
     // D_c = g h and E = c h need no carry: store them now, so these writes overlap the
-    // look-back (after warp 0's publish, whose fence would otherwise wait for them)
+    // look-back (after warp 0's publish, whose fence would otherwise wait for them).  The
+    // g rows then hold e = g c for pass 2, and the c rows are free.
     if (act) {
 #pragma unroll
         for (int k = 0; k < L; ++k) {
             const int64_t t = t0 + k;
             if (t >= T) break;
             const int r = w * L + k;
-            st4(Dc + base + t * N, srow(sg, r, lane) * hv[k + 1]);
-            st4(E + base + t * N, srow(sc, r, lane) * hv[k + 1]);
+            const float4 gk = srow(sg, r, lane), ck = srow(sc, r, lane);
+            st4(Dc + base + t * N, gk * hv[k + 1]);
+            st4(E + base + t * N, ck * hv[k + 1]);
+            *reinterpret_cast<float4 *>(sg + r * SC_SLICE + lane * 4) = gk * ck;
         }
     }
     __syncthreads();   // sQ/sS/sCl now serve as look-back scratch
+    // truncated mode: R at the window end of token t (row t + W - 1, the same local row)
+    // lands in the c rows while the look-back runs
+    if (TRUNC && threadIdx.x == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(smem_u32(&s_bar), uint32_t(TT) * SC_SLICE * 4u);
+        tma_load_2d(smem_u32(sc), &mp.m[3], slice * SC_SLICE, int(b * T + c0 + W - 1), smem_u32(&s_bar));
+    }
     RevSeg carry{f4(0.f), f4(0.f), true};
     if (chunk + 1 < nchunks) {
         carry = cta_lookback<RevSeg>(
@@ -541,19 +551,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
 
     // composite of everything after this warp's tokens, then pass 2 backwards
     G = rseg_then(post, RevSeg{sCQ[lane], sCS[lane], true});
-    // R at the end of each token's window (truncated mode)
-    float4 rv[TRUNC ? L : 1];
-    if (TRUNC) {
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-            const int64_t t = t0 + k;
-            rv[k] = f4(0.f);
-            if (act && t < T && t % W != 0 && (t / W + 1) * W < T) {
-                const int64_t m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
-                rv[k] = ld_keep4(R + base + m * N);
-            }
-        }
-    }
+    if (TRUNC) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
         const int64_t t = t0 + k;
@@ -561,12 +559,18 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan
         const int r = w * L + k;
         const float4 ak = srow(sa, r, lane);
         const float4 bk = t + 1 < T ? srow(sa, r + 1, lane) : f4(0.f);
-        const float4 ek = srow(sg, r, lane) * srow(sc, r, lane);
+        const float4 ek = srow(sg, r, lane);   // e = g c (written after pass 1)
         const bool end = (t == T - 1) || (TRUNC && (t + 1) % W == 0);
         if (end) G = RevSeg{bk, ek, true};
         else G = RevSeg{bk * G.Q, fma4(bk, G.S, ek), true};
         float4 mu = G.S;
-        if (TRUNC && t % W != 0 && (t / W + 1) * W < T) mu = fma4(G.Q, rv[k], G.S);
+        if (TRUNC && t % W != 0 && (t / W + 1) * W < T) {
+            // the window ends at min(t + W - 1, T - 1); past the sequence end the staged row
+            // is not this sequence's, so the last row is read directly
+            const float4 rk = t + W - 1 <= T - 1 ? srow(sc, r, lane)
+                                                 : (act ? ld_keep4(R + base + (T - 1) * N) : f4(0.f));
+            mu = fma4(G.Q, rk, G.S);
+        }
         if (act) {
             st4(Du + base + t * N, mu);
             st4(Da + base + t * N, mu * hv[k] * ak * (f4(1.f) - ak));
@@ -632,14 +636,14 @@ cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, cons
     constexpr int L = SC_BWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
+    const bool trunc = W > 0 && W < T;
     ScanMaps mp;
-    const float *arr[3] = {g, c, a};
-    const int rows[3] = {TT, TT, TT + 1};
-    if (!scan_maps(mp, 3, arr, rows, B, T, N)) return cudaErrorInvalidValue;
+    const float *arr[4] = {g, c, a, R};
+    const int rows[4] = {TT, TT, TT + 1, TT};
+    if (!scan_maps(mp, trunc ? 4 : 3, arr, rows, B, T, N)) return cudaErrorInvalidValue;
     ScanWs d = scan_ws_carve(scan_ws, B, T, N);
     cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
     if (e != cudaSuccess) return e;
-    const bool trunc = W > 0 && W < T;
     const unsigned grid = unsigned(nseq * nchunks);
     const size_t smem = staged_bytes(3 * TT + 1);
 #define ADJ_BWD(TR, TDT)                                                                                          \
