@@ -358,14 +358,14 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *maps, const GemmOper
 }
 
 // Convert a raw fp32 tile (R = 128 rows x 64 k, as TMA wrote it) in place into the bf16
-// hi (and lo) tiles: k-contiguous sources into the swizzled K-major layout, row-contiguous
-// sources into the swizzled MN-major layout.  Raw layouts: k-contiguous source:
+// hi (and lo) tiles of the swizzled K-major layout.  Raw layouts: k-contiguous source:
 // row r at r*256 B; row-contiguous source: boxes of 64 rows, box j at j*16 KB holding
 // [k][row] with 256-byte k rows.  Every producer thread reads all its values first, the
 // producers meet at a named barrier, then write (hi at region, lo at region + 16 KB).
-// Both mappings keep shared-memory reads and writes free of bank conflicts: tiles are
-// read as 16-byte vectors, 32 lanes covering 512 contiguous bytes, and written as 8-byte
-// halves of the swizzled 16-byte chunks, 16 lanes filling one 128-byte row.
+// Both mappings keep shared-memory reads and writes free of bank conflicts: k-contiguous
+// tiles are read as 16-byte vectors, 32 lanes covering two full rows, and written as
+// 8-byte halves of the swizzled 16-byte chunks; row-contiguous tiles are read one value
+// per lane (32 consecutive rows) and written as whole chunks of one row per lane.
 __device__ __forceinline__ void put4(uint8_t *hi, uint8_t *lo, int r, int k4, float4 v, bool split) {
     const uint32_t off = uint32_t(r) * 128u + (uint32_t((k4 >> 1) ^ (r & 7)) << 4) + uint32_t(k4 & 1) * 8u;
     uint2 h;
@@ -408,36 +408,22 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
             if (ITEMS % NP == 0 || q < ITEMS) put4(region, region + R * 128, q >> 4, q & 15, v[i], SPLIT);
         }
     } else {
-        // row-contiguous source: no transpose; the product tile keeps the MN-major layout
-        // (blocks of 64 rows x 64 k, 8 KB; element (m, k) at (m/64) 8192 + 128 k +
-        // 16 (((m%64)/8) ^ (k%8)) + 2 (m%8), as TMA writes bf16 MN-major boxes).  A float4 is
-        // 4 consecutive rows at one k (raw box j = m/64 at j * 16 KB, [k][64 rows]).
-        constexpr int ITEMS = R * 16, PER = (ITEMS + NP - 1) / NP;
-        float4 v[PER];
+        constexpr int ITEMS = R * 8, PER = (ITEMS + NP - 1) / NP;    // items (one row, 8 k)
+        float v[PER][8];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int q = ptid + i * NP;
-            if (ITEMS % NP == 0 || q < ITEMS) v[i] = reinterpret_cast<const float4 *>(raw)[q];
+            const int it = ptid + i * NP, r = it % R, kc = it / R;
+            const float *src = raw + (r >> 6) * 4096 + (r & 63);
+            if (ITEMS % NP == 0 || it < ITEMS) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(NP) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int q = ptid + i * NP;
-            if (ITEMS % NP == 0 || q < ITEMS) {
-                const int j = q >> 10, k = (q >> 4) & 63, m4 = q & 15;
-                const uint32_t off = uint32_t(j) * 8192u + uint32_t(k) * 128u +
-                                     (uint32_t((m4 >> 1) ^ (k & 7)) << 4) + uint32_t(m4 & 1) * 8u;
-                uint2 h;
-                h.x = pack_bf16(v[i].x, v[i].y);
-                h.y = pack_bf16(v[i].z, v[i].w);
-                *reinterpret_cast<uint2 *>(region + off) = h;
-                if (SPLIT) {
-                    uint2 l;
-                    l.x = pack_bf16(v[i].x - bf16_round(v[i].x), v[i].y - bf16_round(v[i].y));
-                    l.y = pack_bf16(v[i].z - bf16_round(v[i].z), v[i].w - bf16_round(v[i].w));
-                    *reinterpret_cast<uint2 *>(region + R * 128 + off) = l;
-                }
-            }
+            const int it = ptid + i * NP;
+            if (ITEMS % NP == 0 || it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
         }
     }
 }
@@ -724,9 +710,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     } else if (warp == TC_MMA_WARP) {
         // ---------------- MMA issuer
         if (lane == 0) {
-            // MN-major tiles: bf16 loaded by TMA, and fp32 converted in place from row-contiguous sources
-            const bool a_mn = args.a_ld == LD_TMA_MN || args.a_ld == LD_RAW_MN;
-            const bool b_mn = args.b_ld == LD_TMA_MN || args.b_ld == LD_RAW_MN;
+            const bool a_mn = args.a_ld == LD_TMA_MN, b_mn = args.b_ld == LD_TMA_MN;
             const uint32_t idesc = idesc_bf16(BN, a_mn, b_mn);
             bool ok = !args.b_res || mbar_wait(smem_u32(bready), 0, abort, args.status);
             if (ok) tc_fence_after();
