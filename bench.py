@@ -375,18 +375,39 @@ def run_ours(args, rank, world, local_rank):
     hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (st.dW_in[0], st.db_a[0], st.dW_o[0])]
     h2d = hx.numel() * 4 + ht.numel() * 4
     d2h = 8 + sum(t.numel() * 4 for t in hg)
+    # Inputs are double-buffered: step i+1's inputs are copied on a second stream while step
+    # i computes; every step's copies stay inside the timed region.
+    copy_stream = torch.cuda.Stream(dev)
+    bufs = [(st.x[0], st.target), (torch.empty_like(st.x[0]), torch.empty_like(st.target))]
+    landed = [torch.cuda.Event(), torch.cuda.Event()]      # inputs of buffer b copied
+    used = [torch.cuda.Event(), torch.cuda.Event()]        # step that read buffer b done
+
+    def stage_inputs(b, after):
+        copy_stream.wait_event(after)
+        with torch.cuda.stream(copy_stream):
+            bufs[b][0].copy_(hx, non_blocking=True)
+            bufs[b][1].copy_(ht, non_blocking=True)
+            landed[b].record(copy_stream)
+
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        st.x[0].copy_(hx, non_blocking=True)
-        st.target.copy_(ht, non_blocking=True)
+    stage_inputs(0, e0)
+    for i in range(args.steps):
+        b = i % 2
+        stream.wait_event(landed[b])
+        st.x[0], st.target = bufs[b]
+        if i + 1 < args.steps:
+            # the other buffer was last read by step i-1
+            stage_inputs(1 - b, used[1 - b] if i > 0 else e0)
         st.step(None)
+        used[b].record(stream)
         hl.copy_(st.loss, non_blocking=True)
         for hgt, dg in zip(hg, (st.dW_in[0], st.db_a[0], st.dW_o[0])):
             hgt.copy_(dg, non_blocking=True)
     e1.record(stream)
     barrier()
+    st.x[0], st.target = bufs[0]
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # max over ranks
