@@ -641,8 +641,12 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         else convert_raw128<SPLIT, false>(sa, ptid);
                     }
                     if (b_raw) {
-                        if (args.b_ld == LD_RAW_MN) convert_raw128<SPLIT, true>(sbb, ptid);
-                        else convert_raw128<SPLIT, false>(sbb, ptid);
+                        // a 256-row B tile converts as two independent 128-row halves
+                        const bool bmn = args.b_ld == LD_RAW_MN;
+                        for (uint8_t *bh = sbb; bh < sbb + BN * 256; bh += 2 * TC_BM * 128) {
+                            if (bmn) convert_raw128<SPLIT, true>(bh, ptid);
+                            else convert_raw128<SPLIT, false>(bh, ptid);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
@@ -712,6 +716,10 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         if (lane == 0) {
             const bool a_mn = args.a_ld == LD_TMA_MN, b_mn = args.b_ld == LD_TMA_MN;
             const uint32_t idesc = idesc_bf16(BN, a_mn, b_mn);
+            // a streamed raw B of 256 rows sits as two converted 128-row halves (hi, lo each):
+            // one N = 128 product per half into adjacent accumulator columns
+            const bool b_halves = !args.b_res && ld_raw(args.b_ld) && BN == 2 * TC_BM;
+            const uint32_t idesc_h = idesc_bf16(TC_BM, a_mn, b_mn);
             bool ok = !args.b_res || mbar_wait(smem_u32(bready), 0, abort, args.status);
             if (ok) tc_fence_after();
             int64_t kbg = 0, i = 0;
@@ -743,25 +751,26 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         b_hi = st + Lo.a_reg;
                         b_lo = b_hi + Lo.b_bytes;
                     }
+                    const int nh = b_halves ? 2 : 1;
+                    const uint32_t id = b_halves ? idesc_h : idesc;
+                    for (int h = 0; h < nh; ++h) {
+                        const uint32_t bh0 = b_hi + uint32_t(h) * (2 * TC_BM * 128);
+                        const uint32_t bl0 = b_halves ? bh0 + TC_BM * 128 : b_lo;
+                        const uint32_t dh = dacc + uint32_t(h * TC_BM);
 #pragma unroll
-                    for (int ks = 0; ks < TC_BK / 16; ++ks) {
-                        const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-                        if (SPLIT) {
+                        for (int ks = 0; ks < TC_BK / 16; ++ks) {
+                            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
                             const uint32_t ka = a_mn ? uint32_t(ks) * 2048u : uint32_t(ks) * 32u;
                             const uint32_t kb2 = b_mn ? uint32_t(ks) * 2048u : uint32_t(ks) * 32u;
                             const uint64_t ah = a_mn ? sw128_desc_mn(a_hi + ka) : sw128_desc(a_hi + ka);
-                            const uint64_t al = a_mn ? sw128_desc_mn(a_lo + ka) : sw128_desc(a_lo + ka);
-                            const uint64_t bh = b_mn ? sw128_desc_mn(b_hi + kb2) : sw128_desc(b_hi + kb2);
-                            const uint64_t bl = b_mn ? sw128_desc_mn(b_lo + kb2) : sw128_desc(b_lo + kb2);
-                            mma_bf16(dacc, ah, bh, idesc, acc);
-                            mma_bf16(dacc, ah, bl, idesc, 1u);
-                            mma_bf16(dacc, al, bh, idesc, 1u);
-                        } else {
-                            const uint64_t ad = a_mn ? sw128_desc_mn(a_hi + uint32_t(ks) * 2048u)
-                                                     : sw128_desc(a_hi + uint32_t(ks) * 32u);
-                            const uint64_t bd = b_mn ? sw128_desc_mn(b_hi + uint32_t(ks) * 2048u)
-                                                     : sw128_desc(b_hi + uint32_t(ks) * 32u);
-                            mma_bf16(dacc, ad, bd, idesc, acc);
+                            const uint64_t bh = b_mn ? sw128_desc_mn(bh0 + kb2) : sw128_desc(bh0 + kb2);
+                            mma_bf16(dh, ah, bh, id, acc);
+                            if (SPLIT) {
+                                const uint64_t al = a_mn ? sw128_desc_mn(a_lo + ka) : sw128_desc(a_lo + ka);
+                                const uint64_t bl = b_mn ? sw128_desc_mn(bl0 + kb2) : sw128_desc(bl0 + kb2);
+                                mma_bf16(dh, ah, bl, id, 1u);
+                                mma_bf16(dh, al, bh, id, 1u);
+                            }
                         }
                     }
                     mma_commit(smem_u32(&empty[s]));
@@ -964,7 +973,8 @@ static int tma_mode(const GemmOperand &O, bool is_a, int64_t rows, int64_t K, in
     else if (O.s_row == 1 && O.s_k % vec == 0 && R % 64 == 0) mode = LD_TMA_MN;
     else return LD_REG;
     if (O.bf16) return (split3 && !O.lo[0]) || (!split3 && O.lo[0]) ? LD_REG : mode;   // split mode: bf16 pre-split only
-    return R == TC_BM ? (mode == LD_TMA_K ? LD_RAW_K : LD_RAW_MN) : LD_REG;
+    // raw tiles convert 128 rows at a time: A tiles of 128 rows, B tiles of 128 or 256
+    return (R == TC_BM || (!is_a && R == 2 * TC_BM)) ? (mode == LD_TMA_K ? LD_RAW_K : LD_RAW_MN) : LD_REG;
 }
 
 // Build the maps of an operand for the chosen mode; returns the mode, or LD_REG if a map
@@ -1030,7 +1040,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
         a.b_res = splits == 1 && size_t(res.bres_bytes) + 2 * size_t(res.stage_bytes) <= budget;
         b_mode = tma_mode(Bm, false, Nc, K, BN, split3);
         if (a.b_res && ld_raw(b_mode)) b_mode = LD_REG;          // a resident B is converted once, by registers
-        if (!a.b_res && !Bm.bf16 && !Bm.mul && BN > TC_BM && tma_mode(Bm, false, Nc, K, TC_BM, split3) != LD_REG) {
+        if (!a.b_res && !Bm.bf16 && !Bm.mul && BN > TC_BM && BN != 2 * TC_BM &&
+            tma_mode(Bm, false, Nc, K, TC_BM, split3) != LD_REG) {
             next = TC_BM;                                         // take 128-column tiles to load B raw
             continue;
         }
