@@ -54,8 +54,8 @@ int gemm_splits(int64_t M, int64_t Nc, int64_t K) {
 int splits_in(const adj_dims *d) { return gemm_splits(d->P, 3 * int64_t(d->N), d->B * d->T); }
 int splits_o(const adj_dims *d) { return gemm_splits(d->N, d->P, d->B * d->T); }
 int colsum_blocks(const adj_dims *d) {
-    int64_t n = cdiv(d->B * d->T, 32);   // ~32 rows a block: every thread's loads in one batch
-    if (n > 2432) n = 2432;
+    int64_t n = cdiv(d->B * d->T, 64);   // four blocks on each of the 152 SMs for long inputs
+    if (n > 608) n = 608;
     return n < 1 ? 1 : int(n);
 }
 int loss_blocks(int64_t count) {
@@ -157,6 +157,7 @@ GemmOperand opw(const void *w, int64_t n, bool xbf, void *split, int64_t s_row, 
                 cudaError_t *err) {
     if (xbf) return op1(w, s_row, s_k, true);
     __nv_bfloat16 *hi = static_cast<__nv_bfloat16 *>(split), *lo = hi + n;
+    ProfScope ps(K_WEIGHT_PREP, st);
     *err = launch_split_bf16(static_cast<const float *>(w), n, hi, lo, st);
     GemmOperand o = op1(hi, s_row, s_k, true);
     o.lo[0] = o.lo[1] = o.lo[2] = lo;
@@ -188,10 +189,10 @@ adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a
     e.out0 = g;
     e.ld = N;
     {
-        ProfScope ps(K_COT_PROJ, st);
         cudaError_t err = cudaSuccess;
         const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, dims->x_dtype == ADJ_BF16, at(ws, L.wsplit), P, 1, st, &err);
         ADJ_CUDA(err);
+        ProfScope ps(K_COT_PROJ, st);
         ADJ_CUDA(launch_gemm_tc(BT, N, P, op1(gy, P, 1, false), Wo, e, 1, dims->x_dtype == ADJ_F32, status_word(ws), st));
     }
     const bool trunc = op == ADJ_OP_BWD_TRUNC && Tbar < T;
@@ -242,7 +243,10 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
         // sigmoid (the epilogue maps the chunks back)
         __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(at(ws, L.wsplit));
         __nv_bfloat16 *lo = xbf ? nullptr : hi + int64_t(P) * 3 * N;
-        ADJ_CUDA(launch_prep_win(w->W_in, xbf, P, N, hi, lo, st));
+        {
+            ProfScope pw(K_WEIGHT_PREP, st);
+            ADJ_CUDA(launch_prep_win(w->W_in, xbf, P, N, hi, lo, st));
+        }
         Win = op1(hi, 1, 3 * int64_t(N), true);
         if (lo) Win.lo[0] = Win.lo[1] = Win.lo[2] = lo;
         e.interleave = true;
@@ -342,9 +346,12 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         ADJ_CUDA(launch_gemm_tc(P, 3 * int64_t(N), BT, op1(xhat, 1, P, xbf), op3(D_a, D_u, D_c, N, 1, N, dbf), e, s_in,
                                 !xbf, status_word(ws), st, &su_in));
     }
+    // db_a = sum_t D_a: block partials while D_a is still partly in L2
+    float *part_c = reinterpret_cast<float *>(at(ws, L.part2));
+    const int ncs = colsum_blocks(dims);
     {
-        ProfScope ps(K_SPLITK, st);
-        ADJ_CUDA(launch_splitk_reduce(part_in, su_in, int64_t(P) * 3 * N, dW_in, accumulate, st));
+        ProfScope ps(K_COLSUM, st);
+        ADJ_CUDA(launch_colsum(D_a, dbf, BT, N, part_c, ncs, st));
     }
     // dW_o = E^T gy
     GemmEpilogue e2 = epi(Epi::Partial);
@@ -353,15 +360,13 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         ProfScope ps(K_PARAM_DWO, st);
         ADJ_CUDA(launch_gemm_tc(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s_o, !xbf, status_word(ws), st, &su_o));
     }
+    // the three sums over partials, in one launch
     {
-        ProfScope ps(K_SPLITK, st);
-        ADJ_CUDA(launch_splitk_reduce(part_o, su_o, int64_t(N) * P, dW_o, accumulate, st));
-    }
-    // db_a = sum_t D_a
-    {
-        ProfScope ps(K_COLSUM, st, 2);
-        ADJ_CUDA(launch_colsum(D_a, dbf, BT, N, reinterpret_cast<float *>(at(ws, L.part2)), colsum_blocks(dims), db_a,
-                               accumulate, st));
+        const RedSeg segs[3] = {{part_in, dW_in, int64_t(P) * 3 * N / 4, su_in, 0, 0},
+                                {part_o, dW_o, int64_t(N) * P / 4, su_o, 0, 0},
+                                {part_c, db_a, N / 4, ncs, 0, 0}};
+        ProfScope ps(K_PARAM_REDUCE, st);
+        ADJ_CUDA(launch_reduce_partials(segs, 3, accumulate, st));
     }
     if (gy_prev || dxhat) {
         // dxhat = [D_a | D_u | D_c] W_in^T, or gy_prev = gy + dxhat

@@ -149,10 +149,26 @@ cudaError_t launch_prep_win(const void *w, bool w_bf16, int P, int N, __nv_bfloa
                             cudaStream_t st);
 // hi = bf16(w), lo = bf16(w - hi) for n fp32 values (operands of the split-precision GEMM)
 cudaError_t launch_split_bf16(const float *w, int64_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo, cudaStream_t st);
-cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out,
-                                 int accumulate, cudaStream_t st);
-cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk,
-                          float *out, int accumulate, cudaStream_t st);
+// One array of partials to reduce: out[i] (+)= sum_{z < splits} part[z * 4 n4 + i] over
+// i < 4 n4 (16-byte aligned; group and first, the array's first block, are filled in by
+// the launcher).
+struct RedSeg {
+    const float *part;
+    float *out;
+    int64_t n4;
+    int splits;
+    int group;
+    int64_t first;
+};
+struct RedArgs {
+    RedSeg seg[3];
+    int nseg;
+    int accumulate;
+};
+// Reduces up to three arrays of partials in one launch, deterministically.
+cudaError_t launch_reduce_partials(const RedSeg *segs, int nseg, int accumulate, cudaStream_t st);
+// part[blk][n] = column sums of D over block blk's rows (nblk contiguous row ranges)
+cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk, cudaStream_t st);
 cudaError_t launch_rms_norm(const float *y, void *xhat, bool xbf, float *r, int64_t rows, int P, float eps,
                             cudaStream_t st);
 cudaError_t launch_rms_norm_bwd(const float *y, const float *r, const float *dx, const float *gy, float *gy_prev,

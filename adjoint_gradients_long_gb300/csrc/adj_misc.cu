@@ -79,10 +79,11 @@ cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t 
 }
 
 // ---------------------------------------------------------------- column sums
-// part[blk][n] = sum over the block's rows of D[row][n]; out[n] (+)= sum_blk part[blk][n].
-// A block is 256 threads = (N/4 column groups of 4) x (256/(N/4) row lanes); each thread
-// reads 4 columns (one 8- or 16-byte vector) of every row-lane-th row, several rows in
-// flight, and the row lanes are combined in shared memory.
+// part[blk][n] = sum over the block's rows of D[row][n]; the blocks own contiguous row
+// ranges and their partials are summed by k_reduce_partials.  A block is 256 threads =
+// (N/4 column groups of 4) x (256/(N/4) row lanes); each thread reads 4 columns (one 8- or
+// 16-byte vector) of every row-lane-th row, eight rows in flight, and the row lanes are
+// combined in shared memory in a fixed order.
 template <bool BF>
 __device__ __forceinline__ float4 ld_row4(const void *D, int64_t i) {
     if (BF) {
@@ -108,7 +109,6 @@ __global__ void __launch_bounds__(256) k_colsum(const void *__restrict__ D, int6
         float4 acc = f4(0.f);
         if (rl < lanes && col < N) {
             int64_t r = r0 + rl;
-            // eight rows in flight per thread
             for (; r + 7 * lanes < r1; r += 8 * lanes) {
                 float4 v[8];
 #pragma unroll
@@ -128,59 +128,108 @@ __global__ void __launch_bounds__(256) k_colsum(const void *__restrict__ D, int6
     }
 }
 
-// out[n] (+)= sum over blocks of part[blk][n]: a block owns 4 columns (one float4); its
-// 256 threads each sum every 256th partial (several loads in flight), then a fixed tree
-// combines them (deterministic).
-__global__ void __launch_bounds__(256) k_colsum_final(const float *__restrict__ part, int nblk, int N,
-                                                      float *__restrict__ out, int accumulate) {
-    __shared__ float4 red[256];
-    const int col = blockIdx.x * 4;
-    float4 s = f4(0.f);
-    int b = threadIdx.x;
-    for (; b + 3 * 256 < nblk; b += 4 * 256) {
-        float4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4 *>(part + int64_t(b + u * 256) * N + col);
-        s = s + ((v[0] + v[1]) + (v[2] + v[3]));
-    }
-    for (; b < nblk; b += 256) s = s + *reinterpret_cast<const float4 *>(part + int64_t(b) * N + col);
-    red[threadIdx.x] = s;
-    __syncthreads();
-    for (int o = 128; o > 0; o >>= 1) {
-        if (threadIdx.x < o) red[threadIdx.x] = red[threadIdx.x] + red[threadIdx.x + o];
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        float4 t = red[0];
-        if (accumulate) t = t + *reinterpret_cast<const float4 *>(out + col);
-        *reinterpret_cast<float4 *>(out + col) = t;
-    }
-}
-
-cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk, float *out,
-                          int accumulate, cudaStream_t st) {
+cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *part, int nblk, cudaStream_t st) {
     const int64_t rpb = (rows + nblk - 1) / nblk;
     if (bf16) k_colsum<true><<<nblk, 256, 0, st>>>(D, rows, N, rpb, part);
     else k_colsum<false><<<nblk, 256, 0, st>>>(D, rows, N, rpb, part);
-    k_colsum_final<<<N / 4, 256, 0, st>>>(part, nblk, N, out, accumulate);
     return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- split-K reduction
-__global__ void __launch_bounds__(256) k_splitk_reduce(const float *__restrict__ part, int splits, int64_t count,
-                                                       float *__restrict__ out, int accumulate) {
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count; i += int64_t(gridDim.x) * blockDim.x) {
-        float s = accumulate ? out[i] : 0.f;
-        for (int z = 0; z < splits; ++z) s += part[int64_t(z) * count + i];
-        out[i] = s;
+// ---------------------------------------------------------------- partial reductions
+// out[i] (+)= sum_z part[z][i] for up to three independent arrays (the split-K partials of
+// dW_in and dW_o, the column-sum partials of db_a) in one launch; each array owns a range
+// of blocks.  Wide arrays: a block covers 32 consecutive float4 outputs, warp w sums the
+// partials z = w, w + 8, ... (eight loads in flight, every load a 512-byte row segment)
+// and the eight warp sums are added in warp order.  Narrow arrays with many partials
+// (the column sums): an output float4 is owned by a group of G lanes (a power of two, at
+// most 32, so that a lane loads at most eight partials at a time); lane g sums z = g,
+// g + G, ... and a butterfly of shuffles combines the group.  The order of every addition
+// is fixed, so the result does not depend on scheduling.
+__global__ void __launch_bounds__(256) k_reduce_partials(RedArgs r) {
+    // the array by explicit selection (an indexed parameter array would go to local memory)
+    const int64_t bx = blockIdx.x;
+    const bool s2 = r.nseg > 2 && bx >= r.seg[2].first, s1 = !s2 && r.nseg > 1 && bx >= r.seg[1].first;
+    const float4 *part = reinterpret_cast<const float4 *>(s2 ? r.seg[2].part : s1 ? r.seg[1].part : r.seg[0].part);
+    float4 *out = reinterpret_cast<float4 *>(s2 ? r.seg[2].out : s1 ? r.seg[1].out : r.seg[0].out);
+    const int64_t n4 = s2 ? r.seg[2].n4 : s1 ? r.seg[1].n4 : r.seg[0].n4;
+    const int64_t blk = bx - (s2 ? r.seg[2].first : s1 ? r.seg[1].first : r.seg[0].first);
+    const int splits = s2 ? r.seg[2].splits : s1 ? r.seg[1].splits : r.seg[0].splits;
+    const int G = s2 ? r.seg[2].group : s1 ? r.seg[1].group : r.seg[0].group;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float4 red[8][32];
+    if (G == 0) {
+        const int64_t q = blk * 32 + lane;
+        float4 s = f4(0.f);
+        if (q < n4) {
+            for (int z0 = w; z0 < splits; z0 += 64) {
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int z = z0 + 8 * u;
+                    v[u] = z < splits ? __ldcs(part + int64_t(z) * n4 + q) : f4(0.f);
+                }
+                s = s + (((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7])));
+            }
+        }
+        red[w][lane] = s;
+        __syncthreads();
+        if (w == 0 && q < n4) {
+            float4 t = red[0][lane];
+#pragma unroll
+            for (int k = 1; k < 8; ++k) t = t + red[k][lane];
+            if (r.accumulate) t = out[q] + t;
+            out[q] = t;
+        }
+        return;
+    }
+    const int64_t q = blk * (256 / G) + threadIdx.x / G;
+    const int g = threadIdx.x % G;
+    const bool live = q < n4;
+    float4 s = f4(0.f);
+    if (live) {
+        const float4 *p = part + q;
+        for (int z0 = g; z0 < splits; z0 += 8 * G) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int z = z0 + u * G;
+                v[u] = z < splits ? __ldcs(p + int64_t(z) * n4) : f4(0.f);
+            }
+            s = s + (((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7])));
+        }
+    }
+    for (int o = 1; o < G; o <<= 1) {
+        s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+        s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+        s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+        s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+    }
+    if (live && g == 0) {
+        if (r.accumulate) s = out[q] + s;
+        out[q] = s;
     }
 }
 
-cudaError_t launch_splitk_reduce(const float *part, int splits, int64_t count, float *out, int accumulate,
-                                 cudaStream_t st) {
-    int64_t blocks = (count + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    k_splitk_reduce<<<unsigned(blocks), 256, 0, st>>>(part, splits, count, out, accumulate);
+cudaError_t launch_reduce_partials(const RedSeg *segs, int nseg, int accumulate, cudaStream_t st) {
+    RedArgs r;
+    memset(&r, 0, sizeof(r));
+    if (nseg < 1 || nseg > 3) return cudaErrorInvalidValue;
+    int64_t first = 0;
+    for (int k = 0; k < nseg; ++k) {
+        r.seg[k] = segs[k];
+        int G = 0;                                   // 0: warps over the partials
+        if (segs[k].n4 < 4096) {                     // narrow: lane groups
+            G = 1;
+            while (G < 32 && (segs[k].splits + G - 1) / G > 8) G <<= 1;
+        }
+        r.seg[k].group = G;
+        r.seg[k].first = first;                      // first block of the array
+        first += G == 0 ? (segs[k].n4 + 31) / 32 : (segs[k].n4 * G + 255) / 256;
+    }
+    r.nseg = nseg;
+    r.accumulate = accumulate;
+    if (first < 1) return cudaSuccess;
+    k_reduce_partials<<<unsigned(first), 256, 0, st>>>(r);
     return cudaGetLastError();
 }
 

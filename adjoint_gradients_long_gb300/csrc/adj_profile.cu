@@ -22,8 +22,8 @@ std::vector<Rec> g_recs[K_COUNT];
 std::vector<cudaEvent_t> g_pool;
 
 const char *g_names[K_COUNT] = {"proj_in", "fwd_scan", "proj_out", "loss", "cot_proj", "win_scan",
-                                "bwd_scan", "param_dW_in", "param_dW_o", "splitk_reduce", "colsum",
-                                "input_grad", "rms_norm", "rms_norm_bwd"};
+                                "bwd_scan", "param_dW_in", "param_dW_o", "param_reduce", "colsum",
+                                "input_grad", "rms_norm", "rms_norm_bwd", "weight_prep"};
 
 cudaEvent_t take() {
     if (!g_pool.empty()) {

@@ -14,11 +14,12 @@ enum KernelId {
     K_BWD_SCAN,
     K_PARAM_DWIN,
     K_PARAM_DWO,
-    K_SPLITK,
+    K_PARAM_REDUCE,
     K_COLSUM,
     K_INPUT_GRAD,
     K_RMS_NORM,
     K_RMS_NORM_BWD,
+    K_WEIGHT_PREP,
     K_COUNT
 };
 

@@ -242,7 +242,7 @@ __device__ __forceinline__ float4 srow(const float *s, int r, int lane) {
 // Composite of a token range: h_out = A h_in + H.  (A2,H2) after (A1,H1) = (A2 A1, A2 H1 + H2).
 // Staged: a and u, rows [c0, c0 + 8L).
 template <int L>
-__global__ void __launch_bounds__(256, (L <= 8 ? 3 : L <= 12 ? 2 : 1)) k_fwd_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ h,
+__global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 1)) k_fwd_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ h,
                                                   int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
                                                   ScanWs d, unsigned *status) {
     constexpr int TT = SC_WARPS * L;
@@ -339,7 +339,7 @@ __device__ __forceinline__ FwdSeg fseg_then(const FwdSeg &X, const FwdSeg &Y) {
 
 // Staged: g, c and a, rows [c0, c0 + 8L).
 template <int L>
-__global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_win_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ R,
+__global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1)) k_win_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ R,
                                                   int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
                                                   int64_t W, ScanWs d, unsigned *status) {
     constexpr int TT = SC_WARPS * L;
@@ -442,7 +442,7 @@ __device__ __forceinline__ RevSeg rseg_then(const RevSeg &X, const RevSeg &Y) {
 // before the staging wait.  D_c and E are written right after pass 1, before the
 // look-back; D_u and D_a in pass 2.
 template <int L, bool TRUNC, typename TD>
-__global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 8 ? 2 : 1)) k_bwd_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
+__global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1)) k_bwd_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
                                                   const float *__restrict__ R, TD *__restrict__ Da,
                                                   TD *__restrict__ Du, TD *__restrict__ Dc, TD *__restrict__ E,
                                                   int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,

@@ -57,9 +57,13 @@ def test_noalloc_matches_workspace_path(L):
             assert rel_fro(out[k].cpu().numpy(), ref[k].cpu().numpy()) <= 1e-4, (call, k)
 
 
-def test_noalloc_rejects_problems_beyond_its_scratch(L):
+@pytest.mark.parametrize("B,T", [(1024, 16384), (64, 16383)])   # fused and unfused forward
+def test_noalloc_rejects_problems_beyond_its_scratch(L, B, T):
     from adjoint_gradients_long_gb300 import lib
-    d = lib.dims(64, 16384, 128, 256)          # needs far more than the 32 MiB array
+    d = lib.dims(B, T, 128, 256)
+    # the call below gets 64-float stand-ins for every array: it must be a problem whose
+    # workspace exceeds the 32 MiB array, so that it is rejected before any launch
+    assert L.adj_workspace_bytes(ctypes.byref(d), lib.OP_FWD, 0) > (32 << 20)
     t = torch.zeros(64, dtype=torch.float32, device="cuda")
     w = lib.weights(t, t, t)
     p = t.data_ptr()
