@@ -158,7 +158,7 @@ def kernel_table(P, N, xb, db, trunc):
 # was captured at; None when no summary covers the kernel.
 PROFILE_OF = {"bwd_scan": "k_bwd_scan_ssm1_p128.md", "fwd_scan": "k_fwd_scan_ssm1_p128.md",
               "proj_in": "k_gemm_tc_proj_in_ssm1_p128.md", "proj_out": "k_gemm_tc_proj_out_ssm1_p128.md",
-              "param_dW_in": "k_gemm_tc_param_dWin_ssm1_p128.md"}
+              "cot_proj": "k_gemm_tc_cot_proj_ssm1_p128.md", "param_dW_in": "k_gemm_tc_param_dWin_ssm1_p128.md"}
 
 
 def profiled_traffic(name):
