@@ -132,6 +132,20 @@ class AdjStack:
         self.loss_grad(stream)
         self.backward(Tbar, stream)
 
+    def capture(self, Tbar=None):
+        """A CUDA graph of one step on these buffers (``replay()`` reruns it): the library
+        calls enqueue only kernels and memsets on the current stream, so the whole step
+        captures, and a replay skips the per-call host work and launch gaps."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.step(Tbar)                 # one eager step first: lazy initialisation off the capture
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        with torch.cuda.graph(g):
+            self.step(Tbar)
+        return g
+
     def status(self, stream=None) -> int:
         return lib.stream_status(self.ws, stream)
 

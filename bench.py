@@ -316,7 +316,9 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def timed(window, steps, profile=False):
+    def timed(window, steps, profile=False, graph=None, per_step=0):
+        """Per-step CUDA-event times of `steps` steps, each after an L2 flush: eager library
+        calls, or replays of a captured step (graph; its launches counted at capture)."""
         times = []
         n0 = lib.launch_count()
         if profile:
@@ -327,19 +329,38 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            st.step(window)
+            if graph is not None:
+                graph.replay()
+            else:
+                st.step(window)
             e1.record(stream)
             times.append((e0, e1))
         barrier()
         if profile:
             lib.profile_enable(False)
-        launches = lib.launch_count() - n0
+        launches = per_step * steps if graph is not None else lib.launch_count() - n0
         ms = [a.elapsed_time(b) for a, b in times]
         return ms, launches
 
     for _ in range(max(3, args.warmup)):
         st.step(None)
         st.step(TBAR)
+    barrier()
+    assert st.status() == 0
+
+    # The timed steps replay a CUDA graph of one step (the library enqueues only kernels and
+    # memsets on the caller's stream, so a step captures whole); the replay does the same
+    # work as the eager calls without their launch gaps.  Eager steps are timed too.
+    def capture(window):
+        n0 = lib.launch_count()
+        g = st.capture(window)
+        torch.cuda.synchronize(dev)
+        return g, (lib.launch_count() - n0) // 2     # capture() runs one eager step first
+    g_full, per_full = capture(None)
+    g_trunc, per_trunc = capture(TBAR)
+    for _ in range(max(3, args.warmup)):
+        g_full.replay()
+        g_trunc.replay()
     barrier()
     assert st.status() == 0
 
@@ -351,14 +372,15 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    ms_full, launches_full = timed(None, args.steps)
-    ms_trunc, launches_trunc = timed(TBAR, args.steps)
+    ms_full, launches_full = timed(None, args.steps, graph=g_full, per_step=per_full)
+    ms_trunc, launches_trunc = timed(TBAR, args.steps, graph=g_trunc, per_step=per_trunc)
     t_end = time.time() + 1.0      # keep the same load for a few clock samples if the region was short
     while time.time() < t_end:
-        st.step(None)
+        g_full.replay()
         torch.cuda.synchronize(dev)
     clk = clocks.stop()
     status = st.status()
+    ms_eager, _ = timed(None, args.steps)
 
     # per-kernel device time, recorded with CUDA events on the launching stream
     _, _ = timed(None, args.steps, profile=True)
@@ -378,9 +400,16 @@ def run_ours(args, rank, world, local_rank):
     # Inputs are double-buffered: step i+1's inputs are copied on a second stream while step
     # i computes; every step's copies stay inside the timed region.
     copy_stream = torch.cuda.Stream(dev)
-    bufs = [(st.x[0], st.target), (torch.empty_like(st.x[0]), torch.empty_like(st.target))]
+    bufs = [(st.x[0], st.target), (st.x[0].clone(), st.target.clone())]
     landed = [torch.cuda.Event(), torch.cuda.Event()]      # inputs of buffer b copied
     used = [torch.cuda.Event(), torch.cuda.Event()]        # step that read buffer b done
+    # one captured step per input buffer (a graph keeps the pointers it was captured with)
+    graphs = []
+    for b in range(2):
+        st.x[0], st.target = bufs[b]
+        graphs.append(st.capture(None))
+    st.x[0], st.target = bufs[0]
+    torch.cuda.synchronize(dev)
 
     def stage_inputs(b, after):
         copy_stream.wait_event(after)
@@ -396,11 +425,10 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.steps):
         b = i % 2
         stream.wait_event(landed[b])
-        st.x[0], st.target = bufs[b]
         if i + 1 < args.steps:
             # the other buffer was last read by step i-1
             stage_inputs(1 - b, used[1 - b] if i > 0 else e0)
-        st.step(None)
+        graphs[b].replay()
         used[b].record(stream)
         hl.copy_(st.loss, non_blocking=True)
         for hgt, dg in zip(hg, (st.dW_in[0], st.db_a[0], st.dW_o[0])):
@@ -413,6 +441,7 @@ def run_ours(args, rank, world, local_rank):
     # max over ranks
     mean_full = max_over_ranks(sum(ms_full) / len(ms_full), world, dev)
     mean_trunc = max_over_ranks(sum(ms_trunc) / len(ms_trunc), world, dev)
+    mean_eager = max_over_ranks(sum(ms_eager) / len(ms_eager), world, dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     tokens = B * T * K * world
 
@@ -473,7 +502,10 @@ def run_ours(args, rank, world, local_rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_full, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "B": B, "T": T, "P": P, "N": N, "K": K, "window": "full",
-                       "l2": "flushed before every timed step (256 MB write)", "tokens_per_step": tokens},
+                       "l2": "flushed before every timed step (256 MB write)", "tokens_per_step": tokens,
+                       "launch": "each step replays a CUDA graph of its library calls"},
+            "eager": {"ms_per_step": mean_eager, "value": tokens / (mean_eager * 1e-3),
+                      "note": "the same step as direct library calls (no graph)"},
             "truncated": {"window": TBAR, "value": tokens / (mean_trunc * 1e-3), "ms_per_step": mean_trunc,
                           "gpu_launches": launches_trunc},
             "gpu_launches": launches_full,

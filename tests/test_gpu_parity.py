@@ -122,3 +122,28 @@ def test_repeat_calls_agree_to_rounding():
         a, b = st1.grads_numpy(k), st2.grads_numpy(k)
         for nm in a:
             assert rel_fro(a[nm], b[nm]) <= 1e-6, nm
+
+
+def test_graph_replay_matches_eager_and_oracle():
+    """A captured step (a CUDA graph of the library calls, as the bench times it) replays the
+    same computation: its gradients match the eager step's to fp32 rounding and the oracle's
+    within the fp32 tolerance."""
+    from adjoint_gradients_long_gb300.stack import AdjStack
+    inputs = synth.make_inputs("ssm1_p128", T=512, B=2)
+    B, T, P, N, K = (inputs[k] for k in ("B", "T", "P", "N", "K"))
+    st = AdjStack(B, T, P, N, K, Tbar=128)
+    st.load(inputs)
+    st.step(None)
+    torch.cuda.synchronize()
+    eager = st.grads_numpy(0)
+    g = st.capture(None)
+    for t in (st.dW_in[0], st.db_a[0], st.dW_o[0]):
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    rep = st.grads_numpy(0)
+    ref = oracle.stack_grad(_layers64(inputs), inputs["xhat"], inputs["target"], None)["grads"][0]
+    for nm in eager:
+        assert rel_fro(rep[nm], eager[nm]) <= 1e-6, nm
+        assert rel_fro(rep[nm], ref["d" + nm]) <= TOL[False], nm
