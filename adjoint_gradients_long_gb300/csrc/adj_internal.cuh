@@ -79,13 +79,12 @@ __device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
 // ---------------------------------------------------------------- launchers
 struct ScanWs {               // look-back descriptors carved from the workspace
     unsigned *ticket;         // 1 counter
-    unsigned *flags;          // [nseq * nchunks]
     float4 *agg0, *agg1;      // [nseq * nchunks * 32] chunk aggregates (2 components)
     float4 *inc0, *inc1;      // [nseq * nchunks * 32] inclusive prefixes
 };
 
 size_t scan_ws_bytes(int64_t B, int64_t T, int N);
-ScanWs scan_ws_carve(void *base, int64_t B, int64_t T, int N);
+ScanWs scan_ws_carve(void *base, int64_t nchunks_total);
 
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
                             void *scan_ws, unsigned *status, cudaStream_t st);

@@ -23,11 +23,18 @@
 // both passes read them from shared memory and HBM sees every input byte once.  Lane
 // = 4 channels (one float4 per token row), warp w = tokens [w*L, (w+1)*L) of the
 // chunk.  Pass 1 reduces each thread's L tokens to one composite map; the 8 warp
-// composites are combined in shared memory and warp 0 publishes the chunk aggregate
-// and looks back over its predecessors' descriptors (decoupled look-back).  Pass 2
-// applies the carry and writes the outputs.  Chunks are numbered by an atomic ticket
-// in scan order, so a CTA only ever waits for CTAs that started before it; every wait
-// is bounded.
+// composites are combined in shared memory and warp 0 publishes the chunk aggregate;
+// the CTA then looks back over its predecessors' descriptors (decoupled look-back).
+// Pass 2 applies the carry and writes the outputs.  Chunks are numbered by an atomic
+// ticket in scan order, so a CTA only ever waits for CTAs that started before it; every
+// wait is bounded.
+//
+// Descriptors carry no flags: before each launch every descriptor word is set to the
+// bit pattern 0xFFFFFFFF, a NaN that no arithmetic produces (results that are NaN come
+// out as the canonical 0x7FFFFFFF, and published values are canonicalised), and each
+// word is written exactly once per launch.  A reader that sees no sentinel in a
+// descriptor therefore holds its published value, so one L2 round trip both finds and
+// reads a predecessor's aggregate or inclusive prefix, and publishing needs no fence.
 #include <string.h>
 
 #include "adj_internal.cuh"
@@ -47,25 +54,22 @@ constexpr int SC_WARPS = 8;
 constexpr int SC_FWD_L = ADJ_SCAN_FWD_L, SC_BWD_L = ADJ_SCAN_BWD_L;
 constexpr int SC_SLICE = 128;        // channels per CTA
 constexpr int SC_MIN_CHUNK = 32;     // smallest chunk (L = 4); sizes the descriptor arrays
-constexpr unsigned F_AGG = 1u, F_INC = 2u;
+constexpr unsigned SC_EMPTY = 0xFFFFFFFFu;   // descriptor word not yet published
 
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-static inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t scan_ws_bytes(int64_t B, int64_t T, int N) {
     int64_t n = B * cdiv(N, SC_SLICE) * cdiv(T, SC_MIN_CHUNK);
-    return 256 + al256(size_t(n) * 4) + 4 * al256(size_t(n) * 32 * sizeof(float4));
+    return 256 + 4 * size_t(n) * 32 * sizeof(float4);
 }
 
-ScanWs scan_ws_carve(void *base, int64_t B, int64_t T, int N) {
-    int64_t n = B * cdiv(N, SC_SLICE) * cdiv(T, SC_MIN_CHUNK);
+// Ticket, then the four descriptor arrays of n = nseq * nchunks chunks, back to back.
+ScanWs scan_ws_carve(void *base, int64_t n) {
     char *p = static_cast<char *>(base);
     ScanWs d;
     d.ticket = reinterpret_cast<unsigned *>(p);
     p += 256;
-    d.flags = reinterpret_cast<unsigned *>(p);
-    p += al256(size_t(n) * 4);
-    size_t db = al256(size_t(n) * 32 * sizeof(float4));
+    const size_t db = size_t(n) * 32 * sizeof(float4);
     d.agg0 = reinterpret_cast<float4 *>(p); p += db;
     d.agg1 = reinterpret_cast<float4 *>(p); p += db;
     d.inc0 = reinterpret_cast<float4 *>(p); p += db;
@@ -73,22 +77,38 @@ ScanWs scan_ws_carve(void *base, int64_t B, int64_t T, int N) {
     return d;
 }
 
-// bytes of the ticket + flags prefix that must be zero before a launch
-static size_t scan_reset_bytes(int64_t B, int64_t T, int N) {
-    int64_t n = B * cdiv(N, SC_SLICE) * cdiv(T, SC_MIN_CHUNK);
-    return 256 + al256(size_t(n) * 4);
+// Before a launch over n chunks: ticket zero, every descriptor word empty.
+static cudaError_t scan_ws_reset(void *base, int64_t n, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(base, 0, 256, st);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(static_cast<char *>(base) + 256, 0xFF, 4 * size_t(n) * 32 * sizeof(float4), st);
 }
 
-// Publish one or two float4 per lane and then the flag (release after a fence).
-__device__ __forceinline__ void warp_publish(float4 *p0, float4 v0, float4 *p1, float4 v1,
-                                             unsigned *flag, unsigned fval, int lane) {
-    if (p0) st_cg4(p0, v0);
-    if (p1) st_cg4(p1, v1);
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release(flag, fval);
+__device__ __forceinline__ float canon(float x) {
+    return __float_as_uint(x) == SC_EMPTY ? __uint_as_float(0x7FFFFFFFu) : x;
 }
-
+__device__ __forceinline__ float4 canon4(float4 v) { return make_float4(canon(v.x), canon(v.y), canon(v.z), canon(v.w)); }
+__device__ __forceinline__ bool full4(float4 v) {
+    return __float_as_uint(v.x) != SC_EMPTY && __float_as_uint(v.y) != SC_EMPTY && __float_as_uint(v.z) != SC_EMPTY &&
+           __float_as_uint(v.w) != SC_EMPTY;
+}
+// Publish one or two float4 per lane (p1 may be null); no fence, no flag.
+__device__ __forceinline__ void desc_publish(float4 *p0, float4 v0, float4 *p1, float4 v1) {
+    if (p0) st_cg4(p0, canon4(v0));
+    if (p1) st_cg4(p1, canon4(v1));
+}
+// A descriptor slot as read: the value and whether every word of it was published.
+struct DescRead {
+    float4 a, b;
+    bool ok;
+};
+__device__ __forceinline__ DescRead desc_read(const float4 *p0, const float4 *p1) {
+    DescRead r;
+    r.a = p0 ? ld_cg4(p0) : f4(0.f);
+    r.b = ld_cg4(p1);
+    r.ok = (!p0 || full4(r.a)) && full4(r.b);
+    return r;
+}
 
 // ============================================================================ segment composites
 // Composite maps of token ranges (see each scan below).  Each packs into two float4
@@ -111,92 +131,92 @@ __device__ __forceinline__ void seg_get(float2x4 &c, float4 a, float4 b, bool) {
 __device__ __forceinline__ void seg_get(FwdSeg &c, float4 a, float4 b, bool cl) { c = FwdSeg{a, b, cl}; }
 __device__ __forceinline__ void seg_get(RevSeg &c, float4 a, float4 b, bool cl) { c = RevSeg{a, b, cl}; }
 
-// CTA-wide decoupled look-back (all threads call it).  Each round, warp 0 reads the
-// flags of the next 32 predecessors (nearest first: p0, p0 + dir, ...) and finds how
-// many published aggregates precede the nearest inclusive prefix (or the nearest
-// predecessor that has published nothing); then warp j folds predecessors 4j..4j+3 of
-// them, all warps' descriptor loads in flight at once (the last warp also loads the
-// inclusive prefix found), and warp 0 folds the 8 partial composites in order.  A round
-// costs about two L2 round trips however many aggregates it consumes.  extend(acc, agg)
-// composes one more (older) predecessor; finish(acc, inc) returns the carry.  sx, sy,
-// scl (8 x 32 entries), ix, iy (32 entries) and ctl (2 words) are shared scratch.  The
-// result is valid in warp 0; a wait that gives up finishes with zero_inc.
-constexpr int LB_MORE = 0, LB_WAIT = 1, LB_INC = 2, LB_END = 3, LB_TIMEOUT = 4;
-template <class C, class LA, class LI, class EX, class FI>
-__device__ __forceinline__ C cta_lookback(const unsigned *flags, int64_t p0, int dir, int64_t count, C ident,
-                                          LA load_agg, LI load_inc, EX extend, FI finish, C zero_inc,
-                                          unsigned *status, float4 (*sx)[32], float4 (*sy)[32], bool *scl, float4 *ix,
-                                          float4 *iy, int *ctl, int w, int lane) {
-    C acc = ident, result = zero_inc;
+// CTA-wide decoupled look-back (all threads call it).  Each round, warp j reads the
+// descriptors (aggregate and inclusive prefix) of predecessors done + 2j and
+// done + 2j + 1 (nearest first: p0, p0 + dir, ...), all sixteen in flight at once, and
+// folds them in order until an inclusive prefix (closed: the fold ends there), a
+// predecessor that has published nothing yet, or the end of the sequence (folds
+// zero_inc).  Warp 0 then folds the warps' partial composites in warp order up to the
+// first warp that stopped; a round costs one L2 round trip.  extend(acc, x) composes one
+// more (older) predecessor, or an inclusive prefix, into acc.  load(p) returns the slot's
+// aggregate and inclusive prefix as read.  sx, sy, scl (8 x 32) and ctl (8 + 2 words) are
+// shared scratch.  The carry is valid in warp 0; a wait that gives up records the timeout
+// and finishes with zero_inc.
+constexpr int LB_PER = 2;   // predecessors a warp examines per round
+template <class C, class LD, class EX>
+__device__ __forceinline__ C cta_lookback(int64_t p0, int dir, int64_t count, C ident, LD load, EX extend, C zero_inc,
+                                          unsigned *status, float4 (*sx)[32], float4 (*sy)[32], bool *scl, int *ctl,
+                                          int w, int lane) {
+    C acc = ident;
     int64_t done = 0;
-    bool wait_first = false;
     for (int round = 0; round < SPIN_LIMIT; ++round) {
-        if (w == 0) {
-            int m = 0, state;
-            unsigned ok = 1;
-            if (wait_first) {
-                if (lane == 0) ok = wait_flag(&flags[p0 + dir * done], status);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-            }
-            if (!ok) {
-                state = LB_TIMEOUT;
+        // this warp's predecessors: all loads first
+        C ag[LB_PER], ic[LB_PER];
+        bool aok[LB_PER], iok[LB_PER];
+#pragma unroll
+        for (int i = 0; i < LB_PER; ++i) {
+            const int64_t j = done + LB_PER * w + i;
+            aok[i] = iok[i] = false;
+            if (j < count) load(p0 + dir * j, ag[i], aok[i], ic[i], iok[i]);
+        }
+        C part = ident;
+        int stop = 0;   // 0: all folded, 1: closed (inclusive prefix or sequence end), 2: missing
+        int used = 0;
+#pragma unroll
+        for (int i = 0; i < LB_PER; ++i) {
+            if (stop) break;
+            const int64_t j = done + LB_PER * w + i;
+            if (j >= count) {
+                part = extend(part, zero_inc);
+                stop = 1;
+            } else if (__all_sync(0xffffffffu, iok[i])) {
+                part = extend(part, ic[i]);
+                stop = 1;
+            } else if (__all_sync(0xffffffffu, aok[i])) {
+                part = extend(part, ag[i]);
+                ++used;
             } else {
-                const bool exists = done + lane < count;
-                const unsigned f = exists ? ld_acquire(&flags[p0 + dir * (done + lane)]) : 0u;
-                const unsigned incl = __ballot_sync(0xffffffffu, exists && f == F_INC);
-                const unsigned miss = __ballot_sync(0xffffffffu, exists && f == 0u);
-                const int ji = incl ? __ffs(int(incl)) - 1 : 32, jm = miss ? __ffs(int(miss)) - 1 : 32;
-                m = ji < jm ? ji : jm;
-                if (int64_t(m) > count - done) m = int(count - done);
-                state = (ji < jm && ji == m) ? LB_INC : (done + m >= count) ? LB_END : (m == 0 ? LB_WAIT : LB_MORE);
-            }
-            if (lane == 0) {
-                ctl[0] = m;
-                ctl[1] = state;
+                stop = 2;
             }
         }
-        __syncthreads();   // orders the other warps' descriptor loads after warp 0's flag acquires
-        const int m = ctl[0], state = ctl[1];
-        if (state == LB_TIMEOUT) {
-            result = finish(acc, zero_inc);
-            break;
-        }
-        if (m > 4 * w) {
-            C t[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (4 * w + i < m) t[i] = load_agg(p0 + dir * (done + 4 * w + i));
-            C part = ident;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (4 * w + i < m) part = extend(part, t[i]);
-            bool cl;
-            seg_put(part, sx[w][lane], sy[w][lane], cl);
-            if (lane == 0) scl[w] = cl;
-        }
-        if (state == LB_INC && w == SC_WARPS - 1) {
-            bool cl;
-            seg_put(load_inc(p0 + dir * (done + m)), ix[lane], iy[lane], cl);
+        bool cl;
+        seg_put(part, sx[w][lane], sy[w][lane], cl);
+        if (lane == 0) {
+            scl[w] = cl;
+            ctl[w] = stop | (used << 4);
         }
         __syncthreads();
         if (w == 0) {
-            for (int j = 0; j < SC_WARPS && 4 * j < m; ++j) {
-                C part;
-                seg_get(part, sx[j][lane], sy[j][lane], scl[j]);
-                acc = extend(acc, part);
+            int state = 0;   // 0: more rounds, 1: done, 2: poll again
+            int64_t adv = 0;
+            for (int j = 0; j < SC_WARPS; ++j) {
+                const int st = ctl[j] & 15, u = ctl[j] >> 4;
+                C pj;
+                seg_get(pj, sx[j][lane], sy[j][lane], scl[j]);
+                acc = extend(acc, pj);
+                adv += u;
+                if (st == 1) {
+                    state = 1;
+                    break;
+                }
+                if (st == 2) {
+                    state = 2;
+                    break;
+                }
             }
-            if (state == LB_INC) {
-                C inc;
-                seg_get(inc, ix[lane], iy[lane], true);
-                result = finish(acc, inc);
+            if (lane == 0) {
+                ctl[SC_WARPS] = state;
+                ctl[SC_WARPS + 1] = int(adv);
             }
-            else if (state == LB_END) result = finish(acc, zero_inc);
         }
-        done += m;
-        if (state == LB_INC || state == LB_END) break;
-        wait_first = state == LB_WAIT;
+        __syncthreads();
+        const int state = ctl[SC_WARPS];
+        done += ctl[SC_WARPS + 1];
+        if (state == 1) return acc;
+        if (state == 2 && round > 8) __nanosleep(64);
     }
-    return result;
+    record_timeout(status);
+    return extend(acc, zero_inc);
 }
 
 // ============================================================================ chunk staging
@@ -251,9 +271,9 @@ __global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 
     __shared__ unsigned s_ticket;
     __shared__ uint64_t s_bar;
     __shared__ int s_abort;
-    __shared__ float4 sA[SC_WARPS][32], sH[SC_WARPS][32], sC[32], sI0[32], sI1[32];
+    __shared__ float4 sA[SC_WARPS][32], sH[SC_WARPS][32], sC[32];
     __shared__ bool s_cl[SC_WARPS];
-    __shared__ int s_ctl[2];
+    __shared__ int s_ctl[SC_WARPS + 2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tk = chunk_ticket(d, &s_ticket, &s_bar, &s_abort), chunk = tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
@@ -294,23 +314,28 @@ __global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 
             cH = fma4(sA[j][lane], cH, sH[j][lane]);
             cA = cA * sA[j][lane];
         }
-        if (chunk > 0) warp_publish(&d.agg0[di * 32 + lane], cA, &d.agg1[di * 32 + lane], cH, &d.flags[di], F_AGG, lane);
+        if (chunk > 0) desc_publish(&d.agg0[di * 32 + lane], cA, &d.agg1[di * 32 + lane], cH);
     }
     __syncthreads();   // sA/sH now serve as look-back scratch
     float4 carry = f4(0.f);
     if (chunk > 0) {
         // acc = composite of the chunks between the inclusive prefix found and this chunk
         const float2x4 r = cta_lookback<float2x4>(
-            d.flags + fb, chunk - 1, -1, chunk, float2x4{f4(1.f), f4(0.f)},
-            [&](int64_t p) { return float2x4{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane])}; },
-            [&](int64_t p) { return float2x4{f4(0.f), ld_cg4(&d.inc1[(fb + p) * 32 + lane])}; },
+            chunk - 1, -1, chunk, float2x4{f4(1.f), f4(0.f)},
+            [&](int64_t p, float2x4 &ag, bool &aok, float2x4 &ic, bool &iok) {
+                const DescRead A = desc_read(&d.agg0[(fb + p) * 32 + lane], &d.agg1[(fb + p) * 32 + lane]);
+                const DescRead I = desc_read(nullptr, &d.inc1[(fb + p) * 32 + lane]);
+                ag = float2x4{A.a, A.b};
+                aok = A.ok;
+                ic = float2x4{f4(0.f), I.b};   // inclusive: h at the chunk end, closed
+                iok = I.ok;
+            },
             [](const float2x4 &acc, const float2x4 &g) { return float2x4{acc.x * g.x, fma4(acc.x, g.y, acc.y)}; },
-            [](const float2x4 &acc, const float2x4 &inc) { return float2x4{f4(0.f), fma4(acc.x, inc.y, acc.y)}; },
-            float2x4{f4(0.f), f4(0.f)}, status, sA, sH, s_cl, sI0, sI1, s_ctl, w, lane);
+            float2x4{f4(0.f), f4(0.f)}, status, sA, sH, s_cl, s_ctl, w, lane);
         carry = r.y;
     }
     if (w == 0) {
-        warp_publish(nullptr, f4(0.f), &d.inc1[di * 32 + lane], fma4(cA, carry, cH), &d.flags[di], F_INC, lane);
+        desc_publish(nullptr, f4(0.f), &d.inc1[di * 32 + lane], fma4(cA, carry, cH));
         sC[lane] = carry;
     }
     __syncthreads();
@@ -348,9 +373,9 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     __shared__ unsigned s_ticket;
     __shared__ uint64_t s_bar;
     __shared__ int s_abort;
-    __shared__ float4 sP[SC_WARPS][32], sS[SC_WARPS][32], sCP[32], sCS[32], sI0[32], sI1[32];
+    __shared__ float4 sP[SC_WARPS][32], sS[SC_WARPS][32], sCP[32], sCS[32];
     __shared__ bool sCl[SC_WARPS];
-    __shared__ int s_ctl[2];
+    __shared__ int s_ctl[SC_WARPS + 2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tk = chunk_ticket(d, &s_ticket, &s_bar, &s_abort), chunk = tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
@@ -389,24 +414,29 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
         for (int j = 1; j < SC_WARPS; ++j) agg = fseg_then(agg, FwdSeg{sP[j][lane], sS[j][lane], sCl[j]});
         // A closed aggregate is already the inclusive composite: publish it before looking
         // back.  The look-back still runs, for the tokens before the chunk's first block start.
-        if (agg.cl) warp_publish(&d.inc0[di * 32 + lane], agg.P, &d.inc1[di * 32 + lane], agg.S, &d.flags[di], F_INC, lane);
-        else warp_publish(&d.agg0[di * 32 + lane], agg.P, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
+        if (agg.cl) desc_publish(&d.inc0[di * 32 + lane], agg.P, &d.inc1[di * 32 + lane], agg.S);
+        else desc_publish(&d.agg0[di * 32 + lane], agg.P, &d.agg1[di * 32 + lane], agg.S);
     }
     __syncthreads();   // sP/sS/sCl now serve as look-back scratch
     FwdSeg carry{f4(1.f), f4(0.f), true};
     if (chunk > 0) {
         carry = cta_lookback<FwdSeg>(
-            d.flags + fb, chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
-            [&](int64_t p) { return FwdSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
-            [&](int64_t p) { return FwdSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
+            chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
+            [&](int64_t p, FwdSeg &ag, bool &aok, FwdSeg &ic, bool &iok) {
+                const DescRead A = desc_read(&d.agg0[(fb + p) * 32 + lane], &d.agg1[(fb + p) * 32 + lane]);
+                const DescRead I = desc_read(&d.inc0[(fb + p) * 32 + lane], &d.inc1[(fb + p) * 32 + lane]);
+                ag = FwdSeg{A.a, A.b, false};
+                aok = A.ok;
+                ic = FwdSeg{I.a, I.b, true};
+                iok = I.ok;
+            },
             [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
-            [](const FwdSeg &acc, const FwdSeg &inc) { return fseg_then(inc, acc); },
-            FwdSeg{f4(1.f), f4(0.f), true}, status, sP, sS, sCl, sI0, sI1, s_ctl, w, lane);
+            FwdSeg{f4(1.f), f4(0.f), true}, status, sP, sS, sCl, s_ctl, w, lane);
     }
     if (w == 0) {
         if (!agg.cl) {
             const FwdSeg inc = fseg_then(carry, agg);
-            warp_publish(&d.inc0[di * 32 + lane], inc.P, &d.inc1[di * 32 + lane], inc.S, &d.flags[di], F_INC, lane);
+            desc_publish(&d.inc0[di * 32 + lane], inc.P, &d.inc1[di * 32 + lane], inc.S);
         }
         sCP[lane] = carry.P;
         sCS[lane] = carry.S;
@@ -453,9 +483,9 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     __shared__ unsigned s_ticket;
     __shared__ uint64_t s_bar;
     __shared__ int s_abort;
-    __shared__ float4 sQ[SC_WARPS][32], sS[SC_WARPS][32], sCQ[32], sCS[32], sI0[32], sI1[32];
+    __shared__ float4 sQ[SC_WARPS][32], sS[SC_WARPS][32], sCQ[32], sCS[32];
     __shared__ bool sCl[SC_WARPS];
-    __shared__ int s_ctl[2];
+    __shared__ int s_ctl[SC_WARPS + 2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tk = chunk_ticket(d, &s_ticket, &s_bar, &s_abort), chunk = nchunks - 1 - tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
@@ -503,8 +533,8 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
         for (int j = 1; j < SC_WARPS; ++j) agg = rseg_then(agg, RevSeg{sQ[j][lane], sS[j][lane], sCl[j]});
         // A closed aggregate is already the inclusive composite: publish it before looking
         // back.  The look-back still runs, for the tokens after the chunk's last block end.
-        if (agg.cl) warp_publish(&d.inc0[di * 32 + lane], agg.Q, &d.inc1[di * 32 + lane], agg.S, &d.flags[di], F_INC, lane);
-        else warp_publish(&d.agg0[di * 32 + lane], agg.Q, &d.agg1[di * 32 + lane], agg.S, &d.flags[di], F_AGG, lane);
+        if (agg.cl) desc_publish(&d.inc0[di * 32 + lane], agg.Q, &d.inc1[di * 32 + lane], agg.S);
+        else desc_publish(&d.agg0[di * 32 + lane], agg.Q, &d.agg1[di * 32 + lane], agg.S);
     }
     // D_c = g h and E = c h need no carry: store them now, so these writes overlap the
     // look-back (after warp 0's publish, whose fence would otherwise wait for them).  The
@@ -532,17 +562,22 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     RevSeg carry{f4(0.f), f4(0.f), true};
     if (chunk + 1 < nchunks) {
         carry = cta_lookback<RevSeg>(
-            d.flags + fb, chunk + 1, 1, nchunks - 1 - chunk, RevSeg{f4(1.f), f4(0.f), false},
-            [&](int64_t p) { return RevSeg{ld_cg4(&d.agg0[(fb + p) * 32 + lane]), ld_cg4(&d.agg1[(fb + p) * 32 + lane]), false}; },
-            [&](int64_t p) { return RevSeg{ld_cg4(&d.inc0[(fb + p) * 32 + lane]), ld_cg4(&d.inc1[(fb + p) * 32 + lane]), true}; },
+            chunk + 1, 1, nchunks - 1 - chunk, RevSeg{f4(1.f), f4(0.f), false},
+            [&](int64_t p, RevSeg &ag, bool &aok, RevSeg &ic, bool &iok) {
+                const DescRead A = desc_read(&d.agg0[(fb + p) * 32 + lane], &d.agg1[(fb + p) * 32 + lane]);
+                const DescRead I = desc_read(&d.inc0[(fb + p) * 32 + lane], &d.inc1[(fb + p) * 32 + lane]);
+                ag = RevSeg{A.a, A.b, false};
+                aok = A.ok;
+                ic = RevSeg{I.a, I.b, true};
+                iok = I.ok;
+            },
             [](const RevSeg &acc, const RevSeg &g) { return rseg_then(acc, g); },
-            [](const RevSeg &acc, const RevSeg &inc) { return rseg_then(acc, inc); },
-            RevSeg{f4(0.f), f4(0.f), true}, status, sQ, sS, sCl, sI0, sI1, s_ctl, w, lane);
+            RevSeg{f4(0.f), f4(0.f), true}, status, sQ, sS, sCl, s_ctl, w, lane);
     }
     if (w == 0) {
         if (!agg.cl) {
             const RevSeg inc = rseg_then(agg, carry);
-            warp_publish(&d.inc0[di * 32 + lane], inc.Q, &d.inc1[di * 32 + lane], inc.S, &d.flags[di], F_INC, lane);
+            desc_publish(&d.inc0[di * 32 + lane], inc.Q, &d.inc1[di * 32 + lane], inc.S);
         }
         sCQ[lane] = carry.Q;
         sCS[lane] = carry.S;
@@ -603,8 +638,8 @@ cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B,
     const float *arr[2] = {a, u};
     const int rows[2] = {TT, TT};
     if (!scan_maps(mp, 2, arr, rows, B, T, N)) return cudaErrorInvalidValue;
-    ScanWs d = scan_ws_carve(scan_ws, B, T, N);
-    cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
+    ScanWs d = scan_ws_carve(scan_ws, nseq * nchunks);
+    cudaError_t e = scan_ws_reset(scan_ws, nseq * nchunks, st);
     if (e != cudaSuccess) return e;
     const size_t smem = staged_bytes(2 * TT);
     if ((e = set_smem(k_fwd_scan<L>, smem)) != cudaSuccess) return e;
@@ -621,8 +656,8 @@ cudaError_t launch_win_scan(const float *g, const float *c, const float *a, floa
     const float *arr[3] = {g, c, a};
     const int rows[3] = {TT, TT, TT};
     if (!scan_maps(mp, 3, arr, rows, B, T, N)) return cudaErrorInvalidValue;
-    ScanWs d = scan_ws_carve(scan_ws, B, T, N);
-    cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
+    ScanWs d = scan_ws_carve(scan_ws, nseq * nchunks);
+    cudaError_t e = scan_ws_reset(scan_ws, nseq * nchunks, st);
     if (e != cudaSuccess) return e;
     const size_t smem = staged_bytes(3 * TT);
     if ((e = set_smem(k_win_scan<L>, smem)) != cudaSuccess) return e;
@@ -641,8 +676,8 @@ cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, cons
     const float *arr[4] = {g, c, a, R};
     const int rows[4] = {TT, TT, TT + 1, TT};
     if (!scan_maps(mp, trunc ? 4 : 3, arr, rows, B, T, N)) return cudaErrorInvalidValue;
-    ScanWs d = scan_ws_carve(scan_ws, B, T, N);
-    cudaError_t e = cudaMemsetAsync(scan_ws, 0, scan_reset_bytes(B, T, N), st);
+    ScanWs d = scan_ws_carve(scan_ws, nseq * nchunks);
+    cudaError_t e = scan_ws_reset(scan_ws, nseq * nchunks, st);
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(nseq * nchunks);
     const size_t smem = staged_bytes(3 * TT + 1);
