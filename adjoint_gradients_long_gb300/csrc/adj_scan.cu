@@ -141,7 +141,7 @@ __device__ __forceinline__ void seg_get(RevSeg &c, float4 a, float4 b, bool cl) 
 // more (older) predecessor, or an inclusive prefix, into acc.  load(p) returns the slot's
 // aggregate and inclusive prefix as read.  sx, sy, scl (8 x 32) and ctl (8 + 2 words) are
 // shared scratch.  The carry is valid in warp 0; a wait that gives up records the timeout
-// and finishes with zero_inc.
+// and finishes with zero_inc (so does one that sees another CTA's recorded timeout).
 constexpr int LB_PER = 2;   // predecessors a warp examines per round
 template <class C, class LD, class EX>
 __device__ __forceinline__ C cta_lookback(int64_t p0, int dir, int64_t count, C ident, LD load, EX extend, C zero_inc,
@@ -204,6 +204,10 @@ __device__ __forceinline__ C cta_lookback(int64_t p0, int dir, int64_t count, C 
                     break;
                 }
             }
+            // still waiting: give up early once any CTA has recorded a timeout (the
+            // predecessor may never publish)
+            if (state == 2 && (round & 255) == 255 && *reinterpret_cast<volatile unsigned *>(status) != 0u)
+                state = 3;
             if (lane == 0) {
                 ctl[SC_WARPS] = state;
                 ctl[SC_WARPS + 1] = int(adv);
@@ -213,6 +217,7 @@ __device__ __forceinline__ C cta_lookback(int64_t p0, int dir, int64_t count, C 
         const int state = ctl[SC_WARPS];
         done += ctl[SC_WARPS + 1];
         if (state == 1) return acc;
+        if (state == 3) return extend(acc, zero_inc);
         if (state == 2 && round > 8) __nanosleep(64);
     }
     record_timeout(status);
