@@ -60,7 +60,7 @@ int colsum_blocks(const adj_dims *d) {
 }
 int loss_blocks(int64_t count) {
     int64_t n = cdiv(count, 256 * 8);
-    if (n > 1024) n = 1024;
+    if (n > 608) n = 608;                 // four blocks on each of the 152 SMs
     return n < 1 ? 1 : int(n);
 }
 

@@ -142,8 +142,9 @@ cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *
 // partials z = w, w + 8, ... (eight loads in flight, every load a 512-byte row segment)
 // and the eight warp sums are added in warp order.  Narrow arrays with many partials
 // (the column sums): an output float4 is owned by a group of G lanes (a power of two, at
-// most 32, so that a lane loads at most eight partials at a time); lane g sums z = g,
-// g + G, ... and a butterfly of shuffles combines the group.  The order of every addition
+// most 32, so that a lane loads at most eight partials at a time), or by a whole block
+// when 32 lanes would need more; lane g sums z = g, g + G, ... and a butterfly of
+// shuffles combines the group (then shared memory, in warp order, for a block).  The order of every addition
 // is fixed, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(256) k_reduce_partials(RedArgs r) {
     // the array by explicit selection (an indexed parameter array would go to local memory)
@@ -177,6 +178,38 @@ __global__ void __launch_bounds__(256) k_reduce_partials(RedArgs r) {
             float4 t = red[0][lane];
 #pragma unroll
             for (int k = 1; k < 8; ++k) t = t + red[k][lane];
+            if (r.accumulate) t = out[q] + t;
+            out[q] = t;
+        }
+        return;
+    }
+    if (G == 256) {
+        // one block per output float4: thread t sums z = t, t + 256, ..., then a shuffle
+        // butterfly in each warp and the eight warp sums in warp order
+        const int64_t q = blk;
+        const float4 *p = part + q;
+        float4 s = f4(0.f);
+        for (int z0 = threadIdx.x; z0 < splits; z0 += 8 * 256) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int z = z0 + u * 256;
+                v[u] = z < splits ? __ldcs(p + int64_t(z) * n4) : f4(0.f);
+            }
+            s = s + (((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7])));
+        }
+        for (int o = 1; o < 32; o <<= 1) {
+            s.x += __shfl_xor_sync(0xffffffffu, s.x, o);
+            s.y += __shfl_xor_sync(0xffffffffu, s.y, o);
+            s.z += __shfl_xor_sync(0xffffffffu, s.z, o);
+            s.w += __shfl_xor_sync(0xffffffffu, s.w, o);
+        }
+        if (lane == 0) red[w][0] = s;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float4 t = red[0][0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k) t = t + red[k][0];
             if (r.accumulate) t = out[q] + t;
             out[q] = t;
         }
@@ -218,13 +251,14 @@ cudaError_t launch_reduce_partials(const RedSeg *segs, int nseg, int accumulate,
     for (int k = 0; k < nseg; ++k) {
         r.seg[k] = segs[k];
         int G = 0;                                   // 0: warps over the partials
-        if (segs[k].n4 < 4096) {                     // narrow: lane groups
+        if (segs[k].n4 < 4096) {                     // narrow: lane groups, or whole blocks
             G = 1;
             while (G < 32 && (segs[k].splits + G - 1) / G > 8) G <<= 1;
+            if ((segs[k].splits + G - 1) / G > 8) G = 256;
         }
         r.seg[k].group = G;
         r.seg[k].first = first;                      // first block of the array
-        first += G == 0 ? (segs[k].n4 + 31) / 32 : (segs[k].n4 * G + 255) / 256;
+        first += G == 0 ? (segs[k].n4 + 31) / 32 : G == 256 ? segs[k].n4 : (segs[k].n4 * G + 255) / 256;
     }
     r.nseg = nseg;
     r.accumulate = accumulate;
