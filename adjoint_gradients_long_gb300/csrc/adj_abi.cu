@@ -3,6 +3,8 @@
 // sources are documented in include/adj.h.
 #include <string.h>
 
+#include <algorithm>
+
 #include "adj_internal.cuh"
 #include "adj_profile.cuh"
 
@@ -101,7 +103,7 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
     case ADJ_OP_PARAM: {
         L.part0 = off; off += al256(size_t(splits_in(d)) * d->P * 3 * d->N * 4);
         L.part1 = off; off += al256(size_t(splits_o(d)) * d->N * d->P * 4);
-        L.part2 = off; off += al256(size_t(colsum_blocks(d)) * d->N * 4);
+        L.part2 = off; off += al256(size_t(std::max(colsum_blocks(d), 2 * splits_in(d))) * d->N * 4);
         L.wsplit = off; off += win_s;
         break;
     }
@@ -338,18 +340,23 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
     int su_in = s_in, su_o = s_o;   // split counts the launches took (at most the above)
     float *part_in = reinterpret_cast<float *>(at(ws, L.part0));
     float *part_o = reinterpret_cast<float *>(at(ws, L.part1));
-    // dW_in = xhat^T [D_a | D_u | D_c]
+    // dW_in = xhat^T [D_a | D_u | D_c]; with fp32 seeds the producers also sum D_a's
+    // columns (db_a partials, two a split) while they convert the raw tiles
+    float *part_c = reinterpret_cast<float *>(at(ws, L.part2));
     GemmEpilogue e = epi(Epi::Partial);
     e.out0 = part_in;
+    e.csum = part_c;
+    e.csum_n = N;
+    bool csum_done = false;
     {
         ProfScope ps(K_PARAM_DWIN, st);
         ADJ_CUDA(launch_gemm_tc(P, 3 * int64_t(N), BT, op1(xhat, 1, P, xbf), op3(D_a, D_u, D_c, N, 1, N, dbf), e, s_in,
-                                !xbf, status_word(ws), st, &su_in));
+                                !xbf, status_word(ws), st, &su_in, &csum_done));
     }
-    // db_a = sum_t D_a: block partials while D_a is still partly in L2
-    float *part_c = reinterpret_cast<float *>(at(ws, L.part2));
-    const int ncs = colsum_blocks(dims);
-    {
+    // otherwise db_a = sum_t D_a: block partials while D_a is still partly in L2
+    int ncs = 2 * su_in;
+    if (!csum_done) {
+        ncs = colsum_blocks(dims);
         ProfScope ps(K_COLSUM, st);
         ADJ_CUDA(launch_colsum(D_a, dbf, BT, N, part_c, ncs, st));
     }

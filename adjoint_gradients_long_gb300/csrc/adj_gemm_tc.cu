@@ -380,8 +380,11 @@ __device__ __forceinline__ void put4(uint8_t *hi, uint8_t *lo, int r, int k4, fl
     }
 }
 
+// With csum (row-contiguous tiles only) it returns the sum, in a fixed order, of the raw
+// values of the thread's row r = ptid % 128 (column sums of a token-major operand); else 0.
 template <bool SPLIT, bool MN, bool MUL = false, int NP = TC_PROD>
-__device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
+__device__ __forceinline__ float convert_raw128(uint8_t *region, int ptid, bool csum = false) {
+    float rsum = 0.f;
     constexpr int R = TC_BM;
     const float *raw = reinterpret_cast<const float *>(region);
     if (!MN) {
@@ -419,6 +422,13 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
                 for (int j = 0; j < 8; ++j) v[i][j] = src[(kc * 8 + j) * 64];
             }
         }
+        if (csum) {
+            static_assert(NP % R == 0, "a thread keeps one row");
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) rsum += v[i][j];
+        }
         asm volatile("bar.sync 1, %0;" ::"r"(NP) : "memory");
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
@@ -426,6 +436,7 @@ __device__ __forceinline__ void convert_raw128(uint8_t *region, int ptid) {
             if (ITEMS % NP == 0 || it < ITEMS) put8<SPLIT>(region, region + R * 128, it % R, it / R, v[i]);
         }
     }
+    return rsum;
 }
 
 // Shared-memory layout.  A stage holds the A region then (unless B is resident) the B
@@ -601,6 +612,10 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             mbar_arrive(smem_u32(bready));
         }
         const bool any_raw = a_raw || b_raw;
+        // column sums of B's first ep.csum_n columns (the raw row-contiguous B of a
+        // one-tile-per-CTA split-K product): row ptid % 128 of each 128-row half
+        const bool csum_on = args.ep.csum && b_raw && args.b_ld == LD_RAW_MN && args.ep.kind == Epi::Partial;
+        float csum0 = 0.f, csum1 = 0.f;
         int64_t kbg = 0;   // k-blocks staged so far (ring position)
         for (int64_t t = blockIdx.x; t < ntiles && ok && prod_full; t += gridDim.x) {
             int64_t m0, n0, kb0, ke;
@@ -643,15 +658,32 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     if (b_raw) {
                         // a 256-row B tile converts as two independent 128-row halves
                         const bool bmn = args.b_ld == LD_RAW_MN;
-                        for (uint8_t *bh = sbb; bh < sbb + BN * 256; bh += 2 * TC_BM * 128) {
-                            if (bmn) convert_raw128<SPLIT, true>(bh, ptid);
-                            else convert_raw128<SPLIT, false>(bh, ptid);
+                        int half = 0;
+                        for (uint8_t *bh = sbb; bh < sbb + BN * 256; bh += 2 * TC_BM * 128, ++half) {
+                            if (bmn) {
+                                const float rs = convert_raw128<SPLIT, true>(bh, ptid, csum_on);
+                                if (half == 0) csum0 += rs;
+                                else csum1 += rs;
+                            } else {
+                                convert_raw128<SPLIT, false>(bh, ptid);
+                            }
                         }
                     }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full[s]));
             }
+        }
+        if (csum_on && ok) {
+            // this CTA's one tile: column n0 + 128 h + r; the two threads of a row hold the
+            // even and the odd k chunks: partial [2 z + ptid / 128][n] for n < csum_n
+            int64_t m0, n0, kb0, ke;
+            int z;
+            tile_of(blockIdx.x, m0, n0, z, kb0, ke);
+            float *out = args.ep.csum + (2 * int64_t(z) + ptid / TC_BM) * args.ep.csum_n;
+            const int64_t n = n0 + ptid % TC_BM;
+            if (n < args.ep.csum_n) out[n] = csum0;
+            if (BN > TC_BM && n + TC_BM < args.ep.csum_n) out[n + TC_BM] = csum1;
         }
     }
     if (warp == TC_TMA_WARP) {
@@ -1011,7 +1043,8 @@ static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cuda
 
 cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
                            const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
-                           int *splits_used) {
+                           int *splits_used, bool *csum_done) {
+    if (csum_done) *csum_done = false;
     if (M <= 0 || Nc <= 0) return cudaSuccess;
     if (splits < 1) splits = 1;
     if (g_num_sms == 0) {
@@ -1081,6 +1114,11 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;
     if (grid < a.n_tiles) grid = a.n_tiles;
     if (grid > ntiles) grid = ntiles;
+    // the fused column sums need a raw row-contiguous B, streamed, and one tile per CTA
+    const bool csum = ep.csum && ep.kind == Epi::Partial && a.b_ld == LD_RAW_MN && !a.b_res && grid == ntiles &&
+                      ep.csum_n > 0 && ep.csum_n <= Nc;
+    if (!csum) a.ep.csum = nullptr;
+    if (csum_done) *csum_done = csum;
     const bool need_regs = a.a_ld == LD_REG || (!a.b_res && a.b_ld == LD_REG) || (a.b_res && !ld_tma(a.b_ld));
     if (!need_regs) {
         if (split3) return launch_tc_t<false, false, true, false>(a, unsigned(grid), smem, st);

@@ -121,6 +121,11 @@ struct GemmEpilogue {
     int N;                      // ProjIn: width of each block
     bool interleave;            // ProjIn: product column chunk j (32 columns) is block j % 3,
                                 // channels 32 (j / 3) ...; needs N % 32 == 0 (see prep_win)
+    // Partial with a row-contiguous fp32 B converted by the producers: also the column sums
+    // of B's first csum_n columns, csum [2 * splits][csum_n] (two partials a split).  The
+    // launch reports whether it took them (csum_done); otherwise csum is left untouched.
+    float *csum;
+    int64_t csum_n;
 };
 
 // ProjIn output column n of the product -> block (0 a, 1 u, 2 c) and channel.
@@ -139,7 +144,7 @@ __host__ __device__ inline void projin_col(const GemmEpilogue &ep, int n, int &b
 // split3: fp32-accurate hi/lo bf16 split, otherwise bf16 operands.
 cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
                            const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
-                           int *splits_used = nullptr);
+                           int *splits_used = nullptr, bool *csum_done = nullptr);
 
 // W_in [P, 3N] with its columns interleaved in 32-column chunks (chunk j of the copy =
 // columns 32 (j / 3) ... of block j % 3, so every wide output tile mixes the a, u and c
