@@ -240,14 +240,19 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
     e.out0 = a; e.out1 = u; e.out2 = c; e.bias = w->b_a; e.N = N;
     cudaError_t err = cudaSuccess;
     GemmOperand Win;
+    // W_o's bf16 hi/lo split (fp32 weights), made with W_in's copy when there is one
+    __nv_bfloat16 *wo_hi = reinterpret_cast<__nv_bfloat16 *>(at(ws, L.wsplit + al256(size_t(P) * 3 * N * (xbf ? 2 : 4))));
+    bool wo_done = false;
     if (N % 32 == 0) {
         // interleave the a, u, c column chunks so every output tile carries a share of the
         // sigmoid (the epilogue maps the chunks back)
         __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(at(ws, L.wsplit));
         __nv_bfloat16 *lo = xbf ? nullptr : hi + int64_t(P) * 3 * N;
+        wo_done = y && !xbf;
         {
             ProfScope pw(K_WEIGHT_PREP, st);
-            ADJ_CUDA(launch_prep_win(w->W_in, xbf, P, N, hi, lo, st));
+            ADJ_CUDA(launch_prep_win(w->W_in, xbf, P, N, hi, lo, st, wo_done ? static_cast<const float *>(w->W_o) : nullptr,
+                                     wo_hi, wo_hi + int64_t(N) * P));
         }
         Win = op1(hi, 1, 3 * int64_t(N), true);
         if (lo) Win.lo[0] = Win.lo[1] = Win.lo[2] = lo;
@@ -271,9 +276,14 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
         e2.out0 = y; e2.out_x = y_x; e2.ld = P;
         e2.add = xres ? static_cast<const void *>(xres) : xhat;
         e2.add_bf16 = !xres && xbf;
-        const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, xbf, at(ws, L.wsplit + al256(size_t(P) * 3 * N * (xbf ? 2 : 4))),
-                                   1, P, st, &err);
-        ADJ_CUDA(err);
+        GemmOperand Wo;
+        if (wo_done) {
+            Wo = op1(wo_hi, 1, P, true);
+            Wo.lo[0] = Wo.lo[1] = Wo.lo[2] = wo_hi + int64_t(N) * P;
+        } else {
+            Wo = opw(w->W_o, int64_t(N) * P, xbf, wo_hi, 1, P, st, &err);
+            ADJ_CUDA(err);
+        }
         ProfScope ps(K_PROJ_OUT, st);
         ADJ_CUDA(launch_gemm_tc(BT, P, N, op1(c, N, 1, false, h), Wo, e2, 1, !xbf, status_word(ws), st));
     }

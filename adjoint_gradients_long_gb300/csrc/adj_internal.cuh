@@ -149,8 +149,10 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
 // W_in [P, 3N] with its columns interleaved in 32-column chunks (chunk j of the copy =
 // columns 32 (j / 3) ... of block j % 3, so every wide output tile mixes the a, u and c
 // blocks): fp32 weights -> bf16 hi and lo copies, bf16 weights -> a bf16 copy (lo null).
+// With wo (fp32 [N, P]), the same launch also splits W_o into wo_hi and wo_lo.
 cudaError_t launch_prep_win(const void *w, bool w_bf16, int P, int N, __nv_bfloat16 *hi, __nv_bfloat16 *lo,
-                            cudaStream_t st);
+                            cudaStream_t st, const float *wo = nullptr, __nv_bfloat16 *wo_hi = nullptr,
+                            __nv_bfloat16 *wo_lo = nullptr);
 // hi = bf16(w), lo = bf16(w - hi) for n fp32 values (operands of the split-precision GEMM)
 cudaError_t launch_split_bf16(const float *w, int64_t n, __nv_bfloat16 *hi, __nv_bfloat16 *lo, cudaStream_t st);
 // One array of partials to reduce: out[i] (+)= sum_{z < splits} part[z * 4 n4 + i] over

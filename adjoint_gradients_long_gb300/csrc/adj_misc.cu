@@ -279,8 +279,17 @@ __global__ void __launch_bounds__(256) k_split_bf16(const float *__restrict__ w,
 }
 
 __global__ void __launch_bounds__(256) k_prep_win(const void *__restrict__ w, bool w_bf16, int P, int N,
-                                                  __nv_bfloat16 *__restrict__ hi, __nv_bfloat16 *__restrict__ lo) {
+                                                  __nv_bfloat16 *__restrict__ hi, __nv_bfloat16 *__restrict__ lo,
+                                                  const float *__restrict__ wo, int64_t n_wo,
+                                                  __nv_bfloat16 *__restrict__ wo_hi, __nv_bfloat16 *__restrict__ wo_lo) {
     const int64_t n3 = 3 * int64_t(N), total = int64_t(P) * n3;
+    // the forward's other weight in the same launch: W_o split into bf16 hi and lo
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_wo; i += int64_t(gridDim.x) * blockDim.x) {
+        const float x = wo[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        wo_hi[i] = h;
+        wo_lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+    }
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t p = i / n3;
         const int c = int(i - p * n3), j = c >> 5;
@@ -297,11 +306,12 @@ __global__ void __launch_bounds__(256) k_prep_win(const void *__restrict__ w, bo
 }
 
 cudaError_t launch_prep_win(const void *w, bool w_bf16, int P, int N, __nv_bfloat16 *hi, __nv_bfloat16 *lo,
-                            cudaStream_t st) {
+                            cudaStream_t st, const float *wo, __nv_bfloat16 *wo_hi, __nv_bfloat16 *wo_lo) {
     int64_t blocks = (int64_t(P) * 3 * N + 255) / 256;
     if (blocks > 1024) blocks = 1024;
     if (blocks < 1) return cudaSuccess;
-    k_prep_win<<<unsigned(blocks), 256, 0, st>>>(w, w_bf16, P, N, hi, lo);
+    const int64_t n_wo = wo ? int64_t(N) * P : 0;
+    k_prep_win<<<unsigned(blocks), 256, 0, st>>>(w, w_bf16, P, N, hi, lo, wo, n_wo, wo_hi, wo_lo);
     return cudaGetLastError();
 }
 

@@ -64,7 +64,7 @@ extern "C" adj_status adj_fwd_scan_noalloc(const adj_dims *dims, const adj_weigh
         return ADJ_ECUDA;
     // The status word must read zero at the start of every call: the array is
     // zero-initialised when the library is loaded, and each call clears it after use.
-    // The look-back flags are cleared by the scan launcher itself.
+    // The look-back descriptors are reset by the scan launcher itself.
     if (cudaMemsetAsync(ws, 0, adj::WS_HEADER, st) != cudaSuccess) return ADJ_ECUDA;
     return ADJ_OK;
 }

@@ -77,11 +77,10 @@ ScanWs scan_ws_carve(void *base, int64_t n) {
     return d;
 }
 
-// Before a launch over n chunks: ticket zero, every descriptor word empty.
+// Before a launch over n chunks, one memset: every descriptor word empty, and the ticket
+// 0xFFFFFFFF (a CTA's chunk is the value it read plus one).
 static cudaError_t scan_ws_reset(void *base, int64_t n, cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(base, 0, 256, st);
-    if (e != cudaSuccess) return e;
-    return cudaMemsetAsync(static_cast<char *>(base) + 256, 0xFF, 4 * size_t(n) * 32 * sizeof(float4), st);
+    return cudaMemsetAsync(base, 0xFF, 256 + 4 * size_t(n) * 32 * sizeof(float4), st);
 }
 
 __device__ __forceinline__ float canon(float x) {
@@ -238,7 +237,7 @@ __device__ __forceinline__ float *smem_1k(uint8_t *p) {
 // Take the chunk ticket and set up the staging barrier (thread 0), then the CTA syncs.
 __device__ __forceinline__ unsigned chunk_ticket(const ScanWs &d, unsigned *s_ticket, uint64_t *bar, int *abort_flag) {
     if (threadIdx.x == 0) {
-        *s_ticket = atomicAdd(d.ticket, 1u);
+        *s_ticket = atomicAdd(d.ticket, 1u) + 1u;   // the reset leaves 0xFFFFFFFF: first ticket 0
         mbar_init(smem_u32(bar), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
