@@ -22,7 +22,10 @@
  *    read by adj_stream_status(); zero them once (cudaMemset) before first use.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Calls are asynchronous on that stream.  Calls sharing one `ws` must be
- *    ordered on one stream.
+ *    ordered on one stream.  A call enqueues only kernels and memsets on the
+ *    stream (no allocation, no host synchronisation), so a sequence of calls can
+ *    be captured into a CUDA graph and replayed; the graph keeps the pointers
+ *    and sizes it was captured with.
  *  - Every argument is validated on the host before anything is launched; on an
  *    error nothing is launched and nothing is written.  Launch failures return
  *    ADJ_ECUDA.  Bounded device-side waits that give up record ADJ_ETIMEOUT in
