@@ -147,3 +147,29 @@ def test_graph_replay_matches_eager_and_oracle():
     for nm in eager:
         assert rel_fro(rep[nm], eager[nm]) <= 1e-6, nm
         assert rel_fro(rep[nm], ref["d" + nm]) <= TOL[False], nm
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_param_grad_accumulate_adds(bf16):
+    """accumulate = 1 adds a call's parameter gradients to the arrays: a second backward
+    pass over the same step doubles dW_in, db_a and dW_o (fp32 seeds: db_a comes from the
+    dW_in GEMM's producers; bf16 seeds: from the column-sum kernel)."""
+    from adjoint_gradients_long_gb300.stack import AdjStack
+    if bf16:
+        inputs = synth.make_inputs("ssm8_p512", T=200, B=1, P=64, N=32, K=1)
+    else:
+        inputs = synth.make_inputs("ssm1_p128", T=300, B=2)
+    B, T, P, N, K = (inputs[k] for k in ("B", "T", "P", "N", "K"))
+    st = AdjStack(B, T, P, N, K, x_bf16=bf16, d_bf16=bf16)
+    st.load(inputs)
+    st.forward()
+    st.loss_grad()
+    st.backward(None)
+    torch.cuda.synchronize()
+    once = st.grads_numpy(0)
+    st.backward(None, accumulate=True)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    twice = st.grads_numpy(0)
+    for nm in once:
+        assert rel_fro(twice[nm], 2.0 * once[nm]) <= 1e-5, nm
