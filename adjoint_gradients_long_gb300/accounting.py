@@ -4,7 +4,10 @@
 sharding for very long context training of state space models" (Referee Report,
 major comment on Section 4.5): storing {A_t, C_t, h_t, y_t} for T tokens and K
 layers costs T K (2N + P) + T P values.  ``stored_bytes`` is what this library
-actually keeps per layer: a, c, h in fp32 plus the layer input xhat.
+actually keeps per layer: a, c, h in fp32 plus the layer input xhat.  For comparison
+(the page's central claim is a memory saving over backpropagation, Referee Report major
+comment 3), ``bptt_saved_bytes`` counts what reverse-mode differentiation of the same
+stack must save, and ``checkpoint_saved_bytes`` the peak with activation checkpointing.
 """
 from __future__ import annotations
 
@@ -18,6 +21,27 @@ def stored_bytes(B: int, T: int, K: int, N: int, P: int, x_bytes: int) -> int:
     """Bytes this library keeps between the forward and the backward pass: per layer and
     token, a, c, h (3N fp32) and the layer input xhat (P values of x_bytes each)."""
     return B * T * K * (3 * N * 4 + P * x_bytes)
+
+
+def bptt_saved_bytes(B: int, T: int, K: int, N: int, P: int, x_bytes: int) -> int:
+    """Bytes reverse-mode differentiation of the same stack keeps from the forward pass when
+    every operation saves only what its own derivative reads, per layer and token:
+    the layer input xhat (the three input projections' weight gradients, P values of
+    x_bytes), the gate a (the sigmoid's derivative and the recurrence's dh_{t-1}), the state
+    h (h_{t-1} for the recurrence's da_t, h_t for the product c . h), c (the product), and the
+    product c . h (the output projection's weight gradient): 4N fp32 values."""
+    return B * T * K * (4 * N * 4 + P * x_bytes)
+
+
+def checkpoint_saved_bytes(B: int, T: int, K: int, N: int, P: int, x_bytes: int, segment: int = 0) -> int:
+    """Peak bytes kept by reverse-mode differentiation with activation checkpointing (the
+    input of every segment-th layer is kept; a segment's activations are recomputed during
+    the backward pass and held only while it is differentiated): the kept fp32 residual
+    streams (P values a token each) plus one segment's saved bytes.  segment defaults to the
+    integer nearest sqrt(K)."""
+    s = segment if segment > 0 else max(1, int(round(K ** 0.5)))
+    kept = -(-K // s) * B * T * P * 4
+    return kept + bptt_saved_bytes(B, T, min(s, K), N, P, x_bytes)
 
 
 def step_bytes(P: int, N: int, x_bytes: int, d_bytes: int, window: bool, stacked: bool) -> dict:

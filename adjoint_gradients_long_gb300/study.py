@@ -16,6 +16,13 @@ not depend on the window (their VJPs involve no product of A_t); they are report
 check of the run's own reproducibility.
 
     python -m adjoint_gradients_long_gb300.study --T 16384 --B 4 --P 128 --N 256
+
+``memory_report`` measures the device memory a full-size step of each workload takes through
+the library, beside the stored-state counts of ``accounting`` (this library, reverse-mode
+differentiation, and reverse mode with activation checkpointing): the page's central claim
+is a memory saving over backpropagation ([AS] Referee Report, major comment 3).
+
+    python -m adjoint_gradients_long_gb300.study --memory
 """
 from __future__ import annotations
 
@@ -66,6 +73,37 @@ def truncation_errors(B: int, T: int, P: int, N: int, b_a_values, windows, seed:
     return rows
 
 
+def memory_report(key: str, window=None, device="cuda") -> dict:
+    """Device memory of one full-size step of workload `key` through the library (every
+    buffer the stack driver allocates: stored states, residual streams, seeds, cotangents,
+    gradients and the workspace), beside the stored-state counts of ``accounting``."""
+    import torch
+    from . import accounting, synth
+    from .stack import AdjStack
+
+    w = synth.workload(key)
+    xb = 2 if w.x_dtype == "bf16" else 4
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(device)
+    base = torch.cuda.memory_allocated(device)
+    st = AdjStack(w.B, w.T, w.P, w.N, w.K, x_bf16=xb == 2, d_bf16=xb == 2, device=device,
+                  Tbar=window if window is not None and window < w.T else None)
+    st.load(synth.make_inputs(w))
+    st.step(window)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated(device) - base
+    ok = st.status() == 0
+    out = {"workload": key, "window": window if window is not None else "full", "B": w.B, "T": w.T, "K": w.K,
+           "P": w.P, "N": w.N, "device_peak_bytes": int(peak), "workspace_bytes": int(st.ws_bytes),
+           "stored_bytes": accounting.stored_bytes(w.B, w.T, w.K, w.N, w.P, xb),
+           "bptt_saved_bytes": accounting.bptt_saved_bytes(w.B, w.T, w.K, w.N, w.P, xb),
+           "checkpoint_saved_bytes": accounting.checkpoint_saved_bytes(w.B, w.T, w.K, w.N, w.P, xb),
+           "device_status_ok": ok}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--B", type=int, default=4)
@@ -75,9 +113,15 @@ def main(argv=None):
     ap.add_argument("--b-a", type=float, nargs="+", default=[1.0, 2.0, 3.0, 4.0])
     ap.add_argument("--windows", type=int, nargs="+", default=[16, 64, 256, 1024, 2048, 4096])
     ap.add_argument("--seed", type=int, default=2024)
+    ap.add_argument("--memory", action="store_true", help="device memory of each workload's step instead")
     args = ap.parse_args(argv)
     from . import build
     build.build()
+    if args.memory:
+        from . import synth
+        for key, w in synth.WORKLOADS.items():
+            print(json.dumps(memory_report(key, w.windows[0])), flush=True)
+        return
     for row in truncation_errors(args.B, args.T, args.P, args.N, args.b_a, args.windows, seed=args.seed):
         print(json.dumps(row), flush=True)
 

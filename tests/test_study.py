@@ -67,3 +67,18 @@ def test_study_matches_oracle_errors():
             assert abs(row["err_" + p] - ref) <= 0.02 * ref + 1e-5, (row, p, ref)
         for p in ("W_c", "W_o"):
             assert row["err_" + p] <= 1e-5, (row, p)
+
+
+def test_storage_counts_relations():
+    """Stored-state counts: a stack of one layer gains nothing from checkpointing (it keeps
+    its input and the whole layer); a deep stack keeps less with it than reverse mode does;
+    reverse mode saves the product c . h beyond this library's a, c, h, xhat."""
+    from adjoint_gradients_long_gb300 import accounting as A
+    B, T, N, P = 2, 1000, 256, 128
+    for xb in (2, 4):
+        assert A.checkpoint_saved_bytes(B, T, 1, N, P, xb) == B * T * P * 4 + A.bptt_saved_bytes(B, T, 1, N, P, xb)
+        assert A.checkpoint_saved_bytes(B, T, 100, N, P, xb) < A.bptt_saved_bytes(B, T, 100, N, P, xb)
+        assert A.checkpoint_saved_bytes(B, T, 100, N, P, xb, segment=100) == (
+            B * T * P * 4 + A.bptt_saved_bytes(B, T, 100, N, P, xb))
+        for K in (1, 8, 100):
+            assert A.bptt_saved_bytes(B, T, K, N, P, xb) - A.stored_bytes(B, T, K, N, P, xb) == B * T * K * N * 4
