@@ -31,13 +31,13 @@ __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float4 r = a[u] - b[u];
-            if (gy) st_stream4(gy + 4 * (i + u * stride), r);
+            if (gy) st4(gy + 4 * (i + u * stride), r);   // kept in L2: the cotangent projection reads gy next
             s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
         }
     }
     for (; i < n4; i += stride) {
         const float4 r = ld_stream4(y + 4 * i) - ld_stream4(tg + 4 * i);
-        if (gy) st_stream4(gy + 4 * i, r);
+        if (gy) st4(gy + 4 * i, r);
         s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
     }
     for (int64_t i = 4 * n4 + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count;

@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 
         const int64_t t = t0 + k;
         if (t >= T) break;
         hc = fma4(srow(sa, w * L + k, lane), hc, srow(su, w * L + k, lane));
-        if (act) st_stream4(h + base + t * N, hc);
+        if (act) st4(h + base + t * N, hc);   // kept in L2: the output projection reads h next
     }
 }
 
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
         const float4 ev = srow(sg, r, lane) * srow(sc, r, lane), av = srow(sa, r, lane);
         if (t % W == 0) G = FwdSeg{f4(1.f), ev, true};
         else G = FwdSeg{G.P * av, fma4(G.P * av, ev, G.S), G.cl};
-        if (act) st_stream4(R + base + t * N, G.S);
+        if (act) st4(R + base + t * N, G.S);   // kept in L2: the reverse scan reads R next
     }
 }
 
