@@ -41,8 +41,6 @@ __device__ __forceinline__ void st_cg4(float4 *p, float4 v) { __stcg(p, v); }
 // streaming loads/stores of the big token-major arrays
 __device__ __forceinline__ float4 ld_stream4(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
 __device__ __forceinline__ float4 ld_keep4(const float *p) { return __ldg(reinterpret_cast<const float4 *>(p)); }
-// first of two reads: cache in L2 only (the second read, ld_stream4, is the last use)
-__device__ __forceinline__ float4 ld_l2keep4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
 __device__ __forceinline__ void st_stream4(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
 
 __device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
