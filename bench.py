@@ -49,10 +49,18 @@ def load_peaks():
     if os.path.exists(path):
         try:
             d = json.load(open(path))
-            def find(keys):
+
+            def find(keys, node=None, depth=0):
+                # a top-level number, else the first one found one or two levels down
+                node = d if node is None else node
                 for k in keys:
-                    if k in d and isinstance(d[k], (int, float)):
-                        return float(d[k])
+                    if isinstance(node, dict) and isinstance(node.get(k), (int, float)):
+                        return float(node[k])
+                if depth < 2 and isinstance(node, dict):
+                    for v in node.values():
+                        r = find(keys, v, depth + 1) if isinstance(v, dict) else None
+                        if r is not None:
+                            return r
                 return None
             hbm = find(["hbm_gbs", "hbm_GBps", "hbm_gb_s"])
             bf = find(["bf16_tflops", "bf16_TFLOPs"])
@@ -188,7 +196,8 @@ def roofline_of(name, ent, peaks, split3):
            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"] if gbs is not None else None, "traffic": None}
     if "achieved_tflops" not in ent:
         return hbm
-    tpk = peaks["bf16_tflops"] / (3.0 if split3 else 1.0)
+    # the GEMMs are timed inside a long step: the sustained (power-capped) bf16 figure
+    tpk = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / (3.0 if split3 else 1.0)
     ten = {"kernel": name, "bound": "tensor", "achieved": ent["achieved_tflops"], "peak": tpk, "unit": "TFLOP/s",
            "frac": ent["achieved_tflops"] / tpk, "traffic": None,
            "note": "fp32-accurate 3-term bf16 split: peak = bf16 peak / 3" if split3 else "bf16"}

@@ -48,6 +48,10 @@ def test_roofline_takes_the_closer_bound():
     assert r["bound"] == "tensor" and r["peak"] == pytest.approx(1900.0 / 3) and r["frac"] == pytest.approx(0.9)
     r = bench.roofline_of("g", {"achieved_gbs": 100.0, "achieved_tflops": 570.0}, peaks, split3=False)
     assert r["peak"] == pytest.approx(1900.0) and r["frac"] == pytest.approx(0.3)
+    # GEMMs are timed inside the step: the sustained bf16 figure when there is one
+    r = bench.roofline_of("g", {"achieved_gbs": 100.0, "achieved_tflops": 510.0},
+                          dict(peaks, bf16_tflops_sustained=1700.0), split3=False)
+    assert r["peak"] == pytest.approx(1700.0) and r["frac"] == pytest.approx(0.3)
 
 
 def test_kernel_table_counts_the_path_bytes():
