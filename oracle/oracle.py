@@ -41,11 +41,14 @@ _I64 = ctypes.c_int64
 
 
 def build(force: bool = False) -> str:
-    """Compile adj_oracle.c with gcc into oracle/_build/liborc.so."""
+    """Compile adj_oracle.c with gcc into oracle/_build/liborc.so (with OpenMP when the
+    compiler has it; the results do not depend on the thread count)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        base = ["gcc", "-O3", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        if subprocess.call(base[:1] + ["-fopenmp"] + base[1:], stderr=subprocess.DEVNULL) != 0:
+            subprocess.check_call(base)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -56,6 +59,8 @@ def _bind(path: str):
     lib.orc_layer_forward.restype = None
     lib.orc_layer_grad.argtypes = [_I64] * 5 + [ctypes.c_int] + [_D] * 16
     lib.orc_layer_grad.restype = _I64
+    lib.orc_threads.argtypes = [ctypes.c_int]
+    lib.orc_threads.restype = ctypes.c_int
     return lib
 
 
@@ -73,6 +78,11 @@ def _load():
         lib = _bind(build())
         _lib = lib
     return _lib
+
+
+def threads(n: int = 0) -> int:
+    """Set the oracle's thread count (n > 0) and return the count in use."""
+    return int(_load().orc_threads(int(n)))
 
 
 def _p(x):

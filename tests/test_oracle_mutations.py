@@ -19,7 +19,7 @@ MUTATIONS = {
     "no_sigmoid_slope": ("a_i[n] * (1.0 - a_i[n])", "a_i[n]"),
     "dropped_db_a": ("db_a[n] += s_scratch[n];", ";"),
     "W_o_transposed": ("acc += gyb[t * P + p] * W_o[n * P + p];", "acc += gyb[t * P + p] * W_o[p * N + n];"),
-    "gate_index_shift": ("v[n] *= ab[i * N + n];", "v[n] *= ab[(i > 0 ? i - 1 : 0) * N + n];"),
+    "gate_index_shift": ("v[n] *= ab[i * 8 + n];", "v[n] *= ab[(i > 0 ? i - 1 : 0) * 8 + n];"),
     "literal_product_short": ("for (int64_t j = i + 1; j <= t; ++j)", "for (int64_t j = i + 1; j < t; ++j)"),
     "dx_sign": ("acc += s_scratch[n] * W_a[p * N + n] + v[n] * W_B[p * N + n];",
                 "acc -= s_scratch[n] * W_a[p * N + n] + v[n] * W_B[p * N + n];"),
