@@ -3,19 +3,27 @@
 the dominant kernel, an end-to-end number through the C ABI with host buffers, and
 the fp64 CPU oracle timed beside it.
 
-One step = one pass of the whole path over one batch of the workload
-ssm1_p128 (P=128, N=256, T=16384, B=4, one layer, fp32): adj_fwd_scan,
-adj_loss_mse, adj_bwd_full (or adj_bwd_trunc with Tbar=2048), adj_param_grad.
-The headline value is the full (exact) adjoint; the Tbar=2048 variant is reported
-beside it.  L2 is flushed (a 256 MB write) before every timed step.
+Headline workload: ssm4_p2048, the largest one that fits one GPU -- K = 4 residual
+layers, P = 2048, N = 256, T = 131072, B = 1, bf16 GEMM operands and fp32 scans,
+truncated adjoint with window Tbar = 8192.  One step = one pass of the whole path over
+one batch: for every layer adj_rms_norm (k >= 2) and adj_fwd_scan, then adj_loss_mse,
+then for every layer (top down) adj_bwd_trunc, adj_param_grad and adj_rms_norm_bwd
+(k >= 2).  The timed steps replay a CUDA graph of one step; L2 is flushed (a 256 MB
+write) before every timed step; ms_per_step is the median over the timed steps.
+
+The other workloads (ssm1_1m at both windows, ssm8_p512, ssm1_p128 at both windows)
+are measured the same way and reported under "workloads" as context lines.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun every rank runs its own batch (independent sequences: weak scaling,
 no collective on the data path); rank 0 prints one JSON line.
 """
 import argparse
+import glob
+import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -25,11 +33,14 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "ssm1_p128"
-TBAR = 2048
+HEADLINE = ("ssm4_p2048", 8192)
+CONTEXT = (("ssm1_1m", 4096), ("ssm1_1m", None), ("ssm8_p512", 4096), ("ssm1_p128", None), ("ssm1_p128", 2048))
 METRIC = "adjoint-gradient tokens/sec per layer on 1 GB300; % of HBM/tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-CPU_SAMPLE_T = 4096          # oracle sample: first CPU_SAMPLE_T tokens of one sequence
+# CPU oracle samples (prefixes of one sequence of the headline workload): all cores on
+# CPU_ALL_T tokens, one core on CPU_ONE_T tokens; the reference arm runs CPU_REF_T tokens
+# a step so that its warm-up and timed steps end within a few minutes
+CPU_ALL_T, CPU_ONE_T, CPU_REF_T = 4096, 1024, 1024
 
 
 def parse():
@@ -40,7 +51,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
-                    help="skip the short runs of the bf16 workloads reported under 'workloads'")
+                    help="skip the context lines of the other workloads")
+    ap.add_argument("--workload", default=None, help="run this workload as the headline instead (testing)")
     return ap.parse_args()
 
 
@@ -106,24 +118,33 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines):
+    """Median SM clock, maximum clock and the throttle reasons seen in nvidia-smi csv lines."""
+    sm, mx, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx.append(float(f[2]))
+        except ValueError:
+            continue
+        try:
+            power.append(float(f[3]))
+        except ValueError:
+            pass
+        for nm, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
 # ------------------------------------------------------------------ multi-rank reduction (weak scaling)
@@ -144,12 +165,16 @@ def weak_scaling_value(tokens_per_rank, world, ms_per_step_max):
 
 
 # ------------------------------------------------------------------ per-kernel algorithmic work
-def kernel_table(P, N, xb, db, trunc):
-    """Algorithmic bytes (and flops) per token of each kernel kind, as built."""
+def kernel_table(P, N, xb, db, trunc, K=1):
+    """Algorithmic bytes (and flops) per token of one launch of each kernel kind, as the
+    step runs it.  xb / db: bytes of a GEMM operand / of a VJP seed.  In a stack of K
+    layers the first layer's residual is its bf16 input and the others' the fp32 stream,
+    so proj_out's residual bytes are the mean over the K launches."""
+    res = (P * xb + (K - 1) * 4 * P) / K
     return {
         "proj_in": dict(bytes=P * xb + 3 * N * 4, flops=2 * P * 3 * N),
         "fwd_scan": dict(bytes=3 * N * 4),
-        "proj_out": dict(bytes=2 * N * 4 + P * xb + P * 4, flops=2 * N * P),
+        "proj_out": dict(bytes=2 * N * 4 + res + P * 4, flops=2 * N * P),
         "loss": dict(bytes=3 * P * 4),
         "cot_proj": dict(bytes=P * 4 + N * 4, flops=2 * P * N),
         "win_scan": dict(bytes=4 * N * 4),
@@ -157,221 +182,371 @@ def kernel_table(P, N, xb, db, trunc):
         "param_dW_in": dict(bytes=P * xb + 3 * N * db, flops=2 * P * 3 * N),
         "param_dW_o": dict(bytes=N * db + P * 4, flops=2 * N * P),
         "colsum": dict(bytes=N * db),
-        "input_grad": dict(bytes=3 * N * db + 2 * P * 4, flops=2 * 3 * N * P),
+        # in a stack the input gradient is stored alone (dxhat); with one layer it is added to gy
+        "input_grad": dict(bytes=3 * N * db + (4 * P if K > 1 else 2 * P * 4), flops=2 * 3 * N * P),
+        "rms_norm": dict(bytes=4 * P + P * xb + 4),
+        "rms_norm_bwd": dict(bytes=16 * P + 4),
     }
 
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel, from
-# the committed ncu summary of the bench workload (profiles/), with the code state it
-# was captured at; None when no summary covers the kernel.
-PROFILE_OF = {"bwd_scan": "k_bwd_scan_ssm1_p128.md", "fwd_scan": "k_fwd_scan_ssm1_p128.md",
-              "proj_in": "k_gemm_tc_proj_in_ssm1_p128.md", "proj_out": "k_gemm_tc_proj_out_ssm1_p128.md",
-              "cot_proj": "k_gemm_tc_cot_proj_ssm1_p128.md", "param_dW_in": "k_gemm_tc_param_dWin_ssm1_p128.md"}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel of a
+# workload, from the committed ncu summary (profiles/); each summary records a hash of the
+# library sources it was captured from, and a summary whose hash differs from the current
+# sources gives no traffic (the kernel has changed since).
+PROFILE_OF = {
+    ("ssm1_p128", "bwd_scan"): "k_bwd_scan_ssm1_p128.md",
+    ("ssm1_p128", "fwd_scan"): "k_fwd_scan_ssm1_p128.md",
+    ("ssm1_p128", "proj_in"): "k_gemm_tc_proj_in_ssm1_p128.md",
+    ("ssm1_p128", "proj_out"): "k_gemm_tc_proj_out_ssm1_p128.md",
+    ("ssm1_p128", "cot_proj"): "k_gemm_tc_cot_proj_ssm1_p128.md",
+    ("ssm1_p128", "param_dW_in"): "k_gemm_tc_param_dWin_ssm1_p128.md",
+    ("ssm4_p2048", "proj_in"): "k_gemm_tc_proj_in_ssm4_p2048.md",
+    ("ssm4_p2048", "param_dW_in"): "k_gemm_tc_param_dWin_ssm4_p2048.md",
+    ("ssm4_p2048", "proj_out"): "k_gemm_tc_proj_out_ssm4_p2048.md",
+    ("ssm4_p2048", "input_grad"): "k_gemm_tc_input_grad_ssm4_p2048.md",
+    ("ssm4_p2048", "bwd_scan"): "k_bwd_scan_ssm4_p2048.md",
+    ("ssm4_p2048", "rms_norm_bwd"): "k_rms_norm_bwd_ssm4_p2048.md",
+}
 
 
-def profiled_traffic(name):
-    fn = PROFILE_OF.get(name)
+def source_hash():
+    """Hash of the library sources (csrc and the public header), as recorded in profiles/."""
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "adjoint_gradients_long_gb300", "csrc", "*.cu*")))
+    files.append(os.path.join(ROOT, "include", "adj.h"))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, workload="ssm1_p128"):
+    """(bytes per launch, source hash of the capture, whether it matches the sources now);
+    (None, None, False) when no summary covers the kernel."""
+    fn = PROFILE_OF.get((workload, name))
     path = os.path.join(ROOT, "profiles", fn) if fn else None
     if not path or not os.path.exists(path):
-        return None, None
+        return None, None, False
     scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
-    tot, state = 0.0, None
+    tot, state, per_launch_scale = 0.0, None, 1.0
     for line in open(path):
         for key in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             if line.startswith("| " + key + " |"):
                 val, unit = line.split("|")[2].split()
                 tot += float(val) * scale[unit]
-        if line.startswith("Code state:"):
-            state = line.split(":", 1)[1].split("(")[0].strip().rstrip(".")
-    return (tot if tot > 0 else None), state
+        if line.startswith("Source hash:"):
+            state = line.split(":", 1)[1].strip().split()[0]
+        if line.startswith("Traffic scale:"):
+            per_launch_scale = float(line.split(":", 1)[1].strip().split()[0])
+    if tot <= 0:
+        return None, state, False
+    return tot * per_launch_scale, state, state == source_hash()
 
 
 def roofline_of(name, ent, peaks, split3):
     """Roofline entry of one kernel: HBM-bound kernels against the copy bandwidth; GEMMs
     against both the bandwidth and the tensor peak of their arithmetic (the fp32-accurate
     three-term bf16 split issues 3 bf16 MMAs per product, so its tensor peak is 1/3 of
-    bf16's), reporting the bound they sit closer to."""
+    bf16's), reporting the bound they sit closer to.  The tensor fraction is taken against
+    the burst bf16 peak; the fraction of the sustained (power-capped) figure is given
+    beside it."""
     gbs = ent.get("achieved_gbs")
     hbm = {"kernel": name, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
            "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"] if gbs is not None else None, "traffic": None}
     if "achieved_tflops" not in ent:
         return hbm
-    # the GEMMs are timed inside a long step: the sustained (power-capped) bf16 figure
-    tpk = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / (3.0 if split3 else 1.0)
+    div = 3.0 if split3 else 1.0
+    tpk = peaks["bf16_tflops"] / div
+    tps = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) / div
     ten = {"kernel": name, "bound": "tensor", "achieved": ent["achieved_tflops"], "peak": tpk, "unit": "TFLOP/s",
-           "frac": ent["achieved_tflops"] / tpk, "traffic": None,
+           "frac": ent["achieved_tflops"] / tpk, "peak_sustained": tps,
+           "frac_sustained": ent["achieved_tflops"] / tps, "traffic": None,
            "note": "fp32-accurate 3-term bf16 split: peak = bf16 peak / 3" if split3 else "bf16"}
     return ten if hbm["frac"] is None or ten["frac"] >= hbm["frac"] else hbm
 
 
+def kernels_summary(prof, tab, tokens, peaks, split3):
+    """Per kernel kind: launches, mean device time, share of the step and, where the kind
+    has an algorithmic count, achieved GB/s (TFLOP/s) and its roofline fraction."""
+    tot = sum(ms for _, ms in prof.values())
+    out = {}
+    for name, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        per = ms / n
+        ent = {"launches": n, "ms_per_launch": per, "share": ms / tot if tot else None}
+        if name in tab:
+            ent["algo_bytes_per_launch"] = tab[name]["bytes"] * tokens
+            ent["achieved_gbs"] = tab[name]["bytes"] * tokens / (per * 1e-3) / 1e9
+            ent["hbm_frac"] = ent["achieved_gbs"] / peaks["hbm_gbs"]
+            if "flops" in tab[name]:
+                ent["algo_flops_per_launch"] = tab[name]["flops"] * tokens
+                ent["achieved_tflops"] = tab[name]["flops"] * tokens / (per * 1e-3) / 1e12
+            r = roofline_of(name, ent, peaks, split3)
+            ent["roofline_bound"], ent["roofline_frac"] = r["bound"], r["frac"]
+        out[name] = ent
+    return out
+
+
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
-def oracle_sample(seconds_hint=False):
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_sample(T, threads, key=None, window=None):
+    """Seconds the fp64 oracle takes for one gradient step (forward, loss, adjoint with the
+    workload's window, parameter gradients) on the first T tokens of one sequence of the
+    workload, with `threads` threads (0: all cores).  Returns (tokens, seconds, threads)."""
     import numpy as np
     import oracle
     from adjoint_gradients_long_gb300 import synth
-    inp = synth.make_inputs(WORKLOAD, T=CPU_SAMPLE_T, B=1)
+    key = key or HEADLINE[0]
+    window = HEADLINE[1] if key == HEADLINE[0] and window is None else window
+    inp = synth.make_inputs(key, T=T, B=1)
     layers = [{k: np.asarray(v, np.float64) for k, v in W.items()} for W in inp["layers"]]
+    used = oracle.threads(threads if threads > 0 else (os.cpu_count() or 1))
     t0 = time.perf_counter()
-    oracle.stack_grad(layers, inp["xhat"], inp["target"], None, oracle.AGGREGATED)
+    oracle.stack_grad(layers, inp["xhat"], inp["target"], window, oracle.AGGREGATED)
     dt = time.perf_counter() - t0
-    return CPU_SAMPLE_T, dt
+    return T, dt, used
+
+
+def cpu_baseline(K):
+    """The oracle on the host cores: all cores on a CPU_ALL_T-token prefix (the value) and
+    one core on a CPU_ONE_T-token prefix (beside it), in tokens/s per layer."""
+    toks, dt, used = oracle_sample(CPU_ALL_T, 0)
+    toks1, dt1, _ = oracle_sample(CPU_ONE_T, 1)
+    key, window = HEADLINE
+    return {"value": toks * K / dt, "unit": "tokens/s per layer", "cores": used, "kind": "oracle",
+            "sample": f"first {toks} tokens of one sequence of {key} ({K} layers, window {window}: every "
+                      f"pair is inside it), aggregated-literal fp64 mode, {used} threads ({dt:.1f} s)",
+            "single_thread": {"value": toks1 * K / dt1, "unit": "tokens/s per layer",
+                              "sample": f"first {toks1} tokens, 1 thread ({dt1:.1f} s)"},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args, rank):
+    """The reference arm: the fp64 oracle (this path has no other reference code), one
+    step = one gradient step on a CPU_REF_T-token prefix of the headline workload."""
     if rank != 0:
         return
     import oracle
+    from adjoint_gradients_long_gb300 import synth
     oracle.build()
+    key, window = HEADLINE
+    K = synth.workload(key).K
     for _ in range(args.warmup):
-        oracle_sample()
-    times = []
-    toks = 0
+        oracle_sample(CPU_REF_T, 0)
+    times, used = [], 1
     for _ in range(args.steps):
-        toks, dt = oracle_sample()
+        _, dt, used = oracle_sample(CPU_REF_T, 0)
         times.append(dt)
-    mean = sum(times) / len(times)
-    value = toks / mean
+    med = statistics.median(times)
+    value = CPU_REF_T * K / med
+    sample = (f"first {CPU_REF_T} tokens of one sequence of {key} ({K} layers, window {window}), "
+              f"aggregated-literal fp64 mode, {used} threads")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s per layer", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": f"first {toks} tokens of one sequence", "window": "full"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"first {toks} tokens of one sequence of {WORKLOAD}, full window, "
-                                   "aggregated-literal mode, single thread"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": {"workload": key, "window": window, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s per layer", "cores": used, "kind": "oracle",
+                         "sample": sample, "nproc": os.cpu_count(), "cpu_model": cpu_model()},
+        "e2e": {"value": value, "unit": "tokens/s per layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-# ------------------------------------------------------------------ the other workloads (context lines)
-OTHER = (("ssm8_p512", 4096), ("ssm1_1m", 4096), ("ssm1_1m", None), ("ssm4_p2048", 8192))
+# ------------------------------------------------------------------ one workload on the GPU
+class Workload:
+    """Device buffers of one workload, its captured steps and the timing helpers."""
+
+    def __init__(self, key, window, dev, rank=0):
+        import torch
+        from adjoint_gradients_long_gb300 import synth
+        from adjoint_gradients_long_gb300.stack import AdjStack
+        self.torch = torch
+        self.w = synth.workload(key)
+        self.key, self.window, self.dev = key, window, dev
+        w = self.w
+        self.bf16 = w.x_dtype == "bf16"
+        self.inputs = synth.make_inputs(w, seed=w.seed + 7919 * rank)
+        self.st = AdjStack(w.B, w.T, w.P, w.N, w.K, x_bf16=self.bf16, d_bf16=self.bf16, Tbar=window, device=dev)
+        self.st.load(self.inputs)
+        self.stream = torch.cuda.current_stream(dev)
+        self.flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        self.tokens = w.B * w.T * w.K
+
+    def capture(self):
+        from adjoint_gradients_long_gb300 import lib
+        n0 = lib.launch_count()
+        g = self.st.capture(self.window)
+        self.torch.cuda.synchronize(self.dev)
+        return g, (lib.launch_count() - n0) // 2      # capture() runs one eager step first
+
+    def timed(self, steps, graph=None, profile=False, barrier=None):
+        """Per-step CUDA-event times of `steps` steps, each after an L2 flush: replays of a
+        captured step, or eager library calls."""
+        from adjoint_gradients_long_gb300 import lib
+        torch = self.torch
+        if profile:
+            lib.profile_reset()
+            lib.profile_enable(True)
+        if barrier:
+            barrier()
+        ev = []
+        for _ in range(steps):
+            self.flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                self.st.step(self.window)
+            e1.record(self.stream)
+            ev.append((e0, e1))
+        if barrier:
+            barrier()
+        torch.cuda.synchronize(self.dev)
+        if profile:
+            lib.profile_enable(False)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def kernels(self, steps, peaks):
+        from adjoint_gradients_long_gb300 import lib
+        self.timed(steps, profile=True)
+        prof = lib.profile_read()
+        lib.profile_reset()
+        w = self.w
+        trunc = self.window is not None and self.window < w.T
+        xb = 2 if self.bf16 else 4
+        tab = kernel_table(w.P, w.N, xb, xb, trunc, w.K)
+        return kernels_summary(prof, tab, w.B * w.T, peaks, split3=not self.bf16)
+
+    def e2e(self, steps, barrier):
+        """The same steps through the C ABI with host buffers: each step's inputs are copied
+        from pinned host memory (double-buffered on a second stream, so step i+1's copy
+        overlaps step i) and the loss and every parameter gradient are copied back."""
+        import numpy as np
+        from adjoint_gradients_long_gb300.synth import bf16_bits
+        torch, st, dev, stream = self.torch, self.st, self.dev, self.stream
+        if self.bf16:
+            bits = bf16_bits(np.ascontiguousarray(self.inputs["xhat"], np.float32)).view(np.int16)
+            hx = torch.from_numpy(bits).view(torch.bfloat16).pin_memory()
+        else:
+            hx = torch.from_numpy(np.ascontiguousarray(self.inputs["xhat"], np.float32)).pin_memory()
+        ht = torch.from_numpy(np.ascontiguousarray(self.inputs["target"], np.float32)).pin_memory()
+        hl = torch.empty(1, dtype=torch.float64).pin_memory()
+        grads = [t for k in range(st.K) for t in (st.dW_in[k], st.db_a[k], st.dW_o[k])]
+        hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grads]
+        h2d = hx.numel() * hx.element_size() + ht.numel() * 4
+        d2h = 8 + sum(t.numel() * 4 for t in hg)
+        copy_stream = torch.cuda.Stream(dev)
+        bufs = [(st.x[0], st.target), (st.x[0].clone(), st.target.clone())]
+        landed = [torch.cuda.Event(), torch.cuda.Event()]
+        used = [torch.cuda.Event(), torch.cuda.Event()]
+        graphs = []
+        for b in range(2):
+            st.x[0], st.target = bufs[b]
+            graphs.append(st.capture(self.window))
+        st.x[0], st.target = bufs[0]
+        torch.cuda.synchronize(dev)
+
+        def stage_inputs(b, after):
+            copy_stream.wait_event(after)
+            with torch.cuda.stream(copy_stream):
+                bufs[b][0].copy_(hx, non_blocking=True)
+                bufs[b][1].copy_(ht, non_blocking=True)
+                landed[b].record(copy_stream)
+
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        stage_inputs(0, e0)
+        for i in range(steps):
+            b = i % 2
+            stream.wait_event(landed[b])
+            if i + 1 < steps:
+                stage_inputs(1 - b, used[1 - b] if i > 0 else e0)
+            graphs[b].replay()
+            used[b].record(stream)
+            hl.copy_(st.loss, non_blocking=True)
+            for hgt, dg in zip(hg, grads):
+                hgt.copy_(dg, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        st.x[0], st.target = bufs[0]
+        del graphs, bufs
+        return e0.elapsed_time(e1) / steps, h2d, d2h
+
+    def release(self):
+        del self.st, self.flush, self.inputs
+        self.torch.cuda.empty_cache()
 
 
-def measure_workload(key, window, dev, peaks, steps=3, warmup=2):
-    """Short device-timed run of one of the bf16 workloads at full size (weak evidence:
-    few steps, L2 not flushed, inputs larger than L2).  Returns tokens/s per layer and
-    the per-kernel roofline entries."""
-    import torch
-    from adjoint_gradients_long_gb300 import lib, synth
-    from adjoint_gradients_long_gb300.stack import AdjStack
-    w = synth.workload(key)
-    inputs = synth.make_inputs(w)
-    st = AdjStack(w.B, w.T, w.P, w.N, w.K, x_bf16=True, d_bf16=True, Tbar=window, device=dev)
-    st.load(inputs)
-    del inputs
-    stream = torch.cuda.current_stream(dev)
+def context_line(key, window, dev, peaks, steps, warmup):
+    """One of the other workloads, measured like the headline (graph replay, L2 flushed
+    before every step, median), without the end-to-end and CPU legs."""
+    wl = Workload(key, window, dev)
     for _ in range(warmup):
-        st.step(window)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        st.step(window)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / steps
-    lib.profile_reset()
-    lib.profile_enable(True)
-    st.step(window)
-    torch.cuda.synchronize(dev)
-    lib.profile_enable(False)
-    prof = lib.profile_read()
-    lib.profile_reset()
-    status = st.status()
-    tab = kernel_table(w.P, w.N, 2, 2, window is not None and window < w.T)
-    tok = w.B * w.T
-    kern = {}
-    tot = sum(v[1] for v in prof.values())
-    for name, (n, t) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
-        per = t / n
-        ent = {"launches": n, "ms_per_launch": per, "share": t / tot}
-        if name in tab:
-            ent["achieved_gbs"] = tab[name]["bytes"] * tok / (per * 1e-3) / 1e9
-            if "flops" in tab[name]:
-                ent["achieved_tflops"] = tab[name]["flops"] * tok / (per * 1e-3) / 1e12
-            r = roofline_of(name, ent, peaks, split3=False)
-            ent["roofline_bound"], ent["roofline_frac"] = r["bound"], r["frac"]
-        kern[name] = ent
-    del st
-    torch.cuda.empty_cache()
-    return {"workload": key, "window": window if window is not None else "full", "B": w.B, "T": w.T, "P": w.P,
-            "N": w.N, "K": w.K, "dtype": "bf16 GEMM operands, fp32 scans",
-            "value": tok * w.K / (ms * 1e-3), "unit": "tokens/s per layer", "ms_per_step": ms, "steps": steps,
-            "device_status": lib.STATUS.get(status, status), "kernels": dict(list(kern.items())[:6])}
+        wl.st.step(window)
+    g, per = wl.capture()
+    for _ in range(warmup):
+        g.replay()
+    ms = wl.timed(steps, graph=g)
+    status = wl.st.status()
+    kern = wl.kernels(min(steps, 5), peaks)
+    w = wl.w
+    from adjoint_gradients_long_gb300 import lib
+    med = statistics.median(ms)
+    out = {"workload": key, "window": window if window is not None else "full", "B": w.B, "T": w.T, "P": w.P,
+           "N": w.N, "K": w.K, "dtype": "bf16 GEMM operands, fp32 scans" if wl.bf16 else "f32",
+           "value": wl.tokens / (med * 1e-3), "unit": "tokens/s per layer", "ms_per_step": med,
+           "ms_mean": sum(ms) / len(ms), "steps": steps, "gpu_launches_per_step": per,
+           "device_status": lib.STATUS.get(status, status), "kernels": kern}
+    del g
+    wl.release()
+    return out
 
 
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
-    import numpy as np
     import torch
     import torch.distributed as dist
-    from adjoint_gradients_long_gb300 import build as adj_build, lib, synth
-    from adjoint_gradients_long_gb300.stack import AdjStack
+    from adjoint_gradients_long_gb300 import build as adj_build, lib
 
     adj_build.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = synth.workload(WORKLOAD)
-    B, T, P, N, K = w.B, w.T, w.P, w.N, w.K
-    inputs = synth.make_inputs(w, seed=w.seed + 7919 * rank)
-    st = AdjStack(B, T, P, N, K, Tbar=TBAR, device=dev)
-    st.load(inputs)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    key, window = HEADLINE
+    if args.workload:
+        key, window = args.workload, None
+    peaks, peak_src = load_peaks()
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    def timed(window, steps, profile=False, graph=None, per_step=0):
-        """Per-step CUDA-event times of `steps` steps, each after an L2 flush: eager library
-        calls, or replays of a captured step (graph; its launches counted at capture)."""
-        times = []
-        n0 = lib.launch_count()
-        if profile:
-            lib.profile_reset()
-            lib.profile_enable(True)
-        barrier()
-        for _ in range(steps):
-            flush.fill_(1.0)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            if graph is not None:
-                graph.replay()
-            else:
-                st.step(window)
-            e1.record(stream)
-            times.append((e0, e1))
-        barrier()
-        if profile:
-            lib.profile_enable(False)
-        launches = per_step * steps if graph is not None else lib.launch_count() - n0
-        ms = [a.elapsed_time(b) for a, b in times]
-        return ms, launches
-
+    wl = Workload(key, window, dev, rank)
+    w = wl.w
     for _ in range(max(3, args.warmup)):
-        st.step(None)
-        st.step(TBAR)
+        wl.st.step(window)
     barrier()
-    assert st.status() == 0
+    assert wl.st.status() == 0
 
     # The timed steps replay a CUDA graph of one step (the library enqueues only kernels and
     # memsets on the caller's stream, so a step captures whole); the replay does the same
     # work as the eager calls without their launch gaps.  Eager steps are timed too.
-    def capture(window):
-        n0 = lib.launch_count()
-        g = st.capture(window)
-        torch.cuda.synchronize(dev)
-        return g, (lib.launch_count() - n0) // 2     # capture() runs one eager step first
-    g_full, per_full = capture(None)
-    g_trunc, per_trunc = capture(TBAR)
+    g, per_step = wl.capture()
     for _ in range(max(3, args.warmup)):
-        g_full.replay()
-        g_trunc.replay()
+        g.replay()
     barrier()
-    assert st.status() == 0
+    assert wl.st.status() == 0
 
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -381,148 +556,76 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(uuid)
     clocks.start()
     time.sleep(0.3)
-    ms_full, launches_full = timed(None, args.steps, graph=g_full, per_step=per_full)
-    ms_trunc, launches_trunc = timed(TBAR, args.steps, graph=g_trunc, per_step=per_trunc)
+    ms = wl.timed(args.steps, graph=g, barrier=barrier)
     t_end = time.time() + 1.0      # keep the same load for a few clock samples if the region was short
     while time.time() < t_end:
-        g_full.replay()
+        g.replay()
         torch.cuda.synchronize(dev)
     clk = clocks.stop()
-    status = st.status()
-    ms_eager, _ = timed(None, args.steps)
+    status = wl.st.status()
+    ms_eager = wl.timed(args.steps, barrier=barrier)
+    kern = wl.kernels(args.steps, peaks)
+    e2e_ms, h2d, d2h = wl.e2e(args.steps, barrier)
+    del g
 
-    # per-kernel device time, recorded with CUDA events on the launching stream
-    _, _ = timed(None, args.steps, profile=True)
-    prof_full = lib.profile_read()
-    _, _ = timed(TBAR, args.steps, profile=True)
-    prof_trunc = lib.profile_read()
-    lib.profile_reset()
-
-    # end to end through the C ABI with host buffers: H2D of the step's inputs from pinned
-    # memory, the step, D2H of the loss and the gradients
-    hx = torch.from_numpy(np.ascontiguousarray(inputs["xhat"], np.float32)).pin_memory()
-    ht = torch.from_numpy(np.ascontiguousarray(inputs["target"], np.float32)).pin_memory()
-    hl = torch.empty(1, dtype=torch.float64).pin_memory()
-    hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (st.dW_in[0], st.db_a[0], st.dW_o[0])]
-    h2d = hx.numel() * 4 + ht.numel() * 4
-    d2h = 8 + sum(t.numel() * 4 for t in hg)
-    # Inputs are double-buffered: step i+1's inputs are copied on a second stream while step
-    # i computes; every step's copies stay inside the timed region.
-    copy_stream = torch.cuda.Stream(dev)
-    bufs = [(st.x[0], st.target), (st.x[0].clone(), st.target.clone())]
-    landed = [torch.cuda.Event(), torch.cuda.Event()]      # inputs of buffer b copied
-    used = [torch.cuda.Event(), torch.cuda.Event()]        # step that read buffer b done
-    # one captured step per input buffer (a graph keeps the pointers it was captured with)
-    graphs = []
-    for b in range(2):
-        st.x[0], st.target = bufs[b]
-        graphs.append(st.capture(None))
-    st.x[0], st.target = bufs[0]
-    torch.cuda.synchronize(dev)
-
-    def stage_inputs(b, after):
-        copy_stream.wait_event(after)
-        with torch.cuda.stream(copy_stream):
-            bufs[b][0].copy_(hx, non_blocking=True)
-            bufs[b][1].copy_(ht, non_blocking=True)
-            landed[b].record(copy_stream)
-
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    stage_inputs(0, e0)
-    for i in range(args.steps):
-        b = i % 2
-        stream.wait_event(landed[b])
-        if i + 1 < args.steps:
-            # the other buffer was last read by step i-1
-            stage_inputs(1 - b, used[1 - b] if i > 0 else e0)
-        graphs[b].replay()
-        used[b].record(stream)
-        hl.copy_(st.loss, non_blocking=True)
-        for hgt, dg in zip(hg, (st.dW_in[0], st.db_a[0], st.dW_o[0])):
-            hgt.copy_(dg, non_blocking=True)
-    e1.record(stream)
-    barrier()
-    st.x[0], st.target = bufs[0]
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-
-    # max over ranks
-    mean_full = max_over_ranks(sum(ms_full) / len(ms_full), world, dev)
-    mean_trunc = max_over_ranks(sum(ms_trunc) / len(ms_trunc), world, dev)
-    mean_eager = max_over_ranks(sum(ms_eager) / len(ms_eager), world, dev)
+    med = max_over_ranks(statistics.median(ms), world, dev)
+    mean = max_over_ranks(sum(ms) / len(ms), world, dev)
+    med_eager = max_over_ranks(statistics.median(ms_eager), world, dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    tokens = B * T * K * world
+    tokens = wl.tokens * world
 
-    peaks, peak_src = load_peaks()
-    table = kernel_table(P, N, 4, 4, False)
-    tableT = kernel_table(P, N, 4, 4, True)
-
-    def kernels_summary(prof, tab):
-        tot = sum(ms for _, ms in prof.values())
-        out = {}
-        for name, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
-            per = ms / n
-            ent = {"launches": n, "ms_per_launch": per, "share": ms / tot if tot else None}
-            if name in tab:
-                tok = B * T
-                ent["algo_bytes_per_launch"] = tab[name]["bytes"] * tok
-                ent["achieved_gbs"] = tab[name]["bytes"] * tok / (per * 1e-3) / 1e9
-                ent["hbm_frac"] = ent["achieved_gbs"] / peaks["hbm_gbs"]
-                if "flops" in tab[name]:
-                    ent["algo_flops_per_launch"] = tab[name]["flops"] * tok
-                    ent["achieved_tflops"] = tab[name]["flops"] * tok / (per * 1e-3) / 1e12
-            out[name] = ent
-        return out
-
-    kf = kernels_summary(prof_full, table)
-    kt = kernels_summary(prof_trunc, tableT)
-    # the dominant kernel among those with an algorithmic byte count
-    dom = next((n for n, e in kf.items() if "achieved_gbs" in e), next(iter(kf)))
-    roof = roofline_of(dom, kf[dom], peaks, split3=True)
-    roof["traffic"], state = profiled_traffic(dom)
-    if roof["traffic"] is not None:
+    # the dominant kernel among those with an algorithmic count
+    dom = next((n for n, e in kern.items() if "achieved_gbs" in e), next(iter(kern)))
+    roof = roofline_of(dom, kern[dom], peaks, split3=not wl.bf16)
+    traffic, state, fresh = profiled_traffic(dom, key)
+    roof["traffic"] = traffic if fresh else None
+    if traffic is not None:
         roof["traffic_unit"] = "bytes per launch"
-        roof["traffic_source"] = f"ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/{PROFILE_OF[dom]} ({state})"
+        roof["traffic_source"] = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                                  f"profiles/{PROFILE_OF[(key, dom)]} (sources {state})")
+        if not fresh:
+            roof["traffic_stale"] = f"captured from sources {state}, current sources {source_hash()}"
+    roof["algo_per_launch"] = kern[dom].get("algo_flops_per_launch" if roof["bound"] == "tensor"
+                                            else "algo_bytes_per_launch")
+    roof["ms_per_launch"] = kern[dom]["ms_per_launch"]
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    for name, ent in kf.items():
-        if "achieved_gbs" in ent:
-            r = roofline_of(name, ent, peaks, split3=True)
-            ent["roofline_bound"], ent["roofline_frac"] = r["bound"], r["frac"]
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        toks, dt = oracle_sample()
-        cpu = {"value": toks / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {toks} tokens of one sequence of {WORKLOAD}, full window, aggregated-literal "
-                         f"mode, single thread ({dt:.1f} s)"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload:
+        cpu = cpu_baseline(w.K)
 
     others = []
-    if rank == 0 and world == 1 and not args.no_other_workloads:
-        del st
-        torch.cuda.empty_cache()
-        for key, window in OTHER:
-            others.append(measure_workload(key, window, dev, peaks))
+    if rank == 0 and world == 1 and not args.no_other_workloads and not args.workload:
+        wl.release()
+        del wl
+        for k2, w2 in CONTEXT:
+            others.append(context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3))))
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": weak_scaling_value(B * T * K, world, mean_full), "unit": "tokens/s",
-            "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_full, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": B, "T": T, "P": P, "N": N, "K": K, "window": "full",
+            "metric": METRIC, "value": weak_scaling_value(w.B * w.T * w.K, world, med),
+            "unit": "tokens/s per layer", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": med, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.x_dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": key, "B": w.B, "T": w.T, "P": w.P, "N": w.N, "K": w.K,
+                       "window": window if window is not None else "full",
+                       "precision": ("bf16 GEMM operands (xhat, W, seeds), fp32 accumulate, fp32 scans and "
+                                     "residual stream") if w.x_dtype == "bf16" else "f32",
                        "l2": "flushed before every timed step (256 MB write)", "tokens_per_step": tokens,
-                       "launch": "each step replays a CUDA graph of its library calls"},
-            "eager": {"ms_per_step": mean_eager, "value": tokens / (mean_eager * 1e-3),
+                       "launch": "each step replays a CUDA graph of its library calls",
+                       "ms_per_step": "median of the timed steps"},
+            "ms_mean": mean,
+            "eager": {"ms_per_step": med_eager, "value": tokens / (med_eager * 1e-3),
                       "note": "the same step as direct library calls (no graph)"},
-            "truncated": {"window": TBAR, "value": tokens / (mean_trunc * 1e-3), "ms_per_step": mean_trunc,
-                          "gpu_launches": launches_trunc},
-            "gpu_launches": launches_full,
+            "gpu_launches": per_step * args.steps,
+            "gpu_launches_per_step": per_step,
             "roofline": roof,
-            "kernels": kf,
-            "kernels_truncated": kt,
-            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+            "kernels": kern,
+            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s per layer", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "note": "inputs copied H2D from pinned memory every step (double-buffered), loss and all "
+                            "parameter gradients copied D2H every step, inside the timed region"},
             "cpu_baseline": cpu,
             "clocks": clk,
             "peaks": {"source": peak_src, **peaks},

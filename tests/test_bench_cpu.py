@@ -22,17 +22,30 @@ def _metric(path, key):
     raise KeyError(key)
 
 
-@pytest.mark.parametrize("name", sorted(bench.PROFILE_OF))
-def test_profiled_traffic_is_read_plus_write_of_the_summary(name):
-    path = os.path.join(ROOT, "profiles", bench.PROFILE_OF[name])
-    traffic, state = bench.profiled_traffic(name)
-    expect = _metric(path, "dram__bytes_read.sum") + _metric(path, "dram__bytes_write.sum")
+@pytest.mark.parametrize("key", sorted(k for k in bench.PROFILE_OF
+                                        if os.path.exists(os.path.join(ROOT, "profiles", bench.PROFILE_OF[k]))))
+def test_profiled_traffic_is_read_plus_write_of_the_summary(key):
+    path = os.path.join(ROOT, "profiles", bench.PROFILE_OF[key])
+    traffic, state, fresh = bench.profiled_traffic(key[1], key[0])
+    scale = 1.0
+    for line in open(path):
+        if line.startswith("Traffic scale:"):
+            scale = float(line.split(":", 1)[1].split()[0])
+    expect = (_metric(path, "dram__bytes_read.sum") + _metric(path, "dram__bytes_write.sum")) * scale
     assert traffic == pytest.approx(expect, rel=1e-12)
-    assert re.fullmatch(r"commit [0-9a-f]{7,40}", state), state
+    # a summary names the library sources it was captured from; only a capture of the
+    # current sources is fresh
+    assert state is None or re.fullmatch(r"[0-9a-f]{16}", state), state
+    assert fresh == (state == bench.source_hash())
 
 
 def test_unknown_kernel_has_no_traffic():
-    assert bench.profiled_traffic("no_such_kernel") == (None, None)
+    assert bench.profiled_traffic("no_such_kernel") == (None, None, False)
+
+
+def test_source_hash_is_stable():
+    assert bench.source_hash() == bench.source_hash()
+    assert re.fullmatch(r"[0-9a-f]{16}", bench.source_hash())
 
 
 def test_roofline_takes_the_closer_bound():
@@ -48,10 +61,11 @@ def test_roofline_takes_the_closer_bound():
     assert r["bound"] == "tensor" and r["peak"] == pytest.approx(1900.0 / 3) and r["frac"] == pytest.approx(0.9)
     r = bench.roofline_of("g", {"achieved_gbs": 100.0, "achieved_tflops": 570.0}, peaks, split3=False)
     assert r["peak"] == pytest.approx(1900.0) and r["frac"] == pytest.approx(0.3)
-    # GEMMs are timed inside the step: the sustained bf16 figure when there is one
+    # the tensor fraction is taken against the burst peak, the sustained one given beside it
     r = bench.roofline_of("g", {"achieved_gbs": 100.0, "achieved_tflops": 510.0},
                           dict(peaks, bf16_tflops_sustained=1700.0), split3=False)
-    assert r["peak"] == pytest.approx(1700.0) and r["frac"] == pytest.approx(0.3)
+    assert r["peak"] == pytest.approx(1900.0) and r["frac"] == pytest.approx(510.0 / 1900.0)
+    assert r["peak_sustained"] == pytest.approx(1700.0) and r["frac_sustained"] == pytest.approx(0.3)
 
 
 def test_kernel_table_counts_the_path_bytes():
@@ -66,3 +80,23 @@ def test_kernel_table_counts_the_path_bytes():
     assert t["proj_in"]["bytes"] == P * 4 + 3 * N * 4 and t["proj_in"]["flops"] == 2 * P * 3 * N
     # bf16 seeds halve the seed bytes of the reverse scan's writes
     assert bench.kernel_table(P, N, 2, 2, False)["bwd_scan"]["bytes"] == 4 * N * 4 + 4 * N * 2
+
+
+def test_kernel_table_stack_entries():
+    P, N, K = 2048, 256, 4
+    t = bench.kernel_table(P, N, 2, 2, True, K)
+    # the normalisation's backward reads y, dxhat, gy and writes gy_prev (fp32) plus r
+    assert t["rms_norm_bwd"]["bytes"] == 16 * P + 4
+    # in a stack the input gradient stores dxhat alone
+    assert t["input_grad"]["bytes"] == 3 * N * 2 + 4 * P
+    # proj_out: c, h read, y written, the residual read (bf16 input once, fp32 stream K-1 times)
+    assert t["proj_out"]["bytes"] == 8 * N + 4 * P + (2 * P + 3 * 4 * P) / 4
+
+
+def test_clock_summary_reads_reasons():
+    lines = ["0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active",
+             "0, 2000, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "garbage"]
+    c = bench.summarize_clocks(lines)
+    assert c["sm_mhz"] == 1950 and c["sm_max_mhz"] == 2070 and c["reasons"] == ["sw_power_cap"]
+    assert c["samples"] == 2 and c["power_w_max"] == 1000.0
