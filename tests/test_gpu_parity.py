@@ -101,6 +101,21 @@ def test_ssm4_p2048_shape():
     compare(synth.make_inputs("ssm4_p2048", T=200), 48, True)
 
 
+# --------------------------------------------------------------- the bf16 workloads at their own windows
+
+PREFIX = 16384
+
+
+@pytest.mark.parametrize("key,Tbar", [("ssm1_1m", 4096), ("ssm1_1m", None), ("ssm8_p512", 4096),
+                                      ("ssm4_p2048", 8192)])
+def test_prefix_at_stated_window(key, Tbar):
+    """Each bf16 workload on its first 16384 tokens, at the window it is stated with (full
+    width, full depth): windows of 64-128 scan chunks, whose look-back runs several rounds
+    before it meets a closed composite, and the bf16 split-K parameter reductions over 16K
+    tokens.  Every tensor of every layer is compared with the oracle."""
+    compare(synth.make_inputs(key, T=PREFIX), Tbar, True)
+
+
 # --------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("T,B,Tbar", [(1, 1, None), (1, 2, 1), (33, 3, None), (33, 3, 32), (64, 1, 64), (65, 2, 2)])
