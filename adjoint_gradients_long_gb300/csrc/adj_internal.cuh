@@ -17,8 +17,8 @@ namespace adj {
 constexpr unsigned ST_TIMEOUT = 1u;
 constexpr size_t WS_HEADER = 256;
 
-// Iteration limit of every device-side spin (look-back flags, mbarriers).  With
-// the back-off below one wait gives up after well under a second.
+// Iteration limit of the scans' look-back (rounds, each one L2 round trip plus a short
+// back-off): a wait that never ends gives up after a few seconds.
 constexpr int SPIN_LIMIT = 1 << 22;
 
 __device__ __forceinline__ void record_timeout(unsigned *status) {
@@ -53,17 +53,6 @@ __device__ __forceinline__ void st4(__nv_bfloat16 *p, float4 v) {
     *reinterpret_cast<uint2 *>(p) = u;
 }
 
-// Wait until *flag != 0; returns the flag, or 0 after SPIN_LIMIT polls (status recorded).
-__device__ __forceinline__ unsigned wait_flag(const unsigned *flag, unsigned *status) {
-    for (int it = 0; it < SPIN_LIMIT; ++it) {
-        unsigned v = ld_acquire(flag);
-        if (v) return v;
-        if (it > 64) __nanosleep(128);
-    }
-    record_timeout(status);
-    return 0;
-}
-
 // ---------------------------------------------------------------- float4 arithmetic
 __device__ __forceinline__ float4 f4(float s) { return make_float4(s, s, s, s); }
 __device__ __forceinline__ float4 operator*(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
@@ -84,8 +73,10 @@ struct ScanWs {               // look-back descriptors carved from the workspace
 size_t scan_ws_bytes(int64_t B, int64_t T, int N);
 ScanWs scan_ws_carve(void *base, int64_t nchunks_total);
 
+// withhold_first (self test only, B * ceil(N/128) == 1): chunk 0 never runs, so every
+// other chunk's look-back waits for it until its limit and records a timeout.
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
-                            void *scan_ws, unsigned *status, cudaStream_t st);
+                            void *scan_ws, unsigned *status, cudaStream_t st, bool withhold_first = false);
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t Tbar, void *scan_ws, unsigned *status,
                             cudaStream_t st);

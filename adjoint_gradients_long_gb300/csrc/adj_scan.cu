@@ -634,10 +634,11 @@ static cudaError_t set_smem(K kern, size_t smem) {
 }
 
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
-                            void *scan_ws, unsigned *status, cudaStream_t st) {
+                            void *scan_ws, unsigned *status, cudaStream_t st, bool withhold_first) {
     constexpr int L = SC_FWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
+    if (withhold_first && (nseq != 1 || nchunks < 2)) return cudaErrorInvalidValue;
     ScanMaps mp;
     const float *arr[2] = {a, u};
     const int rows[2] = {TT, TT};
@@ -645,9 +646,14 @@ cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B,
     ScanWs d = scan_ws_carve(scan_ws, nseq * nchunks);
     cudaError_t e = scan_ws_reset(scan_ws, nseq * nchunks, st);
     if (e != cudaSuccess) return e;
+    // self test of the look-back's give-up path: the ticket starts one chunk ahead and the
+    // grid is one chunk short, so chunk 0 never runs and never publishes, and every other
+    // chunk's look-back waits for it until its limit
+    if (withhold_first && (e = cudaMemsetAsync(d.ticket, 0, sizeof(unsigned), st)) != cudaSuccess) return e;
     const size_t smem = staged_bytes(2 * TT);
     if ((e = set_smem(k_fwd_scan<L>, smem)) != cudaSuccess) return e;
-    k_fwd_scan<L><<<unsigned(nseq * nchunks), 256, smem, st>>>(mp, h, T, N, nslices, nseq, nchunks, d, status);
+    const unsigned grid = unsigned(nseq * nchunks - (withhold_first ? 1 : 0));
+    k_fwd_scan<L><<<grid, 256, smem, st>>>(mp, h, T, N, nslices, nseq, nchunks, d, status);
     return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ STATUS = {0: "ADJ_OK", 1: "ADJ_EINVAL", 2: "ADJ_ESHAPE", 3: "ADJ_EALIGN", 4: "AD
 EXPORTS = ("adj_workspace_bytes", "adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc",
            "adj_param_grad", "adj_stream_status", "adj_status_str", "adj_launch_count", "adj_profile_enable",
            "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read", "adj_rms_norm",
-           "adj_rms_norm_bwd", "adj_selftest_waits")
+           "adj_rms_norm_bwd", "adj_selftest_waits", "adj_selftest_ws_bytes")
 
 
 class AdjError(RuntimeError):
@@ -59,6 +59,8 @@ def load(path: str = LIB_PATH):
         lib.adj_rms_norm.argtypes = [_PD] + [_VP] * 4
         lib.adj_selftest_waits.argtypes = [_VP, _SZ, ctypes.c_int, _VP]
         lib.adj_selftest_waits.restype = ctypes.c_int
+        lib.adj_selftest_ws_bytes.argtypes = []
+        lib.adj_selftest_ws_bytes.restype = _SZ
         lib.adj_rms_norm_bwd.argtypes = [_PD] + [_VP] * 6
         lib.adj_stream_status.argtypes = [_VP, _VP]
         lib.adj_status_str.argtypes = [ctypes.c_int]
@@ -176,6 +178,10 @@ def profile_read() -> dict:
         if n.value:
             out[L.adj_profile_name(i).decode()] = (int(n.value), float(ms.value))
     return out
+
+
+def selftest_ws_bytes() -> int:
+    return int(load().adj_selftest_ws_bytes())
 
 
 def selftest_waits(ws, ws_bytes, which, stream=None):

@@ -174,10 +174,16 @@ adj_status adj_fwd_scan_noalloc(const adj_dims *dims, const adj_weights *w, cons
                                 unsigned *status, void *stream);
 
 /* Failure-path self test (a library facility with no counterpart on the pages): runs
- * the bounded device waits the kernels rely on against a look-back flag that is never
- * set (which & 1) and an mbarrier that is never arrived on (which & 2).  Each wait gives
- * up after its limit (about 0.5 s and 2 s), records the timeout in ws's status word and
- * returns; adj_stream_status(ws) then reports ADJ_ETIMEOUT.  ws needs 512 bytes. */
+ * the bounded device waits the kernels rely on against objects that are never released.
+ *   which & 1: the scans' decoupled look-back -- the forward state scan kernel runs over a
+ *              small problem held in ws whose first chunk is never launched, so every
+ *              other chunk waits for a predecessor that never publishes (a few seconds);
+ *   which & 2: an mbarrier wait (TMA staging, GEMM pipeline) on a barrier that is never
+ *              arrived on (about 2 s).
+ * Each wait gives up after its limit, records the timeout in ws's status word and returns;
+ * adj_stream_status(ws) then reports ADJ_ETIMEOUT.  ws: device memory, 256-byte aligned,
+ * at least adj_selftest_ws_bytes() bytes, status word zero before the call. */
+size_t adj_selftest_ws_bytes(void);
 adj_status adj_selftest_waits(void *ws, size_t ws_bytes, int which, void *stream);
 
 /* ---- Launch accounting and per-kernel timing (a library facility; the pages
