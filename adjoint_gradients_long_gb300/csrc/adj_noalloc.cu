@@ -57,14 +57,17 @@ extern "C" adj_status adj_fwd_scan_noalloc(const adj_dims *dims, const adj_weigh
     adj_status s = scratch_address(&ws);
     if (s != ADJ_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // adj_fwd_scan validates every argument before it launches anything
+    // adj_fwd_scan validates every argument before it launches anything: any status but
+    // ADJ_OK and ADJ_ECUDA means nothing was launched and the array is untouched.
     s = adj_fwd_scan(dims, w, xhat, xres, a, c, h, y, y_x, ws, NOALLOC_SCRATCH_BYTES, stream);
-    if (s != ADJ_OK) return s;
+    if (s != ADJ_OK && s != ADJ_ECUDA) return s;
+    // Kernels may have run (ADJ_ECUDA can come after some launches): report the device
+    // status word, then clear the header, so that the next call starts from a zero
+    // status word whatever happened here.  The look-back descriptors are reset by the
+    // scan launcher itself.
+    adj_status out = s;
     if (status && cudaMemcpyAsync(status, ws, sizeof(unsigned), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-        return ADJ_ECUDA;
-    // The status word must read zero at the start of every call: the array is
-    // zero-initialised when the library is loaded, and each call clears it after use.
-    // The look-back descriptors are reset by the scan launcher itself.
-    if (cudaMemsetAsync(ws, 0, adj::WS_HEADER, st) != cudaSuccess) return ADJ_ECUDA;
-    return ADJ_OK;
+        out = ADJ_ECUDA;
+    if (cudaMemsetAsync(ws, 0, adj::WS_HEADER, st) != cudaSuccess) out = ADJ_ECUDA;
+    return out;
 }
