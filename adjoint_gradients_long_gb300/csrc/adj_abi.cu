@@ -84,8 +84,9 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
     const size_t win_f = al256(size_t(d->P) * 3 * d->N * (wsplit ? 4 : 2));
     size_t off = WS_HEADER;
     switch (op) {
-    case ADJ_OP_FWD:            // u
+    case ADJ_OP_FWD:            // u; bf16 layers: c . h in bf16 (the output projection's operand)
         L.buf0 = off; off += btn;
+        if (d->x_dtype == ADJ_BF16) { L.buf1 = off; off += al256(size_t(d->B * d->T) * d->N * 2); }
         L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
         L.wsplit = off; off += win_f + wo_s;
         break;
@@ -265,10 +266,12 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
         ProfScope ps(K_PROJ_IN, st);
         ADJ_CUDA(launch_gemm_tc(BT, 3 * int64_t(N), P, op1(xhat, P, 1, xbf), Win, e, 1, !xbf, status_word(ws), st));
     }
-    // h_t = a_t h_{t-1} + u_t
+    // h_t = a_t h_{t-1} + u_t; bf16 layers that want y also get c . h rounded to bf16 (the
+    // output projection's A operand, loaded by TMA straight into the MMA layout)
+    __nv_bfloat16 *chx = (y && xbf) ? reinterpret_cast<__nv_bfloat16 *>(at(ws, L.buf1)) : nullptr;
     {
         ProfScope ps(K_FWD_SCAN, st);
-        ADJ_CUDA(launch_fwd_scan(a, u, h, B, T, N, at(ws, L.scan), status_word(ws), st));
+        ADJ_CUDA(launch_fwd_scan(a, u, h, B, T, N, at(ws, L.scan), status_word(ws), st, false, chx ? c : nullptr, chx));
     }
     if (y) {
         // y = xres + (c . h) W_o
@@ -285,7 +288,8 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
             ADJ_CUDA(err);
         }
         ProfScope ps(K_PROJ_OUT, st);
-        ADJ_CUDA(launch_gemm_tc(BT, P, N, op1(c, N, 1, false, h), Wo, e2, 1, !xbf, status_word(ws), st));
+        const GemmOperand A = chx ? op1(chx, N, 1, true) : op1(c, N, 1, false, h);
+        ADJ_CUDA(launch_gemm_tc(BT, P, N, A, Wo, e2, 1, !xbf, status_word(ws), st));
     }
     return ADJ_OK;
 }

@@ -75,8 +75,10 @@ ScanWs scan_ws_carve(void *base, int64_t nchunks_total);
 
 // withhold_first (self test only, B * ceil(N/128) == 1): chunk 0 never runs, so every
 // other chunk's look-back waits for it until its limit and records a timeout.
+// c and ch (both or neither): also write ch = bf16(c . h) [B,T,N].
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
-                            void *scan_ws, unsigned *status, cudaStream_t st, bool withhold_first = false);
+                            void *scan_ws, unsigned *status, cudaStream_t st, bool withhold_first = false,
+                            const float *c = nullptr, __nv_bfloat16 *ch = nullptr);
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t Tbar, void *scan_ws, unsigned *status,
                             cudaStream_t st);

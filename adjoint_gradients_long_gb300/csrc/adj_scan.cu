@@ -264,9 +264,12 @@ __device__ __forceinline__ float4 srow(const float *s, int r, int lane) {
 
 // ============================================================================ forward state scan
 // Composite of a token range: h_out = A h_in + H.  (A2,H2) after (A1,H1) = (A2 A1, A2 H1 + H2).
-// Staged: a and u, rows [c0, c0 + 8L).
-template <int L>
+// Staged: a and u, rows [c0, c0 + 8L).  With EOUT the scan also writes chx = c . h rounded
+// to bf16 (the output projection's operand in bf16 layers), reading c from global memory
+// (its loads issued before the staging wait).
+template <int L, bool EOUT>
 __global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 1)) k_fwd_scan(const __grid_constant__ ScanMaps mp, float *__restrict__ h,
+                                                  const float *__restrict__ c, __nv_bfloat16 *__restrict__ chx,
                                                   int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
                                                   ScanWs d, unsigned *status) {
     constexpr int TT = SC_WARPS * L;
@@ -288,6 +291,12 @@ __global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 
         float *dst[2] = {sa, su};
         const int rows[2] = {TT, TT};
         stage_chunk(mp, 2, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+    }
+    const int64_t base = b * T * N + ch;
+    float4 cv[EOUT ? L : 1];
+    if (EOUT) {
+#pragma unroll
+        for (int k = 0; k < L; ++k) cv[k] = (act && t0 + k < T) ? ld_stream4(c + base + (t0 + k) * N) : f4(0.f);
     }
     mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
 
@@ -346,13 +355,15 @@ __global__ void __launch_bounds__(256, (L <= 6 ? 4 : L <= 8 ? 3 : L <= 12 ? 2 : 
 
     // pass 2: h from the carry into this warp's first token
     float4 hc = fma4(pA, sC[lane], pH);
-    const int64_t base = b * T * N + ch;
 #pragma unroll
     for (int k = 0; k < L; ++k) {
         const int64_t t = t0 + k;
         if (t >= T) break;
         hc = fma4(srow(sa, w * L + k, lane), hc, srow(su, w * L + k, lane));
-        if (act) st4(h + base + t * N, hc);   // kept in L2: the output projection reads h next
+        if (act) {
+            st4(h + base + t * N, hc);   // kept in L2 (the output projection reads c . h next)
+            if (EOUT) st4(chx + base + t * N, cv[k] * hc);
+        }
     }
 }
 
@@ -634,7 +645,8 @@ static cudaError_t set_smem(K kern, size_t smem) {
 }
 
 cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B, int64_t T, int N,
-                            void *scan_ws, unsigned *status, cudaStream_t st, bool withhold_first) {
+                            void *scan_ws, unsigned *status, cudaStream_t st, bool withhold_first,
+                            const float *c, __nv_bfloat16 *ch) {
     constexpr int L = SC_FWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
@@ -651,9 +663,14 @@ cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B,
     // chunk's look-back waits for it until its limit
     if (withhold_first && (e = cudaMemsetAsync(d.ticket, 0, sizeof(unsigned), st)) != cudaSuccess) return e;
     const size_t smem = staged_bytes(2 * TT);
-    if ((e = set_smem(k_fwd_scan<L>, smem)) != cudaSuccess) return e;
     const unsigned grid = unsigned(nseq * nchunks - (withhold_first ? 1 : 0));
-    k_fwd_scan<L><<<grid, 256, smem, st>>>(mp, h, T, N, nslices, nseq, nchunks, d, status);
+    if (c && ch) {
+        if ((e = set_smem(k_fwd_scan<L, true>, smem)) != cudaSuccess) return e;
+        k_fwd_scan<L, true><<<grid, 256, smem, st>>>(mp, h, c, ch, T, N, nslices, nseq, nchunks, d, status);
+    } else {
+        if ((e = set_smem(k_fwd_scan<L, false>, smem)) != cudaSuccess) return e;
+        k_fwd_scan<L, false><<<grid, 256, smem, st>>>(mp, h, nullptr, nullptr, T, N, nslices, nseq, nchunks, d, status);
+    }
     return cudaGetLastError();
 }
 

@@ -40,7 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # CPU oracle samples (prefixes of one sequence of the headline workload): all cores on
 # CPU_ALL_T tokens, one core on CPU_ONE_T tokens; the reference arm runs CPU_REF_T tokens
 # a step so that its warm-up and timed steps end within a few minutes
-CPU_ALL_T, CPU_ONE_T, CPU_REF_T = 4096, 1024, 1024
+CPU_ALL_T, CPU_ONE_T, CPU_REF_T = 16384, 1024, 4096
 
 
 def parse():
@@ -171,10 +171,13 @@ def kernel_table(P, N, xb, db, trunc, K=1):
     layers the first layer's residual is its bf16 input and the others' the fp32 stream,
     so proj_out's residual bytes are the mean over the K launches."""
     res = (P * xb + (K - 1) * 4 * P) / K
+    # bf16 layers: the forward scan also reads c and writes c . h in bf16, which the
+    # output projection reads instead of c and h in fp32
+    chb = 2 * N if xb == 2 else 0
     return {
         "proj_in": dict(bytes=P * xb + 3 * N * 4, flops=2 * P * 3 * N),
-        "fwd_scan": dict(bytes=3 * N * 4),
-        "proj_out": dict(bytes=2 * N * 4 + res + P * 4, flops=2 * N * P),
+        "fwd_scan": dict(bytes=3 * N * 4 + (N * 4 + chb if chb else 0)),
+        "proj_out": dict(bytes=(chb if chb else 2 * N * 4) + res + P * 4, flops=2 * N * P),
         "loss": dict(bytes=3 * P * 4),
         "cot_proj": dict(bytes=P * 4 + N * 4, flops=2 * P * N),
         "win_scan": dict(bytes=4 * N * 4),
@@ -288,11 +291,21 @@ def kernels_summary(prof, tab, tokens, peaks, split3):
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
 def cpu_model():
+    """The host CPU's model name (/proc/cpuinfo on x86, lscpu on Arm), else the machine type."""
     try:
         for line in open("/proc/cpuinfo"):
             if line.lower().startswith(("model name", "cpu model")):
                 return line.split(":", 1)[1].strip()
     except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith(("model name", "vendor id")):
+                name = line.split(":", 1)[1].strip()
+                if line.strip().lower().startswith("model name"):
+                    return f"{name} ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
         pass
     return platform.processor() or platform.machine()
 

@@ -89,8 +89,10 @@ def test_kernel_table_stack_entries():
     assert t["rms_norm_bwd"]["bytes"] == 16 * P + 4
     # in a stack the input gradient stores dxhat alone
     assert t["input_grad"]["bytes"] == 3 * N * 2 + 4 * P
-    # proj_out: c, h read, y written, the residual read (bf16 input once, fp32 stream K-1 times)
-    assert t["proj_out"]["bytes"] == 8 * N + 4 * P + (2 * P + 3 * 4 * P) / 4
+    # proj_out: c . h read in bf16, y written, the residual read (bf16 input once, fp32
+    # stream K-1 times); the forward scan reads a, u, c and writes h and c . h
+    assert t["proj_out"]["bytes"] == 2 * N + 4 * P + (2 * P + 3 * 4 * P) / 4
+    assert t["fwd_scan"]["bytes"] == 16 * N + 2 * N
 
 
 def test_clock_summary_reads_reasons():

@@ -14,7 +14,8 @@ each layer k is checked two ways:
     reaches i + Tbar, so the window lies wholly inside it;
   * properties that hold at any size: dW_in = xhat^T [D_a|D_u|D_c], db_a = sum_t D_a,
     dW_o = E^T gy and L = 1/2 ||y - target||^2, recomputed in fp64 from the device's own
-    operands (checks the full-size reductions).
+    operands as the GEMMs read them (gy rounded to bf16 in bf16 workloads), which checks
+    the full-size reductions.
 Tolerances: 1e-4 (fp32 workloads), 2e-2 (bf16 GEMM operands and seeds).
 """
 import numpy as np
@@ -98,9 +99,11 @@ def run_full(key, Tbar, samples_per_layer=None):
         assert rel_fro(st.dW_in[k].cpu().numpy(), (x.T @ D).cpu().numpy()) <= 1e-4, k
         assert rel_fro(st.db_a[k].cpu().numpy(), D[:, :N].sum(0).cpu().numpy()) <= 1e-4, k
         del x, D
+        # the GEMM's operands as it reads them: bf16 workloads round gy to bf16
         Ed = E.double().reshape(B * T, N)
-        assert rel_fro(st.dW_o[k].cpu().numpy(), (Ed.T @ gy.double().reshape(B * T, P)).cpu().numpy()) <= 1e-4, k
-        del Ed
+        gop = (gy.to(torch.bfloat16) if bf16 else gy).double().reshape(B * T, P)
+        assert rel_fro(st.dW_o[k].cpu().numpy(), (Ed.T @ gop).cpu().numpy()) <= 1e-4, k
+        del Ed, gop
         # ---- sampled tokens against the oracle on a slice, from the device's layer input
         Wl = {nm: np.asarray(v, np.float64) for nm, v in inp["layers"][k].items()}
         for b, i in samples:
