@@ -15,6 +15,7 @@
 // Tile: BM = 128 rows (TMEM lanes), BN <= 256 columns (TMEM columns), BK = 64
 // (one 128-byte swizzle row of bf16).  Shared-memory element (r, k) of a tile lives
 // at byte r*128 + ((k/8) ^ (r%8))*16 + (k%8)*2 (8-row atoms of 1024 bytes).
+#include <stdlib.h>
 #include <string.h>
 
 #include <cuda.h>
@@ -57,9 +58,9 @@ __device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr) {
     return d;
 }
 // Instruction descriptor: kind::f16, bf16 x bf16 -> fp32; a_mn / b_mn select MN-major operands.
-__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn = false, bool b_mn = false) {
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn = false, bool b_mn = false, int m = TC_BM) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
-           (uint32_t(n >> 3) << 17) | (uint32_t(TC_BM >> 4) << 24);
+           (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
@@ -72,6 +73,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+// CTA pair: one MMA over both CTAs' operands (A: 128 rows in each CTA; B: half the
+// columns in each), D in both CTAs' tensor memory at the same address.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// CTA pair: arrive on the mbarrier at this shared-memory offset in both CTAs once the
+// pair MMAs issued so far have completed
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -310,6 +330,10 @@ constexpr int TC_EPI_WARPS = ADJ_TC_EPI_WARPS, TC_THREADS_P = (TC_EPI_WARPS + TC
 static_assert(TC_EPI_WARPS % 4 == 0, "epilogue warps cover the four TMEM lane quarters");
 constexpr int TC_MMA_WARP = TC_EPI_WARPS + TC_PROD_WARPS, TC_TMA_WARP = TC_MMA_WARP + 1;
 constexpr uint32_t TC_EPI_SMEM = TC_EPI_WARPS * 32 * 32 * 4;
+// CTA pairs need no producer warps (every operand comes by TMA): a pair kernel with many
+// tiles per CTA runs warps 0-15 as epilogue warps, twice the output chunks in flight
+constexpr int TC_MAX_EPI_WARPS = TC_EPI_WARPS + TC_PROD_WARPS;
+constexpr uint32_t TC_CHUNK_BYTES = 32 * 32 * 4;
 
 // Operand load mode: register staging, or TMA tiles of a bf16 array (K-major: one box of
 // 64 k x R rows; MN-major: R/64 boxes of 64 rows x 64 k).
@@ -323,18 +347,21 @@ struct TcArgs {
     CUtensorMap tmAmul;           // the elementwise factor of a raw-loaded A
     CUtensorMap tmO[3];           // epilogue outputs stored by TMA (ProjIn: a, u, c)
     CUtensorMap tmAdd;            // StoreAdd: the residual, loaded by TMA
+    CUtensorMap tmNx;             // StoreAdd through a normalised input: xhat, prefetched into L2
     int64_t M, Nc, K, kper;
     int BN, stages, n_tiles, m_tiles, splits;
     int a_ld, b_ld;
     bool b_res, a_mul, b_lo;
     bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
+    int nacc;                     // accumulators in tensor memory (2: epilogue overlaps the next tile)
+    int epiw;                     // epilogue warps (CTA pairs: 8 or 16; otherwise TC_EPI_WARPS)
     GemmOperand A, Bm;
     GemmEpilogue ep;
     unsigned *status;
 };
 
 // Issue the TMA loads of rows [row0, row0+R) x k [k0, k0+64) of an operand into dst.
-template <bool IS_A>
+template <bool IS_A, bool PAIRLD = false>
 __device__ __forceinline__ void tma_tile(const CUtensorMap *maps, const GemmOperand &O, int mode, int64_t row0, int R,
                                          int64_t k0, uint8_t *dst, uint32_t bar) {
     int blk = 0;
@@ -350,10 +377,14 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap *maps, const GemmOper
     }
     const void *m = &maps[blk];
     if (mode == LD_TMA_K || mode == LD_RAW_K) {
-        tma_load_2d(smem_u32(dst), m, int(kk), int(rr), bar);
+        if (PAIRLD) tma_load_2d_pair(smem_u32(dst), m, int(kk), int(rr), bar);
+        else tma_load_2d(smem_u32(dst), m, int(kk), int(rr), bar);
     } else {
         const int box = mode == LD_RAW_MN ? 16384 : 8192;   // 64 x 64 fp32 or bf16
-        for (int j = 0; j < R / 64; ++j) tma_load_2d(smem_u32(dst + j * box), m, int(rr) + 64 * j, int(kk), bar);
+        for (int j = 0; j < R / 64; ++j) {
+            if (PAIRLD) tma_load_2d_pair(smem_u32(dst + j * box), m, int(rr) + 64 * j, int(kk), bar);
+            else tma_load_2d(smem_u32(dst + j * box), m, int(rr) + 64 * j, int(kk), bar);
+        }
     }
 }
 
@@ -501,6 +532,23 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
         for (int i = lane >> 3; i < rows; i += 4) {
             float4 v = *reinterpret_cast<const float4 *>(sb + epi_at(i, lane & 7));
             const int64_t o = int64_t(i) * ep.ld;
+            if (add && ep.nr) {
+                // through the normalised input: (acc - xhat mean(xhat . dxhat)) / r, then the add
+                const int64_t row = m0r + i;
+                float sdz = 0.f;
+                for (int sl = 0; sl < ep.nsl; ++sl) sdz += __ldg(ep.ndz + row * ep.nsl + sl);
+                const float mt = sdz * ep.inv_P, ir = 1.f / __ldg(ep.nr + row);
+                float4 x4;
+                if (ep.nx_bf16) {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(ep.nx) + row * ep.ld + n);
+                    const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+                    const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+                    x4 = make_float4(p.x, p.y, q.x, q.y);
+                } else {
+                    x4 = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(ep.nx) + row * ep.ld + n));
+                }
+                v = (v - x4 * f4(mt)) * f4(ir);
+            }
             if (add) {
                 if (ep.add_bf16) {
                     const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(ep.add) +
@@ -528,26 +576,41 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
 // REGS: whether register staging may be needed (any operand with LD_REG, or a resident B
 // not loaded by TMA).  Without it the kernel carries no staging code, which keeps the
 // producers' hot loop free of register spills; ABF/BBF only matter with REGS.
-template <bool ABF, bool BBF, bool SPLIT, bool REGS>
+// PAIR: the kernel runs as clusters of two CTAs on neighbouring SMs.  A pair computes a
+// 256-row x BN tile with one tcgen05.mma.cta_group::2 per k-slice: each CTA stages its
+// 128 rows of A and half of the B tile (BN / 2 output columns) by TMA, both CTAs' loads
+// complete on the leader's (rank 0) stage barrier, the leader issues the MMAs, and the
+// accumulator (128 rows per CTA) lands in both CTAs' tensor memory.  The MMA completion
+// is multicast to both CTAs' stage and accumulator barriers; both epilogues release the
+// accumulator on the leader's barrier.  Per SM this halves the B operand traffic through
+// shared memory for the same MMA work.  Only all-bf16, all-TMA operands take this mode.
+template <bool ABF, bool BBF, bool SPLIT, bool REGS, bool PAIR = false>
 __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_constant__ TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int BN = args.BN, S = args.stages;
-    const TcLayout Lo = tc_layout(BN, args.kper, args.b_res, SPLIT, ld_raw(args.a_ld), ld_raw(args.b_ld), args.a_mul);
+    const int BNS = PAIR ? BN / 2 : BN;   // B rows (output columns) staged by this CTA
+    const TcLayout Lo = tc_layout(BNS, args.kper, args.b_res, SPLIT, ld_raw(args.a_ld), ld_raw(args.b_ld), args.a_mul);
     uint8_t *bres = base;                                         // resident B (hi k-blocks, then lo)
     uint8_t *stages = base + Lo.bres_bytes;                       // ring of A (+B) stages
+    const int EPIW = PAIR ? args.epiw : TC_EPI_WARPS;
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + TC_EPI_SMEM);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES);
     uint64_t *full = bars, *empty = bars + S, *accf = bars + 2 * S, *acce = bars + 2 * S + 2, *bready = bars + 2 * S + 4;
     uint64_t *rawfull = bars + 2 * S + 5, *addb = bars + 3 * S + 5;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5 + TC_EPI_WARPS);
-    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3 * S + 5 + TC_EPI_WARPS) + 1;
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5 + TC_MAX_EPI_WARPS);
+    volatile int *abort = reinterpret_cast<volatile int *>(bars + 3 * S + 5 + TC_MAX_EPI_WARPS) + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t ntiles = int64_t(args.n_tiles) * args.m_tiles * args.splits;
     const int64_t nkb_full = (args.kper + TC_BK - 1) / TC_BK;
+    // tiles are scheduled per CTA, or per pair (unit = cluster) with rank 0 the leader
+    const uint32_t prank = PAIR ? cluster_rank() : 0u;
+    const int64_t unit0 = PAIR ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);
+    const int64_t nunits = PAIR ? int64_t(gridDim.x >> 1) : int64_t(gridDim.x);
+    const int NACC = PAIR ? args.nacc : 2;
     uint32_t ncols = 32;
-    while (ncols < uint32_t(2 * BN)) ncols <<= 1;
+    while (ncols < uint32_t(NACC * BN)) ncols <<= 1;
     // who fills a stage: the producers (register staging or in-place conversion of raw
     // tiles) and/or the TMA warp (bf16 tiles straight into the MMA layout)
     const bool b_here = !args.b_res;
@@ -564,37 +627,56 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accf[b]), 1);
-            mbar_init(smem_u32(&acce[b]), TC_EPI_WARPS * 32);
+            // CTA pair: one arrival per epilogue warp of both CTAs, on the leader's barrier
+            mbar_init(smem_u32(&acce[b]), PAIR ? 2 * EPIW : EPIW * 32);
         }
         mbar_init(smem_u32(bready), ld_tma(args.b_ld) ? 1 : TC_PROD);
-        for (int w = 0; w < TC_EPI_WARPS; ++w) mbar_init(smem_u32(&addb[w]), 1);
+        for (int w = 0; w < EPIW; ++w) mbar_init(smem_u32(&addb[w]), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == TC_MMA_WARP) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(const_cast<uint32_t *>(tmem_slot))),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            // one warp of each CTA of the pair allocates, collectively, in both SMs
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(const_cast<uint32_t *>(tmem_slot))),
+                         "r"(ncols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(const_cast<uint32_t *>(tmem_slot))),
+                         "r"(ncols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync();   // also: the peer's barriers are initialised before any remote use
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // CTA pair: both CTAs must hold the accumulator at the same tensor-memory address (the
+    // pair MMA writes it there in both); otherwise nothing runs and a failure is recorded
+    bool pair_ok = true;
+    if (PAIR) {
+        const uint32_t peer = ld_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(tmem_slot)), prank ^ 1u));
+        pair_ok = peer == tmem;
+        if (!pair_ok && tid == 0) record_timeout(args.status);
+    }
 
     // tile t -> (z, m tile, n tile); k range of split z
     auto tile_of = [&](int64_t t, int64_t &m0, int64_t &n0, int &z, int64_t &kb0, int64_t &ke) {
         const int64_t per_split = int64_t(args.n_tiles) * args.m_tiles;
         z = int(t / per_split);
         const int64_t r = t - int64_t(z) * per_split;
-        m0 = (r / args.n_tiles) * TC_BM;
+        m0 = (r / args.n_tiles) * (PAIR ? 2 * TC_BM : TC_BM) + int64_t(prank) * TC_BM;   // this CTA's rows
         n0 = (r % args.n_tiles) * BN;
         kb0 = int64_t(z) * args.kper;
         ke = kb0 + args.kper < args.K ? kb0 + args.kper : args.K;
     };
 
-    if (warp >= TC_EPI_WARPS && warp < TC_MMA_WARP) {
+    if (warp >= EPIW && warp < TC_MMA_WARP) {
         // ---------------- producers
         const int ptid = tid - TC_EPI_WARPS * 32;
         bool ok = true;
@@ -617,7 +699,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         const bool csum_on = args.ep.csum && b_raw && args.b_ld == LD_RAW_MN && args.ep.kind == Epi::Partial;
         float csum0 = 0.f, csum1 = 0.f;
         int64_t kbg = 0;   // k-blocks staged so far (ring position)
-        for (int64_t t = blockIdx.x; t < ntiles && ok && prod_full; t += gridDim.x) {
+        for (int64_t t = unit0; t < ntiles && ok && prod_full; t += nunits) {
             int64_t m0, n0, kb0, ke;
             int z;
             tile_of(t, m0, n0, z, kb0, ke);
@@ -702,13 +784,25 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                                         bres + size_t(kb) * Lo.bres_kb + Lo.b_bytes, smem_u32(bready));
                 }
             }
-            bool ok = a_dir || b_dir || a_raw || b_raw;
+            bool ok = (a_dir || b_dir || a_raw || b_raw) && pair_ok;
             int64_t kbg = 0;
-            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            // the residual of a TMA StoreAdd epilogue: the epilogue waits on each 32 x 32 box it
+            // loads, so its boxes are prefetched into L2 when the tile's operand loads start,
+            // about a tile ahead of the epilogue
+            const bool pf_add = args.epi_tma && args.ep.kind == Epi::StoreAdd;
+            for (int64_t t = unit0; t < ntiles && ok; t += nunits) {
                 int64_t m0, n0, kb0, ke;
                 int z;
                 tile_of(t, m0, n0, z, kb0, ke);
                 const int64_t nkb = ke > kb0 ? (ke - kb0 + TC_BK - 1) / TC_BK : 0;
+                if (pf_add) {
+                    for (int q = 0; q < TC_BM / 32; ++q)
+                        for (int c = 0; c < BN; c += 32)
+                            if (m0 + 32 * q < args.M && n0 + c < args.Nc) {
+                                tma_prefetch_2d(&args.tmAdd, int(n0 + c), int(m0 + 32 * q));
+                                if (args.ep.nr) tma_prefetch_2d(&args.tmNx, int(n0 + c), int(m0 + 32 * q));
+                            }
+                }
                 for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
                     const int s = int(kbg % S);
                     const int64_t r = kbg / S;
@@ -721,7 +815,14 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     const int64_t k0 = kb0 + kb * TC_BK;
                     const uint32_t txd = (a_dir ? Lo.a_bytes : 0u) + (b_dir ? Lo.b_bytes * (args.b_lo ? 2u : 1u) : 0u);
                     const uint32_t txr = (a_raw ? (args.a_mul ? 4u : 2u) * Lo.a_bytes : 0u) + (b_raw ? 2u * Lo.b_bytes : 0u);
-                    if (txd) {
+                    if (PAIR) {
+                        // bf16 A rows of this CTA and its half of the B columns, counted on the
+                        // leader's barrier, which expects both CTAs' bytes
+                        const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0u);
+                        if (prank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * txd);
+                        tma_tile<true, true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, fb);
+                        tma_tile<false, true>(args.tmB, args.Bm, args.b_ld, n0 + int64_t(prank) * BNS, BNS, k0, sbb, fb);
+                    } else if (txd) {
                         const uint32_t fb = smem_u32(&full[s]);
                         mbar_arrive_expect_tx(fb, txd);
                         if (a_dir) tma_tile<true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, fb);
@@ -745,9 +846,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         __syncwarp();
     } else if (warp == TC_MMA_WARP) {
         // ---------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && prank == 0 && pair_ok) {
             const bool a_mn = args.a_ld == LD_TMA_MN, b_mn = args.b_ld == LD_TMA_MN;
-            const uint32_t idesc = idesc_bf16(BN, a_mn, b_mn);
+            const uint32_t idesc = idesc_bf16(BN, a_mn, b_mn, PAIR ? 2 * TC_BM : TC_BM);
             // a streamed raw B of 256 rows sits as two converted 128-row halves (hi, lo each):
             // one N = 128 product per half into adjacent accumulator columns
             const bool b_halves = !args.b_res && ld_raw(args.b_ld) && BN == 2 * TC_BM;
@@ -755,13 +856,13 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             bool ok = !args.b_res || mbar_wait(smem_u32(bready), 0, abort, args.status);
             if (ok) tc_fence_after();
             int64_t kbg = 0, i = 0;
-            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+            for (int64_t t = unit0; t < ntiles && ok; t += nunits, ++i) {
                 int64_t m0, n0, kb0, ke;
                 int z;
                 tile_of(t, m0, n0, z, kb0, ke);
                 const int64_t nkb = ke > kb0 ? (ke - kb0 + TC_BK - 1) / TC_BK : 0;
-                const int buf = int(i & 1);
-                const int64_t ru = i >> 1;
+                const int buf = int(i % NACC);
+                const int64_t ru = i / NACC;   // earlier uses of this accumulator
                 if (ru > 0 && !mbar_wait(smem_u32(&acce[buf]), uint32_t((ru - 1) & 1), abort, args.status)) break;
                 tc_fence_after();
                 const uint32_t dacc = tmem + uint32_t(buf * BN);
@@ -796,7 +897,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             const uint32_t kb2 = b_mn ? uint32_t(ks) * 2048u : uint32_t(ks) * 32u;
                             const uint64_t ah = a_mn ? sw128_desc_mn(a_hi + ka) : sw128_desc(a_hi + ka);
                             const uint64_t bh = b_mn ? sw128_desc_mn(bh0 + kb2) : sw128_desc(bh0 + kb2);
-                            mma_bf16(dh, ah, bh, id, acc);
+                            if (PAIR) mma_bf16_pair(dh, ah, bh, id, acc);
+                            else mma_bf16(dh, ah, bh, id, acc);
                             if (SPLIT) {
                                 const uint64_t al = a_mn ? sw128_desc_mn(a_lo + ka) : sw128_desc(a_lo + ka);
                                 const uint64_t bl = b_mn ? sw128_desc_mn(bl0 + kb2) : sw128_desc(bl0 + kb2);
@@ -805,13 +907,15 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             }
                         }
                     }
-                    mma_commit(smem_u32(&empty[s]));
+                    if (PAIR) mma_commit_pair(smem_u32(&empty[s]));
+                    else mma_commit(smem_u32(&empty[s]));
                 }
-                mma_commit(smem_u32(&accf[buf]));
+                if (PAIR) mma_commit_pair(smem_u32(&accf[buf]));
+                else mma_commit(smem_u32(&accf[buf]));
             }
         }
         __syncwarp();
-    } else if (warp < TC_EPI_WARPS) {
+    } else if (warp < EPIW) {
         // ---------------- epilogue (warp w: TMEM lanes 32*(w%4).., columns of half w/4)
         // A 32 x 32 chunk goes TMEM -> registers (lane = row) -> the warp's swizzled
         // shared buffer -> global.  With TMA stores (epi_tma) the fused op is applied in
@@ -820,17 +924,19 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         float *sb = esm + warp * (32 * 32);
         const uint32_t sb_s = smem_u32(sb), addbar = smem_u32(&addb[warp]);
         const int q = warp & 3, half = warp >> 2;   // lane quarter; column-chunk phase
-        constexpr int CSTEP = 32 * (TC_EPI_WARPS / 4);
+        const int CSTEP = 32 * (EPIW / 4);
         const GemmEpilogue &ep = args.ep;
         uint32_t add_phase = 0;
         int64_t i = 0;
-        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        // CTA pair: the accumulator is released on the leader's barrier
+        const uint32_t acce_at = PAIR ? mapa_shared(smem_u32(&acce[0]), 0u) : 0u;
+        for (int64_t t = unit0; t < ntiles && pair_ok; t += nunits, ++i) {
             int64_t m0, n0, kb0, ke;
             int z;
             tile_of(t, m0, n0, z, kb0, ke);
             const int64_t nkb = ke > kb0 ? (ke - kb0 + TC_BK - 1) / TC_BK : 0;
-            const int buf = int(i & 1);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&accf[buf]), uint32_t((i >> 1) & 1), abort, args.status));
+            const int buf = int(i % NACC);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&accf[buf]), uint32_t((i / NACC) & 1), abort, args.status));
             tc_fence_after();
             const int64_t m0r = m0 + q * 32;
             for (int c = half * 32; c < BN; c += CSTEP) {
@@ -850,6 +956,25 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         }
                     }
                     __syncwarp();
+                }
+                // through a normalised input: this lane's row scalars and xhat values (bf16: all 32
+                // columns packed; fp32: read per quad below), issued before the TMEM load
+                const bool norm = add_tma && ep.nr != nullptr;
+                const int64_t nrow = m0r + lane;
+                float n_mt = 0.f, n_ir = 0.f;
+                uint4 n_xb[4];
+                if (norm && nrow < args.M) {
+                    float sdz = 0.f;
+                    for (int sl = 0; sl < ep.nsl; ++sl) sdz += __ldg(ep.ndz + nrow * ep.nsl + sl);
+                    n_mt = sdz * ep.inv_P;
+                    n_ir = 1.f / __ldg(ep.nr + nrow);
+                    if (ep.nx_bf16) {
+                        const __nv_bfloat16 *xr = static_cast<const __nv_bfloat16 *>(ep.nx) + nrow * ep.ld + n;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            n_xb[g] = (n + 8 * g < args.Nc) ? __ldg(reinterpret_cast<const uint4 *>(xr + 8 * g))
+                                                            : make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 float v[32];
                 if (ok && nkb > 0) {
@@ -872,6 +997,25 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             v[j + 3] = sigmoidf_fast(v[j + 3] + b4.w);
                         }
                     }
+                    if (norm && nrow < args.M) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 x4;
+                            if (ep.nx_bf16) {
+                                const uint32_t w0 = (&n_xb[j >> 3].x)[(j & 7) >> 1], w1 = (&n_xb[j >> 3].x)[((j & 7) >> 1) + 1];
+                                x4 = make_float4(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u),
+                                                 __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+                            } else {
+                                x4 = (n + j < args.Nc)
+                                         ? __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(ep.nx) + nrow * ep.ld + n + j))
+                                         : f4(0.f);
+                            }
+                            v[j] = (v[j] - x4.x * n_mt) * n_ir;
+                            v[j + 1] = (v[j + 1] - x4.y * n_mt) * n_ir;
+                            v[j + 2] = (v[j + 2] - x4.z * n_mt) * n_ir;
+                            v[j + 3] = (v[j + 3] - x4.w * n_mt) * n_ir;
+                        }
+                    }
                     if (add_tma) {
                         mbar_wait(addbar, add_phase, abort, args.status);
                         add_phase ^= 1u;
@@ -883,6 +1027,20 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             v[j + 2] += r4.z;
                             v[j + 3] += r4.w;
                         }
+                    }
+                    if (ep.out_x && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd) && m0r + lane < args.M) {
+                        // the bf16 copy of this lane's row: four 16-byte stores
+                        __nv_bfloat16 *xr = static_cast<__nv_bfloat16 *>(ep.out_x) + (m0r + lane) * ep.ld + n;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+                            if (n + 8 * g < args.Nc) {
+                                uint4 u;
+                                u.x = pack_bf16(v[8 * g], v[8 * g + 1]);
+                                u.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+                                u.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+                                u.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+                                *reinterpret_cast<uint4 *>(xr + 8 * g) = u;
+                            }
                     }
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
@@ -909,17 +1067,26 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&acce[buf]));
+            if (PAIR) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acce_at + uint32_t(buf) * 8u);
+            } else {
+                mbar_arrive(smem_u32(&acce[buf]));
+            }
             if (!ok) break;
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
     tc_fence_before();
-    __syncthreads();
+    // CTA pair: neither CTA leaves (or frees tensor memory) while the other may still
+    // signal its barriers
+    if (PAIR) cluster_sync();
+    else __syncthreads();
     if (warp == TC_MMA_WARP) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        if (PAIR) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        else asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
     }
 }
 
@@ -976,10 +1143,14 @@ static bool epi_maps(TcArgs &a, const GemmEpilogue &ep, int64_t M, int64_t Nc, i
         return true;
     case Epi::Store:
     case Epi::StoreAdd:
-        if (ep.out_x) return false;
+        // a bf16 copy (out_x) is written by the lanes themselves, beside the TMA store
         if (!make_out_map(&a.tmO[0], ep.out0, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4)) return false;
         if (ep.kind == Epi::StoreAdd &&
             (ep.add_bf16 || !make_out_map(&a.tmAdd, ep.add, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4)))
+            return false;
+        // the normalised input is only prefetched through its map (32 x 32 boxes)
+        if (ep.kind == Epi::StoreAdd && ep.nr &&
+            !make_map(&a.tmNx, ep.nx, ep.nx_bf16, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * (ep.nx_bf16 ? 2 : 4), 32, 32))
             return false;
         return true;
     case Epi::Partial:
@@ -1041,6 +1212,60 @@ static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cuda
     return cudaGetLastError();
 }
 
+// The CTA-pair instantiation (bf16 operands, all by TMA): launched as clusters of two.
+using PairKernel = void (*)(TcArgs);
+static PairKernel pair_kernel() { return k_gemm_tc<false, false, false, false, true>; }
+static cudaLaunchConfig_t pair_config(unsigned grid, size_t smem, cudaStream_t st, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(TC_THREADS_P, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+// Pairs of CTAs that can be resident at once with this much shared memory (0 if none).
+static int pair_slots(size_t smem) {
+    static size_t cached_smem[4] = {0, 0, 0, 0};
+    static int cached[4] = {-1, -1, -1, -1};
+    static int next = 0;
+    for (int i = 0; i < 4; ++i)
+        if (cached[i] >= 0 && cached_smem[i] == smem) return cached[i];
+    if (cudaFuncSetAttribute(pair_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+        return 0;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config(2, smem, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_kernel(), &cfg) != cudaSuccess) n = 0;
+    cached_smem[next] = smem;
+    cached[next] = n;
+    next = (next + 1) % 4;
+    return n;
+}
+static cudaError_t launch_pair(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(pair_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config(grid, smem, st, attr);
+    return cudaLaunchKernelEx(&cfg, pair_kernel(), a);
+}
+
+// Whether GEMMs whose operands are both bf16 and both loaded by TMA run as CTA pairs.
+static int g_pair_mode = -1;   // -1: not read yet
+static bool pair_enabled() {
+    if (g_pair_mode < 0) {
+        const char *v = getenv("ADJ_GEMM_PAIR");
+        g_pair_mode = (v && v[0] == '0') ? 0 : 1;
+    }
+    return g_pair_mode == 1;
+}
+
 cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &A, const GemmOperand &Bm,
                            const GemmEpilogue &ep, int splits, bool split3, unsigned *status, cudaStream_t st,
                            int *splits_used, bool *csum_done) {
@@ -1066,11 +1291,20 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     const bool a_mul = A.mul && ld_raw(a_mode);
     int BN = int(Nc < 256 ? (Nc + 31) / 32 * 32 : 256);
     int S = 0, b_mode = LD_REG;
+    // bf16 operands that TMA loads straight into the MMA layout run as CTA pairs (below),
+    // with six streamed stages: no resident B, whose two stages leave too few operand bytes
+    // in flight per SM to cover the HBM latency of a short-K product
+    const bool pair_cand = pair_enabled() && !split3 && !a_mul && A.bf16 && Bm.bf16 && !A.lo[0] && !Bm.lo[0] &&
+                           (a_mode == LD_TMA_K || a_mode == LD_TMA_MN) && BN % TC_BM == 0;
     for (int next = BN;; BN = next) {
         if (BN == 0) return cudaErrorInvalidConfiguration;
         next = BN > 32 ? (BN / 2 + 31) / 32 * 32 : 0;
         const TcLayout res = tc_layout(BN, a.kper, true, split3, ld_raw(a_mode), false, a_mul);
         a.b_res = splits == 1 && size_t(res.bres_bytes) + 2 * size_t(res.stage_bytes) <= budget;
+        if (pair_cand && BN % TC_BM == 0) {
+            const int bm = tma_mode(Bm, false, Nc, K, BN, split3);
+            if (bm == LD_TMA_K || bm == LD_TMA_MN) a.b_res = false;
+        }
         b_mode = tma_mode(Bm, false, Nc, K, BN, split3);
         if (a.b_res && ld_raw(b_mode)) b_mode = LD_REG;          // a resident B is converted once, by registers
         if (!a.b_res && !Bm.bf16 && !Bm.mul && BN > TC_BM && BN != 2 * TC_BM &&
@@ -1083,10 +1317,29 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
         if (S >= 2) break;
     }
     if (S > 6) S = 6;
+    // CTA pairs: both operands bf16 by TMA (no conversion, no resident B), tiles of 256
+    // rows x BN with BN / 2 columns of B staged in each CTA
+    bool pair = pair_cand && !a.b_res && (b_mode == LD_TMA_K || b_mode == LD_TMA_MN) && BN % TC_BM == 0;
+    int slots = 0;
+    // pairs with many tiles each (no split) use 16 epilogue warps, with one stage fewer
+    const int epiw = (pair && splits == 1) ? TC_MAX_EPI_WARPS : TC_EPI_WARPS;
+    const size_t bar_bytes = size_t(3 * 6 + 6 + TC_MAX_EPI_WARPS) * 8;
+    if (pair) {
+        const TcLayout Lp = tc_layout(BN / 2, a.kper, false, false, false, false, false);
+        const size_t budget_p = 227 * 1024 - 1024 - size_t(epiw) * TC_CHUNK_BYTES - bar_bytes;
+        int Sp = int(budget_p / Lp.stage_bytes);
+        if (Sp > 6) Sp = 6;
+        const size_t smem_p = 1024 + size_t(Sp) * Lp.stage_bytes + size_t(epiw) * TC_CHUNK_BYTES + bar_bytes;
+        slots = Sp >= 2 ? pair_slots(smem_p) : 0;
+        if (slots > 0) S = Sp;
+        else pair = false;
+    }
+    const int64_t rows_per_tile = pair ? 2 * TC_BM : TC_BM;
+    const int64_t units = pair ? slots : g_num_sms;   // tiles in flight: CTA pairs or CTAs
     // split K no further than one wave of CTAs: every CTA then owns exactly one tile
     {
-        const int64_t per_split = ((Nc + BN - 1) / BN) * ((M + TC_BM - 1) / TC_BM);
-        const int64_t cap = (g_num_sms / ((Nc + BN - 1) / BN)) * ((Nc + BN - 1) / BN);
+        const int64_t per_split = ((Nc + BN - 1) / BN) * ((M + rows_per_tile - 1) / rows_per_tile);
+        const int64_t cap = (units / ((Nc + BN - 1) / BN)) * ((Nc + BN - 1) / BN);
         if (splits > 1 && int64_t(splits) * per_split > cap) {
             splits = int(cap / per_split > 1 ? cap / per_split : 1);
             a.splits = splits;
@@ -1097,19 +1350,28 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (splits_used) *splits_used = splits;
     a.BN = BN;
     a.stages = S;
+    a.nacc = 2;   // the epilogue of one tile overlaps the mainloop of the next
+    a.epiw = pair ? epiw : TC_EPI_WARPS;
     a.n_tiles = int((Nc + BN - 1) / BN);
-    a.m_tiles = int((M + TC_BM - 1) / TC_BM);
+    a.m_tiles = int((M + rows_per_tile - 1) / rows_per_tile);
     a.A = A; a.Bm = Bm; a.ep = ep; a.status = status;
     a.a_ld = tma_build(a.tmA, nullptr, &a.tmAmul, A, a_mode, true, M, K, TC_BM);
-    a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, BN);
+    a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, pair ? BN / 2 : BN);
+    if (pair && (a.a_ld != a_mode || a.b_ld != b_mode)) return cudaErrorInvalidValue;   // a map did not build
     a.a_mul = a_mul && a.a_ld != LD_REG;
     a.epi_tma = epi_maps(a, ep, M, Nc, splits);
     a.b_lo = Bm.lo[0] && a.b_ld != LD_REG;
     // the layout was sized for the modes asked for; a mode that fell back to registers
     // uses only part of its region
-    const TcLayout L = tc_layout(BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
-    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + TC_EPI_SMEM + (3 * S + 6 + TC_EPI_WARPS) * 8;
+    const TcLayout L = tc_layout(pair ? BN / 2 : BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
+    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + size_t(a.epiw) * TC_CHUNK_BYTES + bar_bytes;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
+    if (pair) {
+        a.ep.csum = nullptr;
+        if (csum_done) *csum_done = false;
+        const int64_t npairs = ntiles < slots ? ntiles : slots;
+        return launch_pair(a, unsigned(2 * npairs), smem, st);
+    }
     int64_t grid = ntiles;
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;
     if (grid < a.n_tiles) grid = a.n_tiles;
