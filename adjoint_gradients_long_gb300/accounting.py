@@ -66,3 +66,23 @@ def step_bytes(P: int, N: int, x_bytes: int, d_bytes: int, window: bool, stacked
     if stacked:
         par["input_grad"] = 3 * N * d_bytes + P * 4 + P * 4
     return {"fwd": fwd, "bwd": bwd, "param": par}
+
+
+def stack_buffer_bytes(B: int, T: int, K: int, N: int, P: int, x_bytes: int, d_bytes: int) -> dict:
+    """Device bytes of every buffer the stack driver (stack.AdjStack) allocates, by group,
+    workspace excluded: what one gradient step of the library needs besides its scratch.
+      states    a, c, h per layer (fp32) and the layer inputs xhat (x_bytes), r per stacked layer
+      streams   the fp32 residual stream y per layer, the target, two cotangent buffers gy
+                (and, with bf16 GEMM operands, their two bf16 copies)
+      seeds     D_a, D_u, D_c, E (d_bytes) and the row dots dz of a normalised input
+      params    W_in, b_a, W_o per layer (x_bytes; b_a fp32) and their fp32 gradients
+      loss      one fp64 value"""
+    bt = B * T
+    states = K * bt * (3 * N * 4 + P * x_bytes) + (K - 1) * bt * 4
+    streams = K * bt * P * 4 + bt * P * 4 + 2 * bt * P * 4 + (2 * bt * P * 2 if x_bytes == 2 else 0)
+    seeds = 4 * bt * N * d_bytes + (bt * ((N + 127) // 128) * 4 if K > 1 else 0)
+    params = K * (P * 3 * N * x_bytes + N * 4 + N * P * x_bytes) + K * (P * 3 * N + N + N * P) * 4
+    # allocations: x, a, c, h, y per layer; r per stacked layer; target, two gy, loss; four
+    # seeds; dz; W_in, b_a, W_o and their gradients per layer
+    count = 5 * K + (K - 1) + 4 + 4 + (1 if K > 1 else 0) + 6 * K + (2 if x_bytes == 2 else 0)
+    return {"states": states, "streams": streams, "seeds": seeds, "params": params, "loss": 8, "buffers": count}

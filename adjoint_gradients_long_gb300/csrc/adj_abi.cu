@@ -98,7 +98,7 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
     case ADJ_OP_BWD_TRUNC:      // g, R
         L.buf0 = off; off += btn;
         L.buf1 = off; off += (Tbar < d->T ? btn : 0);
-        L.scan = off; off += scan_ws_bytes(d->B, d->T, d->N);
+        L.scan = off; off += std::max(scan_ws_bytes(d->B, d->T, d->N), al256(trunc_ws_bytes(d->B, d->T, d->N)));
         L.wsplit = off; off += wo_s;
         break;
     case ADJ_OP_PARAM: {
@@ -174,11 +174,14 @@ GemmEpilogue epi(Epi k) {
 }
 
 adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a, const float *c, const float *h,
-                      const float *gy, void *D_a, void *D_u, void *D_c, void *E, int64_t Tbar, int op, void *ws,
-                      size_t ws_bytes, void *stream) {
+                      const float *gy, const void *gy_x, void *D_a, void *D_u, void *D_c, void *E, float *dz,
+                      int64_t Tbar, int op, void *ws, size_t ws_bytes, void *stream) {
     ADJ_TRY(check_dims(dims));
     if (!w) return ADJ_EINVAL;
     ADJ_TRY(check_ptrs({w->W_o, a, c, h, gy, D_a, D_u, D_c, E}));
+    ADJ_TRY(check_opt({dz, gy_x}));
+    if (gy_x && dims->x_dtype != ADJ_BF16) return ADJ_EINVAL;
+    if (dz) ADJ_TRY(check_ptrs({w->b_a}));
     if (op == ADJ_OP_BWD_TRUNC && Tbar < 1) return ADJ_EINVAL;
     Layout L;
     ADJ_TRY(check_ws(dims, op, Tbar, ws, ws_bytes, &L));
@@ -196,10 +199,21 @@ adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a
         const GemmOperand Wo = opw(w->W_o, int64_t(N) * P, dims->x_dtype == ADJ_BF16, at(ws, L.wsplit), P, 1, st, &err);
         ADJ_CUDA(err);
         ProfScope ps(K_COT_PROJ, st);
-        ADJ_CUDA(launch_gemm_tc(BT, N, P, op1(gy, P, 1, false), Wo, e, 1, dims->x_dtype == ADJ_F32, status_word(ws), st));
+        // bf16 layers with the cotangent's bf16 copy: the GEMM reads it by TMA (the same
+        // rounding the fp32 operand would get in its conversion)
+        const GemmOperand A = gy_x ? op1(gy_x, P, 1, true) : op1(gy, P, 1, false);
+        ADJ_CUDA(launch_gemm_tc(BT, N, P, A, Wo, e, 1, dims->x_dtype == ADJ_F32, status_word(ws), st));
     }
     const bool trunc = op == ADJ_OP_BWD_TRUNC && Tbar < T;
     float *R = nullptr;
+    if (trunc && trunc_one_launch(T, Tbar)) {
+        // windows of whole scan chunks: the window scan and the reverse scan in one launch
+        ProfScope ps(K_BWD_SCAN, st);
+        ADJ_CUDA(launch_trunc_scan(g, c, a, h, reinterpret_cast<float *>(at(ws, L.buf1)), D_a, D_u, D_c, E,
+                                   dims->d_dtype == ADJ_BF16, B, T, N, Tbar, at(ws, L.scan), status_word(ws), st,
+                                   dz ? w->b_a : nullptr, dz));
+        return ADJ_OK;
+    }
     if (trunc) {
         R = reinterpret_cast<float *>(at(ws, L.buf1));
         ProfScope ps(K_WIN_SCAN, st);
@@ -207,7 +221,7 @@ adj_status bwd_common(const adj_dims *dims, const adj_weights *w, const float *a
     }
     ProfScope ps(K_BWD_SCAN, st);
     ADJ_CUDA(launch_bwd_scan(g, c, a, h, R, D_a, D_u, D_c, E, dims->d_dtype == ADJ_BF16, B, T, N, trunc ? Tbar : 0,
-                             at(ws, L.scan), status_word(ws), st));
+                             at(ws, L.scan), status_word(ws), st, dz ? w->b_a : nullptr, dz));
     return ADJ_OK;
 }
 
@@ -294,12 +308,13 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
     return ADJ_OK;
 }
 
-adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *target, float *gy, double *loss,
-                        void *ws, size_t ws_bytes, void *stream) {
+adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *target, float *gy, void *gy_x,
+                        double *loss, void *ws, size_t ws_bytes, void *stream) {
     ADJ_TRY(check_dims(dims));
     ADJ_TRY(check_ptrs({y, target}));
-    ADJ_TRY(check_opt({gy, loss}));
+    ADJ_TRY(check_opt({gy, gy_x, loss}));
     if (!gy && !loss) return ADJ_EINVAL;
+    if (gy_x && !gy) return ADJ_EINVAL;
     Layout L;
     ADJ_TRY(check_ws(dims, ADJ_OP_LOSS, 0, ws, ws_bytes, &L));
     const int64_t count = dims->B * dims->T * dims->P;
@@ -309,32 +324,37 @@ adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *targe
         return ADJ_OK;
     }
     ProfScope ps(K_LOSS, st);
-    ADJ_CUDA(launch_loss(y, target, gy, count, reinterpret_cast<double *>(at(ws, L.part0)), loss_blocks(count),
+    ADJ_CUDA(launch_loss(y, target, gy, static_cast<__nv_bfloat16 *>(gy_x), count,
+                         reinterpret_cast<double *>(at(ws, L.part0)), loss_blocks(count),
                          status_word(ws) + 1, loss, st));
     return ADJ_OK;
 }
 
 adj_status adj_bwd_full(const adj_dims *dims, const adj_weights *w, const float *a, const float *c, const float *h,
-                        const float *gy, void *D_a, void *D_u, void *D_c, void *E, void *ws, size_t ws_bytes,
-                        void *stream) {
-    return bwd_common(dims, w, a, c, h, gy, D_a, D_u, D_c, E, 0, ADJ_OP_BWD_FULL, ws, ws_bytes, stream);
+                        const float *gy, const void *gy_x, void *D_a, void *D_u, void *D_c, void *E, float *dz,
+                        void *ws, size_t ws_bytes, void *stream) {
+    return bwd_common(dims, w, a, c, h, gy, gy_x, D_a, D_u, D_c, E, dz, 0, ADJ_OP_BWD_FULL, ws, ws_bytes, stream);
 }
 
 adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float *a, const float *c, const float *h,
-                         const float *gy, void *D_a, void *D_u, void *D_c, void *E, int64_t Tbar, void *ws,
-                         size_t ws_bytes, void *stream) {
-    return bwd_common(dims, w, a, c, h, gy, D_a, D_u, D_c, E, Tbar, ADJ_OP_BWD_TRUNC, ws, ws_bytes, stream);
+                         const float *gy, const void *gy_x, void *D_a, void *D_u, void *D_c, void *E, float *dz,
+                         int64_t Tbar, void *ws, size_t ws_bytes, void *stream) {
+    return bwd_common(dims, w, a, c, h, gy, gy_x, D_a, D_u, D_c, E, dz, Tbar, ADJ_OP_BWD_TRUNC, ws, ws_bytes,
+                      stream);
 }
 
 adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void *xhat, const void *D_a,
-                          const void *D_u, const void *D_c, const void *E, const float *gy, float *dW_in,
-                          float *db_a, float *dW_o, float *gy_prev, float *dxhat, int accumulate, void *ws,
-                          size_t ws_bytes, void *stream) {
+                          const void *D_u, const void *D_c, const void *E, const float *gy, const void *gy_x,
+                          float *dW_in, float *db_a, float *dW_o, float *gy_prev, void *gy_prev_x, float *dxhat,
+                          const float *r, const float *dz, int accumulate, void *ws, size_t ws_bytes, void *stream) {
     ADJ_TRY(check_dims(dims));
     if (!w) return ADJ_EINVAL;
     ADJ_TRY(check_ptrs({w->W_in, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o}));
-    ADJ_TRY(check_opt({gy_prev, dxhat}));
+    ADJ_TRY(check_opt({gy_x, gy_prev, gy_prev_x, dxhat, r, dz}));
     if (gy_prev && dxhat) return ADJ_EINVAL;
+    if ((gy_x || gy_prev_x) && dims->x_dtype != ADJ_BF16) return ADJ_EINVAL;
+    if (gy_prev_x && !gy_prev) return ADJ_EINVAL;
+    if ((r != nullptr) != (dz != nullptr) || (r && !gy_prev)) return ADJ_EINVAL;
     if (accumulate != 0 && accumulate != 1) return ADJ_EINVAL;
     Layout L;
     ADJ_TRY(check_ws(dims, ADJ_OP_PARAM, 0, ws, ws_bytes, &L));
@@ -379,7 +399,8 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
     e2.out0 = part_o;
     {
         ProfScope ps(K_PARAM_DWO, st);
-        ADJ_CUDA(launch_gemm_tc(N, P, BT, op1(E, 1, N, dbf), op1(gy, 1, P, false), e2, s_o, !xbf, status_word(ws), st, &su_o));
+        const GemmOperand Bg = gy_x ? op1(gy_x, 1, P, true) : op1(gy, 1, P, false);
+        ADJ_CUDA(launch_gemm_tc(N, P, BT, op1(E, 1, N, dbf), Bg, e2, s_o, !xbf, status_word(ws), st, &su_o));
     }
     // the three sums over partials, in one launch
     {
@@ -390,9 +411,20 @@ adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void
         ADJ_CUDA(launch_reduce_partials(segs, 3, accumulate, st));
     }
     if (gy_prev || dxhat) {
-        // dxhat = [D_a | D_u | D_c] W_in^T, or gy_prev = gy + dxhat
+        // dxhat = [D_a | D_u | D_c] W_in^T, or gy_prev = gy + dxhat, or, through a normalised
+        // input xhat = y / r, gy_prev = gy + (dxhat - xhat (xhat . dxhat) / P) / r with the row
+        // dot products xhat . dxhat = sum of dz over the channel slices
         GemmEpilogue e3 = epi(gy_prev ? Epi::StoreAdd : Epi::Store);
         e3.out0 = gy_prev ? gy_prev : dxhat; e3.add = gy; e3.ld = P;
+        e3.out_x = gy_prev_x;   // the bf16 copy of gy_prev for the next layer's GEMMs
+        if (r) {
+            e3.nr = r;
+            e3.ndz = dz;
+            e3.nsl = int(cdiv(N, 128));
+            e3.nx = xhat;
+            e3.nx_bf16 = xbf;
+            e3.inv_P = 1.f / float(P);
+        }
         cudaError_t err = cudaSuccess;
         const GemmOperand Win = opw(w->W_in, int64_t(P) * 3 * N, xbf, at(ws, L.wsplit), 3 * int64_t(N), 1, st, &err);
         ADJ_CUDA(err);

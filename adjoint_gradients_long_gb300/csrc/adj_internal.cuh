@@ -82,10 +82,21 @@ cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B,
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t Tbar, void *scan_ws, unsigned *status,
                             cudaStream_t st);
+// The truncated adjoint in one launch (window scan and reverse scan interleaved block by
+// block), for windows of whole scan chunks (trunc_one_launch); its scan workspace is
+// trunc_ws_bytes.  R [B,T,N] is its scratch for the window sums.
+bool trunc_one_launch(int64_t T, int64_t W);
+size_t trunc_ws_bytes(int64_t B, int64_t T, int N);
+cudaError_t launch_trunc_scan(const float *g, const float *c, const float *a, const float *h, float *R, void *D_a,
+                              void *D_u, void *D_c, void *E, bool d_bf16, int64_t B, int64_t T, int N, int64_t W,
+                              void *ws, unsigned *status, cudaStream_t st, const float *b_a = nullptr,
+                              float *dz = nullptr);
+// dz (with b_a; both or neither): also the per-token, per-128-channel-slice sums
+// [B*T, ceil(N/128)] of D_a z_a + D_u u + D_c c (the row dot xhat . dxhat of the layer input)
 cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, const float *h,
                             const float *R, void *D_a, void *D_u, void *D_c, void *E, bool d_bf16,
                             int64_t B, int64_t T, int N, int64_t Tbar, void *scan_ws,
-                            unsigned *status, cudaStream_t st);
+                            unsigned *status, cudaStream_t st, const float *b_a = nullptr, float *dz = nullptr);
 
 // GEMM operands: strided, optionally split over up to three arrays.
 struct GemmOperand {
@@ -117,6 +128,15 @@ struct GemmEpilogue {
     // launch reports whether it took them (csum_done); otherwise csum is left untouched.
     float *csum;
     int64_t csum_n;
+    // StoreAdd through a normalised layer input xhat = y / r (nr non-null):
+    //   out0[m,n] = add[m,n] + (acc - nx[m,n] * (sum_{s < nsl} ndz[m * nsl + s]) * inv_P) / nr[m]
+    // with nx [M, ld] (bf16 if nx_bf16, else fp32), nr [M], ndz [M, nsl] fp32.
+    const float *nr;
+    const float *ndz;
+    int nsl;
+    const void *nx;
+    bool nx_bf16;
+    float inv_P;
 };
 
 // ProjIn output column n of the product -> block (0 a, 1 u, 2 c) and channel.
@@ -172,7 +192,7 @@ cudaError_t launch_rms_norm_bwd(const float *y, const float *r, const float *dx,
                                 int64_t rows, int P, cudaStream_t st);
 // ticket: a word of the workspace header (zero before the first call, back at zero after
 // every launch)
-cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t count,
+cudaError_t launch_loss(const float *y, const float *target, float *gy, __nv_bfloat16 *gyx, int64_t count,
                         double *part, int nblk, unsigned *ticket, double *loss, cudaStream_t st);
 
 }  // namespace adj

@@ -13,8 +13,8 @@ namespace adj {
 // does not depend on block order.  FP64 arithmetic is kept out of the per-element loop:
 // GB300's fp64 rate is a small fraction of its fp32 rate.
 __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const float *__restrict__ tg,
-                                              float *__restrict__ gy, int64_t count, double *__restrict__ part,
-                                              unsigned *ticket, double *__restrict__ loss) {
+                                              float *__restrict__ gy, __nv_bfloat16 *__restrict__ gyx, int64_t count,
+                                              double *__restrict__ part, unsigned *ticket, double *__restrict__ loss) {
     __shared__ double red[256];
     __shared__ bool last;
     float s = 0.f;
@@ -32,18 +32,21 @@ __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const
         for (int u = 0; u < 4; ++u) {
             const float4 r = a[u] - b[u];
             if (gy) st4(gy + 4 * (i + u * stride), r);   // kept in L2: the cotangent projection reads gy next
+            if (gyx) st4(gyx + 4 * (i + u * stride), r);
             s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
         }
     }
     for (; i < n4; i += stride) {
         const float4 r = ld_stream4(y + 4 * i) - ld_stream4(tg + 4 * i);
         if (gy) st4(gy + 4 * i, r);
+        if (gyx) st4(gyx + 4 * i, r);
         s += 0.5f * (r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w);
     }
     for (int64_t i = 4 * n4 + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count;
          i += int64_t(gridDim.x) * blockDim.x) {
         const float r = y[i] - tg[i];
         if (gy) gy[i] = r;
+        if (gyx) gyx[i] = __float2bfloat16_rn(r);
         s += 0.5f * r * r;
     }
     red[threadIdx.x] = double(s);
@@ -72,9 +75,9 @@ __global__ void __launch_bounds__(256) k_loss(const float *__restrict__ y, const
     if (threadIdx.x == 0) *loss = red[0];
 }
 
-cudaError_t launch_loss(const float *y, const float *target, float *gy, int64_t count, double *part, int nblk,
-                        unsigned *ticket, double *loss, cudaStream_t st) {
-    k_loss<<<nblk, 256, 0, st>>>(y, target, gy, count, part, ticket, loss);
+cudaError_t launch_loss(const float *y, const float *target, float *gy, __nv_bfloat16 *gyx, int64_t count, double *part,
+                        int nblk, unsigned *ticket, double *loss, cudaStream_t st) {
+    k_loss<<<nblk, 256, 0, st>>>(y, target, gy, gyx, count, part, ticket, loss);
     return cudaGetLastError();
 }
 

@@ -482,16 +482,55 @@ __device__ __forceinline__ RevSeg rseg_then(const RevSeg &X, const RevSeg &Y) {
     return RevSeg{X.Q * Y.Q, fma4(X.Q, Y.S, X.S), Y.cl};
 }
 
+// A seed as the parameter GEMMs read it (rounded to its storage type).
+template <typename TD>
+__device__ __forceinline__ float4 as_stored(float4 v) {
+    if constexpr (sizeof(TD) == 2) {
+        return make_float4(__bfloat162float(__float2bfloat16_rn(v.x)), __bfloat162float(__float2bfloat16_rn(v.y)),
+                           __bfloat162float(__float2bfloat16_rn(v.z)), __bfloat162float(__float2bfloat16_rn(v.w)));
+    } else {
+        return v;
+    }
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) { return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w; }
+// Sums of eight values over the 32 lanes of a warp in 9 shuffles: each exchange halves the
+// values a lane keeps.  Returns, in every lane, the total of value
+// k = 4 (lane >> 4 & 1) + 2 (lane >> 3 & 1) + (lane >> 2 & 1).
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float a[4], b[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = (h16 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, h16 ? v[i] : v[i + 4], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) b[i] = (h8 ? a[i + 2] : a[i]) + __shfl_xor_sync(0xffffffffu, h8 ? a[i] : a[i + 2], 8);
+    float c = (h4 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, h4 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
+}
+__device__ __forceinline__ int warp_sum8_index(int lane) { return 4 * ((lane >> 4) & 1) + 2 * ((lane >> 3) & 1) + ((lane >> 2) & 1); }
+
+// z = logit(a) - b (the gate's pre-activation xhat W_a); 0 where a is 0 or 1, where the
+// gate seed a (1 - a) vanishes
+__device__ __forceinline__ float gate_z(float a, float b) {
+    return (a > 0.f && a < 1.f) ? __logf(__fdividef(a, 1.f - a)) - b : 0.f;
+}
+
 // Staged: g and c, rows [c0, c0 + 8L), and a, rows [c0, c0 + 8L] (one more: b of the
 // chunk's last token).  h (and R) are read from global memory, their loads issued
 // before the staging wait.  D_c and E are written right after pass 1, before the
 // look-back; D_u and D_a in pass 2.
-template <int L, bool TRUNC, typename TD>
+// DZ: also dz[token][slice] = sum over the slice's channels of D_a z_a + D_u u + D_c c
+// (seeds as stored; z_a = logit(a) - b_a, u_t = h_t - a_t h_{t-1}): with z = xhat W_in
+// this is D . (xhat W_in) = xhat . (D W_in^T) = xhat . dxhat, the row dot product that the
+// cotangent through a normalised layer input needs, without reading dxhat.
+template <int L, bool TRUNC, typename TD, bool DZ = false>
 __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1)) k_bwd_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
                                                   const float *__restrict__ R, TD *__restrict__ Da,
                                                   TD *__restrict__ Du, TD *__restrict__ Dc, TD *__restrict__ E,
                                                   int64_t T, int N, int nslices, int64_t nseq, int64_t nchunks,
-                                                  int64_t W, ScanWs d, unsigned *status) {
+                                                  int64_t W, ScanWs d, unsigned *status,
+                                                  const float *__restrict__ b_a, float *__restrict__ dz) {
     constexpr int TT = SC_WARPS * L;
     extern __shared__ uint8_t sm_dyn[];
     float *sg = smem_1k(sm_dyn), *sc = sg + TT * SC_SLICE, *sa = sc + TT * SC_SLICE;
@@ -554,6 +593,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     // D_c = g h and E = c h need no carry: store them now, so these writes overlap the
     // look-back (after warp 0's publish, whose fence would otherwise wait for them).  The
     // g rows then hold e = g c for pass 2, and the c rows are free.
+    float pz[DZ ? L : 1];   // DZ: this lane's share of dz per token (the D_c c part here)
     if (act) {
 #pragma unroll
         for (int k = 0; k < L; ++k) {
@@ -563,6 +603,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
             const float4 gk = srow(sg, r, lane), ck = srow(sc, r, lane);
             st4(Dc + base + t * N, gk * hv[k + 1]);
             st4(E + base + t * N, ck * hv[k + 1]);
+            if (DZ) pz[k] = dot4(as_stored<TD>(gk * hv[k + 1]), ck);
             *reinterpret_cast<float4 *>(sg + r * SC_SLICE + lane * 4) = gk * ck;
         }
     }
@@ -602,6 +643,9 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     // composite of everything after this warp's tokens, then pass 2 backwards
     G = rseg_then(post, RevSeg{sCQ[lane], sCS[lane], true});
     if (TRUNC) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
+    const float4 bav = (DZ && act) ? *reinterpret_cast<const float4 *>(b_a + ch) : f4(0.f);
+    static_assert(!DZ || L == 8, "the row dots are summed eight tokens at a time");
+    float vz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
         const int64_t t = t0 + k;
@@ -621,10 +665,311 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
                                                  : (act ? ld_keep4(R + base + (T - 1) * N) : f4(0.f));
             mu = fma4(G.Q, rk, G.S);
         }
+        const float4 dak = mu * hv[k] * ak * (f4(1.f) - ak);
         if (act) {
             st4(Du + base + t * N, mu);
-            st4(Da + base + t * N, mu * hv[k] * ak * (f4(1.f) - ak));
+            st4(Da + base + t * N, dak);
         }
+        if (DZ && act) {
+            const float4 za = make_float4(gate_z(ak.x, bav.x), gate_z(ak.y, bav.y), gate_z(ak.z, bav.z),
+                                          gate_z(ak.w, bav.w));
+            const float4 uk = hv[k + 1] - ak * hv[k];
+            vz[k & 7] = pz[k] + dot4(as_stored<TD>(dak), za) + dot4(as_stored<TD>(mu), uk);
+        }
+    }
+    if (DZ) {
+        const float tot = warp_sum8(vz, lane);
+        const int k = warp_sum8_index(lane);
+        if ((lane & 3) == 0 && t0 + k < T) dz[(b * T + t0 + k) * nslices + slice] = tot;
+    }
+}
+
+// ============================================================================ truncated adjoint in one launch
+// The window scan R (k_win_scan) and the truncated reverse scan (k_bwd_scan<TRUNC>) in one
+// grid, for windows that are whole chunks (W % (8 L) == 0).  With blocks of W tokens, R of
+// block b+1 is read only by the reverse scan of block b, and both scans restart at every
+// block edge.  The tickets therefore run block by block from the end:
+//     R(nb-1), rev(nb-1), R(nb-2), rev(nb-2), ..., R(1), rev(1), rev(0)
+// (R of block 0 is never read).  R chunks go forward through their block and reverse
+// chunks backward, so every look-back stays inside one block and waits only on CTAs with
+// earlier tickets.  An R chunk raises a flag once its rows are stored; a reverse chunk
+// waits (bounded) on the flags of the R chunks its window ends fall in, all of which
+// have earlier tickets.  The g, c and a rows of a block are read by its R chunks and
+// then again by its reverse chunks a group of tickets later, mostly from L2, and R
+// lives between its writer and its reader in L2: HBM sees about the bytes of the full
+// (untruncated) reverse scan.
+struct TruncTicket {
+    bool rev;          // reverse-scan chunk (else an R chunk)
+    int64_t chunk, seq;
+};
+__device__ __forceinline__ TruncTicket trunc_ticket(int64_t tk, int64_t nseq, int64_t nchunks, int64_t CB) {
+    const int64_t nb = (nchunks + CB - 1) / CB, cl = nchunks - (nb - 1) * CB;
+    TruncTicket r;
+    int64_t b, j;
+    const int64_t s0 = cl * nseq, sb = CB * nseq;
+    if (tk < 2 * s0) {
+        b = nb - 1;
+        r.rev = tk >= s0;
+        j = r.rev ? tk - s0 : tk;
+    } else {
+        const int64_t u = tk - 2 * s0, pp = u / (2 * sb), q = u - pp * 2 * sb;
+        b = nb - 2 - pp;
+        r.rev = b == 0 || q >= sb;
+        j = (b == 0 || q < sb) ? q : q - sb;
+    }
+    const int64_t cb = b == nb - 1 ? cl : CB, pos = j / nseq;
+    r.seq = j - pos * nseq;
+    r.chunk = r.rev ? b * CB + cb - 1 - pos : b * CB + pos;
+    return r;
+}
+
+// dR: descriptors of the R scan; dM: of the reverse scan; flags[seq * nchunks + chunk]:
+// 0 once R chunk `chunk` of sequence `seq` is stored (0xFFFFFFFF before).
+template <int L, typename TD, bool DZ>
+__global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
+                                                      float *__restrict__ R, TD *__restrict__ Da, TD *__restrict__ Du,
+                                                      TD *__restrict__ Dc, TD *__restrict__ E, int64_t T, int N,
+                                                      int nslices, int64_t nseq, int64_t nchunks, int64_t W,
+                                                      ScanWs dR, ScanWs dM, unsigned *flags, unsigned *status,
+                                                      const float *__restrict__ b_a, float *__restrict__ dz) {
+    constexpr int TT = SC_WARPS * L;
+    extern __shared__ uint8_t sm_dyn[];
+    float *sg = smem_1k(sm_dyn), *sc = sg + TT * SC_SLICE, *sa = sc + TT * SC_SLICE;
+    __shared__ unsigned s_ticket;
+    __shared__ uint64_t s_bar;
+    __shared__ int s_abort;
+    __shared__ float4 sX[SC_WARPS][32], sY[SC_WARPS][32], sC0[32], sC1[32];
+    __shared__ bool sCl[SC_WARPS];
+    __shared__ int s_ctl[SC_WARPS + 2];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const TruncTicket tkt = trunc_ticket(chunk_ticket(dR, &s_ticket, &s_bar, &s_abort), nseq, nchunks, W / TT);
+    const int64_t chunk = tkt.chunk, seq = tkt.seq;
+    const int64_t b = seq / nslices;
+    const int slice = int(seq % nslices), ch = slice * SC_SLICE + lane * 4;
+    const bool act = ch < N;
+    const int64_t c0 = chunk * TT, t0 = c0 + w * L;
+    const int64_t base = b * T * N + ch;
+    const int64_t di = seq * nchunks + chunk, fb = seq * nchunks;
+
+    if (!tkt.rev) {
+        // ------------------------------------------------ R chunk (forward, restarted at block starts)
+        {
+            // the maps are the reverse chunks': a's box has one row more, which lands unused
+            // (the barrier must expect every byte the boxes deliver)
+            float *dst[3] = {sg, sc, sa};
+            const int rows[3] = {TT, TT, TT + 1};
+            stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+        }
+        mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
+        FwdSeg G{f4(1.f), f4(0.f), false};
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            if (t >= T) break;
+            const int r = w * L + k;
+            const float4 ev = srow(sg, r, lane) * srow(sc, r, lane), av = srow(sa, r, lane);
+            if (t % W == 0) G = FwdSeg{f4(1.f), ev, true};
+            else G = FwdSeg{G.P * av, fma4(G.P * av, ev, G.S), G.cl};
+        }
+        sX[w][lane] = G.P;
+        sY[w][lane] = G.S;
+        if (lane == 0) sCl[w] = G.cl;
+        __syncthreads();
+        FwdSeg pre{f4(1.f), f4(0.f), false};
+        for (int j = 0; j < w; ++j) pre = fseg_then(pre, FwdSeg{sX[j][lane], sY[j][lane], sCl[j]});
+        FwdSeg agg{sX[0][lane], sY[0][lane], sCl[0]};
+        if (w == 0) {
+#pragma unroll
+            for (int j = 1; j < SC_WARPS; ++j) agg = fseg_then(agg, FwdSeg{sX[j][lane], sY[j][lane], sCl[j]});
+            if (agg.cl) desc_publish(&dR.inc0[di * 32 + lane], agg.P, &dR.inc1[di * 32 + lane], agg.S);
+            else desc_publish(&dR.agg0[di * 32 + lane], agg.P, &dR.agg1[di * 32 + lane], agg.S);
+        }
+        __syncthreads();
+        FwdSeg carry{f4(1.f), f4(0.f), true};
+        if (c0 % W != 0) {   // a block's first chunk starts closed: nothing before it counts
+            carry = cta_lookback<FwdSeg>(
+                chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
+                [&](int64_t p, FwdSeg &ag, bool &aok, FwdSeg &ic, bool &iok) {
+                    const DescRead A = desc_read(&dR.agg0[(fb + p) * 32 + lane], &dR.agg1[(fb + p) * 32 + lane]);
+                    const DescRead I = desc_read(&dR.inc0[(fb + p) * 32 + lane], &dR.inc1[(fb + p) * 32 + lane]);
+                    ag = FwdSeg{A.a, A.b, false};
+                    aok = A.ok;
+                    ic = FwdSeg{I.a, I.b, true};
+                    iok = I.ok;
+                },
+                [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
+                FwdSeg{f4(1.f), f4(0.f), true}, status, sX, sY, sCl, s_ctl, w, lane);
+        }
+        if (w == 0) {
+            if (!agg.cl) {
+                const FwdSeg inc = fseg_then(carry, agg);
+                desc_publish(&dR.inc0[di * 32 + lane], inc.P, &dR.inc1[di * 32 + lane], inc.S);
+            }
+            sC0[lane] = carry.P;
+            sC1[lane] = carry.S;
+        }
+        __syncthreads();
+        G = fseg_then(FwdSeg{sC0[lane], sC1[lane], true}, pre);
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            if (t >= T) break;
+            const int r = w * L + k;
+            const float4 ev = srow(sg, r, lane) * srow(sc, r, lane), av = srow(sa, r, lane);
+            if (t % W == 0) G = FwdSeg{f4(1.f), ev, true};
+            else G = FwdSeg{G.P * av, fma4(G.P * av, ev, G.S), G.cl};
+            if (act) st4(R + base + t * N, G.S);   // kept in L2: the reverse chunks read it soon
+        }
+        // the rows are stored: raise the flag (the CTA barrier orders every thread's stores
+        // before thread 0's release)
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            st_release(flags + di, 0u);
+        }
+        return;
+    }
+
+    // ------------------------------------------------ reverse chunk (restarted at block ends)
+    {
+        float *dst[3] = {sg, sc, sa};
+        const int rows[3] = {TT, TT, TT + 1};
+        stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+    }
+    float4 hv[L + 1];
+    hv[0] = (act && t0 > 0 && t0 - 1 < T) ? ld_keep4(h + base + (t0 - 1) * N) : f4(0.f);
+#pragma unroll
+    for (int k = 0; k < L; ++k) hv[k + 1] = (act && t0 + k < T) ? ld_keep4(h + base + (t0 + k) * N) : f4(0.f);
+    mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
+
+    RevSeg G{f4(1.f), f4(0.f), false};
+#pragma unroll
+    for (int k = L - 1; k >= 0; --k) {
+        const int64_t t = t0 + k;
+        if (t >= T) continue;
+        const int r = w * L + k;
+        const float4 ev = srow(sg, r, lane) * srow(sc, r, lane);
+        const float4 bv = t + 1 < T ? srow(sa, r + 1, lane) : f4(0.f);
+        const bool end = (t == T - 1) || ((t + 1) % W == 0);
+        if (end) G = RevSeg{bv, ev, true};
+        else G = RevSeg{bv * G.Q, fma4(bv, G.S, ev), G.cl};
+    }
+    sX[w][lane] = G.Q;
+    sY[w][lane] = G.S;
+    if (lane == 0) sCl[w] = G.cl;
+    __syncthreads();
+    RevSeg post{f4(1.f), f4(0.f), false};
+    for (int j = w + 1; j < SC_WARPS; ++j) post = rseg_then(post, RevSeg{sX[j][lane], sY[j][lane], sCl[j]});
+    RevSeg agg{sX[0][lane], sY[0][lane], sCl[0]};
+    if (w == 0) {
+#pragma unroll
+        for (int j = 1; j < SC_WARPS; ++j) agg = rseg_then(agg, RevSeg{sX[j][lane], sY[j][lane], sCl[j]});
+        if (agg.cl) desc_publish(&dM.inc0[di * 32 + lane], agg.Q, &dM.inc1[di * 32 + lane], agg.S);
+        else desc_publish(&dM.agg0[di * 32 + lane], agg.Q, &dM.agg1[di * 32 + lane], agg.S);
+    }
+    float pz[DZ ? L : 1];
+    if (act) {
+#pragma unroll
+        for (int k = 0; k < L; ++k) {
+            const int64_t t = t0 + k;
+            if (t >= T) break;
+            const int r = w * L + k;
+            const float4 gk = srow(sg, r, lane), ck = srow(sc, r, lane);
+            st4(Dc + base + t * N, gk * hv[k + 1]);
+            st4(E + base + t * N, ck * hv[k + 1]);
+            if (DZ) pz[k] = dot4(as_stored<TD>(gk * hv[k + 1]), ck);
+            *reinterpret_cast<float4 *>(sg + r * SC_SLICE + lane * 4) = gk * ck;
+        }
+    }
+    __syncthreads();
+    // R rows of this chunk's window ends: once the R chunks holding them have stored them
+    // (their flags; rows past the sequence end read row T - 1, whose chunk is the last one),
+    // TMA brings rows c0 + W - 1 ... into the c rows (free after pass 1) while the look-back
+    // runs
+    const bool need_r = (c0 / W + 1) * W < T;
+    if (need_r && threadIdx.x == 0) {
+        const int64_t lo_row = c0 % W == 0 ? c0 + W : c0 + W - 1;
+        const int64_t hi_row = c0 + TT - 1 + W - 1;
+        const int64_t c_lo = (lo_row < T - 1 ? lo_row : T - 1) / TT, c_hi = (hi_row < T - 1 ? hi_row : T - 1) / TT;
+        for (int64_t pc = c_lo; pc <= c_hi; ++pc) {
+            bool ok = false;
+            for (int it = 0; it < SPIN_LIMIT && !ok; ++it) {
+                ok = ld_acquire(flags + fb + pc) == 0u;
+                if (!ok && it > 8) __nanosleep(64);
+                if (!ok && (it & 255) == 255 && *reinterpret_cast<volatile unsigned *>(status) != 0u) break;
+            }
+            if (!ok) record_timeout(status);
+        }
+        fence_proxy_async_global();   // the rows were stored through the generic proxy
+        fence_proxy_async_smem();     // the c rows were read through it
+        mbar_arrive_expect_tx(smem_u32(&s_bar), uint32_t(TT) * SC_SLICE * 4u);
+        tma_load_2d(smem_u32(sc), &mp.m[3], slice * SC_SLICE, int(b * T + c0 + W - 1), smem_u32(&s_bar));
+    }
+    RevSeg carry{f4(0.f), f4(0.f), true};
+    // a block's last chunk ends closed (W is whole chunks): nothing after it counts
+    if (chunk + 1 < nchunks && (c0 + TT) % W != 0) {
+        carry = cta_lookback<RevSeg>(
+            chunk + 1, 1, nchunks - 1 - chunk, RevSeg{f4(1.f), f4(0.f), false},
+            [&](int64_t p, RevSeg &ag, bool &aok, RevSeg &ic, bool &iok) {
+                const DescRead A = desc_read(&dM.agg0[(fb + p) * 32 + lane], &dM.agg1[(fb + p) * 32 + lane]);
+                const DescRead I = desc_read(&dM.inc0[(fb + p) * 32 + lane], &dM.inc1[(fb + p) * 32 + lane]);
+                ag = RevSeg{A.a, A.b, false};
+                aok = A.ok;
+                ic = RevSeg{I.a, I.b, true};
+                iok = I.ok;
+            },
+            [](const RevSeg &acc, const RevSeg &g) { return rseg_then(acc, g); },
+            RevSeg{f4(0.f), f4(0.f), true}, status, sX, sY, sCl, s_ctl, w, lane);
+    }
+    if (w == 0) {
+        if (!agg.cl) {
+            const RevSeg inc = rseg_then(agg, carry);
+            desc_publish(&dM.inc0[di * 32 + lane], inc.Q, &dM.inc1[di * 32 + lane], inc.S);
+        }
+        sC0[lane] = carry.Q;
+        sC1[lane] = carry.S;
+    }
+    __syncthreads();
+    G = rseg_then(post, RevSeg{sC0[lane], sC1[lane], true});
+    if (need_r) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
+    const float4 bav = (DZ && act) ? *reinterpret_cast<const float4 *>(b_a + ch) : f4(0.f);
+    static_assert(!DZ || L == 8, "the row dots are summed eight tokens at a time");
+    float vz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = L - 1; k >= 0; --k) {
+        const int64_t t = t0 + k;
+        if (t >= T) continue;
+        const int r = w * L + k;
+        const float4 ak = srow(sa, r, lane);
+        const float4 bk = t + 1 < T ? srow(sa, r + 1, lane) : f4(0.f);
+        const float4 ek = srow(sg, r, lane);
+        const bool end = (t == T - 1) || ((t + 1) % W == 0);
+        if (end) G = RevSeg{bk, ek, true};
+        else G = RevSeg{bk * G.Q, fma4(bk, G.S, ek), true};
+        float4 mu = G.S;
+        if (t % W != 0 && (t / W + 1) * W < T) {
+            // the window ends at min(t + W - 1, T - 1); past the sequence end the staged row
+            // is not this sequence's, so the last row is read directly
+            const float4 rk = t + W - 1 <= T - 1 ? srow(sc, r, lane)
+                                                 : (act ? ld_cg4(reinterpret_cast<const float4 *>(R + base + (T - 1) * N)) : f4(0.f));
+            mu = fma4(G.Q, rk, G.S);
+        }
+        const float4 dak = mu * hv[k] * ak * (f4(1.f) - ak);
+        if (act) {
+            st4(Du + base + t * N, mu);
+            st4(Da + base + t * N, dak);
+        }
+        if (DZ && act) {
+            const float4 za = make_float4(gate_z(ak.x, bav.x), gate_z(ak.y, bav.y), gate_z(ak.z, bav.z),
+                                          gate_z(ak.w, bav.w));
+            const float4 uk = hv[k + 1] - ak * hv[k];
+            vz[k & 7] = pz[k] + dot4(as_stored<TD>(dak), za) + dot4(as_stored<TD>(mu), uk);
+        }
+    }
+    if (DZ) {
+        const float tot = warp_sum8(vz, lane);
+        const int k = warp_sum8_index(lane);
+        if ((lane & 3) == 0 && t0 + k < T) dz[(b * T + t0 + k) * nslices + slice] = tot;
     }
 }
 
@@ -692,9 +1037,60 @@ cudaError_t launch_win_scan(const float *g, const float *c, const float *a, floa
     return cudaGetLastError();
 }
 
+// Scan workspace of the one-launch truncated adjoint: two descriptor sets and one flag
+// per chunk, laid out [ticket, R descriptors | ticket (unused), reverse descriptors | flags].
+static int64_t trunc_chunks(int64_t B, int64_t T, int N) {
+    return B * cdiv(N, SC_SLICE) * cdiv(T, SC_WARPS * SC_BWD_L);
+}
+static size_t trunc_desc_bytes(int64_t n) { return 256 + 4 * size_t(n) * 32 * sizeof(float4); }
+size_t trunc_ws_bytes(int64_t B, int64_t T, int N) {
+    const int64_t n = trunc_chunks(B, T, N);
+    return 2 * trunc_desc_bytes(n) + ((size_t(n) * 4 + 255) & ~size_t(255));
+}
+bool trunc_one_launch(int64_t T, int64_t W) { return W > 0 && W < T && W % (SC_WARPS * SC_BWD_L) == 0; }
+
+cudaError_t launch_trunc_scan(const float *g, const float *c, const float *a, const float *h, float *R, void *D_a,
+                              void *D_u, void *D_c, void *E, bool d_bf16, int64_t B, int64_t T, int N, int64_t W,
+                              void *ws, unsigned *status, cudaStream_t st, const float *b_a, float *dz) {
+    constexpr int L = SC_BWD_L, TT = SC_WARPS * L;
+    if (!trunc_one_launch(T, W)) return cudaErrorInvalidValue;
+    const int nslices = int(cdiv(N, SC_SLICE));
+    const int64_t nseq = B * nslices, nchunks = cdiv(T, TT), n = nseq * nchunks;
+    ScanMaps mp;
+    const float *arr[4] = {g, c, a, R};
+    const int rows[4] = {TT, TT, TT + 1, TT};
+    if (!scan_maps(mp, 4, arr, rows, B, T, N)) return cudaErrorInvalidValue;
+    char *p = static_cast<char *>(ws);
+    const ScanWs dR = scan_ws_carve(p, n), dM = scan_ws_carve(p + trunc_desc_bytes(n), n);
+    unsigned *flags = reinterpret_cast<unsigned *>(p + 2 * trunc_desc_bytes(n));
+    // every descriptor word and flag unset, the ticket at 0xFFFFFFFF: one memset
+    cudaError_t e = cudaMemsetAsync(ws, 0xFF, 2 * trunc_desc_bytes(n) + size_t(n) * 4, st);
+    if (e != cudaSuccess) return e;
+    const int64_t CB = W / TT;
+    const unsigned grid = unsigned(nseq * (2 * nchunks - CB));   // no R chunks for block 0
+    const size_t smem = staged_bytes(3 * TT + 1);
+#define ADJ_TRUNC(TDT, DZO)                                                                                      \
+    do {                                                                                                         \
+        if ((e = set_smem(k_trunc_scan<L, TDT, DZO>, smem)) != cudaSuccess) return e;                            \
+        k_trunc_scan<L, TDT, DZO><<<grid, 256, smem, st>>>(mp, h, R, static_cast<TDT *>(D_a), static_cast<TDT *>(D_u), \
+                                                          static_cast<TDT *>(D_c), static_cast<TDT *>(E), T, N,       \
+                                                          nslices, nseq, nchunks, W, dR, dM, flags, status, b_a, dz); \
+    } while (0)
+    if (d_bf16) {
+        if (dz) ADJ_TRUNC(__nv_bfloat16, true);
+        else ADJ_TRUNC(__nv_bfloat16, false);
+    } else {
+        if (dz) ADJ_TRUNC(float, true);
+        else ADJ_TRUNC(float, false);
+    }
+#undef ADJ_TRUNC
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, const float *h, const float *R,
                             void *D_a, void *D_u, void *D_c, void *E, bool d_bf16, int64_t B, int64_t T, int N,
-                            int64_t W, void *scan_ws, unsigned *status, cudaStream_t st) {
+                            int64_t W, void *scan_ws, unsigned *status, cudaStream_t st, const float *b_a,
+                            float *dz) {
     constexpr int L = SC_BWD_L, TT = SC_WARPS * L;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, TT);
@@ -708,20 +1104,27 @@ cudaError_t launch_bwd_scan(const float *g, const float *c, const float *a, cons
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(nseq * nchunks);
     const size_t smem = staged_bytes(3 * TT + 1);
-#define ADJ_BWD(TR, TDT)                                                                                          \
+#define ADJ_BWD(TR, TDT, DZO)                                                                                     \
     do {                                                                                                          \
-        if ((e = set_smem(k_bwd_scan<L, TR, TDT>, smem)) != cudaSuccess) return e;                                \
-        k_bwd_scan<L, TR, TDT><<<grid, 256, smem, st>>>(mp, h, R, static_cast<TDT *>(D_a), static_cast<TDT *>(D_u), \
-                                                        static_cast<TDT *>(D_c), static_cast<TDT *>(E), T, N, nslices,  \
-                                                        nseq, nchunks, trunc ? W : T, d, status);                 \
+        if ((e = set_smem(k_bwd_scan<L, TR, TDT, DZO>, smem)) != cudaSuccess) return e;                           \
+        k_bwd_scan<L, TR, TDT, DZO><<<grid, 256, smem, st>>>(mp, h, R, static_cast<TDT *>(D_a),                   \
+                                                             static_cast<TDT *>(D_u), static_cast<TDT *>(D_c),    \
+                                                             static_cast<TDT *>(E), T, N, nslices, nseq, nchunks, \
+                                                             trunc ? W : T, d, status, b_a, dz);                  \
+    } while (0)
+#define ADJ_BWD_DZ(TR, TDT)               \
+    do {                                  \
+        if (dz) ADJ_BWD(TR, TDT, true);   \
+        else ADJ_BWD(TR, TDT, false);     \
     } while (0)
     if (d_bf16) {
-        if (trunc) ADJ_BWD(true, __nv_bfloat16);
-        else ADJ_BWD(false, __nv_bfloat16);
+        if (trunc) ADJ_BWD_DZ(true, __nv_bfloat16);
+        else ADJ_BWD_DZ(false, __nv_bfloat16);
     } else {
-        if (trunc) ADJ_BWD(true, float);
-        else ADJ_BWD(false, float);
+        if (trunc) ADJ_BWD_DZ(true, float);
+        else ADJ_BWD_DZ(false, float);
     }
+#undef ADJ_BWD_DZ
 #undef ADJ_BWD
     return cudaGetLastError();
 }

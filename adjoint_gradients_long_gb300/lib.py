@@ -52,10 +52,10 @@ def load(path: str = LIB_PATH):
         lib.adj_workspace_bytes.argtypes = [_PD, ctypes.c_int, _I64]
         lib.adj_workspace_bytes.restype = _SZ
         lib.adj_fwd_scan.argtypes = [_PD, _PW] + [_VP] * 8 + [_SZ, _VP]
-        lib.adj_loss_mse.argtypes = [_PD] + [_VP] * 5 + [_SZ, _VP]
-        lib.adj_bwd_full.argtypes = [_PD, _PW] + [_VP] * 9 + [_SZ, _VP]
-        lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 8 + [_I64, _VP, _SZ, _VP]
-        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 11 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_loss_mse.argtypes = [_PD] + [_VP] * 6 + [_SZ, _VP]
+        lib.adj_bwd_full.argtypes = [_PD, _PW] + [_VP] * 11 + [_SZ, _VP]
+        lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 10 + [_I64, _VP, _SZ, _VP]
+        lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 15 + [ctypes.c_int, _VP, _SZ, _VP]
         lib.adj_rms_norm.argtypes = [_PD] + [_VP] * 4
         lib.adj_selftest_waits.argtypes = [_VP, _SZ, ctypes.c_int, _VP]
         lib.adj_selftest_waits.restype = ctypes.c_int
@@ -116,27 +116,29 @@ def fwd_scan(d, w, xhat, xres, a, c, h, y, y_x, ws, ws_bytes, stream=None):
                                ptr(y), ptr(y_x), ptr(ws), ws_bytes, _stream(stream)), "adj_fwd_scan")
 
 
-def loss_mse(d, y, target, gy, loss, ws, ws_bytes, stream=None):
-    _check(load().adj_loss_mse(ctypes.byref(d), ptr(y), ptr(target), ptr(gy), ptr(loss), ptr(ws), ws_bytes,
-                               _stream(stream)), "adj_loss_mse")
+def loss_mse(d, y, target, gy, loss, ws, ws_bytes, stream=None, gy_x=None):
+    _check(load().adj_loss_mse(ctypes.byref(d), ptr(y), ptr(target), ptr(gy), ptr(gy_x), ptr(loss), ptr(ws),
+                               ws_bytes, _stream(stream)), "adj_loss_mse")
 
 
-def bwd_full(d, w, a, c, h, gy, D_a, D_u, D_c, E, ws, ws_bytes, stream=None):
-    _check(load().adj_bwd_full(ctypes.byref(d), ctypes.byref(w), ptr(a), ptr(c), ptr(h), ptr(gy), ptr(D_a),
-                               ptr(D_u), ptr(D_c), ptr(E), ptr(ws), ws_bytes, _stream(stream)), "adj_bwd_full")
+def bwd_full(d, w, a, c, h, gy, D_a, D_u, D_c, E, ws, ws_bytes, stream=None, dz=None, gy_x=None):
+    _check(load().adj_bwd_full(ctypes.byref(d), ctypes.byref(w), ptr(a), ptr(c), ptr(h), ptr(gy), ptr(gy_x),
+                               ptr(D_a), ptr(D_u), ptr(D_c), ptr(E), ptr(dz), ptr(ws), ws_bytes, _stream(stream)),
+           "adj_bwd_full")
 
 
-def bwd_trunc(d, w, a, c, h, gy, D_a, D_u, D_c, E, Tbar, ws, ws_bytes, stream=None):
-    _check(load().adj_bwd_trunc(ctypes.byref(d), ctypes.byref(w), ptr(a), ptr(c), ptr(h), ptr(gy), ptr(D_a),
-                                ptr(D_u), ptr(D_c), ptr(E), int(Tbar), ptr(ws), ws_bytes, _stream(stream)),
-           "adj_bwd_trunc")
+def bwd_trunc(d, w, a, c, h, gy, D_a, D_u, D_c, E, Tbar, ws, ws_bytes, stream=None, dz=None, gy_x=None):
+    _check(load().adj_bwd_trunc(ctypes.byref(d), ctypes.byref(w), ptr(a), ptr(c), ptr(h), ptr(gy), ptr(gy_x),
+                                ptr(D_a), ptr(D_u), ptr(D_c), ptr(E), ptr(dz), int(Tbar), ptr(ws), ws_bytes,
+                                _stream(stream)), "adj_bwd_trunc")
 
 
 def param_grad(d, w, xhat, D_a, D_u, D_c, E, gy, dW_in, db_a, dW_o, gy_prev, dxhat, accumulate, ws, ws_bytes,
-               stream=None):
+               stream=None, r=None, dz=None, gy_x=None, gy_prev_x=None):
     _check(load().adj_param_grad(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(D_a), ptr(D_u), ptr(D_c), ptr(E),
-                                 ptr(gy), ptr(dW_in), ptr(db_a), ptr(dW_o), ptr(gy_prev), ptr(dxhat), int(accumulate),
-                                 ptr(ws), ws_bytes, _stream(stream)), "adj_param_grad")
+                                 ptr(gy), ptr(gy_x), ptr(dW_in), ptr(db_a), ptr(dW_o), ptr(gy_prev), ptr(gy_prev_x),
+                                 ptr(dxhat), ptr(r), ptr(dz), int(accumulate), ptr(ws), ws_bytes, _stream(stream)),
+           "adj_param_grad")
 
 
 def rms_norm(d, y, xhat, r, stream=None):

@@ -9,9 +9,10 @@ the normalised layer inputs):
   for k = 1..K: adj_rms_norm(y^{k-1})      xhat^k = y^{k-1} / r^{k-1}   (k >= 2; xhat^1 = input)
                 adj_fwd_scan(k)            stores a^k, c^k, h^k; y^k = y^{k-1} + ytilde^k
   adj_loss_mse                             gy^K = y^K - target, L
-  for k = K..1: adj_bwd_{full,trunc}(k)    VJP seeds D_a, D_u, D_c, E of layer k
-                adj_param_grad(k)          dW_in^k, db_a^k, dW_o^k and dxhat^k
-                adj_rms_norm_bwd(k)        gy^{k-1} = gy^k + J^T dxhat^k   (k >= 2)
+  for k = K..1: adj_bwd_{full,trunc}(k)    VJP seeds D_a, D_u, D_c, E of layer k (k >= 2: and
+                                           the row dots dz = xhat . dxhat)
+                adj_param_grad(k)          dW_in^k, db_a^k, dW_o^k and (k >= 2)
+                                           gy^{k-1} = gy^k + J^T dxhat^k through the normalisation
 """
 from __future__ import annotations
 
@@ -58,6 +59,10 @@ class AdjStack:
         self.target = z(B, T, P)
         self.D = [z(B, T, N, dtype=dt) for _ in range(4)]     # D_a, D_u, D_c, E
         self.gy = [z(B, T, P), z(B, T, P)]
+        # bf16 layers: the cotangents rounded to bf16, the operand their backward GEMMs read
+        self.gy_x = [z(B, T, P, dtype=torch.bfloat16), z(B, T, P, dtype=torch.bfloat16)] if x_bf16 else [None, None]
+        # per token and 128-channel group: xhat . dxhat of a normalised layer input
+        self.dz = z(B * T, (N + 127) // 128) if K > 1 else None
         self.loss = torch.zeros(1, dtype=torch.float64, device=dev)
         self.W_in = [z(P, 3 * N, dtype=xt) for _ in range(K)]
         self.b_a = [z(N) for _ in range(K)]
@@ -103,7 +108,8 @@ class AdjStack:
                          self.y[k], None, self.ws, self.ws_bytes, stream)
 
     def loss_grad(self, stream=None):
-        lib.loss_mse(self.dims, self.y[-1], self.target, self.gy[0], self.loss, self.ws, self.ws_bytes, stream)
+        lib.loss_mse(self.dims, self.y[-1], self.target, self.gy[0], self.loss, self.ws, self.ws_bytes, stream,
+                     gy_x=self.gy_x[0])
 
     def backward(self, Tbar=None, stream=None, accumulate=False, on_layer=None):
         """Adjoint pass and parameter gradients, layer K down to 1.  Tbar None = full."""
@@ -111,20 +117,23 @@ class AdjStack:
         for k in range(self.K - 1, -1, -1):
             gy = self.gy[cur]
             Da, Du, Dc, E = self.D
+            dz = self.dz if k > 0 else None
+            gx = self.gy_x[cur]
             if Tbar is None:
                 lib.bwd_full(self.dims, self.w[k], self.a[k], self.c[k], self.h[k], gy, Da, Du, Dc, E,
-                             self.ws, self.ws_bytes, stream)
+                             self.ws, self.ws_bytes, stream, dz=dz, gy_x=gx)
             else:
                 lib.bwd_trunc(self.dims, self.w[k], self.a[k], self.c[k], self.h[k], gy, Da, Du, Dc, E, Tbar,
-                              self.ws, self.ws_bytes, stream)
+                              self.ws, self.ws_bytes, stream, dz=dz, gy_x=gx)
             if on_layer is not None:
                 on_layer(k, self)
-            dx = self.gy[1 - cur] if k > 0 else None
+            # k >= 1: gy^{k-1} = gy^k + J^T dxhat^k through the normalised input, in the
+            # input-gradient GEMM's epilogue
+            gp = self.gy[1 - cur] if k > 0 else None
             lib.param_grad(self.dims, self.w[k], self.x[k], Da, Du, Dc, E, gy, self.dW_in[k],
-                           self.db_a[k], self.dW_o[k], None, dx, int(accumulate), self.ws, self.ws_bytes, stream)
-            if k > 0:
-                # gy^{k-1} = gy^k + J^T dxhat^k, in place over dxhat
-                lib.rms_norm_bwd(self.dims, self.y[k - 1], self.r[k - 1], dx, gy, dx, stream)
+                           self.db_a[k], self.dW_o[k], gp, None, int(accumulate), self.ws, self.ws_bytes, stream,
+                           r=self.r[k - 1] if k > 0 else None, dz=dz, gy_x=gx,
+                           gy_prev_x=self.gy_x[1 - cur] if k > 0 else None)
             cur = 1 - cur
 
     def step(self, Tbar=None, stream=None):

@@ -73,31 +73,50 @@ def truncation_errors(B: int, T: int, P: int, N: int, b_a_values, windows, seed:
     return rows
 
 
-def memory_report(key: str, window=None, device="cuda") -> dict:
-    """Device memory of one full-size step of workload `key` through the library (every
-    buffer the stack driver allocates: stored states, residual streams, seeds, cotangents,
-    gradients and the workspace), beside the stored-state counts of ``accounting``."""
+def memory_report(key: str, window=None, device="cuda", T=None, K=None) -> dict:
+    """Device memory of one step of workload `key` (optionally resized) through the library:
+    every buffer the stack driver allocates (stored states, residual streams, seeds,
+    cotangents, gradients, workspace), measured with the torch allocator after the inputs
+    are loaded, and the growth during the step itself (the library allocates nothing, so 0),
+    beside the counts of ``accounting``."""
     import torch
     from . import accounting, synth
     from .stack import AdjStack
 
     w = synth.workload(key)
+    T = w.T if T is None else T
+    K = w.K if K is None else K
     xb = 2 if w.x_dtype == "bf16" else 4
     torch.cuda.synchronize()
-    torch.cuda.reset_peak_memory_stats(device)
     base = torch.cuda.memory_allocated(device)
-    st = AdjStack(w.B, w.T, w.P, w.N, w.K, x_bf16=xb == 2, d_bf16=xb == 2, device=device,
-                  Tbar=window if window is not None and window < w.T else None)
-    st.load(synth.make_inputs(w))
+    st = AdjStack(w.B, T, w.P, w.N, K, x_bf16=xb == 2, d_bf16=xb == 2, device=device,
+                  Tbar=window if window is not None and window < T else None)
+    st.load(synth.make_inputs(w, T=T, K=K))
+    torch.cuda.synchronize()
+    held = torch.cuda.memory_allocated(device) - base
+    # the stack's own device tensors, byte for byte (the allocator's figure above rounds
+    # every allocation up, to 512 bytes or to a whole cached block)
+    tensors = []
+    for v in vars(st).values():
+        for t in (v if isinstance(v, list) else [v]):
+            if isinstance(t, torch.Tensor) and t.is_cuda:
+                tensors.append(t)
+    tensor_bytes = sum(t.untyped_storage().nbytes() for t in tensors if t is not st.ws)
+    torch.cuda.reset_peak_memory_stats(device)
+    before = torch.cuda.memory_allocated(device)
     st.step(window)
     torch.cuda.synchronize()
-    peak = torch.cuda.max_memory_allocated(device) - base
+    growth = torch.cuda.max_memory_allocated(device) - before
     ok = st.status() == 0
-    out = {"workload": key, "window": window if window is not None else "full", "B": w.B, "T": w.T, "K": w.K,
-           "P": w.P, "N": w.N, "device_peak_bytes": int(peak), "workspace_bytes": int(st.ws_bytes),
-           "stored_bytes": accounting.stored_bytes(w.B, w.T, w.K, w.N, w.P, xb),
-           "bptt_saved_bytes": accounting.bptt_saved_bytes(w.B, w.T, w.K, w.N, w.P, xb),
-           "checkpoint_saved_bytes": accounting.checkpoint_saved_bytes(w.B, w.T, w.K, w.N, w.P, xb),
+    bufs = accounting.stack_buffer_bytes(w.B, T, K, w.N, w.P, xb, xb)
+    out = {"workload": key, "window": window if window is not None else "full", "B": w.B, "T": T, "K": K,
+           "P": w.P, "N": w.N, "device_peak_bytes": int(held + growth), "held_bytes": int(held),
+           "tensor_bytes": int(tensor_bytes), "tensor_count": len(tensors) - 1,
+           "step_growth_bytes": int(growth), "workspace_bytes": int(st.ws_bytes),
+           "buffer_bytes": {k: v for k, v in bufs.items() if k != "buffers"}, "buffer_count": bufs["buffers"],
+           "stored_bytes": accounting.stored_bytes(w.B, T, K, w.N, w.P, xb),
+           "bptt_saved_bytes": accounting.bptt_saved_bytes(w.B, T, K, w.N, w.P, xb),
+           "checkpoint_saved_bytes": accounting.checkpoint_saved_bytes(w.B, T, K, w.N, w.P, xb),
            "device_status_ok": ok}
     del st
     torch.cuda.empty_cache()

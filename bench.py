@@ -174,19 +174,26 @@ def kernel_table(P, N, xb, db, trunc, K=1):
     # bf16 layers: the forward scan also reads c and writes c . h in bf16, which the
     # output projection reads instead of c and h in fp32
     chb = 2 * N if xb == 2 else 0
+    # bf16 layers: the cotangent gy also has a bf16 copy (written with it), which the
+    # backward GEMMs read instead of the fp32 values
+    gyx = 2 * P if xb == 2 else 0
+    gyr = 2 * P if xb == 2 else 4 * P
     return {
         "proj_in": dict(bytes=P * xb + 3 * N * 4, flops=2 * P * 3 * N),
         "fwd_scan": dict(bytes=3 * N * 4 + (N * 4 + chb if chb else 0)),
         "proj_out": dict(bytes=(chb if chb else 2 * N * 4) + res + P * 4, flops=2 * N * P),
-        "loss": dict(bytes=3 * P * 4),
-        "cot_proj": dict(bytes=P * 4 + N * 4, flops=2 * P * N),
+        "loss": dict(bytes=3 * P * 4 + gyx),
+        "cot_proj": dict(bytes=gyr + N * 4, flops=2 * P * N),
         "win_scan": dict(bytes=4 * N * 4),
         "bwd_scan": dict(bytes=4 * N * 4 + 4 * N * db + (N * 4 if trunc else 0)),
         "param_dW_in": dict(bytes=P * xb + 3 * N * db, flops=2 * P * 3 * N),
-        "param_dW_o": dict(bytes=N * db + P * 4, flops=2 * N * P),
+        "param_dW_o": dict(bytes=N * db + gyr, flops=2 * N * P),
         "colsum": dict(bytes=N * db),
-        # in a stack the input gradient is stored alone (dxhat); with one layer it is added to gy
-        "input_grad": dict(bytes=3 * N * db + (4 * P if K > 1 else 2 * P * 4), flops=2 * 3 * N * P),
+        # in a stack the input gradient goes through the normalised input in its epilogue: it
+        # reads gy, xhat, r and the row dots dz and writes gy_prev (and its bf16 copy); with
+        # one layer it is gy + dxhat
+        "input_grad": dict(bytes=3 * N * db + 2 * P * 4 + ((P * xb + 4 + 4 * ((N + 127) // 128) + gyx) if K > 1 else 0),
+                           flops=2 * 3 * N * P),
         "rms_norm": dict(bytes=4 * P + P * xb + 4),
         "rms_norm_bwd": dict(bytes=16 * P + 4),
     }

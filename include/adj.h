@@ -96,9 +96,11 @@ adj_status adj_fwd_scan(const adj_dims *dims, const adj_weights *w, const void *
 
 /* Loss of the last layer and its cotangent: L = sum_{b,t} 1/2 ||y_t - target_t||^2,
  * gy = y - target.  y, target, gy [B,T,P] fp32 (gy written; may alias y);
+ * gy_x [B,T,P] bf16: gy rounded to bf16 (written; NULL to skip; needs gy), the operand the
+ * bf16 layers' backward GEMMs read (see gy_x of adj_bwd_* and adj_param_grad);
  * loss: one device double (written; NULL to skip).  Uses dims->B, T, P only. */
 adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *target, float *gy,
-                        double *loss, void *ws, size_t ws_bytes, void *stream);
+                        void *gy_x, double *loss, void *ws, size_t ws_bytes, void *stream);
 
 /* Adjoint pass of one layer, full window ([AS] Core claim, Proposition 2, with
  * lambda_{t,i} = C_t prod_{j=i+1..t} A_j; the sum over t of dl_t/dy_t lambda_{t,i}
@@ -108,17 +110,24 @@ adj_status adj_loss_mse(const adj_dims *dims, const float *y, const float *targe
  *   D_a = mu_i . h_{i-1} . a_i (1 - a_i)   (vjp^{A_i}),   D_u = mu_i   (vjp^{B_i}),
  *   D_c = g_t . h_t,  E = c_t . h_t        (vjp^{C_t}),
  * all [B,T,N] in d_dtype.  a, c, h [B,T,N] fp32 from adj_fwd_scan; gy [B,T,P]
- * fp32 = dL/dy of this layer (the total cotangent). */
+ * fp32 = dL/dy of this layer (the total cotangent).  gy_x [B,T,P] bf16 (NULL to skip;
+ * bf16 layers only): gy rounded to bf16, read in place of gy by the product g = gy W_o^T
+ * (which rounds gy to bf16 in bf16 layers anyway).
+ * dz [B*T, ceil(N/128)] fp32 (NULL to skip; needs w->b_a): per token and group of 128
+ * channels, the sum of D_a z_a + D_u u + D_c c over the group, with the seeds as stored,
+ * z_a = logit(a_t) - b_a = xhat_t W_a and u_t = h_t - a_t h_{t-1} = xhat_t W_B.  Summed
+ * over the groups this is D_t . (xhat_t W_in) = xhat_t . dxhat_t, the row dot product
+ * that adj_param_grad needs for a normalised layer input (see r and dz there). */
 adj_status adj_bwd_full(const adj_dims *dims, const adj_weights *w, const float *a,
-                        const float *c, const float *h, const float *gy, void *D_a, void *D_u,
-                        void *D_c, void *E, void *ws, size_t ws_bytes, void *stream);
+                        const float *c, const float *h, const float *gy, const void *gy_x, void *D_a,
+                        void *D_u, void *D_c, void *E, float *dz, void *ws, size_t ws_bytes, void *stream);
 
 /* As adj_bwd_full, truncated to the window Tbar ([AS] Core claim, last sentence;
  * Referee Report on Section 4.3): mu_i sums only t with t - i < Tbar.  Tbar >= 1;
  * Tbar >= T gives the full result. */
 adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float *a,
-                         const float *c, const float *h, const float *gy, void *D_a, void *D_u,
-                         void *D_c, void *E, int64_t Tbar, void *ws, size_t ws_bytes,
+                         const float *c, const float *h, const float *gy, const void *gy_x, void *D_a,
+                         void *D_u, void *D_c, void *E, float *dz, int64_t Tbar, void *ws, size_t ws_bytes,
                          void *stream);
 
 /* Parameter gradients as reductions over all tokens ([AS] Core claim: the sum over
@@ -130,13 +139,20 @@ adj_status adj_bwd_trunc(const adj_dims *dims, const adj_weights *w, const float
  *   gy_prev [B,T,P] fp32 = gy + [D_a | D_u | D_c] W_in^T: the total cotangent of the
  *           layer below when that layer's output is this layer's input unchanged
  *           ([AS] residual identity; Proposition 3);
- *   dxhat   [B,T,P] fp32 = [D_a | D_u | D_c] W_in^T alone, for a normalised input
- *           (pass it to adj_rms_norm_bwd). */
+ *           with r and dz (both or neither): the layer input is the normalised residual
+ *           stream xhat = y / r of adj_rms_norm, and gy_prev = gy + (dxhat - xhat m / P) / r
+ *           with dxhat = [D_a | D_u | D_c] W_in^T and m = sum of dz's groups, the
+ *           cotangent of y through the normalisation ([AS] Load-bearing premise); r [B,T]
+ *           fp32 from adj_rms_norm, dz from adj_bwd_*, xhat as passed above;
+ *   dxhat   [B,T,P] fp32 = [D_a | D_u | D_c] W_in^T alone (for adj_rms_norm_bwd).
+ * bf16 layers only (NULL to skip): gy_x [B,T,P] bf16, gy rounded to bf16, read in place of
+ * gy by the dW_o product; gy_prev_x [B,T,P] bf16, gy_prev rounded to bf16 (written; needs
+ * gy_prev), the next layer's gy_x. */
 adj_status adj_param_grad(const adj_dims *dims, const adj_weights *w, const void *xhat,
                           const void *D_a, const void *D_u, const void *D_c, const void *E,
-                          const float *gy, float *dW_in, float *db_a, float *dW_o,
-                          float *gy_prev, float *dxhat, int accumulate, void *ws, size_t ws_bytes,
-                          void *stream);
+                          const float *gy, const void *gy_x, float *dW_in, float *db_a, float *dW_o,
+                          float *gy_prev, void *gy_prev_x, float *dxhat, const float *r, const float *dz,
+                          int accumulate, void *ws, size_t ws_bytes, void *stream);
 
 /* Normalised layer input of a stacked layer ([AS] Load-bearing premise: the layers
  * read "normalized inputs"): per token, xhat = y / r with

@@ -73,9 +73,38 @@ def test_rejects_small_workspace(L):
 
 def test_rejects_bad_window(L):
     d = lib.dims(1, 64, 16, 8)
-    st = L.adj_bwd_trunc(ctypes.byref(d), ctypes.byref(_w()), *([FAKE] * 8), 0, FAKE, 1 << 40, None)
+    st = L.adj_bwd_trunc(ctypes.byref(d), ctypes.byref(_w()), *([FAKE] * 4), None, *([FAKE] * 4), None, 0, FAKE,
+                         1 << 40, None)
     assert st == 1
     assert lib.workspace_bytes(d, lib.OP_BWD_TRUNC, 0) == 0
+
+
+def test_rejects_misused_optional_outputs(L):
+    """bf16 copies of the cotangent exist only for bf16 operands; the normalised-input
+    cotangent needs both r and dz and an output; dz needs the gate bias.  Refused before
+    anything launches (the pointers are never dereferenced)."""
+    f32 = lib.dims(1, 64, 16, 8)
+    bf = lib.dims(1, 64, 16, 8, lib.BF16, lib.BF16)
+    w = _w()
+    big = 1 << 40
+    # adj_bwd_full with gy_x on fp32 operands
+    assert L.adj_bwd_full(ctypes.byref(f32), ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                          None, FAKE, big, None) == 1
+    # dz without b_a
+    wn = lib.Weights(FAKE, None, FAKE)
+    assert L.adj_bwd_full(ctypes.byref(bf), ctypes.byref(wn), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+                          FAKE, FAKE, big, None) == 1
+
+    def pg(d, gy_x=None, gy_prev=None, gy_prev_x=None, dxhat=None, r=None, dz=None):
+        return L.adj_param_grad(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, gy_x, FAKE, FAKE,
+                                FAKE, gy_prev, gy_prev_x, dxhat, r, dz, 0, FAKE, big, None)
+    assert pg(f32, gy_x=FAKE) == 1                         # bf16 copy with fp32 operands
+    assert pg(bf, gy_prev_x=FAKE) == 1                     # a copy of an output not asked for
+    assert pg(bf, gy_prev=FAKE, r=FAKE) == 1               # r without dz
+    assert pg(bf, dxhat=FAKE, r=FAKE, dz=FAKE) == 1        # the normalised cotangent goes to gy_prev
+    assert pg(bf, gy_prev=FAKE, dxhat=FAKE) == 1           # at most one input cotangent
+    # adj_loss_mse: a bf16 copy needs gy
+    assert L.adj_loss_mse(ctypes.byref(bf), FAKE, FAKE, None, FAKE, FAKE, FAKE, big, None) == 1
 
 
 def test_workspace_sizes_grow_with_problem(L):

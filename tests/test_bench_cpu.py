@@ -87,8 +87,11 @@ def test_kernel_table_stack_entries():
     t = bench.kernel_table(P, N, 2, 2, True, K)
     # the normalisation's backward reads y, dxhat, gy and writes gy_prev (fp32) plus r
     assert t["rms_norm_bwd"]["bytes"] == 16 * P + 4
-    # in a stack the input gradient stores dxhat alone
-    assert t["input_grad"]["bytes"] == 3 * N * 2 + 4 * P
+    # in a stack the input gradient reads D, gy, xhat, r and the row dots, and writes gy_prev
+    # and its bf16 copy
+    assert t["input_grad"]["bytes"] == 3 * N * 2 + 8 * P + 2 * P + 4 + 4 * 2 + 2 * P
+    # the backward GEMMs read the cotangent's bf16 copy
+    assert t["cot_proj"]["bytes"] == 2 * P + 4 * N and t["param_dW_o"]["bytes"] == 2 * N + 2 * P
     # proj_out: c . h read in bf16, y written, the residual read (bf16 input once, fp32
     # stream K-1 times); the forward scan reads a, u, c and writes h and c . h
     assert t["proj_out"]["bytes"] == 2 * N + 4 * P + (2 * P + 3 * 4 * P) / 4

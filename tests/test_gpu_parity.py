@@ -118,8 +118,11 @@ def test_prefix_at_stated_window(key, Tbar):
 
 # --------------------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("T,B,Tbar", [(1, 1, None), (1, 2, 1), (33, 3, None), (33, 3, 32), (64, 1, 64), (65, 2, 2)])
+@pytest.mark.parametrize("T,B,Tbar", [(1, 1, None), (1, 2, 1), (33, 3, None), (33, 3, 32), (64, 1, 64), (65, 2, 2),
+                                      (129, 1, 64), (300, 3, 64), (300, 2, 128), (640, 1, 64), (700, 2, 192)])
 def test_small_and_ragged(T, B, Tbar):
+    """Degenerate and ragged sizes; windows of whole 64-token chunks take the one-launch
+    truncated adjoint (one-chunk blocks, a ragged last block, several blocks)."""
     compare(synth.make_inputs("ssm1_p16", T=T, B=B), Tbar, False)
 
 

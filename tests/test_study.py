@@ -82,3 +82,26 @@ def test_storage_counts_relations():
             B * T * P * 4 + A.bptt_saved_bytes(B, T, 100, N, P, xb))
         for K in (1, 8, 100):
             assert A.bptt_saved_bytes(B, T, K, N, P, xb) - A.stored_bytes(B, T, K, N, P, xb) == B * T * K * N * 4
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("key,T,K,window", [("ssm8_p512", 1024, 3, 256), ("ssm1_p128", 2048, 1, None)])
+def test_step_memory_is_the_counted_buffers(key, T, K, window):
+    """The device memory one step holds is the buffers the stack driver allocates, exactly as
+    counted from the shapes (accounting.stack_buffer_bytes), plus the caller-sized
+    workspace; the step itself allocates nothing; what is kept between the passes is at
+    least the stored-state count."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from adjoint_gradients_long_gb300 import build, study
+    build.build()
+    r = study.memory_report(key, window, T=T, K=K)
+    assert r["device_status_ok"]
+    # every buffer the stack holds, byte for byte, is one the count names
+    assert r["tensor_bytes"] == sum(r["buffer_bytes"].values()), r
+    assert r["tensor_count"] == r["buffer_count"], r
+    # the allocator holds those plus the workspace (rounded up); the step allocates nothing
+    assert r["held_bytes"] >= r["tensor_bytes"] + r["workspace_bytes"], r
+    assert r["step_growth_bytes"] == 0, r
+    assert r["held_bytes"] >= r["stored_bytes"]
