@@ -82,9 +82,9 @@ cudaError_t launch_fwd_scan(const float *a, const float *u, float *h, int64_t B,
 cudaError_t launch_win_scan(const float *g, const float *c, const float *a, float *R, int64_t B,
                             int64_t T, int N, int64_t Tbar, void *scan_ws, unsigned *status,
                             cudaStream_t st);
-// The truncated adjoint in one launch (window scan and reverse scan interleaved block by
-// block), for windows of whole scan chunks (trunc_one_launch); its scan workspace is
-// trunc_ws_bytes.  R [B,T,N] is its scratch for the window sums.
+// The truncated adjoint in one reverse pass (no separate window scan), for windows of whole
+// scan chunks (trunc_one_launch); its scan workspace is trunc_ws_bytes.  R [B,T,N] is its
+// scratch for the chunk-local window sums.
 bool trunc_one_launch(int64_t T, int64_t W);
 size_t trunc_ws_bytes(int64_t B, int64_t T, int N);
 cudaError_t launch_trunc_scan(const float *g, const float *c, const float *a, const float *h, float *R, void *D_a,

@@ -684,53 +684,44 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     }
 }
 
-// ============================================================================ truncated adjoint in one launch
-// The window scan R (k_win_scan) and the truncated reverse scan (k_bwd_scan<TRUNC>) in one
-// grid, for windows that are whole chunks (W % (8 L) == 0).  With blocks of W tokens, R of
-// block b+1 is read only by the reverse scan of block b, and both scans restart at every
-// block edge.  The tickets therefore run block by block from the end:
-//     R(nb-1), rev(nb-1), R(nb-2), rev(nb-2), ..., R(1), rev(1), rev(0)
-// (R of block 0 is never read).  R chunks go forward through their block and reverse
-// chunks backward, so every look-back stays inside one block and waits only on CTAs with
-// earlier tickets.  An R chunk raises a flag once its rows are stored; a reverse chunk
-// waits (bounded) on the flags of the R chunks its window ends fall in, all of which
-// have earlier tickets.  The g, c and a rows of a block are read by its R chunks and
-// then again by its reverse chunks a group of tickets later, mostly from L2, and R
-// lives between its writer and its reader in L2: HBM sees about the bytes of the full
-// (untruncated) reverse scan.
-struct TruncTicket {
-    bool rev;          // reverse-scan chunk (else an R chunk)
-    int64_t chunk, seq;
-};
-__device__ __forceinline__ TruncTicket trunc_ticket(int64_t tk, int64_t nseq, int64_t nchunks, int64_t CB) {
-    const int64_t nb = (nchunks + CB - 1) / CB, cl = nchunks - (nb - 1) * CB;
-    TruncTicket r;
-    int64_t b, j;
-    const int64_t s0 = cl * nseq, sb = CB * nseq;
-    if (tk < 2 * s0) {
-        b = nb - 1;
-        r.rev = tk >= s0;
-        j = r.rev ? tk - s0 : tk;
-    } else {
-        const int64_t u = tk - 2 * s0, pp = u / (2 * sb), q = u - pp * 2 * sb;
-        b = nb - 2 - pp;
-        r.rev = b == 0 || q >= sb;
-        j = (b == 0 || q < sb) ? q : q - sb;
+// ============================================================================ truncated adjoint in one pass
+// The truncated adjoint in one reverse pass, for windows that are whole chunks
+// (W % (8 L) == 0; blocks of W tokens then start at chunk starts).  With blocks of W tokens
+// and s the start of the block after token i's, mu^W_i = S_i + Q_i R(i + W - 1), where R is
+// the forward scan restarted at every block start (see the reverse scan above).  R is never
+// scanned in a pass of its own:
+//   * every chunk scans e = g c forward over its own rows only and stores these chunk-local
+//     values R_loc (restarted at a block start, so a block's first chunk is closed), then
+//     publishes the chunk's forward aggregate;
+//   * the chunk that starts a block -- in reverse order the last of its block to run --
+//     folds its block's aggregates into inclusive forward prefixes F and publishes them;
+//   * a chunk of the block before reads the one prefix X = F of the chunk preceding its
+//     window ends and gets R(m) = Sigma_X + Pi_X R_loc(m) from the stored local values, which
+//     TMA brings into the freed c rows while its look-back runs.
+// Chunks run in reverse order (one ticket each, like the full reverse scan), so every wait
+// is on a CTA with an earlier ticket: the block's other chunks (aggregates), the block
+// after's first chunk (prefixes).  Writers fence before they publish and readers after
+// they observe, so the stored R_loc rows are visible to the TMA that reads them.  HBM sees
+// the bytes of the full reverse scan plus the R_loc round trip, which mostly stays in L2.
+
+// Wait (bounded) until a forward descriptor slot of this lane is published; returns it.
+__device__ __forceinline__ FwdSeg wait_fdesc(const float4 *p0, const float4 *p1, unsigned *status) {
+    for (int it = 0; it < SPIN_LIMIT; ++it) {
+        const DescRead d = desc_read(p0, p1);
+        if (__all_sync(0xffffffffu, d.ok)) return FwdSeg{d.a, d.b, false};
+        if (it > 8) __nanosleep(64);
+        if ((it & 255) == 255 && *reinterpret_cast<volatile unsigned *>(status) != 0u) break;
     }
-    const int64_t cb = b == nb - 1 ? cl : CB, pos = j / nseq;
-    r.seq = j - pos * nseq;
-    r.chunk = r.rev ? b * CB + cb - 1 - pos : b * CB + pos;
-    return r;
+    record_timeout(status);
+    return FwdSeg{f4(1.f), f4(0.f), false};
 }
 
-// dR: descriptors of the R scan; dM: of the reverse scan; flags[seq * nchunks + chunk]:
-// 0 once R chunk `chunk` of sequence `seq` is stored (0xFFFFFFFF before).
 template <int L, typename TD, bool DZ>
 __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
-                                                      float *__restrict__ R, TD *__restrict__ Da, TD *__restrict__ Du,
+                                                      float *__restrict__ Rl, TD *__restrict__ Da, TD *__restrict__ Du,
                                                       TD *__restrict__ Dc, TD *__restrict__ E, int64_t T, int N,
                                                       int nslices, int64_t nseq, int64_t nchunks, int64_t W,
-                                                      ScanWs dR, ScanWs dM, unsigned *flags, unsigned *status,
+                                                      ScanWs dM, ScanWs dF, unsigned *status,
                                                       const float *__restrict__ b_a, float *__restrict__ dz) {
     constexpr int TT = SC_WARPS * L;
     extern __shared__ uint8_t sm_dyn[];
@@ -742,25 +733,30 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
     __shared__ bool sCl[SC_WARPS];
     __shared__ int s_ctl[SC_WARPS + 2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const TruncTicket tkt = trunc_ticket(chunk_ticket(dR, &s_ticket, &s_bar, &s_abort), nseq, nchunks, W / TT);
-    const int64_t chunk = tkt.chunk, seq = tkt.seq;
+    const int64_t tk = chunk_ticket(dM, &s_ticket, &s_bar, &s_abort), chunk = nchunks - 1 - tk / nseq, seq = tk % nseq;
     const int64_t b = seq / nslices;
     const int slice = int(seq % nslices), ch = slice * SC_SLICE + lane * 4;
     const bool act = ch < N;
     const int64_t c0 = chunk * TT, t0 = c0 + w * L;
     const int64_t base = b * T * N + ch;
     const int64_t di = seq * nchunks + chunk, fb = seq * nchunks;
+    const int64_t CB = W / TT, blk = c0 / W;
+    const bool first_of_block = c0 % W == 0;
+    {
+        float *dst[3] = {sg, sc, sa};
+        const int rows[3] = {TT, TT, TT + 1};
+        stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
+    }
+    float4 hv[L + 1];
+    hv[0] = (act && t0 > 0 && t0 - 1 < T) ? ld_keep4(h + base + (t0 - 1) * N) : f4(0.f);
+#pragma unroll
+    for (int k = 0; k < L; ++k) hv[k + 1] = (act && t0 + k < T) ? ld_keep4(h + base + (t0 + k) * N) : f4(0.f);
+    mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
 
-    if (!tkt.rev) {
-        // ------------------------------------------------ R chunk (forward, restarted at block starts)
-        {
-            // the maps are the reverse chunks': a's box has one row more, which lands unused
-            // (the barrier must expect every byte the boxes deliver)
-            float *dst[3] = {sg, sc, sa};
-            const int rows[3] = {TT, TT, TT + 1};
-            stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
-        }
-        mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
+    // ---------------------------------------------------------------- forward, chunk-local
+    // R_loc of this chunk's rows and the chunk's forward aggregate (blocks after the first
+    // only: R of block 0 is never read)
+    if (blk > 0) {
         FwdSeg G{f4(1.f), f4(0.f), false};
 #pragma unroll
         for (int k = 0; k < L; ++k) {
@@ -775,41 +771,12 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
         sY[w][lane] = G.S;
         if (lane == 0) sCl[w] = G.cl;
         __syncthreads();
-        FwdSeg pre{f4(1.f), f4(0.f), false};
+        FwdSeg pre{f4(1.f), f4(0.f), true};   // the chunk start: nothing before it
         for (int j = 0; j < w; ++j) pre = fseg_then(pre, FwdSeg{sX[j][lane], sY[j][lane], sCl[j]});
-        FwdSeg agg{sX[0][lane], sY[0][lane], sCl[0]};
-        if (w == 0) {
-#pragma unroll
-            for (int j = 1; j < SC_WARPS; ++j) agg = fseg_then(agg, FwdSeg{sX[j][lane], sY[j][lane], sCl[j]});
-            if (agg.cl) desc_publish(&dR.inc0[di * 32 + lane], agg.P, &dR.inc1[di * 32 + lane], agg.S);
-            else desc_publish(&dR.agg0[di * 32 + lane], agg.P, &dR.agg1[di * 32 + lane], agg.S);
-        }
-        __syncthreads();
-        FwdSeg carry{f4(1.f), f4(0.f), true};
-        if (c0 % W != 0) {   // a block's first chunk starts closed: nothing before it counts
-            carry = cta_lookback<FwdSeg>(
-                chunk - 1, -1, chunk, FwdSeg{f4(1.f), f4(0.f), false},
-                [&](int64_t p, FwdSeg &ag, bool &aok, FwdSeg &ic, bool &iok) {
-                    const DescRead A = desc_read(&dR.agg0[(fb + p) * 32 + lane], &dR.agg1[(fb + p) * 32 + lane]);
-                    const DescRead I = desc_read(&dR.inc0[(fb + p) * 32 + lane], &dR.inc1[(fb + p) * 32 + lane]);
-                    ag = FwdSeg{A.a, A.b, false};
-                    aok = A.ok;
-                    ic = FwdSeg{I.a, I.b, true};
-                    iok = I.ok;
-                },
-                [](const FwdSeg &acc, const FwdSeg &g) { return fseg_then(g, acc); },
-                FwdSeg{f4(1.f), f4(0.f), true}, status, sX, sY, sCl, s_ctl, w, lane);
-        }
-        if (w == 0) {
-            if (!agg.cl) {
-                const FwdSeg inc = fseg_then(carry, agg);
-                desc_publish(&dR.inc0[di * 32 + lane], inc.P, &dR.inc1[di * 32 + lane], inc.S);
-            }
-            sC0[lane] = carry.P;
-            sC1[lane] = carry.S;
-        }
-        __syncthreads();
-        G = fseg_then(FwdSeg{sC0[lane], sC1[lane], true}, pre);
+        FwdSeg agg{f4(1.f), f4(0.f), true};
+        if (w == 0)
+            for (int j = 0; j < SC_WARPS; ++j) agg = fseg_then(agg, FwdSeg{sX[j][lane], sY[j][lane], sCl[j]});
+        G = pre;
 #pragma unroll
         for (int k = 0; k < L; ++k) {
             const int64_t t = t0 + k;
@@ -818,30 +785,41 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
             const float4 ev = srow(sg, r, lane) * srow(sc, r, lane), av = srow(sa, r, lane);
             if (t % W == 0) G = FwdSeg{f4(1.f), ev, true};
             else G = FwdSeg{G.P * av, fma4(G.P * av, ev, G.S), G.cl};
-            if (act) st4(R + base + t * N, G.S);   // kept in L2: the reverse chunks read it soon
+            if (act) st4(Rl + base + t * N, G.S);   // kept in L2: the block before reads it soon
         }
-        // the rows are stored: raise the flag (the CTA barrier orders every thread's stores
-        // before thread 0's release)
-        __syncthreads();
-        if (threadIdx.x == 0) {
+        __syncthreads();   // every R_loc row stored (and sX/sY free again)
+        if (w == 0) {
             __threadfence();
-            st_release(flags + di, 0u);
+            desc_publish(&dF.agg0[di * 32 + lane], agg.P, &dF.agg1[di * 32 + lane], agg.S);
         }
-        return;
+        // the block's first chunk runs last of its block: fold the block's aggregates into the
+        // inclusive prefixes the block before reads; warp j folds chunks [j q, (j + 1) q)
+        if (first_of_block) {
+            const int64_t cb = (c0 + W <= T ? W : T - c0 + TT - 1) / TT;   // chunks in this block
+            const int64_t q = (cb + SC_WARPS - 1) / SC_WARPS, j0 = w * q, j1 = j0 + q < cb ? j0 + q : cb;
+            FwdSeg part{f4(1.f), f4(0.f), false};
+            for (int64_t j = j0; j < j1; ++j) {
+                const int64_t cj = fb + chunk + j;
+                FwdSeg a_j = wait_fdesc(&dF.agg0[cj * 32 + lane], &dF.agg1[cj * 32 + lane], status);
+                part = fseg_then(part, a_j);
+            }
+            sX[w][lane] = part.P;
+            sY[w][lane] = part.S;
+            __syncthreads();
+            FwdSeg run{f4(1.f), f4(0.f), true};   // the block start
+            for (int j = 0; j < w; ++j) run = fseg_then(run, FwdSeg{sX[j][lane], sY[j][lane], false});
+            __threadfence();   // every aggregate observed before any prefix is published
+            for (int64_t j = j0; j < j1; ++j) {
+                const int64_t cj = fb + chunk + j;
+                const DescRead d = desc_read(&dF.agg0[cj * 32 + lane], &dF.agg1[cj * 32 + lane]);
+                run = fseg_then(run, FwdSeg{d.a, d.b, false});
+                desc_publish(&dF.inc0[cj * 32 + lane], run.P, &dF.inc1[cj * 32 + lane], run.S);
+            }
+            __syncthreads();   // sX/sY free again
+        }
     }
 
-    // ------------------------------------------------ reverse chunk (restarted at block ends)
-    {
-        float *dst[3] = {sg, sc, sa};
-        const int rows[3] = {TT, TT, TT + 1};
-        stage_chunk(mp, 3, dst, rows, slice * SC_SLICE, b * T + c0, &s_bar);
-    }
-    float4 hv[L + 1];
-    hv[0] = (act && t0 > 0 && t0 - 1 < T) ? ld_keep4(h + base + (t0 - 1) * N) : f4(0.f);
-#pragma unroll
-    for (int k = 0; k < L; ++k) hv[k + 1] = (act && t0 + k < T) ? ld_keep4(h + base + (t0 + k) * N) : f4(0.f);
-    mbar_wait(smem_u32(&s_bar), 0, &s_abort, status);
-
+    // ---------------------------------------------------------------- reverse (restarted at block ends)
     RevSeg G{f4(1.f), f4(0.f), false};
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
@@ -882,28 +860,28 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
         }
     }
     __syncthreads();
-    // R rows of this chunk's window ends: once the R chunks holding them have stored them
-    // (their flags; rows past the sequence end read row T - 1, whose chunk is the last one),
-    // TMA brings rows c0 + W - 1 ... into the c rows (free after pass 1) while the look-back
-    // runs
-    const bool need_r = (c0 / W + 1) * W < T;
-    if (need_r && threadIdx.x == 0) {
-        const int64_t lo_row = c0 % W == 0 ? c0 + W : c0 + W - 1;
-        const int64_t hi_row = c0 + TT - 1 + W - 1;
-        const int64_t c_lo = (lo_row < T - 1 ? lo_row : T - 1) / TT, c_hi = (hi_row < T - 1 ? hi_row : T - 1) / TT;
-        for (int64_t pc = c_lo; pc <= c_hi; ++pc) {
-            bool ok = false;
-            for (int it = 0; it < SPIN_LIMIT && !ok; ++it) {
-                ok = ld_acquire(flags + fb + pc) == 0u;
-                if (!ok && it > 8) __nanosleep(64);
-                if (!ok && (it & 255) == 255 && *reinterpret_cast<volatile unsigned *>(status) != 0u) break;
-            }
-            if (!ok) record_timeout(status);
+    // The window ends m = min(t + W - 1, T - 1) of this chunk's tokens lie in the next block,
+    // in chunk cx = chunk + CB - 1 (only m = c0 + W - 1, the end of cx), in chunk cx + 1, or
+    // at T - 1 in the last chunk cl.  R(m) is then the inclusive prefix of cx (end of cx),
+    // that of cl (m = T - 1), or, inside cx + 1, the prefix of cx composed with the stored
+    // local value (identity prefix when cx + 1 starts the block, i.e. this chunk starts its
+    // own).  Those rows come by TMA into the freed c rows while the look-back runs, once cx + 1's
+    // prefix -- published after every R_loc row of the block was stored -- is seen.
+    const bool need_r = (blk + 1) * W < T;
+    const int64_t cl = nchunks - 1, cx = chunk + CB - 1;
+    const bool use_rows = need_r && c0 + W + 1 < T;                       // some m inside cx + 1
+    const bool use_x = need_r && !first_of_block && c0 + W < T;           // prefix of cx needed
+    const bool use_end = need_r && c0 + TT + W - 2 >= T - 1;              // some m clamped to T - 1
+    if (use_rows && w == 0) {
+        (void)wait_fdesc(&dF.inc0[(fb + cx + 1) * 32 + lane], &dF.inc1[(fb + cx + 1) * 32 + lane], status);
+        if (lane == 0) {
+            __threadfence();
+            fence_proxy_async_global();   // the rows were stored through the generic proxy
+            fence_proxy_async_smem();     // the c rows were read through it
+            mbar_arrive_expect_tx(smem_u32(&s_bar), uint32_t(TT) * SC_SLICE * 4u);
+            tma_load_2d(smem_u32(sc), &mp.m[3], slice * SC_SLICE, int(b * T + c0 + W - 1), smem_u32(&s_bar));
         }
-        fence_proxy_async_global();   // the rows were stored through the generic proxy
-        fence_proxy_async_smem();     // the c rows were read through it
-        mbar_arrive_expect_tx(smem_u32(&s_bar), uint32_t(TT) * SC_SLICE * 4u);
-        tma_load_2d(smem_u32(sc), &mp.m[3], slice * SC_SLICE, int(b * T + c0 + W - 1), smem_u32(&s_bar));
+        __syncwarp();
     }
     RevSeg carry{f4(0.f), f4(0.f), true};
     // a block's last chunk ends closed (W is whole chunks): nothing after it counts
@@ -930,11 +908,16 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
         sC1[lane] = carry.S;
     }
     __syncthreads();
+    // this lane's parts of the prefixes it reads (bounded waits on validated descriptors)
+    FwdSeg X{f4(1.f), f4(0.f), true}, XE{f4(1.f), f4(0.f), true};
+    if (use_x) X = wait_fdesc(&dF.inc0[(fb + cx) * 32 + lane], &dF.inc1[(fb + cx) * 32 + lane], status);
+    if (use_end) XE = wait_fdesc(&dF.inc0[(fb + cl) * 32 + lane], &dF.inc1[(fb + cl) * 32 + lane], status);
     G = rseg_then(post, RevSeg{sC0[lane], sC1[lane], true});
-    if (need_r) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
+    if (use_rows) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
     const float4 bav = (DZ && act) ? *reinterpret_cast<const float4 *>(b_a + ch) : f4(0.f);
     static_assert(!DZ || L == 8, "the row dots are summed eight tokens at a time");
     float vz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int64_t xend = (cx + 1) * TT;   // window ends before this row are the end of chunk cx
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
         const int64_t t = t0 + k;
@@ -947,11 +930,11 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
         if (end) G = RevSeg{bk, ek, true};
         else G = RevSeg{bk * G.Q, fma4(bk, G.S, ek), true};
         float4 mu = G.S;
-        if (t % W != 0 && (t / W + 1) * W < T) {
-            // the window ends at min(t + W - 1, T - 1); past the sequence end the staged row
-            // is not this sequence's, so the last row is read directly
-            const float4 rk = t + W - 1 <= T - 1 ? srow(sc, r, lane)
-                                                 : (act ? ld_cg4(reinterpret_cast<const float4 *>(R + base + (T - 1) * N)) : f4(0.f));
+        if (t % W != 0 && need_r) {
+            const int64_t m = t + W - 1 <= T - 1 ? t + W - 1 : T - 1;
+            const float4 rk = m == T - 1 ? XE.S
+                              : m < xend  ? X.S
+                                          : fma4(X.P, srow(sc, int(m - (c0 + W - 1)), lane), X.S);
             mu = fma4(G.Q, rk, G.S);
         }
         const float4 dak = mu * hv[k] * ak * (f4(1.f) - ak);
@@ -1037,16 +1020,13 @@ cudaError_t launch_win_scan(const float *g, const float *c, const float *a, floa
     return cudaGetLastError();
 }
 
-// Scan workspace of the one-launch truncated adjoint: two descriptor sets and one flag
-// per chunk, laid out [ticket, R descriptors | ticket (unused), reverse descriptors | flags].
+// Scan workspace of the one-pass truncated adjoint: two descriptor sets, laid out
+// [ticket, reverse descriptors | ticket (unused), forward descriptors].
 static int64_t trunc_chunks(int64_t B, int64_t T, int N) {
     return B * cdiv(N, SC_SLICE) * cdiv(T, SC_WARPS * SC_BWD_L);
 }
 static size_t trunc_desc_bytes(int64_t n) { return 256 + 4 * size_t(n) * 32 * sizeof(float4); }
-size_t trunc_ws_bytes(int64_t B, int64_t T, int N) {
-    const int64_t n = trunc_chunks(B, T, N);
-    return 2 * trunc_desc_bytes(n) + ((size_t(n) * 4 + 255) & ~size_t(255));
-}
+size_t trunc_ws_bytes(int64_t B, int64_t T, int N) { return 2 * trunc_desc_bytes(trunc_chunks(B, T, N)); }
 bool trunc_one_launch(int64_t T, int64_t W) { return W > 0 && W < T && W % (SC_WARPS * SC_BWD_L) == 0; }
 
 cudaError_t launch_trunc_scan(const float *g, const float *c, const float *a, const float *h, float *R, void *D_a,
@@ -1061,20 +1041,18 @@ cudaError_t launch_trunc_scan(const float *g, const float *c, const float *a, co
     const int rows[4] = {TT, TT, TT + 1, TT};
     if (!scan_maps(mp, 4, arr, rows, B, T, N)) return cudaErrorInvalidValue;
     char *p = static_cast<char *>(ws);
-    const ScanWs dR = scan_ws_carve(p, n), dM = scan_ws_carve(p + trunc_desc_bytes(n), n);
-    unsigned *flags = reinterpret_cast<unsigned *>(p + 2 * trunc_desc_bytes(n));
-    // every descriptor word and flag unset, the ticket at 0xFFFFFFFF: one memset
-    cudaError_t e = cudaMemsetAsync(ws, 0xFF, 2 * trunc_desc_bytes(n) + size_t(n) * 4, st);
+    const ScanWs dM = scan_ws_carve(p, n), dF = scan_ws_carve(p + trunc_desc_bytes(n), n);
+    // every descriptor word unset, the ticket at 0xFFFFFFFF: one memset
+    cudaError_t e = cudaMemsetAsync(ws, 0xFF, 2 * trunc_desc_bytes(n), st);
     if (e != cudaSuccess) return e;
-    const int64_t CB = W / TT;
-    const unsigned grid = unsigned(nseq * (2 * nchunks - CB));   // no R chunks for block 0
+    const unsigned grid = unsigned(n);
     const size_t smem = staged_bytes(3 * TT + 1);
 #define ADJ_TRUNC(TDT, DZO)                                                                                      \
     do {                                                                                                         \
         if ((e = set_smem(k_trunc_scan<L, TDT, DZO>, smem)) != cudaSuccess) return e;                            \
         k_trunc_scan<L, TDT, DZO><<<grid, 256, smem, st>>>(mp, h, R, static_cast<TDT *>(D_a), static_cast<TDT *>(D_u), \
                                                           static_cast<TDT *>(D_c), static_cast<TDT *>(E), T, N,       \
-                                                          nslices, nseq, nchunks, W, dR, dM, flags, status, b_a, dz); \
+                                                          nslices, nseq, nchunks, W, dM, dF, status, b_a, dz);        \
     } while (0)
     if (d_bf16) {
         if (dz) ADJ_TRUNC(__nv_bfloat16, true);
