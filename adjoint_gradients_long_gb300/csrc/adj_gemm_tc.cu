@@ -501,6 +501,10 @@ __device__ __forceinline__ int epi_at(int r, int q) { return r * 32 + ((q ^ (r &
 
 __device__ __forceinline__ float sigmoidf_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
+// EXT: the epilogue features only some launches use (the cotangent through a normalised
+// input, a lane-written bf16 copy of the output in the TMA path) are compiled in; the other
+// instantiations leave them out, which keeps their register use (and spills) down.
+template <bool EXT>
 __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, int64_t m0r, int n0c, int z, int lane) {
     const GemmEpilogue &ep = args.ep;
     const int64_t M = args.M;
@@ -532,7 +536,7 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
         for (int i = lane >> 3; i < rows; i += 4) {
             float4 v = *reinterpret_cast<const float4 *>(sb + epi_at(i, lane & 7));
             const int64_t o = int64_t(i) * ep.ld;
-            if (add && ep.nr) {
+            if (EXT && add && ep.nr) {
                 // through the normalised input: (acc - xhat mean(xhat . dxhat)) / r, then the add
                 const int64_t row = m0r + i;
                 float sdz = 0.f;
@@ -584,7 +588,7 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
 // is multicast to both CTAs' stage and accumulator barriers; both epilogues release the
 // accumulator on the leader's barrier.  Per SM this halves the B operand traffic through
 // shared memory for the same MMA work.  Only all-bf16, all-TMA operands take this mode.
-template <bool ABF, bool BBF, bool SPLIT, bool REGS, bool PAIR = false>
+template <bool ABF, bool BBF, bool SPLIT, bool REGS, bool PAIR = false, bool EXT = false>
 __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_constant__ TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -959,7 +963,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 }
                 // through a normalised input: this lane's row scalars and xhat values (bf16: all 32
                 // columns packed; fp32: read per quad below), issued before the TMEM load
-                const bool norm = add_tma && ep.nr != nullptr;
+                const bool norm = EXT && add_tma && ep.nr != nullptr;
                 const int64_t nrow = m0r + lane;
                 float n_mt = 0.f, n_ir = 0.f;
                 uint4 n_xb[4];
@@ -1028,7 +1032,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             v[j + 3] += r4.w;
                         }
                     }
-                    if (ep.out_x && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd) && m0r + lane < args.M) {
+                    if (EXT && ep.out_x && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd) && m0r + lane < args.M) {
                         // the bf16 copy of this lane's row: four 16-byte stores
                         __nv_bfloat16 *xr = static_cast<__nv_bfloat16 *>(ep.out_x) + (m0r + lane) * ep.ld + n;
 #pragma unroll
@@ -1062,7 +1066,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4 *>(sb + epi_at(lane, j >> 2)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
                     __syncwarp();
-                    if (m0r < args.M) epi_chunk(args, sb, m0r, n, z, lane);
+                    if (m0r < args.M) epi_chunk<EXT>(args, sb, m0r, n, z, lane);
                     __syncwarp();
                 }
             }
@@ -1203,9 +1207,9 @@ static int tma_build(CUtensorMap *maps, CUtensorMap *lo_maps, CUtensorMap *mul_m
     return mode;
 }
 
-template <bool ABF, bool BBF, bool SPLIT, bool REGS = true>
+template <bool ABF, bool BBF, bool SPLIT, bool REGS = true, bool EXT = true>
 static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st) {
-    auto kern = k_gemm_tc<ABF, BBF, SPLIT, REGS>;
+    auto kern = k_gemm_tc<ABF, BBF, SPLIT, REGS, false, EXT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, TC_THREADS_P, smem, st>>>(a);
@@ -1214,7 +1218,9 @@ static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cuda
 
 // The CTA-pair instantiation (bf16 operands, all by TMA): launched as clusters of two.
 using PairKernel = void (*)(TcArgs);
-static PairKernel pair_kernel() { return k_gemm_tc<false, false, false, false, true>; }
+static PairKernel pair_kernel(bool ext = false) {
+    return ext ? k_gemm_tc<false, false, false, false, true, true> : k_gemm_tc<false, false, false, false, true, false>;
+}
 static cudaLaunchConfig_t pair_config(unsigned grid, size_t smem, cudaStream_t st, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -1248,12 +1254,12 @@ static int pair_slots(size_t smem) {
     next = (next + 1) % 4;
     return n;
 }
-static cudaError_t launch_pair(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(pair_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+static cudaError_t launch_pair(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st, bool ext) {
+    cudaError_t e = cudaFuncSetAttribute(pair_kernel(ext), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config(grid, smem, st, attr);
-    return cudaLaunchKernelEx(&cfg, pair_kernel(), a);
+    return cudaLaunchKernelEx(&cfg, pair_kernel(ext), a);
 }
 
 // Whether GEMMs whose operands are both bf16 and both loaded by TMA run as CTA pairs.
@@ -1366,11 +1372,12 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     const TcLayout L = tc_layout(pair ? BN / 2 : BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
     const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + size_t(a.epiw) * TC_CHUNK_BYTES + bar_bytes;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
+    const bool ext = ep.nr != nullptr || ep.out_x != nullptr;   // the EXT epilogue features
     if (pair) {
         a.ep.csum = nullptr;
         if (csum_done) *csum_done = false;
         const int64_t npairs = ntiles < slots ? ntiles : slots;
-        return launch_pair(a, unsigned(2 * npairs), smem, st);
+        return launch_pair(a, unsigned(2 * npairs), smem, st, ext);
     }
     int64_t grid = ntiles;
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;
@@ -1383,8 +1390,12 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (csum_done) *csum_done = csum;
     const bool need_regs = a.a_ld == LD_REG || (!a.b_res && a.b_ld == LD_REG) || (a.b_res && !ld_tma(a.b_ld));
     if (!need_regs) {
-        if (split3) return launch_tc_t<false, false, true, false>(a, unsigned(grid), smem, st);
-        return launch_tc_t<false, false, false, false>(a, unsigned(grid), smem, st);
+        if (split3) {
+            if (ext) return launch_tc_t<false, false, true, false, true>(a, unsigned(grid), smem, st);
+            return launch_tc_t<false, false, true, false, false>(a, unsigned(grid), smem, st);
+        }
+        if (ext) return launch_tc_t<false, false, false, false, true>(a, unsigned(grid), smem, st);
+        return launch_tc_t<false, false, false, false, false>(a, unsigned(grid), smem, st);
     }
     if (split3) {
         if (A.bf16 && Bm.bf16) return launch_tc_t<true, true, true>(a, unsigned(grid), smem, st);
