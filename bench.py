@@ -206,16 +206,16 @@ def kernel_table(P, N, xb, db, trunc, K=1):
 PROFILE_OF = {
     ("ssm1_p128", "bwd_scan"): "k_bwd_scan_ssm1_p128.md",
     ("ssm1_p128", "fwd_scan"): "k_fwd_scan_ssm1_p128.md",
-    ("ssm1_p128", "proj_in"): "k_gemm_tc_proj_in_ssm1_p128.md",
-    ("ssm1_p128", "proj_out"): "k_gemm_tc_proj_out_ssm1_p128.md",
-    ("ssm1_p128", "cot_proj"): "k_gemm_tc_cot_proj_ssm1_p128.md",
-    ("ssm1_p128", "param_dW_in"): "k_gemm_tc_param_dWin_ssm1_p128.md",
-    ("ssm4_p2048", "proj_in"): "k_gemm_tc_proj_in_ssm4_p2048.md",
-    ("ssm4_p2048", "param_dW_in"): "k_gemm_tc_param_dWin_ssm4_p2048.md",
-    ("ssm4_p2048", "proj_out"): "k_gemm_tc_proj_out_ssm4_p2048.md",
     ("ssm4_p2048", "input_grad"): "k_gemm_tc_input_grad_ssm4_p2048.md",
-    ("ssm4_p2048", "bwd_scan"): "k_bwd_scan_ssm4_p2048.md",
-    ("ssm4_p2048", "rms_norm_bwd"): "k_rms_norm_bwd_ssm4_p2048.md",
+    ("ssm4_p2048", "proj_out"): "k_gemm_tc_proj_out_ssm4_p2048.md",
+    ("ssm4_p2048", "param_dW_in"): "k_gemm_tc_param_dWin_ssm4_p2048.md",
+    ("ssm4_p2048", "proj_in"): "k_gemm_tc_proj_in_ssm4_p2048.md",
+    ("ssm4_p2048", "cot_proj"): "k_gemm_tc_cot_proj_ssm4_p2048.md",
+    ("ssm4_p2048", "param_dW_o"): "k_gemm_tc_param_dWo_ssm4_p2048.md",
+    ("ssm4_p2048", "bwd_scan"): "k_trunc_scan_ssm4_p2048.md",
+    ("ssm4_p2048", "rms_norm"): "k_rms_norm_ssm4_p2048.md",
+    ("ssm4_p2048", "fwd_scan"): "k_fwd_scan_ssm4_p2048.md",
+    ("ssm4_p2048", "loss"): "k_loss_ssm4_p2048.md",
 }
 
 
