@@ -716,6 +716,33 @@ __device__ __forceinline__ FwdSeg wait_fdesc(const float4 *p0, const float4 *p1,
     return FwdSeg{f4(1.f), f4(0.f), false};
 }
 
+// The same for n <= NB consecutive chunks' slots (p0, p1 of the first; a chunk's slots are 32
+// float4 apart): all loads of a poll in flight at once, so a batch costs one L2 round trip.
+template <int NB>
+__device__ __forceinline__ void wait_fdesc_n(const float4 *p0, const float4 *p1, int n, FwdSeg (&out)[NB],
+                                             unsigned *status) {
+    for (int it = 0; it < SPIN_LIMIT; ++it) {
+        DescRead d[NB];
+        bool ok = true;
+#pragma unroll
+        for (int u = 0; u < NB; ++u)
+            if (u < n) {
+                d[u] = desc_read(p0 + u * 32, p1 + u * 32);
+                ok = ok && d[u].ok;
+            }
+        if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+            for (int u = 0; u < NB; ++u) out[u] = u < n ? FwdSeg{d[u].a, d[u].b, false} : FwdSeg{f4(1.f), f4(0.f), false};
+            return;
+        }
+        if (it > 8) __nanosleep(64);
+        if ((it & 255) == 255 && *reinterpret_cast<volatile unsigned *>(status) != 0u) break;
+    }
+    record_timeout(status);
+#pragma unroll
+    for (int u = 0; u < NB; ++u) out[u] = FwdSeg{f4(1.f), f4(0.f), false};
+}
+
 template <int L, typename TD, bool DZ>
 __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
                                                       float *__restrict__ Rl, TD *__restrict__ Da, TD *__restrict__ Du,
@@ -797,11 +824,16 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
         if (first_of_block) {
             const int64_t cb = (c0 + W <= T ? W : T - c0 + TT - 1) / TT;   // chunks in this block
             const int64_t q = (cb + SC_WARPS - 1) / SC_WARPS, j0 = w * q, j1 = j0 + q < cb ? j0 + q : cb;
+            // FOLD_NB aggregates a poll: the fold and the publication each take about q / FOLD_NB
+            // L2 round trips (the block before waits on them)
+            constexpr int FOLD_NB = 4;
             FwdSeg part{f4(1.f), f4(0.f), false};
-            for (int64_t j = j0; j < j1; ++j) {
+            for (int64_t j = j0; j < j1; j += FOLD_NB) {
                 const int64_t cj = fb + chunk + j;
-                FwdSeg a_j = wait_fdesc(&dF.agg0[cj * 32 + lane], &dF.agg1[cj * 32 + lane], status);
-                part = fseg_then(part, a_j);
+                FwdSeg a_j[FOLD_NB];
+                wait_fdesc_n<FOLD_NB>(&dF.agg0[cj * 32 + lane], &dF.agg1[cj * 32 + lane], int(j1 - j), a_j, status);
+#pragma unroll
+                for (int u = 0; u < FOLD_NB; ++u) part = fseg_then(part, a_j[u]);   // identity past j1
             }
             sX[w][lane] = part.P;
             sY[w][lane] = part.S;
@@ -809,11 +841,18 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
             FwdSeg run{f4(1.f), f4(0.f), true};   // the block start
             for (int j = 0; j < w; ++j) run = fseg_then(run, FwdSeg{sX[j][lane], sY[j][lane], false});
             __threadfence();   // every aggregate observed before any prefix is published
-            for (int64_t j = j0; j < j1; ++j) {
+            for (int64_t j = j0; j < j1; j += FOLD_NB) {
                 const int64_t cj = fb + chunk + j;
-                const DescRead d = desc_read(&dF.agg0[cj * 32 + lane], &dF.agg1[cj * 32 + lane]);
-                run = fseg_then(run, FwdSeg{d.a, d.b, false});
-                desc_publish(&dF.inc0[cj * 32 + lane], run.P, &dF.inc1[cj * 32 + lane], run.S);
+                DescRead d[FOLD_NB];
+#pragma unroll
+                for (int u = 0; u < FOLD_NB; ++u)
+                    if (j + u < j1) d[u] = desc_read(&dF.agg0[(cj + u) * 32 + lane], &dF.agg1[(cj + u) * 32 + lane]);
+#pragma unroll
+                for (int u = 0; u < FOLD_NB; ++u)
+                    if (j + u < j1) {
+                        run = fseg_then(run, FwdSeg{d[u].a, d[u].b, false});
+                        desc_publish(&dF.inc0[(cj + u) * 32 + lane], run.P, &dF.inc1[(cj + u) * 32 + lane], run.S);
+                    }
             }
             __syncthreads();   // sX/sY free again
         }
