@@ -16,6 +16,13 @@ Section 3.1 model form; the initialisation is the one the workload list fixes):
              Tbar=4096 and full
   ssm4_p2048 4 layers, P=2048, N=256, T=131072, B=1, bf16 GEMM operands, Tbar=8192
 
+General selective layer (one layer; per channel p the step dt = softplus(z_p), the
+decay exp(dt A_pn), input-dependent B_t, C_t):
+
+  sel1_p16   P=16,   N=8,  T=256,   B=1, fp32,                 full and Tbar=64
+  sel1_p64   P=64,   N=16, T=2048,  B=2, fp32,                 full and Tbar=256
+  sel1_p1024 P=1024, N=16, T=65536, B=1, bf16 GEMM operands,   Tbar=8192 and full
+
 Every tensor is drawn in token chunks of CHUNK tokens from its own counter-keyed
 PCG64 stream (seed, tensor id, batch row, chunk index), so any token range of a
 workload can be regenerated on its own and equals the same slice of the whole.
@@ -32,6 +39,7 @@ CHUNK = 4096
 # tensor stream ids
 _S_XHAT, _S_TARGET = 1, 2
 _S_WA, _S_WB, _S_WC, _S_WO = 11, 12, 13, 14
+_S_WDT, _S_BDT, _S_A = 21, 22, 23
 
 
 @dataclasses.dataclass(frozen=True)
@@ -140,3 +148,51 @@ def make_inputs(w, T: Optional[int] = None, B: Optional[int] = None, P: Optional
         xhat = round_bf16(xhat)
     layers = [make_layer_weights(w, k, P, N, seed) for k in range(K)]
     return dict(xhat=xhat, target=target, layers=layers, workload=w, T=T, B=B, P=P, N=N, K=K)
+
+
+@dataclasses.dataclass(frozen=True)
+class SelWorkload:
+    """A workload of the general selective layer (one layer)."""
+    key: str
+    P: int              # channels
+    N: int              # states per channel
+    T: int              # tokens per sequence
+    B: int              # sequences
+    x_dtype: str        # "f32" or "bf16": GEMM operand storage (xhat, W_in, dz)
+    windows: tuple      # truncation windows; None = full adjoint
+    seed: int
+
+
+SEL_WORKLOADS = {
+    "sel1_p16": SelWorkload("sel1_p16", 16, 8, 256, 1, "f32", (None, 64), 2001),
+    "sel1_p64": SelWorkload("sel1_p64", 64, 16, 2048, 2, "f32", (None, 256), 2002),
+    "sel1_p1024": SelWorkload("sel1_p1024", 1024, 16, 65536, 1, "bf16", (8192, None), 2003),
+}
+
+
+def make_sel_inputs(w, T: Optional[int] = None, B: Optional[int] = None, P: Optional[int] = None,
+                    N: Optional[int] = None, t0: int = 0, seed: Optional[int] = None) -> dict:
+    """Inputs of a selective-layer workload, optionally resized or restricted to tokens
+    [t0, t0+T).  float32 arrays: xhat, target [B,T,P] ~ N(0,1); W_in [P, P+2N] = [W_dt ~
+    N(0, 0.25/P) | W_B ~ N(0, 1/P) | W_C ~ N(0, 1/P)]; b_dt [P] ~ U[-7, -2.3] (so the step
+    softplus(b_dt) spans about 1e-3 .. 1e-1); A [P,N] = -(n+1) U[0.8, 1.2].  bf16 workloads
+    hold bf16-representable xhat and W_in."""
+    if not isinstance(w, SelWorkload):
+        w = SEL_WORKLOADS[w]
+    T = w.T if T is None else T
+    B = w.B if B is None else B
+    P = w.P if P is None else P
+    N = w.N if N is None else N
+    seed = w.seed if seed is None else seed
+    xhat = _tokens(seed, _S_XHAT, B, t0, t0 + T, P)
+    target = _tokens(seed, _S_TARGET, B, t0, t0 + T, P)
+    W_dt = _rng(seed, _S_WDT).standard_normal((P, P), dtype=np.float32) * np.float32(0.5 / np.sqrt(P))
+    W_B = _rng(seed, _S_WB).standard_normal((P, N), dtype=np.float32) * np.float32(1.0 / np.sqrt(P))
+    W_C = _rng(seed, _S_WC).standard_normal((P, N), dtype=np.float32) * np.float32(1.0 / np.sqrt(P))
+    W_in = np.ascontiguousarray(np.concatenate([W_dt, W_B, W_C], axis=1))
+    b_dt = _rng(seed, _S_BDT).uniform(-7.0, -2.3, size=P).astype(np.float32)
+    A = (-(np.arange(N, dtype=np.float32) + 1.0)[None, :]
+         * _rng(seed, _S_A).uniform(0.8, 1.2, size=(P, N)).astype(np.float32)).astype(np.float32)
+    if w.x_dtype == "bf16":
+        xhat, W_in = round_bf16(xhat), round_bf16(W_in)
+    return dict(xhat=xhat, target=target, W_in=W_in, b_dt=b_dt, A=A, workload=w, T=T, B=B, P=P, N=N)

@@ -66,3 +66,58 @@ def test_mutation_is_caught(name, case, tmp_path):
     finally:
         oracle.use_library(None)
     assert worst > 1e-6, (name, worst)
+
+
+# ---------------------------------------------------------------- the general selective layer
+SEL_SRC = os.path.join(os.path.dirname(oracle.__file__), "sel_oracle.c")
+
+SEL_MUTATIONS = {
+    "dropped_input_term": ("ddt[p] += vv * (A[p * N + n] * ab * hp + zr[P + n] * xr[p]);",
+                           "ddt[p] += vv * (A[p * N + n] * ab * hp);"),
+    "decay_of_the_wrong_token": ("const double dti = softplus(z[ri * Z + p]);",
+                                 "const double dti = softplus(z[(ri > 0 ? ri - 1 : 0) * Z + p]);"),
+    "literal_product_short": ("for (int64_t j = i + 1; j <= t; ++j) {", "for (int64_t j = i + 1; j < t; ++j) {"),
+    "no_softplus_slope": ("dz[r * Z + p] = ddt[r * P + p] * sigmoid(z[r * Z + p]);", "dz[r * Z + p] = ddt[r * P + p];"),
+    "B_and_C_swapped": ("v[p * N + n] = gy[rt * P + p] * z[rt * Z + P + N + n] * prod;",
+                        "v[p * N + n] = gy[rt * P + p] * z[rt * Z + P + n] * prod;"),
+    "B_and_C_swapped_agg": ("vv[n] = gy[rt * P + p] * z[rt * Z + P + N + n];", "vv[n] = gy[rt * P + p] * z[rt * Z + P + n];"),
+    "dA_without_step": ("dA[p * N + n] += vv * dt * ab * hp;", "dA[p * N + n] += vv * ab * hp;"),
+    "window_off_by_one": ("int64_t lo = t - W + 1;", "int64_t lo = t - W;"),
+    "h_i_for_h_im1": ("i > 0 ? h + (ri - 1) * PN : NULL", "h + ri * PN"),
+    "bias_on_the_wrong_columns": ("zr[j] = acc + (j < P ? b_dt[j] : 0.0);", "zr[j] = acc + (j < N ? b_dt[j] : 0.0);"),
+}
+
+
+@pytest.fixture(scope="module")
+def sel_case():
+    from oracle import sel_bptt
+    d = synth.make_sel_inputs("sel1_p16", T=18, B=2, P=4, N=3)
+    W = {k: d[k].astype(np.float64) for k in ("W_in", "b_dt", "A")}
+    W["b_dt"] = W["b_dt"] + 4.0
+    x, tgt = d["xhat"].astype(np.float64), d["target"].astype(np.float64)
+    return W, x, tgt, sel_bptt.bptt_grad(W, x, tgt), sel_bptt.bptt_grad(W, x, tgt, 5)
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(SEL_MUTATIONS))
+def test_selective_mutation_is_caught(name, sel_case, tmp_path):
+    from oracle import selective as sel
+    old, new = SEL_MUTATIONS[name]
+    src = open(SEL_SRC).read()
+    assert src.count(old) >= 1, name
+    path_c = tmp_path / "mut.c"
+    path_c.write_text(src.replace(old, new))
+    so = sel.build(force=True, src=str(path_c), out=str(tmp_path / "libmut.so"))
+    W, x, tgt, ref_full, ref5 = sel_case
+    sel.use_library(so)
+    try:
+        worst = 0.0
+        for mode in (sel.LITERAL, sel.AGGREGATED):
+            for Tbar, ref in ((None, ref_full), (5, ref5)):
+                st = sel.forward(W, x)
+                g = sel.grad(W, st, st["y"] - tgt, Tbar, mode)
+                for k in ("W_in", "b_dt", "A"):
+                    worst = max(worst, rel_fro(g["d" + k], ref["d" + k]))
+    finally:
+        sel.use_library(None)
+    assert worst > 1e-6, (name, worst)
