@@ -7,6 +7,7 @@
 
 #include "adj_internal.cuh"
 #include "adj_profile.cuh"
+#include "adj_sel.cuh"
 
 using namespace adj;
 
@@ -19,6 +20,12 @@ inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 // largest grid the scans launch (tickets are 32-bit)
 constexpr int64_t MAX_CHUNKS = int64_t(1) << 31;
 
+#define ADJ_TRY_(x)                                 \
+    do {                                            \
+        adj_status s_ = (x);                        \
+        if (s_ != ADJ_OK) return s_;                \
+    } while (0)
+
 adj_status check_dims(const adj_dims *d) {
     if (!d) return ADJ_EINVAL;
     if (d->B < 0 || d->T < 0 || d->P <= 0 || d->N <= 0) return ADJ_ESHAPE;
@@ -26,6 +33,14 @@ adj_status check_dims(const adj_dims *d) {
     if ((d->x_dtype != ADJ_F32 && d->x_dtype != ADJ_BF16) || (d->d_dtype != ADJ_F32 && d->d_dtype != ADJ_BF16))
         return ADJ_EDTYPE;
     if (d->B * cdiv(d->N, 128) * cdiv(d->T, 32) >= MAX_CHUNKS) return ADJ_ESHAPE;
+    return ADJ_OK;
+}
+
+// the general selective layer: N = 8 or 16 states a channel, one grid row per sequence
+adj_status check_sel_dims(const adj_dims *d) {
+    ADJ_TRY_(check_dims(d));
+    if (d->N != 8 && d->N != 16) return ADJ_ESHAPE;
+    if (d->B > 65535) return ADJ_ESHAPE;
     return ADJ_OK;
 }
 
@@ -111,6 +126,29 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
     case ADJ_OP_LOSS:
         L.part0 = off; off += al256(size_t(loss_blocks(d->B * d->T * d->P)) * 8);
         break;
+    case ADJ_OP_SEL_FWD: {      // chunk aggregates (2); fp32 weights: W_in's bf16 hi/lo split
+        const size_t agg = al256(size_t(d->B * cdiv(d->T, sel_chunk(d->T, 0))) * d->P * d->N * 4);
+        L.buf0 = off; off += agg;
+        L.buf1 = off; off += agg;
+        L.wsplit = off; off += wsplit ? al256(size_t(d->P) * (d->P + 2 * d->N) * 4) : 0;
+        break;
+    }
+    case ADJ_OP_SEL_BWD: {      // aggregates (2, 4 truncated), R (truncated), dB/dC and dA partials
+        const bool tr = Tbar > 0 && Tbar < d->T;
+        const int64_t nch = cdiv(d->T, sel_chunk(d->T, tr ? Tbar : 0));
+        const size_t agg = al256(size_t(d->B * nch) * d->P * d->N * 4);
+        L.buf0 = off; off += (tr ? 4 : 2) * agg;
+        L.buf1 = off; off += tr ? al256(size_t(d->B * d->T) * d->P * d->N * 4) : 0;
+        L.part0 = off; off += al256(size_t(d->B * d->T) * sel_slices(d->P, d->N) * 2 * d->N * 4);
+        L.part1 = off; off += agg;
+        break;
+    }
+    case ADJ_OP_SEL_PARAM: {    // dW_in split partials, db_dt block partials
+        const int64_t zw = d->P + 2 * int64_t(d->N);
+        L.part0 = off; off += al256(size_t(gemm_splits(d->P, zw, d->B * d->T)) * d->P * zw * 4);
+        L.part1 = off; off += al256(size_t(colsum_blocks(d)) * d->P * 4);
+        break;
+    }
     default:
         return Layout{};
     }
@@ -232,6 +270,9 @@ extern "C" {
 size_t adj_workspace_bytes(const adj_dims *dims, int op, int64_t Tbar) {
     if (check_dims(dims) != ADJ_OK) return 0;
     if (op == ADJ_OP_BWD_TRUNC && Tbar < 1) return 0;
+    if ((op == ADJ_OP_SEL_FWD || op == ADJ_OP_SEL_BWD || op == ADJ_OP_SEL_PARAM) && check_sel_dims(dims) != ADJ_OK)
+        return 0;
+    if (op == ADJ_OP_SEL_BWD && !sel_window_ok(dims->T, Tbar)) return 0;
     return layout(dims, op, Tbar).total;
 }
 
@@ -455,6 +496,109 @@ adj_status adj_rms_norm_bwd(const adj_dims *dims, const float *y, const float *r
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ProfScope ps(K_RMS_NORM_BWD, st);
     ADJ_CUDA(launch_rms_norm_bwd(y, r, dxhat, gy, gy_prev, rows, dims->P, st));
+    return ADJ_OK;
+}
+
+// ---------------------------------------------------------------- the general selective layer
+adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, float *z, float *h, float *y,
+                       void *ws, size_t ws_bytes, void *stream) {
+    ADJ_TRY(check_sel_dims(dims));
+    if (!w) return ADJ_EINVAL;
+    ADJ_TRY(check_ptrs({w->W_in, w->b_dt, w->A, xhat, z, h, y}));
+    Layout L;
+    ADJ_TRY(check_ws(dims, ADJ_OP_SEL_FWD, 0, ws, ws_bytes, &L));
+    const int64_t B = dims->B, T = dims->T, BT = B * T;
+    const int P = dims->P, N = dims->N;
+    if (BT == 0) return ADJ_OK;
+    const bool xbf = dims->x_dtype == ADJ_BF16;
+    const int64_t zw = P + 2 * int64_t(N);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // z = xhat W_in
+    {
+        cudaError_t err = cudaSuccess;
+        const GemmOperand Win = opw(w->W_in, int64_t(P) * zw, xbf, at(ws, L.wsplit), 1, zw, st, &err);
+        ADJ_CUDA(err);
+        GemmEpilogue e = epi(Epi::Store);
+        e.out0 = z;
+        e.ld = zw;
+        ProfScope ps(K_SEL_PROJ, st);
+        ADJ_CUDA(launch_gemm_tc(BT, zw, P, op1(xhat, P, 1, xbf), Win, e, 1, !xbf, status_word(ws), st));
+    }
+    ProfScope ps(K_SEL_FWD, st, 3);
+    ADJ_CUDA(launch_sel_fwd(z, xhat, xbf, w->b_dt, w->A, h, y, reinterpret_cast<float *>(at(ws, L.buf0)),
+                            reinterpret_cast<float *>(at(ws, L.buf1)), B, T, P, N, st));
+    return ADJ_OK;
+}
+
+adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const float *z,
+                       const float *h, const float *gy, int64_t Tbar, void *dz, float *dA, void *ws, size_t ws_bytes,
+                       void *stream) {
+    ADJ_TRY(check_sel_dims(dims));
+    if (!w) return ADJ_EINVAL;
+    ADJ_TRY(check_ptrs({w->b_dt, w->A, xhat, z, h, gy, dz, dA}));
+    if (!sel_window_ok(dims->T, Tbar)) return ADJ_EINVAL;
+    Layout L;
+    ADJ_TRY(check_ws(dims, ADJ_OP_SEL_BWD, Tbar, ws, ws_bytes, &L));
+    const int64_t B = dims->B, T = dims->T, BT = B * T;
+    const int P = dims->P, N = dims->N;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (BT == 0) {
+        ADJ_CUDA(cudaMemsetAsync(dA, 0, size_t(P) * N * 4, st));
+        return ADJ_OK;
+    }
+    const bool tr = Tbar > 0 && Tbar < T;
+    const size_t agg = al256(size_t(B * cdiv(T, sel_chunk(T, tr ? Tbar : 0))) * P * N * 4);
+    SelBwdWs sw;
+    sw.aggX = reinterpret_cast<float *>(at(ws, L.buf0));
+    sw.aggY = reinterpret_cast<float *>(at(ws, L.buf0 + agg));
+    sw.winX = tr ? reinterpret_cast<float *>(at(ws, L.buf0 + 2 * agg)) : nullptr;
+    sw.winY = tr ? reinterpret_cast<float *>(at(ws, L.buf0 + 3 * agg)) : nullptr;
+    sw.R = tr ? reinterpret_cast<float *>(at(ws, L.buf1)) : nullptr;
+    sw.bc = reinterpret_cast<float *>(at(ws, L.part0));
+    sw.dAp = reinterpret_cast<float *>(at(ws, L.part1));
+    ProfScope ps(K_SEL_BWD, st, tr ? 8 : 5);
+    ADJ_CUDA(launch_sel_bwd(z, xhat, dims->x_dtype == ADJ_BF16, gy, h, w->b_dt, w->A, dz, dims->d_dtype == ADJ_BF16, dA,
+                            sw, B, T, P, N, tr ? Tbar : 0, st));
+    return ADJ_OK;
+}
+
+adj_status adj_sel_param_grad(const adj_dims *dims, const void *xhat, const void *dz, float *dW_in, float *db_dt,
+                              int accumulate, void *ws, size_t ws_bytes, void *stream) {
+    ADJ_TRY(check_sel_dims(dims));
+    ADJ_TRY(check_ptrs({xhat, dz, dW_in, db_dt}));
+    Layout L;
+    ADJ_TRY(check_ws(dims, ADJ_OP_SEL_PARAM, 0, ws, ws_bytes, &L));
+    const int64_t BT = dims->B * dims->T;
+    const int P = dims->P, N = dims->N;
+    const int64_t zw = P + 2 * int64_t(N);
+    const bool xbf = dims->x_dtype == ADJ_BF16, dbf = dims->d_dtype == ADJ_BF16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (BT == 0) {
+        if (!accumulate) {
+            ADJ_CUDA(cudaMemsetAsync(dW_in, 0, size_t(P) * zw * 4, st));
+            ADJ_CUDA(cudaMemsetAsync(db_dt, 0, size_t(P) * 4, st));
+        }
+        return ADJ_OK;
+    }
+    const int s = gemm_splits(P, zw, BT);
+    int su = s;
+    float *part = reinterpret_cast<float *>(at(ws, L.part0));
+    float *part_b = reinterpret_cast<float *>(at(ws, L.part1));
+    GemmEpilogue e = epi(Epi::Partial);
+    e.out0 = part;
+    {
+        ProfScope ps(K_SEL_DW, st);
+        ADJ_CUDA(launch_gemm_tc(P, zw, BT, op1(xhat, 1, P, xbf), op1(dz, 1, zw, dbf), e, s, !xbf, status_word(ws), st,
+                                &su));
+    }
+    const int nb = colsum_blocks(dims);
+    {
+        ProfScope ps(K_COLSUM, st);
+        ADJ_CUDA(launch_sel_colsum(dz, dbf, BT, P, int(zw), nb, part_b, st));
+    }
+    const RedSeg segs[2] = {{part, dW_in, int64_t(P) * zw / 4, su, 0, 0}, {part_b, db_dt, P / 4, nb, 0, 0}};
+    ProfScope ps(K_PARAM_REDUCE, st);
+    ADJ_CUDA(launch_reduce_partials(segs, 2, accumulate, st));
     return ADJ_OK;
 }
 

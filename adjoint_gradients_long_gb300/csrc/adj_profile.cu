@@ -23,7 +23,8 @@ std::vector<cudaEvent_t> g_pool;
 
 const char *g_names[K_COUNT] = {"proj_in", "fwd_scan", "proj_out", "loss", "cot_proj", "win_scan",
                                 "bwd_scan", "param_dW_in", "param_dW_o", "param_reduce", "colsum",
-                                "input_grad", "rms_norm", "rms_norm_bwd", "weight_prep"};
+                                "input_grad", "rms_norm", "rms_norm_bwd", "weight_prep",
+                                "sel_proj", "sel_fwd", "sel_bwd", "sel_dW"};
 
 cudaEvent_t take() {
     if (!g_pool.empty()) {

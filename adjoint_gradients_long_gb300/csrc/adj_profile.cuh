@@ -20,6 +20,10 @@ enum KernelId {
     K_RMS_NORM,
     K_RMS_NORM_BWD,
     K_WEIGHT_PREP,
+    K_SEL_PROJ,
+    K_SEL_FWD,
+    K_SEL_BWD,
+    K_SEL_DW,
     K_COUNT
 };
 

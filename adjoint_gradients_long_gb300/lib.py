@@ -14,12 +14,14 @@ LIB_PATH = os.path.join(_HERE, "_build", "libadj.so")
 
 F32, BF16 = 0, 1
 OP_FWD, OP_BWD_FULL, OP_BWD_TRUNC, OP_PARAM, OP_LOSS = 0, 1, 2, 3, 4
+OP_SEL_FWD, OP_SEL_BWD, OP_SEL_PARAM = 5, 6, 7
 STATUS = {0: "ADJ_OK", 1: "ADJ_EINVAL", 2: "ADJ_ESHAPE", 3: "ADJ_EALIGN", 4: "ADJ_EDTYPE",
           5: "ADJ_EWORKSPACE", 6: "ADJ_ECUDA", 7: "ADJ_ETIMEOUT"}
 EXPORTS = ("adj_workspace_bytes", "adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc",
            "adj_param_grad", "adj_stream_status", "adj_status_str", "adj_launch_count", "adj_profile_enable",
            "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read", "adj_rms_norm",
-           "adj_rms_norm_bwd", "adj_selftest_waits", "adj_selftest_ws_bytes")
+           "adj_rms_norm_bwd", "adj_selftest_waits", "adj_selftest_ws_bytes", "adj_sel_fwd", "adj_sel_bwd",
+           "adj_sel_param_grad")
 
 
 class AdjError(RuntimeError):
@@ -37,9 +39,14 @@ class Weights(ctypes.Structure):
     _fields_ = [("W_in", ctypes.c_void_p), ("b_a", ctypes.c_void_p), ("W_o", ctypes.c_void_p)]
 
 
+class SelWeights(ctypes.Structure):
+    """adj_sel_weights: W_in [P, P+2N], b_dt [P], A [P,N]."""
+    _fields_ = [("W_in", ctypes.c_void_p), ("b_dt", ctypes.c_void_p), ("A", ctypes.c_void_p)]
+
+
 _lib = None
 _VP, _SZ, _I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
-_PD, _PW = ctypes.POINTER(Dims), ctypes.POINTER(Weights)
+_PD, _PW, _PS = ctypes.POINTER(Dims), ctypes.POINTER(Weights), ctypes.POINTER(SelWeights)
 
 
 def load(path: str = LIB_PATH):
@@ -57,6 +64,9 @@ def load(path: str = LIB_PATH):
         lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 10 + [_I64, _VP, _SZ, _VP]
         lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 15 + [ctypes.c_int, _VP, _SZ, _VP]
         lib.adj_rms_norm.argtypes = [_PD] + [_VP] * 4
+        lib.adj_sel_fwd.argtypes = [_PD, _PS] + [_VP] * 5 + [_SZ, _VP]
+        lib.adj_sel_bwd.argtypes = [_PD, _PS] + [_VP] * 4 + [_I64] + [_VP] * 3 + [_SZ, _VP]
+        lib.adj_sel_param_grad.argtypes = [_PD] + [_VP] * 4 + [ctypes.c_int, _VP, _SZ, _VP]
         lib.adj_selftest_waits.argtypes = [_VP, _SZ, ctypes.c_int, _VP]
         lib.adj_selftest_waits.restype = ctypes.c_int
         lib.adj_selftest_ws_bytes.argtypes = []
@@ -72,7 +82,8 @@ def load(path: str = LIB_PATH):
         lib.adj_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
         lib.adj_profile_read.restype = ctypes.c_int
         for f in ("adj_fwd_scan", "adj_loss_mse", "adj_bwd_full", "adj_bwd_trunc", "adj_param_grad",
-                  "adj_stream_status", "adj_rms_norm", "adj_rms_norm_bwd"):
+                  "adj_stream_status", "adj_rms_norm", "adj_rms_norm_bwd", "adj_sel_fwd", "adj_sel_bwd",
+                  "adj_sel_param_grad"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -188,3 +199,24 @@ def selftest_ws_bytes() -> int:
 
 def selftest_waits(ws, ws_bytes, which, stream=None):
     _check(load().adj_selftest_waits(ptr(ws), ws_bytes, int(which), _stream(stream)), "adj_selftest_waits")
+
+
+# ---------------------------------------------------------------- the general selective layer
+def sel_weights(W_in, b_dt, A) -> SelWeights:
+    return SelWeights(ptr(W_in), ptr(b_dt), ptr(A))
+
+
+def sel_fwd(d, w, xhat, z, h, y, ws, ws_bytes, stream=None):
+    _check(load().adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(z), ptr(h), ptr(y), ptr(ws), ws_bytes,
+                              _stream(stream)), "adj_sel_fwd")
+
+
+def sel_bwd(d, w, xhat, z, h, gy, Tbar, dz, dA, ws, ws_bytes, stream=None):
+    _check(load().adj_sel_bwd(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(z), ptr(h), ptr(gy),
+                              0 if Tbar is None else int(Tbar), ptr(dz), ptr(dA), ptr(ws), ws_bytes, _stream(stream)),
+           "adj_sel_bwd")
+
+
+def sel_param_grad(d, xhat, dz, dW_in, db_dt, accumulate, ws, ws_bytes, stream=None):
+    _check(load().adj_sel_param_grad(ctypes.byref(d), ptr(xhat), ptr(dz), ptr(dW_in), ptr(db_dt), int(accumulate),
+                                     ptr(ws), ws_bytes, _stream(stream)), "adj_sel_param_grad")

@@ -35,6 +35,8 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = ("ssm4_p2048", 8192)
 CONTEXT = (("ssm1_1m", 4096), ("ssm1_1m", None), ("ssm8_p512", 4096), ("ssm1_p128", None), ("ssm1_p128", 2048))
+# the general selective layer (one layer), measured the same way
+SEL_CONTEXT = (("sel1_p1024", 8192), ("sel1_p1024", None))
 METRIC = "adjoint-gradient tokens/sec per layer on 1 GB300; % of HBM/tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # CPU oracle samples (prefixes of one sequence of the headline workload): all cores on
@@ -196,6 +198,23 @@ def kernel_table(P, N, xb, db, trunc, K=1):
                            flops=2 * 3 * N * P),
         "rms_norm": dict(bytes=4 * P + P * xb + 4),
         "rms_norm_bwd": dict(bytes=16 * P + 4),
+    }
+
+
+def sel_kernel_table(P, N, xb, db):
+    """The general selective layer: algorithmic bytes (and flops) per token of each call's
+    kernels (each scan counts its three launches together).  The forward scan reads z and
+    xhat and writes h and y; the reverse scan reads z, xhat, gy and h and writes dz (the
+    truncated form also writes and reads the window sums R, 8 P N bytes a token beyond
+    these counts)."""
+    zw = P + 2 * N
+    return {
+        "sel_proj": dict(bytes=P * xb + zw * 4, flops=2 * P * zw),
+        "sel_fwd": dict(bytes=zw * 4 + P * xb + 4 * P * N + 4 * P),
+        "loss": dict(bytes=3 * P * 4),
+        "sel_bwd": dict(bytes=zw * 4 + P * xb + 4 * P + 4 * P * N + zw * db),
+        "sel_dW": dict(bytes=P * xb + zw * db, flops=2 * P * zw),
+        "colsum": dict(bytes=P * db),
     }
 
 
@@ -533,6 +552,64 @@ def context_line(key, window, dev, peaks, steps, warmup):
     return out
 
 
+def sel_context_line(key, window, dev, peaks, steps, warmup):
+    """The general selective layer on one of its workloads: graph replay of one step
+    (forward, loss, reverse, parameter gradients), L2 flushed before every step, median."""
+    import torch
+    from adjoint_gradients_long_gb300 import lib, synth
+    from adjoint_gradients_long_gb300.sel_layer import SelLayer
+    w = synth.SEL_WORKLOADS[key]
+    bf16 = w.x_dtype == "bf16"
+    L = SelLayer(w.B, w.T, w.P, w.N, x_bf16=bf16, Tbar=window, device=dev)
+    L.load(synth.make_sel_inputs(w))
+    for _ in range(warmup):
+        L.step(window)
+    n0 = lib.launch_count()
+    g = L.capture(window)
+    torch.cuda.synchronize(dev)
+    per = (lib.launch_count() - n0) // 2
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(n, replay=True):
+        ev = []
+        for _ in range(n):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if replay:
+                g.replay()
+            else:
+                L.step(window)
+            e1.record(stream)
+            ev.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    for _ in range(warmup):
+        g.replay()
+    ms = timed(steps)
+    status = L.status()
+    lib.profile_reset()
+    lib.profile_enable(True)
+    timed(min(steps, 5), replay=False)
+    lib.profile_enable(False)
+    prof = lib.profile_read()
+    lib.profile_reset()
+    xb = 2 if bf16 else 4
+    kern = kernels_summary(prof, sel_kernel_table(w.P, w.N, xb, xb), w.B * w.T, peaks, split3=not bf16)
+    med = statistics.median(ms)
+    out = {"workload": key, "layer": "general selective (softplus step, exp(dt A) decay, input-dependent B_t, C_t)",
+           "window": window if window is not None else "full", "B": w.B, "T": w.T, "P": w.P, "N": w.N, "K": 1,
+           "dtype": "bf16 GEMM operands, fp32 scans" if bf16 else "f32",
+           "value": w.B * w.T / (med * 1e-3), "unit": "tokens/s per layer", "ms_per_step": med,
+           "ms_mean": sum(ms) / len(ms), "steps": steps, "gpu_launches_per_step": per,
+           "device_status": lib.STATUS.get(status, status), "kernels": kern}
+    del g, L, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -620,6 +697,8 @@ def run_ours(args, rank, world, local_rank):
         del wl
         for k2, w2 in CONTEXT:
             others.append(context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3))))
+        for k2, w2 in SEL_CONTEXT:
+            others.append(sel_context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3))))
 
     if rank == 0:
         line = {

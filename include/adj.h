@@ -74,10 +74,13 @@ typedef struct {
     const void *W_o;
 } adj_weights;
 
-enum { ADJ_OP_FWD = 0, ADJ_OP_BWD_FULL = 1, ADJ_OP_BWD_TRUNC = 2, ADJ_OP_PARAM = 3, ADJ_OP_LOSS = 4 };
+enum {
+    ADJ_OP_FWD = 0, ADJ_OP_BWD_FULL = 1, ADJ_OP_BWD_TRUNC = 2, ADJ_OP_PARAM = 3, ADJ_OP_LOSS = 4,
+    ADJ_OP_SEL_FWD = 5, ADJ_OP_SEL_BWD = 6, ADJ_OP_SEL_PARAM = 7   /* the general selective layer (below) */
+};
 
 /* Workspace bytes that call `op` needs for these sizes (Tbar: the window of
- * ADJ_OP_BWD_TRUNC, ignored otherwise).  One workspace of the maximum over the
+ * ADJ_OP_BWD_TRUNC and ADJ_OP_SEL_BWD, ignored otherwise).  One workspace of the maximum over the
  * ops used serves them all.  Returns 0 for invalid sizes. */
 size_t adj_workspace_bytes(const adj_dims *dims, int op, int64_t Tbar);
 
@@ -166,6 +169,57 @@ adj_status adj_rms_norm(const adj_dims *dims, const float *y, void *xhat, float 
  * gy_prev [B,T,P] fp32 may alias dxhat or gy. */
 adj_status adj_rms_norm_bwd(const adj_dims *dims, const float *y, const float *r, const float *dxhat,
                             const float *gy, float *gy_prev, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The general selective layer.  The pages give the layer only in its general form
+ * h_t = A_t h_{t-1} + B_t xhat_t, y_t = C_t h_t with A_t, B_t, C_t functions of the token
+ * ([AS] Circularity Check, assumptions); these calls take its selective reading, per
+ * channel p < P and state n < N (N = 8 or 16):
+ *     z_t = xhat_t W_in                      W_in [P, P+2N] = [W_dt | W_B | W_C]
+ *     dt_t,p = softplus(z_t,p + b_dt,p),  B_t,n = z_t,P+n,  C_t,n = z_t,P+N+n
+ *     Abar_t,pn = exp(dt_t,p A_pn)            A [P,N], the continuous-time decay
+ *     h_t,pn = Abar_t,pn h_t-1,pn + dt_t,p B_t,n xhat_t,p   (h_-1 = 0)
+ *     y_t,p = xhat_t,p + sum_n C_t,n h_t,pn   (the residual identity)
+ * i.e. a PN-dimensional state with A_t = diag(Abar_t) and the full P x PN output map
+ * C_t[p, (p,n)] = C_t,n.  Its gradient is the same sum over token pairs of independent
+ * VJPs as the diagonal layer's ([AS] Core claim, Proposition 2), full or truncated to a
+ * window.  Sizes: adj_dims with N = 8 or 16, P a multiple of 8, B <= 65535; x_dtype is
+ * the storage of xhat and W_in, d_dtype that of dz.  h is [B,T,P,N] fp32 (state index
+ * last).  No call waits on another CTA, so none records ADJ_ETIMEOUT.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const void *W_in;    /* [P, P+2N] x_dtype */
+    const float *b_dt;   /* [P] */
+    const float *A;      /* [P, N] */
+} adj_sel_weights;
+
+/* Forward pass storing what the adjoint needs ([AS] Referee Report on Algorithm 1: the
+ * per-token states are kept):
+ *   xhat [B,T,P] x_dtype    layer input
+ *   z    [B,T,P+2N] fp32    xhat W_in, without b_dt (written)
+ *   h    [B,T,P,N] fp32     states (written)
+ *   y    [B,T,P] fp32       layer output (written) */
+adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, float *z, float *h,
+                       float *y, void *ws, size_t ws_bytes, void *stream);
+
+/* Adjoint of one selective layer for the cotangent gy = dL/dy [B,T,P] fp32: the window
+ * sums mu_i = sum_{t=i}^{min(T-1, i+Tbar-1)} gy_t^T C_t prod_{j=i+1..t} A_j (all t >= i when
+ * Tbar <= 0 or Tbar >= T; otherwise Tbar must be a multiple of 16), and the VJP of every
+ * token's step and output map ([AS] Core claim, Proposition 2; last sentence: truncation):
+ *   dz [B,T,P+2N] d_dtype   cotangent of z (written): columns p < P: the step's
+ *                           (sum_n mu_pn (A_pn Abar_pn h_{t-1},pn + B_n xhat_p)) sigmoid(z_p + b_dt,p);
+ *                           columns P+n: sum_p mu_pn dt_p xhat_p (B_t); P+N+n: sum_p gy_p h_t,pn (C_t)
+ *   dA [P,N] fp32           sum_t mu_pn dt_p Abar_pn h_{t-1},pn (written)
+ * xhat, z, h as written by adj_sel_fwd. */
+adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const float *z,
+                       const float *h, const float *gy, int64_t Tbar, void *dz, float *dA, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Parameter gradients from dz ([AS] Core claim: the sum over tokens of the VJPs):
+ *   dW_in [P, P+2N] fp32 = sum_t xhat_t^T dz_t,   db_dt [P] fp32 = sum_t dz_t[:P].
+ * accumulate != 0 adds into the outputs instead of overwriting them. */
+adj_status adj_sel_param_grad(const adj_dims *dims, const void *xhat, const void *dz, float *dW_in, float *db_dt,
+                              int accumulate, void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronise `stream`, return and clear the sticky device status of `ws`
  * (ADJ_OK or ADJ_ETIMEOUT); ADJ_ECUDA if the stream reports an error. */

@@ -189,8 +189,18 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
             }
         free(v);
     } else {
-        /* V_i = sum_{t=i}^{i+W-1} v_{t,i}, each pair's vector formed walking i down */
+        /* V_i = sum_{t=i}^{i+W-1} v_{t,i}, each pair's vector formed walking i down; the
+         * factors Abar_i,pn = exp(dt_i,p A_pn) are tabulated once */
         double *V = calloc((size_t)(B * T * PN), sizeof(double));
+        double *Ab = malloc(sizeof(double) * (size_t)(B * T * PN));
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+        for (int64_t r = 0; r < B * T; ++r)
+            for (int64_t p = 0; p < P; ++p) {
+                const double dt = softplus(z[r * Z + p]);
+                for (int64_t n = 0; n < N; ++n) Ab[r * PN + p * N + n] = exp(dt * A[p * N + n]);
+            }
 #ifdef _OPENMP
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
 #endif
@@ -204,15 +214,17 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
                     if (lo < 0) lo = 0;
                     for (int64_t i = t; i >= lo; --i) {
                         const int64_t ri = b * T + i;
-                        for (int64_t n = 0; n < N; ++n) V[ri * PN + p * N + n] += vv[n];
+                        double *Vi = V + ri * PN + p * N;
+                        for (int64_t n = 0; n < N; ++n) Vi[n] += vv[n];
                         if (i > lo) {   /* v_{t,i-1} = v_{t,i} . Abar_i */
-                            const double dti = softplus(z[ri * Z + p]);
-                            for (int64_t n = 0; n < N; ++n) vv[n] *= exp(dti * A[p * N + n]);
+                            const double *ab = Ab + ri * PN + p * N;
+                            for (int64_t n = 0; n < N; ++n) vv[n] *= ab[n];
                         }
                     }
                 }
                 free(vv);
             }
+        free(Ab);
         for (int64_t b = 0; b < B; ++b)
             for (int64_t i = 0; i < T; ++i) {
                 const int64_t ri = b * T + i;
@@ -228,4 +240,81 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
     free(ddt);
     param_from_dz(B * T, P, N, x, dz, dW_in, db_dt);
     return count;
+}
+
+/* dz at sampled rows, for sequences too long for sel_grad: the same window sums
+ * mu_i = sum_{t=i}^{min(T-1,i+W-1)} gy_t C_t prod_{j=i+1..t} Abar_j and the same step and
+ * output VJPs, evaluated at the sampled tokens only.  x [B,T,P] and target [B,T,P] are
+ * the layer input and target, z [B,T,P+2N] its projection with the bias (any exact
+ * evaluation of xhat W_in + [b_dt, 0, 0]).  The forward recurrence runs over every token
+ * of each sampled sequence, keeping y only on the tokens some window needs.
+ * samp_b[s], samp_t[s] (s < ns): the sampled rows; dz_out [ns, P+2N]. */
+void sel_dz_rows(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, const double *x, const double *A,
+                 const double *z, const double *target, int64_t ns, const int64_t *samp_b, const int64_t *samp_t,
+                 double *dz_out)
+{
+    const int64_t Z = P + 2 * N, PN = P * N, W = window_of(T, Tbar);
+    (void)B;
+    for (int64_t s = 0; s < ns; ++s) {
+        const int64_t b = samp_b[s], i = samp_t[s];
+        const int64_t tend = (i + W - 1 < T - 1) ? i + W - 1 : T - 1;
+        const int64_t nw = tend - i + 1;
+        double *gw = malloc(sizeof(double) * (size_t)(nw * P));    /* gy_t, t in [i, tend] */
+        double *hp = calloc((size_t)PN, sizeof(double));           /* h_{i-1} */
+        double *hi = malloc(sizeof(double) * (size_t)PN);          /* h_i */
+        /* forward over [0, tend], channels in parallel */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+        for (int64_t p = 0; p < P; ++p) {
+            double *hv = calloc((size_t)N, sizeof(double));
+            for (int64_t t = 0; t <= tend; ++t) {
+                const int64_t r = b * T + t;
+                const double *zr = z + r * Z;
+                const double dt = softplus(zr[p]);
+                double out = x[r * P + p];
+                for (int64_t n = 0; n < N; ++n) {
+                    hv[n] = exp(dt * A[p * N + n]) * hv[n] + dt * zr[P + n] * x[r * P + p];
+                    out += zr[P + N + n] * hv[n];
+                }
+                if (t == i - 1)
+                    for (int64_t n = 0; n < N; ++n) hp[p * N + n] = hv[n];
+                if (t == i)
+                    for (int64_t n = 0; n < N; ++n) hi[p * N + n] = hv[n];
+                if (t >= i) gw[(t - i) * P + p] = out - target[r * P + p];
+            }
+            free(hv);
+        }
+        /* mu_i by its definition, then the VJPs of token i */
+        double *mu = calloc((size_t)PN, sizeof(double));
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+        for (int64_t p = 0; p < P; ++p)
+            for (int64_t n = 0; n < N; ++n) {
+                double prod = 1.0, acc = 0.0;
+                for (int64_t t = i; t <= tend; ++t) {
+                    if (t > i) prod *= exp(softplus(z[(b * T + t) * Z + p]) * A[p * N + n]);
+                    acc += gw[(t - i) * P + p] * z[(b * T + t) * Z + P + N + n] * prod;
+                }
+                mu[p * N + n] = acc;
+            }
+        const int64_t ri = b * T + i;
+        const double *zr = z + ri * Z, *xr = x + ri * P;
+        double *out = dz_out + s * Z;
+        memset(out, 0, sizeof(double) * (size_t)Z);
+        for (int64_t p = 0; p < P; ++p) {
+            const double dt = softplus(zr[p]);
+            double ddt = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double ab = exp(dt * A[p * N + n]);
+                const double v = mu[p * N + n];
+                ddt += v * (A[p * N + n] * ab * hp[p * N + n] + zr[P + n] * xr[p]);
+                out[P + n] += v * dt * xr[p];
+                out[P + N + n] += gw[p] * hi[p * N + n];
+            }
+            out[p] = ddt * sigmoid(zr[p]);
+        }
+        free(mu); free(gw); free(hp); free(hi);
+    }
 }

@@ -50,6 +50,8 @@ def _bind(path: str):
     lib.sel_forward.restype = None
     lib.sel_grad.argtypes = [_I64] * 5 + [ctypes.c_int] + [_D] * 10
     lib.sel_grad.restype = _I64
+    lib.sel_dz_rows.argtypes = [_I64] * 5 + [_D] * 4 + [_I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64), _D]
+    lib.sel_dz_rows.restype = None
     return lib
 
 
@@ -125,3 +127,25 @@ def loss_and_cotangent(y: np.ndarray, target: np.ndarray):
     """L = sum 1/2 ||y - target||^2 and gy = y - target (fp64)."""
     d = _f64(y) - _f64(target)
     return 0.5 * float(np.sum(d * d)), d
+
+
+def dz_rows(W: dict, xhat: np.ndarray, target: np.ndarray, rows, Tbar=None) -> np.ndarray:
+    """dz at sampled rows [(b, t), ...] of a long sequence (fp64): the window sums and VJPs
+    of those tokens only, with the forward recurrence run over every token before them.
+    The projection z = xhat W_in + [b_dt, 0, 0] is taken with a library matmul."""
+    lib = _load()
+    x = _f64(xhat)
+    B, T, P = x.shape
+    N = W["A"].shape[1]
+    A = _f64(W["A"])
+    z = x.reshape(B * T, P) @ _f64(W["W_in"])
+    z[:, :P] += _f64(W["b_dt"])
+    z = np.ascontiguousarray(z)
+    tg = _f64(target)
+    sb = np.ascontiguousarray([r[0] for r in rows], dtype=np.int64)
+    stt = np.ascontiguousarray([r[1] for r in rows], dtype=np.int64)
+    out = np.empty((len(rows), P + 2 * N))
+    pi = ctypes.POINTER(_I64)
+    lib.sel_dz_rows(B, T, P, N, 0 if Tbar is None else int(Tbar), _p(x), _p(A), _p(z), _p(tg), len(rows),
+                    sb.ctypes.data_as(pi), stt.ctypes.data_as(pi), _p(out))
+    return out

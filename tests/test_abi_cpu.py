@@ -144,3 +144,33 @@ def test_binding_arities_match_header(L):
         fn = getattr(L, name)
         if fn.argtypes is not None:
             assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
+def test_selective_layer_rejects_bad_arguments(L):
+    """The general selective layer's calls: N must be 8 or 16, a truncation window a
+    multiple of 16, every pointer present, the workspace large enough; refused before
+    anything launches (the pointers are never dereferenced)."""
+    big = 1 << 40
+    w = lib.SelWeights(FAKE, FAKE, FAKE)
+
+    def fwd(d, ws_bytes=big, h=FAKE):
+        return L.adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, h, FAKE, FAKE, ws_bytes, None)
+
+    def bwd(d, Tbar=0, dz=FAKE):
+        return L.adj_sel_bwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, Tbar, dz, FAKE, FAKE, big, None)
+
+    assert fwd(lib.dims(1, 64, 32, 24)) == 2                 # N = 24
+    assert fwd(lib.dims(1, 64, 32, 32)) == 2                 # N = 32
+    assert fwd(lib.dims(1, 64, 32, 16), h=None) == 1
+    assert fwd(lib.dims(1, 64, 32, 16), h=FAKE + 4) == 3
+    d = lib.dims(2, 1000, 64, 16)
+    assert fwd(d, ws_bytes=lib.workspace_bytes(d, lib.OP_SEL_FWD) - 1) == 5
+    assert fwd(lib.dims(0, 64, 32, 16)) == 0                 # empty batch: nothing to do
+    assert bwd(lib.dims(1, 1000, 32, 16), Tbar=100) == 1     # window not a multiple of 16
+    assert bwd(lib.dims(1, 1000, 32, 16), dz=None) == 1
+    assert L.adj_sel_param_grad(ctypes.byref(lib.dims(1, 64, 32, 16)), FAKE, None, FAKE, FAKE, 0, FAKE, big,
+                                None) == 1
+    for op in (lib.OP_SEL_FWD, lib.OP_SEL_BWD, lib.OP_SEL_PARAM):
+        assert lib.workspace_bytes(lib.dims(1, 64, 32, 24), op) == 0
+    # the truncated window's scratch (aggregates and R) makes its workspace the larger
+    assert lib.workspace_bytes(d, lib.OP_SEL_BWD, 256) > lib.workspace_bytes(d, lib.OP_SEL_BWD, 0)

@@ -145,3 +145,15 @@ def test_sequences_are_independent():
     b, _, _ = oracle_grad(W, x[1:], tgt[1:], Tbar=5)
     for k in ("dW_in", "db_dt", "dA"):
         assert rel(both[k], a[k] + b[k]) < 1e-13, k
+
+
+@pytest.mark.parametrize("Tbar", [None, 6])
+def test_sampled_rows_equal_the_whole_gradient(Tbar):
+    """The sampled-row evaluation (for sequences too long for the whole sum) gives the
+    same dz rows as the aggregated gradient."""
+    W, x, tgt = tiny(T=30, B=2)
+    g, _, _ = oracle_grad(W, x, tgt, Tbar)
+    rows = [(0, 0), (0, 17), (1, 29), (1, 3)]
+    got = sel.dz_rows(W, x, tgt, rows, Tbar)
+    for s, (b, t) in enumerate(rows):
+        assert rel(got[s], g["dz"][b, t]) < 1e-12, (b, t)
