@@ -558,7 +558,7 @@ adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const voi
     sw.dAp = reinterpret_cast<float *>(at(ws, L.part1));
     ProfScope ps(K_SEL_BWD, st, tr ? 8 : 5);
     ADJ_CUDA(launch_sel_bwd(z, xhat, dims->x_dtype == ADJ_BF16, gy, h, w->b_dt, w->A, dz, dims->d_dtype == ADJ_BF16, dA,
-                            sw, B, T, P, N, tr ? Tbar : 0, st));
+                            sw, B, T, P, N, tr ? Tbar : 0, status_word(ws), st));
     return ADJ_OK;
 }
 

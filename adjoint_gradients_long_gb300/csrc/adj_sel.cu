@@ -16,67 +16,166 @@
 // diagonal layer's: S, Q the reverse scan restarted at every block end, R the forward scan
 // restarted at every block start, R(m) = sum_{t=s}^{m} e_t prod_{j=s+1..t} Abar_j).
 //
-// Work decomposition.  A thread owns one channel p and 8 of its states (SEL_NT); a CTA of
+// Work decomposition.  A thread owns one channel p and SEL_NT = 8 of its states; a CTA of
 // 256 threads owns 256 / (NS / 8) channels of one chunk of TT consecutive tokens of one
 // sequence and walks the chunk token by token.  Every scan runs in three launches with no
 // CTA ever waiting on another: (1) each chunk's aggregate (the composite of its tokens),
 // (2) one pass per (sequence, channel, state) over the chunk aggregates in scan order,
 // writing each chunk's incoming carry in place, (3) each chunk again from its carry,
-// writing the outputs.  The per-token inputs of the scans (z, xhat, gy: P + 2NS values a
-// token) are small next to the state (P NS values), so reading them twice costs little;
-// h is written once (forward) and read once (reverse).
+// writing the outputs.  The per-token inputs (the step dt = softplus(z + b_dt), xhat, gy,
+// B_t, C_t: P + 2NS values a token) are staged in shared memory a sub-chunk at a time by
+// coalesced loads of the whole CTA, so the per-token walk reads only shared memory; they
+// are small next to the state (P NS values a token), so reading them in both passes costs
+// little.  h is written once (forward, streaming stores) and read once (reverse): the
+// reverse pass has one more warp that only brings the chunk's state rows (and, truncated,
+// the window sums R) into a ring of shared-memory stages by bulk copies, counted on a
+// "full" mbarrier per stage; the walking warps release a stage on its "empty" mbarrier
+// (bounded waits on both).
 #include <math.h>
 
 #include "adj_internal.cuh"
+#include "adj_ptx.cuh"
 #include "adj_sel.cuh"
 
 namespace adj {
 
 namespace {
 
-constexpr int SEL_THREADS = 256;
+constexpr int SEL_THREADS = 256;   // the walking threads of a CTA
 constexpr float LOG2E = 1.4426950408889634f;
 
 __device__ __forceinline__ float softplus_f(float z) { return z > 20.f ? z : log1pf(expf(z)); }
-__device__ __forceinline__ float sigmoid_f(float z) { return 1.f / (1.f + expf(-z)); }
 __device__ __forceinline__ float ldx(const float *p) { return __ldg(p); }
 __device__ __forceinline__ float ldx(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+// 2^x by the SFU's approximate exponential (relative error about 2^-22; subnormal results
+// flush to zero, a decay that small is zero for every purpose here)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// barrier 1 among the 256 walking threads (the reverse pass's copy warp stays out)
+__device__ __forceinline__ void walkers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int NS>
-struct Geo {   // a thread's place: channel p, states n0 .. n0 + 8
-    static constexpr int LP = NS / SEL_NT;               // threads per channel
-    static constexpr int PC = SEL_THREADS / LP;          // channels per CTA
-    int p, n0;
+struct Geo {   // a thread's place: channel p (q within the slice), states n0 .. n0 + SEL_NT
+    static constexpr int LP = NS / SEL_NT;               // threads a channel (adjacent lanes)
+    static constexpr int PC = SEL_THREADS / LP;          // channels a CTA
+    static constexpr int SC = 2048 / PC;                 // tokens a staged sub-chunk
+    int q, p, n0;
     bool act;
     __device__ Geo(int slice, int P) {
-        p = slice * PC + int(threadIdx.x) / LP;
+        q = int(threadIdx.x) / LP;
+        p = slice * PC + q;
         n0 = (int(threadIdx.x) % LP) * SEL_NT;
         act = p < P;
     }
 };
 
-// 8 consecutive floats of a row (32-byte aligned)
-__device__ __forceinline__ void ld8(const float *p, float (&v)[SEL_NT]) {
-    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p)), b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+// sum over the LP lanes of a channel
+template <int LP>
+__device__ __forceinline__ float chan_sum(float v) {
+    if (LP >= 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v;
+}
+
+__device__ __forceinline__ void ld8s(const float *p, float (&v)[SEL_NT]) {   // shared
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-__device__ __forceinline__ void st8(float *p, const float (&v)[SEL_NT]) {
+__device__ __forceinline__ void ld8g(const float *p, float (&v)[SEL_NT]) {   // global, L2
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p)), b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st8v(float *p, const float (&v)[SEL_NT]) {
     reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
     reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
-__device__ __forceinline__ void st8_stream(float *p, const float (&v)[SEL_NT]) {
+__device__ __forceinline__ void st8s(float *p, const float (&v)[SEL_NT]) {   // streaming
     __stcs(reinterpret_cast<float4 *>(p), make_float4(v[0], v[1], v[2], v[3]));
     __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
 }
 
-// Stage columns [col0, col0 + NS) of the chunk's z rows (B_t or C_t), zero past T.
+// Shared staging of one sub-chunk (rows [r0, r0 + nr) of the chunk starting at global row
+// row0; zero past nr and past P): dt [SC][PC], xhat [SC][PC] (WX), gy [SC][PC] (WG), and
+// the z columns of B_t and C_t [SC][NS] each.
 template <int NS>
-__device__ __forceinline__ void stage_cols(float (*dst)[NS], const float *z, int64_t row0, int64_t rows, int ZW,
-                                           int col0, int TT) {
-    for (int i = threadIdx.x; i < TT * NS; i += SEL_THREADS) {
-        const int r = i / NS, n = i % NS;
-        dst[r][n] = r < rows ? z[(row0 + r) * ZW + col0 + n] : 0.f;
+struct Stage {
+    float *dt, *x, *g, *sig, *B, *C;
+};
+template <int NS>
+__device__ __forceinline__ Stage<NS> stage_carve(float *base) {
+    constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC;
+    Stage<NS> s;
+    s.dt = base;
+    s.x = s.dt + SC * PC;
+    s.g = s.x + SC * PC;
+    s.sig = s.g + SC * PC;
+    s.B = s.sig + SC * PC;
+    s.C = s.B + SC * NS;
+    return s;
+}
+template <int NS>
+constexpr size_t stage_floats() {
+    return size_t(Geo<NS>::SC) * Geo<NS>::PC * 4 + size_t(Geo<NS>::SC) * NS * 2;
+}
+// The sub-chunk's per-token inputs as loaded into registers (a thread's share).
+template <int NS>
+struct StageRegs {
+    static constexpr int PER = Geo<NS>::SC * Geo<NS>::PC / SEL_THREADS;
+    float z[PER], x[PER], g[PER], b[PER], bc[(Geo<NS>::SC * 2 * NS + SEL_THREADS - 1) / SEL_THREADS];
+};
+template <int NS, typename TX, bool WX, bool WG>
+__device__ __forceinline__ void stage_load(StageRegs<NS> &R, const float *__restrict__ z, const TX *__restrict__ x,
+                                           const float *__restrict__ gy, const float *__restrict__ b_dt, int P,
+                                           int ZW, int64_t row0, int r0, int nr, int p0) {
+    constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC, PER = StageRegs<NS>::PER;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {   // every load of the sub-chunk in flight at once
+        const int i = int(threadIdx.x) + u * SEL_THREADS, r = i / PC, p = p0 + i % PC;
+        const bool ok = r < nr && p < P;
+        const int64_t row = row0 + r0 + r;
+        R.z[u] = ok ? z[row * ZW + p] : 0.f;
+        R.b[u] = ok ? __ldg(b_dt + p) : 0.f;
+        R.x[u] = (WX && ok) ? ldx(x + row * P + p) : 0.f;
+        R.g[u] = (WG && ok) ? gy[row * P + p] : 0.f;
     }
+#pragma unroll
+    for (int u = 0; u < int(sizeof(R.bc) / sizeof(float)); ++u) {
+        const int i = int(threadIdx.x) + u * SEL_THREADS, r = i / (2 * NS), j = i % (2 * NS);
+        R.bc[u] = (i < SC * 2 * NS && r < nr) ? z[(row0 + r0 + r) * ZW + P + j] : 0.f;
+    }
+}
+template <int NS, bool WX, bool WG>
+__device__ __forceinline__ void stage_store(const Stage<NS> &s, const StageRegs<NS> &R, int nr, int p0, int P) {
+    constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC, PER = StageRegs<NS>::PER;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int i = int(threadIdx.x) + u * SEL_THREADS, r = i / PC, p = p0 + i % PC;
+        const bool ok = r < nr && p < P;
+        // dt = softplus(s) and, for the reverse pass, sigmoid(s) = e^s / (1 + e^s), s = z + b_dt
+        const float sv = R.z[u] + R.b[u], es = expf(fminf(sv, 20.f));
+        s.dt[i] = ok ? (sv > 20.f ? sv : log1pf(es)) : 0.f;
+        if (WG) s.sig[i] = ok ? es / (1.f + es) : 0.f;
+        if (WX) s.x[i] = R.x[u];
+        if (WG) s.g[i] = R.g[u];
+    }
+#pragma unroll
+    for (int u = 0; u < int(sizeof(R.bc) / sizeof(float)); ++u) {
+        const int i = int(threadIdx.x) + u * SEL_THREADS, r = i / (2 * NS), j = i % (2 * NS);
+        if (i < SC * 2 * NS) {
+            if (j < NS) s.B[r * NS + j] = R.bc[u];
+            else s.C[r * NS + j - NS] = R.bc[u];
+        }
+    }
+}
+template <int NS, typename TX, bool WX, bool WG>
+__device__ __forceinline__ void stage_sub(const Stage<NS> &s, const float *__restrict__ z, const TX *__restrict__ x,
+                                          const float *__restrict__ gy, const float *__restrict__ b_dt, int P,
+                                          int ZW, int64_t row0, int r0, int nr, int p0) {
+    StageRegs<NS> R;
+    stage_load<NS, TX, WX, WG>(R, z, x, gy, b_dt, P, ZW, row0, r0, nr, p0);
+    stage_store<NS, WX, WG>(s, R, nr, p0, P);
 }
 
 // ------------------------------------------------------------------ forward state scan
@@ -88,56 +187,62 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
                                                         float *__restrict__ h, float *__restrict__ y, int64_t T, int P,
                                                         int TT, int64_t nchunks) {
-    extern __shared__ float sm_sel[];
-    float(*sB)[NS] = reinterpret_cast<float(*)[NS]>(sm_sel);
-    float(*sC)[NS] = reinterpret_cast<float(*)[NS]>(sm_sel + TT * NS);
+    extern __shared__ __align__(16) float sm_sel[];
+    constexpr int PC = Geo<NS>::PC, LP = Geo<NS>::LP, SC = Geo<NS>::SC;
+    const Stage<NS> sg = stage_carve<NS>(sm_sel);
     const int64_t c = blockIdx.x, b = blockIdx.z;
-    const Geo<NS> g(int(blockIdx.y), P);
+    const int slice = int(blockIdx.y);
+    const Geo<NS> g(slice, P);
     const int ZW = P + 2 * NS;
-    const int64_t c0 = c * TT, rows = (c0 + TT <= T ? TT : T - c0), row0 = b * T + c0;
-    stage_cols<NS>(sB, z, row0, rows, ZW, P, TT);
-    if (MODE == 1) stage_cols<NS>(sC, z, row0, rows, ZW, P + NS, TT);
-    __syncthreads();
-    // a channel's threads are adjacent lanes, so a warp's lanes past P are whole channels;
-    // they stay in the loop (on channel 0's inputs, storing nothing) for the lane-pair sum
+    const int64_t c0 = c * TT, row0 = b * T + c0;
+    const int rows = int(c0 + TT <= T ? TT : T - c0);
+    // a channel's lanes past P stay in the walk (on zeros, storing nothing) for the lane sums
     const int pp = g.act ? g.p : 0;
     float A2[SEL_NT], st[SEL_NT], pr[SEL_NT];
 #pragma unroll
     for (int k = 0; k < SEL_NT; ++k) {
         A2[k] = A[pp * NS + g.n0 + k] * LOG2E;
         pr[k] = 1.f;
+        st[k] = 0.f;
     }
     const int64_t ai = ((b * nchunks + c) * P + pp) * NS + g.n0;
-    if (MODE == 1) {
-#pragma unroll
-        for (int k = 0; k < SEL_NT; ++k) st[k] = aggY[ai + k];
-    } else {
-#pragma unroll
-        for (int k = 0; k < SEL_NT; ++k) st[k] = 0.f;
-    }
-    const float bd = b_dt[pp];
-    for (int r = 0; r < rows; ++r) {
-        const int64_t row = row0 + r;
-        const float dt = softplus_f(z[row * ZW + pp] + bd);
-        const float xv = ldx(x + row * P + pp);
-        const float dx = dt * xv;
-        float yp = 0.f;
-#pragma unroll
-        for (int k = 0; k < SEL_NT; ++k) {
-            const float ab = exp2f(dt * A2[k]);
-            st[k] = fmaf(ab, st[k], dx * sB[r][g.n0 + k]);
-            if (MODE == 0) pr[k] *= ab;
-            else yp = fmaf(sC[r][g.n0 + k], st[k], yp);
+    if (MODE == 1 && g.act) ld8g(aggY + ai, st);
+    // the next sub-chunk's inputs load into registers while this one is walked
+    StageRegs<NS> R;
+    stage_load<NS, TX, true, false>(R, z, x, nullptr, b_dt, P, ZW, row0, 0, rows < SC ? rows : SC, slice * PC);
+    for (int r0 = 0; r0 < rows; r0 += SC) {
+        const int nr = rows - r0 < SC ? rows - r0 : SC;
+        __syncthreads();   // the previous sub-chunk is consumed
+        stage_store<NS, true, false>(sg, R, nr, slice * PC, P);
+        __syncthreads();
+        if (r0 + SC < rows) {
+            const int nn = rows - r0 - SC < SC ? rows - r0 - SC : SC;
+            stage_load<NS, TX, true, false>(R, z, x, nullptr, b_dt, P, ZW, row0, r0 + SC, nn, slice * PC);
         }
-        if (MODE == 1) {
-            if (g.act) st8_stream(h + (row * P + pp) * NS + g.n0, st);
-            if (Geo<NS>::LP == 2) yp += __shfl_xor_sync(0xffffffffu, yp, 1);
-            if (g.act && g.n0 == 0) y[row * P + pp] = xv + yp;
+        for (int r = 0; r < nr; ++r) {
+            const float dt = sg.dt[r * PC + g.q], xv = sg.x[r * PC + g.q], dx = dt * xv;
+            float Bv[SEL_NT], Cv[SEL_NT];
+            ld8s(sg.B + r * NS + g.n0, Bv);
+            if (MODE == 1) ld8s(sg.C + r * NS + g.n0, Cv);
+            float yp = 0.f;
+#pragma unroll
+            for (int k = 0; k < SEL_NT; ++k) {
+                const float ab = ex2(dt * A2[k]);
+                st[k] = fmaf(ab, st[k], dx * Bv[k]);
+                if (MODE == 0) pr[k] *= ab;
+                else yp = fmaf(Cv[k], st[k], yp);
+            }
+            if (MODE == 1) {
+                const int64_t row = row0 + r0 + r;
+                if (g.act) st8s(h + (row * P + pp) * NS + g.n0, st);
+                yp = chan_sum<LP>(yp);
+                if (g.act && g.n0 == 0) y[row * P + pp] = xv + yp;
+            }
         }
     }
     if (MODE == 0 && g.act) {
-        st8(aggX + ai, pr);
-        st8(aggY + ai, st);
+        st8v(aggX + ai, pr);
+        st8v(aggY + ai, st);
     }
 }
 
@@ -151,39 +256,56 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sel_win(const float *__restrict
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
                                                         float *__restrict__ R, int64_t T, int P, int TT,
                                                         int64_t nchunks, int64_t W) {
-    extern __shared__ float sm_sel[];
-    float(*sC)[NS] = reinterpret_cast<float(*)[NS]>(sm_sel);
+    extern __shared__ __align__(16) float sm_sel[];
+    constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC;
+    const Stage<NS> sg = stage_carve<NS>(sm_sel);
     const int64_t c = blockIdx.x, b = blockIdx.z;
-    const Geo<NS> g(int(blockIdx.y), P);
+    const int slice = int(blockIdx.y);
+    const Geo<NS> g(slice, P);
     const int ZW = P + 2 * NS;
-    const int64_t c0 = c * TT, rows = (c0 + TT <= T ? TT : T - c0), row0 = b * T + c0;
-    stage_cols<NS>(sC, z, row0, rows, ZW, P + NS, TT);
-    __syncthreads();
-    if (!g.act) return;
+    const int64_t c0 = c * TT, row0 = b * T + c0;
+    const int rows = int(c0 + TT <= T ? TT : T - c0);
+    const int pp = g.act ? g.p : 0;
     float A2[SEL_NT], pi[SEL_NT], rr[SEL_NT];
-    const int64_t ai = ((b * nchunks + c) * P + g.p) * NS + g.n0;
+    const int64_t ai = ((b * nchunks + c) * P + pp) * NS + g.n0;
 #pragma unroll
     for (int k = 0; k < SEL_NT; ++k) {
-        A2[k] = A[g.p * NS + g.n0 + k] * LOG2E;
-        pi[k] = MODE == 1 ? aggX[ai + k] : 1.f;
-        rr[k] = MODE == 1 ? aggY[ai + k] : 0.f;
+        A2[k] = A[pp * NS + g.n0 + k] * LOG2E;
+        pi[k] = 1.f;
+        rr[k] = 0.f;
     }
-    const float bd = b_dt[g.p];
-    for (int r = 0; r < rows; ++r) {
-        const int64_t row = row0 + r;
-        const float gv = gy[row * P + g.p];
-        if ((c0 + r) % W != 0) {
-            const float dt = softplus_f(z[row * ZW + g.p] + bd);
-#pragma unroll
-            for (int k = 0; k < SEL_NT; ++k) pi[k] *= exp2f(dt * A2[k]);
+    if (MODE == 1 && g.act) {
+        ld8g(aggX + ai, pi);
+        ld8g(aggY + ai, rr);
+    }
+    StageRegs<NS> RG;
+    stage_load<NS, float, false, true>(RG, z, nullptr, gy, b_dt, P, ZW, row0, 0, rows < SC ? rows : SC, slice * PC);
+    for (int r0 = 0; r0 < rows; r0 += SC) {
+        const int nr = rows - r0 < SC ? rows - r0 : SC;
+        __syncthreads();
+        stage_store<NS, false, true>(sg, RG, nr, slice * PC, P);
+        __syncthreads();
+        if (r0 + SC < rows) {
+            const int nn = rows - r0 - SC < SC ? rows - r0 - SC : SC;
+            stage_load<NS, float, false, true>(RG, z, nullptr, gy, b_dt, P, ZW, row0, r0 + SC, nn, slice * PC);
         }
+        for (int r = 0; r < nr; ++r) {
+            const float gv = sg.g[r * PC + g.q];
+            if ((c0 + r0 + r) % W != 0) {
+                const float dt = sg.dt[r * PC + g.q];
 #pragma unroll
-        for (int k = 0; k < SEL_NT; ++k) rr[k] = fmaf(pi[k], gv * sC[r][g.n0 + k], rr[k]);
-        if (MODE == 1) st8(R + (row * P + g.p) * NS + g.n0, rr);
+                for (int k = 0; k < SEL_NT; ++k) pi[k] *= ex2(dt * A2[k]);
+            }
+            float Cv[SEL_NT];
+            ld8s(sg.C + r * NS + g.n0, Cv);
+#pragma unroll
+            for (int k = 0; k < SEL_NT; ++k) rr[k] = fmaf(pi[k], gv * Cv[k], rr[k]);
+            if (MODE == 1 && g.act) st8s(R + ((row0 + r0 + r) * P + pp) * NS + g.n0, rr);
+        }
     }
-    if (MODE == 0) {
-        st8(aggX + ai, pi);
-        st8(aggY + ai, rr);
+    if (MODE == 0 && g.act) {
+        st8v(aggX + ai, pi);
+        st8v(aggY + ai, rr);
     }
 }
 
@@ -248,22 +370,19 @@ __global__ void __launch_bounds__(256) k_sel_carry(float *__restrict__ X, float 
 }
 
 // ------------------------------------------------------------------ reverse adjoint scan + VJPs
-// Butterfly transpose-sum over the lanes whose bit `lb` and above index the channel: each
-// of the 2 SEL_NT values v[] ends summed over the 32 / LP channels of the warp, one value
-// per lane (lane l holds value idx(l)).
+// Butterfly transpose-sum of the 2 SEL_NT shares v[] (dB then dC of the thread's states)
+// over the warp's channels: levels over lane bits 4..1 halve the values each time, so every
+// lane ends with one value summed over the 16 lanes that share its bit 0; with LP == 1
+// (one lane a channel) the lane pairs across bit 0 are added last (lanes l, l ^ 1 agree).
 template <int LP>
 __device__ __forceinline__ float warp_tsum16(float (&v)[2 * SEL_NT], int lane) {
-    // levels over lane bits 4..1, the 16 values halving each level; with LP == 1 the lane
-    // pairs (bit 0) are summed last
-    constexpr int V = 2 * SEL_NT;
-    int cnt = V;
+    // (fixed trip counts, so every index is a compile-time constant and v stays in registers)
 #pragma unroll
-    for (int bit = 4; bit >= 1; --bit) {
-        const int s = 1 << bit;
+    for (int lv = 0; lv < 4; ++lv) {
+        const int s = 16 >> lv, cnt = 8 >> lv;
         const bool up = (lane & s) != 0;
-        cnt >>= 1;
 #pragma unroll
-        for (int i = 0; i < V / 2; ++i) {
+        for (int i = 0; i < 8; ++i) {
             if (i < cnt) {
                 const float send = up ? v[i] : v[i + cnt];
                 const float keep = up ? v[i + cnt] : v[i];
@@ -275,142 +394,276 @@ __device__ __forceinline__ float warp_tsum16(float (&v)[2 * SEL_NT], int lane) {
     if (LP == 1) r += __shfl_xor_sync(0xffffffffu, r, 1);
     return r;
 }
-// the value index lane l holds after warp_tsum16
-__device__ __forceinline__ int tsum_index(int lane) {
+// the share index lane l holds after warp_tsum16
+__device__ __forceinline__ int tsum16_index(int lane) {
     return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
+// Bounded wait on an mbarrier phase that sleeps between polls (the waiting warp gives its
+// issue slots to the others); gives up after 2 s, recording the timeout.
+__device__ __forceinline__ void mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int *abort, unsigned *status,
+                                                uint32_t hint_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (ok) return;
+        if ((it & 15u) == 15u) {
+            if (*abort) return;
+            const uint64_t t = gtimer();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > TC_WAIT_NS) {
+                *abort = 1;
+                record_timeout(status);
+                return;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Threads of the reverse output pass: the walking warps plus one copy warp.
+constexpr int SEL_BWD_THREADS = SEL_THREADS + 32;
+#ifndef ADJ_SEL_BWD_MINB
+#define ADJ_SEL_BWD_MINB 2   // CTAs an SM the register budget is cut for
+#endif
+#ifndef ADJ_SEL_PRODUCER_SLEEP_NS
+#define ADJ_SEL_PRODUCER_SLEEP_NS 200u   // the copy warp's suspend hint while a stage is in use
+#endif
+constexpr int SEL_NSTG = 3;   // stages in the ring of state rows
+template <bool TRUNC>
+constexpr int sel_group() { return TRUNC ? 1 : 2; }   // tokens a stage
+
 // MODE 0: chunk aggregates of the reverse scan (Q = prod_{c0 < j <= c1} Abar_j, S = mu_c0
-// from mu_c1 = 0) -> aggX, aggY.
+// from mu_c1 = 0) -> aggX, aggY.  256 threads.
 // MODE 1: outputs from the carries (q_in, mu_in) in aggX, aggY: dz[:, :P] (the dt part,
 // through the softplus), the CTA's partial sums over its channels of dB and dC per token
 // -> bc [B*T, nslices, 2 NS], and the chunk's dA partial -> dAp [B*nchunks, P, NS].
 // TRUNC: mu^W = mu + q R(min(t+W-1, T-1)) where a later block exists and t starts none.
+// 256 + 32 threads: warp 8 copies the state rows (and R rows) into the stages: stage k
+// holds the rows of group k (tokens counted down from the chunk's top, G a group), one more
+// stage the row before the chunk; group k reads stages k and k + 1.
 template <int NS, typename TX, typename TD, int MODE, bool TRUNC>
-__global__ void __launch_bounds__(SEL_THREADS) k_sel_bwd(const float *__restrict__ z, const TX *__restrict__ x,
-                                                        const float *__restrict__ gy, const float *__restrict__ h,
-                                                        const float *__restrict__ R, const float *__restrict__ b_dt,
-                                                        const float *__restrict__ A, float *__restrict__ aggX,
-                                                        float *__restrict__ aggY, TD *__restrict__ dz,
-                                                        float *__restrict__ bc, float *__restrict__ dAp, int64_t T,
-                                                        int P, int TT, int64_t nchunks, int nslices, int64_t W) {
-    extern __shared__ float sm_sel[];
-    constexpr int LP = Geo<NS>::LP;
-    constexpr int TB = 16;   // tokens per batch of the cross-warp sums
-    float(*sB)[NS] = reinterpret_cast<float(*)[NS]>(sm_sel);
-    float(*sC)[NS] = reinterpret_cast<float(*)[NS]>(sm_sel + TT * NS);
-    float(*sW)[TB][32] = reinterpret_cast<float(*)[TB][32]>(sm_sel + 2 * TT * NS);   // [8 warps]
+__global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(const float *__restrict__ z, const TX *__restrict__ x,
+                                                            const float *__restrict__ gy, const float *__restrict__ h,
+                                                            const float *__restrict__ R, const float *__restrict__ b_dt,
+                                                            const float *__restrict__ A, float *__restrict__ aggX,
+                                                            float *__restrict__ aggY, TD *__restrict__ dz,
+                                                            float *__restrict__ bc, float *__restrict__ dAp, int64_t T,
+                                                            int P, int TT, int64_t nchunks, int nslices, int64_t W,
+                                                            unsigned *status) {
+    extern __shared__ __align__(16) float sm_sel[];
+    constexpr int PC = Geo<NS>::PC, LP = Geo<NS>::LP, SC = Geo<NS>::SC;
+    constexpr int G = sel_group<TRUNC>();
+    constexpr int RF = PC * NS;                            // floats of one row segment
+    constexpr int STG = G * RF * (TRUNC ? 2 : 1);          // floats a stage
+    __shared__ uint64_t s_full[SEL_NSTG], s_empty[SEL_NSTG];
+    __shared__ int s_abort;
+    const Stage<NS> sg = stage_carve<NS>(sm_sel);
+    float *sW = sm_sel + stage_floats<NS>();               // [8 warps][SC][32]
+    float *sH = sW + (SEL_THREADS / 32) * SC * 32;         // [SEL_NSTG][STG]
     const int64_t c = blockIdx.x, b = blockIdx.z;
     const int slice = int(blockIdx.y);
-    const Geo<NS> g(slice, P);
     const int ZW = P + 2 * NS, lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
-    const int64_t c0 = c * TT, rows = (c0 + TT <= T ? TT : T - c0), row0 = b * T + c0;
-    if (MODE == 1) stage_cols<NS>(sB, z, row0, rows, ZW, P, TT);
-    stage_cols<NS>(sC, z, row0, rows, ZW, P + NS, TT);
-    __syncthreads();
-    const int pp = g.act ? g.p : 0;   // inactive threads run the loop (the warp sums need them) on zeros
-    float A2[SEL_NT], mu[SEL_NT], q[SEL_NT], abn[SEL_NT], dA[SEL_NT], hc[SEL_NT];
+    const int64_t c0 = c * TT, row0 = b * T + c0;
+    const int rows = int(c0 + TT <= T ? TT : T - c0);
+    const int p0 = slice * PC;
+    const int ngroups = (rows + G - 1) / G;
+    const int nst = ngroups + (c0 > 0 ? 1 : 0);
+
+    if (MODE == 1) {
+        if (threadIdx.x == 0) {
+            for (int j = 0; j < SEL_NSTG; ++j) {
+                mbar_init(smem_u32(&s_full[j]), 1);
+                mbar_init(smem_u32(&s_empty[j]), SEL_THREADS / 32);
+            }
+            s_abort = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (wp == SEL_THREADS / 32) {   // the copy warp
+            if (lane == 0) {
+                const int pw = P - p0 < PC ? P - p0 : PC;
+                const uint32_t rowb = uint32_t(pw) * NS * 4u;
+                for (int k = 0; k < nst; ++k) {
+                    const int slot = k % SEL_NSTG;
+                    if (k >= SEL_NSTG)   // the walkers are done with the slot's last stage
+                        mbar_wait_sleep(smem_u32(&s_empty[slot]), uint32_t((k / SEL_NSTG - 1) & 1), &s_abort,
+                                        status, ADJ_SEL_PRODUCER_SLEEP_NS);
+                    const uint32_t bar = smem_u32(&s_full[slot]);
+                    float *dst = sH + slot * STG;
+                    if (k < ngroups) {
+                        const int hi = rows - G * k, lo = hi - G > 0 ? hi - G : 0, n = hi - lo;
+                        mbar_arrive_expect_tx(bar, uint32_t(n) * rowb * (TRUNC ? 2u : 1u));
+                        for (int j = 0; j < n; ++j)
+                            bulk_g2s(smem_u32(dst + j * RF), h + ((row0 + lo + j) * P + p0) * NS, rowb, bar);
+                        if (TRUNC)
+                            for (int j = 0; j < n; ++j) {
+                                const int64_t t = c0 + lo + j, m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
+                                bulk_g2s(smem_u32(dst + (G + j) * RF), R + ((b * T + m) * P + p0) * NS, rowb, bar);
+                            }
+                    } else {
+                        mbar_arrive_expect_tx(bar, rowb);
+                        bulk_g2s(smem_u32(dst), h + ((row0 - 1) * P + p0) * NS, rowb, bar);
+                    }
+                }
+            }
+            return;
+        }
+    }
+
+    const Geo<NS> g(slice, P);
+    const int pp = g.act ? g.p : 0;   // lanes past P walk on zeros (the lane sums need them)
+    float A2[SEL_NT], mu[SEL_NT], qv[SEL_NT], abn[SEL_NT], dA[SEL_NT], hc[SEL_NT];
     const int64_t ai = ((b * nchunks + c) * P + pp) * NS + g.n0;
-    const float bd = b_dt[pp];
-    // Abar of the token after the chunk (0 past the sequence end)
-    float dtn = 0.f;
     const bool has_next = c0 + rows < T;
-    if (has_next) dtn = softplus_f(z[(row0 + rows) * ZW + pp] + bd);
+    const float dtn = has_next ? softplus_f(z[(row0 + rows) * ZW + pp] + b_dt[pp]) : 0.f;
 #pragma unroll
     for (int k = 0; k < SEL_NT; ++k) {
         A2[k] = A[pp * NS + g.n0 + k] * LOG2E;
-        abn[k] = has_next ? exp2f(dtn * A2[k]) : 0.f;
-        mu[k] = MODE == 1 && g.act ? aggY[ai + k] : 0.f;
-        q[k] = MODE == 1 && g.act ? aggX[ai + k] : 1.f;
+        abn[k] = has_next ? ex2(dtn * A2[k]) : 0.f;   // Abar of the token after the chunk
+        mu[k] = 0.f;
+        qv[k] = 1.f;
         dA[k] = 0.f;
+        hc[k] = 0.f;
     }
-    if (MODE == 1) {
-        if (g.act) ld8(h + ((row0 + rows - 1) * P + pp) * NS + g.n0, hc);
-        else
-#pragma unroll
-            for (int k = 0; k < SEL_NT; ++k) hc[k] = 0.f;
+    if (MODE == 1 && g.act) {
+        ld8g(aggY + ai, mu);
+        if (TRUNC) ld8g(aggX + ai, qv);
     }
     const bool next_block = TRUNC && (c0 / W + 1) * W < T;
-    for (int r = int(rows) - 1; r >= 0; --r) {
-        const int64_t t = c0 + r, row = row0 + r;
-        const float gv = g.act ? gy[row * P + pp] : 0.f;
-        const float zr = z[row * ZW + pp] + bd;
-        const float dt = softplus_f(zr);
-        float ab[SEL_NT];
+    const int off = g.q * NS + g.n0;
+
+    // flush the warp sums of the tokens [lo_s, hi_s) of the last sub-chunk to bc
+    auto flush = [&](int lo_s, int hi_s) {
+        for (int e = threadIdx.x; e < SC * 32; e += SEL_THREADS) {
+            const int j = e / 32, l = e % 32;
+            if (j >= hi_s - lo_s || (LP == 1 && (l & 1))) continue;
+            float acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < SEL_NT; ++k) {
-            mu[k] = fmaf(abn[k], mu[k], gv * sC[r][g.n0 + k]);
-            if (MODE == 0 || TRUNC) q[k] *= abn[k];   // MODE 0: the aggregate's product
-            ab[k] = exp2f(dt * A2[k]);
+            for (int w8 = 0; w8 < SEL_THREADS / 32; ++w8) acc += sW[(w8 * SC + j) * 32 + l];
+            const int vi = tsum16_index(l), which = vi >> 3;
+            const int n = (LP == 2 ? (l & 1) : 0) * SEL_NT + (vi & 7);
+            const int64_t trow = row0 + (hi_s - 1 - j);
+            bc[(trow * nslices + slice) * (2 * NS) + which * NS + n] = acc;
         }
-        if (MODE == 1) {
-            float mw[SEL_NT];
-#pragma unroll
-            for (int k = 0; k < SEL_NT; ++k) mw[k] = mu[k];
-            if (TRUNC && next_block && t % W != 0 && g.act) {
-                const int64_t m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
-                float rv[SEL_NT];
-                ld8(R + ((b * T + m) * P + pp) * NS + g.n0, rv);
-#pragma unroll
-                for (int k = 0; k < SEL_NT; ++k) mw[k] = fmaf(q[k], rv[k], mw[k]);
+    };
+
+    int slo = rows, shi = rows;   // the staged sub-chunk [slo, shi)
+    StageRegs<NS> R0;             // MODE 0: the next sub-chunk's inputs
+    for (int gi = 0; gi < ngroups; ++gi) {
+        const int hi = rows - G * gi, lo = hi - G > 0 ? hi - G : 0;
+        if (hi == slo || gi == 0) {   // a new sub-chunk of the per-token inputs
+            walkers_sync();
+            if (MODE == 1 && gi > 0) {
+                flush(slo, shi);
+                walkers_sync();
             }
-            // h_{t-1}
-            float hp[SEL_NT];
-            if (t > 0 && g.act) ld8(h + ((row - 1) * P + pp) * NS + g.n0, hp);
-            else
-#pragma unroll
-                for (int k = 0; k < SEL_NT; ++k) hp[k] = 0.f;
-            const float xv = g.act ? ldx(x + row * P + pp) : 0.f;
-            float ddt = 0.f, v[2 * SEL_NT];
+            shi = hi;
+            slo = hi - SC > 0 ? hi - SC : 0;
+            if (MODE == 0) {   // registers to spare: the next sub-chunk loads while this one is walked
+                if (gi == 0) stage_load<NS, TX, false, true>(R0, z, x, gy, b_dt, P, ZW, row0, slo, shi - slo, p0);
+                stage_store<NS, false, true>(sg, R0, shi - slo, p0, P);
+                if (slo > 0) {
+                    const int nlo = slo - SC > 0 ? slo - SC : 0;
+                    stage_load<NS, TX, false, true>(R0, z, x, gy, b_dt, P, ZW, row0, nlo, slo - nlo, p0);
+                }
+            } else {
+                stage_sub<NS, TX, true, true>(sg, z, x, gy, b_dt, P, ZW, row0, slo, shi - slo, p0);
+            }
+            walkers_sync();
+        }
+        const float *stg = sH + (gi % SEL_NSTG) * STG;
+        if (MODE == 1) {
+            mbar_wait(smem_u32(&s_full[gi % SEL_NSTG]), uint32_t((gi / SEL_NSTG) & 1), &s_abort, status);
+            if (gi == 0 && g.act) ld8s(stg + (hi - 1 - lo) * RF + off, hc);   // h of the chunk's last token
+            if (gi + 1 < nst)
+                mbar_wait(smem_u32(&s_full[(gi + 1) % SEL_NSTG]), uint32_t(((gi + 1) / SEL_NSTG) & 1), &s_abort,
+                          status);
+        }
+        for (int r = hi - 1; r >= lo; --r) {
+            const int rr = r - slo;
+            const float gv = sg.g[rr * PC + g.q], dt = sg.dt[rr * PC + g.q];
+            float Cv[SEL_NT], ab[SEL_NT];
+            ld8s(sg.C + rr * NS + g.n0, Cv);
 #pragma unroll
             for (int k = 0; k < SEL_NT; ++k) {
-                const float aah = ab[k] * hp[k];
-                ddt = fmaf(mw[k], fmaf(A2[k], aah * (1.f / LOG2E), sB[r][g.n0 + k] * xv), ddt);
-                dA[k] = fmaf(mw[k] * dt, aah, dA[k]);
-                v[k] = mw[k] * dt * xv;          // dB_t,n share
-                v[SEL_NT + k] = gv * hc[k];      // dC_t,n share
-                hc[k] = hp[k];
+                mu[k] = fmaf(abn[k], mu[k], gv * Cv[k]);
+                if (MODE == 0 || TRUNC) qv[k] *= abn[k];
+                ab[k] = ex2(dt * A2[k]);
             }
-            if (LP == 2) ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
-            if (g.act && g.n0 == 0) {
-                const float val = ddt * sigmoid_f(zr);
-                if constexpr (sizeof(TD) == 2) dz[row * ZW + pp] = __float2bfloat16_rn(val);
-                else dz[row * ZW + pp] = val;
-            }
-            // per-token sums over the CTA's channels: warp butterfly, then the 8 warps in
-            // order, TB tokens a batch
-            const float wsum = warp_tsum16<LP>(v, lane);
-            const int slot = r % TB;
-            sW[wp][slot][lane] = wsum;
-            if (slot == 0 || r == 0) {
-                __syncthreads();
-                const int nb = TB - slot;   // tokens of this batch: rows r .. r + nb - 1 ... clipped
-                for (int e = threadIdx.x; e < TB * 32; e += SEL_THREADS) {
-                    const int s2 = e / 32, l = e % 32;
-                    if (s2 < slot || s2 >= slot + nb || r + (s2 - slot) >= rows) continue;
-                    float acc = 0.f;
+            if (MODE == 1) {
+                // h_{r-1}: the row below in this stage, the top row of the next stage, or zero
+                float hp[SEL_NT], Bv[SEL_NT], v[2 * SEL_NT];
 #pragma unroll
-                    for (int w8 = 0; w8 < SEL_THREADS / 32; ++w8) acc += sW[w8][s2][l];
-                    // lane l's value index: n-block (LP == 2: lane bit 0) and tsum index
-                    const int vi = tsum_index(l);
-                    const int nblk = LP == 2 ? (l & 1) : 0;
-                    const int which = vi >> 3, n = nblk * SEL_NT + (vi & 7);
-                    if (LP == 1 && (l & 1)) continue;   // duplicate of lane l - 1
-                    const int64_t trow = row0 + r + (s2 - slot);
-                    bc[(trow * nslices + slice) * (2 * NS) + which * NS + n] = acc;
+                for (int k = 0; k < SEL_NT; ++k) hp[k] = 0.f;
+                if (g.act) {
+                    if (r > lo) ld8s(stg + (r - 1 - lo) * RF + off, hp);
+                    else if (gi + 1 < nst) {
+                        const int lo2 = lo - G > 0 ? lo - G : 0;
+                        const int top = gi + 1 < ngroups ? lo - 1 - lo2 : 0;
+                        ld8s(sH + ((gi + 1) % SEL_NSTG) * STG + top * RF + off, hp);
+                    }
                 }
-                __syncthreads();
-            }
-        }
+                float mw[SEL_NT];   // the window sum mu^W of this token (the scan keeps mu)
 #pragma unroll
-        for (int k = 0; k < SEL_NT; ++k) abn[k] = ab[k];
+                for (int k = 0; k < SEL_NT; ++k) mw[k] = mu[k];
+                if (TRUNC && next_block && (c0 + r) % W != 0 && g.act) {
+                    float rv[SEL_NT];
+                    ld8s(stg + (G + r - lo) * RF + off, rv);
+#pragma unroll
+                    for (int k = 0; k < SEL_NT; ++k) mw[k] = fmaf(qv[k], rv[k], mu[k]);
+                }
+                ld8s(sg.B + rr * NS + g.n0, Bv);
+                const float xv = sg.x[rr * PC + g.q], dtx = dt * xv;
+                float dda = 0.f, ddb = 0.f;
+#pragma unroll
+                for (int k = 0; k < SEL_NT; ++k) {
+                    const float ma = mw[k] * (ab[k] * hp[k]);
+                    dda = fmaf(A2[k], ma, dda);
+                    ddb = fmaf(mw[k], Bv[k], ddb);
+                    dA[k] = fmaf(dt, ma, dA[k]);
+                    v[k] = mw[k] * dtx;             // dB_t,n share
+                    v[SEL_NT + k] = gv * hc[k];     // dC_t,n share
+                    hc[k] = hp[k];
+                }
+                const float ddt = chan_sum<LP>(fmaf(dda, 1.f / LOG2E, ddb * xv));
+                if (g.act && g.n0 == 0) {
+                    const float val = ddt * sg.sig[rr * PC + g.q];   // through the softplus
+                    if constexpr (sizeof(TD) == 2) dz[(row0 + r) * ZW + pp] = __float2bfloat16_rn(val);
+                    else dz[(row0 + r) * ZW + pp] = val;
+                }
+                sW[(wp * SC + (shi - 1 - r)) * 32 + lane] = warp_tsum16<LP>(v, lane);
+            }
+#pragma unroll
+            for (int k = 0; k < SEL_NT; ++k) abn[k] = ab[k];
+        }
+        if (MODE == 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s_empty[gi % SEL_NSTG]));
+        }
+    }
+    if (MODE == 1) {
+        walkers_sync();
+        flush(slo, shi);
     }
     if (!g.act) return;
     if (MODE == 0) {
-        st8(aggX + ai, q);
-        st8(aggY + ai, mu);
+        st8v(aggX + ai, qv);
+        st8v(aggY + ai, mu);
     } else {
-        st8(dAp + ((b * nchunks + c) * P + g.p) * NS + g.n0, dA);
+        st8v(dAp + ((b * nchunks + c) * P + g.p) * NS + g.n0, dA);
     }
 }
 
@@ -480,7 +733,7 @@ static cudaError_t sel_fwd_t(const float *z, const void *x, const float *b_dt, c
     const int TT = sel_chunk(T, 0);
     const int64_t nchunks = (T + TT - 1) / TT;
     const dim3 grid = sel_grid(B, nchunks, P, NS);
-    const size_t smem = size_t(2) * TT * NS * 4;
+    const size_t smem = stage_floats<NS>() * 4;
     const TX *xt = static_cast<const TX *>(x);
     cudaError_t e;
     if ((e = smem_attr(k_sel_fwd<NS, TX, 0>, smem)) != cudaSuccess) return e;
@@ -504,7 +757,7 @@ cudaError_t launch_sel_fwd(const float *z, const void *x, bool x_bf16, const flo
 template <int NS, typename TX, typename TD>
 static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, const float *h, const float *b_dt,
                              const float *A, void *dz, float *dA, const SelBwdWs &w, int64_t B, int64_t T, int P,
-                             int64_t W, cudaStream_t st) {
+                             int64_t W, unsigned *status, cudaStream_t st) {
     const bool trunc = W > 0 && W < T;
     const int TT = sel_chunk(T, trunc ? W : 0);
     const int64_t nchunks = (T + TT - 1) / TT, Wk = trunc ? W : T;
@@ -516,23 +769,29 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
     TD *dzt = static_cast<TD *>(dz);
     cudaError_t e;
     if (trunc) {
-        const size_t sm1 = size_t(TT) * NS * 4;
+        const size_t sm1 = stage_floats<NS>() * 4;
         if ((e = smem_attr(k_sel_win<NS, 0>, sm1)) != cudaSuccess) return e;
         if ((e = smem_attr(k_sel_win<NS, 1>, sm1)) != cudaSuccess) return e;
         k_sel_win<NS, 0><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk);
         k_sel_carry<2><<<cgrid, 256, 0, st>>>(w.winX, w.winY, B, int64_t(P) * NS, nchunks, T, TT, Wk);
         k_sel_win<NS, 1><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk);
     }
-    const size_t sm = size_t(2) * TT * NS * 4 + size_t(SEL_THREADS / 32) * 16 * 32 * 4;
+    // MODE 0: the staged inputs; MODE 1: also the warp sums and the ring of row stages
+    const size_t sm0 = stage_floats<NS>() * 4;
+    const size_t sm_ws = size_t(SEL_THREADS / 32) * Geo<NS>::SC * 32 * 4;
+    const size_t row_seg = size_t(Geo<NS>::PC) * NS * 4;
 #define ADJ_SEL_BWD(TR)                                                                                            \
     do {                                                                                                           \
-        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 0, TR>, sm)) != cudaSuccess) return e;                            \
-        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 1, TR>, sm)) != cudaSuccess) return e;                            \
-        k_sel_bwd<NS, TX, TD, 0, TR><<<grid, SEL_THREADS, sm, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY,    \
-                                                                    dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk); \
+        const size_t sm1 = sm0 + sm_ws + size_t(SEL_NSTG) * sel_group<TR>() * row_seg * (TR ? 2 : 1);              \
+        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 0, TR>, sm0)) != cudaSuccess) return e;                           \
+        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 1, TR>, sm1)) != cudaSuccess) return e;                           \
+        k_sel_bwd<NS, TX, TD, 0, TR><<<grid, SEL_THREADS, sm0, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY,   \
+                                                                     dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, \
+                                                                     status);                                      \
         k_sel_carry<1><<<cgrid, 256, 0, st>>>(w.aggX, w.aggY, B, int64_t(P) * NS, nchunks, T, TT, Wk);             \
-        k_sel_bwd<NS, TX, TD, 1, TR><<<grid, SEL_THREADS, sm, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY,    \
-                                                                    dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk); \
+        k_sel_bwd<NS, TX, TD, 1, TR><<<grid, SEL_BWD_THREADS, sm1, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX,       \
+                                                                         w.aggY, dzt, w.bc, w.dAp, T, P, TT,       \
+                                                                         nchunks, nsl, Wk, status);                \
     } while (0)
     if (trunc) ADJ_SEL_BWD(true);
     else ADJ_SEL_BWD(false);
@@ -546,15 +805,18 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
 
 cudaError_t launch_sel_bwd(const float *z, const void *x, bool x_bf16, const float *gy, const float *h,
                            const float *b_dt, const float *A, void *dz, bool d_bf16, float *dA, const SelBwdWs &w,
-                           int64_t B, int64_t T, int P, int NS, int64_t W, cudaStream_t st) {
+                           int64_t B, int64_t T, int P, int NS, int64_t W, unsigned *status, cudaStream_t st) {
 #define ADJ_SEL_B(NSV)                                                                                              \
     do {                                                                                                            \
         if (x_bf16) {                                                                                               \
-            if (d_bf16) return sel_bwd_t<NSV, __nv_bfloat16, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, st); \
-            return sel_bwd_t<NSV, __nv_bfloat16, float>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, st);          \
+            if (d_bf16)                                                                                             \
+                return sel_bwd_t<NSV, __nv_bfloat16, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W,    \
+                                                                    status, st);                                    \
+            return sel_bwd_t<NSV, __nv_bfloat16, float>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, status, st);  \
         }                                                                                                           \
-        if (d_bf16) return sel_bwd_t<NSV, float, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, st);   \
-        return sel_bwd_t<NSV, float, float>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, st);                       \
+        if (d_bf16)                                                                                                 \
+            return sel_bwd_t<NSV, float, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, status, st);   \
+        return sel_bwd_t<NSV, float, float>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, status, st);               \
     } while (0)
     if (NS == 16) ADJ_SEL_B(16);
     if (NS == 8) ADJ_SEL_B(8);

@@ -33,10 +33,11 @@ struct SelBwdWs {
 cudaError_t launch_sel_fwd(const float *z, const void *x, bool x_bf16, const float *b_dt, const float *A, float *h,
                            float *y, float *aggX, float *aggY, int64_t B, int64_t T, int P, int NS, cudaStream_t st);
 // dz [B,T,P+2NS] (d_bf16: bf16) and dA [P,NS] for the cotangent gy [B,T,P]; W <= 0 or
-// W >= T: full adjoint.
+// W >= T: full adjoint.  status: the workspace status word (a bounded wait for a bulk copy
+// that gave up records the timeout there).
 cudaError_t launch_sel_bwd(const float *z, const void *x, bool x_bf16, const float *gy, const float *h,
                            const float *b_dt, const float *A, void *dz, bool d_bf16, float *dA, const SelBwdWs &w,
-                           int64_t B, int64_t T, int P, int NS, int64_t W, cudaStream_t st);
+                           int64_t B, int64_t T, int P, int NS, int64_t W, unsigned *status, cudaStream_t st);
 // part[blk][p] = sum of dz[:, p] over row block blk (nblk contiguous blocks of the rows)
 cudaError_t launch_sel_colsum(const void *dz, bool d_bf16, int64_t rows, int P, int ld, int nblk, float *part,
                               cudaStream_t st);
