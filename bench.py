@@ -368,6 +368,29 @@ def cpu_baseline(K):
             "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
+SEL_CPU_T = 1024   # tokens of the selective workload's oracle sample
+
+
+def sel_cpu_baseline(key, window):
+    """The selective layer's fp64 oracle on the host cores (forward, loss, adjoint with the
+    window, parameter gradients) on the first SEL_CPU_T tokens of the workload, all cores."""
+    import numpy as np
+    import oracle
+    from oracle import selective
+    from adjoint_gradients_long_gb300 import synth
+    inp = synth.make_sel_inputs(key, T=SEL_CPU_T, B=1)
+    W = {k: np.asarray(inp[k], np.float64) for k in ("W_in", "b_dt", "A")}
+    used = oracle.threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    st = selective.forward(W, inp["xhat"])
+    _, gy = selective.loss_and_cotangent(st["y"], inp["target"])
+    selective.grad(W, st, gy, window)
+    dt = time.perf_counter() - t0
+    return {"value": SEL_CPU_T / dt, "unit": "tokens/s per layer", "cores": used, "kind": "oracle",
+            "sample": f"first {SEL_CPU_T} tokens of {key} (window {window if window else 'full'}: every pair "
+                      f"of the sample is inside it), aggregated fp64 mode, {used} threads ({dt:.1f} s)"}
+
+
 def run_reference(args, rank):
     """The reference arm: the fp64 oracle (this path has no other reference code), one
     step = one gradient step on a CPU_REF_T-token prefix of the headline workload."""
@@ -552,7 +575,7 @@ def context_line(key, window, dev, peaks, steps, warmup):
     return out
 
 
-def sel_context_line(key, window, dev, peaks, steps, warmup):
+def sel_context_line(key, window, dev, peaks, steps, warmup, cpu=False):
     """The general selective layer on one of its workloads: graph replay of one step
     (forward, loss, reverse, parameter gradients), L2 flushed before every step, median."""
     import torch
@@ -605,6 +628,8 @@ def sel_context_line(key, window, dev, peaks, steps, warmup):
            "value": w.B * w.T / (med * 1e-3), "unit": "tokens/s per layer", "ms_per_step": med,
            "ms_mean": sum(ms) / len(ms), "steps": steps, "gpu_launches_per_step": per,
            "device_status": lib.STATUS.get(status, status), "kernels": kern}
+    if cpu:
+        out["cpu_baseline"] = sel_cpu_baseline(key, window)
     del g, L, flush
     torch.cuda.empty_cache()
     return out
@@ -698,7 +723,8 @@ def run_ours(args, rank, world, local_rank):
         for k2, w2 in CONTEXT:
             others.append(context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3))))
         for k2, w2 in SEL_CONTEXT:
-            others.append(sel_context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3))))
+            others.append(sel_context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3)),
+                                           cpu=not args.no_cpu_baseline))
 
     if rank == 0:
         line = {

@@ -105,3 +105,16 @@ def test_clock_summary_reads_reasons():
     c = bench.summarize_clocks(lines)
     assert c["sm_mhz"] == 1950 and c["sm_max_mhz"] == 2070 and c["reasons"] == ["sw_power_cap"]
     assert c["samples"] == 2 and c["power_w_max"] == 1000.0
+
+
+def test_selective_kernel_table():
+    """The general selective layer: the forward scan reads z and xhat and writes h (P N
+    states a token) and y; the reverse scan reads z, xhat, gy and h and writes dz."""
+    P, N = 1024, 16
+    t = bench.sel_kernel_table(P, N, 2, 2)
+    zw = P + 2 * N
+    assert t["sel_fwd"]["bytes"] == 4 * zw + 2 * P + 4 * P * N + 4 * P
+    assert t["sel_bwd"]["bytes"] == 4 * zw + 2 * P + 4 * P + 4 * P * N + 2 * zw
+    assert t["sel_proj"]["flops"] == 2 * P * zw and t["sel_dW"]["flops"] == 2 * P * zw
+    # the state dominates: the scans move about 4 P N bytes a token
+    assert 4 * P * N / t["sel_bwd"]["bytes"] > 0.9
