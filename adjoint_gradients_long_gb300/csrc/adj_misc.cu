@@ -383,9 +383,51 @@ __global__ void __launch_bounds__(256) k_rms_norm_bwd(const float *__restrict__ 
     }
 }
 
+// The same with the row held in registers (NV float4 a lane, P = 128 NV): every byte of y
+// is read from HBM once and all of a row's loads are in flight together.
+template <bool XBF, int NV>
+__global__ void __launch_bounds__(256) k_rms_norm_reg(const float *__restrict__ y, void *__restrict__ xhat,
+                                                      float *__restrict__ r, int64_t rows, float eps) {
+    constexpr int P = 128 * NV;
+    const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float *yr = y + row * P;
+    float4 v[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = ld_stream4(yr + lane * 4 + j * 128);
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rr = sqrtf(ss / float(P) + eps), inv = 1.f / rr;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const float4 w = v[j] * f4(inv);
+        if (XBF) st4(static_cast<__nv_bfloat16 *>(xhat) + row * P + lane * 4 + j * 128, w);
+        else st4(static_cast<float *>(xhat) + row * P + lane * 4 + j * 128, w);
+    }
+    if (lane == 0) r[row] = rr;
+}
+
 cudaError_t launch_rms_norm(const float *y, void *xhat, bool xbf, float *r, int64_t rows, int P, float eps,
                             cudaStream_t st) {
     const unsigned grid = unsigned((rows + 7) / 8);
+#define ADJ_RMS_REG(NV)                                                                    \
+    do {                                                                                   \
+        if (xbf) k_rms_norm_reg<true, NV><<<grid, 256, 0, st>>>(y, xhat, r, rows, eps);    \
+        else k_rms_norm_reg<false, NV><<<grid, 256, 0, st>>>(y, xhat, r, rows, eps);       \
+        return cudaGetLastError();                                                         \
+    } while (0)
+    switch (P) {
+    case 256: ADJ_RMS_REG(2);
+    case 512: ADJ_RMS_REG(4);
+    case 1024: ADJ_RMS_REG(8);
+    case 2048: ADJ_RMS_REG(16);
+    default: break;
+    }
+#undef ADJ_RMS_REG
     if (xbf) k_rms_norm<true><<<grid, 256, 0, st>>>(y, xhat, r, rows, P, eps);
     else k_rms_norm<false><<<grid, 256, 0, st>>>(y, xhat, r, rows, P, eps);
     return cudaGetLastError();
