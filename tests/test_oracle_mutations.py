@@ -74,8 +74,8 @@ SEL_SRC = os.path.join(os.path.dirname(oracle.__file__), "sel_oracle.c")
 SEL_MUTATIONS = {
     "dropped_input_term": ("ddt[p] += vv * (A[p * N + n] * ab * hp + zr[P + n] * xr[p]);",
                            "ddt[p] += vv * (A[p * N + n] * ab * hp);"),
-    "decay_of_the_wrong_token": ("const double dti = softplus(z[ri * Z + p]);",
-                                 "const double dti = softplus(z[(ri > 0 ? ri - 1 : 0) * Z + p]);"),
+    "decay_of_the_wrong_token": ("const double *ab = Ab + ri * PN + p * N;",
+                                 "const double *ab = Ab + (ri > 0 ? ri - 1 : 0) * PN + p * N;"),
     "literal_product_short": ("for (int64_t j = i + 1; j <= t; ++j) {", "for (int64_t j = i + 1; j < t; ++j) {"),
     "no_softplus_slope": ("dz[r * Z + p] = ddt[r * P + p] * sigmoid(z[r * Z + p]);", "dz[r * Z + p] = ddt[r * P + p];"),
     "B_and_C_swapped": ("v[p * N + n] = gy[rt * P + p] * z[rt * Z + P + N + n] * prod;",
