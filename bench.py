@@ -238,10 +238,26 @@ PROFILE_OF = {
 }
 
 
-def source_hash():
-    """Hash of the library sources (csrc and the public header), as recorded in profiles/."""
+# The translation unit that holds each kernel kind; a summary's hash covers that file and
+# the shared headers, so a change elsewhere in the library leaves it fresh.
+KERNEL_TU = {
+    "input_grad": "adj_gemm_tc.cu", "proj_out": "adj_gemm_tc.cu", "param_dW_in": "adj_gemm_tc.cu",
+    "proj_in": "adj_gemm_tc.cu", "cot_proj": "adj_gemm_tc.cu", "param_dW_o": "adj_gemm_tc.cu",
+    "bwd_scan": "adj_scan.cu", "fwd_scan": "adj_scan.cu", "win_scan": "adj_scan.cu",
+    "rms_norm": "adj_misc.cu", "loss": "adj_misc.cu", "colsum": "adj_misc.cu",
+    "sel_fwd": "adj_sel.cu", "sel_bwd": "adj_sel.cu",
+}
+
+
+def source_hash(tu=None):
+    """Hash of library sources, as recorded in profiles/: one translation unit of csrc (tu)
+    with the shared headers (csrc/*.cuh and the public header), or every source (tu None)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "adjoint_gradients_long_gb300", "csrc", "*.cu*")))
+    csrc = os.path.join(ROOT, "adjoint_gradients_long_gb300", "csrc")
+    if tu is None:
+        files = sorted(glob.glob(os.path.join(csrc, "*.cu*")))
+    else:
+        files = [os.path.join(csrc, tu)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
     files.append(os.path.join(ROOT, "include", "adj.h"))
     for f in files:
         h.update(os.path.basename(f).encode())
@@ -269,7 +285,7 @@ def profiled_traffic(name, workload="ssm1_p128"):
             per_launch_scale = float(line.split(":", 1)[1].strip().split()[0])
     if tot <= 0:
         return None, state, False
-    return tot * per_launch_scale, state, state == source_hash()
+    return tot * per_launch_scale, state, state == source_hash(KERNEL_TU.get(name))
 
 
 def roofline_of(name, ent, peaks, split3):
@@ -706,7 +722,7 @@ def run_ours(args, rank, world, local_rank):
         roof["traffic_source"] = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum, "
                                   f"profiles/{PROFILE_OF[(key, dom)]} (sources {state})")
         if not fresh:
-            roof["traffic_stale"] = f"captured from sources {state}, current sources {source_hash()}"
+            roof["traffic_stale"] = f"captured from sources {state}, current sources {source_hash(KERNEL_TU.get(dom))}"
     roof["algo_per_launch"] = kern[dom].get("algo_flops_per_launch" if roof["bound"] == "tensor"
                                             else "algo_bytes_per_launch")
     roof["ms_per_launch"] = kern[dom]["ms_per_launch"]

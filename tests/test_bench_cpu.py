@@ -36,7 +36,7 @@ def test_profiled_traffic_is_read_plus_write_of_the_summary(key):
     # a summary names the library sources it was captured from; only a capture of the
     # current sources is fresh
     assert state is None or re.fullmatch(r"[0-9a-f]{16}", state), state
-    assert fresh == (state == bench.source_hash())
+    assert fresh == (state == bench.source_hash(bench.KERNEL_TU.get(key[1])))
 
 
 def test_unknown_kernel_has_no_traffic():
@@ -46,6 +46,10 @@ def test_unknown_kernel_has_no_traffic():
 def test_source_hash_is_stable():
     assert bench.source_hash() == bench.source_hash()
     assert re.fullmatch(r"[0-9a-f]{16}", bench.source_hash())
+    # a kernel's hash covers its own translation unit and the headers only
+    assert bench.source_hash("adj_scan.cu") != bench.source_hash("adj_gemm_tc.cu")
+    for name, tu in bench.KERNEL_TU.items():
+        assert os.path.exists(os.path.join(ROOT, "adjoint_gradients_long_gb300", "csrc", tu)), name
 
 
 def test_roofline_takes_the_closer_bound():
