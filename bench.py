@@ -22,6 +22,7 @@ import argparse
 import glob
 import hashlib
 import json
+import re
 import os
 import platform
 import statistics
@@ -239,7 +240,7 @@ PROFILE_OF = {
 
 
 # The translation unit that holds each kernel kind; a summary's hash covers that file and
-# the shared headers, so a change elsewhere in the library leaves it fresh.
+# the headers it includes, so a change elsewhere in the library leaves it fresh.
 KERNEL_TU = {
     "input_grad": "adj_gemm_tc.cu", "proj_out": "adj_gemm_tc.cu", "param_dW_in": "adj_gemm_tc.cu",
     "proj_in": "adj_gemm_tc.cu", "cot_proj": "adj_gemm_tc.cu", "param_dW_o": "adj_gemm_tc.cu",
@@ -249,16 +250,30 @@ KERNEL_TU = {
 }
 
 
+def _includes(path, seen):
+    """path and the local headers it includes, recursively (#include "...")."""
+    if path in seen or not os.path.exists(path):
+        return
+    seen.add(path)
+    for line in open(path, encoding="utf-8", errors="replace"):
+        m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+        if m:
+            _includes(os.path.normpath(os.path.join(os.path.dirname(path), m.group(1))), seen)
+
+
 def source_hash(tu=None):
     """Hash of library sources, as recorded in profiles/: one translation unit of csrc (tu)
-    with the shared headers (csrc/*.cuh and the public header), or every source (tu None)."""
+    with the library headers it includes, or every source and the public header (tu None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "adjoint_gradients_long_gb300", "csrc")
     if tu is None:
-        files = sorted(glob.glob(os.path.join(csrc, "*.cu*")))
+        files = sorted(glob.glob(os.path.join(csrc, "*.cu*"))) + [os.path.join(ROOT, "include", "adj.h")]
     else:
-        files = [os.path.join(csrc, tu)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")))
-    files.append(os.path.join(ROOT, "include", "adj.h"))
+        # the public header only declares the C entry points (no device code reads it), so a
+        # new or changed declaration there leaves every kernel's summary fresh
+        seen = set()
+        _includes(os.path.join(csrc, tu), seen)
+        files = sorted((f for f in seen if os.path.basename(f) != "adj.h"), key=os.path.basename)
     for f in files:
         h.update(os.path.basename(f).encode())
         h.update(open(f, "rb").read())
