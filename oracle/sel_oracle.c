@@ -18,8 +18,9 @@
  *   B_t,n    = z_t,P+n,   C_t,n = z_t,P+N+n     input-dependent input and output maps
  *   Abar_t,pn = exp(dt_t,p A_pn)                A: [P, N], the continuous-time decay (< 0)
  *   h_t,pn   = Abar_t,pn h_t-1,pn + dt_t,p B_t,n xhat_t,p,   h_-1 = 0
- *   y_t,p    = xhat_t,p + sum_n C_t,n h_t,pn    (residual identity, [AS] What carries the
- *                                                argument)
+ *   y_t,p    = xres_t,p + sum_n C_t,n h_t,pn    (residual identity, [AS] What carries the
+ *                                                argument; xres = y^{k-1}, the residual stream
+ *                                                entering the layer, xhat itself for a lone layer)
  *
  * In the pages' notation the state is the PN-vector h_t, A_t = diag(Abar_t) is diagonal,
  * B_t xhat_t = (dt_t,p B_t,n xhat_t,p)_pn, and C_t is the P x PN matrix with
@@ -42,6 +43,9 @@
  *   output t: dC_t,n  += sum_p gy_t,p h_t,pn
  *   then      dz_i = [ddt_i . sigmoid(z_i,0..P-1) | dB_i | dC_i],
  *             dW_in += xhat_i^T dz_i,  db_dt += dz_i,0..P-1
+ *   input path (for stacks, [AS] Core claim, Proposition 3):
+ *             dxhat_i,p = sum_j dz_i,j W_in[p,j] + dt_i,p sum_n v_pn B_i,n
+ *             (the projection, and xhat's own factor in the input term dt B xhat)
  *
  * Two evaluation modes, both summing every (t, i) pair in the window:
  *   literal:    every product prod_{j=i+1..t} Abar_j by explicit multiplication and every
@@ -61,10 +65,10 @@
 static double softplus(double z) { return z > 30.0 ? z : log1p(exp(z)); }
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
-/* Forward pass.  x [B,T,P], W_in [P, P+2N], b_dt [P], A [P,N].
+/* Forward pass.  x [B,T,P], xres [B,T,P] (NULL: x), W_in [P, P+2N], b_dt [P], A [P,N].
  * Writes z [B,T,P+2N] (with the bias), h [B,T,P,N], y [B,T,P]. */
-void sel_forward(int64_t B, int64_t T, int64_t P, int64_t N, const double *x, const double *W_in,
-                 const double *b_dt, const double *A, double *z, double *h, double *y)
+void sel_forward(int64_t B, int64_t T, int64_t P, int64_t N, const double *x, const double *xres,
+                 const double *W_in, const double *b_dt, const double *A, double *z, double *h, double *y)
 {
     const int64_t Z = P + 2 * N;
 #ifdef _OPENMP
@@ -82,10 +86,10 @@ void sel_forward(int64_t B, int64_t T, int64_t P, int64_t N, const double *x, co
     for (int64_t b = 0; b < B; ++b) {
         for (int64_t t = 0; t < T; ++t) {
             const int64_t r = b * T + t;
-            const double *zr = z + r * Z, *xr = x + r * P;
+            const double *zr = z + r * Z, *xr = x + r * P, *rr = (xres ? xres : x) + r * P;
             for (int64_t p = 0; p < P; ++p) {
                 const double dt = softplus(zr[p]);
-                double out = xr[p];
+                double out = rr[p];
                 for (int64_t n = 0; n < N; ++n) {
                     const double prev = t > 0 ? h[((r - 1) * P + p) * N + n] : 0.0;
                     const double hv = exp(dt * A[p * N + n]) * prev + dt * zr[P + n] * xr[p];
@@ -101,7 +105,7 @@ void sel_forward(int64_t B, int64_t T, int64_t P, int64_t N, const double *x, co
 /* The VJP of step i (row r = b T + i) for the seed v [P,N]: adds into ddt [P] and dB [N]
  * of that row, and into dA [P,N]. */
 static void vjp_step(int64_t P, int64_t N, const double *zr, const double *xr, const double *hprev,
-                     const double *A, const double *v, double *ddt, double *dB, double *dA)
+                     const double *A, const double *v, double *ddt, double *dB, double *dA, double *dx)
 {
     for (int64_t p = 0; p < P; ++p) {
         const double dt = softplus(zr[p]);
@@ -112,6 +116,7 @@ static void vjp_step(int64_t P, int64_t N, const double *zr, const double *xr, c
             ddt[p] += vv * (A[p * N + n] * ab * hp + zr[P + n] * xr[p]);
             dA[p * N + n] += vv * dt * ab * hp;
             dB[n] += vv * dt * xr[p];
+            if (dx) dx[p] += vv * dt * zr[P + n];
         }
     }
 }
@@ -146,12 +151,13 @@ static void param_from_dz(int64_t BT, int64_t P, int64_t N, const double *x, con
 static int64_t window_of(int64_t T, int64_t Tbar) { return (Tbar <= 0 || Tbar > T) ? T : Tbar; }
 
 /* Gradient of one layer.  z, h from sel_forward; gy [B,T,P].  mode 0: literal, 1:
- * aggregated.  Writes (zeroing first) dz [B,T,P+2N], dW_in [P,P+2N], db_dt [P], dA [P,N]
- * and, if mu is not NULL, mu [B,T,P,N] = sum over the window of v_{t,i}.  Returns the
- * number of (t, i) pairs summed per sequence. */
+ * aggregated.  Writes (zeroing first) dz [B,T,P+2N], dW_in [P,P+2N], db_dt [P], dA [P,N],
+ * if mu is not NULL mu [B,T,P,N] = sum over the window of v_{t,i}, and if dx is not NULL
+ * the input path's cotangent dx [B,T,P] (not the residual's).  Returns the number of
+ * (t, i) pairs summed per sequence. */
 int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int mode,
-                 const double *x, const double *A, const double *z, const double *h, const double *gy,
-                 double *dz, double *dW_in, double *db_dt, double *dA, double *mu)
+                 const double *x, const double *W_in, const double *A, const double *z, const double *h,
+                 const double *gy, double *dz, double *dW_in, double *db_dt, double *dA, double *mu, double *dx)
 {
     const int64_t Z = P + 2 * N, PN = P * N, W = window_of(T, Tbar);
     memset(dz, 0, sizeof(double) * (size_t)(B * T * Z));
@@ -159,6 +165,7 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
     memset(db_dt, 0, sizeof(double) * (size_t)P);
     memset(dA, 0, sizeof(double) * (size_t)PN);
     if (mu) memset(mu, 0, sizeof(double) * (size_t)(B * T * PN));
+    if (dx) memset(dx, 0, sizeof(double) * (size_t)(B * T * P));
     int64_t count = 0;
     for (int64_t t = 0; t < T; ++t) count += (t + 1 < W ? t + 1 : W);
 
@@ -184,7 +191,7 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
                             if (mu) mu[ri * PN + p * N + n] += v[p * N + n];
                         }
                     vjp_step(P, N, z + ri * Z, x + ri * P, i > 0 ? h + (ri - 1) * PN : NULL, A, v,
-                             ddt + ri * P, dz + ri * Z + P, dA);
+                             ddt + ri * P, dz + ri * Z + P, dA, dx ? dx + ri * P : NULL);
                 }
             }
         free(v);
@@ -230,7 +237,7 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
                 const int64_t ri = b * T + i;
                 vjp_out(P, N, gy + ri * P, h + ri * PN, dz + ri * Z + P + N);
                 vjp_step(P, N, z + ri * Z, x + ri * P, i > 0 ? h + (ri - 1) * PN : NULL, A, V + ri * PN,
-                         ddt + ri * P, dz + ri * Z + P, dA);
+                         ddt + ri * P, dz + ri * Z + P, dA, dx ? dx + ri * P : NULL);
             }
         if (mu) memcpy(mu, V, sizeof(double) * (size_t)(B * T * PN));
         free(V);
@@ -239,6 +246,17 @@ int64_t sel_grad(int64_t B, int64_t T, int64_t P, int64_t N, int64_t Tbar, int m
         for (int64_t p = 0; p < P; ++p) dz[r * Z + p] = ddt[r * P + p] * sigmoid(z[r * Z + p]);
     free(ddt);
     param_from_dz(B * T, P, N, x, dz, dW_in, db_dt);
+    if (dx) {   /* the projection's share: dz W_in^T */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+        for (int64_t r = 0; r < B * T; ++r)
+            for (int64_t p = 0; p < P; ++p) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < Z; ++j) acc += dz[r * Z + j] * W_in[p * Z + j];
+                dx[r * P + p] += acc;
+            }
+    }
     return count;
 }
 

@@ -85,6 +85,9 @@ SEL_MUTATIONS = {
     "window_off_by_one": ("int64_t lo = t - W + 1;", "int64_t lo = t - W;"),
     "h_i_for_h_im1": ("i > 0 ? h + (ri - 1) * PN : NULL", "h + ri * PN"),
     "bias_on_the_wrong_columns": ("zr[j] = acc + (j < P ? b_dt[j] : 0.0);", "zr[j] = acc + (j < N ? b_dt[j] : 0.0);"),
+    "dropped_direct_input_term": ("if (dx) dx[p] += vv * dt * zr[P + n];", ";"),
+    "residual_from_xhat": ("*rr = (xres ? xres : x) + r * P;", "*rr = x + r * P;"),
+    "projection_transposed": ("acc += dz[r * Z + j] * W_in[p * Z + j];", "acc += dz[r * Z + j] * W_in[(j % P) * Z + p];"),
 }
 
 
@@ -94,8 +97,12 @@ def sel_case():
     d = synth.make_sel_inputs("sel1_p16", T=18, B=2, P=4, N=3)
     W = {k: d[k].astype(np.float64) for k in ("W_in", "b_dt", "A")}
     W["b_dt"] = W["b_dt"] + 4.0
+    W2 = {k: synth.make_sel_inputs("sel1_p16", T=18, B=2, P=4, N=3, seed=99)[k].astype(np.float64)
+          for k in ("W_in", "b_dt", "A")}
+    W2["b_dt"] = W2["b_dt"] + 4.0
     x, tgt = d["xhat"].astype(np.float64), d["target"].astype(np.float64)
-    return W, x, tgt, sel_bptt.bptt_grad(W, x, tgt), sel_bptt.bptt_grad(W, x, tgt, 5)
+    return (W, x, tgt, sel_bptt.bptt_grad(W, x, tgt), sel_bptt.bptt_grad(W, x, tgt, 5), [W, W2],
+            sel_bptt.stack_bptt_grad([W, W2], x, tgt, 5))
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
@@ -108,7 +115,7 @@ def test_selective_mutation_is_caught(name, sel_case, tmp_path):
     path_c = tmp_path / "mut.c"
     path_c.write_text(src.replace(old, new))
     so = sel.build(force=True, src=str(path_c), out=str(tmp_path / "libmut.so"))
-    W, x, tgt, ref_full, ref5 = sel_case
+    W, x, tgt, ref_full, ref5, layers, ref_stack = sel_case
     sel.use_library(so)
     try:
         worst = 0.0
@@ -118,6 +125,11 @@ def test_selective_mutation_is_caught(name, sel_case, tmp_path):
                 g = sel.grad(W, st, st["y"] - tgt, Tbar, mode)
                 for k in ("W_in", "b_dt", "A"):
                     worst = max(worst, rel_fro(g["d" + k], ref["d" + k]))
+            # a 2-layer stack (the input gradient and the residual input) against its BPTT
+            res = sel.stack_grad(layers, x, tgt, 5, mode)
+            for kk in range(2):
+                for k in ("W_in", "b_dt", "A"):
+                    worst = max(worst, rel_fro(res["grads"][kk]["d" + k], ref_stack[kk]["d" + k]))
     finally:
         sel.use_library(None)
     assert worst > 1e-6, (name, worst)

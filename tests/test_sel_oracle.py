@@ -157,3 +157,49 @@ def test_sampled_rows_equal_the_whole_gradient(Tbar):
     got = sel.dz_rows(W, x, tgt, rows, Tbar)
     for s, (b, t) in enumerate(rows):
         assert rel(got[s], g["dz"][b, t]) < 1e-12, (b, t)
+
+
+# ---------------------------------------------------------------- residual stacks of selective layers
+def tiny_stack(K=3, T=16, B=2, P=4, N=3):
+    out = []
+    for k in range(K):
+        W, x, tgt = tiny(T=T, B=B, P=P, N=N, seed=11 + k)
+        out.append(W)
+    _, x, tgt = tiny(T=T, B=B, P=P, N=N, seed=7)
+    return out, x, tgt
+
+
+def test_input_gradient_is_bptt():
+    """A lone layer's input-path cotangent (the projection and the input term) against BPTT."""
+    W, x, tgt = tiny(T=18, B=2)
+    g, _, _ = oracle_grad(W, x, tgt)
+    ref = sel_bptt.bptt_grad(W, x, tgt)
+    assert rel(g["dxhat"], ref["dxhat"]) < 1e-11
+
+
+@pytest.mark.parametrize("Tbar", [None, 5])
+def test_stack_equals_bptt(Tbar):
+    layers, x, tgt = tiny_stack()
+    res = sel.stack_grad(layers, x, tgt, Tbar)
+    ref = sel_bptt.stack_bptt_grad(layers, x, tgt, Tbar)
+    for k in range(len(layers)):
+        for nm in ("W_in", "b_dt", "A"):
+            assert rel(res["grads"][k]["d" + nm], ref[k]["d" + nm]) < 1e-10, (k, nm, Tbar)
+
+
+def test_stack_complex_step():
+    """Every layer's parameters of a 2-layer stack against the complex step on the loss."""
+    layers, x, tgt = tiny_stack(K=2, T=10, B=1, P=3, N=2)
+    res = sel.stack_grad(layers, x, tgt)
+    for k in range(2):
+        for nm in ("W_in", "b_dt", "A"):
+            cs = sel_bptt.stack_complex_step_grad(layers, x, tgt, k, nm)
+            assert rel(res["grads"][k]["d" + nm], cs) < 1e-9, (k, nm)
+
+
+def test_stack_of_one_is_the_layer():
+    W, x, tgt = tiny(T=12, B=2)
+    res = sel.stack_grad([W], x, tgt, 4)
+    g, _, _ = oracle_grad(W, x, tgt, 4)
+    for k in ("dW_in", "db_dt", "dA", "dz"):
+        assert rel(res["grads"][0][k], g[k]) < 1e-15, k
