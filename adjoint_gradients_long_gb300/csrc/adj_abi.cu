@@ -143,10 +143,11 @@ Layout layout(const adj_dims *d, int op, int64_t Tbar) {
         L.part1 = off; off += agg;
         break;
     }
-    case ADJ_OP_SEL_PARAM: {    // dW_in split partials, db_dt block partials
+    case ADJ_OP_SEL_PARAM: {    // dW_in split partials, db_dt block partials; fp32: W_in's split
         const int64_t zw = d->P + 2 * int64_t(d->N);
         L.part0 = off; off += al256(size_t(gemm_splits(d->P, zw, d->B * d->T)) * d->P * zw * 4);
         L.part1 = off; off += al256(size_t(colsum_blocks(d)) * d->P * 4);
+        L.wsplit = off; off += wsplit ? al256(size_t(d->P) * zw * 4) : 0;
         break;
     }
     default:
@@ -500,11 +501,17 @@ adj_status adj_rms_norm_bwd(const adj_dims *dims, const float *y, const float *r
 }
 
 // ---------------------------------------------------------------- the general selective layer
-adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, float *z, float *h, float *y,
-                       void *ws, size_t ws_bytes, void *stream) {
+size_t adj_sel_rowdot_cols(const adj_dims *dims) {
+    if (check_sel_dims(dims) != ADJ_OK) return 0;
+    return size_t(sel_slices(dims->P, dims->N)) + 1;
+}
+
+adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const float *xres, float *z,
+                       float *h, float *y, void *ws, size_t ws_bytes, void *stream) {
     ADJ_TRY(check_sel_dims(dims));
     if (!w) return ADJ_EINVAL;
     ADJ_TRY(check_ptrs({w->W_in, w->b_dt, w->A, xhat, z, h, y}));
+    ADJ_TRY(check_opt({xres}));
     Layout L;
     ADJ_TRY(check_ws(dims, ADJ_OP_SEL_FWD, 0, ws, ws_bytes, &L));
     const int64_t B = dims->B, T = dims->T, BT = B * T;
@@ -525,17 +532,19 @@ adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const voi
         ADJ_CUDA(launch_gemm_tc(BT, zw, P, op1(xhat, P, 1, xbf), Win, e, 1, !xbf, status_word(ws), st));
     }
     ProfScope ps(K_SEL_FWD, st, 3);
-    ADJ_CUDA(launch_sel_fwd(z, xhat, xbf, w->b_dt, w->A, h, y, reinterpret_cast<float *>(at(ws, L.buf0)),
+    ADJ_CUDA(launch_sel_fwd(z, xhat, xbf, w->b_dt, w->A, h, y, xres, reinterpret_cast<float *>(at(ws, L.buf0)),
                             reinterpret_cast<float *>(at(ws, L.buf1)), B, T, P, N, st));
     return ADJ_OK;
 }
 
 adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const float *z,
-                       const float *h, const float *gy, int64_t Tbar, void *dz, float *dA, void *ws, size_t ws_bytes,
-                       void *stream) {
+                       const float *h, const float *gy, int64_t Tbar, void *dz, float *dA, const float *r, float *gadd,
+                       float *rowdot, void *ws, size_t ws_bytes, void *stream) {
     ADJ_TRY(check_sel_dims(dims));
     if (!w) return ADJ_EINVAL;
     ADJ_TRY(check_ptrs({w->b_dt, w->A, xhat, z, h, gy, dz, dA}));
+    ADJ_TRY(check_opt({r, gadd, rowdot}));
+    if ((r != nullptr) != (gadd != nullptr) || (r != nullptr) != (rowdot != nullptr)) return ADJ_EINVAL;
     if (!sel_window_ok(dims->T, Tbar)) return ADJ_EINVAL;
     Layout L;
     ADJ_TRY(check_ws(dims, ADJ_OP_SEL_BWD, Tbar, ws, ws_bytes, &L));
@@ -557,15 +566,26 @@ adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const voi
     sw.bc = reinterpret_cast<float *>(at(ws, L.part0));
     sw.dAp = reinterpret_cast<float *>(at(ws, L.part1));
     ProfScope ps(K_SEL_BWD, st, tr ? 8 : 5);
+    SelInp inp;
+    inp.r = r;
+    inp.gadd = gadd;
+    inp.rowdot = rowdot;
     ADJ_CUDA(launch_sel_bwd(z, xhat, dims->x_dtype == ADJ_BF16, gy, h, w->b_dt, w->A, dz, dims->d_dtype == ADJ_BF16, dA,
-                            sw, B, T, P, N, tr ? Tbar : 0, status_word(ws), st));
+                            sw, inp, B, T, P, N, tr ? Tbar : 0, status_word(ws), st));
     return ADJ_OK;
 }
 
-adj_status adj_sel_param_grad(const adj_dims *dims, const void *xhat, const void *dz, float *dW_in, float *db_dt,
-                              int accumulate, void *ws, size_t ws_bytes, void *stream) {
+adj_status adj_sel_param_grad(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const void *dz,
+                              float *dW_in, float *db_dt, const float *r, const float *gadd, const float *rowdot,
+                              float *gy_prev, int accumulate, void *ws, size_t ws_bytes, void *stream) {
     ADJ_TRY(check_sel_dims(dims));
     ADJ_TRY(check_ptrs({xhat, dz, dW_in, db_dt}));
+    ADJ_TRY(check_opt({r, gadd, rowdot, gy_prev}));
+    const bool inpath = gy_prev != nullptr;
+    if ((r != nullptr) != inpath || (gadd != nullptr) != inpath || (rowdot != nullptr) != inpath) return ADJ_EINVAL;
+    if (inpath && (!w || !w->W_in)) return ADJ_EINVAL;
+    if (inpath) ADJ_TRY(check_ptrs({w->W_in}));
+    if (accumulate != 0 && accumulate != 1) return ADJ_EINVAL;
     Layout L;
     ADJ_TRY(check_ws(dims, ADJ_OP_SEL_PARAM, 0, ws, ws_bytes, &L));
     const int64_t BT = dims->B * dims->T;
@@ -597,8 +617,30 @@ adj_status adj_sel_param_grad(const adj_dims *dims, const void *xhat, const void
         ADJ_CUDA(launch_sel_colsum(dz, dbf, BT, P, int(zw), nb, part_b, st));
     }
     const RedSeg segs[2] = {{part, dW_in, int64_t(P) * zw / 4, su, 0, 0}, {part_b, db_dt, P / 4, nb, 0, 0}};
-    ProfScope ps(K_PARAM_REDUCE, st);
-    ADJ_CUDA(launch_reduce_partials(segs, 2, accumulate, st));
+    {
+        ProfScope ps(K_PARAM_REDUCE, st);
+        ADJ_CUDA(launch_reduce_partials(segs, 2, accumulate, st));
+    }
+    if (inpath) {
+        // the cotangent of the residual stream below: with dxhat = dz W_in^T + dxd,
+        // gy_prev = gy + (dxhat - xhat (xhat . dxhat) / P) / r, where gadd = gy + dxd / r
+        // and the row dots xhat . dxhat come summed over rowdot's slices
+        GemmEpilogue e3 = epi(Epi::StoreAdd);
+        e3.out0 = gy_prev;
+        e3.add = gadd;
+        e3.ld = P;
+        e3.nr = r;
+        e3.ndz = rowdot;
+        e3.nsl = sel_slices(P, N) + 1;
+        e3.nx = xhat;
+        e3.nx_bf16 = xbf;
+        e3.inv_P = 1.f / float(P);
+        cudaError_t err = cudaSuccess;
+        const GemmOperand Win = opw(w->W_in, int64_t(P) * zw, xbf, at(ws, L.wsplit), zw, 1, st, &err);
+        ADJ_CUDA(err);
+        ProfScope ps(K_SEL_DX, st);
+        ADJ_CUDA(launch_gemm_tc(BT, P, zw, op1(dz, zw, 1, dbf), Win, e3, 1, !xbf, status_word(ws), st));
+    }
     return ADJ_OK;
 }
 

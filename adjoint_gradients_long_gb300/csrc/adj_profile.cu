@@ -24,7 +24,7 @@ std::vector<cudaEvent_t> g_pool;
 const char *g_names[K_COUNT] = {"proj_in", "fwd_scan", "proj_out", "loss", "cot_proj", "win_scan",
                                 "bwd_scan", "param_dW_in", "param_dW_o", "param_reduce", "colsum",
                                 "input_grad", "rms_norm", "rms_norm_bwd", "weight_prep",
-                                "sel_proj", "sel_fwd", "sel_bwd", "sel_dW"};
+                                "sel_proj", "sel_fwd", "sel_bwd", "sel_dW", "sel_dx"};
 
 cudaEvent_t take() {
     if (!g_pool.empty()) {

@@ -24,6 +24,7 @@ enum KernelId {
     K_SEL_FWD,
     K_SEL_BWD,
     K_SEL_DW,
+    K_SEL_DX,
     K_COUNT
 };
 

@@ -101,10 +101,11 @@ __device__ __forceinline__ void st8s(float *p, const float (&v)[SEL_NT]) {   // 
 // the z columns of B_t and C_t [SC][NS] each.
 template <int NS>
 struct Stage {
-    float *dt, *x, *g, *sig, *B, *C;
+    float *dt, *x, *g, *sig, *B, *C, *zr;
 };
+// wz: also the raw z of the dt columns (the reverse pass's input path)
 template <int NS>
-__device__ __forceinline__ Stage<NS> stage_carve(float *base) {
+__device__ __forceinline__ Stage<NS> stage_carve(float *base, bool wz = false) {
     constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC;
     Stage<NS> s;
     s.dt = base;
@@ -113,11 +114,12 @@ __device__ __forceinline__ Stage<NS> stage_carve(float *base) {
     s.sig = s.g + SC * PC;
     s.B = s.sig + SC * PC;
     s.C = s.B + SC * NS;
+    s.zr = wz ? s.C + SC * NS : nullptr;
     return s;
 }
 template <int NS>
-constexpr size_t stage_floats() {
-    return size_t(Geo<NS>::SC) * Geo<NS>::PC * 4 + size_t(Geo<NS>::SC) * NS * 2;
+constexpr size_t stage_floats(bool wz = false) {
+    return size_t(Geo<NS>::SC) * Geo<NS>::PC * (wz ? 5 : 4) + size_t(Geo<NS>::SC) * NS * 2;
 }
 // The sub-chunk's per-token inputs as loaded into registers (a thread's share).
 template <int NS>
@@ -146,7 +148,7 @@ __device__ __forceinline__ void stage_load(StageRegs<NS> &R, const float *__rest
         R.bc[u] = (i < SC * 2 * NS && r < nr) ? z[(row0 + r0 + r) * ZW + P + j] : 0.f;
     }
 }
-template <int NS, bool WX, bool WG>
+template <int NS, bool WX, bool WG, bool WZ = false>
 __device__ __forceinline__ void stage_store(const Stage<NS> &s, const StageRegs<NS> &R, int nr, int p0, int P) {
     constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC, PER = StageRegs<NS>::PER;
 #pragma unroll
@@ -159,6 +161,7 @@ __device__ __forceinline__ void stage_store(const Stage<NS> &s, const StageRegs<
         if (WG) s.sig[i] = ok ? es / (1.f + es) : 0.f;
         if (WX) s.x[i] = R.x[u];
         if (WG) s.g[i] = R.g[u];
+        if (WZ) s.zr[i] = ok ? R.z[u] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < int(sizeof(R.bc) / sizeof(float)); ++u) {
@@ -169,24 +172,26 @@ __device__ __forceinline__ void stage_store(const Stage<NS> &s, const StageRegs<
         }
     }
 }
-template <int NS, typename TX, bool WX, bool WG>
+template <int NS, typename TX, bool WX, bool WG, bool WZ = false>
 __device__ __forceinline__ void stage_sub(const Stage<NS> &s, const float *__restrict__ z, const TX *__restrict__ x,
                                           const float *__restrict__ gy, const float *__restrict__ b_dt, int P,
                                           int ZW, int64_t row0, int r0, int nr, int p0) {
     StageRegs<NS> R;
     stage_load<NS, TX, WX, WG>(R, z, x, gy, b_dt, P, ZW, row0, r0, nr, p0);
-    stage_store<NS, WX, WG>(s, R, nr, p0, P);
+    stage_store<NS, WX, WG, WZ>(s, R, nr, p0, P);
 }
 
 // ------------------------------------------------------------------ forward state scan
 // MODE 0: aggregates (prod Abar, h at the chunk end from h = 0) -> aggX, aggY.
-// MODE 1: outputs from the carries in aggY: h [B,T,P,NS] and y [B,T,P].
+// MODE 1: outputs from the carries in aggY: h [B,T,P,NS] and y = xres + sum_n C h [B,T,P]
+// (xres null: xhat's values).
 template <int NS, typename TX, int MODE>
 __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict__ z, const TX *__restrict__ x,
                                                         const float *__restrict__ b_dt, const float *__restrict__ A,
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
-                                                        float *__restrict__ h, float *__restrict__ y, int64_t T, int P,
-                                                        int TT, int64_t nchunks) {
+                                                        float *__restrict__ h, float *__restrict__ y,
+                                                        const float *__restrict__ xres, int64_t T, int P, int TT,
+                                                        int64_t nchunks) {
     extern __shared__ __align__(16) float sm_sel[];
     constexpr int PC = Geo<NS>::PC, LP = Geo<NS>::LP, SC = Geo<NS>::SC;
     const Stage<NS> sg = stage_carve<NS>(sm_sel);
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict
                 const int64_t row = row0 + r0 + r;
                 if (g.act) st8s(h + (row * P + pp) * NS + g.n0, st);
                 yp = chan_sum<LP>(yp);
-                if (g.act && g.n0 == 0) y[row * P + pp] = xv + yp;
+                if (g.act && g.n0 == 0) y[row * P + pp] = (xres ? __ldcs(xres + row * P + pp) : xv) + yp;
             }
         }
     }
@@ -454,7 +459,13 @@ constexpr int sel_group() { return TRUNC ? 1 : 2; }   // tokens a stage
 // 256 + 32 threads: warp 8 copies the state rows (and R rows) into the stages: stage k
 // holds the rows of group k (tokens counted down from the chunk's top, G a group), one more
 // stage the row before the chunk; group k reads stages k and k + 1.
-template <int NS, typename TX, typename TD, int MODE, bool TRUNC>
+// INP (MODE 1, stacked layers): also the input path's share that does not go through the
+// projection, dxd = dt sum_n mu^W B (xhat's factor in the input term), written as
+// gadd = gy + dxd / r (r: the rms of the layer's input stream), and the CTA's partial row
+// dots xhat . dxhat = sum_p (dz_dt,p z_p + xhat_p dxd_p) -> rowdot [B*T, nslices + 1]
+// (the last slice is k_sel_bc_reduce's, for the dB and dC columns; together with dz z they
+// give xhat . (dz W_in^T) without the product, since z = xhat W_in).
+template <int NS, typename TX, typename TD, int MODE, bool TRUNC, bool INP = false>
 __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(const float *__restrict__ z, const TX *__restrict__ x,
                                                             const float *__restrict__ gy, const float *__restrict__ h,
                                                             const float *__restrict__ R, const float *__restrict__ b_dt,
@@ -462,7 +473,8 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
                                                             float *__restrict__ aggY, TD *__restrict__ dz,
                                                             float *__restrict__ bc, float *__restrict__ dAp, int64_t T,
                                                             int P, int TT, int64_t nchunks, int nslices, int64_t W,
-                                                            unsigned *status) {
+                                                            unsigned *status, const float *__restrict__ rin,
+                                                            float *__restrict__ gadd, float *__restrict__ rowdot) {
     extern __shared__ __align__(16) float sm_sel[];
     constexpr int PC = Geo<NS>::PC, LP = Geo<NS>::LP, SC = Geo<NS>::SC;
     constexpr int G = sel_group<TRUNC>();
@@ -470,8 +482,9 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
     constexpr int STG = G * RF * (TRUNC ? 2 : 1);          // floats a stage
     __shared__ uint64_t s_full[SEL_NSTG], s_empty[SEL_NSTG];
     __shared__ int s_abort;
-    const Stage<NS> sg = stage_carve<NS>(sm_sel);
-    float *sW = sm_sel + stage_floats<NS>();               // [8 warps][SC][32]
+    __shared__ float s_rd[SEL_THREADS / 32][16];           // INP: the warps' row-dot shares
+    const Stage<NS> sg = stage_carve<NS>(sm_sel, INP);
+    float *sW = sm_sel + stage_floats<NS>(INP);            // [8 warps][SC][32]
     float *sH = sW + (SEL_THREADS / 32) * SC * 32;         // [SEL_NSTG][STG]
     const int64_t c = blockIdx.x, b = blockIdx.z;
     const int slice = int(blockIdx.y);
@@ -558,6 +571,13 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
             const int64_t trow = row0 + (hi_s - 1 - j);
             bc[(trow * nslices + slice) * (2 * NS) + which * NS + n] = acc;
         }
+        if (INP)
+            for (int j = threadIdx.x; j < hi_s - lo_s; j += SEL_THREADS) {
+                float acc = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < SEL_THREADS / 32; ++w8) acc += s_rd[w8][j];
+                rowdot[(row0 + (hi_s - 1 - j)) * (nslices + 1) + slice] = acc;
+            }
     };
 
     int slo = rows, shi = rows;   // the staged sub-chunk [slo, shi)
@@ -580,7 +600,7 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
                     stage_load<NS, TX, false, true>(R0, z, x, gy, b_dt, P, ZW, row0, nlo, slo - nlo, p0);
                 }
             } else {
-                stage_sub<NS, TX, true, true>(sg, z, x, gy, b_dt, P, ZW, row0, slo, shi - slo, p0);
+                stage_sub<NS, TX, true, true, INP>(sg, z, x, gy, b_dt, P, ZW, row0, slo, shi - slo, p0);
             }
             walkers_sync();
         }
@@ -639,10 +659,28 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
                     hc[k] = hp[k];
                 }
                 const float ddt = chan_sum<LP>(fmaf(dda, 1.f / LOG2E, ddb * xv));
+                float dzs = 0.f;   // dz_dt as stored
                 if (g.act && g.n0 == 0) {
                     const float val = ddt * sg.sig[rr * PC + g.q];   // through the softplus
-                    if constexpr (sizeof(TD) == 2) dz[(row0 + r) * ZW + pp] = __float2bfloat16_rn(val);
-                    else dz[(row0 + r) * ZW + pp] = val;
+                    if constexpr (sizeof(TD) == 2) {
+                        const __nv_bfloat16 vb = __float2bfloat16_rn(val);
+                        dz[(row0 + r) * ZW + pp] = vb;
+                        dzs = __bfloat162float(vb);
+                    } else {
+                        dz[(row0 + r) * ZW + pp] = val;
+                        dzs = val;
+                    }
+                }
+                if (INP) {
+                    const float dxd = dt * chan_sum<LP>(ddb);
+                    float rd = 0.f;
+                    if (g.act && g.n0 == 0) {
+                        gadd[(row0 + r) * P + pp] = sg.g[rr * PC + g.q] + dxd / __ldg(rin + row0 + r);
+                        rd = fmaf(dzs, sg.zr[rr * PC + g.q], xv * dxd);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) rd += __shfl_xor_sync(0xffffffffu, rd, o);
+                    if (lane == 0) s_rd[wp][shi - 1 - r] = rd;
                 }
                 sW[(wp * SC + (shi - 1 - r)) * 32 + lane] = warp_tsum16<LP>(v, lane);
             }
@@ -667,18 +705,33 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
     }
 }
 
-// dz[:, P + j] = sum over slices of bc (j < 2 NS), in the dz storage type.
+// dz[:, P + j] = sum over slices of bc (j < 2 NS), in the dz storage type.  With rowdot
+// (stacked layers): the row's sum_j dz_P+j z_P+j (as stored) -> rowdot[r * (nslices + 1) + nslices];
+// a row's NS2 threads are adjacent lanes (NS2 = 16 or 32).
 template <typename TD>
 __global__ void k_sel_bc_reduce(const float *__restrict__ bc, TD *__restrict__ dz, int64_t rows, int P, int NS2,
-                                int nslices) {
+                                int nslices, const float *__restrict__ z, float *__restrict__ rowdot) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= rows * NS2) return;
+    const bool live = i < rows * NS2;
     const int64_t r = i / NS2;
     const int j = int(i % NS2);
-    float acc = 0.f;
-    for (int s = 0; s < nslices; ++s) acc += bc[(r * nslices + s) * NS2 + j];
-    if constexpr (sizeof(TD) == 2) dz[r * (P + NS2) + P + j] = __float2bfloat16_rn(acc);
-    else dz[r * (P + NS2) + P + j] = acc;
+    float sv = 0.f;
+    if (live) {
+        float acc = 0.f;
+        for (int s = 0; s < nslices; ++s) acc += bc[(r * nslices + s) * NS2 + j];
+        if constexpr (sizeof(TD) == 2) {
+            const __nv_bfloat16 vb = __float2bfloat16_rn(acc);
+            dz[r * (P + NS2) + P + j] = vb;
+            sv = __bfloat162float(vb);
+        } else {
+            dz[r * (P + NS2) + P + j] = acc;
+            sv = acc;
+        }
+    }
+    if (rowdot == nullptr) return;
+    float c = live ? sv * z[r * (P + NS2) + P + j] : 0.f;
+    for (int o = NS2 / 2; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o, NS2);
+    if (live && j == 0) rowdot[r * (nslices + 1) + nslices] = c;
 }
 
 // dA[j] = sum over parts (rows of dAp) in order.
@@ -729,7 +782,7 @@ static dim3 sel_grid(int64_t B, int64_t nchunks, int P, int NS) {
 
 template <int NS, typename TX>
 static cudaError_t sel_fwd_t(const float *z, const void *x, const float *b_dt, const float *A, float *h, float *y,
-                             float *aggX, float *aggY, int64_t B, int64_t T, int P, cudaStream_t st) {
+                             const float *xres, float *aggX, float *aggY, int64_t B, int64_t T, int P, cudaStream_t st) {
     const int TT = sel_chunk(T, 0);
     const int64_t nchunks = (T + TT - 1) / TT;
     const dim3 grid = sel_grid(B, nchunks, P, NS);
@@ -738,26 +791,29 @@ static cudaError_t sel_fwd_t(const float *z, const void *x, const float *b_dt, c
     cudaError_t e;
     if ((e = smem_attr(k_sel_fwd<NS, TX, 0>, smem)) != cudaSuccess) return e;
     if ((e = smem_attr(k_sel_fwd<NS, TX, 1>, smem)) != cudaSuccess) return e;
-    k_sel_fwd<NS, TX, 0><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, T, P, TT, nchunks);
+    k_sel_fwd<NS, TX, 0><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, xres, T, P, TT,
+                                                          nchunks);
     const int64_t n = B * int64_t(P) * NS;
     k_sel_carry<0><<<unsigned((n + 255) / 256), 256, 0, st>>>(aggX, aggY, B, int64_t(P) * NS, nchunks, T, TT, T);
-    k_sel_fwd<NS, TX, 1><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, T, P, TT, nchunks);
+    k_sel_fwd<NS, TX, 1><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, xres, T, P, TT,
+                                                          nchunks);
     return cudaGetLastError();
 }
 
 cudaError_t launch_sel_fwd(const float *z, const void *x, bool x_bf16, const float *b_dt, const float *A, float *h,
-                           float *y, float *aggX, float *aggY, int64_t B, int64_t T, int P, int NS, cudaStream_t st) {
-    if (NS == 16) return x_bf16 ? sel_fwd_t<16, __nv_bfloat16>(z, x, b_dt, A, h, y, aggX, aggY, B, T, P, st)
-                                : sel_fwd_t<16, float>(z, x, b_dt, A, h, y, aggX, aggY, B, T, P, st);
-    if (NS == 8) return x_bf16 ? sel_fwd_t<8, __nv_bfloat16>(z, x, b_dt, A, h, y, aggX, aggY, B, T, P, st)
-                               : sel_fwd_t<8, float>(z, x, b_dt, A, h, y, aggX, aggY, B, T, P, st);
+                           float *y, const float *xres, float *aggX, float *aggY, int64_t B, int64_t T, int P, int NS,
+                           cudaStream_t st) {
+    if (NS == 16) return x_bf16 ? sel_fwd_t<16, __nv_bfloat16>(z, x, b_dt, A, h, y, xres, aggX, aggY, B, T, P, st)
+                                : sel_fwd_t<16, float>(z, x, b_dt, A, h, y, xres, aggX, aggY, B, T, P, st);
+    if (NS == 8) return x_bf16 ? sel_fwd_t<8, __nv_bfloat16>(z, x, b_dt, A, h, y, xres, aggX, aggY, B, T, P, st)
+                               : sel_fwd_t<8, float>(z, x, b_dt, A, h, y, xres, aggX, aggY, B, T, P, st);
     return cudaErrorInvalidValue;
 }
 
 template <int NS, typename TX, typename TD>
 static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, const float *h, const float *b_dt,
-                             const float *A, void *dz, float *dA, const SelBwdWs &w, int64_t B, int64_t T, int P,
-                             int64_t W, unsigned *status, cudaStream_t st) {
+                             const float *A, void *dz, float *dA, const SelBwdWs &w, const SelInp &inp, int64_t B,
+                             int64_t T, int P, int64_t W, unsigned *status, cudaStream_t st) {
     const bool trunc = W > 0 && W < T;
     const int TT = sel_chunk(T, trunc ? W : 0);
     const int64_t nchunks = (T + TT - 1) / TT, Wk = trunc ? W : T;
@@ -776,28 +832,37 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
         k_sel_carry<2><<<cgrid, 256, 0, st>>>(w.winX, w.winY, B, int64_t(P) * NS, nchunks, T, TT, Wk);
         k_sel_win<NS, 1><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk);
     }
-    // MODE 0: the staged inputs; MODE 1: also the warp sums and the ring of row stages
+    // MODE 0: the staged inputs; MODE 1: also the warp sums and the ring of row stages (and,
+    // with the input path, the raw z of the dt columns)
+    const bool inpath = inp.gadd != nullptr;
     const size_t sm0 = stage_floats<NS>() * 4;
     const size_t sm_ws = size_t(SEL_THREADS / 32) * Geo<NS>::SC * 32 * 4;
     const size_t row_seg = size_t(Geo<NS>::PC) * NS * 4;
-#define ADJ_SEL_BWD(TR)                                                                                            \
+#define ADJ_SEL_BWD(TR, IN)                                                                                        \
     do {                                                                                                           \
-        const size_t sm1 = sm0 + sm_ws + size_t(SEL_NSTG) * sel_group<TR>() * row_seg * (TR ? 2 : 1);              \
+        const size_t sm1 = stage_floats<NS>(IN) * 4 + sm_ws +                                                      \
+                           size_t(SEL_NSTG) * sel_group<TR>() * row_seg * (TR ? 2 : 1);                            \
         if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 0, TR>, sm0)) != cudaSuccess) return e;                           \
-        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 1, TR>, sm1)) != cudaSuccess) return e;                           \
+        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 1, TR, IN>, sm1)) != cudaSuccess) return e;                       \
         k_sel_bwd<NS, TX, TD, 0, TR><<<grid, SEL_THREADS, sm0, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY,   \
                                                                      dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, \
-                                                                     status);                                      \
+                                                                     status, nullptr, nullptr, nullptr);           \
         k_sel_carry<1><<<cgrid, 256, 0, st>>>(w.aggX, w.aggY, B, int64_t(P) * NS, nchunks, T, TT, Wk);             \
-        k_sel_bwd<NS, TX, TD, 1, TR><<<grid, SEL_BWD_THREADS, sm1, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX,       \
-                                                                         w.aggY, dzt, w.bc, w.dAp, T, P, TT,       \
-                                                                         nchunks, nsl, Wk, status);                \
+        k_sel_bwd<NS, TX, TD, 1, TR, IN><<<grid, SEL_BWD_THREADS, sm1, st>>>(                                      \
+            z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY, dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, status,      \
+            inp.r, inp.gadd, inp.rowdot);                                                                          \
     } while (0)
-    if (trunc) ADJ_SEL_BWD(true);
-    else ADJ_SEL_BWD(false);
+    if (trunc) {
+        if (inpath) ADJ_SEL_BWD(true, true);
+        else ADJ_SEL_BWD(true, false);
+    } else {
+        if (inpath) ADJ_SEL_BWD(false, true);
+        else ADJ_SEL_BWD(false, false);
+    }
 #undef ADJ_SEL_BWD
     const int64_t nbc = B * T * 2 * NS;
-    k_sel_bc_reduce<TD><<<unsigned((nbc + 255) / 256), 256, 0, st>>>(w.bc, dzt, B * T, P, 2 * NS, nsl);
+    k_sel_bc_reduce<TD><<<unsigned((nbc + 255) / 256), 256, 0, st>>>(w.bc, dzt, B * T, P, 2 * NS, nsl,
+                                                                     inpath ? z : nullptr, inp.rowdot);
     k_sel_rows_sum<<<unsigned((int64_t(P) * NS + 255) / 256), 256, 0, st>>>(w.dAp, dA, B * nchunks,
                                                                           int64_t(P) * NS);
     return cudaGetLastError();
@@ -805,18 +870,21 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
 
 cudaError_t launch_sel_bwd(const float *z, const void *x, bool x_bf16, const float *gy, const float *h,
                            const float *b_dt, const float *A, void *dz, bool d_bf16, float *dA, const SelBwdWs &w,
-                           int64_t B, int64_t T, int P, int NS, int64_t W, unsigned *status, cudaStream_t st) {
+                           const SelInp &inp, int64_t B, int64_t T, int P, int NS, int64_t W, unsigned *status,
+                           cudaStream_t st) {
 #define ADJ_SEL_B(NSV)                                                                                              \
     do {                                                                                                            \
         if (x_bf16) {                                                                                               \
             if (d_bf16)                                                                                             \
-                return sel_bwd_t<NSV, __nv_bfloat16, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W,    \
-                                                                    status, st);                                    \
-            return sel_bwd_t<NSV, __nv_bfloat16, float>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, status, st);  \
+                return sel_bwd_t<NSV, __nv_bfloat16, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, inp, B, T, P,  \
+                                                                    W, status, st);                                 \
+            return sel_bwd_t<NSV, __nv_bfloat16, float>(z, x, gy, h, b_dt, A, dz, dA, w, inp, B, T, P, W, status,  \
+                                                        st);                                                        \
         }                                                                                                           \
         if (d_bf16)                                                                                                 \
-            return sel_bwd_t<NSV, float, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, status, st);   \
-        return sel_bwd_t<NSV, float, float>(z, x, gy, h, b_dt, A, dz, dA, w, B, T, P, W, status, st);               \
+            return sel_bwd_t<NSV, float, __nv_bfloat16>(z, x, gy, h, b_dt, A, dz, dA, w, inp, B, T, P, W, status,  \
+                                                        st);                                                        \
+        return sel_bwd_t<NSV, float, float>(z, x, gy, h, b_dt, A, dz, dA, w, inp, B, T, P, W, status, st);          \
     } while (0)
     if (NS == 16) ADJ_SEL_B(16);
     if (NS == 8) ADJ_SEL_B(8);

@@ -21,7 +21,7 @@ EXPORTS = ("adj_workspace_bytes", "adj_fwd_scan", "adj_loss_mse", "adj_bwd_full"
            "adj_param_grad", "adj_stream_status", "adj_status_str", "adj_launch_count", "adj_profile_enable",
            "adj_profile_reset", "adj_profile_kernels", "adj_profile_name", "adj_profile_read", "adj_rms_norm",
            "adj_rms_norm_bwd", "adj_selftest_waits", "adj_selftest_ws_bytes", "adj_sel_fwd", "adj_sel_bwd",
-           "adj_sel_param_grad")
+           "adj_sel_param_grad", "adj_sel_rowdot_cols")
 
 
 class AdjError(RuntimeError):
@@ -64,9 +64,11 @@ def load(path: str = LIB_PATH):
         lib.adj_bwd_trunc.argtypes = [_PD, _PW] + [_VP] * 10 + [_I64, _VP, _SZ, _VP]
         lib.adj_param_grad.argtypes = [_PD, _PW] + [_VP] * 15 + [ctypes.c_int, _VP, _SZ, _VP]
         lib.adj_rms_norm.argtypes = [_PD] + [_VP] * 4
-        lib.adj_sel_fwd.argtypes = [_PD, _PS] + [_VP] * 5 + [_SZ, _VP]
-        lib.adj_sel_bwd.argtypes = [_PD, _PS] + [_VP] * 4 + [_I64] + [_VP] * 3 + [_SZ, _VP]
-        lib.adj_sel_param_grad.argtypes = [_PD] + [_VP] * 4 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_sel_fwd.argtypes = [_PD, _PS] + [_VP] * 6 + [_SZ, _VP]
+        lib.adj_sel_bwd.argtypes = [_PD, _PS] + [_VP] * 4 + [_I64] + [_VP] * 6 + [_SZ, _VP]
+        lib.adj_sel_param_grad.argtypes = [_PD, _PS] + [_VP] * 8 + [ctypes.c_int, _VP, _SZ, _VP]
+        lib.adj_sel_rowdot_cols.argtypes = [_PD]
+        lib.adj_sel_rowdot_cols.restype = _SZ
         lib.adj_selftest_waits.argtypes = [_VP, _SZ, ctypes.c_int, _VP]
         lib.adj_selftest_waits.restype = ctypes.c_int
         lib.adj_selftest_ws_bytes.argtypes = []
@@ -206,17 +208,23 @@ def sel_weights(W_in, b_dt, A) -> SelWeights:
     return SelWeights(ptr(W_in), ptr(b_dt), ptr(A))
 
 
-def sel_fwd(d, w, xhat, z, h, y, ws, ws_bytes, stream=None):
-    _check(load().adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(z), ptr(h), ptr(y), ptr(ws), ws_bytes,
-                              _stream(stream)), "adj_sel_fwd")
+def sel_fwd(d, w, xhat, z, h, y, ws, ws_bytes, stream=None, xres=None):
+    _check(load().adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(xres), ptr(z), ptr(h), ptr(y),
+                              ptr(ws), ws_bytes, _stream(stream)), "adj_sel_fwd")
 
 
-def sel_bwd(d, w, xhat, z, h, gy, Tbar, dz, dA, ws, ws_bytes, stream=None):
+def sel_rowdot_cols(d) -> int:
+    return int(load().adj_sel_rowdot_cols(ctypes.byref(d)))
+
+
+def sel_bwd(d, w, xhat, z, h, gy, Tbar, dz, dA, ws, ws_bytes, stream=None, r=None, gadd=None, rowdot=None):
     _check(load().adj_sel_bwd(ctypes.byref(d), ctypes.byref(w), ptr(xhat), ptr(z), ptr(h), ptr(gy),
-                              0 if Tbar is None else int(Tbar), ptr(dz), ptr(dA), ptr(ws), ws_bytes, _stream(stream)),
-           "adj_sel_bwd")
+                              0 if Tbar is None else int(Tbar), ptr(dz), ptr(dA), ptr(r), ptr(gadd), ptr(rowdot),
+                              ptr(ws), ws_bytes, _stream(stream)), "adj_sel_bwd")
 
 
-def sel_param_grad(d, xhat, dz, dW_in, db_dt, accumulate, ws, ws_bytes, stream=None):
-    _check(load().adj_sel_param_grad(ctypes.byref(d), ptr(xhat), ptr(dz), ptr(dW_in), ptr(db_dt), int(accumulate),
-                                     ptr(ws), ws_bytes, _stream(stream)), "adj_sel_param_grad")
+def sel_param_grad(d, xhat, dz, dW_in, db_dt, accumulate, ws, ws_bytes, stream=None, w=None, r=None, gadd=None,
+                   rowdot=None, gy_prev=None):
+    _check(load().adj_sel_param_grad(ctypes.byref(d), None if w is None else ctypes.byref(w), ptr(xhat), ptr(dz),
+                                     ptr(dW_in), ptr(db_dt), ptr(r), ptr(gadd), ptr(rowdot), ptr(gy_prev),
+                                     int(accumulate), ptr(ws), ws_bytes, _stream(stream)), "adj_sel_param_grad")

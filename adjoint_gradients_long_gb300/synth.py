@@ -186,6 +186,12 @@ def make_sel_inputs(w, T: Optional[int] = None, B: Optional[int] = None, P: Opti
     seed = w.seed if seed is None else seed
     xhat = _tokens(seed, _S_XHAT, B, t0, t0 + T, P)
     target = _tokens(seed, _S_TARGET, B, t0, t0 + T, P)
+    if w.x_dtype == "bf16":
+        xhat = round_bf16(xhat)
+    return dict(xhat=xhat, target=target, **_sel_weights(seed, P, N, w.x_dtype), workload=w, T=T, B=B, P=P, N=N)
+
+
+def _sel_weights(seed: int, P: int, N: int, x_dtype: str) -> dict:
     W_dt = _rng(seed, _S_WDT).standard_normal((P, P), dtype=np.float32) * np.float32(0.5 / np.sqrt(P))
     W_B = _rng(seed, _S_WB).standard_normal((P, N), dtype=np.float32) * np.float32(1.0 / np.sqrt(P))
     W_C = _rng(seed, _S_WC).standard_normal((P, N), dtype=np.float32) * np.float32(1.0 / np.sqrt(P))
@@ -193,6 +199,21 @@ def make_sel_inputs(w, T: Optional[int] = None, B: Optional[int] = None, P: Opti
     b_dt = _rng(seed, _S_BDT).uniform(-7.0, -2.3, size=P).astype(np.float32)
     A = (-(np.arange(N, dtype=np.float32) + 1.0)[None, :]
          * _rng(seed, _S_A).uniform(0.8, 1.2, size=(P, N)).astype(np.float32)).astype(np.float32)
-    if w.x_dtype == "bf16":
-        xhat, W_in = round_bf16(xhat), round_bf16(W_in)
-    return dict(xhat=xhat, target=target, W_in=W_in, b_dt=b_dt, A=A, workload=w, T=T, B=B, P=P, N=N)
+    if x_dtype == "bf16":
+        W_in = round_bf16(W_in)
+    return dict(W_in=W_in, b_dt=b_dt, A=A)
+
+
+def make_sel_stack_inputs(w, K: int, T: Optional[int] = None, B: Optional[int] = None, P: Optional[int] = None,
+                          N: Optional[int] = None, t0: int = 0, seed: Optional[int] = None) -> dict:
+    """A residual stack of K selective layers: the input, target and layer 1's weights of
+    make_sel_inputs, and layer k's (k >= 2) weights drawn the same way from the seed
+    seed + 1000 (k - 1).  layers: a list of K dicts W_in, b_dt, A."""
+    d = make_sel_inputs(w, T, B, P, N, t0, seed)
+    s0 = d["workload"].seed if seed is None else seed
+    layers = [dict(W_in=d["W_in"], b_dt=d["b_dt"], A=d["A"])]
+    for k in range(1, K):
+        layers.append(_sel_weights(s0 + 1000 * k, d["P"], d["N"], d["workload"].x_dtype))
+    d["layers"] = layers
+    d["K"] = K
+    return d

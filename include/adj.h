@@ -179,13 +179,24 @@ adj_status adj_rms_norm_bwd(const adj_dims *dims, const float *y, const float *r
  *     dt_t,p = softplus(z_t,p + b_dt,p),  B_t,n = z_t,P+n,  C_t,n = z_t,P+N+n
  *     Abar_t,pn = exp(dt_t,p A_pn)            A [P,N], the continuous-time decay
  *     h_t,pn = Abar_t,pn h_t-1,pn + dt_t,p B_t,n xhat_t,p   (h_-1 = 0)
- *     y_t,p = xhat_t,p + sum_n C_t,n h_t,pn   (the residual identity)
+ *     y_t,p = xres_t,p + sum_n C_t,n h_t,pn   (the residual identity; xres = xhat
+ *                                             for a lone layer)
  * i.e. a PN-dimensional state with A_t = diag(Abar_t) and the full P x PN output map
  * C_t[p, (p,n)] = C_t,n.  Its gradient is the same sum over token pairs of independent
  * VJPs as the diagonal layer's ([AS] Core claim, Proposition 2), full or truncated to a
  * window.  Sizes: adj_dims with N = 8 or 16, P a multiple of 8, B <= 65535; x_dtype is
  * the storage of xhat and W_in, d_dtype that of dz.  h is [B,T,P,N] fp32 (state index
- * last).  No call waits on another CTA, so none records ADJ_ETIMEOUT.
+ * last).  No call waits on another CTA; adj_sel_bwd's waits for its own bulk copies are
+ * bounded and record ADJ_ETIMEOUT in the workspace if one gives up.
+ *
+ * Stacks ([AS] What carries the argument: y^K = y^0 + sum_k ytilde^k; Load-bearing
+ * premise: normalised inputs): layer 1 reads the input, layer k >= 2 reads the residual
+ * stream y^{k-1} normalised per token, xhat^k = y^{k-1} / r (adj_rms_norm), with
+ * xres = y^{k-1}.  Its input path then passes the cotangent down:
+ *     gy^{k-1} = gy^k + (dxhat - xhat (xhat . dxhat) / P) / r,
+ *     dxhat_t,p = (dz_t W_in^T)_p + dt_t,p sum_n mu_t,pn B_t,n
+ * (the projection and the input term of the step), computed by adj_sel_bwd (r, gadd,
+ * rowdot) and adj_sel_param_grad (gy_prev).
  * ------------------------------------------------------------------------- */
 typedef struct {
     const void *W_in;    /* [P, P+2N] x_dtype */
@@ -196,11 +207,16 @@ typedef struct {
 /* Forward pass storing what the adjoint needs ([AS] Referee Report on Algorithm 1: the
  * per-token states are kept):
  *   xhat [B,T,P] x_dtype    layer input
+ *   xres [B,T,P] fp32       residual input (NULL: xhat's values; a stacked layer passes
+ *                           the residual stream y^{k-1} it normalised into xhat)
  *   z    [B,T,P+2N] fp32    xhat W_in, without b_dt (written)
  *   h    [B,T,P,N] fp32     states (written)
- *   y    [B,T,P] fp32       layer output (written) */
-adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, float *z, float *h,
-                       float *y, void *ws, size_t ws_bytes, void *stream);
+ *   y    [B,T,P] fp32       layer output (written; may not alias xres) */
+adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const float *xres,
+                       float *z, float *h, float *y, void *ws, size_t ws_bytes, void *stream);
+
+/* Columns of adj_sel_bwd's rowdot for these sizes (0 for sizes the selective calls reject). */
+size_t adj_sel_rowdot_cols(const adj_dims *dims);
 
 /* Adjoint of one selective layer for the cotangent gy = dL/dy [B,T,P] fp32: the window
  * sums mu_i = sum_{t=i}^{min(T-1, i+Tbar-1)} gy_t^T C_t prod_{j=i+1..t} A_j (all t >= i when
@@ -210,16 +226,28 @@ adj_status adj_sel_fwd(const adj_dims *dims, const adj_sel_weights *w, const voi
  *                           (sum_n mu_pn (A_pn Abar_pn h_{t-1},pn + B_n xhat_p)) sigmoid(z_p + b_dt,p);
  *                           columns P+n: sum_p mu_pn dt_p xhat_p (B_t); P+N+n: sum_p gy_p h_t,pn (C_t)
  *   dA [P,N] fp32           sum_t mu_pn dt_p Abar_pn h_{t-1},pn (written)
- * xhat, z, h as written by adj_sel_fwd. */
+ * xhat, z, h as written by adj_sel_fwd.
+ * The input path of a stacked layer (all three or none; NULL for a lone layer or layer 1):
+ *   r      [B,T] fp32                   the rms from adj_rms_norm (xhat = y^{k-1} / r)
+ *   gadd   [B,T,P] fp32 (written)       gy + dt sum_n mu B / r, the input term's share
+ *   rowdot [B*T, adj_sel_rowdot_cols] fp32 (written)  partial sums of xhat . dxhat, the
+ *                                       projection's share taken as dz . z (z = xhat W_in,
+ *                                       dz as stored), which adj_sel_param_grad sums
+ * gadd may not alias gy. */
 adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const float *z,
-                       const float *h, const float *gy, int64_t Tbar, void *dz, float *dA, void *ws,
-                       size_t ws_bytes, void *stream);
+                       const float *h, const float *gy, int64_t Tbar, void *dz, float *dA, const float *r,
+                       float *gadd, float *rowdot, void *ws, size_t ws_bytes, void *stream);
 
 /* Parameter gradients from dz ([AS] Core claim: the sum over tokens of the VJPs):
  *   dW_in [P, P+2N] fp32 = sum_t xhat_t^T dz_t,   db_dt [P] fp32 = sum_t dz_t[:P].
- * accumulate != 0 adds into the outputs instead of overwriting them. */
-adj_status adj_sel_param_grad(const adj_dims *dims, const void *xhat, const void *dz, float *dW_in, float *db_dt,
-                              int accumulate, void *ws, size_t ws_bytes, void *stream);
+ * accumulate (0 or 1) adds into the outputs instead of overwriting them.
+ * With the input path (r, gadd, rowdot from adj_sel_bwd and gy_prev, all or none; w->W_in
+ * then required, w may be NULL otherwise): gy_prev [B,T,P] fp32 (written) =
+ * gadd + (dz W_in^T - xhat m / P) / r with m the sum of rowdot's columns, the cotangent
+ * of the residual stream y^{k-1} below. */
+adj_status adj_sel_param_grad(const adj_dims *dims, const adj_sel_weights *w, const void *xhat, const void *dz,
+                              float *dW_in, float *db_dt, const float *r, const float *gadd, const float *rowdot,
+                              float *gy_prev, int accumulate, void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronise `stream`, return and clear the sticky device status of `ws`
  * (ADJ_OK or ADJ_ETIMEOUT); ADJ_ECUDA if the stream reports an error. */

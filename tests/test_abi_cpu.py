@@ -154,10 +154,14 @@ def test_selective_layer_rejects_bad_arguments(L):
     w = lib.SelWeights(FAKE, FAKE, FAKE)
 
     def fwd(d, ws_bytes=big, h=FAKE):
-        return L.adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, h, FAKE, FAKE, ws_bytes, None)
+        return L.adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), FAKE, None, FAKE, h, FAKE, FAKE, ws_bytes, None)
 
-    def bwd(d, Tbar=0, dz=FAKE):
-        return L.adj_sel_bwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, Tbar, dz, FAKE, FAKE, big, None)
+    def bwd(d, Tbar=0, dz=FAKE, inp=(None, None, None)):
+        return L.adj_sel_bwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, FAKE, FAKE, Tbar, dz, FAKE, *inp, FAKE,
+                             big, None)
+
+    def param(d, dz=FAKE, wp=None, inp=(None, None, None, None), acc=0):
+        return L.adj_sel_param_grad(ctypes.byref(d), wp, FAKE, dz, FAKE, FAKE, *inp, acc, FAKE, big, None)
 
     assert fwd(lib.dims(1, 64, 32, 24)) == 2                 # N = 24
     assert fwd(lib.dims(1, 64, 32, 32)) == 2                 # N = 32
@@ -165,11 +169,23 @@ def test_selective_layer_rejects_bad_arguments(L):
     assert fwd(lib.dims(1, 64, 32, 16), h=FAKE + 4) == 3
     d = lib.dims(2, 1000, 64, 16)
     assert fwd(d, ws_bytes=lib.workspace_bytes(d, lib.OP_SEL_FWD) - 1) == 5
+    assert L.adj_sel_fwd(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, big, None) == 3
     assert fwd(lib.dims(0, 64, 32, 16)) == 0                 # empty batch: nothing to do
     assert bwd(lib.dims(1, 1000, 32, 16), Tbar=100) == 1     # window not a multiple of 16
     assert bwd(lib.dims(1, 1000, 32, 16), dz=None) == 1
-    assert L.adj_sel_param_grad(ctypes.byref(lib.dims(1, 64, 32, 16)), FAKE, None, FAKE, FAKE, 0, FAKE, big,
-                                None) == 1
+    assert param(lib.dims(1, 64, 32, 16), dz=None) == 1
+    assert param(lib.dims(1, 64, 32, 16), acc=2) == 1
+    # the input path of a stacked layer: all of its buffers or none, and W_in with it
+    d1 = lib.dims(1, 64, 32, 16)
+    assert bwd(d1, inp=(FAKE, FAKE, None)) == 1
+    assert bwd(d1, inp=(None, FAKE, FAKE)) == 1
+    assert bwd(d1, inp=(FAKE, FAKE, FAKE + 4)) == 3
+    assert param(d1, inp=(FAKE, FAKE, FAKE, None)) == 1
+    assert param(d1, inp=(FAKE, FAKE, FAKE, FAKE)) == 1                    # no weights
+    assert param(d1, wp=ctypes.byref(lib.SelWeights(None, FAKE, FAKE)), inp=(FAKE,) * 4) == 1
+    assert lib.sel_rowdot_cols(lib.dims(1, 64, 1024, 16)) == 1024 // 128 + 1
+    assert lib.sel_rowdot_cols(lib.dims(1, 64, 1000, 8)) == 4 + 1
+    assert lib.sel_rowdot_cols(lib.dims(1, 64, 32, 24)) == 0
     for op in (lib.OP_SEL_FWD, lib.OP_SEL_BWD, lib.OP_SEL_PARAM):
         assert lib.workspace_bytes(lib.dims(1, 64, 32, 24), op) == 0
     # the truncated window's scratch (aggregates and R) makes its workspace the larger
