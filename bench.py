@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 HEADLINE = ("ssm4_p2048", 8192)
 CONTEXT = (("ssm1_1m", 4096), ("ssm1_1m", None), ("ssm8_p512", 4096), ("ssm1_p128", None), ("ssm1_p128", 2048))
 # the general selective layer (one layer), measured the same way
-SEL_CONTEXT = (("sel1_p1024", 8192), ("sel1_p1024", None))
+SEL_CONTEXT = (("sel1_p1024", 8192, 1), ("sel1_p1024", None, 1), ("sel1_p1024", None, 4))
 METRIC = "adjoint-gradient tokens/sec per layer on 1 GB300; % of HBM/tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # CPU oracle samples (prefixes of one sequence of the headline workload): all cores on
@@ -202,21 +202,31 @@ def kernel_table(P, N, xb, db, trunc, K=1):
     }
 
 
-def sel_kernel_table(P, N, xb, db):
+def sel_kernel_table(P, N, xb, db, K=1):
     """The general selective layer: algorithmic bytes (and flops) per token of each call's
     kernels (each scan counts its three launches together).  The forward scan reads z and
     xhat and writes h and y; the reverse scan reads z, xhat, gy and h and writes dz (the
     truncated form also writes and reads the window sums R, 8 P N bytes a token beyond
-    these counts)."""
+    these counts).  In a stack of K layers, layers 2..K also read the residual input in the
+    forward scan and, in the reverse scan, read r and write gadd and the row dots (the
+    table gives the mean over the K launches); sel_dx (the input GEMM with the
+    normalisation in its epilogue: dz, gadd, xhat, r and the row dots in, gy_prev out) and
+    rms_norm run K - 1 times."""
     zw = P + 2 * N
-    return {
+    nsl = -(-P // (256 // (N // 8)))
+    f = (K - 1) / K
+    tab = {
         "sel_proj": dict(bytes=P * xb + zw * 4, flops=2 * P * zw),
-        "sel_fwd": dict(bytes=zw * 4 + P * xb + 4 * P * N + 4 * P),
+        "sel_fwd": dict(bytes=zw * 4 + P * xb + 4 * P * N + 4 * P + f * 4 * P),
         "loss": dict(bytes=3 * P * 4),
-        "sel_bwd": dict(bytes=zw * 4 + P * xb + 4 * P + 4 * P * N + zw * db),
+        "sel_bwd": dict(bytes=zw * 4 + P * xb + 4 * P + 4 * P * N + zw * db + f * (4 + 4 * P + 4 * (nsl + 1))),
         "sel_dW": dict(bytes=P * xb + zw * db, flops=2 * P * zw),
         "colsum": dict(bytes=P * db),
     }
+    if K > 1:
+        tab["sel_dx"] = dict(bytes=zw * db + 4 * P + P * xb + 4 + 4 * (nsl + 1) + 4 * P, flops=2 * zw * P)
+        tab["rms_norm"] = dict(bytes=4 * P + P * xb + 4)
+    return tab
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel of a
@@ -246,7 +256,8 @@ KERNEL_TU = {
     "proj_in": "adj_gemm_tc.cu", "cot_proj": "adj_gemm_tc.cu", "param_dW_o": "adj_gemm_tc.cu",
     "bwd_scan": "adj_scan.cu", "fwd_scan": "adj_scan.cu", "win_scan": "adj_scan.cu",
     "rms_norm": "adj_misc.cu", "loss": "adj_misc.cu", "colsum": "adj_misc.cu",
-    "sel_fwd": "adj_sel.cu", "sel_bwd": "adj_sel.cu",
+    "sel_fwd": "adj_sel.cu", "sel_bwd": "adj_sel.cu", "sel_proj": "adj_gemm_tc.cu", "sel_dW": "adj_gemm_tc.cu",
+    "sel_dx": "adj_gemm_tc.cu",
 }
 
 
@@ -606,16 +617,22 @@ def context_line(key, window, dev, peaks, steps, warmup):
     return out
 
 
-def sel_context_line(key, window, dev, peaks, steps, warmup, cpu=False):
-    """The general selective layer on one of its workloads: graph replay of one step
-    (forward, loss, reverse, parameter gradients), L2 flushed before every step, median."""
+def sel_context_line(key, window, dev, peaks, steps, warmup, cpu=False, K=1):
+    """The general selective layer on one of its workloads, alone (K = 1) or as a residual
+    stack of K layers: graph replay of one step (forward, loss, reverse, parameter
+    gradients and, in a stack, the cotangents passed down), L2 flushed before every step,
+    median."""
     import torch
     from adjoint_gradients_long_gb300 import lib, synth
-    from adjoint_gradients_long_gb300.sel_layer import SelLayer
+    from adjoint_gradients_long_gb300.sel_layer import SelLayer, SelStack
     w = synth.SEL_WORKLOADS[key]
     bf16 = w.x_dtype == "bf16"
-    L = SelLayer(w.B, w.T, w.P, w.N, x_bf16=bf16, Tbar=window, device=dev)
-    L.load(synth.make_sel_inputs(w))
+    if K == 1:
+        L = SelLayer(w.B, w.T, w.P, w.N, x_bf16=bf16, Tbar=window, device=dev)
+        L.load(synth.make_sel_inputs(w))
+    else:
+        L = SelStack(w.B, w.T, w.P, w.N, K, x_bf16=bf16, Tbar=window, device=dev)
+        L.load(synth.make_sel_stack_inputs(w, K))
     for _ in range(warmup):
         L.step(window)
     n0 = lib.launch_count()
@@ -651,15 +668,16 @@ def sel_context_line(key, window, dev, peaks, steps, warmup, cpu=False):
     prof = lib.profile_read()
     lib.profile_reset()
     xb = 2 if bf16 else 4
-    kern = kernels_summary(prof, sel_kernel_table(w.P, w.N, xb, xb), w.B * w.T, peaks, split3=not bf16)
+    kern = kernels_summary(prof, sel_kernel_table(w.P, w.N, xb, xb, K), w.B * w.T, peaks, split3=not bf16)
     med = statistics.median(ms)
-    out = {"workload": key, "layer": "general selective (softplus step, exp(dt A) decay, input-dependent B_t, C_t)",
-           "window": window if window is not None else "full", "B": w.B, "T": w.T, "P": w.P, "N": w.N, "K": 1,
+    out = {"workload": key, "layer": "general selective (softplus step, exp(dt A) decay, input-dependent B_t, C_t)"
+           + (f", residual stack of {K} with normalised inputs" if K > 1 else ""),
+           "window": window if window is not None else "full", "B": w.B, "T": w.T, "P": w.P, "N": w.N, "K": K,
            "dtype": "bf16 GEMM operands, fp32 scans" if bf16 else "f32",
-           "value": w.B * w.T / (med * 1e-3), "unit": "tokens/s per layer", "ms_per_step": med,
+           "value": w.B * w.T * K / (med * 1e-3), "unit": "tokens/s per layer", "ms_per_step": med,
            "ms_mean": sum(ms) / len(ms), "steps": steps, "gpu_launches_per_step": per,
            "device_status": lib.STATUS.get(status, status), "kernels": kern}
-    if cpu:
+    if cpu and K == 1:
         out["cpu_baseline"] = sel_cpu_baseline(key, window)
     del g, L, flush
     torch.cuda.empty_cache()
@@ -753,9 +771,9 @@ def run_ours(args, rank, world, local_rank):
         del wl
         for k2, w2 in CONTEXT:
             others.append(context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3))))
-        for k2, w2 in SEL_CONTEXT:
+        for k2, w2, K2 in SEL_CONTEXT:
             others.append(sel_context_line(k2, w2, dev, peaks, min(args.steps, 10), max(3, min(args.warmup, 3)),
-                                           cpu=not args.no_cpu_baseline))
+                                           cpu=not args.no_cpu_baseline, K=K2))
 
     if rank == 0:
         line = {

@@ -122,3 +122,19 @@ def test_selective_kernel_table():
     assert t["sel_proj"]["flops"] == 2 * P * zw and t["sel_dW"]["flops"] == 2 * P * zw
     # the state dominates: its 4 P N bytes are over four fifths of a scan's bytes a token
     assert 4 * P * N / t["sel_bwd"]["bytes"] > 0.8
+
+
+def test_selective_stack_kernel_table():
+    """A stack of K selective layers: layers 2..K add the residual input to the forward
+    scan, r, gadd and the row dots (slices + 1 floats) to the reverse scan, and run the input
+    GEMM and the normalisation once each; the table's scan counts are means over the K."""
+    P, N, K = 1024, 16, 4
+    one = bench.sel_kernel_table(P, N, 2, 2)
+    t = bench.sel_kernel_table(P, N, 2, 2, K)
+    zw, nsl = P + 2 * N, P // 128
+    assert "sel_dx" not in one and "rms_norm" not in one
+    assert t["sel_fwd"]["bytes"] - one["sel_fwd"]["bytes"] == (K - 1) / K * 4 * P
+    assert t["sel_bwd"]["bytes"] - one["sel_bwd"]["bytes"] == (K - 1) / K * (4 + 4 * P + 4 * (nsl + 1))
+    assert t["sel_dx"]["bytes"] == 2 * zw + 4 * P + 2 * P + 4 + 4 * (nsl + 1) + 4 * P
+    assert t["sel_dx"]["flops"] == 2 * zw * P
+    assert t["rms_norm"]["bytes"] == 4 * P + 2 * P + 4
