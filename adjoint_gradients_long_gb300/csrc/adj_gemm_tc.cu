@@ -341,6 +341,28 @@ enum { LD_REG = 0, LD_TMA_K = 1, LD_TMA_MN = 2, LD_RAW_K = 3, LD_RAW_MN = 4 };
 __host__ __device__ inline bool ld_raw(int m) { return m >= LD_RAW_K; }
 __host__ __device__ inline bool ld_tma(int m) { return m != LD_REG; }
 
+// L2 priorities for a streamed StoreAdd epilogue: the outputs and the consumed residual and
+// xhat lines are marked evict-first, so that the boxes prefetched a tile ahead are not the
+// ones pushed out of L2 by the output stream.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, int x, int y, uint32_t src, uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(src), "l"(pol)
+                 : "memory");
+}
+
 struct TcArgs {
     CUtensorMap tmA[3], tmB[3];   // one map per array of a blocked operand
     CUtensorMap tmBlo[3];         // low parts of a pre-split B
@@ -353,6 +375,7 @@ struct TcArgs {
     int a_ld, b_ld;
     bool b_res, a_mul, b_lo;
     bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
+    bool stream_out;              // StoreAdd whose output far exceeds L2: evict-first hints
     int nacc;                     // accumulators in tensor memory (2: epilogue overlaps the next tile)
     int epiw;                     // epilogue warps (CTA pairs: 8 or 16; otherwise TC_EPI_WARPS)
     GemmOperand A, Bm;
@@ -792,8 +815,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             int64_t kbg = 0;
             // the residual of a TMA StoreAdd epilogue: the epilogue waits on each 32 x 32 box it
             // loads, so its boxes are prefetched into L2 when the tile's operand loads start,
-            // about a tile ahead of the epilogue
-            const bool pf_add = args.epi_tma && args.ep.kind == Epi::StoreAdd;
+            // about a tile ahead of the epilogue (a streamed output: the epilogue warps prefetch
+            // one chunk ahead instead, since a tile ahead the lines would not survive in L2)
+            const bool pf_add = args.epi_tma && args.ep.kind == Epi::StoreAdd && !args.stream_out;
             for (int64_t t = unit0; t < ntiles && ok; t += nunits) {
                 int64_t m0, n0, kb0, ke;
                 int z;
@@ -953,10 +977,30 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 const bool add_tma = via_tma && ep.kind == Epi::StoreAdd;
                 if (via_tma) {
                     if (lane == 0) {
+                        if (add_tma && args.stream_out) {
+                            // L2 prefetch of this warp's next chunk: the next column chunk of the
+                            // tile, else the first chunk of the CTA's next tile
+                            int64_t pm = m0r, pn = int64_t(n) + CSTEP;
+                            if (c + CSTEP >= BN) {
+                                pm = args.M;
+                                if (t + nunits < ntiles) {
+                                    int64_t m1, n1, kb1, ke1;
+                                    int z1;
+                                    tile_of(t + nunits, m1, n1, z1, kb1, ke1);
+                                    pm = m1 + q * 32;
+                                    pn = n1 + half * 32;
+                                }
+                            }
+                            if (pm < args.M && pn < args.Nc) {
+                                tma_prefetch_2d(&args.tmAdd, int(pn), int(pm));
+                                if (ep.nr) tma_prefetch_2d(&args.tmNx, int(pn), int(pm));
+                            }
+                        }
                         bulk_wait_read();   // the previous chunk's store has read the buffer
                         if (add_tma) {
                             mbar_arrive_expect_tx(addbar, 32 * 32 * 4);
-                            tma_load_2d(sb_s, &args.tmAdd, n, int(m0r), addbar);
+                            if (args.stream_out) tma_load_2d_hint(sb_s, &args.tmAdd, n, int(m0r), addbar, l2_evict_first());
+                            else tma_load_2d(sb_s, &args.tmAdd, n, int(m0r), addbar);
                         }
                     }
                     __syncwarp();
@@ -976,8 +1020,10 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         const __nv_bfloat16 *xr = static_cast<const __nv_bfloat16 *>(ep.nx) + nrow * ep.ld + n;
 #pragma unroll
                         for (int g = 0; g < 4; ++g)
-                            n_xb[g] = (n + 8 * g < args.Nc) ? __ldg(reinterpret_cast<const uint4 *>(xr + 8 * g))
-                                                            : make_uint4(0u, 0u, 0u, 0u);
+                            n_xb[g] = (n + 8 * g < args.Nc)
+                                          ? (args.stream_out ? __ldcs(reinterpret_cast<const uint4 *>(xr + 8 * g))
+                                                             : __ldg(reinterpret_cast<const uint4 *>(xr + 8 * g)))
+                                          : make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
                 float v[32];
@@ -1043,7 +1089,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                                 u.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
                                 u.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
                                 u.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
-                                *reinterpret_cast<uint4 *>(xr + 8 * g) = u;
+                                if (args.stream_out) __stcs(reinterpret_cast<uint4 *>(xr + 8 * g), u);
+                                else *reinterpret_cast<uint4 *>(xr + 8 * g) = u;
                             }
                     }
 #pragma unroll
@@ -1056,6 +1103,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             tma_store_3d(&args.tmO[0], n, int(m0r), z, sb_s);
                         } else if (ep.kind == Epi::ProjIn) {
                             tma_store_2d(&args.tmO[pblk], pch, int(m0r), sb_s);
+                        } else if (args.stream_out) {
+                            tma_store_2d_hint(&args.tmO[0], n, int(m0r), sb_s, l2_evict_first());
                         } else {
                             tma_store_2d(&args.tmO[0], n, int(m0r), sb_s);
                         }
@@ -1366,6 +1415,9 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (pair && (a.a_ld != a_mode || a.b_ld != b_mode)) return cudaErrorInvalidValue;   // a map did not build
     a.a_mul = a_mul && a.a_ld != LD_REG;
     a.epi_tma = epi_maps(a, ep, M, Nc, splits);
+    // a residual stream far larger than L2 (129 MB): its output lines cannot serve a later
+    // reader from L2, so they go out first
+    a.stream_out = a.epi_tma && ep.kind == Epi::StoreAdd && uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20);
     a.b_lo = Bm.lo[0] && a.b_ld != LD_REG;
     // the layout was sized for the modes asked for; a mode that fell back to registers
     // uses only part of its region
