@@ -1376,8 +1376,9 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     // rows x BN with BN / 2 columns of B staged in each CTA
     bool pair = pair_cand && !a.b_res && (b_mode == LD_TMA_K || b_mode == LD_TMA_MN) && BN % TC_BM == 0;
     int slots = 0;
-    // pairs with many tiles each (no split) use 16 epilogue warps, with one stage fewer
-    const int epiw = (pair && splits == 1) ? TC_MAX_EPI_WARPS : TC_EPI_WARPS;
+    // pairs with many tiles each (no split) and a short K use 16 epilogue warps, with one
+    // stage fewer; a long K keeps the stage (its mainloop outlasts the epilogue of 8 warps)
+    const int epiw = (pair && splits == 1 && K <= 1024) ? TC_MAX_EPI_WARPS : TC_EPI_WARPS;
     const size_t bar_bytes = size_t(3 * 6 + 6 + TC_MAX_EPI_WARPS) * 8;
     if (pair) {
         const TcLayout Lp = tc_layout(BN / 2, a.kper, false, false, false, false, false);
