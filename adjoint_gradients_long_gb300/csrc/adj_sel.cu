@@ -72,6 +72,12 @@ struct Geo {   // a thread's place: channel p (q within the slice), states n0 ..
     }
 };
 
+// two floats as bf16 (round to nearest even), the first in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
 // sum over the LP lanes of a channel
 template <int LP>
 __device__ __forceinline__ float chan_sum(float v) {
@@ -184,8 +190,8 @@ __device__ __forceinline__ void stage_sub(const Stage<NS> &s, const float *__res
 // ------------------------------------------------------------------ forward state scan
 // MODE 0: aggregates (prod Abar, h at the chunk end from h = 0) -> aggX, aggY.
 // MODE 1: outputs from the carries in aggY: h [B,T,P,NS] and y = xres + sum_n C h [B,T,P]
-// (xres null: xhat's values).
-template <int NS, typename TX, int MODE>
+// (XR: the residual input xres, staged with the other per-token inputs; else xhat's values).
+template <int NS, typename TX, int MODE, bool XR = false>
 __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict__ z, const TX *__restrict__ x,
                                                         const float *__restrict__ b_dt, const float *__restrict__ A,
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
@@ -213,16 +219,16 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict
     const int64_t ai = ((b * nchunks + c) * P + pp) * NS + g.n0;
     if (MODE == 1 && g.act) ld8g(aggY + ai, st);
     // the next sub-chunk's inputs load into registers while this one is walked
-    StageRegs<NS> R;
-    stage_load<NS, TX, true, false>(R, z, x, nullptr, b_dt, P, ZW, row0, 0, rows < SC ? rows : SC, slice * PC);
+    StageRegs<NS> R;   // (XR: xres rides in the slot of gy, which the forward pass does not use)
+    stage_load<NS, TX, true, XR>(R, z, x, xres, b_dt, P, ZW, row0, 0, rows < SC ? rows : SC, slice * PC);
     for (int r0 = 0; r0 < rows; r0 += SC) {
         const int nr = rows - r0 < SC ? rows - r0 : SC;
         __syncthreads();   // the previous sub-chunk is consumed
-        stage_store<NS, true, false>(sg, R, nr, slice * PC, P);
+        stage_store<NS, true, XR>(sg, R, nr, slice * PC, P);
         __syncthreads();
         if (r0 + SC < rows) {
             const int nn = rows - r0 - SC < SC ? rows - r0 - SC : SC;
-            stage_load<NS, TX, true, false>(R, z, x, nullptr, b_dt, P, ZW, row0, r0 + SC, nn, slice * PC);
+            stage_load<NS, TX, true, XR>(R, z, x, xres, b_dt, P, ZW, row0, r0 + SC, nn, slice * PC);
         }
         for (int r = 0; r < nr; ++r) {
             const float dt = sg.dt[r * PC + g.q], xv = sg.x[r * PC + g.q], dx = dt * xv;
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict
                 const int64_t row = row0 + r0 + r;
                 if (g.act) st8s(h + (row * P + pp) * NS + g.n0, st);
                 yp = chan_sum<LP>(yp);
-                if (g.act && g.n0 == 0) y[row * P + pp] = (xres ? __ldcs(xres + row * P + pp) : xv) + yp;
+                if (g.act && g.n0 == 0) y[row * P + pp] = (XR ? sg.g[r * PC + g.q] : xv) + yp;
             }
         }
     }
@@ -483,6 +489,7 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
     __shared__ uint64_t s_full[SEL_NSTG], s_empty[SEL_NSTG];
     __shared__ int s_abort;
     __shared__ float s_rd[SEL_THREADS / 32][16];           // INP: the warps' row-dot shares
+    __shared__ float s_rin[16];                            // INP: the sub-chunk's 1 / r
     const Stage<NS> sg = stage_carve<NS>(sm_sel, INP);
     float *sW = sm_sel + stage_floats<NS>(INP);            // [8 warps][SC][32]
     float *sH = sW + (SEL_THREADS / 32) * SC * 32;         // [SEL_NSTG][STG]
@@ -578,6 +585,33 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
                 for (int w8 = 0; w8 < SEL_THREADS / 32; ++w8) acc += s_rd[w8][j];
                 rowdot[(row0 + (hi_s - 1 - j)) * (nslices + 1) + slice] = acc;
             }
+        // dz's dt columns (from the sigma slots) and gadd (from the z slots) of the sub-chunk's
+        // rows [lo_s, hi_s), 8 channels a thread-step (P is a multiple of 8)
+        const int pw = P - p0 < PC ? P - p0 : PC;
+        for (int e = threadIdx.x; e < (hi_s - lo_s) * (PC / 8); e += SEL_THREADS) {
+            const int j = e / (PC / 8), c8 = (e % (PC / 8)) * 8;
+            if (c8 >= pw) continue;
+            const int64_t trow = row0 + lo_s + j;
+            const float4 a0 = *reinterpret_cast<const float4 *>(sg.sig + j * PC + c8);
+            const float4 a1 = *reinterpret_cast<const float4 *>(sg.sig + j * PC + c8 + 4);
+            TD *dst = dz + trow * ZW + p0 + c8;
+            if constexpr (sizeof(TD) == 2) {
+                uint4 u;
+                u.x = pack_bf16x2(a0.x, a0.y);
+                u.y = pack_bf16x2(a0.z, a0.w);
+                u.z = pack_bf16x2(a1.x, a1.y);
+                u.w = pack_bf16x2(a1.z, a1.w);
+                *reinterpret_cast<uint4 *>(dst) = u;
+            } else {
+                reinterpret_cast<float4 *>(dst)[0] = a0;
+                reinterpret_cast<float4 *>(dst)[1] = a1;
+            }
+            if (INP) {
+                float *gdst = gadd + trow * P + p0 + c8;
+                reinterpret_cast<float4 *>(gdst)[0] = *reinterpret_cast<const float4 *>(sg.zr + j * PC + c8);
+                reinterpret_cast<float4 *>(gdst)[1] = *reinterpret_cast<const float4 *>(sg.zr + j * PC + c8 + 4);
+            }
+        }
     };
 
     int slo = rows, shi = rows;   // the staged sub-chunk [slo, shi)
@@ -601,6 +635,9 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
                 }
             } else {
                 stage_sub<NS, TX, true, true, INP>(sg, z, x, gy, b_dt, P, ZW, row0, slo, shi - slo, p0);
+                if (INP)
+                    for (int j = threadIdx.x; j < shi - slo; j += SEL_THREADS)
+                        s_rin[j] = 1.f / __ldg(rin + row0 + slo + j);
             }
             walkers_sync();
         }
@@ -659,27 +696,26 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
                     hc[k] = hp[k];
                 }
                 const float ddt = chan_sum<LP>(fmaf(dda, 1.f / LOG2E, ddb * xv));
+                // dz's dt column (through the softplus) replaces sigma in its shared slot and
+                // goes out with the sub-chunk's flush, as whole rows
                 float dzs = 0.f;   // dz_dt as stored
                 if (g.act && g.n0 == 0) {
-                    const float val = ddt * sg.sig[rr * PC + g.q];   // through the softplus
-                    if constexpr (sizeof(TD) == 2) {
-                        const __nv_bfloat16 vb = __float2bfloat16_rn(val);
-                        dz[(row0 + r) * ZW + pp] = vb;
-                        dzs = __bfloat162float(vb);
-                    } else {
-                        dz[(row0 + r) * ZW + pp] = val;
-                        dzs = val;
-                    }
+                    const float val = ddt * sg.sig[rr * PC + g.q];
+                    sg.sig[rr * PC + g.q] = val;
+                    if constexpr (sizeof(TD) == 2) dzs = __bfloat162float(__float2bfloat16_rn(val));
+                    else dzs = val;
                 }
                 if (INP) {
                     const float dxd = dt * chan_sum<LP>(ddb);
                     float rd = 0.f;
                     if (g.act && g.n0 == 0) {
-                        gadd[(row0 + r) * P + pp] = sg.g[rr * PC + g.q] + dxd / __ldg(rin + row0 + r);
                         rd = fmaf(dzs, sg.zr[rr * PC + g.q], xv * dxd);
+                        sg.zr[rr * PC + g.q] = sg.g[rr * PC + g.q] + dxd * s_rin[rr];   // gadd, flushed too
                     }
+                    // a channel's value sits on its first lane: with two lanes a channel the odd
+                    // lanes hold zeros and the last level is not needed
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) rd += __shfl_xor_sync(0xffffffffu, rd, o);
+                    for (int o = 16; o >= (LP == 2 ? 2 : 1); o >>= 1) rd += __shfl_xor_sync(0xffffffffu, rd, o);
                     if (lane == 0) s_rd[wp][shi - 1 - r] = rd;
                 }
                 sW[(wp * SC + (shi - 1 - r)) * 32 + lane] = warp_tsum16<LP>(v, lane);
@@ -791,12 +827,17 @@ static cudaError_t sel_fwd_t(const float *z, const void *x, const float *b_dt, c
     cudaError_t e;
     if ((e = smem_attr(k_sel_fwd<NS, TX, 0>, smem)) != cudaSuccess) return e;
     if ((e = smem_attr(k_sel_fwd<NS, TX, 1>, smem)) != cudaSuccess) return e;
-    k_sel_fwd<NS, TX, 0><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, xres, T, P, TT,
+    if ((e = smem_attr(k_sel_fwd<NS, TX, 1, true>, smem)) != cudaSuccess) return e;
+    k_sel_fwd<NS, TX, 0><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, nullptr, T, P, TT,
                                                           nchunks);
     const int64_t n = B * int64_t(P) * NS;
     k_sel_carry<0><<<unsigned((n + 255) / 256), 256, 0, st>>>(aggX, aggY, B, int64_t(P) * NS, nchunks, T, TT, T);
-    k_sel_fwd<NS, TX, 1><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, xres, T, P, TT,
-                                                          nchunks);
+    if (xres)
+        k_sel_fwd<NS, TX, 1, true><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, xres, T, P, TT,
+                                                                    nchunks);
+    else
+        k_sel_fwd<NS, TX, 1><<<grid, SEL_THREADS, smem, st>>>(z, xt, b_dt, A, aggX, aggY, h, y, nullptr, T, P, TT,
+                                                              nchunks);
     return cudaGetLastError();
 }
 
