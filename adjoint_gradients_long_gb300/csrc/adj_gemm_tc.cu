@@ -86,8 +86,7 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t a, uint6
 }
 // CTA pair: arrive on the mbarrier at this shared-memory offset in both CTAs once the
 // pair MMAs issued so far have completed
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    const uint16_t mask = 3;
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask = 3) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(mask)
@@ -340,6 +339,18 @@ constexpr uint32_t TC_CHUNK_BYTES = 32 * 32 * 4;
 enum { LD_REG = 0, LD_TMA_K = 1, LD_TMA_MN = 2, LD_RAW_K = 3, LD_RAW_MN = 4 };
 __host__ __device__ inline bool ld_raw(int m) { return m >= LD_RAW_K; }
 __host__ __device__ inline bool ld_tma(int m) { return m != LD_REG; }
+
+// Four-CTA clusters (two pairs on the same n tile and neighbouring m tiles): a 2-D tiled TMA
+// load multicast to the CTAs of `mask` (the same shared offset in each); each destination's
+// completion is counted on the mbarrier at `bar`'s offset in the leader CTA of that
+// destination's pair (bar: the issuing pair's leader barrier, peer bit clear).
+__device__ __forceinline__ void tma_load_2d_quad(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                                 uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+}
 
 // L2 priorities for a streamed StoreAdd epilogue: the outputs and the consumed residual and
 // xhat lines are marked evict-first, so that the boxes prefetched a tile ahead are not the
@@ -611,7 +622,11 @@ __device__ __forceinline__ void epi_chunk(const TcArgs &args, const float *sb, i
 // is multicast to both CTAs' stage and accumulator barriers; both epilogues release the
 // accumulator on the leader's barrier.  Per SM this halves the B operand traffic through
 // shared memory for the same MMA work.  Only all-bf16, all-TMA operands take this mode.
-template <bool ABF, bool BBF, bool SPLIT, bool REGS, bool PAIR = false, bool EXT = false>
+// QUAD (with PAIR): clusters of four CTAs, two pairs on the same n tile and the two halves
+// of a 512-row m tile.  The pairs' B halves are the same: each CTA loads half of its B half
+// and multicasts it to its counterpart in the other pair, so B crosses L2 once per four
+// CTAs instead of twice.  A stage is refilled only once both pairs' MMAs have released it.
+template <bool ABF, bool BBF, bool SPLIT, bool REGS, bool PAIR = false, bool EXT = false, bool QUAD = false>
 __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_constant__ TcArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -631,10 +646,12 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t ntiles = int64_t(args.n_tiles) * args.m_tiles * args.splits;
     const int64_t nkb_full = (args.kper + TC_BK - 1) / TC_BK;
-    // tiles are scheduled per CTA, or per pair (unit = cluster) with rank 0 the leader
-    const uint32_t prank = PAIR ? cluster_rank() : 0u;
-    const int64_t unit0 = PAIR ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);
-    const int64_t nunits = PAIR ? int64_t(gridDim.x >> 1) : int64_t(gridDim.x);
+    // tiles are scheduled per CTA, or per pair (unit = cluster) with rank 0 the leader; a
+    // four-CTA cluster holds pairs {0, 1} and {2, 3} (leaders 0 and 2)
+    const uint32_t crank = PAIR ? cluster_rank() : 0u;
+    const uint32_t prank = crank & 1u, lead = crank & ~1u, pq = QUAD ? crank >> 1 : 0u;
+    const int64_t unit0 = QUAD ? int64_t(blockIdx.x >> 2) : PAIR ? int64_t(blockIdx.x >> 1) : int64_t(blockIdx.x);
+    const int64_t nunits = QUAD ? int64_t(gridDim.x >> 2) : PAIR ? int64_t(gridDim.x >> 1) : int64_t(gridDim.x);
     const int NACC = PAIR ? args.nacc : 2;
     uint32_t ncols = 32;
     while (ncols < uint32_t(NACC * BN)) ncols <<= 1;
@@ -649,7 +666,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), (prod_full ? TC_PROD : 0) + (tma_full ? 1 : 0));
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), QUAD ? 2 : 1);   // QUAD: both pairs' MMAs release the stage
             mbar_init(smem_u32(&rawfull[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -687,7 +704,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     // pair MMA writes it there in both); otherwise nothing runs and a failure is recorded
     bool pair_ok = true;
     if (PAIR) {
-        const uint32_t peer = ld_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(tmem_slot)), prank ^ 1u));
+        const uint32_t peer = ld_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t *>(tmem_slot)), crank ^ 1u));
         pair_ok = peer == tmem;
         if (!pair_ok && tid == 0) record_timeout(args.status);
     }
@@ -697,7 +714,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         const int64_t per_split = int64_t(args.n_tiles) * args.m_tiles;
         z = int(t / per_split);
         const int64_t r = t - int64_t(z) * per_split;
-        m0 = (r / args.n_tiles) * (PAIR ? 2 * TC_BM : TC_BM) + int64_t(prank) * TC_BM;   // this CTA's rows
+        m0 = (r / args.n_tiles) * (QUAD ? 4 * TC_BM : PAIR ? 2 * TC_BM : TC_BM) + int64_t(pq) * 2 * TC_BM +
+             int64_t(prank) * TC_BM;   // this CTA's rows
         n0 = (r % args.n_tiles) * BN;
         kb0 = int64_t(z) * args.kper;
         ke = kb0 + args.kper < args.K ? kb0 + args.kper : args.K;
@@ -846,10 +864,27 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     if (PAIR) {
                         // bf16 A rows of this CTA and its half of the B columns, counted on the
                         // leader's barrier, which expects both CTAs' bytes
-                        const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0u);
+                        const uint32_t fb = mapa_shared(smem_u32(&full[s]), lead);
                         if (prank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * txd);
                         tma_tile<true, true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, fb);
-                        tma_tile<false, true>(args.tmB, args.Bm, args.b_ld, n0 + int64_t(prank) * BNS, BNS, k0, sbb, fb);
+                        if (QUAD) {
+                            // this CTA's half of its B half (64 rows), to itself and its counterpart
+                            const int64_t row = n0 + int64_t(prank) * BNS + int64_t(pq) * (BNS / 2);
+                            const uint16_t mc = uint16_t((1u << prank) | (1u << (prank + 2u)));
+                            int blk = 0;
+                            int64_t rr = row;
+                            if (args.Bm.blk < (int64_t(1) << 30)) {
+                                blk = int(row / args.Bm.blk);
+                                rr = row - int64_t(blk) * args.Bm.blk;
+                            }
+                            // K-major: 64 rows of 128 bytes (a whole number of swizzle atoms);
+                            // MN-major: one 64 x 64 box
+                            const uint32_t dq = smem_u32(sbb + size_t(pq) * (size_t(BNS / 2) * 128));
+                            if (args.b_ld == LD_TMA_K) tma_load_2d_quad(dq, &args.tmB[blk], int(k0), int(rr), fb, mc);
+                            else tma_load_2d_quad(dq, &args.tmB[blk], int(rr), int(k0), fb, mc);
+                        } else {
+                            tma_tile<false, true>(args.tmB, args.Bm, args.b_ld, n0 + int64_t(prank) * BNS, BNS, k0, sbb, fb);
+                        }
                     } else if (txd) {
                         const uint32_t fb = smem_u32(&full[s]);
                         mbar_arrive_expect_tx(fb, txd);
@@ -935,10 +970,11 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             }
                         }
                     }
-                    if (PAIR) mma_commit_pair(smem_u32(&empty[s]));
+                    // QUAD: the stage is released in all four CTAs (the other pair multicasts into it)
+                    if (PAIR) mma_commit_pair(smem_u32(&empty[s]), QUAD ? uint16_t(0xF) : uint16_t(3u << lead));
                     else mma_commit(smem_u32(&empty[s]));
                 }
-                if (PAIR) mma_commit_pair(smem_u32(&accf[buf]));
+                if (PAIR) mma_commit_pair(smem_u32(&accf[buf]), uint16_t(3u << lead));
                 else mma_commit(smem_u32(&accf[buf]));
             }
         }
@@ -957,7 +993,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         uint32_t add_phase = 0;
         int64_t i = 0;
         // CTA pair: the accumulator is released on the leader's barrier
-        const uint32_t acce_at = PAIR ? mapa_shared(smem_u32(&acce[0]), 0u) : 0u;
+        const uint32_t acce_at = PAIR ? mapa_shared(smem_u32(&acce[0]), lead) : 0u;
         for (int64_t t = unit0; t < ntiles && pair_ok; t += nunits, ++i) {
             int64_t m0, n0, kb0, ke;
             int z;
@@ -1265,12 +1301,17 @@ static cudaError_t launch_tc_t(const TcArgs &a, unsigned grid, size_t smem, cuda
     return cudaGetLastError();
 }
 
-// The CTA-pair instantiation (bf16 operands, all by TMA): launched as clusters of two.
+// The CTA-pair instantiation (bf16 operands, all by TMA): launched as clusters of two, or
+// of four (two pairs sharing B by multicast).
 using PairKernel = void (*)(TcArgs);
-static PairKernel pair_kernel(bool ext = false) {
+static PairKernel pair_kernel(bool ext = false, bool quad = false) {
+    if (quad)
+        return ext ? k_gemm_tc<false, false, false, false, true, true, true>
+                   : k_gemm_tc<false, false, false, false, true, false, true>;
     return ext ? k_gemm_tc<false, false, false, false, true, true> : k_gemm_tc<false, false, false, false, true, false>;
 }
-static cudaLaunchConfig_t pair_config(unsigned grid, size_t smem, cudaStream_t st, cudaLaunchAttribute *attr) {
+static cudaLaunchConfig_t pair_config(unsigned grid, size_t smem, cudaStream_t st, cudaLaunchAttribute *attr,
+                                      unsigned cluster = 2) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(grid, 1, 1);
@@ -1278,37 +1319,53 @@ static cudaLaunchConfig_t pair_config(unsigned grid, size_t smem, cudaStream_t s
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cfg;
 }
-// Pairs of CTAs that can be resident at once with this much shared memory (0 if none).
-static int pair_slots(size_t smem) {
-    static size_t cached_smem[4] = {0, 0, 0, 0};
-    static int cached[4] = {-1, -1, -1, -1};
+// Clusters of two (pairs) or four (quads) CTAs that can be resident at once with this much
+// shared memory (0 if none).
+static int pair_slots(size_t smem, bool quad = false) {
+    static size_t cached_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    static int cached[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    static bool cached_quad[8] = {false, false, false, false, false, false, false, false};
     static int next = 0;
-    for (int i = 0; i < 4; ++i)
-        if (cached[i] >= 0 && cached_smem[i] == smem) return cached[i];
-    if (cudaFuncSetAttribute(pair_kernel(), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    for (int i = 0; i < 8; ++i)
+        if (cached[i] >= 0 && cached_smem[i] == smem && cached_quad[i] == quad) return cached[i];
+    if (cudaFuncSetAttribute(pair_kernel(false, quad), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
         return 0;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pair_config(2, smem, nullptr, attr);
+    const cudaLaunchConfig_t cfg = pair_config(quad ? 4 : 2, smem, nullptr, attr, quad ? 4 : 2);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_kernel(), &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_kernel(false, quad), &cfg) != cudaSuccess) n = 0;
     cached_smem[next] = smem;
     cached[next] = n;
-    next = (next + 1) % 4;
+    cached_quad[next] = quad;
+    next = (next + 1) % 8;
     return n;
 }
-static cudaError_t launch_pair(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st, bool ext) {
-    cudaError_t e = cudaFuncSetAttribute(pair_kernel(ext), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+static cudaError_t launch_pair(const TcArgs &a, unsigned grid, size_t smem, cudaStream_t st, bool ext,
+                               bool quad = false) {
+    cudaError_t e =
+        cudaFuncSetAttribute(pair_kernel(ext, quad), cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pair_config(grid, smem, st, attr);
-    return cudaLaunchKernelEx(&cfg, pair_kernel(ext), a);
+    const cudaLaunchConfig_t cfg = pair_config(grid, smem, st, attr, quad ? 4 : 2);
+    return cudaLaunchKernelEx(&cfg, pair_kernel(ext, quad), a);
+}
+
+// Whether pair GEMMs with a long K (a mainloop bound by operand delivery) run as quads.
+static int g_quad_mode = -1;
+static bool quad_enabled() {
+    if (g_quad_mode < 0) {
+        const char *v = getenv("ADJ_GEMM_QUAD");
+        g_quad_mode = (v && v[0] == '0') ? 0 : 1;
+    }
+    return g_quad_mode == 1;
 }
 
 // Whether GEMMs whose operands are both bf16 and both loaded by TMA run as CTA pairs.
@@ -1390,8 +1447,22 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
         if (slots > 0) S = Sp;
         else pair = false;
     }
-    const int64_t rows_per_tile = pair ? 2 * TC_BM : TC_BM;
-    const int64_t units = pair ? slots : g_num_sms;   // tiles in flight: CTA pairs or CTAs
+    // quads: two pairs on neighbouring 256-row tiles share B by multicast, for a long K (a
+    // mainloop bound by operand delivery) and B spread over several n tiles (a single n tile
+    // of B stays close in L2 anyway); at least two pair rows of tiles, whole 64-row halves
+    bool quad = false;
+    if (pair && quad_enabled() && K > 1024 && (Nc + BN - 1) / BN >= 2 && (M + 2 * TC_BM - 1) / (2 * TC_BM) >= 2 &&
+        (BN / 2) % 64 == 0) {
+        const TcLayout Lp = tc_layout(BN / 2, a.kper, false, false, false, false, false);
+        const size_t smem_p = 1024 + size_t(S) * Lp.stage_bytes + size_t(epiw) * TC_CHUNK_BYTES + bar_bytes;
+        const int q = pair_slots(smem_p, true);
+        if (q > 0) {
+            quad = true;
+            slots = q;
+        }
+    }
+    const int64_t rows_per_tile = quad ? 4 * TC_BM : pair ? 2 * TC_BM : TC_BM;
+    const int64_t units = pair ? slots : g_num_sms;   // tiles in flight: clusters (pairs, quads) or CTAs
     // split K no further than one wave of CTAs: every CTA then owns exactly one tile
     {
         const int64_t per_split = ((Nc + BN - 1) / BN) * ((M + rows_per_tile - 1) / rows_per_tile);
@@ -1412,7 +1483,7 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.m_tiles = int((M + rows_per_tile - 1) / rows_per_tile);
     a.A = A; a.Bm = Bm; a.ep = ep; a.status = status;
     a.a_ld = tma_build(a.tmA, nullptr, &a.tmAmul, A, a_mode, true, M, K, TC_BM);
-    a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, pair ? BN / 2 : BN);
+    a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, quad ? BN / 4 : pair ? BN / 2 : BN);
     if (pair && (a.a_ld != a_mode || a.b_ld != b_mode)) return cudaErrorInvalidValue;   // a map did not build
     a.a_mul = a_mul && a.a_ld != LD_REG;
     a.epi_tma = epi_maps(a, ep, M, Nc, splits);
@@ -1429,8 +1500,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (pair) {
         a.ep.csum = nullptr;
         if (csum_done) *csum_done = false;
-        const int64_t npairs = ntiles < slots ? ntiles : slots;
-        return launch_pair(a, unsigned(2 * npairs), smem, st, ext);
+        const int64_t nclus = ntiles < slots ? ntiles : slots;
+        return launch_pair(a, unsigned((quad ? 4 : 2) * nclus), smem, st, ext, quad);
     }
     int64_t grid = ntiles;
     if (grid > g_num_sms) grid = (g_num_sms / a.n_tiles) * a.n_tiles;
