@@ -410,48 +410,20 @@ __device__ __forceinline__ int tsum16_index(int lane) {
     return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
-// Bounded wait on an mbarrier phase that sleeps between polls (the waiting warp gives its
-// issue slots to the others); gives up after 2 s, recording the timeout.
-__device__ __forceinline__ void mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int *abort, unsigned *status,
-                                                uint32_t hint_ns) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}\n"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity), "r"(hint_ns)
-            : "memory");
-        if (ok) return;
-        if ((it & 15u) == 15u) {
-            if (*abort) return;
-            const uint64_t t = gtimer();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > TC_WAIT_NS) {
-                *abort = 1;
-                record_timeout(status);
-                return;
-            }
-        }
-    }
-}
-
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
 
-// Threads of the reverse output pass: the walking warps plus one copy warp.
-constexpr int SEL_BWD_THREADS = SEL_THREADS + 32;
-#ifndef ADJ_SEL_BWD_MINB
-#define ADJ_SEL_BWD_MINB 2   // CTAs an SM the register budget is cut for
-#endif
-#ifndef ADJ_SEL_PRODUCER_SLEEP_NS
-#define ADJ_SEL_PRODUCER_SLEEP_NS 200u   // the copy warp's suspend hint while a stage is in use
-#endif
+// Running count of the warps done with a stage: acquire-release, so the last warp's refill
+// is ordered after every warp's reads of the stage.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
+
 constexpr int SEL_NSTG = 3;   // stages in the ring of state rows
 template <bool TRUNC>
 constexpr int sel_group() { return TRUNC ? 1 : 2; }   // tokens a stage
@@ -462,9 +434,11 @@ constexpr int sel_group() { return TRUNC ? 1 : 2; }   // tokens a stage
 // through the softplus), the CTA's partial sums over its channels of dB and dC per token
 // -> bc [B*T, nslices, 2 NS], and the chunk's dA partial -> dAp [B*nchunks, P, NS].
 // TRUNC: mu^W = mu + q R(min(t+W-1, T-1)) where a later block exists and t starts none.
-// 256 + 32 threads: warp 8 copies the state rows (and R rows) into the stages: stage k
-// holds the rows of group k (tokens counted down from the chunk's top, G a group), one more
-// stage the row before the chunk; group k reads stages k and k + 1.
+// The state rows (and R rows) arrive by bulk copies into a ring of stages: stage k holds the
+// rows of group k (tokens counted down from the chunk's top, G a group), one more stage the
+// row before the chunk; group k reads stages k and k + 1.  Thread 0 issues the first stages;
+// afterwards the last of the eight warps to finish with a stage refills it, so no thread
+// waits for a stage to drain and the 8 warps keep 128 registers a thread.
 // INP (MODE 1, stacked layers): also the input path's share that does not go through the
 // projection, dxd = dt sum_n mu^W B (xhat's factor in the input term), written as
 // gadd = gy + dxd / r (r: the rms of the layer's input stream), and the CTA's partial row
@@ -472,7 +446,7 @@ constexpr int sel_group() { return TRUNC ? 1 : 2; }   // tokens a stage
 // (the last slice is k_sel_bc_reduce's, for the dB and dC columns; together with dz z they
 // give xhat . (dz W_in^T) without the product, since z = xhat W_in).
 template <int NS, typename TX, typename TD, int MODE, bool TRUNC, bool INP = false>
-__global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(const float *__restrict__ z, const TX *__restrict__ x,
+__global__ void __launch_bounds__(SEL_THREADS, 2) k_sel_bwd(const float *__restrict__ z, const TX *__restrict__ x,
                                                             const float *__restrict__ gy, const float *__restrict__ h,
                                                             const float *__restrict__ R, const float *__restrict__ b_dt,
                                                             const float *__restrict__ A, float *__restrict__ aggX,
@@ -486,7 +460,8 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
     constexpr int G = sel_group<TRUNC>();
     constexpr int RF = PC * NS;                            // floats of one row segment
     constexpr int STG = G * RF * (TRUNC ? 2 : 1);          // floats a stage
-    __shared__ uint64_t s_full[SEL_NSTG], s_empty[SEL_NSTG];
+    __shared__ uint64_t s_full[SEL_NSTG];
+    __shared__ unsigned s_done[SEL_NSTG];                  // warps done with each slot, running
     __shared__ int s_abort;
     __shared__ float s_rd[SEL_THREADS / 32][16];           // INP: the warps' row-dot shares
     __shared__ float s_rin[16];                            // INP: the sub-chunk's 1 / r
@@ -502,45 +477,40 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
     const int ngroups = (rows + G - 1) / G;
     const int nst = ngroups + (c0 > 0 ? 1 : 0);
 
+    // the bulk copies of stage k (one thread): the rows of group k, or the row before the chunk
+    auto issue_stage = [&](int k) {
+        const int pw = P - p0 < PC ? P - p0 : PC;
+        const uint32_t rowb = uint32_t(pw) * NS * 4u;
+        const int slot = k % SEL_NSTG;
+        const uint32_t bar = smem_u32(&s_full[slot]);
+        float *dst = sH + slot * STG;
+        if (k < ngroups) {
+            const int hi = rows - G * k, lo = hi - G > 0 ? hi - G : 0, n = hi - lo;
+            mbar_arrive_expect_tx(bar, uint32_t(n) * rowb * (TRUNC ? 2u : 1u));
+            for (int j = 0; j < n; ++j)
+                bulk_g2s(smem_u32(dst + j * RF), h + ((row0 + lo + j) * P + p0) * NS, rowb, bar);
+            if (TRUNC)
+                for (int j = 0; j < n; ++j) {
+                    const int64_t t = c0 + lo + j, m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
+                    bulk_g2s(smem_u32(dst + (G + j) * RF), R + ((b * T + m) * P + p0) * NS, rowb, bar);
+                }
+        } else {
+            mbar_arrive_expect_tx(bar, rowb);
+            bulk_g2s(smem_u32(dst), h + ((row0 - 1) * P + p0) * NS, rowb, bar);
+        }
+    };
     if (MODE == 1) {
         if (threadIdx.x == 0) {
             for (int j = 0; j < SEL_NSTG; ++j) {
                 mbar_init(smem_u32(&s_full[j]), 1);
-                mbar_init(smem_u32(&s_empty[j]), SEL_THREADS / 32);
+                s_done[j] = 0u;
             }
             s_abort = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
         __syncthreads();
-        if (wp == SEL_THREADS / 32) {   // the copy warp
-            if (lane == 0) {
-                const int pw = P - p0 < PC ? P - p0 : PC;
-                const uint32_t rowb = uint32_t(pw) * NS * 4u;
-                for (int k = 0; k < nst; ++k) {
-                    const int slot = k % SEL_NSTG;
-                    if (k >= SEL_NSTG)   // the walkers are done with the slot's last stage
-                        mbar_wait_sleep(smem_u32(&s_empty[slot]), uint32_t((k / SEL_NSTG - 1) & 1), &s_abort,
-                                        status, ADJ_SEL_PRODUCER_SLEEP_NS);
-                    const uint32_t bar = smem_u32(&s_full[slot]);
-                    float *dst = sH + slot * STG;
-                    if (k < ngroups) {
-                        const int hi = rows - G * k, lo = hi - G > 0 ? hi - G : 0, n = hi - lo;
-                        mbar_arrive_expect_tx(bar, uint32_t(n) * rowb * (TRUNC ? 2u : 1u));
-                        for (int j = 0; j < n; ++j)
-                            bulk_g2s(smem_u32(dst + j * RF), h + ((row0 + lo + j) * P + p0) * NS, rowb, bar);
-                        if (TRUNC)
-                            for (int j = 0; j < n; ++j) {
-                                const int64_t t = c0 + lo + j, m = t + W - 1 < T - 1 ? t + W - 1 : T - 1;
-                                bulk_g2s(smem_u32(dst + (G + j) * RF), R + ((b * T + m) * P + p0) * NS, rowb, bar);
-                            }
-                    } else {
-                        mbar_arrive_expect_tx(bar, rowb);
-                        bulk_g2s(smem_u32(dst), h + ((row0 - 1) * P + p0) * NS, rowb, bar);
-                    }
-                }
-            }
-            return;
-        }
+        if (threadIdx.x == 0)
+            for (int k = 0; k < nst && k < SEL_NSTG; ++k) issue_stage(k);
     }
 
     const Geo<NS> g(slice, P);
@@ -724,8 +694,15 @@ __global__ void __launch_bounds__(SEL_BWD_THREADS, ADJ_SEL_BWD_MINB) k_sel_bwd(c
             for (int k = 0; k < SEL_NT; ++k) abn[k] = ab[k];
         }
         if (MODE == 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&s_empty[gi % SEL_NSTG]));
+            __syncwarp();   // the warp's reads of the stage are done
+            if (lane == 0) {
+                const int slot = gi % SEL_NSTG;
+                const unsigned prev = atom_add_acq_rel(&s_done[slot], 1u);
+                if (prev % (SEL_THREADS / 32) == SEL_THREADS / 32 - 1 && gi + SEL_NSTG < nst) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // reads before the copies' writes
+                    issue_stage(gi + SEL_NSTG);
+                }
+            }
         }
     }
     if (MODE == 1) {
@@ -889,7 +866,7 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
                                                                      dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, \
                                                                      status, nullptr, nullptr, nullptr);           \
         k_sel_carry<1><<<cgrid, 256, 0, st>>>(w.aggX, w.aggY, B, int64_t(P) * NS, nchunks, T, TT, Wk);             \
-        k_sel_bwd<NS, TX, TD, 1, TR, IN><<<grid, SEL_BWD_THREADS, sm1, st>>>(                                      \
+        k_sel_bwd<NS, TX, TD, 1, TR, IN><<<grid, SEL_THREADS, sm1, st>>>(                                      \
             z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY, dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, status,      \
             inp.r, inp.gadd, inp.rowdot);                                                                          \
     } while (0)

@@ -101,6 +101,13 @@ def test_ssm4_p2048_shape():
     compare(synth.make_inputs("ssm4_p2048", T=200), 48, True)
 
 
+def test_four_cta_clusters_with_a_partial_last_cluster():
+    """P=2048 (K = 2048 > 1024 in the input projection: four-CTA clusters sharing B), T=700:
+    three 256-row pair tiles, so the second cluster's second pair lies wholly past the last
+    token and its first pair partly; two layers, full window."""
+    compare(synth.make_inputs("ssm4_p2048", T=700, K=2), None, True)
+
+
 # --------------------------------------------------------------- the bf16 workloads at their own windows
 
 PREFIX = 16384

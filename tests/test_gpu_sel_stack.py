@@ -96,6 +96,12 @@ def test_bf16_stack(Tbar):
     compare(synth.make_sel_stack_inputs("sel1_p1024", 3, T=1024, P=128), Tbar, True)
 
 
+def test_bf16_stack_four_cta_clusters():
+    """P=1024: the input GEMM (K = P + 2N = 1056) and dW_in run as four-CTA clusters; T=600
+    gives three 256-row pair tiles, the last cluster half past the last token."""
+    compare(synth.make_sel_stack_inputs("sel1_p1024", 2, T=600), None, True)
+
+
 def test_stack_of_one_is_the_layer():
     """K = 1 makes no normalisation and no input-path call: the lone layer's results."""
     from adjoint_gradients_long_gb300.sel_layer import SelLayer
