@@ -188,11 +188,12 @@ __device__ __forceinline__ void stage_sub(const Stage<NS> &s, const float *__res
 }
 
 // ------------------------------------------------------------------ forward state scan
+// Forward and window scans run three CTAs an SM (80 registers a thread; four, at 64, spill).
 // MODE 0: aggregates (prod Abar, h at the chunk end from h = 0) -> aggX, aggY.
 // MODE 1: outputs from the carries in aggY: h [B,T,P,NS] and y = xres + sum_n C h [B,T,P]
 // (XR: the residual input xres, staged with the other per-token inputs; else xhat's values).
 template <int NS, typename TX, int MODE, bool XR = false>
-__global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict__ z, const TX *__restrict__ x,
+__global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_fwd(const float *__restrict__ z, const TX *__restrict__ x,
                                                         const float *__restrict__ b_dt, const float *__restrict__ A,
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
                                                         float *__restrict__ h, float *__restrict__ y,
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sel_fwd(const float *__restrict
 // start), e = gy C.  MODE 0: aggregates (Pi, R of the chunk from (1, 0), the block start's
 // Abar left out) -> aggX, aggY; MODE 1: R [B,T,P,NS] from the carries (Pi_in, R_in).
 template <int NS, int MODE>
-__global__ void __launch_bounds__(SEL_THREADS) k_sel_win(const float *__restrict__ z, const float *__restrict__ gy,
+__global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_win(const float *__restrict__ z, const float *__restrict__ gy,
                                                         const float *__restrict__ b_dt, const float *__restrict__ A,
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
                                                         float *__restrict__ R, int64_t T, int P, int TT,
