@@ -54,7 +54,7 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// barrier 1 among the 256 walking threads (the reverse pass's copy warp stays out)
+// barrier 1 among the CTA's 256 walking threads
 __device__ __forceinline__ void walkers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 template <int NS>
