@@ -565,7 +565,7 @@ adj_status adj_sel_bwd(const adj_dims *dims, const adj_sel_weights *w, const voi
     sw.R = tr ? reinterpret_cast<float *>(at(ws, L.buf1)) : nullptr;
     sw.bc = reinterpret_cast<float *>(at(ws, L.part0));
     sw.dAp = reinterpret_cast<float *>(at(ws, L.part1));
-    ProfScope ps(K_SEL_BWD, st, tr ? 8 : 5);
+    ProfScope ps(K_SEL_BWD, st, tr ? 7 : 5);
     SelInp inp;
     inp.r = r;
     inp.gadd = gadd;

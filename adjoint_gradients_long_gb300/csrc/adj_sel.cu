@@ -188,12 +188,13 @@ __device__ __forceinline__ void stage_sub(const Stage<NS> &s, const float *__res
 }
 
 // ------------------------------------------------------------------ forward state scan
-// Forward and window scans run three CTAs an SM (80 registers a thread; four, at 64, spill).
+// Forward and window scans run three CTAs an SM (80 registers a thread; four, at 64, spill),
+// except the forward output pass of a stacked layer (residual input), which ran slower so.
 // MODE 0: aggregates (prod Abar, h at the chunk end from h = 0) -> aggX, aggY.
 // MODE 1: outputs from the carries in aggY: h [B,T,P,NS] and y = xres + sum_n C h [B,T,P]
 // (XR: the residual input xres, staged with the other per-token inputs; else xhat's values).
 template <int NS, typename TX, int MODE, bool XR = false>
-__global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_fwd(const float *__restrict__ z, const TX *__restrict__ x,
+__global__ void __launch_bounds__(SEL_THREADS, XR ? 2 : 3) k_sel_fwd(const float *__restrict__ z, const TX *__restrict__ x,
                                                         const float *__restrict__ b_dt, const float *__restrict__ A,
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
                                                         float *__restrict__ h, float *__restrict__ y,
@@ -260,14 +261,20 @@ __global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_fwd(const float *__restr
 
 // ------------------------------------------------------------------ window scan R (truncated mode)
 // R(m) = sum_{t=s}^{m} e_t prod_{j=s+1..t} Abar_j within each block of W tokens (s its
-// start), e = gy C.  MODE 0: aggregates (Pi, R of the chunk from (1, 0), the block start's
-// Abar left out) -> aggX, aggY; MODE 1: R [B,T,P,NS] from the carries (Pi_in, R_in).
+// start), e = gy C.  MODE 1: R [B,T,P,NS] from the carries (Pi_in, R_in) in aggX, aggY.
+// MODE 0: both scans' chunk aggregates in one forward walk.  With Pc = prod_{c0 < j <= t}
+// Abar_j and Sc = sum_t e_t Pc(t) over the chunk [c0, c1]:
+//   window (Pi, R from (1, 0), the block start's Abar left out): (a0 Pc(c1), a0 Sc), a0 =
+//   Abar_c0, or 1 where the chunk starts a block  -> aggX, aggY;
+//   reverse (Q, mu_c0 from mu_c1 = 0; the reverse pass's aggregate): (Pc(c1) Abar_{c1+1}, Sc),
+//   Abar_{c1+1} = 0 past the sequence end  -> revX, revY.
 template <int NS, int MODE>
 __global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_win(const float *__restrict__ z, const float *__restrict__ gy,
                                                         const float *__restrict__ b_dt, const float *__restrict__ A,
                                                         float *__restrict__ aggX, float *__restrict__ aggY,
                                                         float *__restrict__ R, int64_t T, int P, int TT,
-                                                        int64_t nchunks, int64_t W) {
+                                                        int64_t nchunks, int64_t W, float *__restrict__ revX,
+                                                        float *__restrict__ revY) {
     extern __shared__ __align__(16) float sm_sel[];
     constexpr int PC = Geo<NS>::PC, SC = Geo<NS>::SC;
     const Stage<NS> sg = stage_carve<NS>(sm_sel);
@@ -303,7 +310,13 @@ __global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_win(const float *__restr
         }
         for (int r = 0; r < nr; ++r) {
             const float gv = sg.g[r * PC + g.q];
-            if ((c0 + r0 + r) % W != 0) {
+            if (MODE == 1) {
+                if ((c0 + r0 + r) % W != 0) {
+                    const float dt = sg.dt[r * PC + g.q];
+#pragma unroll
+                    for (int k = 0; k < SEL_NT; ++k) pi[k] *= ex2(dt * A2[k]);
+                }
+            } else if (r0 + r > 0) {   // Pc: the factors after the chunk's first token
                 const float dt = sg.dt[r * PC + g.q];
 #pragma unroll
                 for (int k = 0; k < SEL_NT; ++k) pi[k] *= ex2(dt * A2[k]);
@@ -316,8 +329,22 @@ __global__ void __launch_bounds__(SEL_THREADS, 3) k_sel_win(const float *__restr
         }
     }
     if (MODE == 0 && g.act) {
-        st8v(aggX + ai, pi);
-        st8v(aggY + ai, rr);
+        // a0: the chunk's first Abar unless the chunk starts a block; Abar of the token after
+        const bool starts = c0 % W == 0, has_next = c0 + rows < T;
+        const float dt0 = starts ? 0.f : softplus_f(z[row0 * ZW + pp] + b_dt[pp]);
+        const float dtn = has_next ? softplus_f(z[(row0 + rows) * ZW + pp] + b_dt[pp]) : 0.f;
+        float wx[SEL_NT], wy[SEL_NT], qx[SEL_NT];
+#pragma unroll
+        for (int k = 0; k < SEL_NT; ++k) {
+            const float a0 = starts ? 1.f : ex2(dt0 * A2[k]);
+            wx[k] = a0 * pi[k];
+            wy[k] = a0 * rr[k];
+            qx[k] = has_next ? pi[k] * ex2(dtn * A2[k]) : 0.f;
+        }
+        st8v(aggX + ai, wx);
+        st8v(aggY + ai, wy);
+        st8v(revX + ai, qx);
+        st8v(revY + ai, rr);
     }
 }
 
@@ -847,9 +874,12 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
         const size_t sm1 = stage_floats<NS>() * 4;
         if ((e = smem_attr(k_sel_win<NS, 0>, sm1)) != cudaSuccess) return e;
         if ((e = smem_attr(k_sel_win<NS, 1>, sm1)) != cudaSuccess) return e;
-        k_sel_win<NS, 0><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk);
+        // one walk gives both scans' chunk aggregates (the reverse ones into aggX, aggY)
+        k_sel_win<NS, 0><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk,
+                                                         w.aggX, w.aggY);
         k_sel_carry<2><<<cgrid, 256, 0, st>>>(w.winX, w.winY, B, int64_t(P) * NS, nchunks, T, TT, Wk);
-        k_sel_win<NS, 1><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk);
+        k_sel_win<NS, 1><<<grid, SEL_THREADS, sm1, st>>>(z, gy, b_dt, A, w.winX, w.winY, w.R, T, P, TT, nchunks, Wk,
+                                                         nullptr, nullptr);
     }
     // MODE 0: the staged inputs; MODE 1: also the warp sums and the ring of row stages (and,
     // with the input path, the raw z of the dt columns)
@@ -861,11 +891,14 @@ static cudaError_t sel_bwd_t(const float *z, const void *x, const float *gy, con
     do {                                                                                                           \
         const size_t sm1 = stage_floats<NS>(IN) * 4 + sm_ws +                                                      \
                            size_t(SEL_NSTG) * sel_group<TR>() * row_seg * (TR ? 2 : 1);                            \
-        if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 0, TR>, sm0)) != cudaSuccess) return e;                           \
         if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 1, TR, IN>, sm1)) != cudaSuccess) return e;                       \
-        k_sel_bwd<NS, TX, TD, 0, TR><<<grid, SEL_THREADS, sm0, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY,   \
-                                                                     dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, \
-                                                                     status, nullptr, nullptr, nullptr);           \
+        if (!TR) { /* the truncated form has its reverse aggregates from the window walk */                        \
+            if ((e = smem_attr(k_sel_bwd<NS, TX, TD, 0, TR>, sm0)) != cudaSuccess) return e;                       \
+            k_sel_bwd<NS, TX, TD, 0, TR><<<grid, SEL_THREADS, sm0, st>>>(z, xt, gy, h, w.R, b_dt, A, w.aggX,       \
+                                                                         w.aggY, dzt, w.bc, w.dAp, T, P, TT,       \
+                                                                         nchunks, nsl, Wk, status, nullptr,        \
+                                                                         nullptr, nullptr);                        \
+        }                                                                                                          \
         k_sel_carry<1><<<cgrid, 256, 0, st>>>(w.aggX, w.aggY, B, int64_t(P) * NS, nchunks, T, TT, Wk);             \
         k_sel_bwd<NS, TX, TD, 1, TR, IN><<<grid, SEL_THREADS, sm1, st>>>(                                      \
             z, xt, gy, h, w.R, b_dt, A, w.aggX, w.aggY, dzt, w.bc, w.dAp, T, P, TT, nchunks, nsl, Wk, status,      \
