@@ -178,6 +178,37 @@ __device__ __forceinline__ void stage_store(const Stage<NS> &s, const StageRegs<
         }
     }
 }
+// L2 prefetch of a sub-chunk's per-token inputs (rows [r0, r0 + nr) of the chunk at row0,
+// this CTA's channels): z's dt columns, xhat and gy a 128-byte line a thread-step, and the
+// row's B and C columns; only addresses inside the arrays.
+template <int NS, typename TX>
+__device__ __forceinline__ void stage_prefetch(const float *__restrict__ z, const TX *__restrict__ x,
+                                               const float *__restrict__ gy, int P, int ZW, int64_t row0, int r0,
+                                               int nr, int p0) {
+    constexpr int PC = Geo<NS>::PC;
+    constexpr int LZ = PC * 4 / 128, LX = PC * int(sizeof(TX)) / 128;   // lines a row
+    constexpr int PER_ROW = 2 * LZ + LX + 1;                            // z, gy, xhat, B|C
+    const int pw = P - p0 < PC ? P - p0 : PC;
+    for (int e = int(threadIdx.x); e < nr * PER_ROW; e += SEL_THREADS) {
+        const int r = e / PER_ROW, k = e % PER_ROW;
+        const int64_t row = row0 + r0 + r;
+        const void *a;
+        if (k < LZ) {
+            if (k * 32 >= pw) continue;
+            a = z + row * ZW + p0 + k * 32;
+        } else if (k < 2 * LZ) {
+            if ((k - LZ) * 32 >= pw) continue;
+            a = gy + row * P + p0 + (k - LZ) * 32;
+        } else if (k < 2 * LZ + LX) {
+            if ((k - 2 * LZ) * (128 / int(sizeof(TX))) >= pw) continue;
+            a = x + row * P + p0 + (k - 2 * LZ) * (128 / int(sizeof(TX)));
+        } else {
+            a = z + row * ZW + P;
+        }
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+}
+
 template <int NS, typename TX, bool WX, bool WG, bool WZ = false>
 __device__ __forceinline__ void stage_sub(const Stage<NS> &s, const float *__restrict__ z, const TX *__restrict__ x,
                                           const float *__restrict__ gy, const float *__restrict__ b_dt, int P,
@@ -636,6 +667,11 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) k_sel_bwd(const float *__restr
                 if (INP)
                     for (int j = threadIdx.x; j < shi - slo; j += SEL_THREADS)
                         s_rin[j] = 1.f / __ldg(rin + row0 + slo + j);
+                // the next sub-chunk's inputs into L2 while this one is walked
+                if (slo > 0) {
+                    const int nlo = slo - SC > 0 ? slo - SC : 0;
+                    stage_prefetch<NS, TX>(z, x, gy, P, ZW, row0, nlo, slo - nlo, p0);
+                }
             }
             walkers_sync();
         }
