@@ -387,6 +387,8 @@ struct TcArgs {
     bool b_res, a_mul, b_lo;
     bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
     bool stream_out;              // StoreAdd whose output far exceeds L2: evict-first hints
+    bool outx_tma;                // the bf16 copy (out_x) staged per warp and stored by TMA
+    CUtensorMap tmOx;             // out_x: 32 x 32 bf16 boxes, unswizzled
     int nacc;                     // accumulators in tensor memory (2: epilogue overlaps the next tile)
     int epiw;                     // epilogue warps (CTA pairs: 8 or 16; otherwise TC_EPI_WARPS)
     GemmOperand A, Bm;
@@ -637,7 +639,10 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     uint8_t *stages = base + Lo.bres_bytes;                       // ring of A (+B) stages
     const int EPIW = PAIR ? args.epiw : TC_EPI_WARPS;
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES);
+    // (outx_tma) then EPIW bf16 chunk buffers of 2 KB
+    uint16_t *esx = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES +
+                                                  (args.outx_tma ? size_t(EPIW) * TC_CHUNK_BYTES / 2 : 0));
     uint64_t *full = bars, *empty = bars + S, *accf = bars + 2 * S, *acce = bars + 2 * S + 2, *bready = bars + 2 * S + 4;
     uint64_t *rawfull = bars + 2 * S + 5, *addb = bars + 3 * S + 5;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5 + TC_MAX_EPI_WARPS);
@@ -1114,7 +1119,21 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             v[j + 3] += r4.w;
                         }
                     }
-                    if (EXT && ep.out_x && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd) && m0r + lane < args.M) {
+                    if (EXT && args.outx_tma) {
+                        // the bf16 copy of this lane's row into the warp's bf16 buffer (dense 64-byte
+                        // rows), stored below by TMA with the fp32 chunk: whole lines reach L2
+                        uint4 *xr = reinterpret_cast<uint4 *>(esx + warp * (32 * 32) + lane * 32);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            uint4 u;
+                            u.x = pack_bf16(v[8 * g], v[8 * g + 1]);
+                            u.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+                            u.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+                            u.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+                            xr[g] = u;
+                        }
+                    } else if (EXT && ep.out_x && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd) &&
+                               m0r + lane < args.M) {
                         // the bf16 copy of this lane's row: four 16-byte stores
                         __nv_bfloat16 *xr = static_cast<__nv_bfloat16 *>(ep.out_x) + (m0r + lane) * ep.ld + n;
 #pragma unroll
@@ -1143,6 +1162,11 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             tma_store_2d_hint(&args.tmO[0], n, int(m0r), sb_s, l2_evict_first());
                         } else {
                             tma_store_2d(&args.tmO[0], n, int(m0r), sb_s);
+                        }
+                        if (EXT && args.outx_tma) {
+                            const uint32_t sx = smem_u32(esx + warp * (32 * 32));
+                            if (args.stream_out) tma_store_2d_hint(&args.tmOx, n, int(m0r), sx, l2_evict_first());
+                            else tma_store_2d(&args.tmOx, n, int(m0r), sx);
                         }
                         bulk_commit();
                     }
@@ -1221,6 +1245,20 @@ static bool make_out_map(CUtensorMap *m, const void *base, uint64_t cols, uint64
 
 // Epilogue through TMA stores when every map builds: fp32 outputs (no bf16 copy), an
 // fp32 residual, ProjIn blocks that 32-column chunks do not straddle.
+// Tensor map of the bf16 output copy: 32 x 32 boxes, dense 64-byte rows in shared memory.
+static bool make_outx_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t pitch_bytes) {
+    auto enc = encode_fn();
+    if (!enc || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || (pitch_bytes & 15u) || cols == 0 || rows == 0)
+        return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool epi_maps(TcArgs &a, const GemmEpilogue &ep, int64_t M, int64_t Nc, int splits) {
     switch (ep.kind) {
     case Epi::ProjIn:
@@ -1436,13 +1474,16 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     // pairs with many tiles each (no split) and a short K use 16 epilogue warps, with one
     // stage fewer; a long K keeps the stage (its mainloop outlasts the epilogue of 8 warps)
     const int epiw = (pair && splits == 1 && K <= 1024) ? TC_MAX_EPI_WARPS : TC_EPI_WARPS;
+    // a pair epilogue with a bf16 output copy stages it per warp (2 KB) and stores it by TMA
+    const bool outx = pair_cand && ep.out_x != nullptr && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd);
+    const size_t epi_bytes = size_t(epiw) * TC_CHUNK_BYTES * (outx ? 3 : 2) / 2;
     const size_t bar_bytes = size_t(3 * 6 + 6 + TC_MAX_EPI_WARPS) * 8;
     if (pair) {
         const TcLayout Lp = tc_layout(BN / 2, a.kper, false, false, false, false, false);
-        const size_t budget_p = 227 * 1024 - 1024 - size_t(epiw) * TC_CHUNK_BYTES - bar_bytes;
+        const size_t budget_p = 227 * 1024 - 1024 - epi_bytes - bar_bytes;
         int Sp = int(budget_p / Lp.stage_bytes);
         if (Sp > 6) Sp = 6;
-        const size_t smem_p = 1024 + size_t(Sp) * Lp.stage_bytes + size_t(epiw) * TC_CHUNK_BYTES + bar_bytes;
+        const size_t smem_p = 1024 + size_t(Sp) * Lp.stage_bytes + epi_bytes + bar_bytes;
         slots = Sp >= 2 ? pair_slots(smem_p) : 0;
         if (slots > 0) S = Sp;
         else pair = false;
@@ -1454,7 +1495,7 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (pair && quad_enabled() && K > 1024 && (Nc + BN - 1) / BN >= 2 && (M + 2 * TC_BM - 1) / (2 * TC_BM) >= 2 &&
         (BN / 2) % 64 == 0) {
         const TcLayout Lp = tc_layout(BN / 2, a.kper, false, false, false, false, false);
-        const size_t smem_p = 1024 + size_t(S) * Lp.stage_bytes + size_t(epiw) * TC_CHUNK_BYTES + bar_bytes;
+        const size_t smem_p = 1024 + size_t(S) * Lp.stage_bytes + epi_bytes + bar_bytes;
         const int q = pair_slots(smem_p, true);
         if (q > 0) {
             quad = true;
@@ -1487,6 +1528,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     if (pair && (a.a_ld != a_mode || a.b_ld != b_mode)) return cudaErrorInvalidValue;   // a map did not build
     a.a_mul = a_mul && a.a_ld != LD_REG;
     a.epi_tma = epi_maps(a, ep, M, Nc, splits);
+    a.outx_tma = outx && pair && a.epi_tma &&
+                 make_outx_map(&a.tmOx, ep.out_x, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 2);
     // a residual stream far larger than L2 (129 MB): its output lines cannot serve a later
     // reader from L2, so they go out first
     a.stream_out = a.epi_tma && ep.kind == Epi::StoreAdd && uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20);
@@ -1494,7 +1537,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     // the layout was sized for the modes asked for; a mode that fell back to registers
     // uses only part of its region
     const TcLayout L = tc_layout(pair ? BN / 2 : BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
-    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes + size_t(a.epiw) * TC_CHUNK_BYTES + bar_bytes;
+    const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes +
+                        size_t(a.epiw) * TC_CHUNK_BYTES * ((pair && outx) ? 3 : 2) / 2 + bar_bytes;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
     const bool ext = ep.nr != nullptr || ep.out_x != nullptr;   // the EXT epilogue features
     if (pair) {
