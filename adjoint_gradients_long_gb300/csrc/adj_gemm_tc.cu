@@ -388,7 +388,9 @@ struct TcArgs {
     bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
     bool stream_out;              // StoreAdd whose output far exceeds L2: evict-first hints
     bool outx_tma;                // the bf16 copy (out_x) staged per warp and stored by TMA
+    bool nx_tma;                  // (with outx_tma) the bf16 normalised input loaded into that buffer by TMA
     CUtensorMap tmOx;             // out_x: 32 x 32 bf16 boxes, unswizzled
+    CUtensorMap tmNxl;            // nx (bf16) for loads: the same box shape
     int nacc;                     // accumulators in tensor memory (2: epilogue overlaps the next tile)
     int epiw;                     // epilogue warps (CTA pairs: 8 or 16; otherwise TC_EPI_WARPS)
     GemmOperand A, Bm;
@@ -1039,9 +1041,17 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         }
                         bulk_wait_read();   // the previous chunk's store has read the buffer
                         if (add_tma) {
-                            mbar_arrive_expect_tx(addbar, 32 * 32 * 4);
+                            const bool nxl = EXT && args.nx_tma && ep.nr != nullptr;
+                            mbar_arrive_expect_tx(addbar, 32 * 32 * 4 + (nxl ? 32 * 32 * 2 : 0));
                             if (args.stream_out) tma_load_2d_hint(sb_s, &args.tmAdd, n, int(m0r), addbar, l2_evict_first());
                             else tma_load_2d(sb_s, &args.tmAdd, n, int(m0r), addbar);
+                            // the chunk's xhat rows into the bf16 buffer (free: the stores above
+                            // have read it)
+                            if (nxl) {
+                                const uint32_t sx = smem_u32(esx + warp * (32 * 32));
+                                if (args.stream_out) tma_load_2d_hint(sx, &args.tmNxl, n, int(m0r), addbar, l2_evict_first());
+                                else tma_load_2d(sx, &args.tmNxl, n, int(m0r), addbar);
+                            }
                         }
                     }
                     __syncwarp();
@@ -1049,6 +1059,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 // through a normalised input: this lane's row scalars and xhat values (bf16: all 32
                 // columns packed; fp32: read per quad below), issued before the TMEM load
                 const bool norm = EXT && add_tma && ep.nr != nullptr;
+                const bool nxt = norm && args.nx_tma;   // xhat arrives by TMA with the residual
                 const int64_t nrow = m0r + lane;
                 float n_mt = 0.f, n_ir = 0.f;
                 uint4 n_xb[4];
@@ -1057,7 +1068,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                     for (int sl = 0; sl < ep.nsl; ++sl) sdz += __ldg(ep.ndz + nrow * ep.nsl + sl);
                     n_mt = sdz * ep.inv_P;
                     n_ir = 1.f / __ldg(ep.nr + nrow);
-                    if (ep.nx_bf16) {
+                    if (ep.nx_bf16 && !nxt) {
                         const __nv_bfloat16 *xr = static_cast<const __nv_bfloat16 *>(ep.nx) + nrow * ep.ld + n;
 #pragma unroll
                         for (int g = 0; g < 4; ++g)
@@ -1088,6 +1099,15 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             v[j + 3] = sigmoidf_fast(v[j + 3] + b4.w);
                         }
                     }
+                    bool waited = false;
+                    if (nxt) {
+                        mbar_wait(addbar, add_phase, abort, args.status);
+                        add_phase ^= 1u;
+                        waited = true;
+                        const uint4 *xs = reinterpret_cast<const uint4 *>(esx + warp * (32 * 32) + lane * 32);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) n_xb[g] = xs[g];
+                    }
                     if (norm && nrow < args.M) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
@@ -1108,8 +1128,10 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         }
                     }
                     if (add_tma) {
-                        mbar_wait(addbar, add_phase, abort, args.status);
-                        add_phase ^= 1u;
+                        if (!waited) {
+                            mbar_wait(addbar, add_phase, abort, args.status);
+                            add_phase ^= 1u;
+                        }
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
                             const float4 r4 = *reinterpret_cast<const float4 *>(sb + epi_at(lane, j >> 2));
@@ -1530,6 +1552,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.epi_tma = epi_maps(a, ep, M, Nc, splits);
     a.outx_tma = outx && pair && a.epi_tma &&
                  make_outx_map(&a.tmOx, ep.out_x, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 2);
+    a.nx_tma = a.outx_tma && ep.kind == Epi::StoreAdd && ep.nr && ep.nx_bf16 &&
+               make_outx_map(&a.tmNxl, ep.nx, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 2);
     // a residual stream far larger than L2 (129 MB): its output lines cannot serve a later
     // reader from L2, so they go out first
     a.stream_out = a.epi_tma && ep.kind == Epi::StoreAdd && uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20);
