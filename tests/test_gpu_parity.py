@@ -101,6 +101,13 @@ def test_ssm4_p2048_shape():
     compare(synth.make_inputs("ssm4_p2048", T=200), 48, True)
 
 
+def test_bf16_stack_with_ragged_channels():
+    """bf16 layers with P = 200 (not a multiple of the 32-column epilogue chunk): the input
+    gradient's bf16 output copy and x-hat chunks move by TMA with boxes that cross the last
+    column (clipped stores, zero-filled loads); three layers, window 64."""
+    compare(synth.make_inputs("ssm8_p512", T=300, P=200, N=64, K=3), 64, True)
+
+
 def test_four_cta_clusters_with_a_partial_last_cluster():
     """P=2048 (K = 2048 > 1024 in the input projection: four-CTA clusters sharing B), T=700:
     three 256-row pair tiles, so the second cluster's second pair lies wholly past the last
