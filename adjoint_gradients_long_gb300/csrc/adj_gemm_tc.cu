@@ -352,6 +352,15 @@ __device__ __forceinline__ void tma_load_2d_quad(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Advance a ring position (slot s of S, round r) by one stage, without a 64-bit division in
+// the hot loops of the single-thread TMA and MMA issuers.
+__device__ __forceinline__ void ring_next(int &s, int64_t &r, int S) {
+    if (++s == S) {
+        s = 0;
+        ++r;
+    }
+}
+
 // L2 priorities for a streamed StoreAdd epilogue: the outputs and the consumed residual and
 // xhat lines are marked evict-first, so that the boxes prefetched a tile ahead are not the
 // ones pushed out of L2 by the output stream.
@@ -751,14 +760,16 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         const bool csum_on = args.ep.csum && b_raw && args.b_ld == LD_RAW_MN && args.ep.kind == Epi::Partial;
         float csum0 = 0.f, csum1 = 0.f;
         int64_t kbg = 0;   // k-blocks staged so far (ring position)
+        int rs = 0;        // its slot and round
+        int64_t rr = 0;
         for (int64_t t = unit0; t < ntiles && ok && prod_full; t += nunits) {
             int64_t m0, n0, kb0, ke;
             int z;
             tile_of(t, m0, n0, z, kb0, ke);
             const int64_t nkb = ke > kb0 ? (ke - kb0 + TC_BK - 1) / TC_BK : 0;
-            for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
-                const int s = int(kbg % S);
-                const int64_t r = kbg / S;
+            for (int64_t kb = 0; kb < nkb; ++kb, ++kbg, ring_next(rs, rr, S)) {
+                const int s = rs;
+                const int64_t r = rr;
                 uint8_t *st = stages + size_t(s) * Lo.stage_bytes;
                 uint8_t *sa = st, *sbb = st + Lo.a_reg;
                 const int64_t k0 = kb0 + kb * TC_BK;
@@ -838,6 +849,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             }
             bool ok = (a_dir || b_dir || a_raw || b_raw) && pair_ok;
             int64_t kbg = 0;
+            int rs = 0;   // ring slot and round of kbg
+            int64_t rr = 0;
             // the residual of a TMA StoreAdd epilogue: the epilogue waits on each 32 x 32 box it
             // loads, so its boxes are prefetched into L2 when the tile's operand loads start,
             // about a tile ahead of the epilogue (a streamed output: the epilogue warps prefetch
@@ -856,9 +869,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                                 if (args.ep.nr) tma_prefetch_2d(&args.tmNx, int(n0 + c), int(m0 + 32 * q));
                             }
                 }
-                for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const int s = int(kbg % S);
-                    const int64_t r = kbg / S;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++kbg, ring_next(rs, rr, S)) {
+                    const int s = rs;
+                    const int64_t r = rr;
                     if (r > 0 && !mbar_wait(smem_u32(&empty[s]), uint32_t((r - 1) & 1), abort, args.status)) {
                         ok = false;
                         break;
@@ -926,6 +939,8 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             bool ok = !args.b_res || mbar_wait(smem_u32(bready), 0, abort, args.status);
             if (ok) tc_fence_after();
             int64_t kbg = 0, i = 0;
+            int rs = 0;   // ring slot and round of kbg
+            int64_t rr = 0;
             for (int64_t t = unit0; t < ntiles && ok; t += nunits, ++i) {
                 int64_t m0, n0, kb0, ke;
                 int z;
@@ -936,9 +951,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 if (ru > 0 && !mbar_wait(smem_u32(&acce[buf]), uint32_t((ru - 1) & 1), abort, args.status)) break;
                 tc_fence_after();
                 const uint32_t dacc = tmem + uint32_t(buf * BN);
-                for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
-                    const int s = int(kbg % S);
-                    const int64_t r = kbg / S;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++kbg, ring_next(rs, rr, S)) {
+                    const int s = rs;
+                    const int64_t r = rr;
                     if (!mbar_wait(smem_u32(&full[s]), uint32_t(r & 1), abort, args.status)) {
                         ok = false;
                         break;
