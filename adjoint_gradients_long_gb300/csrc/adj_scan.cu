@@ -50,8 +50,12 @@ constexpr int SC_WARPS = 8;
 #ifndef ADJ_SCAN_BWD_L
 #define ADJ_SCAN_BWD_L 8
 #endif
-// tokens per warp (chunk = 8 L tokens) of the forward scan and of the window and reverse scans
-constexpr int SC_FWD_L = ADJ_SCAN_FWD_L, SC_BWD_L = ADJ_SCAN_BWD_L;
+#ifndef ADJ_SCAN_TRUNC_L
+#define ADJ_SCAN_TRUNC_L 8
+#endif
+// tokens per warp (chunk = 8 L tokens) of the forward scan, of the window and reverse scans,
+// and of the one-pass truncated adjoint
+constexpr int SC_FWD_L = ADJ_SCAN_FWD_L, SC_BWD_L = ADJ_SCAN_BWD_L, SC_TRUNC_L = ADJ_SCAN_TRUNC_L;
 constexpr int SC_SLICE = 128;        // channels per CTA
 constexpr int SC_MIN_CHUNK = 32;     // smallest chunk (L = 4); sizes the descriptor arrays
 constexpr unsigned SC_EMPTY = 0xFFFFFFFFu;   // descriptor word not yet published
@@ -644,7 +648,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     G = rseg_then(post, RevSeg{sCQ[lane], sCS[lane], true});
     if (TRUNC) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
     const float4 bav = (DZ && act) ? *reinterpret_cast<const float4 *>(b_a + ch) : f4(0.f);
-    static_assert(!DZ || L == 8, "the row dots are summed eight tokens at a time");
+    static_assert(!DZ || L <= 8, "the row dots are summed eight tokens at a time");
     float vz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = L - 1; k >= 0; --k) {
@@ -680,7 +684,7 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
     if (DZ) {
         const float tot = warp_sum8(vz, lane);
         const int k = warp_sum8_index(lane);
-        if ((lane & 3) == 0 && t0 + k < T) dz[(b * T + t0 + k) * nslices + slice] = tot;
+        if ((lane & 3) == 0 && k < L && t0 + k < T) dz[(b * T + t0 + k) * nslices + slice] = tot;
     }
 }
 
@@ -698,9 +702,9 @@ __global__ void __launch_bounds__(256, (L <= 4 ? 4 : L <= 6 ? 3 : L <= 8 ? 2 : 1
 //   * a chunk of the block before reads the one prefix X = F of the chunk preceding its
 //     window ends and gets R(m) = Sigma_X + Pi_X R_loc(m) from the stored local values, which
 //     TMA brings into the freed c rows while its look-back runs.
-// Chunks run in reverse order (one ticket each, like the full reverse scan), so every wait
-// is on a CTA with an earlier ticket: the block's other chunks (aggregates), the block
-// after's first chunk (prefixes).  Writers fence before they publish and readers after
+// Chunks run block by block from the last, each block's chunks in reverse (one ticket each;
+// trunc_order below), so every wait is on a CTA with an earlier ticket: the block's other
+// chunks (aggregates), the block after's first chunk (prefixes).  Writers fence before they publish and readers after
 // they observe, so the stored R_loc rows are visible to the TMA that reads them.  HBM sees
 // the bytes of the full reverse scan plus the R_loc round trip, which mostly stays in L2.
 
@@ -718,6 +722,26 @@ __device__ __forceinline__ FwdSeg wait_fdesc(const float4 *p0, const float4 *p1,
 
 // The same for n <= NB consecutive chunks' slots (p0, p1 of the first; a chunk's slots are 32
 // float4 apart): all loads of a poll in flight at once, so a batch costs one L2 round trip.
+// Ticket order: blocks of CB chunks from the last block back, and within a block each
+// sequence's chunks in reverse, one sequence after the other (the last block may be short).
+// The chunks of block k - 1 wait for the prefixes that block k's first chunk -- the last of
+// its block and sequence to run -- folds; with several sequences the other sequences' chunks
+// of block k run in between, so the fold is usually published before it is needed.  Every
+// wait is still on an earlier ticket: a chunk's successors in its block and sequence, and
+// the folds of later blocks of its sequence.
+__device__ __forceinline__ void trunc_order(int64_t tk, int64_t nseq, int64_t nchunks, int64_t CB, int64_t &chunk,
+                                            int64_t &seq) {
+    const int64_t nblk = (nchunks + CB - 1) / CB, tail = nchunks - (nblk - 1) * CB;
+    if (tk < nseq * tail) {
+        seq = tk / tail;
+        chunk = nchunks - 1 - tk % tail;
+    } else {
+        const int64_t u = tk - nseq * tail, g = u / (nseq * CB), r = u % (nseq * CB);
+        seq = r / CB;
+        chunk = (nblk - 2 - g) * CB + CB - 1 - r % CB;
+    }
+}
+
 template <int NB>
 __device__ __forceinline__ void wait_fdesc_n(const float4 *p0, const float4 *p1, int n, FwdSeg (&out)[NB],
                                              unsigned *status) {
@@ -744,7 +768,7 @@ __device__ __forceinline__ void wait_fdesc_n(const float4 *p0, const float4 *p1,
 }
 
 template <int L, typename TD, bool DZ>
-__global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
+__global__ void __launch_bounds__(256, (L <= 4 ? 3 : 2)) k_trunc_scan(const __grid_constant__ ScanMaps mp, const float *__restrict__ h,
                                                       float *__restrict__ Rl, TD *__restrict__ Da, TD *__restrict__ Du,
                                                       TD *__restrict__ Dc, TD *__restrict__ E, int64_t T, int N,
                                                       int nslices, int64_t nseq, int64_t nchunks, int64_t W,
@@ -760,14 +784,16 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
     __shared__ bool sCl[SC_WARPS];
     __shared__ int s_ctl[SC_WARPS + 2];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tk = chunk_ticket(dM, &s_ticket, &s_bar, &s_abort), chunk = nchunks - 1 - tk / nseq, seq = tk % nseq;
+    const int64_t CB = W / TT;
+    int64_t chunk, seq;
+    trunc_order(chunk_ticket(dM, &s_ticket, &s_bar, &s_abort), nseq, nchunks, CB, chunk, seq);
     const int64_t b = seq / nslices;
     const int slice = int(seq % nslices), ch = slice * SC_SLICE + lane * 4;
     const bool act = ch < N;
     const int64_t c0 = chunk * TT, t0 = c0 + w * L;
     const int64_t base = b * T * N + ch;
     const int64_t di = seq * nchunks + chunk, fb = seq * nchunks;
-    const int64_t CB = W / TT, blk = c0 / W;
+    const int64_t blk = c0 / W;
     const bool first_of_block = c0 % W == 0;
     {
         float *dst[3] = {sg, sc, sa};
@@ -954,7 +980,7 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
     G = rseg_then(post, RevSeg{sC0[lane], sC1[lane], true});
     if (use_rows) mbar_wait(smem_u32(&s_bar), 1, &s_abort, status);
     const float4 bav = (DZ && act) ? *reinterpret_cast<const float4 *>(b_a + ch) : f4(0.f);
-    static_assert(!DZ || L == 8, "the row dots are summed eight tokens at a time");
+    static_assert(!DZ || L <= 8, "the row dots are summed eight tokens at a time");
     float vz[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const int64_t xend = (cx + 1) * TT;   // window ends before this row are the end of chunk cx
 #pragma unroll
@@ -991,7 +1017,7 @@ __global__ void __launch_bounds__(256, 2) k_trunc_scan(const __grid_constant__ S
     if (DZ) {
         const float tot = warp_sum8(vz, lane);
         const int k = warp_sum8_index(lane);
-        if ((lane & 3) == 0 && t0 + k < T) dz[(b * T + t0 + k) * nslices + slice] = tot;
+        if ((lane & 3) == 0 && k < L && t0 + k < T) dz[(b * T + t0 + k) * nslices + slice] = tot;
     }
 }
 
@@ -1062,16 +1088,16 @@ cudaError_t launch_win_scan(const float *g, const float *c, const float *a, floa
 // Scan workspace of the one-pass truncated adjoint: two descriptor sets, laid out
 // [ticket, reverse descriptors | ticket (unused), forward descriptors].
 static int64_t trunc_chunks(int64_t B, int64_t T, int N) {
-    return B * cdiv(N, SC_SLICE) * cdiv(T, SC_WARPS * SC_BWD_L);
+    return B * cdiv(N, SC_SLICE) * cdiv(T, SC_WARPS * SC_TRUNC_L);
 }
 static size_t trunc_desc_bytes(int64_t n) { return 256 + 4 * size_t(n) * 32 * sizeof(float4); }
 size_t trunc_ws_bytes(int64_t B, int64_t T, int N) { return 2 * trunc_desc_bytes(trunc_chunks(B, T, N)); }
-bool trunc_one_launch(int64_t T, int64_t W) { return W > 0 && W < T && W % (SC_WARPS * SC_BWD_L) == 0; }
+bool trunc_one_launch(int64_t T, int64_t W) { return W > 0 && W < T && W % (SC_WARPS * SC_TRUNC_L) == 0; }
 
 cudaError_t launch_trunc_scan(const float *g, const float *c, const float *a, const float *h, float *R, void *D_a,
                               void *D_u, void *D_c, void *E, bool d_bf16, int64_t B, int64_t T, int N, int64_t W,
                               void *ws, unsigned *status, cudaStream_t st, const float *b_a, float *dz) {
-    constexpr int L = SC_BWD_L, TT = SC_WARPS * L;
+    constexpr int L = SC_TRUNC_L, TT = SC_WARPS * L;
     if (!trunc_one_launch(T, W)) return cudaErrorInvalidValue;
     const int nslices = int(cdiv(N, SC_SLICE));
     const int64_t nseq = B * nslices, nchunks = cdiv(T, TT), n = nseq * nchunks;
