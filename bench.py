@@ -55,7 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip the context lines of the other workloads")
-    ap.add_argument("--workload", default=None, help="run this workload as the headline instead (testing)")
+    ap.add_argument("--workload", default=None,
+                    help="KEY[:WINDOW]: run this workload (full window unless WINDOW) as the headline instead (testing)")
     return ap.parse_args()
 
 
@@ -695,7 +696,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     key, window = HEADLINE
     if args.workload:
-        key, window = args.workload, None
+        key, _, win = args.workload.partition(":")
+        window = int(win) if win and win != "full" else None
     peaks, peak_src = load_peaks()
 
     def barrier():
