@@ -333,6 +333,22 @@ constexpr uint32_t TC_EPI_SMEM = TC_EPI_WARPS * 32 * 32 * 4;
 // tiles per CTA runs warps 0-15 as epilogue warps, twice the output chunks in flight
 constexpr int TC_MAX_EPI_WARPS = TC_EPI_WARPS + TC_PROD_WARPS;
 constexpr uint32_t TC_CHUNK_BYTES = 32 * 32 * 4;
+// A streamed StoreAdd pair product with a short K (the output projection) can keep each CTA's
+// half of the B tile resident (TC_RO_BRES) and stream only A through TC_RO_STAGES stages; the
+// shared memory that frees gives TC_RO_EPI_WARPS epilogue warps a residual buffer and an
+// output buffer each.  16 warps with two A stages measured best (12 warps with four stages, or
+// three streamed A+B stages without the resident B, were slower)
+#ifndef ADJ_TC_RO_EPI_WARPS
+#define ADJ_TC_RO_EPI_WARPS 16
+#endif
+#ifndef ADJ_TC_RO_STAGES
+#define ADJ_TC_RO_STAGES 2
+#endif
+#ifndef ADJ_TC_RO_BRES
+#define ADJ_TC_RO_BRES 1
+#endif
+constexpr int TC_RO_EPI_WARPS = ADJ_TC_RO_EPI_WARPS, TC_RO_STAGES = ADJ_TC_RO_STAGES;
+constexpr bool TC_RO_BRES = ADJ_TC_RO_BRES;
 
 // Operand load mode: register staging, or TMA tiles of a bf16 array (K-major: one box of
 // 64 k x R rows; MN-major: R/64 boxes of 64 rows x 64 k).
@@ -396,6 +412,7 @@ struct TcArgs {
     bool b_res, a_mul, b_lo;
     bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
     bool stream_out;              // StoreAdd whose output far exceeds L2: evict-first hints
+    bool ro;                      // streamed StoreAdd with separate residual and output buffers
     bool outx_tma;                // the bf16 copy (out_x) staged per warp and stored by TMA
     bool nx_tma;                  // (with outx_tma) the bf16 normalised input loaded into that buffer by TMA
     CUtensorMap tmOx;             // out_x: 32 x 32 bf16 boxes, unswizzled
@@ -650,10 +667,14 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     uint8_t *stages = base + Lo.bres_bytes;                       // ring of A (+B) stages
     const int EPIW = PAIR ? args.epiw : TC_EPI_WARPS;
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
-    // (outx_tma) then EPIW bf16 chunk buffers of 2 KB
-    uint16_t *esx = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES);
+    // (ro) EPIW output chunk buffers, (outx_tma) then EPIW bf16 chunk buffers of 2 KB
+    // only a pair kernel (no quad) without the EXT epilogue features is launched with ro
+    const bool RO = PAIR && !QUAD && !EXT && args.ro;
+    const size_t ro_bytes = RO ? size_t(EPIW) * TC_CHUNK_BYTES : 0;
+    uint16_t *esx =
+        reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES + ro_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES +
-                                                  (args.outx_tma ? size_t(EPIW) * TC_CHUNK_BYTES / 2 : 0));
+                                                  ro_bytes + (args.outx_tma ? size_t(EPIW) * TC_CHUNK_BYTES / 2 : 0));
     uint64_t *full = bars, *empty = bars + S, *accf = bars + 2 * S, *acce = bars + 2 * S + 2, *bready = bars + 2 * S + 4;
     uint64_t *rawfull = bars + 2 * S + 5, *addb = bars + 3 * S + 5;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 3 * S + 5 + TC_MAX_EPI_WARPS);
@@ -835,16 +856,28 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         // ---------------- TMA issuer
         if (lane == 0) {
             if (args.b_res && ld_tma(args.b_ld)) {
+                // the n tile is the same for every tile of this CTA (or pair)
                 int64_t m0, n0, kb0, ke;
                 int z;
-                tile_of(blockIdx.x, m0, n0, z, kb0, ke);
-                mbar_arrive_expect_tx(smem_u32(bready), uint32_t(nkb_full) * Lo.b_bytes * (args.b_lo ? 2u : 1u));
-                for (int64_t kb = 0; kb < nkb_full; ++kb) {
-                    tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
-                                    bres + size_t(kb) * Lo.bres_kb, smem_u32(bready));
-                    if (args.b_lo)
-                        tma_tile<false>(args.tmBlo, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
-                                        bres + size_t(kb) * Lo.bres_kb + Lo.b_bytes, smem_u32(bready));
+                tile_of(unit0, m0, n0, z, kb0, ke);
+                const uint32_t bbytes = uint32_t(nkb_full) * Lo.b_bytes * (args.b_lo ? 2u : 1u);
+                if (PAIR) {
+                    // each CTA's half of the B columns, counted on the leader's barrier, which
+                    // expects both halves (the leader's MMAs read both)
+                    const uint32_t rb = mapa_shared(smem_u32(bready), lead);
+                    if (prank == 0) mbar_arrive_expect_tx(smem_u32(bready), 2u * bbytes);
+                    for (int64_t kb = 0; kb < nkb_full; ++kb)
+                        tma_tile<false, true>(args.tmB, args.Bm, args.b_ld, n0 + int64_t(prank) * BNS, BNS,
+                                              kb0 + kb * TC_BK, bres + size_t(kb) * Lo.bres_kb, rb);
+                } else {
+                    mbar_arrive_expect_tx(smem_u32(bready), bbytes);
+                    for (int64_t kb = 0; kb < nkb_full; ++kb) {
+                        tma_tile<false>(args.tmB, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
+                                        bres + size_t(kb) * Lo.bres_kb, smem_u32(bready));
+                        if (args.b_lo)
+                            tma_tile<false>(args.tmBlo, args.Bm, args.b_ld, n0, BN, kb0 + kb * TC_BK,
+                                            bres + size_t(kb) * Lo.bres_kb + Lo.b_bytes, smem_u32(bready));
+                    }
                 }
             }
             bool ok = (a_dir || b_dir || a_raw || b_raw) && pair_ok;
@@ -887,7 +920,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         const uint32_t fb = mapa_shared(smem_u32(&full[s]), lead);
                         if (prank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * txd);
                         tma_tile<true, true>(args.tmA, args.A, args.a_ld, m0, TC_BM, k0, sa, fb);
-                        if (QUAD) {
+                        if (!b_dir) {
+                            // B resident
+                        } else if (QUAD) {
                             // this CTA's half of its B half (64 rows), to itself and its counterpart
                             const int64_t row = n0 + int64_t(prank) * BNS + int64_t(pq) * (BNS / 2);
                             const uint16_t mc = uint16_t((1u << prank) | (1u << (prank + 2u)));
@@ -1007,8 +1042,13 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
         // shared buffer -> global.  With TMA stores (epi_tma) the fused op is applied in
         // registers, the residual of StoreAdd arrives in the buffer by TMA while TMEM is
         // read, and one lane stores the chunk; otherwise lanes store column quads.
+        // ro: the residual arrives in sb and the output leaves from its own buffer ob, so the
+        // next chunk's residual load is issued as soon as this chunk has read sb, and the wait
+        // for the previous store to read ob is a chunk old when it is checked
         float *sb = esm + warp * (32 * 32);
-        const uint32_t sb_s = smem_u32(sb), addbar = smem_u32(&addb[warp]);
+        float *ob = RO ? esm + (EPIW + warp) * (32 * 32) : sb;
+        const uint32_t sb_s = smem_u32(sb), ob_s = smem_u32(ob), addbar = smem_u32(&addb[warp]);
+        bool ahead = false;   // ro: this warp's next chunk's residual load is in flight (lane 0)
         const int q = warp & 3, half = warp >> 2;   // lane quarter; column-chunk phase
         const int CSTEP = 32 * (EPIW / 4);
         const GemmEpilogue &ep = args.ep;
@@ -1033,6 +1073,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                 if (args.epi_tma && !live) continue;
                 const bool via_tma = args.epi_tma;
                 const bool add_tma = via_tma && ep.kind == Epi::StoreAdd;
+                int64_t nx_m = args.M, nx_n = 0;   // this warp's next chunk (lane 0, streamed StoreAdd)
                 if (via_tma) {
                     if (lane == 0) {
                         if (add_tma && args.stream_out) {
@@ -1053,9 +1094,13 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                                 tma_prefetch_2d(&args.tmAdd, int(pn), int(pm));
                                 if (ep.nr) tma_prefetch_2d(&args.tmNx, int(pn), int(pm));
                             }
+                            nx_m = pm;
+                            nx_n = pn;
                         }
-                        bulk_wait_read();   // the previous chunk's store has read the buffer
-                        if (add_tma) {
+                        if (!RO) bulk_wait_read();   // the previous chunk's store has read the buffer
+                        if (RO && ahead) {
+                            ahead = false;   // the previous chunk issued this chunk's residual load
+                        } else if (add_tma) {
                             const bool nxl = EXT && args.nx_tma && ep.nr != nullptr;
                             mbar_arrive_expect_tx(addbar, 32 * 32 * 4 + (nxl ? 32 * 32 * 2 : 0));
                             if (args.stream_out) tma_load_2d_hint(sb_s, &args.tmAdd, n, int(m0r), addbar, l2_evict_first());
@@ -1185,20 +1230,25 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                                 else *reinterpret_cast<uint4 *>(xr + 8 * g) = u;
                             }
                     }
+                    if (RO) {
+                        if (lane == 0) bulk_wait_read();   // the previous chunk's store has read ob
+                        __syncwarp();
+                    }
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(sb + epi_at(lane, j >> 2)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        *reinterpret_cast<float4 *>(ob + epi_at(lane, j >> 2)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    // orders the lanes' reads of sb and writes of ob before the bulk copies below
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         if (ep.kind == Epi::Partial) {
-                            tma_store_3d(&args.tmO[0], n, int(m0r), z, sb_s);
+                            tma_store_3d(&args.tmO[0], n, int(m0r), z, ob_s);
                         } else if (ep.kind == Epi::ProjIn) {
-                            tma_store_2d(&args.tmO[pblk], pch, int(m0r), sb_s);
+                            tma_store_2d(&args.tmO[pblk], pch, int(m0r), ob_s);
                         } else if (args.stream_out) {
-                            tma_store_2d_hint(&args.tmO[0], n, int(m0r), sb_s, l2_evict_first());
+                            tma_store_2d_hint(&args.tmO[0], n, int(m0r), ob_s, l2_evict_first());
                         } else {
-                            tma_store_2d(&args.tmO[0], n, int(m0r), sb_s);
+                            tma_store_2d(&args.tmO[0], n, int(m0r), ob_s);
                         }
                         if (EXT && args.outx_tma) {
                             const uint32_t sx = smem_u32(esx + warp * (32 * 32));
@@ -1206,6 +1256,12 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             else tma_store_2d(&args.tmOx, n, int(m0r), sx);
                         }
                         bulk_commit();
+                        if (RO && nx_m < args.M && nx_n < args.Nc) {
+                            // the next chunk's residual into sb, which this chunk has read
+                            mbar_arrive_expect_tx(addbar, 32 * 32 * 4);
+                            tma_load_2d_hint(sb_s, &args.tmAdd, int(nx_n), int(nx_m), addbar, l2_evict_first());
+                            ahead = true;
+                        }
                     }
                 } else {
 #pragma unroll
@@ -1225,6 +1281,9 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
             }
             if (!ok) break;
         }
+        // ro: a load issued ahead for a chunk that was not reached (an abandoned step) lands
+        // before the CTA leaves
+        if (lane == 0 && ahead) (void)mbar_wait(addbar, add_phase, abort, args.status);
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
@@ -1433,6 +1492,17 @@ static cudaError_t launch_pair(const TcArgs &a, unsigned grid, size_t smem, cuda
     return cudaLaunchKernelEx(&cfg, pair_kernel(ext, quad), a);
 }
 
+// Whether a streamed StoreAdd pair product with a short K keeps B resident and gives its
+// epilogue warps separate residual and output buffers (TC_RO_*).
+static int g_ro_mode = -1;
+static bool ro_enabled() {
+    if (g_ro_mode < 0) {
+        const char *v = getenv("ADJ_GEMM_RO");
+        g_ro_mode = (v && v[0] == '0') ? 0 : 1;
+    }
+    return g_ro_mode == 1;
+}
+
 // Whether pair GEMMs with a long K (a mainloop bound by operand delivery) run as quads.
 static int g_quad_mode = -1;
 static bool quad_enabled() {
@@ -1510,7 +1580,7 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     int slots = 0;
     // pairs with many tiles each (no split) and a short K use 16 epilogue warps, with one
     // stage fewer; a long K keeps the stage (its mainloop outlasts the epilogue of 8 warps)
-    const int epiw = (pair && splits == 1 && K <= 1024) ? TC_MAX_EPI_WARPS : TC_EPI_WARPS;
+    int epiw = (pair && splits == 1 && K <= 1024) ? TC_MAX_EPI_WARPS : TC_EPI_WARPS;
     // a pair epilogue with a bf16 output copy stages it per warp (2 KB) and stores it by TMA
     const bool outx = pair_cand && ep.out_x != nullptr && (ep.kind == Epi::Store || ep.kind == Epi::StoreAdd);
     const size_t epi_bytes = size_t(epiw) * TC_CHUNK_BYTES * (outx ? 3 : 2) / 2;
@@ -1537,6 +1607,26 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
         if (q > 0) {
             quad = true;
             slots = q;
+        }
+    }
+    // a streamed StoreAdd pair product whose B half fits resident (the output projection):
+    // resident B, TC_RO_STAGES A stages, TC_RO_EPI_WARPS epilogue warps with a residual and an
+    // output buffer each; every pair then keeps one n tile, so the pairs are a multiple of the
+    // n tiles
+    bool ro = false;
+    if (pair && !quad && ro_enabled() && splits == 1 && ep.kind == Epi::StoreAdd && ep.nr == nullptr && !outx &&
+        !ep.add_bf16 && uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20) && epi_maps(a, ep, M, Nc, splits)) {
+        const TcLayout Lr = tc_layout(BN / 2, a.kper, TC_RO_BRES, false, false, false, false);
+        const size_t smem_r = 1024 + size_t(Lr.bres_bytes) + size_t(TC_RO_STAGES) * Lr.stage_bytes +
+                              size_t(TC_RO_EPI_WARPS) * TC_CHUNK_BYTES * 2 + bar_bytes;
+        const int nt = TC_RO_BRES ? int((Nc + BN - 1) / BN) : 1;
+        const int q = smem_r <= size_t(227) * 1024 ? pair_slots(smem_r) : 0;
+        if (q >= nt) {
+            ro = true;
+            a.b_res = TC_RO_BRES;
+            S = TC_RO_STAGES;
+            epiw = TC_RO_EPI_WARPS;
+            slots = q / nt * nt;
         }
     }
     const int64_t rows_per_tile = quad ? 4 * TC_BM : pair ? 2 * TC_BM : TC_BM;
@@ -1572,12 +1662,15 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     // a residual stream far larger than L2 (129 MB): its output lines cannot serve a later
     // reader from L2, so they go out first
     a.stream_out = a.epi_tma && ep.kind == Epi::StoreAdd && uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20);
+    a.ro = ro && a.stream_out;
+    if (ro && !a.ro) return cudaErrorInvalidValue;   // its maps were built above
     a.b_lo = Bm.lo[0] && a.b_ld != LD_REG;
     // the layout was sized for the modes asked for; a mode that fell back to registers
     // uses only part of its region
     const TcLayout L = tc_layout(pair ? BN / 2 : BN, a.kper, a.b_res, split3, ld_raw(a_mode), ld_raw(b_mode), a_mul);
     const size_t smem = 1024 + size_t(L.bres_bytes) + size_t(S) * L.stage_bytes +
-                        size_t(a.epiw) * TC_CHUNK_BYTES * ((pair && outx) ? 3 : 2) / 2 + bar_bytes;
+                        size_t(a.epiw) * TC_CHUNK_BYTES * ((pair && outx) ? 3 : 2) / 2 +
+                        (a.ro ? size_t(a.epiw) * TC_CHUNK_BYTES : 0) + bar_bytes;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
     const bool ext = ep.nr != nullptr || ep.out_x != nullptr;   // the EXT epilogue features
     if (pair) {

@@ -115,6 +115,35 @@ def test_four_cta_clusters_with_a_partial_last_cluster():
     compare(synth.make_inputs("ssm4_p2048", T=700, K=2), None, True)
 
 
+def test_streamed_output_projection_elementwise():
+    """The output projection over an output far larger than L2 (34000 x 2048 fp32, 278 MB)
+    keeps its B half resident and gives each epilogue warp separate residual and output
+    buffers; 34000 tokens leave the last 256-row pair tile partly filled.  Each layer's output
+    y^k is checked element by element against y^{k-1} (xhat for the first layer) + bf16(c h) W_o
+    recomputed in fp64 from the same run's c, h and W_o ([AS] What carries the argument: the
+    residual stack), so a chunk written from the wrong buffer or rows cannot hide in a norm.
+    The bound is the fp32 accumulation of 256 products: 1e-4 of sum |a w| (about 2^-13)."""
+    from adjoint_gradients_long_gb300.stack import AdjStack
+    T, P, N, K = 34000, 2048, 256, 2
+    st = AdjStack(1, T, P, N, K, x_bf16=True, d_bf16=True)
+    st.load(synth.make_inputs("ssm4_p2048", T=T, K=K))
+    st.forward()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    for k in range(K):
+        ch = synth.round_bf16(st.c[k][0].cpu().numpy() * st.h[k][0].cpu().numpy()).astype(np.float64)
+        W = st.W_o[k].float().cpu().numpy().astype(np.float64)
+        res = (st.x[0][0].float() if k == 0 else st.y[k - 1][0]).cpu().numpy()
+        y = st.y[k][0].cpu().numpy()
+        for r0 in range(0, T, 4096):
+            sl = slice(r0, r0 + 4096)
+            ref = res[sl].astype(np.float64) + ch[sl] @ W
+            bound = 1e-4 * (np.abs(ch[sl]) @ np.abs(W)) + 1e-6 * np.abs(ref) + 1e-30
+            err = np.abs(y[sl].astype(np.float64) - ref)
+            bad = err > bound
+            assert not bad.any(), (k, r0, int(bad.sum()), np.argwhere(bad)[:4].tolist(), float((err / bound).max()))
+
+
 # --------------------------------------------------------------- the bf16 workloads at their own windows
 
 PREFIX = 16384
