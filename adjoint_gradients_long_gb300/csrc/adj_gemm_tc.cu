@@ -413,6 +413,7 @@ struct TcArgs {
     bool epi_tma;                 // epilogue through TMA stores (tmO, tmAdd)
     bool stream_out;              // StoreAdd whose output far exceeds L2: evict-first hints
     bool ro;                      // streamed StoreAdd with separate residual and output buffers
+    bool add16;                   // StoreAdd residual in bf16 by TMA (32 x 32 boxes, dense 64-byte rows)
     bool outx_tma;                // the bf16 copy (out_x) staged per warp and stored by TMA
     bool nx_tma;                  // (with outx_tma) the bf16 normalised input loaded into that buffer by TMA
     CUtensorMap tmOx;             // out_x: 32 x 32 bf16 boxes, unswizzled
@@ -668,8 +669,11 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
     const int EPIW = PAIR ? args.epiw : TC_EPI_WARPS;
     float *esm = reinterpret_cast<float *>(stages + size_t(S) * Lo.stage_bytes);
     // (ro) EPIW output chunk buffers, (outx_tma) then EPIW bf16 chunk buffers of 2 KB
-    // only a pair kernel (no quad) without the EXT epilogue features is launched with ro
+    // only a pair kernel (no quad) without the EXT epilogue features is launched with ro, and
+    // only a pair kernel without them with a bf16 residual by TMA
     const bool RO = PAIR && !QUAD && !EXT && args.ro;
+    const bool ADD16 = PAIR && !EXT && args.add16;
+    const uint32_t add_tx = ADD16 ? 32u * 32u * 2u : 32u * 32u * 4u;   // residual bytes a chunk
     const size_t ro_bytes = RO ? size_t(EPIW) * TC_CHUNK_BYTES : 0;
     uint16_t *esx =
         reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(esm) + size_t(EPIW) * TC_CHUNK_BYTES + ro_bytes);
@@ -1102,7 +1106,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             ahead = false;   // the previous chunk issued this chunk's residual load
                         } else if (add_tma) {
                             const bool nxl = EXT && args.nx_tma && ep.nr != nullptr;
-                            mbar_arrive_expect_tx(addbar, 32 * 32 * 4 + (nxl ? 32 * 32 * 2 : 0));
+                            mbar_arrive_expect_tx(addbar, add_tx + (nxl ? 32 * 32 * 2 : 0));
                             if (args.stream_out) tma_load_2d_hint(sb_s, &args.tmAdd, n, int(m0r), addbar, l2_evict_first());
                             else tma_load_2d(sb_s, &args.tmAdd, n, int(m0r), addbar);
                             // the chunk's xhat rows into the bf16 buffer (free: the stores above
@@ -1192,13 +1196,28 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                             mbar_wait(addbar, add_phase, abort, args.status);
                             add_phase ^= 1u;
                         }
+                        if (ADD16) {
+                            // this lane's row of the bf16 residual: 32 values, 64 bytes
+                            uint4 rb[4];
+                            const uint4 *rs = reinterpret_cast<const uint4 *>(sb) + lane * 4;
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 r4 = *reinterpret_cast<const float4 *>(sb + epi_at(lane, j >> 2));
-                            v[j] += r4.x;
-                            v[j + 1] += r4.y;
-                            v[j + 2] += r4.z;
-                            v[j + 3] += r4.w;
+                            for (int g = 0; g < 4; ++g) rb[g] = rs[g];
+                            __syncwarp();   // every row read before any lane writes its output over it
+#pragma unroll
+                            for (int j = 0; j < 32; j += 2) {
+                                const uint32_t w = (&rb[j >> 3].x)[(j & 7) >> 1];
+                                v[j] += __uint_as_float(w << 16);
+                                v[j + 1] += __uint_as_float(w & 0xFFFF0000u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 r4 = *reinterpret_cast<const float4 *>(sb + epi_at(lane, j >> 2));
+                                v[j] += r4.x;
+                                v[j + 1] += r4.y;
+                                v[j + 2] += r4.z;
+                                v[j + 3] += r4.w;
+                            }
                         }
                     }
                     if (EXT && args.outx_tma) {
@@ -1258,7 +1277,7 @@ __global__ void __launch_bounds__(TC_THREADS_P, 1) k_gemm_tc(const __grid_consta
                         bulk_commit();
                         if (RO && nx_m < args.M && nx_n < args.Nc) {
                             // the next chunk's residual into sb, which this chunk has read
-                            mbar_arrive_expect_tx(addbar, 32 * 32 * 4);
+                            mbar_arrive_expect_tx(addbar, add_tx);
                             tma_load_2d_hint(sb_s, &args.tmAdd, int(nx_n), int(nx_m), addbar, l2_evict_first());
                             ahead = true;
                         }
@@ -1355,7 +1374,9 @@ static bool make_outx_map(CUtensorMap *m, const void *base, uint64_t cols, uint6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static bool epi_maps(TcArgs &a, const GemmEpilogue &ep, int64_t M, int64_t Nc, int splits) {
+// add16_ok: a bf16 StoreAdd residual may arrive by TMA (pair kernels without the EXT features);
+// otherwise such an epilogue stays on the lane-store path
+static bool epi_maps(TcArgs &a, const GemmEpilogue &ep, int64_t M, int64_t Nc, int splits, bool add16_ok) {
     switch (ep.kind) {
     case Epi::ProjIn:
         if (ep.N % 32) return false;
@@ -1368,9 +1389,12 @@ static bool epi_maps(TcArgs &a, const GemmEpilogue &ep, int64_t M, int64_t Nc, i
     case Epi::StoreAdd:
         // a bf16 copy (out_x) is written by the lanes themselves, beside the TMA store
         if (!make_out_map(&a.tmO[0], ep.out0, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4)) return false;
-        if (ep.kind == Epi::StoreAdd &&
-            (ep.add_bf16 || !make_out_map(&a.tmAdd, ep.add, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4)))
-            return false;
+        if (ep.kind == Epi::StoreAdd) {
+            const bool ok = ep.add_bf16
+                                ? add16_ok && make_outx_map(&a.tmAdd, ep.add, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 2)
+                                : make_out_map(&a.tmAdd, ep.add, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 4);
+            if (!ok) return false;
+        }
         // the normalised input is only prefetched through its map (32 x 32 boxes)
         if (ep.kind == Epi::StoreAdd && ep.nr &&
             !make_map(&a.tmNx, ep.nx, ep.nx_bf16, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * (ep.nx_bf16 ? 2 : 4), 32, 32))
@@ -1613,9 +1637,10 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     // resident B, TC_RO_STAGES A stages, TC_RO_EPI_WARPS epilogue warps with a residual and an
     // output buffer each; every pair then keeps one n tile, so the pairs are a multiple of the
     // n tiles
+    const bool ext = ep.nr != nullptr || ep.out_x != nullptr;   // the EXT epilogue features
     bool ro = false;
-    if (pair && !quad && ro_enabled() && splits == 1 && ep.kind == Epi::StoreAdd && ep.nr == nullptr && !outx &&
-        !ep.add_bf16 && uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20) && epi_maps(a, ep, M, Nc, splits)) {
+    if (pair && !quad && ro_enabled() && splits == 1 && ep.kind == Epi::StoreAdd && !ext &&
+        uint64_t(M) * uint64_t(Nc) * 4u > (uint64_t(256) << 20) && epi_maps(a, ep, M, Nc, splits, true)) {
         const TcLayout Lr = tc_layout(BN / 2, a.kper, TC_RO_BRES, false, false, false, false);
         const size_t smem_r = 1024 + size_t(Lr.bres_bytes) + size_t(TC_RO_STAGES) * Lr.stage_bytes +
                               size_t(TC_RO_EPI_WARPS) * TC_CHUNK_BYTES * 2 + bar_bytes;
@@ -1654,7 +1679,8 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
     a.b_ld = tma_build(a.tmB, a.tmBlo, nullptr, Bm, b_mode, false, Nc, K, quad ? BN / 4 : pair ? BN / 2 : BN);
     if (pair && (a.a_ld != a_mode || a.b_ld != b_mode)) return cudaErrorInvalidValue;   // a map did not build
     a.a_mul = a_mul && a.a_ld != LD_REG;
-    a.epi_tma = epi_maps(a, ep, M, Nc, splits);
+    a.epi_tma = epi_maps(a, ep, M, Nc, splits, pair && !ext);
+    a.add16 = a.epi_tma && ep.kind == Epi::StoreAdd && ep.add_bf16;
     a.outx_tma = outx && pair && a.epi_tma &&
                  make_outx_map(&a.tmOx, ep.out_x, uint64_t(Nc), uint64_t(M), uint64_t(ep.ld) * 2);
     a.nx_tma = a.outx_tma && ep.kind == Epi::StoreAdd && ep.nr && ep.nx_bf16 &&
@@ -1672,7 +1698,6 @@ cudaError_t launch_gemm_tc(int64_t M, int64_t Nc, int64_t K, const GemmOperand &
                         size_t(a.epiw) * TC_CHUNK_BYTES * ((pair && outx) ? 3 : 2) / 2 +
                         (a.ro ? size_t(a.epiw) * TC_CHUNK_BYTES : 0) + bar_bytes;
     const int64_t ntiles = int64_t(a.n_tiles) * a.m_tiles * splits;
-    const bool ext = ep.nr != nullptr || ep.out_x != nullptr;   // the EXT epilogue features
     if (pair) {
         a.ep.csum = nullptr;
         if (csum_done) *csum_done = false;
