@@ -141,12 +141,13 @@ cudaError_t launch_colsum(const void *D, bool bf16, int64_t rows, int N, float *
 // ---------------------------------------------------------------- partial reductions
 // out[i] (+)= sum_z part[z][i] for up to three independent arrays (the split-K partials of
 // dW_in and dW_o, the column-sum partials of db_a) in one launch; each array owns a range
-// of blocks.  Wide arrays: a block covers 32 consecutive float4 outputs, warp w sums the
-// partials z = w, w + 8, ... (eight loads in flight, every load a 512-byte row segment)
-// and the eight warp sums are added in warp order.  Narrow arrays with many partials
-// (the column sums): an output float4 is owned by a group of G lanes (a power of two, at
-// most 32, so that a lane loads at most eight partials at a time), or by a whole block
-// when 32 lanes would need more; lane g sums z = g, g + G, ... and a butterfly of
+// of blocks.  Wide arrays with more than 32 partials: a block covers 32 consecutive float4
+// outputs, warp w sums the partials z = w, w + 8, ... (eight loads in flight, every load a
+// 512-byte row segment) and the eight warp sums are added in warp order.  Narrow arrays
+// (the column sums) and wide arrays with at most 32 partials (the split-K products): an
+// output float4 is owned by a group of G lanes (a power of two, at most 32, so that a lane
+// loads at most eight partials at a time), or by a whole block when 32 lanes would need
+// more; lane g sums z = g, g + G, ... and a butterfly of
 // shuffles combines the group (then shared memory, in warp order, for a block).  The order of every addition
 // is fixed, so the result does not depend on scheduling.
 __global__ void __launch_bounds__(256) k_reduce_partials(RedArgs r) {
@@ -254,7 +255,9 @@ cudaError_t launch_reduce_partials(const RedSeg *segs, int nseg, int accumulate,
     for (int k = 0; k < nseg; ++k) {
         r.seg[k] = segs[k];
         int G = 0;                                   // 0: warps over the partials
-        if (segs[k].n4 < 4096) {                     // narrow: lane groups, or whole blocks
+        // narrow arrays, or few partials (a wide array's warps would mostly idle over them):
+        // lane groups, or whole blocks
+        if (segs[k].n4 < 4096 || segs[k].splits <= 32) {
             G = 1;
             while (G < 32 && (segs[k].splits + G - 1) / G > 8) G <<= 1;
             if ((segs[k].splits + G - 1) / G > 8) G = 256;
