@@ -60,6 +60,12 @@ def parse():
     return ap.parse_args()
 
 
+def workload_arg(spec):
+    """--workload KEY[:WINDOW] -> (key, window); no WINDOW, or "full", is the full window."""
+    key, _, win = spec.partition(":")
+    return key, (int(win) if win and win != "full" else None)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -696,8 +702,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     key, window = HEADLINE
     if args.workload:
-        key, _, win = args.workload.partition(":")
-        window = int(win) if win and win != "full" else None
+        key, window = workload_arg(args.workload)
     peaks, peak_src = load_peaks()
 
     def barrier():

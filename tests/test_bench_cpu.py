@@ -138,3 +138,9 @@ def test_selective_stack_kernel_table():
     assert t["sel_dx"]["bytes"] == 2 * zw + 4 * P + 2 * P + 4 + 4 * (nsl + 1) + 4 * P
     assert t["sel_dx"]["flops"] == 2 * zw * P
     assert t["rms_norm"]["bytes"] == 4 * P + 2 * P + 4
+
+
+def test_workload_arg():
+    assert bench.workload_arg("ssm1_1m") == ("ssm1_1m", None)
+    assert bench.workload_arg("ssm1_1m:full") == ("ssm1_1m", None)
+    assert bench.workload_arg("ssm8_p512:4096") == ("ssm8_p512", 4096)
